@@ -1,0 +1,360 @@
+"""CPU oracle for the MoE layer with an expert slot cache.
+
+TEST INFRASTRUCTURE ONLY.  This module is the slow, plain statement of what
+the hot path computes.  Only the tests, the smoke check and the benchmark's
+CPU-baseline leg may import it; the library never does, and it shares no
+code with the CUDA path.
+
+Sources (web pages; cited by title and section):
+  [SGB]   "Nudge, don't cut" (PGO-SGB), section "The method in five lines":
+          bias[l][e] = max(cap, ln(b[l][e] / b_edge[l])) on cold experts, 0 on
+          hot ones; pick top-k by logit + bias; weights are the router's own
+          softmax over the k picked, from the unbiased logits (selection only).
+  [PORT]  "Porting vllm-expert-cache to NVIDIA GPUs", sections "What this
+          package does" (manage picks victims among slots the step does not
+          need and emits a miss list; gather copies missing experts host to
+          slot; routing ids are remapped to slot space), "Prove it is correct
+          before measuring" (fields: expert-to-slot table, cold map, slot
+          contents, priorities, miss list; deterministic, no atomics;
+          16-byte slabs), "Measuring, without fooling yourself" (sizing trap:
+          a step is served from slots only when tokens x top_k <= slots).
+  [ZERO]  "RTX 3060 runs a 35B MoE with llama.cpp" (video transcript), chapter
+          "Designing a fixed expert cache with zero-return for missing
+          experts": a missing expert returns zeros; a second pass over the
+          missing experts is added, which gives exactly the full result.
+
+Precision.  Router logits decide integers (the top-k ids), so they are taken
+in fp32 in one fixed order that the kernels follow as well: for each (t, e),
+acc = 0 then acc = fma(x[t][h], Wr[h][e], acc) for h = 0..H-1.  A bf16 x bf16
+product is exact in fp32, so "multiply then add in fp32" is that same fma.
+Selection compares fp32 scores logit + bias (one IEEE add).  Everything else
+(softmax weights, the SwiGLU expert FFN, the combine) is evaluated in fp64.
+
+Readings of points the pages leave open (each listed in the design notes):
+  * top-k order: descending score, equal scores -> lower expert id first;
+  * softmax over the k picked (equal to a full softmax renormalised);
+  * hot set = the n_hot brightest experts (ties -> lower id); b_edge = the
+    smallest brightness in it; bias computed in fp64, rounded to fp32; b = 0
+    gives the cap;
+  * SwiGLU: h = silu(x Wg) * (x Wu), silu(z) = z / (1 + exp(-z)), y = h Wd,
+    no biases; slab = [Wg (HxI) | Wu (HxI) | Wd (IxH)] input-major;
+  * manage: stamp += 1 per call.  LRU: prio = stamp on hit or load.  LFU:
+    prio += 1 on a hit (once per call), prio = 1 on load.  STATIC: no
+    eviction, no priority change; misses listed with slot -1.  Victims are
+    slots not needed by the call: empty slots first (ascending slot), then
+    ascending prio, then ascending slot.  The i-th missing expert (ascending
+    id) takes the i-th victim.  Eviction clears the old expert's entry.
+  * a step larger than the pool (T*k > S while S < E) is split into chunks of
+    floor(S/k) consecutive tokens, each chunk managed, gathered and computed
+    in turn; S < k cannot be served.
+  * zero-return: residency is e2s[e] >= 0 after a STATIC manage; the output is
+    the sum of the resident partial and the missing partial.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import numpy as np
+
+LRU, LFU, STATIC = 0, 1, 2
+RESIDENT, GATHER, ZERO_RETURN = 0, 1, 2
+
+
+# ----------------------------------------------------------------------------
+# Routing  [SGB "The method in five lines"]
+# ----------------------------------------------------------------------------
+
+def router_logits(x: np.ndarray, wr: np.ndarray, logit_offset=None) -> np.ndarray:
+    """logit[t][e] = sum_h x[t][h] * Wr[h][e], fp32, h ascending.
+
+    ``x`` [T][H] and ``wr`` [H][E] hold bf16 values (as float32 arrays).  The
+    optional per-expert ``logit_offset`` [E] is added after the sum.
+    """
+    x = np.asarray(x, dtype=np.float32)
+    wr = np.asarray(wr, dtype=np.float32)
+    T, H = x.shape
+    acc = np.zeros((T, wr.shape[1]), dtype=np.float32)
+    for h in range(H):
+        acc += x[:, h:h + 1] * wr[h:h + 1, :]
+    if logit_offset is not None:
+        acc = acc + np.asarray(logit_offset, dtype=np.float32)[None, :]
+    return acc
+
+
+def bias_table(b: np.ndarray, n_hot: int, cap: float) -> np.ndarray:
+    """Soft selection bias for one layer: 0 on the hot set, else max(cap, ln(b/b_edge))."""
+    b = np.asarray(b, dtype=np.float32)
+    E = b.shape[0]
+    order = sorted(range(E), key=lambda e: (-float(b[e]), e))
+    hot = set(order[:n_hot])
+    b_edge = min(float(b[e]) for e in hot)
+    out = np.zeros(E, dtype=np.float32)
+    for e in range(E):
+        if e in hot:
+            continue
+        be = float(b[e])
+        val = cap if be <= 0.0 else max(cap, float(np.log(be / b_edge)))
+        out[e] = np.float32(val)
+    return out
+
+
+def select_topk(logits: np.ndarray, k: int, bias=None) -> np.ndarray:
+    """ids[t][0..k-1]: the k largest fp32 scores logit + bias, descending, ties -> lower id."""
+    logits = np.asarray(logits, dtype=np.float32)
+    scores = logits if bias is None else (logits + np.asarray(bias, dtype=np.float32)[None, :])
+    T, E = scores.shape
+    ids = np.empty((T, k), dtype=np.int32)
+    for t in range(T):
+        order = sorted(range(E), key=lambda e: (-float(scores[t, e]), e))
+        ids[t] = order[:k]
+    return ids
+
+
+def route_weights(logits: np.ndarray, ids: np.ndarray) -> np.ndarray:
+    """w[t][j] = exp(logit[t][ids[t][j]]) / sum_j' exp(logit[t][ids[t][j']]), fp64, unbiased logits."""
+    T, k = ids.shape
+    w = np.empty((T, k), dtype=np.float64)
+    for t in range(T):
+        l = np.array([float(logits[t, e]) for e in ids[t]], dtype=np.float64)
+        p = np.exp(l - l.max())
+        w[t] = p / p.sum()
+    return w
+
+
+def route(x, wr, k, logit_offset=None, bias=None):
+    logits = router_logits(x, wr, logit_offset)
+    ids = select_topk(logits, k, bias)
+    return ids, route_weights(logits, ids), logits
+
+
+# ----------------------------------------------------------------------------
+# Permutation into per-expert groups
+# ----------------------------------------------------------------------------
+
+def permute(ids: np.ndarray, E: int):
+    """Group the flat routing slots t*k+j by expert, stable in the flat index.
+
+    Returns count[E], offset[E+1] (exclusive prefix), rows[T*k] (the flat
+    index at each grouped position) and pos[T*k] (grouped position of each
+    flat index).
+    """
+    flat = np.asarray(ids, dtype=np.int64).reshape(-1)
+    n = flat.shape[0]
+    count = np.zeros(E, dtype=np.int32)
+    for e in flat:
+        count[e] += 1
+    offset = np.zeros(E + 1, dtype=np.int32)
+    for e in range(E):
+        offset[e + 1] = offset[e] + count[e]
+    rows = np.array(sorted(range(n), key=lambda i: (int(flat[i]), i)), dtype=np.int32)
+    pos = np.empty(n, dtype=np.int32)
+    for p, i in enumerate(rows):
+        pos[i] = p
+    return count, offset, rows, pos
+
+
+# ----------------------------------------------------------------------------
+# Slot cache  [PORT "What this package does", "Prove it is correct ..."]
+# ----------------------------------------------------------------------------
+
+@dataclass
+class CacheState:
+    e2s: np.ndarray            # int32 [E], -1 = cold (host only)
+    s2e: np.ndarray            # int32 [S], -1 = empty slot
+    prio: np.ndarray           # uint32 [S]
+    stamp: int = 0
+
+    @staticmethod
+    def from_slots(s2e, E: int) -> "CacheState":
+        s2e = np.asarray(s2e, dtype=np.int32).copy()
+        e2s = np.full(E, -1, dtype=np.int32)
+        for s, e in enumerate(s2e):
+            if e >= 0:
+                e2s[e] = s
+        return CacheState(e2s, s2e, np.zeros(len(s2e), dtype=np.uint32), 0)
+
+    def copy(self) -> "CacheState":
+        return CacheState(self.e2s.copy(), self.s2e.copy(), self.prio.copy(), self.stamp)
+
+
+@dataclass
+class ManageResult:
+    miss_e: list = field(default_factory=list)
+    miss_s: list = field(default_factory=list)
+    hit_e: list = field(default_factory=list)
+    sid: np.ndarray = None
+
+
+class CapacityError(ValueError):
+    pass
+
+
+def manage(state: CacheState, ids: np.ndarray, policy: int) -> ManageResult:
+    """One expert_cache_manage call on the flat routing ids of a step (updates ``state``)."""
+    flat = [int(e) for e in np.asarray(ids).reshape(-1)]
+    S = state.s2e.shape[0]
+    state.stamp += 1
+    stamp = state.stamp
+    needed = sorted(set(flat))
+    if policy != STATIC and len(needed) > S:
+        raise CapacityError(f"{len(needed)} experts needed, {S} slots")
+    hits = [e for e in needed if state.e2s[e] >= 0]
+    misses = [e for e in needed if state.e2s[e] < 0]
+    res = ManageResult(miss_e=list(misses), hit_e=list(hits))
+    if policy == LRU:
+        for e in hits:
+            state.prio[state.e2s[e]] = stamp
+    elif policy == LFU:
+        for e in hits:
+            state.prio[state.e2s[e]] += 1
+    if policy == STATIC:
+        res.miss_s = [-1] * len(misses)
+    else:
+        used = {int(state.e2s[e]) for e in hits}
+        cands = [s for s in range(S) if s not in used]
+        empty = [s for s in cands if state.s2e[s] < 0]
+        full = sorted((s for s in cands if state.s2e[s] >= 0), key=lambda s: (int(state.prio[s]), s))
+        victims = (empty + full)[: len(misses)]
+        for e, s in zip(misses, victims):
+            old = int(state.s2e[s])
+            if old >= 0:
+                state.e2s[old] = -1
+            state.s2e[s] = e
+            state.e2s[e] = s
+            state.prio[s] = stamp if policy == LRU else 1
+        res.miss_s = list(victims)
+    res.sid = np.array([state.e2s[e] for e in flat], dtype=np.int32).reshape(np.asarray(ids).shape)
+    return res
+
+
+def gather(host: np.ndarray, pool: np.ndarray, miss_e, miss_s) -> None:
+    """Copy each missing expert's slab bytes from the host store into its slot."""
+    for e, s in zip(miss_e, miss_s):
+        pool[s] = host[e]
+
+
+def chunk_tokens(T: int, k: int, S: int, E: int) -> int:
+    """Tokens per chunk so that every chunk fits the pool (sizing trap reading)."""
+    if S >= E or T * k <= S:
+        return T
+    if S < k:
+        raise CapacityError(f"S={S} < k={k}")
+    return S // k
+
+
+# ----------------------------------------------------------------------------
+# Expert FFN and combine (fp64)
+# ----------------------------------------------------------------------------
+
+def unpack_slab(slab: np.ndarray, H: int, I: int):
+    """Split a flat slab into Wg [H][I], Wu [H][I], Wd [I][H] (fp64)."""
+    s = np.asarray(slab, dtype=np.float64).reshape(-1)
+    n = H * I
+    return s[:n].reshape(H, I), s[n:2 * n].reshape(H, I), s[2 * n:3 * n].reshape(I, H)
+
+
+def silu(z):
+    return z / (1.0 + np.exp(-z))
+
+
+def swiglu_expert(x_rows: np.ndarray, slab: np.ndarray, H: int, I: int) -> np.ndarray:
+    """y = (silu(x Wg) * (x Wu)) Wd for a block of rows x [n][H]."""
+    wg, wu, wd = unpack_slab(slab, H, I)
+    xr = np.asarray(x_rows, dtype=np.float64)
+    return (silu(xr @ wg) * (xr @ wu)) @ wd
+
+
+def expert_ffn(x, rows, offset, k, slabs, H, I, experts=None) -> np.ndarray:
+    """Grouped FFN.  y[p] for grouped position p of expert e uses token rows[p] // k.
+
+    ``slabs`` maps expert id -> flat slab (an [E][3HI] array works).  Rows of
+    experts not in ``experts`` (when given) are left as NaN.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    E = len(offset) - 1
+    y = np.full((len(rows), H), np.nan, dtype=np.float64)
+    for e in range(E):
+        a, b = int(offset[e]), int(offset[e + 1])
+        if a == b or (experts is not None and e not in experts):
+            continue
+        tok = np.asarray(rows[a:b]) // k
+        y[a:b] = swiglu_expert(x[tok], slabs[e], H, I)
+    return y
+
+
+def combine(y, w, pos, T, k, resident=None):
+    """out[t] = sum_j w[t][j] y[pos[t*k+j]], j ascending (fp64).
+
+    With ``resident`` (bool [T][k]) also returns the resident and missing
+    partial sums; the output is then their sum.
+    """
+    y = np.asarray(y, dtype=np.float64)
+    H = y.shape[1]
+    out = np.zeros((T, H))
+    if resident is None:
+        for t in range(T):
+            for j in range(k):
+                out[t] += w[t][j] * y[pos[t * k + j]]
+        return out
+    res = np.zeros((T, H))
+    miss = np.zeros((T, H))
+    for t in range(T):
+        for j in range(k):
+            term = w[t][j] * y[pos[t * k + j]]
+            if resident[t][j]:
+                res[t] += term
+            else:
+                miss[t] += term
+    return res + miss, res, miss
+
+
+# ----------------------------------------------------------------------------
+# Whole layer
+# ----------------------------------------------------------------------------
+
+def layer_forward(x, wr, host, H, I, k, mode, policy=LRU, state=None, pool=None,
+                  logit_offset=None, bias=None):
+    """One MoE layer forward with the slot cache.
+
+    ``host`` [E][3HI] holds every expert (authoritative copy); ``pool``
+    [S][3HI] the slot contents (updated by the gather); ``state`` the cache
+    state (updated).  Returns a dict with the routing, the per-chunk cache
+    results and the outputs (fp64).
+    """
+    x = np.asarray(x, dtype=np.float32)
+    T = x.shape[0]
+    E = wr.shape[1]
+    ids, w, logits = route(x, wr, k, logit_offset, bias)
+    out = np.zeros((T, H))
+    out_res = np.zeros((T, H))
+    out_miss = np.zeros((T, H))
+    chunks = []
+    if mode == RESIDENT:
+        C = T
+    else:
+        S = state.s2e.shape[0]
+        C = T if policy == STATIC else chunk_tokens(T, k, S, E)
+    for t0 in range(0, T, C):
+        t1 = min(T, t0 + C)
+        cids = ids[t0:t1]
+        count, offset, rows, pos = permute(cids, E)
+        rec = {"t0": t0, "t1": t1, "count": count, "offset": offset, "rows": rows, "pos": pos}
+        if mode != RESIDENT:
+            mr = manage(state, cids, policy)
+            rec.update(miss_e=mr.miss_e, miss_s=mr.miss_s, hit_e=mr.hit_e, sid=mr.sid,
+                       e2s=state.e2s.copy(), s2e=state.s2e.copy(), prio=state.prio.copy(),
+                       stamp=state.stamp)
+            if mode == GATHER and pool is not None:
+                gather(host, pool, mr.miss_e, mr.miss_s)
+        y = expert_ffn(x[t0:t1], rows, offset, k, host, H, I)
+        if mode == ZERO_RETURN:
+            resident = state.e2s[cids] >= 0
+            o, r, m = combine(y, w[t0:t1], pos, t1 - t0, k, resident)
+            out[t0:t1], out_res[t0:t1], out_miss[t0:t1] = o, r, m
+        else:
+            out[t0:t1] = combine(y, w[t0:t1], pos, t1 - t0, k)
+        chunks.append(rec)
+    res = {"ids": ids, "w": w, "logits": logits, "out": out, "chunks": chunks}
+    if mode == ZERO_RETURN:
+        res["out_res"], res["out_miss"] = out_res, out_miss
+    return res

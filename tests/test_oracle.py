@@ -1,0 +1,448 @@
+"""Pins for the CPU oracle, independent of the oracle itself.
+
+Each test checks the oracle against something it does not compute from:
+hand-derived fixtures (tests/golden), closed forms, exact integer sums,
+error bounds, library routines (numpy/torch sort, topk, matmul), a second
+cache model written differently, and brute-force dense evaluation.
+"""
+import itertools
+import json
+import math
+import os
+from collections import OrderedDict
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from harness import configs as C
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _gold(name):
+    with open(os.path.join(GOLD, name)) as f:
+        return json.load(f)
+
+
+def _bf16(a):
+    return torch.tensor(np.asarray(a, dtype=np.float32)).to(torch.bfloat16).float().numpy()
+
+
+# ----------------------------------------------------------------------------
+# Router logits
+# ----------------------------------------------------------------------------
+
+def test_logit_order_golden():
+    g = _gold("logit_order.json")
+    x = np.array([g["x"]], dtype=np.float32)
+    w = np.array(g["w"], dtype=np.float32)[:, None]
+    assert O.router_logits(x, w)[0, 0] == np.float32(g["logit"])
+    assert g["exact_sum"] == sum(a * b for a, b in zip(g["x"], g["w"]))
+
+
+def test_logits_exact_on_small_integers():
+    rng = np.random.default_rng(7)
+    x = rng.integers(-8, 9, size=(5, 64)).astype(np.float32)
+    w = rng.integers(-8, 9, size=(64, 12)).astype(np.float32)
+    exact = [[sum(int(x[t, h]) * int(w[h, e]) for h in range(64)) for e in range(12)] for t in range(5)]
+    assert np.array_equal(O.router_logits(x, w), np.array(exact, dtype=np.float32))
+
+
+def test_logits_within_sequential_error_bound():
+    rng = np.random.default_rng(8)
+    T, H, E = 3, 512, 9
+    x = _bf16(rng.normal(0, 1, (T, H)))
+    w = _bf16(rng.normal(0, 0.02, (H, E)))
+    got = O.router_logits(x, w)
+    u = 2.0 ** -24
+    gam = H * u / (1 - H * u)
+    for t in range(T):
+        for e in range(E):
+            prods = [Fraction(float(x[t, h])) * Fraction(float(w[h, e])) for h in range(H)]
+            exact = sum(prods)
+            bound = gam * float(sum(abs(p) for p in prods))
+            assert abs(float(got[t, e]) - float(exact)) <= bound
+
+
+def test_logit_offset_added_after_sum():
+    x = np.array([[1.0, 2.0]], dtype=np.float32)
+    w = np.array([[1.0, 0.5], [0.25, 2.0]], dtype=np.float32)
+    off = np.array([10.0, -1.0], dtype=np.float32)
+    assert np.array_equal(O.router_logits(x, w, off), np.array([[11.5, 3.5]], dtype=np.float32))
+
+
+# ----------------------------------------------------------------------------
+# Top-k, weights, bias
+# ----------------------------------------------------------------------------
+
+def test_route_examples_golden():
+    g = _gold("route_examples.json")
+    logits = np.array([g["logits"]], dtype=np.float32)
+    for case in g["cases"]:
+        bias = None if case["bias"] is None else np.array(case["bias"], dtype=np.float32)
+        ids = O.select_topk(logits, g["k"], bias)
+        assert ids[0].tolist() == case["ids"]
+        w = O.route_weights(logits, ids)
+        assert np.allclose(w[0], case["w"], atol=1e-9)
+
+
+def _topk_by_counting(scores, k):
+    # rank(e) = number of experts ahead of e; the expert of rank j is the j-th pick
+    E = len(scores)
+    rank = [sum(1 for f in range(E) if scores[f] > scores[e] or (scores[f] == scores[e] and f < e)) for e in range(E)]
+    return [rank.index(j) for j in range(k)]
+
+
+def test_topk_matches_counting_definition_with_ties():
+    rng = np.random.default_rng(3)
+    for _ in range(50):
+        E, k = int(rng.integers(4, 20)), int(rng.integers(1, 4))
+        s = rng.integers(-3, 4, size=(2, E)).astype(np.float32)  # many ties
+        ids = O.select_topk(s, k)
+        for t in range(2):
+            assert ids[t].tolist() == _topk_by_counting(s[t].tolist(), k)
+
+
+def test_topk_matches_torch_on_distinct_scores():
+    rng = np.random.default_rng(4)
+    s = rng.normal(size=(16, 128)).astype(np.float32)
+    ids = O.select_topk(s, 8)
+    ref = torch.topk(torch.from_numpy(s), 8, dim=1, sorted=True).indices.numpy()
+    assert np.array_equal(ids, ref)
+
+
+def test_weights_closed_forms():
+    rng = np.random.default_rng(5)
+    logits = rng.normal(size=(6, 32)).astype(np.float32)
+    ids = O.select_topk(logits, 5)
+    w = O.route_weights(logits, ids)
+    assert np.allclose(w.sum(1), 1.0, atol=1e-12)
+    for t in range(6):
+        for a, b in itertools.combinations(range(5), 2):
+            r = math.exp(float(logits[t, ids[t, a]]) - float(logits[t, ids[t, b]]))
+            assert w[t, a] / w[t, b] == pytest.approx(r, rel=1e-12)
+    ids1 = O.select_topk(logits, 1)
+    assert np.all(O.route_weights(logits, ids1) == 1.0)
+
+
+def test_bias_table_golden():
+    g = _gold("bias_table.json")
+    b = np.array(g["b"], dtype=np.float32)
+    got = O.bias_table(b, g["n_hot"], g["cap"])
+    assert np.allclose(got, g["bias"], atol=1e-6)
+    assert np.array_equal(O.bias_table(b, g["n_hot"], 0.0), np.array(g["cap_zero_bias"], dtype=np.float32))
+    assert np.zeros((48, 512), dtype=np.float32).nbytes == g["table_bytes_48x512_fp32"]
+
+
+def test_bias_rounding_is_one_fp32_round_of_fp64():
+    rng = np.random.default_rng(9)
+    b = rng.random(64).astype(np.float32) ** 3
+    got = O.bias_table(b, 16, -2.0)
+    hot = sorted(range(64), key=lambda e: (-float(b[e]), e))[:16]
+    edge = min(float(b[e]) for e in hot)
+    for e in range(64):
+        want = 0.0 if e in hot else max(-2.0, math.log(float(b[e]) / edge))
+        assert got[e] == np.float32(want)
+
+
+def test_zero_bias_reproduces_unbiased_topk():
+    cfg = C.FLASH.with_(T=8, H=256, E=64, k=10, I=64)
+    x = C.draw_x(cfg).float().numpy()
+    wr = C.draw_router(cfg).float().numpy()
+    logits = O.router_logits(x, wr)
+    b, _ = C.draw_brightness(cfg)
+    bias0 = O.bias_table(b, 16, 0.0)
+    assert np.all(bias0 == 0.0)
+    assert np.array_equal(O.select_topk(logits, 10, bias0), O.select_topk(logits, 10))
+    # a real bias moves picks towards the hot set but leaves the weights the router's own
+    bias = O.bias_table(b, 16, -1.0)
+    ids_b = O.select_topk(logits, 10, bias)
+    w_b = O.route_weights(logits, ids_b)
+    for t in range(8):
+        l = np.array([float(logits[t, e]) for e in ids_b[t]])
+        assert np.allclose(w_b[t], np.exp(l - l.max()) / np.exp(l - l.max()).sum())
+
+
+# ----------------------------------------------------------------------------
+# Permute
+# ----------------------------------------------------------------------------
+
+def test_permute_matches_stable_sort():
+    rng = np.random.default_rng(11)
+    for T, k, E in [(1, 1, 4), (7, 3, 5), (64, 8, 128), (33, 10, 512)]:
+        ids = rng.integers(0, E, size=(T, k)).astype(np.int32)
+        count, offset, rows, pos = O.permute(ids, E)
+        flat = ids.reshape(-1)
+        assert np.array_equal(rows, np.argsort(flat, kind="stable"))
+        assert np.array_equal(count, np.bincount(flat, minlength=E))
+        assert offset[0] == 0 and offset[E] == T * k
+        assert np.array_equal(rows[pos], np.arange(T * k))
+        for e in range(E):
+            assert np.all(flat[rows[offset[e]:offset[e + 1]]] == e)
+
+
+# ----------------------------------------------------------------------------
+# Manage / gather
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("trace", _gold("manage_traces.json")["traces"], ids=lambda t: t["name"])
+def test_manage_golden_traces(trace):
+    st = O.CacheState.from_slots(trace["s2e0"], trace["E"])
+    for step in trace["steps"]:
+        r = O.manage(st, np.array(step["ids"]), trace["policy"])
+        assert r.miss_e == step["miss_e"]
+        assert r.miss_s == step["miss_s"]
+        assert r.hit_e == step["hit_e"]
+        assert r.sid.tolist() == step["sid"]
+        assert st.s2e.tolist() == step["s2e"]
+        assert st.e2s.tolist() == step["e2s"]
+        assert st.prio.tolist() == step["prio"]
+        assert st.stamp == step["stamp"]
+
+
+class _SecondModel:
+    """An independently written cache model: per-slot records, greedy victim picking."""
+
+    def __init__(self, s2e0, E, policy):
+        self.E, self.policy = E, policy
+        self.occ = OrderedDict((s, int(e)) for s, e in enumerate(s2e0))
+        self.score = {s: 0 for s in self.occ}
+        self.calls = 0
+
+    def step(self, ids):
+        self.calls += 1
+        want = sorted(set(int(e) for e in ids))
+        where = {e: s for s, e in self.occ.items() if e >= 0}
+        hits = [e for e in want if e in where]
+        miss = [e for e in want if e not in where]
+        for e in hits:
+            if self.policy == O.LRU:
+                self.score[where[e]] = self.calls
+            elif self.policy == O.LFU:
+                self.score[where[e]] += 1
+        taken = {where[e] for e in hits}
+        placed = []
+        for e in miss:
+            if self.policy == O.STATIC:
+                placed.append(-1)
+                continue
+            free = [s for s, v in self.occ.items() if v < 0 and s not in taken]
+            if free:
+                s = min(free)
+            else:
+                s = min((s for s in self.occ if s not in taken), key=lambda s: (self.score[s], s))
+            self.occ[s] = e
+            self.score[s] = self.calls if self.policy == O.LRU else 1
+            taken.add(s)
+            placed.append(s)
+        return miss, placed
+
+    def tables(self):
+        s2e = [self.occ[s] for s in range(len(self.occ))]
+        e2s = [-1] * self.E
+        for s, e in enumerate(s2e):
+            if e >= 0:
+                e2s[e] = s
+        return s2e, e2s, [self.score[s] for s in range(len(self.occ))]
+
+
+def _zipf_ids(rng, steps, T, k, E, s=1.1):
+    p = np.arange(1, E + 1, dtype=np.float64) ** -s
+    p /= p.sum()
+    perm = rng.permutation(E)
+    out = []
+    for _ in range(steps):
+        rows = [perm[rng.choice(E, size=k, replace=False, p=p)] for _ in range(T)]
+        out.append(np.array(rows, dtype=np.int32))
+    return out
+
+
+@pytest.mark.parametrize("policy", [O.LRU, O.LFU, O.STATIC])
+@pytest.mark.parametrize("dist", ["uniform", "zipf"])
+def test_manage_matches_second_model(policy, dist):
+    rng = np.random.default_rng(100 + policy)
+    E, S, T, k = 32, 12, 3, 4
+    s2e0 = rng.permutation(E)[:S].astype(np.int32)
+    s2e0[rng.integers(0, S)] = -1
+    st = O.CacheState.from_slots(s2e0, E)
+    m = _SecondModel(s2e0, E, policy)
+    if dist == "zipf":
+        traces = _zipf_ids(rng, 60, T, k, E)
+    else:
+        traces = [np.stack([rng.choice(E, k, replace=False) for _ in range(T)]).astype(np.int32) for _ in range(60)]
+    for ids in traces:
+        r = O.manage(st, ids, policy)
+        miss, placed = m.step(ids.reshape(-1))
+        assert r.miss_e == miss and r.miss_s == placed
+        s2e, e2s, score = m.tables()
+        assert st.s2e.tolist() == s2e and st.e2s.tolist() == e2s
+        assert st.prio.tolist() == score
+
+
+@pytest.mark.parametrize("policy", [O.LRU, O.LFU])
+def test_manage_invariants(policy):
+    rng = np.random.default_rng(200 + policy)
+    E, S, T, k = 64, 24, 3, 8
+    st = O.CacheState.from_slots(rng.permutation(E)[:S], E)
+    for ids in _zipf_ids(rng, 80, T, k, E):
+        before = set(int(e) for e in np.nonzero(st.e2s >= 0)[0])
+        need = set(int(e) for e in ids.reshape(-1))
+        used_slots = {int(st.e2s[e]) for e in need & before}
+        r = O.manage(st, ids, policy)
+        assert len(r.miss_e) == len(need - before)
+        assert not (set(r.miss_s) & used_slots)
+        assert all(st.e2s[e] >= 0 for e in need)
+        for s, e in enumerate(st.s2e):
+            if e >= 0:
+                assert st.e2s[e] == s
+        assert np.sum(st.e2s >= 0) == np.sum(st.s2e >= 0)
+        assert np.array_equal(r.sid, st.e2s[ids])
+
+
+def test_manage_all_resident_never_misses():
+    E = 16
+    st = O.CacheState.from_slots(np.arange(E), E)
+    rng = np.random.default_rng(1)
+    for _ in range(20):
+        r = O.manage(st, rng.integers(0, E, size=(4, 2)), O.LRU)
+        assert r.miss_e == []
+        assert np.array_equal(st.s2e, np.arange(E))
+
+
+def test_manage_capacity_and_chunking():
+    st = O.CacheState.from_slots(np.arange(4), 8)
+    with pytest.raises(O.CapacityError):
+        O.manage(st, np.arange(5).reshape(1, 5), O.LRU)
+    assert O.chunk_tokens(64, 8, 64, 128) == 8
+    assert O.chunk_tokens(8, 8, 64, 128) == 8
+    assert O.chunk_tokens(64, 8, 128, 128) == 64
+    with pytest.raises(O.CapacityError):
+        O.chunk_tokens(4, 8, 6, 128)
+
+
+def test_gather_copies_bytes():
+    rng = np.random.default_rng(2)
+    host = rng.integers(0, 2 ** 16, size=(8, 40), dtype=np.uint16)
+    pool = np.zeros((3, 40), dtype=np.uint16)
+    O.gather(host, pool, [5, 1], [2, 0])
+    assert np.array_equal(pool[2], host[5]) and np.array_equal(pool[0], host[1])
+    assert not pool[1].any()
+
+
+# ----------------------------------------------------------------------------
+# FFN and combine
+# ----------------------------------------------------------------------------
+
+def test_silu_closed_forms():
+    z = np.array([0.0, math.log(3.0), -math.log(3.0)])
+    assert np.allclose(O.silu(z), [0.0, 0.75 * math.log(3.0), -0.25 * math.log(3.0)], rtol=1e-15, atol=0)
+
+
+def test_swiglu_closed_form():
+    H, I = 8, 4
+    a = [0.0, math.log(3.0), -math.log(3.0), 2.0]
+    bu = [1.0, 2.0, -4.0, 0.5]
+    c = [3.0, 1.0, 2.0, -1.0]
+    wg = np.zeros((H, I)); wu = np.zeros((H, I)); wd = np.zeros((I, H))
+    wg[0] = a
+    wu[0] = bu
+    for i in range(I):
+        wd[i, i + 2] = c[i]
+    slab = np.concatenate([wg.ravel(), wu.ravel(), wd.ravel()])
+    x = np.zeros((1, H)); x[0, 0] = 1.0
+    y = O.swiglu_expert(x, slab, H, I)[0]
+    want = np.zeros(H)
+    for i in range(I):
+        s = a[i] / (1.0 + math.exp(-a[i]))
+        want[i + 2] = s * bu[i] * c[i]
+    assert np.allclose(y, want, rtol=1e-14, atol=1e-15)
+    assert y[4] == pytest.approx(-0.25 * math.log(3.0) * -4.0 * 2.0, rel=1e-14)
+
+
+def test_swiglu_matches_explicit_loops():
+    rng = np.random.default_rng(12)
+    H, I, n = 6, 5, 3
+    slab = rng.normal(size=3 * H * I)
+    x = rng.normal(size=(n, H))
+    y = O.swiglu_expert(x, slab, H, I)
+    for r in range(n):
+        h = []
+        for i in range(I):
+            g = sum(x[r, q] * slab[q * I + i] for q in range(H))
+            u = sum(x[r, q] * slab[H * I + q * I + i] for q in range(H))
+            h.append(g / (1 + math.exp(-g)) * u)
+        for o in range(H):
+            yo = sum(h[i] * slab[2 * H * I + i * H + o] for i in range(I))
+            assert y[r, o] == pytest.approx(yo, rel=1e-12, abs=1e-14)
+
+
+def _tiny_inputs(cfg=C.TINY):
+    x = C.draw_x(cfg).float().numpy()
+    wr = C.draw_router(cfg).float().numpy()
+    host = C.draw_slabs(cfg).float().numpy()
+    return x, wr, host
+
+
+def test_layer_matches_dense_bruteforce():
+    """Tiny config: evaluate every expert on every token, mask to the top-k, weight."""
+    cfg = C.TINY
+    x, wr, host = _tiny_inputs(cfg)
+    res = O.layer_forward(x, wr, host, cfg.H, cfg.I, cfg.k, O.RESIDENT)
+    logits = O.router_logits(x, wr)
+    dense = np.stack([O.swiglu_expert(x, host[e], cfg.H, cfg.I) for e in range(cfg.E)])  # [E][T][H]
+    ids = O.select_topk(logits, cfg.k)
+    want = np.zeros((cfg.T, cfg.H))
+    for t in range(cfg.T):
+        mask = np.zeros(cfg.E, dtype=bool)
+        mask[ids[t]] = True
+        l = logits[t].astype(np.float64)
+        p = np.where(mask, np.exp(l - l[mask].max()), 0.0)
+        p /= p.sum()
+        want[t] = (p[:, None] * dense[:, t, :]).sum(0)
+    assert np.allclose(res["out"], want, rtol=1e-12, atol=1e-14)
+    assert np.abs(want).max() > 0.01
+
+
+def test_ffn_matches_torch_fp64_matmul():
+    cfg = C.TINY
+    x, wr, host = _tiny_inputs(cfg)
+    e = 3
+    xt = torch.from_numpy(x).double()
+    s = torch.from_numpy(host[e]).double()
+    n = cfg.H * cfg.I
+    wg, wu, wd = s[:n].view(cfg.H, cfg.I), s[n:2 * n].view(cfg.H, cfg.I), s[2 * n:].view(cfg.I, cfg.H)
+    ref = torch.matmul(torch.nn.functional.silu(xt @ wg) * (xt @ wu), wd).numpy()
+    assert np.allclose(O.swiglu_expert(x, host[e], cfg.H, cfg.I), ref, rtol=1e-12, atol=1e-14)
+
+
+def test_zero_return_partials_sum_to_full():
+    cfg = C.TINY.with_(S=6)
+    x, wr, host = _tiny_inputs(cfg)
+    full = O.layer_forward(x, wr, host, cfg.H, cfg.I, cfg.k, O.RESIDENT)
+    st = O.CacheState.from_slots(C.initial_residency(cfg.with_(S=6)), cfg.E)
+    zr = O.layer_forward(x, wr, host, cfg.H, cfg.I, cfg.k, O.ZERO_RETURN, O.STATIC, st)
+    assert np.allclose(zr["out_res"] + zr["out_miss"], full["out"], rtol=1e-12, atol=1e-14)
+    assert np.abs(zr["out_miss"]).max() > 0 and np.abs(zr["out_res"]).max() > 0
+    st_all = O.CacheState.from_slots(np.arange(cfg.E), cfg.E)
+    zr_all = O.layer_forward(x, wr, host, cfg.H, cfg.I, cfg.k, O.ZERO_RETURN, O.STATIC, st_all)
+    assert np.all(zr_all["out_miss"] == 0.0)
+    assert np.array_equal(zr_all["out_res"], zr_all["out"])
+
+
+def test_gather_mode_chunked_equals_resident():
+    cfg = C.TINY.with_(T=9, S=5, k=2)
+    x = C.draw_x(cfg).float().numpy()
+    wr = C.draw_router(cfg).float().numpy()
+    host = C.draw_slabs(cfg).float().numpy()
+    full = O.layer_forward(x, wr, host, cfg.H, cfg.I, cfg.k, O.RESIDENT)
+    s2e0 = C.initial_residency(cfg)
+    st = O.CacheState.from_slots(s2e0, cfg.E)
+    pool = host[s2e0].copy()
+    g = O.layer_forward(x, wr, host, cfg.H, cfg.I, cfg.k, O.GATHER, O.LRU, st, pool)
+    assert len(g["chunks"]) == 5  # floor(5/2) = 2 tokens per chunk
+    assert np.allclose(g["out"], full["out"], rtol=1e-12, atol=1e-14)
+    for s, e in enumerate(st.s2e):
+        assert np.array_equal(pool[s], host[e])
