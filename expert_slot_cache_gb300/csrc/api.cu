@@ -1,0 +1,228 @@
+// C ABI entry points that compose the kernels: the expert FFN, the combine and
+// the whole layer forward (route, then per chunk permute, manage, gather on
+// the side stream overlapped with the hit experts' FFN, the missed experts'
+// FFN, combine).
+#include <algorithm>
+#include <mutex>
+
+#include "internal.cuh"
+
+namespace moe {
+
+static bool shape_ok(int T, int H, int I, int k, int E) {
+  return T >= 1 && H >= 64 && H % 64 == 0 && I >= 32 && I % 32 == 0 && k >= 1 && k <= kMaxK && E >= k &&
+         E <= kMaxE;
+}
+
+static size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+// Workspace layout of the layer forward, for chunks of up to n = C*k routing slots.
+struct LayerWs {
+  int32_t *count, *offset, *rows, *pos, *act_e, *n_act, *miss_e, *miss_s, *n_miss, *hit_e, *n_hit;
+  float *hbuf, *y;
+  size_t bytes;
+};
+
+static LayerWs carve(void* base, int n, int H, int E, int I) {
+  LayerWs w{};
+  size_t off = 0;
+  char* b = (char*)base;
+  auto take = [&](size_t bytes) {
+    char* p = b ? b + off : nullptr;
+    off += align256(bytes);
+    return p;
+  };
+  const int lmax = std::min(n, E);
+  w.count = (int32_t*)take(4 * (size_t)E);
+  w.offset = (int32_t*)take(4 * (size_t)(E + 1));
+  w.rows = (int32_t*)take(4 * (size_t)n);
+  w.pos = (int32_t*)take(4 * (size_t)n);
+  w.act_e = (int32_t*)take(4 * (size_t)E);
+  w.n_act = (int32_t*)take(4);
+  w.miss_e = (int32_t*)take(4 * (size_t)lmax);
+  w.miss_s = (int32_t*)take(4 * (size_t)lmax);
+  w.n_miss = (int32_t*)take(4);
+  w.hit_e = (int32_t*)take(4 * (size_t)lmax);
+  w.n_hit = (int32_t*)take(4);
+  w.hbuf = (float*)take(4 * (size_t)n * I);
+  w.y = (float*)take(4 * (size_t)n * H);
+  w.bytes = off;
+  return w;
+}
+
+static int chunk_tokens(int T, int k, int S, int E, int mode, int policy) {
+  if (mode != MOE_MODE_GATHER || policy == MOE_POLICY_STATIC) return T;
+  if (S >= E || T * k <= S) return T;
+  return S / k;
+}
+
+// Two cached events per device for the fork/join with the side stream.
+struct DevEvents {
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+static DevEvents g_events[64];
+static std::mutex g_events_mu;
+
+static int get_events(DevEvents** out) {
+  int dev = 0;
+  MOE_CUDA_TRY(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_events_mu);
+  DevEvents& d = g_events[dev];
+  if (!d.fork) {
+    MOE_CUDA_TRY(cudaEventCreateWithFlags(&d.fork, cudaEventDisableTiming));
+    MOE_CUDA_TRY(cudaEventCreateWithFlags(&d.join, cudaEventDisableTiming));
+  }
+  *out = &d;
+  return MOE_OK;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" const char* moe_status_str(int s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_ARG: return "invalid argument";
+    case MOE_ERR_CAPACITY: return "step needs more slots than the pool holds";
+    case MOE_ERR_ALIGN: return "slab size or pointer not a 16-byte multiple (or workspace too small)";
+    case MOE_ERR_NOT_DEVICE_ACCESSIBLE: return "host store is not addressable by the device";
+    case MOE_ERR_CUDA: return "CUDA runtime error";
+    case MOE_ERR_DEVICE_STATUS: return "a kernel reported an invalid item";
+    default: return "unknown status";
+  }
+}
+
+extern "C" size_t moe_ffn_workspace_bytes(int T, int k, int I) {
+  if (T < 1 || k < 1 || I < 1) return 0;
+  return align256(4 * (size_t)T * k * I);
+}
+
+extern "C" int moe_expert_ffn(const void* x, int T, int H, int I, int k, int E, const int32_t* offset,
+                              const int32_t* rows, const int32_t* list_e, const int32_t* n_list, int max_list,
+                              const void* pool, const int32_t* e2s, const void* host_slabs, float* y,
+                              void* workspace, size_t workspace_bytes, int32_t* dev_status, moe_stream_t stream) {
+  if (!x || !offset || !rows || !list_e || !n_list || !pool || !y || !workspace) return MOE_ERR_ARG;
+  if (!shape_ok(T, H, I, k, E) || max_list < 0) return MOE_ERR_ARG;
+  if ((uintptr_t)pool % 16 || (uintptr_t)y % 16 || (uintptr_t)workspace % 16) return MOE_ERR_ALIGN;
+  if (workspace_bytes < moe_ffn_workspace_bytes(T, k, I)) return MOE_ERR_ALIGN;
+  if (host_slabs) {
+    if ((uintptr_t)host_slabs % 16) return MOE_ERR_ALIGN;
+    const int acc = check_host_accessible(host_slabs);
+    if (acc != MOE_OK) return acc;
+  }
+  FfnArgs a{(const uint16_t*)x, T, H, I, k, E, offset, rows, list_e, n_list, (const uint16_t*)pool, e2s,
+            (const uint16_t*)host_slabs, (size_t)3 * H * I, (float*)workspace, y, dev_status};
+  return launch_ffn(a, std::min(max_list, E), (cudaStream_t)stream);
+}
+
+extern "C" int moe_combine(const float* y, const float* w, const int32_t* pos, const int32_t* ids, const int32_t* e2s,
+                           int T, int k, int H, int E, int split, void* out, float* out_res, float* out_miss,
+                           moe_stream_t stream) {
+  if (!y || !w || !pos || !out || T < 1 || k < 1 || k > kMaxK || H < 4 || H % 4 || E < 1) return MOE_ERR_ARG;
+  if (split && (!ids || !e2s || !out_res || !out_miss)) return MOE_ERR_ARG;
+  if ((uintptr_t)y % 16 || (uintptr_t)out % 8) return MOE_ERR_ALIGN;
+  if (split && ((uintptr_t)out_res % 16 || (uintptr_t)out_miss % 16)) return MOE_ERR_ALIGN;
+  return launch_combine(y, w, pos, ids, e2s, T, k, H, E, split, out, out_res, out_miss, (cudaStream_t)stream);
+}
+
+extern "C" size_t moe_layer_workspace_bytes(int T, int H, int E, int k, int I, int S) {
+  if (T < 1 || k < 1 || E < 1 || S < 1) return 0;
+  // Worst case over modes: the largest chunk is all T tokens.
+  return carve(nullptr, T * k, H, E, I).bytes;
+}
+
+extern "C" int moe_layer_forward(const moe_layer_args* a, moe_stream_t main_s, moe_stream_t side_s) {
+  if (!a) return MOE_ERR_ARG;
+  const int T = a->T, H = a->H, E = a->E, k = a->k, I = a->I, S = a->S;
+  if (!shape_ok(T, H, I, k, E) || S < 1) return MOE_ERR_ARG;
+  if (!a->x || !a->w_router || !a->pool || !a->ids || !a->w || !a->out || !a->workspace) return MOE_ERR_ARG;
+  const int mode = a->mode, policy = a->policy;
+  if (mode < MOE_MODE_RESIDENT || mode > MOE_MODE_ZERO_RETURN) return MOE_ERR_ARG;
+  if (mode == MOE_MODE_GATHER && policy != MOE_POLICY_LRU && policy != MOE_POLICY_LFU) return MOE_ERR_ARG;
+  if (mode == MOE_MODE_ZERO_RETURN && policy != MOE_POLICY_STATIC) return MOE_ERR_ARG;
+  if (mode != MOE_MODE_RESIDENT) {
+    if (!a->e2s || !a->s2e || !a->prio || !a->stamp || !a->host_slabs) return MOE_ERR_ARG;
+    if ((uintptr_t)a->host_slabs % 16) return MOE_ERR_ALIGN;
+    const int acc = check_host_accessible(a->host_slabs);
+    if (acc != MOE_OK) return acc;
+  } else if (!a->e2s && S < E) {
+    return MOE_ERR_ARG;
+  }
+  if (mode == MOE_MODE_ZERO_RETURN && (!a->out_res || !a->out_miss)) return MOE_ERR_ARG;
+  if (mode == MOE_MODE_GATHER && S < E && S < k) return MOE_ERR_CAPACITY;
+  if ((uintptr_t)a->pool % 16 || (uintptr_t)a->workspace % 256) return MOE_ERR_ALIGN;
+
+  const int C = chunk_tokens(T, k, S, E, mode, policy);
+  LayerWs ws = carve(a->workspace, C * k, H, E, I);
+  if (a->workspace_bytes < ws.bytes) return MOE_ERR_ALIGN;
+
+  cudaStream_t ms = (cudaStream_t)main_s;
+  cudaStream_t ss = (cudaStream_t)side_s;
+  const bool two = ss != nullptr && ss != ms;
+  DevEvents* ev = nullptr;
+  if (two) {
+    const int r = get_events(&ev);
+    if (r != MOE_OK) return r;
+  }
+  int64_t* stats = a->stats;
+  const size_t slab_bytes = (size_t)6 * H * I;
+  int r = moe_route(a->x, a->w_router, a->logit_offset, a->sel_bias, T, H, E, k, nullptr, a->ids, a->w, main_s);
+  if (r != MOE_OK) return r;
+
+  for (int t0 = 0; t0 < T; t0 += C) {
+    const int tc = std::min(C, T - t0);
+    const int n = tc * k;
+    const int lmax = std::min(n, E);
+    const int32_t* ids_c = a->ids + (size_t)t0 * k;
+    r = moe_permute(ids_c, n, E, ws.count, ws.offset, ws.rows, ws.pos, ws.act_e, ws.n_act, a->dev_status, main_s);
+    if (r != MOE_OK) return r;
+    FfnArgs f{(const uint16_t*)a->x + (size_t)t0 * H, tc, H, I, k, E, ws.offset, ws.rows, nullptr, nullptr,
+              (const uint16_t*)a->pool, a->e2s, (const uint16_t*)a->host_slabs, (size_t)3 * H * I, ws.hbuf, ws.y,
+              a->dev_status};
+    if (mode == MOE_MODE_RESIDENT) {
+      f.list_e = ws.act_e;
+      f.n_list = ws.n_act;
+      f.host = nullptr;
+      if ((r = launch_ffn(f, lmax, ms)) != MOE_OK) return r;
+    } else {
+      r = launch_manage(ids_c, n, E, S, policy, a->e2s, a->s2e, a->prio, a->stamp, ws.miss_e, ws.miss_s, ws.n_miss,
+                        ws.hit_e, ws.n_hit, nullptr, stats, a->dev_status, ms);
+      if (r != MOE_OK) return r;
+      FfnArgs fh = f, fm = f;
+      fh.list_e = ws.hit_e;
+      fh.n_list = ws.n_hit;
+      fm.list_e = ws.miss_e;
+      fm.n_list = ws.n_miss;
+      if (two) {
+        MOE_CUDA_TRY(cudaEventRecord(ev->fork, ms));
+        MOE_CUDA_TRY(cudaStreamWaitEvent(ss, ev->fork, 0));
+      }
+      cudaStream_t side = two ? ss : ms;
+      if (mode == MOE_MODE_GATHER) {
+        // side: gather the misses; main: the hit experts' FFN meanwhile; then the misses.
+        r = launch_gather(a->host_slabs, a->pool, slab_bytes, E, S, ws.miss_e, ws.miss_s, ws.n_miss, lmax, stats,
+                          a->dev_status, side);
+        if (r != MOE_OK) return r;
+        if (two) MOE_CUDA_TRY(cudaEventRecord(ev->join, ss));
+        if ((r = launch_ffn(fh, lmax, ms)) != MOE_OK) return r;
+        if (two) MOE_CUDA_TRY(cudaStreamWaitEvent(ms, ev->join, 0));
+        if ((r = launch_ffn(fm, lmax, ms)) != MOE_OK) return r;
+      } else {
+        // zero-return: resident experts from the pool on main, missing ones
+        // straight from the host store on the side stream; then one add.
+        if ((r = launch_ffn(fm, lmax, side)) != MOE_OK) return r;
+        if (two) MOE_CUDA_TRY(cudaEventRecord(ev->join, ss));
+        if ((r = launch_ffn(fh, lmax, ms)) != MOE_OK) return r;
+        if (two) MOE_CUDA_TRY(cudaStreamWaitEvent(ms, ev->join, 0));
+      }
+    }
+    const int split = mode == MOE_MODE_ZERO_RETURN;
+    r = launch_combine(ws.y, a->w + (size_t)t0 * k, ws.pos, ids_c, a->e2s, tc, k, H, E, split,
+                       (uint16_t*)a->out + (size_t)t0 * H, split ? a->out_res + (size_t)t0 * H : nullptr,
+                       split ? a->out_miss + (size_t)t0 * H : nullptr, ms);
+    if (r != MOE_OK) return r;
+  }
+  return MOE_OK;
+}

@@ -1,0 +1,279 @@
+// expert_cache_manage and expert_cache_gather.
+//
+// "Porting vllm-expert-cache to NVIDIA GPUs", "What this package does": per
+// MoE layer and step, manage picks victims among the slots this step does not
+// need and emits a miss list; gather copies the missing experts host-to-slot;
+// routing ids are remapped to slot space.  "Prove it is correct before
+// measuring": the manager must stay deterministic (no atomics, no
+// order-dependent reduction), the gather reads host memory from the device,
+// and per-expert slabs are 16-byte multiples.  "Betelgeuse ... on an RTX
+// 3060", "What it actually does under the hood": hits are resolved by an
+// in-stream kernel on the device, with no host synchronisation.
+#include <algorithm>
+
+#include "internal.cuh"
+
+namespace moe {
+
+constexpr int kManageThreads = 1024;
+constexpr int kMaxS = 4096;
+
+// Shared memory (dynamic): need[E] | e2s[E] | mrank[E] | hrank[E] | s2e[S] | prio[S] | cand[S] | vict[S]
+__global__ void __launch_bounds__(kManageThreads) manage_kernel(
+    const int32_t* __restrict__ ids, int n, int E, int S, int policy, int32_t* __restrict__ e2s_g,
+    int32_t* __restrict__ s2e_g, uint32_t* __restrict__ prio_g, uint32_t* __restrict__ stamp_g,
+    int32_t* __restrict__ miss_e, int32_t* __restrict__ miss_s, int32_t* __restrict__ n_miss,
+    int32_t* __restrict__ hit_e, int32_t* __restrict__ n_hit, int32_t* __restrict__ sid,
+    int64_t* __restrict__ stats, int32_t* __restrict__ status) {
+  extern __shared__ int man_smem[];
+  int* need = man_smem;
+  int* e2s = need + E;
+  int* mrank = e2s + E;
+  int* hrank = mrank + E;
+  int* s2e = hrank + E;
+  uint32_t* prio = reinterpret_cast<uint32_t*>(s2e + S);
+  int* cand = reinterpret_cast<int*>(prio + S);
+  int* vict = cand + S;
+  __shared__ int tmp[33];
+  __shared__ int s_nmiss, s_nhit;
+  const int tid = threadIdx.x;
+
+  for (int e = tid; e < E; e += kManageThreads) {
+    need[e] = 0;
+    e2s[e] = e2s_g[e];
+  }
+  for (int s = tid; s < S; s += kManageThreads) {
+    s2e[s] = s2e_g[s];
+    prio[s] = prio_g[s];
+    vict[s] = -1;
+  }
+  __syncthreads();
+  for (int i = tid; i < n; i += kManageThreads) {
+    const int e = ids[i];
+    if (e < 0 || e >= E) {
+      set_status(status, MOE_DEV_BAD_EXPERT);
+      continue;
+    }
+    need[e] = 1;  // same value from every writer
+  }
+  __syncthreads();
+  const uint32_t stamp = *stamp_g + 1u;
+
+  // Ranks of misses and hits in ascending expert order.
+  int carry_m = 0, carry_h = 0;
+  for (int e0 = 0; e0 < E; e0 += kManageThreads) {
+    const int e = e0 + tid;
+    const bool nd = e < E && need[e];
+    const bool res = nd && e2s[e] >= 0 && e2s[e] < S;
+    int tm, th;
+    const int xm = block_exclusive_scan(nd && !res ? 1 : 0, tmp, &tm);
+    const int xh = block_exclusive_scan(res ? 1 : 0, tmp, &th);
+    if (e < E) {
+      mrank[e] = nd && !res ? carry_m + xm : -1;
+      hrank[e] = res ? carry_h + xh : -1;
+    }
+    carry_m += tm;
+    carry_h += th;
+  }
+  if (tid == 0) {
+    s_nmiss = carry_m;
+    s_nhit = carry_h;
+  }
+  // Candidate slots: not holding an expert this step needs.
+  for (int s = tid; s < S; s += kManageThreads) {
+    const int e = s2e[s];
+    cand[s] = !(e >= 0 && e < E && need[e]);
+  }
+  __syncthreads();
+  const int nm = s_nmiss;
+
+  if (policy != MOE_POLICY_STATIC) {
+    // Victim rank of each candidate: empty first (ascending slot), then
+    // ascending prio, then ascending slot.
+    for (int s = tid; s < S; s += kManageThreads) {
+      if (!cand[s]) continue;
+      const bool es = s2e[s] < 0;
+      const uint32_t ps = prio[s];
+      int r = 0;
+      for (int q = 0; q < S; ++q) {
+        if (!cand[q] || q == s) continue;
+        const bool eq = s2e[q] < 0;
+        bool before;
+        if (eq != es)
+          before = eq;
+        else if (es)
+          before = q < s;
+        else
+          before = prio[q] < ps || (prio[q] == ps && q < s);
+        r += before;
+      }
+      if (r < nm) vict[r] = s;
+    }
+  }
+  __syncthreads();
+
+  // Apply.  Hit slots and victim slots are disjoint; evicted experts are
+  // resident, missing experts are not, so no two writes touch one entry.
+  for (int e = tid; e < E; e += kManageThreads) {
+    if (hrank[e] >= 0) {
+      const int s = e2s[e];
+      if (policy == MOE_POLICY_LRU) prio[s] = stamp;
+      else if (policy == MOE_POLICY_LFU) prio[s] = prio[s] + 1u;
+      if (hit_e) hit_e[hrank[e]] = e;
+    }
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += kManageThreads) {
+    const int r = mrank[e];
+    if (r < 0) continue;
+    miss_e[r] = e;
+    if (policy == MOE_POLICY_STATIC) {
+      miss_s[r] = -1;
+      continue;
+    }
+    const int s = vict[r];
+    miss_s[r] = s;
+    if (s < 0) {  // cannot happen when the step fits the pool (checked on the host)
+      set_status(status, MOE_DEV_BAD_SLOT);
+      continue;
+    }
+    const int old = s2e[s];
+    if (old >= 0 && old < E) e2s[old] = -1;
+    s2e[s] = e;
+    e2s[e] = s;
+    prio[s] = policy == MOE_POLICY_LRU ? stamp : 1u;
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += kManageThreads) e2s_g[e] = e2s[e];
+  for (int s = tid; s < S; s += kManageThreads) {
+    s2e_g[s] = s2e[s];
+    prio_g[s] = prio[s];
+  }
+  if (sid) {
+    for (int i = tid; i < n; i += kManageThreads) {
+      const int e = ids[i];
+      sid[i] = (e >= 0 && e < E) ? e2s[e] : -1;
+    }
+  }
+  if (tid == 0) {
+    *stamp_g = stamp;
+    *n_miss = nm;
+    if (n_hit) *n_hit = s_nhit;
+    if (stats) {
+      stats[0] += nm;
+      stats[1] += 1;
+    }
+  }
+}
+
+// Gather: each (miss, chunk) work item copies one chunk of a slab with
+// 16-byte loads from mapped pinned host memory.  Grid-stride over items; the
+// number of misses is read on the device.
+constexpr int kGatherThreads = 256;
+constexpr int kGatherUnroll = 8;
+constexpr int kGatherChunkVec = kGatherThreads * kGatherUnroll;  // 32 KB per item
+
+__global__ void __launch_bounds__(kGatherThreads) gather_kernel(const uint4* __restrict__ host,
+                                                                uint4* __restrict__ pool, size_t slab_vec,
+                                                                int E, int S, const int32_t* __restrict__ miss_e,
+                                                                const int32_t* __restrict__ miss_s,
+                                                                const int32_t* __restrict__ n_miss,
+                                                                int64_t* __restrict__ stats,
+                                                                int32_t* __restrict__ status) {
+  const int nm = *n_miss;
+  const size_t chunks = (slab_vec + kGatherChunkVec - 1) / kGatherChunkVec;
+  const size_t items = (size_t)nm * chunks;
+  for (size_t it = blockIdx.x; it < items; it += gridDim.x) {
+    const int m = (int)(it / chunks);
+    const size_t c = it - (size_t)m * chunks;
+    const int e = miss_e[m], s = miss_s[m];
+    if (e < 0 || e >= E || s < 0 || s >= S) {
+      if (threadIdx.x == 0) set_status(status, e < 0 || e >= E ? MOE_DEV_BAD_EXPERT : MOE_DEV_BAD_SLOT);
+      continue;
+    }
+    const uint4* src = host + (size_t)e * slab_vec + c * kGatherChunkVec;
+    uint4* dst = pool + (size_t)s * slab_vec + c * kGatherChunkVec;
+    const size_t lim = min((size_t)kGatherChunkVec, slab_vec - c * kGatherChunkVec);
+    uint4 v[kGatherUnroll];
+#pragma unroll
+    for (int u = 0; u < kGatherUnroll; ++u) {
+      const size_t j = threadIdx.x + (size_t)u * kGatherThreads;
+      if (j < lim) v[u] = ldg_stream(src + j);
+    }
+#pragma unroll
+    for (int u = 0; u < kGatherUnroll; ++u) {
+      const size_t j = threadIdx.x + (size_t)u * kGatherThreads;
+      if (j < lim) dst[j] = v[u];
+    }
+  }
+  if (stats && blockIdx.x == 0 && threadIdx.x == 0) stats[2] += (int64_t)nm * (int64_t)slab_vec * 16;
+}
+
+int launch_manage(const int32_t* ids, int n, int E, int S, int policy, int32_t* e2s, int32_t* s2e, uint32_t* prio,
+                  uint32_t* stamp, int32_t* miss_e, int32_t* miss_s, int32_t* n_miss, int32_t* hit_e,
+                  int32_t* n_hit, int32_t* sid, int64_t* stats, int32_t* dev_status, cudaStream_t stream) {
+  const size_t smem = (size_t)4 * E * sizeof(int) + (size_t)4 * S * sizeof(int);
+  static bool attr_done[64] = {};
+  MOE_CUDA_TRY(ensure_smem(manage_kernel, (int)(4 * kMaxE * 4 + 4 * kMaxS * 4), attr_done));
+  manage_kernel<<<1, kManageThreads, smem, stream>>>(ids, n, E, S, policy, e2s, s2e, prio, stamp, miss_e, miss_s,
+                                                     n_miss, hit_e, n_hit, sid, stats, dev_status);
+  MOE_LAUNCH_CHECK();
+  return MOE_OK;
+}
+
+int check_host_accessible(const void* p) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ERR_NOT_DEVICE_ACCESSIBLE;
+  }
+  if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) return MOE_OK;
+  if (a.type == cudaMemoryTypeHost && a.devicePointer == p) return MOE_OK;
+  return MOE_ERR_NOT_DEVICE_ACCESSIBLE;
+}
+
+int launch_gather(const void* host_slabs, void* pool, size_t slab_bytes, int E, int S, const int32_t* miss_e,
+                  const int32_t* miss_s, const int32_t* n_miss, int max_miss, int64_t* stats, int32_t* dev_status,
+                  cudaStream_t stream) {
+  if (max_miss <= 0) return MOE_OK;
+  const size_t slab_vec = slab_bytes / 16;
+  const size_t chunks = (slab_vec + kGatherChunkVec - 1) / kGatherChunkVec;
+  int sms = 0, dev = 0;
+  MOE_CUDA_TRY(cudaGetDevice(&dev));
+  MOE_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  const size_t items = (size_t)max_miss * chunks;
+  const int grid = (int)std::min<size_t>(items, (size_t)sms * 8);
+  gather_kernel<<<grid, kGatherThreads, 0, stream>>>((const uint4*)host_slabs, (uint4*)pool, slab_vec, E, S,
+                                                      miss_e, miss_s, n_miss, stats, dev_status);
+  MOE_LAUNCH_CHECK();
+  return MOE_OK;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" int moe_cache_manage(const int32_t* ids, int n, int E, int S, int policy, int32_t* e2s, int32_t* s2e,
+                                uint32_t* prio, uint32_t* stamp, int32_t* miss_e, int32_t* miss_s,
+                                int32_t* n_miss, int32_t* hit_e, int32_t* n_hit, int32_t* sid,
+                                int32_t* dev_status, moe_stream_t stream) {
+  if (!ids || !e2s || !s2e || !prio || !stamp || !miss_e || !miss_s || !n_miss) return MOE_ERR_ARG;
+  if ((hit_e == nullptr) != (n_hit == nullptr)) return MOE_ERR_ARG;
+  if (n < 1 || E < 1 || E > kMaxE || S < 1 || S > kMaxS) return MOE_ERR_ARG;
+  if (policy < MOE_POLICY_LRU || policy > MOE_POLICY_STATIC) return MOE_ERR_ARG;
+  if (policy != MOE_POLICY_STATIC && S < E && n > S) return MOE_ERR_CAPACITY;
+  return launch_manage(ids, n, E, S, policy, e2s, s2e, prio, stamp, miss_e, miss_s, n_miss, hit_e, n_hit, sid,
+                       nullptr, dev_status, (cudaStream_t)stream);
+}
+
+extern "C" int moe_cache_gather(const void* host_slabs, void* pool, size_t slab_bytes, int E, int S,
+                                const int32_t* miss_e, const int32_t* miss_s, const int32_t* n_miss,
+                                int max_miss, int32_t* dev_status, moe_stream_t stream) {
+  if (!host_slabs || !pool || !miss_e || !miss_s || !n_miss) return MOE_ERR_ARG;
+  if (E < 1 || S < 1 || max_miss < 0 || slab_bytes == 0) return MOE_ERR_ARG;
+  if (slab_bytes % 16 || (uintptr_t)host_slabs % 16 || (uintptr_t)pool % 16) return MOE_ERR_ALIGN;
+  const int acc = check_host_accessible(host_slabs);
+  if (acc != MOE_OK) return acc;
+  return launch_gather(host_slabs, pool, slab_bytes, E, S, miss_e, miss_s, n_miss, max_miss, nullptr, dev_status,
+                       (cudaStream_t)stream);
+}

@@ -1,0 +1,286 @@
+// Grouped SwiGLU expert FFN, weight-streaming form for decode-sized groups.
+//
+// "Porting vllm-expert-cache to NVIDIA GPUs", "What this package does": the
+// expert GEMM runs on slot-remapped ids.  "RTX 3060 runs a 35B MoE with
+// llama.cpp", chapter "Designing a fixed expert cache with zero-return for
+// missing experts": one pass over the experts in VRAM, one over the experts
+// still in host memory.
+//
+// Work is a device-side list of experts.  Each (expert, column tile) work
+// item streams that tile's weight columns once, 16 bytes per load, for all
+// the expert's tokens (processed in batches of <= 8).  Threads own 8 output
+// columns and walk the input dimension, with the activations broadcast from
+// shared memory, so a thread accumulates its outputs in registers; the
+// partial sums of the 32 k-groups are reduced in a fixed order.
+//   gate/up : tile = 32 columns of Wg and the same 32 of Wu; h = silu(g) * u
+//   down    : tile = 64 columns of Wd; y = h Wd
+#include <algorithm>
+
+#include "internal.cuh"
+
+namespace moe {
+
+constexpr int kFfnThreads = 256;
+constexpr int kRB = 8;       // tokens per batch (max)
+constexpr int kUnroll = 8;   // weight rows in flight per thread
+constexpr int kKG = 32;      // k-groups per CTA
+constexpr int kGUTile = 32;  // gate/up columns per tile
+constexpr int kDTile = 64;   // down columns per tile
+
+__device__ __forceinline__ void unpack8(const uint4 v, float* f) {
+  f[0] = bf16_lo(v.x);
+  f[1] = bf16_hi(v.x);
+  f[2] = bf16_lo(v.y);
+  f[3] = bf16_hi(v.y);
+  f[4] = bf16_lo(v.z);
+  f[5] = bf16_hi(v.z);
+  f[6] = bf16_lo(v.w);
+  f[7] = bf16_hi(v.w);
+}
+
+// Weights of expert e (slot copy when resident, else the host store).
+__device__ __forceinline__ const uint16_t* expert_weights(const FfnArgs& a, int e) {
+  if (!a.e2s) return a.pool + (size_t)e * a.slab_elems;
+  const int s = a.e2s[e];
+  if (s >= 0) return a.pool + (size_t)s * a.slab_elems;
+  return a.host ? a.host + (size_t)e * a.slab_elems : nullptr;
+}
+
+// Stream K rows of a [K][ldw] matrix for this thread's 8 columns (wcol = column
+// base) and accumulate acc[r][q] += w[row][q] * in[r][row] over rows
+// row = g + kKG * j.
+template <int RB>
+__device__ __forceinline__ void stream_rows(const uint16_t* __restrict__ wcol, int ldw, int K, int g,
+                                            const float* __restrict__ in_s, int ld_in, float (&acc)[RB][8]) {
+  constexpr int U = RB >= 8 ? kUnroll / 2 : kUnroll;
+  const int nrows = K / kKG;
+  for (int j0 = 0; j0 < nrows; j0 += U) {
+    uint4 wv[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int row = g + kKG * (j0 + u);
+      if (j0 + u < nrows) wv[u] = ldg_stream(wcol + (size_t)row * ldw);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (j0 + u < nrows) {
+        const int row = g + kKG * (j0 + u);
+        float wf[8];
+        unpack8(wv[u], wf);
+#pragma unroll
+        for (int r = 0; r < RB; ++r) {
+          const float xv = in_s[r * ld_in + row];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) acc[r][q] = fmaf(wf[q], xv, acc[r][q]);
+        }
+      }
+    }
+  }
+}
+
+// Reduce acc over the 4 k-groups of a warp (lanes differing in bits 3 and 4)
+// and store the warp partial of column-thread c = lane (lanes 0..7).
+template <int RB>
+__device__ __forceinline__ void warp_partials(float (&acc)[RB][8], float* __restrict__ red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int r = 0; r < RB; ++r)
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      float v = acc[r][q];
+      v += __shfl_xor_sync(MOE_FULL_MASK, v, 8);
+      v += __shfl_xor_sync(MOE_FULL_MASK, v, 16);
+      acc[r][q] = v;
+    }
+  if (lane < 8) {
+#pragma unroll
+    for (int r = 0; r < RB; ++r)
+#pragma unroll
+      for (int q = 0; q < 8; ++q) red[((warp * 8 + lane) * RB + r) * 8 + q] = acc[r][q];
+  }
+}
+
+template <int RB>
+__device__ __forceinline__ void gateup_batch(const FfnArgs& a, const uint16_t* __restrict__ w, int i0, int p0,
+                                             int nb, float* __restrict__ xs, float* __restrict__ red) {
+  const int tid = threadIdx.x, c = tid & 7, g = tid >> 3;
+  const int H = a.H, I = a.I;
+  for (int idx = tid; idx < RB * H; idx += kFfnThreads) {
+    const int r = idx / H, h = idx - r * H;
+    float v = 0.f;
+    if (r < nb) {
+      const int t = a.rows[p0 + r] / a.k;
+      v = bf16_to_f32(a.x[(size_t)t * H + h]);
+    }
+    xs[idx] = v;
+  }
+  __syncthreads();
+  float acc[RB][8];
+#pragma unroll
+  for (int r = 0; r < RB; ++r)
+#pragma unroll
+    for (int q = 0; q < 8; ++q) acc[r][q] = 0.f;
+  // c < 4: gate columns i0 + 8c; c >= 4: up columns i0 + 8(c - 4)
+  const uint16_t* mat = w + (c < 4 ? 0 : (size_t)H * I);
+  const uint16_t* wcol = mat + i0 + 8 * (c & 3);
+  stream_rows<RB>(wcol, I, H, g, xs, H, acc);
+  warp_partials<RB>(acc, red);
+  __syncthreads();
+  for (int o = tid; o < kGUTile * RB; o += kFfnThreads) {
+    const int r = o / kGUTile, il = o - r * kGUTile;
+    const int cg = il >> 3, q = il & 7;
+    float gs = 0.f, us = 0.f;
+#pragma unroll
+    for (int wp = 0; wp < kFfnThreads / 32; ++wp) {
+      gs += red[((wp * 8 + cg) * RB + r) * 8 + q];
+      us += red[((wp * 8 + cg + 4) * RB + r) * 8 + q];
+    }
+    if (r < nb) a.hbuf[(size_t)(p0 + r) * I + i0 + il] = gs / (1.f + expf(-gs)) * us;
+  }
+  __syncthreads();
+}
+
+template <int RB>
+__device__ __forceinline__ void down_batch(const FfnArgs& a, const uint16_t* __restrict__ w, int o0, int p0, int nb,
+                                           float* __restrict__ hs, float* __restrict__ red) {
+  const int tid = threadIdx.x, c = tid & 7, g = tid >> 3;
+  const int H = a.H, I = a.I;
+  for (int idx = tid; idx < RB * I; idx += kFfnThreads) {
+    const int r = idx / I, i = idx - r * I;
+    hs[idx] = r < nb ? a.hbuf[(size_t)(p0 + r) * I + i] : 0.f;
+  }
+  __syncthreads();
+  float acc[RB][8];
+#pragma unroll
+  for (int r = 0; r < RB; ++r)
+#pragma unroll
+    for (int q = 0; q < 8; ++q) acc[r][q] = 0.f;
+  const uint16_t* wd = w + 2 * (size_t)H * I;
+  stream_rows<RB>(wd + o0 + 8 * c, H, I, g, hs, I, acc);
+  warp_partials<RB>(acc, red);
+  __syncthreads();
+  for (int o = tid; o < kDTile * RB; o += kFfnThreads) {
+    const int r = o / kDTile, ol = o - r * kDTile;
+    const int cg = ol >> 3, q = ol & 7;
+    float s = 0.f;
+#pragma unroll
+    for (int wp = 0; wp < kFfnThreads / 32; ++wp) s += red[((wp * 8 + cg) * RB + r) * 8 + q];
+    if (r < nb) a.y[(size_t)(p0 + r) * H + o0 + ol] = s;
+  }
+  __syncthreads();
+}
+
+template <bool kDown>
+__global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(const FfnArgs a) {
+  extern __shared__ __align__(16) float ffn_smem[];
+  float* in_s = ffn_smem;                             // [kRB][K]
+  float* red = ffn_smem + kRB * (kDown ? a.I : a.H);  // [8 warps][8][kRB][8]
+  const int tiles = kDown ? a.H / kDTile : a.I / kGUTile;
+  const int nl = *a.n_list;
+  const int items = nl * tiles;
+  for (int it = blockIdx.x; it < items; it += gridDim.x) {
+    const int li = it / tiles, tile = it - li * tiles;
+    const int e = a.list_e[li];
+    if (e < 0 || e >= a.E) {
+      if (threadIdx.x == 0) set_status(a.status, MOE_DEV_BAD_EXPERT);
+      continue;
+    }
+    const uint16_t* w = expert_weights(a, e);
+    if (!w) {
+      if (threadIdx.x == 0) set_status(a.status, MOE_DEV_BAD_SLOT);
+      continue;
+    }
+    const int pb = a.offset[e], pe = a.offset[e + 1];
+    for (int p0 = pb; p0 < pe; p0 += kRB) {
+      const int nb = min(kRB, pe - p0);
+      if (kDown) {
+        const int o0 = tile * kDTile;
+        if (nb == 1) down_batch<1>(a, w, o0, p0, nb, in_s, red);
+        else if (nb == 2) down_batch<2>(a, w, o0, p0, nb, in_s, red);
+        else if (nb <= 4) down_batch<4>(a, w, o0, p0, nb, in_s, red);
+        else down_batch<8>(a, w, o0, p0, nb, in_s, red);
+      } else {
+        const int i0 = tile * kGUTile;
+        if (nb == 1) gateup_batch<1>(a, w, i0, p0, nb, in_s, red);
+        else if (nb == 2) gateup_batch<2>(a, w, i0, p0, nb, in_s, red);
+        else if (nb <= 4) gateup_batch<4>(a, w, i0, p0, nb, in_s, red);
+        else gateup_batch<8>(a, w, i0, p0, nb, in_s, red);
+      }
+    }
+  }
+}
+
+static size_t ffn_smem_bytes(int K) { return (size_t)(kRB * K + 8 * 8 * kRB * 8) * sizeof(float); }
+
+int launch_ffn(const FfnArgs& a, int max_list, cudaStream_t stream) {
+  if (max_list <= 0) return MOE_OK;
+  constexpr int kSmemCap = 160 * 1024;
+  const size_t smem_gu = ffn_smem_bytes(a.H), smem_d = ffn_smem_bytes(a.I);
+  if (smem_gu > (size_t)kSmemCap || smem_d > (size_t)kSmemCap) return MOE_ERR_ARG;
+  static bool done_gu[64] = {}, done_d[64] = {};
+  MOE_CUDA_TRY(ensure_smem(ffn_kernel<false>, kSmemCap, done_gu));
+  MOE_CUDA_TRY(ensure_smem(ffn_kernel<true>, kSmemCap, done_d));
+  int dev = 0, sms = 0;
+  MOE_CUDA_TRY(cudaGetDevice(&dev));
+  MOE_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  const int g1 = std::min(max_list * (a.I / kGUTile), sms);
+  const int g2 = std::min(max_list * (a.H / kDTile), sms);
+  ffn_kernel<false><<<g1, kFfnThreads, smem_gu, stream>>>(a);
+  MOE_LAUNCH_CHECK();
+  ffn_kernel<true><<<g2, kFfnThreads, smem_d, stream>>>(a);
+  MOE_LAUNCH_CHECK();
+  return MOE_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Combine: out[t] = sum_j w[t][j] y[pos[t*k+j]] in fp32, j ascending.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ y, const float* __restrict__ w,
+                                                      const int32_t* __restrict__ pos,
+                                                      const int32_t* __restrict__ ids,
+                                                      const int32_t* __restrict__ e2s, int k, int H, int E,
+                                                      int split, uint16_t* __restrict__ out,
+                                                      float* __restrict__ out_res, float* __restrict__ out_miss) {
+  const int t = blockIdx.x;
+  for (int c = threadIdx.x * 4; c < H; c += blockDim.x * 4) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f), accm = acc;
+    for (int j = 0; j < k; ++j) {
+      const int p = pos[(size_t)t * k + j];
+      if (p < 0) continue;
+      const float wj = w[(size_t)t * k + j];
+      const float4 v = *reinterpret_cast<const float4*>(y + (size_t)p * H + c);
+      bool res = true;
+      if (split) {
+        const int e = ids[(size_t)t * k + j];
+        res = e >= 0 && e < E && e2s[e] >= 0;
+      }
+      float4& d = res ? acc : accm;
+      d.x = fmaf(wj, v.x, d.x);
+      d.y = fmaf(wj, v.y, d.y);
+      d.z = fmaf(wj, v.z, d.z);
+      d.w = fmaf(wj, v.w, d.w);
+    }
+    const size_t o = (size_t)t * H + c;
+    float4 tot = acc;
+    if (split) {
+      *reinterpret_cast<float4*>(out_res + o) = acc;
+      *reinterpret_cast<float4*>(out_miss + o) = accm;
+      tot = make_float4(acc.x + accm.x, acc.y + accm.y, acc.z + accm.z, acc.w + accm.w);
+    }
+    uint2 pk;
+    pk.x = uint32_t(f32_to_bf16(tot.x)) | (uint32_t(f32_to_bf16(tot.y)) << 16);
+    pk.y = uint32_t(f32_to_bf16(tot.z)) | (uint32_t(f32_to_bf16(tot.w)) << 16);
+    *reinterpret_cast<uint2*>(out + o) = pk;
+  }
+}
+
+int launch_combine(const float* y, const float* w, const int32_t* pos, const int32_t* ids, const int32_t* e2s, int T,
+                   int k, int H, int E, int split, void* out, float* out_res, float* out_miss, cudaStream_t stream) {
+  const int threads = std::min(256, std::max(32, H / 4));
+  combine_kernel<<<T, threads, 0, stream>>>(y, w, pos, ids, e2s, k, H, E, split, (uint16_t*)out, out_res,
+                                            out_miss);
+  MOE_LAUNCH_CHECK();
+  return MOE_OK;
+}
+
+}  // namespace moe

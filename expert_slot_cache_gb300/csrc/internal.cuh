@@ -1,0 +1,35 @@
+// Internal launchers shared by the translation units of the library.
+#pragma once
+
+#include "common.cuh"
+
+namespace moe {
+
+struct FfnArgs {
+  const uint16_t* x;      // device bf16 [T][H]
+  int T, H, I, k, E;
+  const int32_t* offset;  // [E+1]
+  const int32_t* rows;    // [T*k]
+  const int32_t* list_e;  // experts to process
+  const int32_t* n_list;  // device count
+  const uint16_t* pool;   // slot pool
+  const int32_t* e2s;     // NULL = expert e in slot e
+  const uint16_t* host;   // host store (zero-return second pass) or NULL
+  size_t slab_elems;
+  float* hbuf;            // [T*k][I]
+  float* y;               // [T*k][H]
+  int32_t* status;
+};
+
+int launch_ffn(const FfnArgs& a, int max_list, cudaStream_t stream);
+int launch_combine(const float* y, const float* w, const int32_t* pos, const int32_t* ids, const int32_t* e2s, int T,
+                   int k, int H, int E, int split, void* out, float* out_res, float* out_miss, cudaStream_t stream);
+int launch_manage(const int32_t* ids, int n, int E, int S, int policy, int32_t* e2s, int32_t* s2e, uint32_t* prio,
+                  uint32_t* stamp, int32_t* miss_e, int32_t* miss_s, int32_t* n_miss, int32_t* hit_e,
+                  int32_t* n_hit, int32_t* sid, int64_t* stats, int32_t* dev_status, cudaStream_t stream);
+int launch_gather(const void* host_slabs, void* pool, size_t slab_bytes, int E, int S, const int32_t* miss_e,
+                  const int32_t* miss_s, const int32_t* n_miss, int max_miss, int64_t* stats, int32_t* dev_status,
+                  cudaStream_t stream);
+int check_host_accessible(const void* p);
+
+}  // namespace moe

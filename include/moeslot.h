@@ -1,0 +1,265 @@
+/*
+ * moeslot.h -- C ABI of the slot-cached MoE layer (GB300, sm_103a).
+ *
+ * One MoE layer forward whose expert weights sit partly in a fixed pool of
+ * VRAM slots and partly in pinned host memory:
+ *   route (logits, soft-biased top-k, softmax weights) -> permute into
+ *   per-expert groups -> expert_cache_manage -> expert_cache_gather (or
+ *   zero-return) -> grouped SwiGLU expert FFN -> weighted combine.
+ *
+ * Conventions for every entry point
+ *   - Pointers named "device" must be device memory (or managed memory);
+ *     "host store" pointers must be pinned host memory the GPU can address
+ *     (cudaHostAlloc / torch pin_memory()).  The caller allocates and owns
+ *     every buffer; the library allocates no memory.  It keeps only cached
+ *     CUDA event handles for the two-stream layer forward.
+ *   - bf16 tensors are passed as void* (IEEE bfloat16, little endian).
+ *   - Every call only enqueues work on the given stream(s) and returns; the
+ *     results are valid once that work has completed.  No call synchronises
+ *     with the host.  A NULL stream is the legacy default stream.
+ *   - Host-detectable argument errors return a negative moe_status before
+ *     anything is enqueued.  Errors found on the device (an expert id out of
+ *     range) are written as a nonzero code into the caller's device int32
+ *     `dev_status` (which the caller zeroes), the offending item is skipped,
+ *     and no kernel traps.
+ *   - Slab layout for expert e (bf16, contiguous, 3*H*I elements):
+ *       [ Wg (H x I) | Wu (H x I) | Wd (I x H) ]  each row-major, input-major,
+ *     so g = x Wg, u = x Wu, h = silu(g) * u, y = h Wd.
+ *   - Shape limits: H % 64 == 0, I % 32 == 0, 1 <= k <= 16, k <= E <= 1024,
+ *     1 <= T, 1 <= S <= 4096.  Pointers read with 16-byte vectors must be
+ *     16-byte aligned (slabs, pool, host store, y, workspace).
+ */
+#ifndef MOESLOT_H
+#define MOESLOT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* moe_stream_t; /* same handle as cudaStream_t */
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_ARG = -1,                   /* null pointer, bad shape, bad enum */
+  MOE_ERR_CAPACITY = -2,              /* step needs more slots than the pool has */
+  MOE_ERR_ALIGN = -3,                 /* slab size or a pointer not a 16-byte multiple, workspace too small */
+  MOE_ERR_NOT_DEVICE_ACCESSIBLE = -4, /* host store not addressable by the GPU */
+  MOE_ERR_CUDA = -5,                  /* a CUDA runtime call failed */
+  MOE_ERR_DEVICE_STATUS = -6          /* reserved: a kernel reported a bad item */
+} moe_status;
+
+typedef enum { MOE_POLICY_LRU = 0, MOE_POLICY_LFU = 1, MOE_POLICY_STATIC = 2 } moe_policy;
+typedef enum { MOE_MODE_RESIDENT = 0, MOE_MODE_GATHER = 1, MOE_MODE_ZERO_RETURN = 2 } moe_mode;
+
+/* Device status codes written into dev_status. */
+#define MOE_DEV_BAD_EXPERT 1 /* an expert id outside [0, E) */
+#define MOE_DEV_BAD_SLOT 2   /* a slot id outside [0, S) where a slot was required */
+
+const char* moe_status_str(int status);
+
+/*
+ * Soft selection bias for one layer.
+ * Source: "Nudge, don't cut" (PGO-SGB), section "The method in five lines":
+ * bias[e] = max(cap, ln(b[e] / b_edge)) outside the hot set, 0 inside it;
+ * the hot set is the n_hot brightest experts (ties: lower id), b_edge the
+ * smallest brightness in it.  Evaluated in fp64, rounded to fp32; b[e] <= 0
+ * gives cap.  Built once per layer, before serving (the page reads the
+ * table once at startup).
+ *   b     device fp32 [E], brightness (>= 0)
+ *   bias  device fp32 [E], output
+ * Errors: MOE_ERR_ARG if a pointer is NULL, E < 1, E > 1024 or n_hot not in [1, E].
+ */
+int moe_bias_table(const float* b, int E, int n_hot, float cap, float* bias, moe_stream_t stream);
+
+/*
+ * Router: logits, top-k by logit + bias, softmax weights over the picked k.
+ * Source: "Nudge, don't cut" (PGO-SGB), "The method in five lines" (pick
+ * top-k by logit + bias; weights are the router's own softmax over the k
+ * picked, from the unbiased logits).
+ *   x            device bf16 [T][H]
+ *   w_router     device bf16 [H][E]
+ *   logit_offset device fp32 [E] added to every logit after the sum, or NULL
+ *   sel_bias     device fp32 [E] selection-only bias, or NULL
+ *   logits       device fp32 [T][E] output (unbiased logits), or NULL
+ *   ids          device int32 [T][k] output, descending score, ties -> lower id
+ *   w            device fp32 [T][k] output, sums to 1 per token
+ * logit[t][e] is accumulated in fp32 in h order (acc = fma(x, Wr, acc) for
+ * h = 0..H-1), so ids are reproducible bit for bit.
+ * Errors: MOE_ERR_ARG on NULL required pointers or shapes out of range.
+ */
+int moe_route(const void* x, const void* w_router, const float* logit_offset, const float* sel_bias,
+              int T, int H, int E, int k, float* logits, int32_t* ids, float* w, moe_stream_t stream);
+
+/*
+ * Permute: group the n = T*k routing slots by expert.
+ * Source: "Porting vllm-expert-cache to NVIDIA GPUs", "What this package
+ * does" (the fused MoE kernel runs on grouped, slot-remapped ids).
+ *   ids     device int32 [n] (flat t*k + j)
+ *   count   device int32 [E]      tokens routed to each expert
+ *   offset  device int32 [E + 1]  exclusive prefix of count; offset[E] = n
+ *   rows    device int32 [n]      flat index at each grouped position; within
+ *                                 an expert, ascending flat index (stable)
+ *   pos     device int32 [n]      grouped position of each flat index
+ *   act_e   device int32 [E]      experts with count > 0, ascending
+ *   n_act   device int32 [1]      their number
+ *   dev_status device int32 [1]   set to MOE_DEV_BAD_EXPERT on an id outside [0, E)
+ * Errors: MOE_ERR_ARG on NULL pointers, n < 1 or E out of range.
+ */
+int moe_permute(const int32_t* ids, int n, int E, int32_t* count, int32_t* offset, int32_t* rows,
+                int32_t* pos, int32_t* act_e, int32_t* n_act, int32_t* dev_status, moe_stream_t stream);
+
+/*
+ * expert_cache_manage: update the slot cache for one step and emit the miss list.
+ * Source: "Porting vllm-expert-cache to NVIDIA GPUs", "What this package does"
+ * (victims are picked among slots this step does not need; a miss list is
+ * emitted; ids are remapped to slot space), "Prove it is correct before
+ * measuring" (fields: expert-to-slot table, cold map, slot contents,
+ * priorities, miss list; deterministic, no atomics), "Measuring, without
+ * fooling yourself" (a step is served from slots only when tokens x top_k <= slots).
+ * One CTA, no atomics; the result does not depend on thread timing.
+ *   ids       device int32 [n] routing ids of the step
+ *   e2s       device int32 [E]  expert -> slot, -1 = cold (in/out)
+ *   s2e       device int32 [S]  slot -> expert, -1 = empty (in/out)
+ *   prio      device uint32 [S] policy priority (in/out)
+ *   stamp     device uint32 [1] call counter, +1 per call (in/out)
+ *   miss_e    device int32 [>= min(n, E)] missing experts, ascending id
+ *   miss_s    device int32 [same]   slot each one goes to (-1 under STATIC)
+ *   n_miss    device int32 [1]
+ *   hit_e     device int32 [>= min(n, E)] needed experts already resident, ascending, or NULL
+ *   n_hit     device int32 [1], or NULL (both or neither)
+ *   sid       device int32 [n] slot of each routing id after the call, or NULL
+ * Policies: LRU (prio = stamp on hit or load), LFU (prio += 1 once per call
+ * on a hit, prio = 1 on load), STATIC (never evicts; misses are listed with
+ * slot -1 and left for a zero-return pass).  Victim order: empty slots
+ * (ascending), then ascending prio, then ascending slot; the i-th missing
+ * expert takes the i-th victim.  Eviction sets e2s[old] = -1 (no write-back:
+ * the host store stays authoritative).
+ * Errors: MOE_ERR_CAPACITY if policy != STATIC, S < E and n > S;
+ * MOE_ERR_ARG on NULL pointers or bad shapes/policy.
+ */
+int moe_cache_manage(const int32_t* ids, int n, int E, int S, int policy, int32_t* e2s, int32_t* s2e,
+                     uint32_t* prio, uint32_t* stamp, int32_t* miss_e, int32_t* miss_s, int32_t* n_miss,
+                     int32_t* hit_e, int32_t* n_hit, int32_t* sid, int32_t* dev_status, moe_stream_t stream);
+
+/*
+ * expert_cache_gather: copy each missing expert's slab from the host store into its slot.
+ * Source: "Porting vllm-expert-cache to NVIDIA GPUs", "What this package does"
+ * (copies the missing experts host-to-slot), "1. Kernels" (16-byte copy
+ * unit), "Prove it is correct before measuring" (the device reads host
+ * memory; per-expert slabs must stay 16-byte multiples).
+ * The kernel reads pinned host memory directly, 16 bytes per access; the
+ * number of misses is read on the device, so no host round trip is needed.
+ *   host_slabs  pinned host bf16 [E][slab_bytes/2], GPU-addressable (read)
+ *   pool        device [S][slab_bytes/2] (written for listed slots only)
+ *   miss_e, miss_s, n_miss  device, as written by moe_cache_manage
+ *   max_miss    host upper bound on *n_miss (sizes the grid)
+ * Errors: MOE_ERR_ALIGN if slab_bytes or a base pointer is not a 16-byte
+ * multiple; MOE_ERR_NOT_DEVICE_ACCESSIBLE if host_slabs is not addressable
+ * by the current device; MOE_ERR_ARG otherwise.  A listed slot outside
+ * [0, S) or expert outside [0, E) is skipped and flagged in dev_status.
+ */
+int moe_cache_gather(const void* host_slabs, void* pool, size_t slab_bytes, int E, int S,
+                     const int32_t* miss_e, const int32_t* miss_s, const int32_t* n_miss, int max_miss,
+                     int32_t* dev_status, moe_stream_t stream);
+
+/*
+ * Grouped SwiGLU expert FFN over a device-side list of experts.
+ * Sources: "Porting vllm-expert-cache to NVIDIA GPUs", "What this package
+ * does" (the expert GEMM runs on slot-remapped ids); "RTX 3060 runs a 35B
+ * MoE with llama.cpp", chapter "Designing a fixed expert cache with
+ * zero-return for missing experts" (a pass over the experts on the GPU and
+ * a pass over the ones still in host memory).
+ * For each expert e in list_e[0 .. *n_list) and each grouped position p in
+ * [offset[e], offset[e+1]): token t = rows[p] / k,
+ *   h = silu(x[t] Wg_e) * (x[t] Wu_e)  (fp32),   y[p] = h Wd_e  (fp32).
+ * Weights of e are read from pool + e2s[e] * slab when e2s[e] >= 0, else
+ * straight from host_slabs + e * slab (the zero-return second pass).  With
+ * e2s == NULL expert e sits in slot e.
+ *   x          device bf16 [T][H]
+ *   offset     device int32 [E + 1], rows device int32 [T*k] (moe_permute)
+ *   list_e     device int32 [>= *n_list], n_list device int32 [1]
+ *   max_list   host upper bound on *n_list
+ *   y          device fp32 [T*k][H]; only rows of listed experts are written
+ *   workspace  device scratch of moe_ffn_workspace_bytes(T, k, I) bytes (holds h)
+ * Errors: MOE_ERR_ARG on NULL pointers or bad shapes, MOE_ERR_ALIGN on
+ * unaligned weight/output pointers or a workspace that is too small.
+ */
+int moe_expert_ffn(const void* x, int T, int H, int I, int k, int E, const int32_t* offset,
+                   const int32_t* rows, const int32_t* list_e, const int32_t* n_list, int max_list,
+                   const void* pool, const int32_t* e2s, const void* host_slabs, float* y,
+                   void* workspace, size_t workspace_bytes, int32_t* dev_status, moe_stream_t stream);
+
+size_t moe_ffn_workspace_bytes(int T, int k, int I);
+
+/*
+ * Weighted scatter-combine back to token order.
+ * Source: "RTX 3060 runs a 35B MoE with llama.cpp", chapters "Designing a
+ * fixed expert cache with zero-return for missing experts" and "Fixing
+ * scheduler order to improve performance" (two runs, then one add).
+ *   out[t] = bf16( sum_{j=0..k-1} w[t][j] * y[pos[t*k+j]] ), fp32, j ascending.
+ * With split != 0 a routing slot counts as resident when e2s[ids[t][j]] >= 0;
+ * out_res / out_miss (fp32 [T][H]) get the two partial sums and
+ * out = bf16(out_res + out_miss).
+ *   y device fp32 [T*k][H]; w device fp32 [T][k]; pos device int32 [T*k]
+ *   ids, e2s device int32 (split only; e2s has E entries); out device bf16 [T][H]
+ * Errors: MOE_ERR_ARG on NULL pointers or bad shapes.
+ */
+int moe_combine(const float* y, const float* w, const int32_t* pos, const int32_t* ids, const int32_t* e2s,
+                int T, int k, int H, int E, int split, void* out, float* out_res, float* out_miss,
+                moe_stream_t stream);
+
+/* Arguments of moe_layer_forward.  Field meanings as in the calls above. */
+typedef struct moe_layer_args {
+  int32_t T, H, E, k, I, S;
+  int32_t mode;   /* moe_mode */
+  int32_t policy; /* moe_policy (GATHER: LRU or LFU; ZERO_RETURN: STATIC) */
+  const void* x;             /* device bf16 [T][H] */
+  const void* w_router;      /* device bf16 [H][E] */
+  const float* logit_offset; /* device fp32 [E] or NULL */
+  const float* sel_bias;     /* device fp32 [E] or NULL */
+  void* pool;                /* device bf16 [S][3HI] slot pool */
+  const void* host_slabs;    /* pinned host bf16 [E][3HI]; NULL in RESIDENT mode */
+  int32_t* e2s;              /* device cache state (RESIDENT: e2s may be NULL = identity) */
+  int32_t* s2e;
+  uint32_t* prio;
+  uint32_t* stamp;
+  int32_t* ids;              /* device int32 [T][k] routing ids (output) */
+  float* w;                  /* device fp32 [T][k] routing weights (output) */
+  void* out;                 /* device bf16 [T][H] (output) */
+  float* out_res;            /* device fp32 [T][H] (ZERO_RETURN output) */
+  float* out_miss;           /* device fp32 [T][H] (ZERO_RETURN output) */
+  int64_t* stats;            /* device int64 [4] or NULL: [0] += misses, [1] += manage calls, [2] += bytes gathered */
+  int32_t* dev_status;       /* device int32 [1] */
+  void* workspace;           /* device scratch, moe_layer_workspace_bytes() */
+  size_t workspace_bytes;
+} moe_layer_args;
+
+/*
+ * One MoE layer forward: route, then per chunk of tokens permute, manage,
+ * gather on the side stream while the hit experts' FFN runs on the main
+ * stream, the missed experts' FFN after the gather, and combine.
+ * Sources: as for the calls above; "Betelgeuse: Running Qwen 3.8 Flash Next
+ * ... on an RTX 3060", "What it actually does under the hood" (hits are
+ * resolved on the device, no host sync inside the step, the decode pass
+ * replays as one CUDA graph).
+ * Chunking: when the policy can evict, S < E and T*k > S, the tokens are
+ * processed in chunks of floor(S/k) consecutive tokens (a step is served
+ * from slots only when tokens x top_k <= slots), each chunk managed,
+ * gathered and computed in turn.  ZERO_RETURN (STATIC) never chunks.
+ * `side` may be NULL or equal to `main` (then everything runs on `main`).
+ * The sequence of launches depends only on the shapes, so it can be
+ * captured into a CUDA graph.
+ * Errors: as the calls above; MOE_ERR_CAPACITY if S < k in GATHER mode.
+ */
+int moe_layer_forward(const moe_layer_args* args, moe_stream_t main, moe_stream_t side);
+
+size_t moe_layer_workspace_bytes(int T, int H, int E, int k, int I, int S);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOESLOT_H */
