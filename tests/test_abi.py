@@ -1,0 +1,64 @@
+"""The C-ABI library loads, exports every declared entry point, and rejects
+bad arguments on the host (no GPU needed: these paths return before any
+CUDA call)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from expert_slot_cache_gb300 import build
+    build.build()
+    return ctypes.CDLL(build.LIB)
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "moeslot.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert len(names) >= 11
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    lib.moe_status_str.restype = ctypes.c_char_p
+    for code in range(0, -7, -1):
+        assert lib.moe_status_str(code) and lib.moe_status_str(code) != b"unknown status"
+
+
+def test_host_side_argument_errors(lib):
+    buf = (ctypes.c_int32 * 64)()
+    p = ctypes.cast(buf, ctypes.c_void_p)
+    null = ctypes.c_void_p(0)
+    # NULL inputs
+    assert lib.moe_route(null, null, null, null, 4, 256, 16, 2, null, null, null, null) == -1
+    # k > E
+    assert lib.moe_route(p, p, null, null, 4, 256, 4, 8, null, p, p, null) == -1
+    # a step larger than the pool when the policy can evict
+    assert lib.moe_cache_manage(p, 65, 128, 64, 0, p, p, p, p, p, p, p, null, null, null, null, null) == -2
+    # bad policy
+    assert lib.moe_cache_manage(p, 8, 128, 64, 7, p, p, p, p, p, p, p, null, null, null, null, null) == -1
+    # slab not a 16-byte multiple
+    assert lib.moe_cache_gather(p, p, ctypes.c_size_t(24), 4, 2, p, p, p, 2, null, null) == -3
+    # shapes the FFN does not take (H % 64 != 0)
+    assert lib.moe_expert_ffn(p, 4, 100, 128, 2, 16, p, p, p, p, 4, p, null, null, p, p,
+                              ctypes.c_size_t(1 << 20), null, null) == -1
+
+
+def test_workspace_sizes(lib):
+    lib.moe_layer_workspace_bytes.restype = ctypes.c_size_t
+    lib.moe_ffn_workspace_bytes.restype = ctypes.c_size_t
+    ws = lib.moe_layer_workspace_bytes(64, 2048, 128, 8, 768, 64)
+    # h (n*I fp32) and y (n*H fp32) dominate
+    assert ws >= 4 * 512 * (768 + 2048)
+    assert lib.moe_ffn_workspace_bytes(64, 8, 768) == 4 * 512 * 768

@@ -1,0 +1,366 @@
+"""Parity of the CUDA path (through the C ABI) against the CPU oracle.
+
+Integer results (ids, groups, cache state, miss lists, gathered bytes) must
+match bit for bit; floating outputs within max-abs 2e-2 and relative L2 1e-2
+(bf16 outputs) or relative L2 1e-5 (fp32 intermediates).
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from harness import configs as C
+from tests._setup import HostSlabs, assert_f32_close, assert_out_close, stage_layer
+
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    import expert_slot_cache_gb300 as M
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+DEV = "cuda"
+
+
+def _np(t):
+    return t.detach().cpu().numpy()
+
+
+# ----------------------------------------------------------------------------
+# Bias table and routing
+# ----------------------------------------------------------------------------
+
+def test_bias_table_bit_exact():
+    for cfg, cap in [(C.FLASH, -1.0), (C.FLASH, -0.25), (C.FLASH, 0.0), (C.STACK.with_(n_hot=144, zipf_s=1.1), -0.5)]:
+        b, _ = C.draw_brightness(cfg)
+        got = M.bias_table(torch.from_numpy(b).to(DEV), cfg.n_hot, cap)
+        want = O.bias_table(b, cfg.n_hot, cap)
+        assert np.array_equal(_np(got), want)
+    g = json.load(open(os.path.join(GOLD, "bias_table.json")))
+    b = np.array(g["b"], dtype=np.float32)
+    got = M.bias_table(torch.from_numpy(b).to(DEV), g["n_hot"], g["cap"])
+    assert np.allclose(_np(got), g["bias"], atol=1e-6)
+
+
+ROUTE_CASES = [
+    ("tiny", C.TINY, None, False),
+    ("qwen_T1", C.qwen(1), None, False),
+    ("qwen_T8", C.qwen(8), None, False),
+    ("qwen_T37_ragged", C.qwen(37), None, False),
+    ("qwen_T64", C.qwen(64), None, False),
+    ("flash_T16_bias", C.FLASH, -1.0, False),
+    ("stack_T32_E288", C.STACK, None, False),
+    ("prefill_T4096_offset", C.PREFILL, None, True),
+]
+
+
+@pytest.mark.parametrize("name,cfg,cap,offset", ROUTE_CASES, ids=[c[0] for c in ROUTE_CASES])
+def test_route_parity(name, cfg, cap, offset):
+    x = C.draw_x(cfg, DEV)
+    wr = C.draw_router(cfg, DEV)
+    off = C.draw_logit_offset(cfg, DEV) if offset else None
+    bias_np = bias_d = None
+    if cap is not None:
+        b, _ = C.draw_brightness(cfg)
+        bias_np = O.bias_table(b, cfg.n_hot, cap)
+        bias_d = M.bias_table(torch.from_numpy(b).to(DEV), cfg.n_hot, cap)
+    ids, w, logits = M.route(x, wr, cfg.k, off, bias_d, return_logits=True)
+    torch.cuda.synchronize()
+    want_logits = O.router_logits(_np(x.float()), _np(wr.float()), None if off is None else _np(off))
+    assert np.array_equal(_np(logits), want_logits), "logits differ"
+    want_ids = O.select_topk(want_logits, cfg.k, bias_np)
+    assert np.array_equal(_np(ids), want_ids), "ids differ"
+    want_w = O.route_weights(want_logits, want_ids)
+    assert np.abs(_np(w) - want_w).max() <= 1e-6
+    if cap is not None:  # the bias moved some picks, and the weights stay the router's own
+        assert not np.array_equal(want_ids, O.select_topk(want_logits, cfg.k))
+
+
+# ----------------------------------------------------------------------------
+# Permute
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("n,E", [(1, 16), (7, 5), (64, 128), (640, 512), (1024, 128), (3001, 288), (32768, 128)])
+def test_permute_parity(n, E):
+    rng = np.random.default_rng(n * 7 + E)
+    ids = rng.integers(0, E, size=n).astype(np.int32)
+    g = M.permute(torch.from_numpy(ids).to(DEV), E)
+    torch.cuda.synchronize()
+    count, offset, rows, pos = O.permute(ids.reshape(1, -1), E)
+    assert np.array_equal(_np(g.count), count)
+    assert np.array_equal(_np(g.offset), offset)
+    assert np.array_equal(_np(g.rows), rows)
+    assert np.array_equal(_np(g.pos), pos)
+    act = np.nonzero(count)[0]
+    assert int(_np(g.n_act)[0]) == len(act)
+    assert np.array_equal(_np(g.act_e)[: len(act)], act)
+
+
+def test_permute_flags_bad_ids():
+    ids = torch.tensor([0, 3, 9, 1], dtype=torch.int32, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    g = M.permute(ids, 4, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st[0]) == 1
+    assert _np(g.offset)[4] == 3 and _np(g.pos)[2] == -1
+
+
+# ----------------------------------------------------------------------------
+# Manage / gather
+# ----------------------------------------------------------------------------
+
+def _check_state(gs, os_, what):
+    assert _np(gs.e2s).tolist() == os_.e2s.tolist(), f"{what}: e2s"
+    assert _np(gs.s2e).tolist() == os_.s2e.tolist(), f"{what}: s2e"
+    assert (_np(gs.prio).astype(np.uint32)).tolist() == os_.prio.tolist(), f"{what}: prio"
+    assert int(_np(gs.stamp)[0]) == os_.stamp, f"{what}: stamp"
+
+
+def _check_manage(mo, r, what):
+    nm = int(_np(mo.n_miss)[0])
+    nh = int(_np(mo.n_hit)[0])
+    assert _np(mo.miss_e)[:nm].tolist() == r.miss_e, f"{what}: miss_e"
+    assert _np(mo.miss_s)[:nm].tolist() == r.miss_s, f"{what}: miss_s"
+    assert _np(mo.hit_e)[:nh].tolist() == r.hit_e, f"{what}: hit_e"
+    assert np.array_equal(_np(mo.sid), r.sid), f"{what}: sid"
+
+
+def test_manage_golden_traces_on_gpu():
+    g = json.load(open(os.path.join(GOLD, "manage_traces.json")))
+    for tr in g["traces"]:
+        st = M.CacheState.from_slots(tr["s2e0"], tr["E"])
+        for i, step in enumerate(tr["steps"]):
+            ids = torch.tensor(step["ids"], dtype=torch.int32, device=DEV)
+            mo = M.cache_manage(ids, st, tr["policy"])
+            torch.cuda.synchronize()
+            nm = int(_np(mo.n_miss)[0])
+            assert _np(mo.miss_e)[:nm].tolist() == step["miss_e"], (tr["name"], i)
+            assert _np(mo.miss_s)[:nm].tolist() == step["miss_s"], (tr["name"], i)
+            assert _np(mo.sid).tolist() == step["sid"], (tr["name"], i)
+            assert _np(st.s2e).tolist() == step["s2e"], (tr["name"], i)
+            assert _np(st.e2s).tolist() == step["e2s"], (tr["name"], i)
+            assert _np(st.prio).tolist() == step["prio"], (tr["name"], i)
+
+
+def _zipf_trace(rng, steps, T, k, E, s=1.1):
+    p = np.arange(1, E + 1, dtype=np.float64) ** -s
+    p /= p.sum()
+    perm = rng.permutation(E)
+    return [np.stack([perm[rng.choice(E, k, replace=False, p=p)] for _ in range(T)]).astype(np.int32)
+            for _ in range(steps)]
+
+
+@pytest.mark.parametrize("policy", [0, 1, 2], ids=["lru", "lfu", "static"])
+@pytest.mark.parametrize("E,S,T,k,dist", [(128, 64, 8, 8, "uniform"), (128, 64, 8, 8, "zipf"),
+                                          (512, 192, 16, 10, "zipf"), (288, 144, 18, 8, "uniform"),
+                                          (16, 16, 4, 2, "uniform")])
+def test_manage_parity_every_step(policy, E, S, T, k, dist):
+    rng = np.random.default_rng(E + S + policy)
+    if dist == "zipf":
+        trace = _zipf_trace(rng, 40, T, k, E)
+    else:
+        trace = [np.stack([rng.choice(E, k, replace=False) for _ in range(T)]).astype(np.int32) for _ in range(40)]
+    s2e0 = C.initial_residency(C.TINY.with_(E=E, S=S, seed=E))
+    ost = O.CacheState.from_slots(s2e0, E)
+    gst = M.CacheState.from_slots(s2e0, E)
+    for i, ids in enumerate(trace):
+        mo = M.cache_manage(torch.from_numpy(ids).to(DEV), gst, policy)
+        torch.cuda.synchronize()
+        r = O.manage(ost, ids, policy)
+        _check_manage(mo, r, f"step {i}")
+        _check_state(gst, ost, f"step {i}")
+
+
+def test_manage_capacity_error():
+    st = M.CacheState.from_slots(np.arange(4), 8)
+    ids = torch.arange(5, dtype=torch.int32, device=DEV)
+    with pytest.raises(M.MoeError) as ei:
+        M.cache_manage(ids, st, 0)
+    assert ei.value.code == -2
+
+
+def test_gather_bytes():
+    E, S, n = 12, 5, 4099 * 8  # slab not a multiple of the 32 KB chunk
+    rng = np.random.default_rng(5)
+    host = torch.from_numpy(rng.integers(-2 ** 15, 2 ** 15, size=(E, n), dtype=np.int16)).pin_memory()
+    pool = torch.zeros(S, n, dtype=torch.int16, device=DEV)
+    miss_e = torch.tensor([7, 2, 11, 0], dtype=torch.int32, device=DEV)
+    miss_s = torch.tensor([3, 0, 4, 1], dtype=torch.int32, device=DEV)
+    n_miss = torch.tensor([3], dtype=torch.int32, device=DEV)  # the 4th entry is not copied
+    M.cache_gather(host, pool, miss_e, miss_s, n_miss, 4)
+    torch.cuda.synchronize()
+    p = _np(pool)
+    assert np.array_equal(p[3], host[7].numpy()) and np.array_equal(p[0], host[2].numpy())
+    assert np.array_equal(p[4], host[11].numpy())
+    assert not p[1].any() and not p[2].any()
+
+
+def test_gather_rejects_unpinned_host():
+    host = torch.zeros(2, 64, dtype=torch.int16)
+    pool = torch.zeros(2, 64, dtype=torch.int16, device=DEV)
+    z = torch.zeros(2, dtype=torch.int32, device=DEV)
+    with pytest.raises(M.MoeError) as ei:
+        M.cache_gather(host, pool, z, z, z[:1], 2)
+    assert ei.value.code == -4
+
+
+# ----------------------------------------------------------------------------
+# Expert FFN and combine
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("cfg,T", [(C.TINY, 4), (C.qwen(8), 8), (C.qwen(64), 64), (C.FLASH, 16)],
+                         ids=["tiny", "qwen_T8", "qwen_T64", "flash_T16"])
+def test_expert_ffn_parity(cfg, T):
+    rng = np.random.default_rng(T)
+    E = cfg.E
+    # a skewed routing so groups span 1..many tokens (batches of 1, 2, 4, 8 and more)
+    p = np.arange(1, E + 1, dtype=np.float64) ** -1.2
+    p /= p.sum()
+    ids = np.stack([rng.choice(E, cfg.k, replace=False, p=p) for _ in range(T)]).astype(np.int32)
+    count, offset, rows, pos = O.permute(ids, E)
+    x = C.draw_x(cfg, DEV, T=T)
+    host = torch.empty(E, cfg.slab_elems, dtype=torch.bfloat16, pin_memory=True)
+    used = np.nonzero(count)[0]
+    for e in used:
+        host[e].copy_(C.draw_slab(cfg, int(e), DEV))
+    # half the used experts in slots (pool), the rest read straight from the host store
+    S = max(1, len(used) // 2)
+    pool = torch.empty(S, cfg.slab_elems, dtype=torch.bfloat16, device=DEV)
+    e2s = np.full(E, -1, dtype=np.int32)
+    for s, e in enumerate(used[:S]):
+        e2s[e] = s
+        pool[s].copy_(host[e])
+    lst = torch.from_numpy(used.astype(np.int32)).to(DEV)
+    g = M.permute(torch.from_numpy(ids).to(DEV), E)
+    y = M.expert_ffn(x, cfg.k, cfg.I, E, g.offset, g.rows, lst, torch.tensor([len(used)], dtype=torch.int32,
+                     device=DEV), len(used), pool, torch.from_numpy(e2s).to(DEV), host)
+    torch.cuda.synchronize()
+    want = O.expert_ffn(_np(x.float()), rows, offset, cfg.k, HostSlabs(host), cfg.H, cfg.I)
+    assert_f32_close(_np(y), want, "y")
+
+
+def test_combine_parity_split():
+    rng = np.random.default_rng(3)
+    T, k, H, E = 5, 3, 128, 9
+    y = rng.normal(size=(T * k, H)).astype(np.float32)
+    w = rng.random((T, k)).astype(np.float32)
+    ids = np.stack([rng.choice(E, k, replace=False) for _ in range(T)]).astype(np.int32)
+    pos = rng.permutation(T * k).astype(np.int32)
+    e2s = np.where(rng.random(E) < 0.5, -1, np.arange(E)).astype(np.int32)
+    t = lambda a: torch.from_numpy(a).to(DEV)
+    out = M.combine(t(y), t(w), t(pos), T, k, E)
+    out_s, res, miss = M.combine(t(y), t(w), t(pos), T, k, E, ids=t(ids), e2s=t(e2s), split=True)
+    torch.cuda.synchronize()
+    want = O.combine(y, w, pos, T, k)
+    wo, wr_, wm = O.combine(y, w, pos, T, k, resident=e2s[ids] >= 0)
+    assert_out_close(_np(out.float()), want)
+    assert_out_close(_np(out_s.float()), wo)
+    assert_f32_close(_np(res), wr_, "out_res")
+    assert_f32_close(_np(miss), wm, "out_miss")
+
+
+# ----------------------------------------------------------------------------
+# Whole layer
+# ----------------------------------------------------------------------------
+
+def _run_layer(cfg, steps=1, side=True, policy=None, T=None):
+    T = cfg.T if T is None else T
+    policy = cfg.policy if policy is None else policy
+    st = stage_layer(cfg)
+    bias_np = bias_d = None
+    if cfg.bias_cap is not None:
+        b, _ = C.draw_brightness(cfg)
+        bias_np = O.bias_table(b, cfg.n_hot, cfg.bias_cap)
+        bias_d = M.bias_table(torch.from_numpy(b).to(DEV), cfg.n_hot, cfg.bias_cap)
+    s2e0 = C.initial_residency(cfg)
+    if cfg.mode == C.MODE_RESIDENT:
+        pool, gstate, ostate, opool = st["slabs_dev"], None, None, None
+    else:
+        pool = torch.empty(cfg.S, cfg.slab_elems, dtype=torch.bfloat16, device=DEV)
+        for s, e in enumerate(s2e0):
+            if e >= 0:
+                pool[s].copy_(st["slabs_dev"][e])
+        gstate = M.CacheState.from_slots(s2e0, cfg.E)
+        ostate = O.CacheState.from_slots(s2e0, cfg.E)
+        opool = None
+    layer = M.SlotCachedMoELayer(st["wr"], pool, cfg.k, cfg.I, cfg.mode, policy,
+                                 host_slabs=None if cfg.mode == C.MODE_RESIDENT else st["host"], state=gstate,
+                                 logit_offset=st["logit_offset"], sel_bias=bias_d, max_tokens=T, side_stream=side)
+    wr_np = _np(st["wr"].float())
+    off_np = None if st["logit_offset"] is None else _np(st["logit_offset"])
+    slabs = HostSlabs(st["host"])
+    total_miss = 0
+    for step in range(steps):
+        x = C.draw_x(cfg, DEV, step=step, T=T)
+        res = layer.forward(x)
+        torch.cuda.synchronize()
+        want = O.layer_forward(_np(x.float()), wr_np, slabs, cfg.H, cfg.I, cfg.k, cfg.mode, policy, ostate,
+                               opool, off_np, bias_np)
+        assert np.array_equal(_np(res["ids"]), want["ids"]), f"step {step}: ids"
+        assert np.abs(_np(res["w"]) - want["w"]).max() <= 1e-6
+        assert_out_close(_np(res["out"].float()), want["out"], f"step {step}: out")
+        if cfg.mode == C.MODE_ZERO_RETURN:
+            assert_f32_close(_np(res["out_res"]), want["out_res"], "out_res")
+            assert_f32_close(_np(res["out_miss"]), want["out_miss"], "out_miss")
+            assert np.abs(want["out_miss"]).max() > 0
+        if ostate is not None:
+            _check_state(gstate, ostate, f"step {step}")
+            total_miss += sum(len(c["miss_e"]) for c in want["chunks"])
+    assert int(_np(layer.dev_status)[0]) == 0
+    if ostate is not None:
+        stats = _np(layer.stats)
+        assert stats[0] == total_miss
+        if cfg.mode == C.MODE_GATHER:
+            assert stats[2] == total_miss * cfg.slab_bytes
+            # every occupied slot holds exactly its expert's bytes
+            s2e = _np(gstate.s2e)
+            for s, e in enumerate(s2e):
+                assert torch.equal(pool[s].cpu(), st["host"][e]), f"slot {s}"
+    return layer
+
+
+def test_layer_tiny_resident():
+    _run_layer(C.TINY, steps=2)
+
+
+@pytest.mark.parametrize("T", [1, 8, 32, 64])
+def test_layer_qwen_gather_lru(T):
+    _run_layer(C.qwen(T), steps=2)
+
+
+def test_layer_qwen_gather_lfu_single_stream():
+    _run_layer(C.qwen(8, policy=C.POLICY_LFU), steps=3, side=False)
+
+
+def test_layer_qwen_all_resident():
+    _run_layer(C.qwen(64, S=128, mode=C.MODE_RESIDENT), steps=1)
+
+
+def test_layer_flash_zero_return():
+    _run_layer(C.FLASH, steps=2)
+
+
+def test_layer_stack_shape_gather_chunked():
+    _run_layer(C.STACK_SLOTS, steps=2)
+
+
+def test_layer_prefill_sampled_tokens():
+    cfg = C.PREFILL
+    st = stage_layer(cfg)
+    layer = M.SlotCachedMoELayer(st["wr"], st["slabs_dev"], cfg.k, cfg.I, cfg.mode, max_tokens=cfg.T)
+    x = C.draw_x(cfg, DEV)
+    res = layer.forward(x)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(0)
+    tok = np.sort(rng.choice(cfg.T, 48, replace=False))
+    tok[-1] = cfg.T - 1
+    xs = _np(x.float())[tok]
+    want = O.layer_forward(xs, _np(st["wr"].float()), HostSlabs(st["host"]), cfg.H, cfg.I, cfg.k, cfg.mode,
+                           logit_offset=_np(st["logit_offset"]))
+    assert np.array_equal(_np(res["ids"])[tok], want["ids"])
+    assert_out_close(_np(res["out"].float())[tok], want["out"])
+    # groups are uneven under the logit offset
+    counts = np.bincount(_np(res["ids"]).ravel(), minlength=cfg.E)
+    assert counts.max() > 2 * counts.mean()
