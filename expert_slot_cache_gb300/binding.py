@@ -30,6 +30,14 @@ POLICY_LRU, POLICY_LFU, POLICY_STATIC = 0, 1, 2
 DEV_BAD_EXPERT, DEV_BAD_SLOT = 1, 2
 
 
+PROF_CLASSES = ("route", "permute", "manage", "gather", "ffn_gateup", "ffn_down", "combine")
+
+
+class Prof(ctypes.Structure):
+    _fields_ = [("events", POINTER(c_void_p)), ("capacity", c_int32), ("used", c_int32),
+                ("tags", POINTER(c_int32))]
+
+
 class LayerArgs(ctypes.Structure):
     _fields_ = [("T", c_int32), ("H", c_int32), ("E", c_int32), ("k", c_int32), ("I", c_int32), ("S", c_int32),
                 ("mode", c_int32), ("policy", c_int32),
@@ -38,7 +46,7 @@ class LayerArgs(ctypes.Structure):
                 ("e2s", c_void_p), ("s2e", c_void_p), ("prio", c_void_p), ("stamp", c_void_p),
                 ("ids", c_void_p), ("w", c_void_p), ("out", c_void_p), ("out_res", c_void_p),
                 ("out_miss", c_void_p), ("stats", c_void_p), ("dev_status", c_void_p),
-                ("workspace", c_void_p), ("workspace_bytes", c_size_t)]
+                ("workspace", c_void_p), ("workspace_bytes", c_size_t), ("prof", POINTER(Prof))]
 
 
 def _sig(name, argtypes, restype=c_int):
@@ -244,7 +252,7 @@ class SlotCachedMoELayer:
                                      dtype=torch.uint8, device=dev)
         self.side = torch.cuda.Stream(device=dev) if side_stream else None
 
-    def forward(self, x, out=None, ids=None, w=None, out_res=None, out_miss=None, stream=None):
+    def forward(self, x, out=None, ids=None, w=None, out_res=None, out_miss=None, stream=None, prof=None):
         T = x.shape[0]
         if T > self.max_tokens:
             raise ValueError(f"T={T} > max_tokens={self.max_tokens}")
@@ -263,7 +271,7 @@ class SlotCachedMoELayer:
                       _ptr(st.prio if st else None), _ptr(st.stamp if st else None),
                       ids.data_ptr(), w.data_ptr(), out.data_ptr(), _ptr(out_res), _ptr(out_miss),
                       self.stats.data_ptr(), self.dev_status.data_ptr(), self.workspace.data_ptr(),
-                      self.workspace.numel())
+                      self.workspace.numel(), ctypes.pointer(prof) if prof is not None else None)
         main = torch.cuda.current_stream() if stream is None else stream
         # the library forks to and joins back from the side stream itself
         _ck(_layer(ctypes.byref(a), c_void_p(main.cuda_stream),

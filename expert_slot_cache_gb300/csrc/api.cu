@@ -167,17 +167,24 @@ extern "C" int moe_layer_forward(const moe_layer_args* a, moe_stream_t main_s, m
     if (r != MOE_OK) return r;
   }
   int64_t* stats = a->stats;
+  Prof prof;
+  prof.p = a->prof;
+  if (prof.p) prof.p->used = 0;
   const size_t slab_bytes = (size_t)6 * H * I;
+  prof.begin(MOE_PROF_ROUTE, ms);
   int r = moe_route(a->x, a->w_router, a->logit_offset, a->sel_bias, T, H, E, k, nullptr, a->ids, a->w, main_s);
   if (r != MOE_OK) return r;
+  prof.end(ms);
 
   for (int t0 = 0; t0 < T; t0 += C) {
     const int tc = std::min(C, T - t0);
     const int n = tc * k;
     const int lmax = std::min(n, E);
     const int32_t* ids_c = a->ids + (size_t)t0 * k;
+    prof.begin(MOE_PROF_PERMUTE, ms);
     r = moe_permute(ids_c, n, E, ws.count, ws.offset, ws.rows, ws.pos, ws.act_e, ws.n_act, a->dev_status, main_s);
     if (r != MOE_OK) return r;
+    prof.end(ms);
     FfnArgs f{(const uint16_t*)a->x + (size_t)t0 * H, tc, H, I, k, E, ws.offset, ws.rows, nullptr, nullptr,
               (const uint16_t*)a->pool, a->e2s, (const uint16_t*)a->host_slabs, (size_t)3 * H * I, ws.hbuf, ws.y,
               a->dev_status};
@@ -185,11 +192,13 @@ extern "C" int moe_layer_forward(const moe_layer_args* a, moe_stream_t main_s, m
       f.list_e = ws.act_e;
       f.n_list = ws.n_act;
       f.host = nullptr;
-      if ((r = launch_ffn(f, lmax, ms)) != MOE_OK) return r;
+      if ((r = launch_ffn(f, lmax, ms, &prof)) != MOE_OK) return r;
     } else {
+      prof.begin(MOE_PROF_MANAGE, ms);
       r = launch_manage(ids_c, n, E, S, policy, a->e2s, a->s2e, a->prio, a->stamp, ws.miss_e, ws.miss_s, ws.n_miss,
                         ws.hit_e, ws.n_hit, nullptr, stats, a->dev_status, ms);
       if (r != MOE_OK) return r;
+      prof.end(ms);
       FfnArgs fh = f, fm = f;
       fh.list_e = ws.hit_e;
       fh.n_list = ws.n_hit;
@@ -202,27 +211,31 @@ extern "C" int moe_layer_forward(const moe_layer_args* a, moe_stream_t main_s, m
       cudaStream_t side = two ? ss : ms;
       if (mode == MOE_MODE_GATHER) {
         // side: gather the misses; main: the hit experts' FFN meanwhile; then the misses.
+        prof.begin(MOE_PROF_GATHER, side);
         r = launch_gather(a->host_slabs, a->pool, slab_bytes, E, S, ws.miss_e, ws.miss_s, ws.n_miss, lmax, stats,
                           a->dev_status, side);
         if (r != MOE_OK) return r;
+        prof.end(side);
         if (two) MOE_CUDA_TRY(cudaEventRecord(ev->join, ss));
-        if ((r = launch_ffn(fh, lmax, ms)) != MOE_OK) return r;
+        if ((r = launch_ffn(fh, lmax, ms, &prof)) != MOE_OK) return r;
         if (two) MOE_CUDA_TRY(cudaStreamWaitEvent(ms, ev->join, 0));
-        if ((r = launch_ffn(fm, lmax, ms)) != MOE_OK) return r;
+        if ((r = launch_ffn(fm, lmax, ms, &prof)) != MOE_OK) return r;
       } else {
         // zero-return: resident experts from the pool on main, missing ones
         // straight from the host store on the side stream; then one add.
-        if ((r = launch_ffn(fm, lmax, side)) != MOE_OK) return r;
+        if ((r = launch_ffn(fm, lmax, side, &prof)) != MOE_OK) return r;
         if (two) MOE_CUDA_TRY(cudaEventRecord(ev->join, ss));
-        if ((r = launch_ffn(fh, lmax, ms)) != MOE_OK) return r;
+        if ((r = launch_ffn(fh, lmax, ms, &prof)) != MOE_OK) return r;
         if (two) MOE_CUDA_TRY(cudaStreamWaitEvent(ms, ev->join, 0));
       }
     }
     const int split = mode == MOE_MODE_ZERO_RETURN;
+    prof.begin(MOE_PROF_COMBINE, ms);
     r = launch_combine(ws.y, a->w + (size_t)t0 * k, ws.pos, ids_c, a->e2s, tc, k, H, E, split,
                        (uint16_t*)a->out + (size_t)t0 * H, split ? a->out_res + (size_t)t0 * H : nullptr,
                        split ? a->out_miss + (size_t)t0 * H : nullptr, ms);
     if (r != MOE_OK) return r;
+    prof.end(ms);
   }
   return MOE_OK;
 }

@@ -212,7 +212,7 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(const FfnArgs a) {
 
 static size_t ffn_smem_bytes(int K) { return (size_t)(kRB * K + 8 * 8 * kRB * 8) * sizeof(float); }
 
-int launch_ffn(const FfnArgs& a, int max_list, cudaStream_t stream) {
+int launch_ffn(const FfnArgs& a, int max_list, cudaStream_t stream, Prof* prof) {
   if (max_list <= 0) return MOE_OK;
   constexpr int kSmemCap = 160 * 1024;
   const size_t smem_gu = ffn_smem_bytes(a.H), smem_d = ffn_smem_bytes(a.I);
@@ -225,10 +225,14 @@ int launch_ffn(const FfnArgs& a, int max_list, cudaStream_t stream) {
   MOE_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
   const int g1 = std::min(max_list * (a.I / kGUTile), sms);
   const int g2 = std::min(max_list * (a.H / kDTile), sms);
+  if (prof) prof->begin(MOE_PROF_FFN_GATEUP, stream);
   ffn_kernel<false><<<g1, kFfnThreads, smem_gu, stream>>>(a);
   MOE_LAUNCH_CHECK();
+  if (prof) prof->end(stream);
+  if (prof) prof->begin(MOE_PROF_FFN_DOWN, stream);
   ffn_kernel<true><<<g2, kFfnThreads, smem_d, stream>>>(a);
   MOE_LAUNCH_CHECK();
+  if (prof) prof->end(stream);
   return MOE_OK;
 }
 

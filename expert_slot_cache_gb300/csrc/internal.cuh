@@ -21,7 +21,26 @@ struct FfnArgs {
   int32_t* status;
 };
 
-int launch_ffn(const FfnArgs& a, int max_list, cudaStream_t stream);
+// Records (start, end) event pairs around kernel launches when tracing is on.
+struct Prof {
+  moe_prof* p = nullptr;
+  int cur = -1;
+  void begin(int tag, cudaStream_t s) {
+    cur = -1;
+    if (!p || !p->events || p->used + 2 > p->capacity) return;
+    cur = p->used;
+    cudaEventRecord((cudaEvent_t)p->events[cur], s);
+    if (p->tags) p->tags[cur / 2] = tag;
+  }
+  void end(cudaStream_t s) {
+    if (cur < 0) return;
+    cudaEventRecord((cudaEvent_t)p->events[cur + 1], s);
+    p->used = cur + 2;
+    cur = -1;
+  }
+};
+
+int launch_ffn(const FfnArgs& a, int max_list, cudaStream_t stream, Prof* prof = nullptr);
 int launch_combine(const float* y, const float* w, const int32_t* pos, const int32_t* ids, const int32_t* e2s, int T,
                    int k, int H, int E, int split, void* out, float* out_res, float* out_miss, cudaStream_t stream);
 int launch_manage(const int32_t* ids, int n, int E, int S, int policy, int32_t* e2s, int32_t* s2e, uint32_t* prio,

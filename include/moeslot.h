@@ -211,6 +211,31 @@ int moe_combine(const float* y, const float* w, const int32_t* pos, const int32_
                 int T, int k, int H, int E, int split, void* out, float* out_res, float* out_miss,
                 moe_stream_t stream);
 
+/*
+ * Optional per-kernel timing of moe_layer_forward (tracing).  `events` holds
+ * `capacity` cudaEvent_t handles created by the caller with timing enabled.
+ * The layer forward records one (start, end) pair around each kernel it
+ * launches, on the stream that kernel runs on, in launch order, while pairs
+ * remain; `used` (out) is the number of handles recorded and tags[i] (out)
+ * the kernel class of pair i.  Recording events adds no synchronisation.
+ */
+enum {
+  MOE_PROF_ROUTE = 0,
+  MOE_PROF_PERMUTE = 1,
+  MOE_PROF_MANAGE = 2,
+  MOE_PROF_GATHER = 3,
+  MOE_PROF_FFN_GATEUP = 4,
+  MOE_PROF_FFN_DOWN = 5,
+  MOE_PROF_COMBINE = 6,
+  MOE_PROF_CLASSES = 7
+};
+typedef struct moe_prof {
+  void** events;    /* cudaEvent_t[capacity] */
+  int32_t capacity;
+  int32_t used;     /* out */
+  int32_t* tags;    /* [capacity / 2] out */
+} moe_prof;
+
 /* Arguments of moe_layer_forward.  Field meanings as in the calls above. */
 typedef struct moe_layer_args {
   int32_t T, H, E, k, I, S;
@@ -235,6 +260,7 @@ typedef struct moe_layer_args {
   int32_t* dev_status;       /* device int32 [1] */
   void* workspace;           /* device scratch, moe_layer_workspace_bytes() */
   size_t workspace_bytes;
+  moe_prof* prof;            /* host struct, or NULL: per-kernel timing events */
 } moe_layer_args;
 
 /*

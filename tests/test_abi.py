@@ -12,9 +12,10 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 @pytest.fixture(scope="module")
 def lib():
-    from expert_slot_cache_gb300 import build
-    build.build()
-    return ctypes.CDLL(build.LIB)
+    import __graft_entry__
+    b = __graft_entry__._build_module()
+    b.build()
+    return ctypes.CDLL(b.LIB)
 
 
 def _declared():
