@@ -1,0 +1,457 @@
+#!/usr/bin/env python
+"""Benchmark of the slot-cached MoE layer forward on GB300.
+
+Default workload (one "step" = one full layer forward: route, permute,
+expert_cache_manage, expert_cache_gather on a side stream, grouped SwiGLU
+FFN, combine): a Qwen3-30B-A3B-shaped decode layer, T=64 tokens, hidden 2048,
+128 experts, top-8, intermediate 768, bf16, 64 of 128 experts in the VRAM slot
+pool, the rest in pinned host memory, LRU.  Each step gets a fresh seeded
+batch, so the routing (near-uniform) changes every step and the cache sees a
+steady miss stream.  Inputs are synthetic (no weights or traces exist here).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  --impl reference times the CPU oracle on the
+host cores on a bounded sample of the same workload.  N > 1 (under torchrun)
+runs N independent replicas, one per GPU: the path has no exchange step.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+if "--impl" in sys.argv and "reference" in sys.argv:
+    # the oracle leg: pin the BLAS pools before numpy loads, so "cores" is exact
+    _thr = os.environ.get("MOE_ORACLE_THREADS", "1")
+    for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[_v] = _thr
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from harness import configs as C  # noqa: E402
+
+METRIC = "MoE-layer tokens/s at 1 GB300; decode HBM GB/s vs roofline; prefill TFLOP/s"
+UNIT = "tokens/s"
+PROF_NAMES = ("route", "permute", "manage", "gather", "ffn_gateup", "ffn_down", "combine")
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p["bf16_tflops_sustained"], "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ----------------------------------------------------------------------------
+# distributed plumbing (replicas only)
+# ----------------------------------------------------------------------------
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+        return ws, rank, local, dist
+    return 1, 0, local, None
+
+
+def _barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def _max_over_ranks(v: float, dist) -> float:
+    if dist is None:
+        return v
+    t = torch.tensor([v], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t[0])
+
+
+# ----------------------------------------------------------------------------
+# clocks during the timed region
+# ----------------------------------------------------------------------------
+
+class Clocks:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.p = None
+
+    def start(self):
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                       "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                                      stderr=subprocess.DEVNULL)
+        except Exception:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return None
+        time.sleep(0.25)
+        self.p.terminate()
+        try:
+            self.p.wait(timeout=5)
+        except Exception:
+            self.p.kill()
+        self.f.flush()
+        self.f.seek(0)
+        rows = [r.split(",") for r in self.f.read().strip().splitlines() if r.count(",") >= 8]
+        os.unlink(self.f.name)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.strip() == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------
+# workload setup
+# ----------------------------------------------------------------------------
+
+class Workload:
+    """One layer's weights, slot pool, host store, cache state and input batches."""
+
+    def __init__(self, cfg: C.LayerConfig, n_batches: int, dev: str):
+        import expert_slot_cache_gb300 as M
+        self.cfg, self.dev, self.M = cfg, dev, M
+        self.wr = C.draw_router(cfg, dev)
+        slabs = torch.empty(cfg.E, cfg.slab_elems, dtype=torch.bfloat16, device=dev)
+        C.draw_slabs(cfg, dev, out=slabs)
+        self.off = C.draw_logit_offset(cfg, dev)
+        self.bias = None
+        if cfg.bias_cap is not None:
+            b, _ = C.draw_brightness(cfg)
+            self.bias = M.bias_table(torch.from_numpy(b).to(dev), cfg.n_hot, cfg.bias_cap)
+        if cfg.mode == C.MODE_RESIDENT:
+            self.host, self.pool, self.state = None, slabs, None
+        else:
+            self.host = torch.empty(cfg.E, cfg.slab_elems, dtype=torch.bfloat16, pin_memory=True)
+            self.host.copy_(slabs)
+            s2e0 = C.initial_residency(cfg)
+            self.pool = slabs[torch.from_numpy(s2e0.astype(np.int64)).to(dev)].contiguous()
+            del slabs
+            self.state = M.CacheState.from_slots(s2e0, cfg.E, dev)
+        self.layer = M.SlotCachedMoELayer(self.wr, self.pool, cfg.k, cfg.I, cfg.mode, cfg.policy,
+                                          host_slabs=self.host, state=self.state, logit_offset=self.off,
+                                          sel_bias=self.bias, max_tokens=cfg.T)
+        self.xs = [C.draw_x(cfg, dev, step=i) for i in range(n_batches)]
+        self.out = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16, device=dev)
+        self.out_res = self.out_miss = None
+        if cfg.mode == C.MODE_ZERO_RETURN:
+            self.out_res = torch.empty(cfg.T, cfg.H, dtype=torch.float32, device=dev)
+            self.out_miss = torch.empty(cfg.T, cfg.H, dtype=torch.float32, device=dev)
+        self.ids = torch.empty(cfg.T, cfg.k, dtype=torch.int32, device=dev)
+        self.w = torch.empty(cfg.T, cfg.k, dtype=torch.float32, device=dev)
+
+    def chunk(self) -> int:
+        c = self.cfg
+        if c.mode != C.MODE_GATHER or c.S >= c.E or c.T * c.k <= c.S:
+            return c.T
+        return c.S // c.k
+
+    def step(self, i, prof=None, x=None):
+        return self.layer.forward(self.xs[i] if x is None else x, out=self.out, ids=self.ids, w=self.w,
+                                  out_res=self.out_res, out_miss=self.out_miss, prof=prof)
+
+    def unique_per_chunk(self, ids: np.ndarray) -> int:
+        C_ = self.chunk()
+        return sum(len(np.unique(ids[t0:t0 + C_])) for t0 in range(0, ids.shape[0], C_))
+
+
+def _make_prof(M, pairs: int):
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * pairs)]
+    for ev in evs:  # torch creates the underlying event lazily, on its first record
+        ev.record()
+    arr = (M.binding.c_void_p * (2 * pairs))(*[e.cuda_event for e in evs])
+    tags = (M.binding.c_int32 * pairs)()
+    p = M.binding.Prof(arr, 2 * pairs, 0, tags)
+    return p, evs, arr, tags
+
+
+def _prof_times(p, evs) -> dict:
+    out = {n: [] for n in PROF_NAMES}
+    for i in range(p.used // 2):
+        out[PROF_NAMES[p.tags[i]]].append(evs[2 * i].elapsed_time(evs[2 * i + 1]))
+    return out
+
+
+def time_steps(wl: Workload, steps: int, warmup: int, dist=None, clocks=None, profile=True):
+    """Device-timed K steps after W warm-ups; per-kernel live times from events."""
+    M = wl.M
+    for i in range(warmup):
+        wl.step(i)
+    pairs = 2 + wl.cfg.T * 16
+    profs = [_make_prof(M, pairs) for _ in range(steps)] if profile else None
+    uniq, misses0 = [], int(wl.layer.stats[0])
+    gathered0 = int(wl.layer.stats[2])
+    torch.cuda.synchronize()
+    _barrier(dist)
+    if clocks:
+        clocks.start()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for i in range(steps):
+        wl.step(warmup + i, prof=profs[i][0] if profile else None)
+    e.record()
+    torch.cuda.synchronize()
+    cl = clocks.stop() if clocks else None
+    _barrier(dist)
+    ms = s.elapsed_time(e)
+    ms = _max_over_ranks(ms, dist)
+    kern = {n: 0.0 for n in PROF_NAMES}
+    launches = {n: 0 for n in PROF_NAMES}
+    if profile:
+        for p, evs, _, _ in profs:
+            for n, v in _prof_times(p, evs).items():
+                kern[n] += sum(v)
+                launches[n] += len(v)
+    # work counts (for the roofline), from the step's outputs: replay the last step's ids only
+    uniq = wl.unique_per_chunk(wl.ids.cpu().numpy())
+    misses = int(wl.layer.stats[0]) - misses0
+    gathered = int(wl.layer.stats[2]) - gathered0
+    return {"ms": ms, "kern_ms": kern, "launches": launches, "clocks": cl, "misses": misses,
+            "gathered_bytes": gathered, "unique_last": uniq}
+
+
+def count_unique_all(wl: Workload, steps: int, warmup: int) -> int:
+    """Expert-chunk units streamed by the FFN over the timed steps (re-run routing only)."""
+    M = wl.M
+    tot = 0
+    for i in range(steps):
+        ids, _ = M.route(wl.xs[warmup + i], wl.wr, wl.cfg.k, wl.off, wl.bias)
+        tot += wl.unique_per_chunk(ids.cpu().numpy())
+    return tot
+
+
+def host_link_peak(dev: str, nbytes: int = 1 << 30) -> float:
+    """Pinned host -> device copy bandwidth (GB/s), measured here with cudaMemcpyAsync."""
+    h = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    d = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    d.copy_(h, non_blocking=True)
+    torch.cuda.synchronize()
+    best = 0.0
+    for _ in range(3):
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        d.copy_(h, non_blocking=True)
+        e.record()
+        torch.cuda.synchronize()
+        best = max(best, nbytes / (s.elapsed_time(e) * 1e-3) / 1e9)
+    del h, d
+    return best
+
+
+def e2e_steps(wl: Workload, steps: int, warmup: int, dist=None):
+    """Same metric through the public API with host buffers: H2D of x and D2H of out in the timed region."""
+    cfg = wl.cfg
+    hx = [wl.xs[i].cpu().pin_memory() for i in range(warmup + steps)]
+    hout = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16, pin_memory=True)
+    dx = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16, device=wl.dev)
+    for i in range(warmup):
+        dx.copy_(hx[i], non_blocking=True)
+        wl.step(0, x=dx)
+        hout.copy_(wl.out, non_blocking=True)
+    torch.cuda.synchronize()
+    _barrier(dist)
+    t0 = time.perf_counter()
+    for i in range(steps):
+        dx.copy_(hx[warmup + i], non_blocking=True)
+        wl.step(0, x=dx)
+        hout.copy_(wl.out, non_blocking=True)
+    torch.cuda.synchronize()
+    dt = _max_over_ranks(time.perf_counter() - t0, dist)
+    nb = cfg.T * cfg.H * 2
+    return {"value": cfg.T * steps / dt, "unit": UNIT, "h2d_bytes_per_step": nb, "d2h_bytes_per_step": nb}
+
+
+# ----------------------------------------------------------------------------
+# the CPU oracle leg
+# ----------------------------------------------------------------------------
+
+def oracle_sample(cfg: C.LayerConfig, steps: int, warmup: int, dev: str):
+    """Time the oracle on ``steps`` layer forwards of the workload (after ``warmup``)."""
+    import oracle as O
+    gen_dev = dev if torch.cuda.is_available() else "cpu"
+    wr = C.draw_router(cfg, gen_dev).float().cpu().numpy()
+    host = torch.empty(cfg.E, cfg.slab_elems, dtype=torch.bfloat16)
+    for e in range(cfg.E):
+        host[e].copy_(C.draw_slab(cfg, e, gen_dev))
+
+    class _S:
+        def __getitem__(self, e):
+            return host[int(e)].float().numpy()
+
+    s2e0 = C.initial_residency(cfg)
+    st = O.CacheState.from_slots(s2e0, cfg.E)
+    mode = cfg.mode
+    off = C.draw_logit_offset(cfg, gen_dev)
+    off = None if off is None else off.cpu().numpy()
+    xs = [C.draw_x(cfg, gen_dev, step=i).float().cpu().numpy() for i in range(warmup + steps)]
+    for i in range(warmup):
+        O.layer_forward(xs[i], wr, _S(), cfg.H, cfg.I, cfg.k, mode, cfg.policy, st, None, off)
+    t0 = time.perf_counter()
+    for i in range(steps):
+        O.layer_forward(xs[warmup + i], wr, _S(), cfg.H, cfg.I, cfg.k, mode, cfg.policy, st, None, off)
+    dt = time.perf_counter() - t0
+    cores = int(os.environ.get("OPENBLAS_NUM_THREADS", "0") or 0) or os.cpu_count()
+    return {"value": cfg.T * steps / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{steps} full layer forward(s) of the benchmarked workload (T={cfg.T}), after {warmup} "
+                      f"warm-up; numpy oracle, fp64 FFN", "seconds": dt}
+
+
+def run_reference(args, ws, rank, dist):
+    if rank != 0:
+        return
+    cfg = main_config()
+    steps = max(1, min(args.steps, 20))
+    warm = min(args.warmup, 1)
+    r = oracle_sample(cfg, steps, warm, "cuda:0")
+    line = {"impl": "reference", "metric": METRIC, "value": r["value"], "unit": UNIT, "n_gpus": args.gpus,
+            "steps": steps, "warmup": warm, "ms_per_step": 1e3 * r["seconds"] / steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_obj(cfg), "cpu_baseline": r,
+            "e2e": {"value": r["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------
+# main
+# ----------------------------------------------------------------------------
+
+def main_config() -> C.LayerConfig:
+    return C.qwen(64, S=64, mode=C.MODE_GATHER, policy=C.POLICY_LRU)
+
+
+def config_obj(cfg: C.LayerConfig) -> dict:
+    return {"workload": f"qwen3-30b-a3b-shaped MoE decode layer, T={cfg.T}, H={cfg.H}, E={cfg.E}, k={cfg.k}, "
+                        f"I={cfg.I}, bf16, slot pool {cfg.S} of {cfg.E} (rest pinned host), LRU, gather",
+            "T": cfg.T, "H": cfg.H, "E": cfg.E, "k": cfg.k, "I": cfg.I, "S": cfg.S, "mode": "gather",
+            "policy": "lru", "l2": "inputs larger than L2 (expert weights 1.21 GB; every step streams its experts)",
+            "parallelism": "replicas"}
+
+
+def ffn_roofline(wl: Workload, r: dict, units: int, peaks: dict) -> dict:
+    cfg = wl.cfg
+    bytes_per_unit = cfg.slab_bytes  # gate/up (4HI bytes) + down (2HI bytes) per expert-chunk unit
+    t = (r["kern_ms"]["ffn_gateup"] + r["kern_ms"]["ffn_down"]) * 1e-3
+    ach = units * bytes_per_unit / t / 1e9 if t > 0 else 0.0
+    return {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": ach / peaks["hbm_gbs"], "traffic": None, "kernel": "ffn_gateup+ffn_down",
+            "bytes_per_unit": bytes_per_unit, "units": units, "peak_source": peaks["source"]}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-variants", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    ws, rank, local, dist = _dist()
+    if args.impl == "reference":
+        run_reference(args, ws, rank, dist)
+        return
+    args.warmup = max(3, args.warmup)
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    peaks = _peaks()
+    cfg = main_config()
+    K, W = args.steps, args.warmup
+
+    wl = Workload(cfg, K + W, dev)
+    clocks = Clocks(local)
+    r = time_steps(wl, K, W, dist, clocks)
+    units = count_unique_all(wl, K, W)
+    value = ws * cfg.T * K / (r["ms"] * 1e-3)
+    link_peak = host_link_peak(dev)
+    kern = r["kern_ms"]
+    dominant = max(kern, key=kern.get)
+    if dominant == "gather":
+        t = kern["gather"] * 1e-3
+        ach = r["gathered_bytes"] / t / 1e9 if t > 0 else 0.0
+        roof = {"bound": "host-link", "achieved": ach, "peak": link_peak, "unit": "GB/s", "frac": ach / link_peak,
+                "traffic": None, "kernel": "gather", "bytes_per_unit": cfg.slab_bytes,
+                "units": r["misses"], "peak_source": "pinned-host->device cudaMemcpyAsync measured in this run"}
+    else:
+        roof = ffn_roofline(wl, r, units, peaks)
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": K, "warmup": W,
+            "ms_per_step": r["ms"] / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic (seeded, Irwin-Hall normal weights/activations)",
+            "config": config_obj(cfg), "roofline": roof, "clocks": r["clocks"],
+            "gpu_launches": sum(r["launches"].values()),
+            "kernels_ms_per_step": {n: v / K for n, v in kern.items()},
+            "misses_per_step": r["misses"] / K, "gathered_GB_per_step": r["gathered_bytes"] / K / 1e9,
+            "host_link_peak_gbs": link_peak,
+            "roofline_ffn_hbm": ffn_roofline(wl, r, units, peaks)}
+    line["e2e"] = e2e_steps(wl, K, W, dist)
+    del wl
+    torch.cuda.empty_cache()
+
+    if not args.no_variants:
+        var = {}
+        # all-resident control: the HBM roofline of the decode FFN
+        for T in (1, 8, 64):
+            c2 = C.qwen(T, S=128, mode=C.MODE_RESIDENT)
+            w2 = Workload(c2, 10 + 3, dev)
+            r2 = time_steps(w2, 10, 3)
+            u2 = count_unique_all(w2, 10, 3)
+            var[f"all_resident_T{T}"] = {"tokens_per_s": T * 10 / (r2["ms"] * 1e-3), "ms_per_step": r2["ms"] / 10,
+                                         "ffn_hbm": ffn_roofline(w2, r2, u2, peaks),
+                                         "layer_hbm_frac": u2 * c2.slab_bytes / (r2["ms"] * 1e-3) / 1e9
+                                         / peaks["hbm_gbs"]}
+            del w2
+        for T in (1, 8, 32):
+            c3 = C.qwen(T, S=64)
+            w3 = Workload(c3, 10 + 3, dev)
+            r3 = time_steps(w3, 10, 3, profile=False)
+            var[f"gather_T{T}"] = {"tokens_per_s": T * 10 / (r3["ms"] * 1e-3), "ms_per_step": r3["ms"] / 10,
+                                   "misses_per_step": r3["misses"] / 10}
+            del w3
+        torch.cuda.empty_cache()
+        line["variants"] = var
+
+    if not args.no_cpu_baseline and rank == 0:
+        env = dict(os.environ, MOE_ORACLE_THREADS="1", WORLD_SIZE="1", RANK="0", LOCAL_RANK=str(local))
+        p = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "2",
+                            "--warmup", "0"], capture_output=True, text=True, env=env)
+        try:
+            ref = json.loads(p.stdout.strip().splitlines()[-1])
+            line["cpu_baseline"] = ref["cpu_baseline"]
+        except Exception:
+            line["cpu_baseline"] = {"value": None, "error": (p.stderr or p.stdout)[-300:]}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

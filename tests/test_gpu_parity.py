@@ -349,7 +349,8 @@ def test_layer_stack_shape_gather_chunked():
 def test_layer_prefill_sampled_tokens():
     cfg = C.PREFILL
     st = stage_layer(cfg)
-    layer = M.SlotCachedMoELayer(st["wr"], st["slabs_dev"], cfg.k, cfg.I, cfg.mode, max_tokens=cfg.T)
+    layer = M.SlotCachedMoELayer(st["wr"], st["slabs_dev"], cfg.k, cfg.I, cfg.mode, max_tokens=cfg.T,
+                                 logit_offset=st["logit_offset"])
     x = C.draw_x(cfg, DEV)
     res = layer.forward(x)
     torch.cuda.synchronize()
