@@ -90,6 +90,7 @@ extern "C" const char* moe_status_str(int s) {
     case MOE_ERR_NOT_DEVICE_ACCESSIBLE: return "host store is not addressable by the device";
     case MOE_ERR_CUDA: return "CUDA runtime error";
     case MOE_ERR_DEVICE_STATUS: return "a kernel reported an invalid item";
+    case MOE_ERR_SCRATCH_LIMIT: return "request exceeds the fixed scratch of the allocation-free entry point";
     default: return "unknown status";
   }
 }

@@ -48,7 +48,8 @@ typedef enum {
   MOE_ERR_ALIGN = -3,                 /* slab size or a pointer not a 16-byte multiple, workspace too small */
   MOE_ERR_NOT_DEVICE_ACCESSIBLE = -4, /* host store not addressable by the GPU */
   MOE_ERR_CUDA = -5,                  /* a CUDA runtime call failed */
-  MOE_ERR_DEVICE_STATUS = -6          /* reserved: a kernel reported a bad item */
+  MOE_ERR_DEVICE_STATUS = -6,         /* reserved: a kernel reported a bad item */
+  MOE_ERR_SCRATCH_LIMIT = -7          /* request larger than the fixed scratch of moe_expert_ffn_noalloc */
 } moe_status;
 
 typedef enum { MOE_POLICY_LRU = 0, MOE_POLICY_LFU = 1, MOE_POLICY_STATIC = 2 } moe_policy;
@@ -193,6 +194,35 @@ int moe_expert_ffn(const void* x, int T, int H, int I, int k, int E, const int32
                    void* workspace, size_t workspace_bytes, int32_t* dev_status, moe_stream_t stream);
 
 size_t moe_ffn_workspace_bytes(int T, int k, int I);
+
+/*
+ * The grouped expert FFN for callers that cannot allocate device memory.
+ * The pages have no counterpart: this is a deployment variant of
+ * moe_expert_ffn, not part of the method.
+ *
+ * Some callers cannot call cudaMalloc (or any allocator) where they run the
+ * FFN, for example code running in a host callback, a plug-in that must not
+ * touch its host's memory pool, or a runtime whose allocator is frozen after
+ * start-up.  This variant takes no workspace: the intermediate h lives in one
+ * fixed device array inside the library, MOE_FFN_NOALLOC_MAX_H fp32 values
+ * (4 MiB) that every GPU which loads the library holds until the process
+ * exits.  It calls no cudaMalloc, cudaFree or other allocating routine.
+ * Arguments, outputs and results are those of moe_expert_ffn.
+ *   - Limit: T * k * I <= MOE_FFN_NOALLOC_MAX_H, else MOE_ERR_SCRATCH_LIMIT
+ *     is returned and nothing is enqueued.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - All calls share the array and it keeps the last call's contents.
+ *     Nothing in it needs to start at zero (each call writes every h row it
+ *     reads), but calls that overlap on the GPU (other streams, other host
+ *     threads) race on it: serialise them.
+ */
+#define MOE_FFN_NOALLOC_MAX_H (1u << 20)
+int moe_expert_ffn_noalloc(const void* x, int T, int H, int I, int k, int E, const int32_t* offset,
+                           const int32_t* rows, const int32_t* list_e, const int32_t* n_list, int max_list,
+                           const void* pool, const int32_t* e2s, const void* host_slabs, float* y,
+                           int32_t* dev_status, moe_stream_t stream);
 
 /*
  * Weighted scatter-combine back to token order.
