@@ -64,7 +64,7 @@ _route = _sig("moe_route", [V, V, V, V, I32, I32, I32, I32, V, V, V, V])
 _permute = _sig("moe_permute", [V, I32, I32, V, V, V, V, V, V, V, V])
 _manage = _sig("moe_cache_manage", [V, I32, I32, I32, I32, V, V, V, V, V, V, V, V, V, V, V, V])
 _gather = _sig("moe_cache_gather", [V, V, c_size_t, I32, I32, V, V, V, I32, V, V])
-_ffn = _sig("moe_expert_ffn", [V, I32, I32, I32, I32, I32, V, V, V, V, I32, V, V, V, V, V, c_size_t, V, V])
+_ffn = _sig("moe_expert_ffn", [V, I32, I32, I32, I32, I32, V, V, V, V, I32, V, I32, V, V, V, V, c_size_t, V, V])
 _ffn_ws = _sig("moe_ffn_workspace_bytes", [I32, I32, I32], c_size_t)
 _combine = _sig("moe_combine", [V, V, V, V, V, I32, I32, I32, I32, I32, V, V, V, V])
 _layer = _sig("moe_layer_forward", [POINTER(LayerArgs), V, V])
@@ -204,7 +204,8 @@ def expert_ffn(x, k, I, E, offset, rows, list_e, n_list, max_list, pool, e2s=Non
         y = torch.zeros(T * k, H, dtype=torch.float32, device=x.device)
     if workspace is None:
         workspace = torch.empty(ffn_workspace_bytes(T, k, I), dtype=torch.uint8, device=x.device)
-    _ck(_ffn(_p(x), T, H, I, k, E, _p(offset), _p(rows), _p(list_e), _p(n_list), max_list, _p(pool), _p(e2s),
+    _ck(_ffn(_p(x), T, H, I, k, E, _p(offset), _p(rows), _p(list_e), _p(n_list), max_list, _p(pool),
+             pool.shape[0], _p(e2s),
              _p(host_slabs), _p(y), _p(workspace), workspace.numel(), _p(dev_status), _s(stream)),
         "moe_expert_ffn")
     return y

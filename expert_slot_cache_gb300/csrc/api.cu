@@ -102,10 +102,10 @@ extern "C" size_t moe_ffn_workspace_bytes(int T, int k, int I) {
 
 extern "C" int moe_expert_ffn(const void* x, int T, int H, int I, int k, int E, const int32_t* offset,
                               const int32_t* rows, const int32_t* list_e, const int32_t* n_list, int max_list,
-                              const void* pool, const int32_t* e2s, const void* host_slabs, float* y,
+                              const void* pool, int S, const int32_t* e2s, const void* host_slabs, float* y,
                               void* workspace, size_t workspace_bytes, int32_t* dev_status, moe_stream_t stream) {
   if (!x || !offset || !rows || !list_e || !n_list || !pool || !y || !workspace) return MOE_ERR_ARG;
-  if (!shape_ok(T, H, I, k, E) || max_list < 0) return MOE_ERR_ARG;
+  if (!shape_ok(T, H, I, k, E) || max_list < 0 || S < 1 || (!e2s && S < E)) return MOE_ERR_ARG;
   if ((uintptr_t)pool % 16 || (uintptr_t)y % 16 || (uintptr_t)workspace % 16) return MOE_ERR_ALIGN;
   if (workspace_bytes < moe_ffn_workspace_bytes(T, k, I)) return MOE_ERR_ALIGN;
   if (host_slabs) {
@@ -114,7 +114,8 @@ extern "C" int moe_expert_ffn(const void* x, int T, int H, int I, int k, int E, 
     if (acc != MOE_OK) return acc;
   }
   FfnArgs a{(const uint16_t*)x, T, H, I, k, E, offset, rows, list_e, n_list, (const uint16_t*)pool, e2s,
-            (const uint16_t*)host_slabs, (size_t)3 * H * I, (float*)workspace, y, dev_status};
+            (const uint16_t*)host_slabs, (size_t)3 * H * I, (float*)workspace, y, dev_status, S,
+            host_slabs == nullptr};
   return launch_ffn(a, std::min(max_list, E), (cudaStream_t)stream);
 }
 
@@ -188,7 +189,7 @@ extern "C" int moe_layer_forward(const moe_layer_args* a, moe_stream_t main_s, m
     prof.end(ms);
     FfnArgs f{(const uint16_t*)a->x + (size_t)t0 * H, tc, H, I, k, E, ws.offset, ws.rows, nullptr, nullptr,
               (const uint16_t*)a->pool, a->e2s, (const uint16_t*)a->host_slabs, (size_t)3 * H * I, ws.hbuf, ws.y,
-              a->dev_status};
+              a->dev_status, S, 1};
     if (mode == MOE_MODE_RESIDENT) {
       f.list_e = ws.act_e;
       f.n_list = ws.n_act;
@@ -201,6 +202,7 @@ extern "C" int moe_layer_forward(const moe_layer_args* a, moe_stream_t main_s, m
       if (r != MOE_OK) return r;
       prof.end(ms);
       FfnArgs fh = f, fm = f;
+      fm.pool_only = mode == MOE_MODE_GATHER;  // zero-return reads the missing experts from host memory
       fh.list_e = ws.hit_e;
       fh.n_list = ws.n_hit;
       fm.list_e = ws.miss_e;

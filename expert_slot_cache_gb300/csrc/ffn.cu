@@ -17,6 +17,7 @@
 #include <algorithm>
 
 #include "internal.cuh"
+#include "tma.cuh"
 
 namespace moe {
 
@@ -210,6 +211,211 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(const FfnArgs a) {
   }
 }
 
+// ---------------------------------------------------------------------------
+// TMA-staged variant (weights in the slot pool).
+//
+// Same work items, thread mapping, summation order and reduction as
+// ffn_kernel, but the weight tiles are brought into a ring of shared-memory
+// stages by one producer thread with 3-D tensor-map bulk copies
+// (cp.async.bulk.tensor), so the bytes in flight no longer sit in registers.
+// Warps 0-7 consume, warp 8 produces.  The pool is viewed as 3*S matrices of
+// H*I bf16: gate of slot s = matrix 3s, up = 3s+1 (both [H][I]), down = 3s+2
+// ([I][H]).  A stage holds kKB rows of the tile (16 KB).
+// ---------------------------------------------------------------------------
+constexpr int kStages = 6;
+constexpr int kKB = 128;
+constexpr int kStageBytes = 16384;
+constexpr int kTmaThreads = kFfnThreads + 32;
+
+__device__ __forceinline__ int ffn_slot_of(const FfnArgs& a, int e) { return a.e2s ? a.e2s[e] : e; }
+
+template <bool kDown, int RB>
+__device__ __forceinline__ void tma_consume_batch(const FfnArgs& a, int tile, int p0, int nb, unsigned char* stages,
+                                                  uint64_t* full, uint64_t* empty, float* __restrict__ in_s,
+                                                  float* __restrict__ red, uint32_t& it, volatile int* abort_flag) {
+  const int tid = threadIdx.x, c = tid & 7, g = tid >> 3, lane = tid & 31;
+  const int H = a.H, I = a.I;
+  const int K = kDown ? I : H;
+  // stage the batch's inputs (x rows, or h rows) as fp32 [RB][K]
+  named_sync(1, kFfnThreads);
+  for (int idx = tid; idx < RB * K; idx += kFfnThreads) {
+    const int r = idx / K, kk = idx - r * K;
+    float v = 0.f;
+    if (r < nb) {
+      if (kDown) {
+        v = a.hbuf[(size_t)(p0 + r) * I + kk];
+      } else {
+        const int t = a.rows[p0 + r] / a.k;
+        v = bf16_to_f32(a.x[(size_t)t * H + kk]);
+      }
+    }
+    in_s[idx] = v;
+  }
+  named_sync(1, kFfnThreads);
+  float acc[RB][8];
+#pragma unroll
+  for (int r = 0; r < RB; ++r)
+#pragma unroll
+    for (int q = 0; q < 8; ++q) acc[r][q] = 0.f;
+  // byte offset of this thread's 16 bytes within a stage row block
+  const int mat_off = kDown ? 0 : (c < 4 ? 0 : kStageBytes / 2);
+  const int row_bytes = kDown ? kDTile * 2 : kGUTile * 2;
+  const int col_off = kDown ? 16 * c : 16 * (c & 3);
+  const int nkc = K / kKB;
+  for (int kc = 0; kc < nkc; ++kc, ++it) {
+    const int sl = it % kStages;
+    const uint32_t use = it / kStages;
+    if (!*abort_flag && !mbar_wait(&full[sl], use & 1u)) {
+      *abort_flag = 1;
+      set_status(a.status, MOE_DEV_TIMEOUT);
+    }
+    const unsigned char* st = stages + sl * kStageBytes + mat_off + col_off;
+#pragma unroll
+    for (int j = 0; j < kKB / kKG; ++j) {
+      const int rl = g + kKG * j;
+      const uint4 wv = *reinterpret_cast<const uint4*>(st + rl * row_bytes);
+      float wf[8];
+      unpack8(wv, wf);
+      const int row = kc * kKB + rl;
+#pragma unroll
+      for (int r = 0; r < RB; ++r) {
+        const float xv = in_s[r * K + row];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc[r][q] = fmaf(wf[q], xv, acc[r][q]);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[sl]);
+  }
+  warp_partials<RB>(acc, red);
+  named_sync(1, kFfnThreads);
+  if (kDown) {
+    const int o0 = tile * kDTile;
+    for (int o = tid; o < kDTile * RB; o += kFfnThreads) {
+      const int r = o / kDTile, ol = o - r * kDTile;
+      const int cg = ol >> 3, q = ol & 7;
+      float s = 0.f;
+#pragma unroll
+      for (int wp = 0; wp < kFfnThreads / 32; ++wp) s += red[((wp * 8 + cg) * RB + r) * 8 + q];
+      if (r < nb) a.y[(size_t)(p0 + r) * H + o0 + ol] = s;
+    }
+  } else {
+    const int i0 = tile * kGUTile;
+    for (int o = tid; o < kGUTile * RB; o += kFfnThreads) {
+      const int r = o / kGUTile, il = o - r * kGUTile;
+      const int cg = il >> 3, q = il & 7;
+      float gs = 0.f, us = 0.f;
+#pragma unroll
+      for (int wp = 0; wp < kFfnThreads / 32; ++wp) {
+        gs += red[((wp * 8 + cg) * RB + r) * 8 + q];
+        us += red[((wp * 8 + cg + 4) * RB + r) * 8 + q];
+      }
+      if (r < nb) a.hbuf[(size_t)(p0 + r) * I + i0 + il] = gs / (1.f + expf(-gs)) * us;
+    }
+  }
+}
+
+template <bool kDown>
+__global__ void __launch_bounds__(kTmaThreads, 1) ffn_tma_kernel(const FfnArgs a,
+                                                                 const __grid_constant__ CUtensorMap tmap) {
+  extern __shared__ __align__(16) unsigned char tsm_raw[];
+  // stages start on a 1024-byte boundary (the allocation carries 1 KB of slack)
+  unsigned char* tsm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(tsm_raw) + 1023) & ~uintptr_t(1023));
+  const int K = kDown ? a.I : a.H;
+  unsigned char* stages = tsm;
+  float* in_s = reinterpret_cast<float*>(tsm + kStages * kStageBytes);
+  float* red = in_s + kRB * K;
+  uint64_t* full = reinterpret_cast<uint64_t*>(red + 8 * 8 * kRB * 8);
+  uint64_t* empty = full + kStages;
+  __shared__ int s_abort;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kFfnThreads / 32);
+    }
+    s_abort = 0;
+    mbar_fence_init();
+  }
+  __syncthreads();
+  volatile int* abort_flag = &s_abort;
+  const int tiles = kDown ? a.H / kDTile : a.I / kGUTile;
+  const int items = *a.n_list * tiles;
+  const int nkc = K / kKB;
+
+  if (warp == kFfnThreads / 32) {
+    // producer
+    if (lane == 0) {
+      uint32_t it = 0;
+      int last_use[kStages];
+      for (int s = 0; s < kStages; ++s) last_use[s] = -1;
+      for (int item = blockIdx.x; item < items && !*abort_flag; item += gridDim.x) {
+        const int li = item / tiles, tile = item - li * tiles;
+        const int e = a.list_e[li];
+        if (e < 0 || e >= a.E) continue;
+        const int slot = ffn_slot_of(a, e);
+        if (slot < 0 || slot >= a.S) continue;
+        const int nbat = (a.offset[e + 1] - a.offset[e] + kRB - 1) / kRB;
+        for (int b = 0; b < nbat; ++b) {
+          for (int kc = 0; kc < nkc; ++kc, ++it) {
+            const int sl = it % kStages;
+            const uint32_t use = it / kStages;
+            if (use > 0 && !*abort_flag && !mbar_wait(&empty[sl], (use - 1) & 1u)) {
+              *abort_flag = 1;
+              set_status(a.status, MOE_DEV_TIMEOUT);
+            }
+            if (*abort_flag) break;
+            mbar_expect_tx(&full[sl], kStageBytes);
+            unsigned char* dst = stages + sl * kStageBytes;
+            if (kDown) {
+              tma_load_3d(dst, &tmap, &full[sl], tile * kDTile, kc * kKB, 3 * slot + 2);
+            } else {
+              tma_load_3d(dst, &tmap, &full[sl], tile * kGUTile, kc * kKB, 3 * slot);
+              tma_load_3d(dst + kStageBytes / 2, &tmap, &full[sl], tile * kGUTile, kc * kKB, 3 * slot + 1);
+            }
+            last_use[sl] = (int)use;
+          }
+        }
+      }
+      if (*abort_flag) {
+        // let every copy this thread issued land before the CTA exits
+        for (int s = 0; s < kStages; ++s)
+          if (last_use[s] >= 0) mbar_wait(&full[s], (uint32_t)last_use[s] & 1u);
+      }
+    }
+  } else {
+    // consumers
+    uint32_t it = 0;
+    for (int item = blockIdx.x; item < items; item += gridDim.x) {
+      const int li = item / tiles, tile = item - li * tiles;
+      const int e = a.list_e[li];
+      if (e < 0 || e >= a.E) {
+        if (threadIdx.x == 0) set_status(a.status, MOE_DEV_BAD_EXPERT);
+        continue;
+      }
+      const int slot = ffn_slot_of(a, e);
+      if (slot < 0 || slot >= a.S) {
+        if (threadIdx.x == 0) set_status(a.status, MOE_DEV_BAD_SLOT);
+        continue;
+      }
+      const int pb = a.offset[e], pe = a.offset[e + 1];
+      for (int p0 = pb; p0 < pe; p0 += kRB) {
+        const int nb = min(kRB, pe - p0);
+        if (nb == 1) tma_consume_batch<kDown, 1>(a, tile, p0, nb, stages, full, empty, in_s, red, it, abort_flag);
+        else if (nb == 2) tma_consume_batch<kDown, 2>(a, tile, p0, nb, stages, full, empty, in_s, red, it, abort_flag);
+        else if (nb <= 4) tma_consume_batch<kDown, 4>(a, tile, p0, nb, stages, full, empty, in_s, red, it, abort_flag);
+        else tma_consume_batch<kDown, 8>(a, tile, p0, nb, stages, full, empty, in_s, red, it, abort_flag);
+      }
+    }
+  }
+  __syncthreads();
+}
+
+static size_t tma_smem_bytes(int K) {
+  return 1024 + (size_t)kStages * kStageBytes + (size_t)(kRB * K + 8 * 8 * kRB * 8) * sizeof(float) +
+         2 * kStages * sizeof(uint64_t);
+}
+
 static size_t ffn_smem_bytes(int K) { return (size_t)(kRB * K + 8 * 8 * kRB * 8) * sizeof(float); }
 
 int launch_ffn(const FfnArgs& a, int max_list, cudaStream_t stream, Prof* prof) {
@@ -225,6 +431,33 @@ int launch_ffn(const FfnArgs& a, int max_list, cudaStream_t stream, Prof* prof) 
   MOE_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
   const int g1 = std::min(max_list * (a.I / kGUTile), sms);
   const int g2 = std::min(max_list * (a.H / kDTile), sms);
+  const bool tma = a.pool_only && a.S > 0 && a.H % kKB == 0 && a.I % kKB == 0 && tma_smem_bytes(a.H) <= 200 * 1024;
+  if (tma) {
+    static bool done_t1[64] = {}, done_t2[64] = {};
+    MOE_CUDA_TRY(ensure_smem(ffn_tma_kernel<false>, 200 * 1024, done_t1));
+    MOE_CUDA_TRY(ensure_smem(ffn_tma_kernel<true>, 200 * 1024, done_t2));
+    const size_t mat = (size_t)a.H * a.I;
+    CUtensorMap m_gu, m_d;
+    const uint64_t d_gu[3] = {(uint64_t)a.I, (uint64_t)a.H, 3ull * a.S};
+    const uint64_t s_gu[2] = {(uint64_t)a.I * 2, mat * 2};
+    const uint32_t b_gu[3] = {kGUTile, kKB, 1};
+    const uint64_t d_d[3] = {(uint64_t)a.H, (uint64_t)a.I, 3ull * a.S};
+    const uint64_t s_d[2] = {(uint64_t)a.H * 2, mat * 2};
+    const uint32_t b_d[3] = {kDTile, kKB, 1};
+    int r = encode_tmap_3d_bf16(&m_gu, a.pool, d_gu, s_gu, b_gu, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (r != MOE_OK) return r;
+    r = encode_tmap_3d_bf16(&m_d, a.pool, d_d, s_d, b_d, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (r != MOE_OK) return r;
+    if (prof) prof->begin(MOE_PROF_FFN_GATEUP, stream);
+    ffn_tma_kernel<false><<<g1, kTmaThreads, tma_smem_bytes(a.H), stream>>>(a, m_gu);
+    MOE_LAUNCH_CHECK();
+    if (prof) prof->end(stream);
+    if (prof) prof->begin(MOE_PROF_FFN_DOWN, stream);
+    ffn_tma_kernel<true><<<g2, kTmaThreads, tma_smem_bytes(a.I), stream>>>(a, m_d);
+    MOE_LAUNCH_CHECK();
+    if (prof) prof->end(stream);
+    return MOE_OK;
+  }
   if (prof) prof->begin(MOE_PROF_FFN_GATEUP, stream);
   ffn_kernel<false><<<g1, kFfnThreads, smem_gu, stream>>>(a);
   MOE_LAUNCH_CHECK();

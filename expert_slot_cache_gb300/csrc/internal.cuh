@@ -19,6 +19,8 @@ struct FfnArgs {
   float* hbuf;            // [T*k][I]
   float* y;               // [T*k][H]
   int32_t* status;
+  int S;                  // slots in pool (0 = unknown)
+  int pool_only;          // every listed expert is in the pool (e2s[e] >= 0 or e2s == NULL)
 };
 
 // Records (start, end) event pairs around kernel launches when tracing is on.

@@ -67,6 +67,7 @@ template <bool kSameE>
 __device__ __forceinline__ void route_logits(const uint16_t* __restrict__ xs, const uint16_t* __restrict__ wr,
                                              const float* __restrict__ off, int TT, int nt, int H, int E,
                                              float* __restrict__ ls) {
+  constexpr int kPF = 8;  // router rows loaded ahead of the fma chains
   const int tid = threadIdx.x;
   int tm[kMG], em[kMG];
   bool vm[kMG];
@@ -76,6 +77,10 @@ __device__ __forceinline__ void route_logits(const uint16_t* __restrict__ xs, co
     tm[m] = o / E;
     em[m] = o - tm[m] * E;
     vm[m] = (o < TT * E) && (tm[m] < nt);
+    if (!vm[m]) {  // keep idle chains in bounds; their results are discarded
+      tm[m] = 0;
+      em[m] = 0;
+    }
   }
   float acc[kMG];
 #pragma unroll
@@ -84,21 +89,35 @@ __device__ __forceinline__ void route_logits(const uint16_t* __restrict__ xs, co
   bool any = false;
 #pragma unroll
   for (int m = 0; m < kMG; ++m) any |= vm[m];
-  if (any) {
-    for (int h = 0; h < H; ++h) {
-      const uint16_t* wrow = wr + (size_t)h * E;
-      if (kSameE) {
-        // TT * E == kRouteThreads * kMG here, so tm[m] < TT for every m.
-        const float wv = bf16_to_f32(__ldg(wrow + em[0]));
+  if (!any) return;
+  const int Hm = H - H % kPF;
+  for (int h0 = 0; h0 < Hm; h0 += kPF) {
+    if (kSameE) {
+      // every chain of this thread has expert em[0]: one router load per h
+      float wv[kPF];
 #pragma unroll
-        for (int m = 0; m < kMG; ++m) acc[m] = fmaf(bf16_to_f32(xs[tm[m] * H + h]), wv, acc[m]);
-      } else {
+      for (int u = 0; u < kPF; ++u) wv[u] = bf16_to_f32(__ldg(wr + (size_t)(h0 + u) * E + em[0]));
 #pragma unroll
-        for (int m = 0; m < kMG; ++m) {
-          if (vm[m]) acc[m] = fmaf(bf16_to_f32(xs[tm[m] * H + h]), bf16_to_f32(__ldg(wrow + em[m])), acc[m]);
-        }
-      }
+      for (int u = 0; u < kPF; ++u)
+#pragma unroll
+        for (int m = 0; m < kMG; ++m) acc[m] = fmaf(bf16_to_f32(xs[tm[m] * H + h0 + u]), wv[u], acc[m]);
+    } else {
+      float wv[kPF][kMG];
+#pragma unroll
+      for (int u = 0; u < kPF; ++u)
+#pragma unroll
+        for (int m = 0; m < kMG; ++m)
+          wv[u][m] = vm[m] ? bf16_to_f32(__ldg(wr + (size_t)(h0 + u) * E + em[m])) : 0.f;
+#pragma unroll
+      for (int u = 0; u < kPF; ++u)
+#pragma unroll
+        for (int m = 0; m < kMG; ++m) acc[m] = fmaf(bf16_to_f32(xs[tm[m] * H + h0 + u]), wv[u][m], acc[m]);
     }
+  }
+  for (int h = Hm; h < H; ++h) {
+#pragma unroll
+    for (int m = 0; m < kMG; ++m)
+      acc[m] = fmaf(bf16_to_f32(xs[tm[m] * H + h]), bf16_to_f32(__ldg(wr + (size_t)h * E + em[m])), acc[m]);
   }
 #pragma unroll
   for (int m = 0; m < kMG; ++m) {
@@ -199,7 +218,12 @@ extern "C" int moe_route(const void* x, const void* w_router, const float* logit
   if (!x || !w_router || !ids || !w) return MOE_ERR_ARG;
   if (T < 1 || H < 1 || E < 1 || E > kMaxE || k < 1 || k > kMaxK || k > E) return MOE_ERR_ARG;
   constexpr int kSmemCap = 160 * 1024;
+  int sms = 0, dev = 0;
+  MOE_CUDA_TRY(cudaGetDevice(&dev));
+  MOE_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  // Enough CTAs to cover the SMs first, then up to kMG chains per thread.
   int TT = route_tt(E);
+  while (TT > 1 && (T + TT - 1) / TT < sms) TT /= 2;
   auto smem_of = [&](int tt) { return (size_t)tt * H * 2 + (size_t)tt * E * 4; };
   while (TT > 1 && smem_of(TT) > (size_t)kSmemCap) TT /= 2;
   if (smem_of(TT) > (size_t)kSmemCap) return MOE_ERR_ARG;

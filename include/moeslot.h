@@ -58,6 +58,7 @@ typedef enum { MOE_MODE_RESIDENT = 0, MOE_MODE_GATHER = 1, MOE_MODE_ZERO_RETURN 
 /* Device status codes written into dev_status. */
 #define MOE_DEV_BAD_EXPERT 1 /* an expert id outside [0, E) */
 #define MOE_DEV_BAD_SLOT 2   /* a slot id outside [0, S) where a slot was required */
+#define MOE_DEV_TIMEOUT 3    /* a kernel gave up waiting for its own asynchronous copies */
 
 const char* moe_status_str(int status);
 
@@ -178,7 +179,9 @@ int moe_cache_gather(const void* host_slabs, void* pool, size_t slab_bytes, int 
  *   h = silu(x[t] Wg_e) * (x[t] Wu_e)  (fp32),   y[p] = h Wd_e  (fp32).
  * Weights of e are read from pool + e2s[e] * slab when e2s[e] >= 0, else
  * straight from host_slabs + e * slab (the zero-return second pass).  With
- * e2s == NULL expert e sits in slot e.
+ * e2s == NULL expert e sits in slot e.  The pool holds S slots.  With
+ * host_slabs == NULL every listed expert must be in the pool; the weight
+ * tiles are then streamed through shared memory with tensor-map bulk copies.
  *   x          device bf16 [T][H]
  *   offset     device int32 [E + 1], rows device int32 [T*k] (moe_permute)
  *   list_e     device int32 [>= *n_list], n_list device int32 [1]
@@ -190,7 +193,7 @@ int moe_cache_gather(const void* host_slabs, void* pool, size_t slab_bytes, int 
  */
 int moe_expert_ffn(const void* x, int T, int H, int I, int k, int E, const int32_t* offset,
                    const int32_t* rows, const int32_t* list_e, const int32_t* n_list, int max_list,
-                   const void* pool, const int32_t* e2s, const void* host_slabs, float* y,
+                   const void* pool, int S, const int32_t* e2s, const void* host_slabs, float* y,
                    void* workspace, size_t workspace_bytes, int32_t* dev_status, moe_stream_t stream);
 
 size_t moe_ffn_workspace_bytes(int T, int k, int I);

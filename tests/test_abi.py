@@ -52,7 +52,7 @@ def test_host_side_argument_errors(lib):
     # slab not a 16-byte multiple
     assert lib.moe_cache_gather(p, p, ctypes.c_size_t(24), 4, 2, p, p, p, 2, null, null) == -3
     # shapes the FFN does not take (H % 64 != 0)
-    assert lib.moe_expert_ffn(p, 4, 100, 128, 2, 16, p, p, p, p, 4, p, null, null, p, p,
+    assert lib.moe_expert_ffn(p, 4, 100, 128, 2, 16, p, p, p, p, 4, p, 16, null, null, p, p,
                               ctypes.c_size_t(1 << 20), null, null) == -1
 
 
