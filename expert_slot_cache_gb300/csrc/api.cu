@@ -106,7 +106,8 @@ extern "C" int moe_expert_ffn(const void* x, int T, int H, int I, int k, int E, 
                               void* workspace, size_t workspace_bytes, int32_t* dev_status, moe_stream_t stream) {
   if (!x || !offset || !rows || !list_e || !n_list || !pool || !y || !workspace) return MOE_ERR_ARG;
   if (!shape_ok(T, H, I, k, E) || max_list < 0 || S < 1 || (!e2s && S < E)) return MOE_ERR_ARG;
-  if ((uintptr_t)pool % 16 || (uintptr_t)y % 16 || (uintptr_t)workspace % 16) return MOE_ERR_ALIGN;
+  if ((uintptr_t)pool % 16 || (uintptr_t)y % 16 || (uintptr_t)workspace % 16 || (uintptr_t)x % 16)
+    return MOE_ERR_ALIGN;
   if (workspace_bytes < moe_ffn_workspace_bytes(T, k, I)) return MOE_ERR_ALIGN;
   if (host_slabs) {
     if ((uintptr_t)host_slabs % 16) return MOE_ERR_ALIGN;
@@ -154,7 +155,7 @@ extern "C" int moe_layer_forward(const moe_layer_args* a, moe_stream_t main_s, m
   }
   if (mode == MOE_MODE_ZERO_RETURN && (!a->out_res || !a->out_miss)) return MOE_ERR_ARG;
   if (mode == MOE_MODE_GATHER && S < E && S < k) return MOE_ERR_CAPACITY;
-  if ((uintptr_t)a->pool % 16 || (uintptr_t)a->workspace % 256) return MOE_ERR_ALIGN;
+  if ((uintptr_t)a->pool % 16 || (uintptr_t)a->workspace % 256 || (uintptr_t)a->x % 16) return MOE_ERR_ALIGN;
 
   const int C = chunk_tokens(T, k, S, E, mode, policy);
   LayerWs ws = carve(a->workspace, C * k, H, E, I);

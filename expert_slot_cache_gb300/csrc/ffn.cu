@@ -238,18 +238,30 @@ __device__ __forceinline__ void tma_consume_batch(const FfnArgs& a, int tile, in
   const int K = kDown ? I : H;
   // stage the batch's inputs (x rows, or h rows) as fp32 [RB][K]
   named_sync(1, kFfnThreads);
-  for (int idx = tid; idx < RB * K; idx += kFfnThreads) {
-    const int r = idx / K, kk = idx - r * K;
-    float v = 0.f;
+  // 8 inputs per thread per step: one 16-byte load of bf16 x, or two of fp32 h
+  const int K8 = K / 8;
+#pragma unroll
+  for (int r = 0; r < RB; ++r) {
+    float4* dst = reinterpret_cast<float4*>(in_s + r * K);
     if (r < nb) {
       if (kDown) {
-        v = a.hbuf[(size_t)(p0 + r) * I + kk];
+        const float4* src = reinterpret_cast<const float4*>(a.hbuf + (size_t)(p0 + r) * I);
+        for (int v = tid; v < K8; v += kFfnThreads) {
+          dst[2 * v] = src[2 * v];
+          dst[2 * v + 1] = src[2 * v + 1];
+        }
       } else {
         const int t = a.rows[p0 + r] / a.k;
-        v = bf16_to_f32(a.x[(size_t)t * H + kk]);
+        const uint4* src = reinterpret_cast<const uint4*>(a.x + (size_t)t * H);
+        for (int v = tid; v < K8; v += kFfnThreads) {
+          const uint4 u = src[v];
+          dst[2 * v] = make_float4(bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y));
+          dst[2 * v + 1] = make_float4(bf16_lo(u.z), bf16_hi(u.z), bf16_lo(u.w), bf16_hi(u.w));
+        }
       }
+    } else {
+      for (int v = tid; v < K8; v += kFfnThreads) dst[2 * v] = dst[2 * v + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    in_s[idx] = v;
   }
   named_sync(1, kFfnThreads);
   float acc[RB][8];

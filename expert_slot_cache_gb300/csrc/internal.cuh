@@ -24,19 +24,29 @@ struct FfnArgs {
 };
 
 // Records (start, end) event pairs around kernel launches when tracing is on.
+// Inside a stream capture the records become graph nodes (external records),
+// so a replayed graph still timestamps every launch.
 struct Prof {
   moe_prof* p = nullptr;
   int cur = -1;
+  static void record(void* ev, cudaStream_t s) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaStreamIsCapturing(s, &cs);
+    if (cs == cudaStreamCaptureStatusActive)
+      cudaEventRecordWithFlags((cudaEvent_t)ev, s, cudaEventRecordExternal);
+    else
+      cudaEventRecord((cudaEvent_t)ev, s);
+  }
   void begin(int tag, cudaStream_t s) {
     cur = -1;
     if (!p || !p->events || p->used + 2 > p->capacity) return;
     cur = p->used;
-    cudaEventRecord((cudaEvent_t)p->events[cur], s);
+    record(p->events[cur], s);
     if (p->tags) p->tags[cur / 2] = tag;
   }
   void end(cudaStream_t s) {
     if (cur < 0) return;
-    cudaEventRecord((cudaEvent_t)p->events[cur + 1], s);
+    record(p->events[cur + 1], s);
     p->used = cur + 2;
     cur = -1;
   }
