@@ -42,7 +42,7 @@ from harness import configs as C  # noqa: E402
 
 METRIC = "MoE-layer tokens/s at 1 GB300; decode HBM GB/s vs roofline; prefill TFLOP/s"
 UNIT = "tokens/s"
-PROF_NAMES = ("route", "permute", "manage", "gather", "ffn_gateup", "ffn_down", "combine")
+PROF_NAMES = ("route", "permute", "manage", "gather", "ffn_gateup", "ffn_down", "combine", "ffn_rows")
 
 
 def _peaks():

@@ -30,7 +30,7 @@ POLICY_LRU, POLICY_LFU, POLICY_STATIC = 0, 1, 2
 DEV_BAD_EXPERT, DEV_BAD_SLOT = 1, 2
 
 
-PROF_CLASSES = ("route", "permute", "manage", "gather", "ffn_gateup", "ffn_down", "combine")
+PROF_CLASSES = ("route", "permute", "manage", "gather", "ffn_gateup", "ffn_down", "combine", "ffn_rows")
 
 
 class Prof(ctypes.Structure):
@@ -65,7 +65,7 @@ _permute = _sig("moe_permute", [V, I32, I32, V, V, V, V, V, V, V, V])
 _manage = _sig("moe_cache_manage", [V, I32, I32, I32, I32, V, V, V, V, V, V, V, V, V, V, V, V])
 _gather = _sig("moe_cache_gather", [V, V, c_size_t, I32, I32, V, V, V, I32, V, V])
 _ffn = _sig("moe_expert_ffn", [V, I32, I32, I32, I32, I32, V, V, V, V, I32, V, I32, V, V, V, V, c_size_t, V, V])
-_ffn_ws = _sig("moe_ffn_workspace_bytes", [I32, I32, I32], c_size_t)
+_ffn_ws = _sig("moe_ffn_workspace_bytes", [I32, I32, I32, I32], c_size_t)
 _combine = _sig("moe_combine", [V, V, V, V, V, I32, I32, I32, I32, I32, V, V, V, V])
 _layer = _sig("moe_layer_forward", [POINTER(LayerArgs), V, V])
 _layer_ws = _sig("moe_layer_workspace_bytes", [I32, I32, I32, I32, I32, I32], c_size_t)
@@ -193,8 +193,8 @@ def cache_gather(host_slabs, pool, miss_e, miss_s, n_miss, max_miss, dev_status=
                 _p(dev_status), _s(stream)), "moe_cache_gather")
 
 
-def ffn_workspace_bytes(T: int, k: int, I: int) -> int:
-    return int(_ffn_ws(T, k, I))
+def ffn_workspace_bytes(T: int, H: int, k: int, I: int) -> int:
+    return int(_ffn_ws(T, H, k, I))
 
 
 def expert_ffn(x, k, I, E, offset, rows, list_e, n_list, max_list, pool, e2s=None, host_slabs=None,
@@ -203,7 +203,7 @@ def expert_ffn(x, k, I, E, offset, rows, list_e, n_list, max_list, pool, e2s=Non
     if y is None:
         y = torch.zeros(T * k, H, dtype=torch.float32, device=x.device)
     if workspace is None:
-        workspace = torch.empty(ffn_workspace_bytes(T, k, I), dtype=torch.uint8, device=x.device)
+        workspace = torch.empty(ffn_workspace_bytes(T, H, k, I), dtype=torch.uint8, device=x.device)
     _ck(_ffn(_p(x), T, H, I, k, E, _p(offset), _p(rows), _p(list_e), _p(n_list), max_list, _p(pool),
              pool.shape[0], _p(e2s),
              _p(host_slabs), _p(y), _p(workspace), workspace.numel(), _p(dev_status), _s(stream)),

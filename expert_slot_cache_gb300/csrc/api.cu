@@ -19,11 +19,13 @@ static size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 // Workspace layout of the layer forward, for chunks of up to n = C*k routing slots.
 struct LayerWs {
   int32_t *count, *offset, *rows, *pos, *act_e, *n_act, *miss_e, *miss_s, *n_miss, *hit_e, *n_hit;
-  float *hbuf, *y;
+  float *hbuf, *y, *logits;
+  uint16_t *xp, *hb;
   size_t bytes;
 };
 
-static LayerWs carve(void* base, int n, int H, int E, int I) {
+// n = routing slots per chunk, T = tokens of the whole step (router logits).
+static LayerWs carve(void* base, int n, int H, int E, int I, int T) {
   LayerWs w{};
   size_t off = 0;
   char* b = (char*)base;
@@ -46,6 +48,11 @@ static LayerWs carve(void* base, int n, int H, int E, int I) {
   w.n_hit = (int32_t*)take(4);
   w.hbuf = (float*)take(4 * (size_t)n * I);
   w.y = (float*)take(4 * (size_t)n * H);
+  w.logits = (float*)take(4 * (size_t)T * E);
+  if (prefill_extra_bytes(n, H, I) > 0) {
+    w.xp = (uint16_t*)take(2 * (size_t)n * H);
+    w.hb = (uint16_t*)take(2 * (size_t)n * I);
+  }
   w.bytes = off;
   return w;
 }
@@ -95,9 +102,12 @@ extern "C" const char* moe_status_str(int s) {
   }
 }
 
-extern "C" size_t moe_ffn_workspace_bytes(int T, int k, int I) {
-  if (T < 1 || k < 1 || I < 1) return 0;
-  return align256(4 * (size_t)T * k * I);
+extern "C" size_t moe_ffn_workspace_bytes(int T, int H, int k, int I) {
+  if (T < 1 || H < 1 || k < 1 || I < 1) return 0;
+  const size_t n = (size_t)T * k;
+  size_t b = align256(4 * n * I);
+  if (prefill_extra_bytes((int)n, H, I) > 0) b += align256(2 * n * H) + align256(2 * n * I);
+  return b;
 }
 
 extern "C" int moe_expert_ffn(const void* x, int T, int H, int I, int k, int E, const int32_t* offset,
@@ -108,7 +118,8 @@ extern "C" int moe_expert_ffn(const void* x, int T, int H, int I, int k, int E, 
   if (!shape_ok(T, H, I, k, E) || max_list < 0 || S < 1 || (!e2s && S < E)) return MOE_ERR_ARG;
   if ((uintptr_t)pool % 16 || (uintptr_t)y % 16 || (uintptr_t)workspace % 16 || (uintptr_t)x % 16)
     return MOE_ERR_ALIGN;
-  if (workspace_bytes < moe_ffn_workspace_bytes(T, k, I)) return MOE_ERR_ALIGN;
+  const size_t n = (size_t)T * k;
+  if (workspace_bytes < align256(4 * n * I)) return MOE_ERR_ALIGN;
   if (host_slabs) {
     if ((uintptr_t)host_slabs % 16) return MOE_ERR_ALIGN;
     const int acc = check_host_accessible(host_slabs);
@@ -116,7 +127,12 @@ extern "C" int moe_expert_ffn(const void* x, int T, int H, int I, int k, int E, 
   }
   FfnArgs a{(const uint16_t*)x, T, H, I, k, E, offset, rows, list_e, n_list, (const uint16_t*)pool, e2s,
             (const uint16_t*)host_slabs, (size_t)3 * H * I, (float*)workspace, y, dev_status, S,
-            host_slabs == nullptr};
+            host_slabs == nullptr, nullptr, nullptr};
+  if (prefill_extra_bytes((int)n, H, I) > 0 && workspace_bytes >= moe_ffn_workspace_bytes(T, H, k, I)) {
+    char* b = (char*)workspace + align256(4 * n * I);
+    a.xp = (uint16_t*)b;
+    a.hb = (uint16_t*)(b + align256(2 * n * H));
+  }
   return launch_ffn(a, std::min(max_list, E), (cudaStream_t)stream);
 }
 
@@ -133,7 +149,7 @@ extern "C" int moe_combine(const float* y, const float* w, const int32_t* pos, c
 extern "C" size_t moe_layer_workspace_bytes(int T, int H, int E, int k, int I, int S) {
   if (T < 1 || k < 1 || E < 1 || S < 1) return 0;
   // Worst case over modes: the largest chunk is all T tokens.
-  return carve(nullptr, T * k, H, E, I).bytes;
+  return carve(nullptr, T * k, H, E, I, T).bytes;
 }
 
 extern "C" int moe_layer_forward(const moe_layer_args* a, moe_stream_t main_s, moe_stream_t side_s) {
@@ -158,7 +174,7 @@ extern "C" int moe_layer_forward(const moe_layer_args* a, moe_stream_t main_s, m
   if ((uintptr_t)a->pool % 16 || (uintptr_t)a->workspace % 256 || (uintptr_t)a->x % 16) return MOE_ERR_ALIGN;
 
   const int C = chunk_tokens(T, k, S, E, mode, policy);
-  LayerWs ws = carve(a->workspace, C * k, H, E, I);
+  LayerWs ws = carve(a->workspace, C * k, H, E, I, T);
   if (a->workspace_bytes < ws.bytes) return MOE_ERR_ALIGN;
 
   cudaStream_t ms = (cudaStream_t)main_s;
@@ -175,7 +191,7 @@ extern "C" int moe_layer_forward(const moe_layer_args* a, moe_stream_t main_s, m
   if (prof.p) prof.p->used = 0;
   const size_t slab_bytes = (size_t)6 * H * I;
   prof.begin(MOE_PROF_ROUTE, ms);
-  int r = moe_route(a->x, a->w_router, a->logit_offset, a->sel_bias, T, H, E, k, nullptr, a->ids, a->w, main_s);
+  int r = moe_route(a->x, a->w_router, a->logit_offset, a->sel_bias, T, H, E, k, ws.logits, a->ids, a->w, main_s);
   if (r != MOE_OK) return r;
   prof.end(ms);
 
@@ -190,7 +206,7 @@ extern "C" int moe_layer_forward(const moe_layer_args* a, moe_stream_t main_s, m
     prof.end(ms);
     FfnArgs f{(const uint16_t*)a->x + (size_t)t0 * H, tc, H, I, k, E, ws.offset, ws.rows, nullptr, nullptr,
               (const uint16_t*)a->pool, a->e2s, (const uint16_t*)a->host_slabs, (size_t)3 * H * I, ws.hbuf, ws.y,
-              a->dev_status, S, 1};
+              a->dev_status, S, 1, ws.xp, ws.hb};
     if (mode == MOE_MODE_RESIDENT) {
       f.list_e = ws.act_e;
       f.n_list = ws.n_act;

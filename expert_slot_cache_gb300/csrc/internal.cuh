@@ -21,6 +21,8 @@ struct FfnArgs {
   int32_t* status;
   int S;                  // slots in pool (0 = unknown)
   int pool_only;          // every listed expert is in the pool (e2s[e] >= 0 or e2s == NULL)
+  uint16_t* xp;           // bf16 [T*k][H] grouped copy of x (tensor-core path), or NULL
+  uint16_t* hb;           // bf16 [T*k][I] h for the tensor-core path, or NULL
 };
 
 // Records (start, end) event pairs around kernel launches when tracing is on.
@@ -53,6 +55,9 @@ struct Prof {
 };
 
 int launch_ffn(const FfnArgs& a, int max_list, cudaStream_t stream, Prof* prof = nullptr);
+bool prefill_eligible(const FfnArgs& a, int n);
+size_t prefill_extra_bytes(int n, int H, int I);
+int launch_prefill(const FfnArgs& a, int n, int max_list, cudaStream_t stream, Prof* prof);
 int launch_combine(const float* y, const float* w, const int32_t* pos, const int32_t* ids, const int32_t* e2s, int T,
                    int k, int H, int E, int split, void* out, float* out_res, float* out_miss, cudaStream_t stream);
 int launch_manage(const int32_t* ids, int n, int E, int S, int policy, int32_t* e2s, int32_t* s2e, uint32_t* prio,

@@ -43,161 +43,154 @@ __global__ void __launch_bounds__(1024) bias_table_kernel(const float* __restric
 }
 
 // ---------------------------------------------------------------------------
-// Route kernel.  One CTA = TT tokens x all E experts, 256 threads.
-//
-// Logits: each output (t, e) is one fp32 chain acc = fma(x[t][h], Wr[h][e], acc)
-// over h = 0..H-1 in order (the order the oracle follows).  A thread owns up
-// to kMG chains.  When every chain of a thread has the same expert, one Wr
-// load feeds all of them.
-//
+// Logits kernel.  CTA = (8*CH tokens) x (32 experts), 256 threads: warp w owns
+// token lanes t = w + 8c (c < CH), lane = expert.  Each output (t, e) is one
+// fp32 chain acc = fma(x[t][h], Wr[h][e], acc) over h = 0..H-1 in order (the
+// order the oracle follows).  Wr[:, e0:e0+32] and the CTA's x rows stream
+// through a 4-stage cp.async ring of 128-row chunks in shared memory, so the
+// chains never wait on a global load.
+// ---------------------------------------------------------------------------
+constexpr int kRouteThreads = 256;
+constexpr int kEB = 32;        // experts per CTA
+constexpr int kHC = 128;       // rows of Wr per stage
+constexpr int kRStages = 4;
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, bool pred) {
+  const int n = pred ? 16 : 0;  // src-size 0 zero-fills
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(smem))),
+               "l"(gmem), "r"(n)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+template <int CH>
+__global__ void __launch_bounds__(kRouteThreads) logits_kernel(const uint16_t* __restrict__ x,
+                                                               const uint16_t* __restrict__ wr,
+                                                               const float* __restrict__ off, int T, int H, int E,
+                                                               float* __restrict__ logits) {
+  constexpr int TT = 8 * CH;
+  // stage s: W [kHC][kEB] bf16 (8 KB) | x [TT][kHC] bf16
+  constexpr int kWBytes = kHC * kEB * 2;
+  constexpr int kXBytes = TT * kHC * 2;
+  constexpr int kStage = kWBytes + kXBytes;
+  extern __shared__ __align__(16) unsigned char rsm[];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int t0 = blockIdx.x * TT, e0 = blockIdx.y * kEB;
+  const int nt = min(TT, T - t0);
+  const int nchunk = (H + kHC - 1) / kHC;
+
+  auto load_chunk = [&](int c, int st) {
+    unsigned char* sw = rsm + st * kStage;
+    unsigned char* sx = sw + kWBytes;
+    const int h0 = c * kHC;
+    // W: kHC rows x 64 bytes = 4 x 16 B per row
+    for (int v = tid; v < kHC * 4; v += kRouteThreads) {
+      const int r = v >> 2, q = v & 3;
+      const bool ok = h0 + r < H && e0 + 8 * q < E;
+      const uint16_t* src = ok ? wr + (size_t)(h0 + r) * E + e0 + 8 * q : wr;
+      cp_async16(sw + r * 64 + q * 16, src, ok);
+    }
+    // x: TT rows x kHC bf16 = TT x 16 x 16 B
+    for (int v = tid; v < TT * (kHC / 8); v += kRouteThreads) {
+      const int r = v / (kHC / 8), q = v % (kHC / 8);
+      const bool ok = r < nt && h0 + 8 * q < H;
+      const uint16_t* src = ok ? x + (size_t)(t0 + r) * H + h0 + 8 * q : x;
+      cp_async16(sx + (r * kHC + 8 * q) * 2, src, ok);
+    }
+  };
+
+  float acc[CH];
+#pragma unroll
+  for (int c = 0; c < CH; ++c) acc[c] = 0.f;
+#pragma unroll
+  for (int c = 0; c < kRStages - 1; ++c) {
+    if (c < nchunk) load_chunk(c, c);
+    cp_async_commit();
+  }
+  for (int c = 0; c < nchunk; ++c) {
+    cp_async_wait<kRStages - 2>();
+    __syncthreads();
+    // refill the stage freed by chunk c-1
+    if (c + kRStages - 1 < nchunk) load_chunk(c + kRStages - 1, (c + kRStages - 1) % kRStages);
+    cp_async_commit();
+    const unsigned char* sw = rsm + (c % kRStages) * kStage;
+    const uint16_t* ws = reinterpret_cast<const uint16_t*>(sw);
+    const uint16_t* xs = reinterpret_cast<const uint16_t*>(sw + kWBytes);
+    const int hn = min(kHC, H - c * kHC);
+    for (int h = 0; h < hn; ++h) {
+      const float wv = bf16_to_f32(ws[h * kEB + lane]);
+#pragma unroll
+      for (int cc = 0; cc < CH; ++cc) acc[cc] = fmaf(bf16_to_f32(xs[(warp + 8 * cc) * kHC + h]), wv, acc[cc]);
+    }
+  }
+  cp_async_wait<0>();
+  const int e = e0 + lane;
+  if (e < E) {
+#pragma unroll
+    for (int cc = 0; cc < CH; ++cc) {
+      const int t = warp + 8 * cc;
+      if (t < nt) logits[(size_t)(t0 + t) * E + e] = off ? acc[cc] + off[e] : acc[cc];
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Top-k: one warp per token.  k rounds of a warp-wide argmax over
 // score = logit + bias (ties -> lower id); the winner is marked taken.
+// Weights: softmax over the k picked, from the unbiased logits.
 // ---------------------------------------------------------------------------
-constexpr int kMG = 8;
-constexpr int kRouteThreads = 256;
-
-inline int route_tt(int E) {
-  const int tt = (kRouteThreads * kMG) / E;
-  int p = 1;
-  while (p * 2 <= tt) p *= 2;
-  return p;
-}
-
-template <bool kSameE>
-__device__ __forceinline__ void route_logits(const uint16_t* __restrict__ xs, const uint16_t* __restrict__ wr,
-                                             const float* __restrict__ off, int TT, int nt, int H, int E,
-                                             float* __restrict__ ls) {
-  constexpr int kPF = 8;  // router rows loaded ahead of the fma chains
-  const int tid = threadIdx.x;
-  int tm[kMG], em[kMG];
-  bool vm[kMG];
-#pragma unroll
-  for (int m = 0; m < kMG; ++m) {
-    const int o = tid + kRouteThreads * m;
-    tm[m] = o / E;
-    em[m] = o - tm[m] * E;
-    vm[m] = (o < TT * E) && (tm[m] < nt);
-    if (!vm[m]) {  // keep idle chains in bounds; their results are discarded
-      tm[m] = 0;
-      em[m] = 0;
-    }
-  }
-  float acc[kMG];
-#pragma unroll
-  for (int m = 0; m < kMG; ++m) acc[m] = 0.f;
-
-  bool any = false;
-#pragma unroll
-  for (int m = 0; m < kMG; ++m) any |= vm[m];
-  if (!any) return;
-  const int Hm = H - H % kPF;
-  for (int h0 = 0; h0 < Hm; h0 += kPF) {
-    if (kSameE) {
-      // every chain of this thread has expert em[0]: one router load per h
-      float wv[kPF];
-#pragma unroll
-      for (int u = 0; u < kPF; ++u) wv[u] = bf16_to_f32(__ldg(wr + (size_t)(h0 + u) * E + em[0]));
-#pragma unroll
-      for (int u = 0; u < kPF; ++u)
-#pragma unroll
-        for (int m = 0; m < kMG; ++m) acc[m] = fmaf(bf16_to_f32(xs[tm[m] * H + h0 + u]), wv[u], acc[m]);
-    } else {
-      float wv[kPF][kMG];
-#pragma unroll
-      for (int u = 0; u < kPF; ++u)
-#pragma unroll
-        for (int m = 0; m < kMG; ++m)
-          wv[u][m] = vm[m] ? bf16_to_f32(__ldg(wr + (size_t)(h0 + u) * E + em[m])) : 0.f;
-#pragma unroll
-      for (int u = 0; u < kPF; ++u)
-#pragma unroll
-        for (int m = 0; m < kMG; ++m) acc[m] = fmaf(bf16_to_f32(xs[tm[m] * H + h0 + u]), wv[u][m], acc[m]);
-    }
-  }
-  for (int h = Hm; h < H; ++h) {
-#pragma unroll
-    for (int m = 0; m < kMG; ++m)
-      acc[m] = fmaf(bf16_to_f32(xs[tm[m] * H + h]), bf16_to_f32(__ldg(wr + (size_t)h * E + em[m])), acc[m]);
-  }
-#pragma unroll
-  for (int m = 0; m < kMG; ++m) {
-    if (vm[m]) ls[tm[m] * E + em[m]] = off ? acc[m] + off[em[m]] : acc[m];
-  }
-}
-
-__global__ void __launch_bounds__(kRouteThreads) route_kernel(const uint16_t* __restrict__ x,
-                                                              const uint16_t* __restrict__ wr,
-                                                              const float* __restrict__ off,
-                                                              const float* __restrict__ bias, int T, int H,
-                                                              int E, int k, int TT, int same_e,
-                                                              float* __restrict__ logits,
-                                                              int32_t* __restrict__ ids, float* __restrict__ wout) {
-  extern __shared__ __align__(16) unsigned char route_smem[];
-  uint16_t* xs = reinterpret_cast<uint16_t*>(route_smem);                 // [TT][H] bf16
-  float* ls = reinterpret_cast<float*>(route_smem + (size_t)TT * H * 2);  // [TT][E]
+__global__ void __launch_bounds__(kRouteThreads) topk_kernel(const float* __restrict__ logits,
+                                                             const float* __restrict__ bias, int T, int E, int k,
+                                                             int32_t* __restrict__ ids, float* __restrict__ wout) {
   __shared__ float sel_l[kRouteThreads / 32][kMaxK];
   __shared__ int sel_i[kRouteThreads / 32][kMaxK];
-
-  const int t0 = blockIdx.x * TT;
-  const int nt = min(TT, T - t0);
-  for (int i = threadIdx.x; i < nt * H; i += blockDim.x) xs[i] = x[(size_t)t0 * H + i];
-  for (int i = nt * H + threadIdx.x; i < TT * H; i += blockDim.x) xs[i] = 0;
-  __syncthreads();
-
-  if (same_e)
-    route_logits<true>(xs, wr, off, TT, nt, H, E, ls);
-  else
-    route_logits<false>(xs, wr, off, TT, nt, H, E, ls);
-  __syncthreads();
-
-  if (logits) {
-    for (int i = threadIdx.x; i < nt * E; i += blockDim.x) logits[(size_t)t0 * E + i] = ls[i];
-  }
-
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  for (int t = warp; t < nt; t += kRouteThreads / 32) {
-    const float* lrow = ls + t * E;
-    unsigned taken = 0;
-    for (int j = 0; j < k; ++j) {
-      float best = -INFINITY;
-      int bi = INT_MAX;
-      for (int q = 0; lane + 32 * q < E; ++q) {
-        if ((taken >> q) & 1u) continue;
-        const int e = lane + 32 * q;
-        const float s = bias ? lrow[e] + bias[e] : lrow[e];
-        if (bi == INT_MAX || s > best || (s == best && e < bi)) {
-          best = s;
-          bi = e;
-        }
+  const int t = blockIdx.x * (kRouteThreads / 32) + warp;
+  if (t >= T) return;
+  const float* lrow = logits + (size_t)t * E;
+  unsigned taken = 0;
+  for (int j = 0; j < k; ++j) {
+    float best = -INFINITY;
+    int bi = INT_MAX;
+    for (int q = 0; lane + 32 * q < E; ++q) {
+      if ((taken >> q) & 1u) continue;
+      const int e = lane + 32 * q;
+      const float s = bias ? lrow[e] + bias[e] : lrow[e];
+      if (bi == INT_MAX || s > best || (s == best && e < bi)) {
+        best = s;
+        bi = e;
       }
+    }
 #pragma unroll
-      for (int d = 16; d; d >>= 1) {
-        const float ob = __shfl_xor_sync(MOE_FULL_MASK, best, d);
-        const int oi = __shfl_xor_sync(MOE_FULL_MASK, bi, d);
-        if (oi != INT_MAX && (bi == INT_MAX || ob > best || (ob == best && oi < bi))) {
-          best = ob;
-          bi = oi;
-        }
-      }
-      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-      if (lane == 0) {
-        sel_i[warp][j] = bi;
-        sel_l[warp][j] = lrow[bi];
+    for (int d = 16; d; d >>= 1) {
+      const float ob = __shfl_xor_sync(MOE_FULL_MASK, best, d);
+      const int oi = __shfl_xor_sync(MOE_FULL_MASK, bi, d);
+      if (oi != INT_MAX && (bi == INT_MAX || ob > best || (ob == best && oi < bi))) {
+        best = ob;
+        bi = oi;
       }
     }
-    __syncwarp();
+    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
     if (lane == 0) {
-      float mx = sel_l[warp][0];
-      for (int j = 1; j < k; ++j) mx = fmaxf(mx, sel_l[warp][j]);
-      float sum = 0.f;
-      for (int j = 0; j < k; ++j) sum += expf(sel_l[warp][j] - mx);
-      const size_t base = (size_t)(t0 + t) * k;
-      for (int j = 0; j < k; ++j) {
-        ids[base + j] = sel_i[warp][j];
-        wout[base + j] = expf(sel_l[warp][j] - mx) / sum;
-      }
+      sel_i[warp][j] = bi;
+      sel_l[warp][j] = lrow[bi];
     }
-    __syncwarp();
+  }
+  __syncwarp();
+  if (lane == 0) {
+    float mx = sel_l[warp][0];
+    for (int j = 1; j < k; ++j) mx = fmaxf(mx, sel_l[warp][j]);
+    float sum = 0.f;
+    for (int j = 0; j < k; ++j) sum += expf(sel_l[warp][j] - mx);
+    const size_t base = (size_t)t * k;
+    for (int j = 0; j < k; ++j) {
+      ids[base + j] = sel_i[warp][j];
+      wout[base + j] = expf(sel_l[warp][j] - mx) / sum;
+    }
   }
 }
 
@@ -215,25 +208,42 @@ extern "C" int moe_bias_table(const float* b, int E, int n_hot, float cap, float
 
 extern "C" int moe_route(const void* x, const void* w_router, const float* logit_offset, const float* sel_bias,
                          int T, int H, int E, int k, float* logits, int32_t* ids, float* w, moe_stream_t stream) {
-  if (!x || !w_router || !ids || !w) return MOE_ERR_ARG;
-  if (T < 1 || H < 1 || E < 1 || E > kMaxE || k < 1 || k > kMaxK || k > E) return MOE_ERR_ARG;
-  constexpr int kSmemCap = 160 * 1024;
+  if (!x || !w_router || !ids || !w || !logits) return MOE_ERR_ARG;
+  if (T < 1 || H < 8 || H % 8 || E < 1 || E > kMaxE || E % 8 || k < 1 || k > kMaxK || k > E) return MOE_ERR_ARG;
+  if ((uintptr_t)x % 16 || (uintptr_t)w_router % 16) return MOE_ERR_ALIGN;
   int sms = 0, dev = 0;
   MOE_CUDA_TRY(cudaGetDevice(&dev));
   MOE_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-  // Enough CTAs to cover the SMs first, then up to kMG chains per thread.
-  int TT = route_tt(E);
-  while (TT > 1 && (T + TT - 1) / TT < sms) TT /= 2;
-  auto smem_of = [&](int tt) { return (size_t)tt * H * 2 + (size_t)tt * E * 4; };
-  while (TT > 1 && smem_of(TT) > (size_t)kSmemCap) TT /= 2;
-  if (smem_of(TT) > (size_t)kSmemCap) return MOE_ERR_ARG;
-  const int same_e = (kRouteThreads % E == 0) && (TT * E == kRouteThreads * kMG);
-  static bool attr_done[64] = {};
-  MOE_CUDA_TRY(ensure_smem(route_kernel, kSmemCap, attr_done));
-  const int grid = (T + TT - 1) / TT;
-  route_kernel<<<grid, kRouteThreads, smem_of(TT), (cudaStream_t)stream>>>(
-      (const uint16_t*)x, (const uint16_t*)w_router, logit_offset, sel_bias, T, H, E, k, TT, same_e, logits, ids,
-      w);
+  cudaStream_t s = (cudaStream_t)stream;
+  const int eb = (E + kEB - 1) / kEB;
+  // tokens per CTA: fewest that still give every SM a CTA, at most 64
+  int ch = 8;
+  while (ch > 1 && ((T + 8 * ch - 1) / (8 * ch)) * eb < sms) ch /= 2;
+  const dim3 grid((T + 8 * ch - 1) / (8 * ch), eb);
+  const size_t smem = (size_t)kRStages * (kHC * kEB * 2 + 8 * ch * kHC * 2);
+  static bool d1[64] = {}, d2[64] = {}, d4[64] = {}, d8[64] = {};
+  const uint16_t* xb = (const uint16_t*)x;
+  const uint16_t* wb = (const uint16_t*)w_router;
+  switch (ch) {
+    case 1:
+      MOE_CUDA_TRY(ensure_smem(logits_kernel<1>, (int)smem, d1));
+      logits_kernel<1><<<grid, kRouteThreads, smem, s>>>(xb, wb, logit_offset, T, H, E, logits);
+      break;
+    case 2:
+      MOE_CUDA_TRY(ensure_smem(logits_kernel<2>, (int)smem, d2));
+      logits_kernel<2><<<grid, kRouteThreads, smem, s>>>(xb, wb, logit_offset, T, H, E, logits);
+      break;
+    case 4:
+      MOE_CUDA_TRY(ensure_smem(logits_kernel<4>, (int)smem, d4));
+      logits_kernel<4><<<grid, kRouteThreads, smem, s>>>(xb, wb, logit_offset, T, H, E, logits);
+      break;
+    default:
+      MOE_CUDA_TRY(ensure_smem(logits_kernel<8>, (int)smem, d8));
+      logits_kernel<8><<<grid, kRouteThreads, smem, s>>>(xb, wb, logit_offset, T, H, E, logits);
+      break;
+  }
+  MOE_LAUNCH_CHECK();
+  topk_kernel<<<(T + 7) / 8, kRouteThreads, 0, s>>>(logits, sel_bias, T, E, k, ids, w);
   MOE_LAUNCH_CHECK();
   return MOE_OK;
 }

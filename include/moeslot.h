@@ -85,12 +85,14 @@ int moe_bias_table(const float* b, int E, int n_hot, float cap, float* bias, moe
  *   w_router     device bf16 [H][E]
  *   logit_offset device fp32 [E] added to every logit after the sum, or NULL
  *   sel_bias     device fp32 [E] selection-only bias, or NULL
- *   logits       device fp32 [T][E] output (unbiased logits), or NULL
+ *   logits       device fp32 [T][E] output (unbiased logits; also the scratch
+ *                between the logits kernel and the top-k kernel)
  *   ids          device int32 [T][k] output, descending score, ties -> lower id
  *   w            device fp32 [T][k] output, sums to 1 per token
  * logit[t][e] is accumulated in fp32 in h order (acc = fma(x, Wr, acc) for
  * h = 0..H-1), so ids are reproducible bit for bit.
- * Errors: MOE_ERR_ARG on NULL required pointers or shapes out of range.
+ * Errors: MOE_ERR_ARG on NULL pointers or shapes out of range (H % 8 and
+ * E % 8 must be 0); MOE_ERR_ALIGN if x or w_router is not 16-byte aligned.
  */
 int moe_route(const void* x, const void* w_router, const float* logit_offset, const float* sel_bias,
               int T, int H, int E, int k, float* logits, int32_t* ids, float* w, moe_stream_t stream);
@@ -187,7 +189,11 @@ int moe_cache_gather(const void* host_slabs, void* pool, size_t slab_bytes, int 
  *   list_e     device int32 [>= *n_list], n_list device int32 [1]
  *   max_list   host upper bound on *n_list
  *   y          device fp32 [T*k][H]; only rows of listed experts are written
- *   workspace  device scratch of moe_ffn_workspace_bytes(T, k, I) bytes (holds h)
+ *   workspace  device scratch of moe_ffn_workspace_bytes(T, H, k, I) bytes (holds h)
+ * Large groups (T*k >= 4096, weights in the pool) run as two tcgen05 grouped
+ * GEMMs (M = 128 rows x N = 256 columns, fp32 accumulation in TMEM, bf16 h)
+ * when the workspace holds the extra buffers; smaller ones stream the weight
+ * tiles once per batch of <= 8 rows.
  * Errors: MOE_ERR_ARG on NULL pointers or bad shapes, MOE_ERR_ALIGN on
  * unaligned weight/output pointers or a workspace that is too small.
  */
@@ -196,7 +202,9 @@ int moe_expert_ffn(const void* x, int T, int H, int I, int k, int E, const int32
                    const void* pool, int S, const int32_t* e2s, const void* host_slabs, float* y,
                    void* workspace, size_t workspace_bytes, int32_t* dev_status, moe_stream_t stream);
 
-size_t moe_ffn_workspace_bytes(int T, int k, int I);
+/* Workspace of moe_expert_ffn: fp32 h [T*k][I]; for T*k >= 4096 also the
+ * bf16 grouped rows of x [T*k][H] and bf16 h [T*k][I] of the tensor-core path. */
+size_t moe_ffn_workspace_bytes(int T, int H, int k, int I);
 
 /*
  * The grouped expert FFN for callers that cannot allocate device memory.
@@ -260,7 +268,8 @@ enum {
   MOE_PROF_FFN_GATEUP = 4,
   MOE_PROF_FFN_DOWN = 5,
   MOE_PROF_COMBINE = 6,
-  MOE_PROF_CLASSES = 7
+  MOE_PROF_FFN_ROWS = 7, /* grouped copy of the routed rows of x (tensor-core path) */
+  MOE_PROF_CLASSES = 8
 };
 typedef struct moe_prof {
   void** events;    /* cudaEvent_t[capacity] */

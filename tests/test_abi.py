@@ -44,7 +44,9 @@ def test_host_side_argument_errors(lib):
     # NULL inputs
     assert lib.moe_route(null, null, null, null, 4, 256, 16, 2, null, null, null, null) == -1
     # k > E
-    assert lib.moe_route(p, p, null, null, 4, 256, 4, 8, null, p, p, null) == -1
+    assert lib.moe_route(p, p, null, null, 4, 256, 8, 9, p, p, p, null) == -1
+    # logits buffer is required
+    assert lib.moe_route(p, p, null, null, 4, 256, 16, 2, null, p, p, null) == -1
     # a step larger than the pool when the policy can evict
     assert lib.moe_cache_manage(p, 65, 128, 64, 0, p, p, p, p, p, p, p, null, null, null, null, null) == -2
     # bad policy
@@ -62,4 +64,6 @@ def test_workspace_sizes(lib):
     ws = lib.moe_layer_workspace_bytes(64, 2048, 128, 8, 768, 64)
     # h (n*I fp32) and y (n*H fp32) dominate
     assert ws >= 4 * 512 * (768 + 2048)
-    assert lib.moe_ffn_workspace_bytes(64, 8, 768) == 4 * 512 * 768
+    assert lib.moe_ffn_workspace_bytes(64, 2048, 8, 768) == 4 * 512 * 768
+    # the tensor-core path adds bf16 grouped x and bf16 h
+    assert lib.moe_ffn_workspace_bytes(4096, 2048, 8, 768) == 4 * 32768 * 768 + 2 * 32768 * (2048 + 768)

@@ -365,3 +365,36 @@ def test_layer_prefill_sampled_tokens():
     # groups are uneven under the logit offset
     counts = np.bincount(_np(res["ids"]).ravel(), minlength=cfg.E)
     assert counts.max() > 2 * counts.mean()
+
+
+# bf16 h in the tensor-core path: rounding h to bf16 (relative 2^-9, random
+# sign) gives y a relative L2 error of about 2^-9 / sqrt(3) ~ 1.1e-3.
+RL2_Y_BF16_H = 5e-3
+
+
+@pytest.mark.parametrize("T,skew", [(512, 1.2), (520, 0.0)], ids=["T512_skewed", "T520_uniform_ragged"])
+def test_expert_ffn_tensor_core_parity(T, skew):
+    """Groups large enough for the tcgen05 grouped GEMMs (T*k >= 4096)."""
+    cfg = C.qwen(T, S=128, mode=C.MODE_RESIDENT)
+    E = cfg.E
+    rng = np.random.default_rng(T)
+    p = np.arange(1, E + 1, dtype=np.float64) ** -skew
+    p /= p.sum()
+    ids = np.stack([rng.choice(E, cfg.k, replace=False, p=p) for _ in range(T)]).astype(np.int32)
+    count, offset, rows, pos = O.permute(ids, E)
+    x = C.draw_x(cfg, DEV, T=T)
+    st = stage_layer(cfg)
+    used = np.nonzero(count)[0]
+    lst = torch.from_numpy(used.astype(np.int32)).to(DEV)
+    g = M.permute(torch.from_numpy(ids).to(DEV), E)
+    y = M.expert_ffn(x, cfg.k, cfg.I, E, g.offset, g.rows, lst, torch.tensor([len(used)], dtype=torch.int32,
+                     device=DEV), len(used), st["slabs_dev"])
+    torch.cuda.synchronize()
+    want = O.expert_ffn(_np(x.float()), rows, offset, cfg.k, HostSlabs(st["host"]), cfg.H, cfg.I)
+    got = _np(y)
+    from tests._setup import rel_l2
+    assert rel_l2(got, want) <= RL2_Y_BF16_H
+    # every group, including ragged last tiles and single-row groups, is right
+    for e in used:
+        a, b = offset[e], offset[e + 1]
+        assert rel_l2(got[a:b], want[a:b]) <= 2 * RL2_Y_BF16_H, f"expert {e} ({b - a} rows)"
