@@ -210,7 +210,8 @@ def time_steps(wl: Workload, steps: int, warmup: int, dist=None, clocks=None, pr
     M = wl.M
     for i in range(warmup):
         wl.step(i)
-    pairs = 2 + wl.cfg.T * 16
+    n_chunks = (wl.cfg.T + wl.chunk() - 1) // wl.chunk()
+    pairs = 4 + 12 * n_chunks
     profs = [_make_prof(M, pairs) for _ in range(steps)] if profile else [None] * steps
     torch.cuda.synchronize()
     g = None
@@ -442,6 +443,22 @@ def main():
                                          "layer_hbm_frac": u2 * c2.slab_bytes / (r2["ms"] * 1e-3) / 1e9
                                          / peaks["hbm_gbs"]}
             del w2
+        # prefill: all experts resident, T=4096, skewed groups (tcgen05 grouped GEMMs)
+        cp = C.PREFILL
+        wp = Workload(cp, 3 + 3, dev)
+        rp = time_steps(wp, 3, 3)
+        flops = 6.0 * cp.T * cp.k * cp.H * cp.I
+        t_ffn = (rp["kern_ms"]["ffn_gateup"] + rp["kern_ms"]["ffn_down"]) * 1e-3 / 3
+        t_layer = rp["ms"] * 1e-3 / 3
+        pk = peaks["bf16_tflops"]
+        var["prefill_T4096"] = {"tokens_per_s": cp.T / t_layer, "ms_per_step": rp["ms"] / 3,
+                                "kernels_ms_per_step": {n: v / 3 for n, v in rp["kern_ms"].items()},
+                                "ffn_tensor": {"bound": "tensor", "achieved": flops / t_ffn / 1e12, "peak": pk,
+                                               "unit": "TFLOP/s", "frac": flops / t_ffn / 1e12 / pk,
+                                               "flops_per_step": flops, "kernel": "ffn_gateup+ffn_down (tcgen05)"},
+                                "layer_tflops": flops / t_layer / 1e12}
+        del wp
+        torch.cuda.empty_cache()
         for T in (1, 8, 32):
             c3 = C.qwen(T, S=64)
             w3 = Workload(c3, 10 + 3, dev)

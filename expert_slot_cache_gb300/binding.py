@@ -114,7 +114,7 @@ def route(x, w_router, k, logit_offset=None, sel_bias=None, return_logits=False,
     E = w_router.shape[1]
     ids = torch.empty(T, k, dtype=torch.int32, device=x.device)
     w = torch.empty(T, k, dtype=torch.float32, device=x.device)
-    logits = torch.empty(T, E, dtype=torch.float32, device=x.device) if return_logits else None
+    logits = torch.empty(T, E, dtype=torch.float32, device=x.device)
     _ck(_route(_p(x), _p(w_router), _p(logit_offset), _p(sel_bias), T, H, E, k, _p(logits), _p(ids), _p(w),
                _s(stream)), "moe_route")
     return (ids, w, logits) if return_logits else (ids, w)
