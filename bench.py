@@ -386,6 +386,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-variants", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default="main",
+                    help="main (default) | prefill | resident_T<n> | gather_T<n>: one workload alone "
+                         "(for profiling); prints its own JSON line")
     args = ap.parse_args()
     ws, rank, local, dist = _dist()
     if args.impl == "reference":
@@ -397,6 +400,23 @@ def main():
     torch.cuda.set_device(local)
     dev = f"cuda:{local}"
     peaks = _peaks()
+    if args.workload != "main":
+        w = args.workload
+        if w == "prefill":
+            c = C.PREFILL
+        elif w.startswith("resident_T"):
+            c = C.qwen(int(w[len("resident_T"):]), S=128, mode=C.MODE_RESIDENT)
+        elif w.startswith("gather_T"):
+            c = C.qwen(int(w[len("gather_T"):]), S=64)
+        else:
+            raise SystemExit(f"unknown workload {w}")
+        wl = Workload(c, args.steps + args.warmup, dev)
+        r = time_steps(wl, args.steps, args.warmup)
+        if rank == 0:
+            print(json.dumps({"workload": w, "ms_per_step": r["ms"] / args.steps,
+                              "tokens_per_s": c.T * args.steps / (r["ms"] * 1e-3),
+                              "kernels_ms_per_step": {n: v / args.steps for n, v in r["kern_ms"].items()}}))
+        return
     cfg = main_config()
     K, W = args.steps, args.warmup
 
@@ -439,6 +459,7 @@ def main():
             r2 = time_steps(w2, 10, 3)
             u2 = count_unique_all(w2, 10, 3)
             var[f"all_resident_T{T}"] = {"tokens_per_s": T * 10 / (r2["ms"] * 1e-3), "ms_per_step": r2["ms"] / 10,
+                                         "kernels_ms_per_step": {n: v / 10 for n, v in r2["kern_ms"].items()},
                                          "ffn_hbm": ffn_roofline(w2, r2, u2, peaks),
                                          "layer_hbm_frac": u2 * c2.slab_bytes / (r2["ms"] * 1e-3) / 1e9
                                          / peaks["hbm_gbs"]}

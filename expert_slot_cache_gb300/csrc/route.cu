@@ -120,11 +120,24 @@ __global__ void __launch_bounds__(kRouteThreads) logits_kernel(const uint16_t* _
     const unsigned char* sw = rsm + (c % kRStages) * kStage;
     const uint16_t* ws = reinterpret_cast<const uint16_t*>(sw);
     const uint16_t* xs = reinterpret_cast<const uint16_t*>(sw + kWBytes);
-    const int hn = min(kHC, H - c * kHC);
-    for (int h = 0; h < hn; ++h) {
-      const float wv = bf16_to_f32(ws[h * kEB + lane]);
+    const int hn = min(kHC, H - c * kHC);  // a multiple of 8
+    for (int h0 = 0; h0 < hn; h0 += 8) {
+      // operands of 8 consecutive h first, then the 8 fma steps of each chain
+      float wv[8];
 #pragma unroll
-      for (int cc = 0; cc < CH; ++cc) acc[cc] = fmaf(bf16_to_f32(xs[(warp + 8 * cc) * kHC + h]), wv, acc[cc]);
+      for (int u = 0; u < 8; ++u) wv[u] = bf16_to_f32(ws[(h0 + u) * kEB + lane]);
+#pragma unroll
+      for (int cc = 0; cc < CH; ++cc) {
+        const uint4 xv = *reinterpret_cast<const uint4*>(xs + (warp + 8 * cc) * kHC + h0);
+        acc[cc] = fmaf(bf16_lo(xv.x), wv[0], acc[cc]);
+        acc[cc] = fmaf(bf16_hi(xv.x), wv[1], acc[cc]);
+        acc[cc] = fmaf(bf16_lo(xv.y), wv[2], acc[cc]);
+        acc[cc] = fmaf(bf16_hi(xv.y), wv[3], acc[cc]);
+        acc[cc] = fmaf(bf16_lo(xv.z), wv[4], acc[cc]);
+        acc[cc] = fmaf(bf16_hi(xv.z), wv[5], acc[cc]);
+        acc[cc] = fmaf(bf16_lo(xv.w), wv[6], acc[cc]);
+        acc[cc] = fmaf(bf16_hi(xv.w), wv[7], acc[cc]);
+      }
     }
   }
   cp_async_wait<0>();
