@@ -25,6 +25,7 @@ import subprocess
 import sys
 import tempfile
 import time
+from typing import Optional
 
 if "--impl" in sys.argv and "reference" in sys.argv:
     # the oracle leg: pin the BLAS pools before numpy loads, so "cores" is exact
@@ -180,6 +181,42 @@ class Workload:
     def unique_per_chunk(self, ids: np.ndarray) -> int:
         C_ = self.chunk()
         return sum(len(np.unique(ids[t0:t0 + C_])) for t0 in range(0, ids.shape[0], C_))
+
+
+class StackWorkload:
+    """The 48-layer stack: per-layer router, experts, pool and cache state."""
+
+    def __init__(self, cfg: C.LayerConfig, dev: str, layers: Optional[int] = None, steps: int = 0):
+        import expert_slot_cache_gb300 as M
+        self.cfg, self.dev, self.M = cfg, dev, M
+        L = cfg.layers if layers is None else layers
+        self.L = L
+        self.hosts, self.layers = [], []
+        for l in range(L):
+            wr = C.draw_router(cfg, dev, l)
+            slabs = torch.empty(cfg.E, cfg.slab_elems, dtype=torch.bfloat16, device=dev)
+            C.draw_slabs(cfg, dev, l, out=slabs)
+            if cfg.mode == C.MODE_RESIDENT:
+                host, pool, state = None, slabs, None
+            else:
+                host = torch.empty(cfg.E, cfg.slab_elems, dtype=torch.bfloat16, pin_memory=True)
+                host.copy_(slabs)
+                s2e0 = C.initial_residency(cfg, l)
+                pool = slabs[torch.from_numpy(s2e0.astype(np.int64)).to(dev)].contiguous()
+                del slabs
+                state = M.CacheState.from_slots(s2e0, cfg.E, dev)
+            self.hosts.append(host)
+            self.layers.append(M.SlotCachedMoELayer(wr, pool, cfg.k, cfg.I, cfg.mode, cfg.policy, host_slabs=host,
+                                                    state=state, max_tokens=cfg.T))
+        self.stack = M.LayerStack(self.layers, cfg.T)
+        # inputs of every step and layer, drawn up front: [steps][L][T][H]
+        self.inputs = torch.empty(max(steps, 1), L, cfg.T, cfg.H, dtype=torch.bfloat16, device=dev)
+        for st in range(steps):
+            for l in range(L):
+                self.inputs[st, l].copy_(C.draw_x(cfg, dev, layer=l, step=st))
+
+    def load_step(self, st: int):
+        self.stack.x_all.copy_(self.inputs[st])
 
 
 def _make_prof(M, pairs: int):

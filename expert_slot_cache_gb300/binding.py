@@ -281,3 +281,45 @@ class SlotCachedMoELayer:
         if self.mode == MODE_ZERO_RETURN:
             res["out_res"], res["out_miss"] = out_res, out_miss
         return res
+
+
+class LayerStack:
+    """Several layers' forwards replayed as one CUDA graph.
+
+    "Betelgeuse ... on an RTX 3060", "What it actually does under the hood":
+    with hits resolved on the device and no host sync inside a layer, a whole
+    decode pass over all layers replays as a single CUDA graph.  Each layer
+    reads its own input buffer ``xs[l]`` and writes ``outs[l]``; the caller
+    refreshes the inputs between replays.  Cache state and slot pools evolve
+    on the device across replays.
+    """
+
+    def __init__(self, layers, T: int):
+        self.layers = layers
+        dev = layers[0].pool.device
+        H = layers[0].H
+        # one contiguous [L][T][H] input block, so a step's inputs arrive in one copy
+        self.x_all = torch.zeros(len(layers), T, H, dtype=torch.bfloat16, device=dev)
+        self.xs = list(self.x_all.unbind(0))
+        self.out_all = torch.empty(len(layers), T, H, dtype=torch.bfloat16, device=dev)
+        self.outs = list(self.out_all.unbind(0))
+        self.ids = [torch.empty(T, l.k, dtype=torch.int32, device=dev) for l in layers]
+        self.ws = [torch.empty(T, l.k, dtype=torch.float32, device=dev) for l in layers]
+        self.graph = None
+
+    def _run(self, prof=None):
+        for i, l in enumerate(self.layers):
+            l.forward(self.xs[i], out=self.outs[i], ids=self.ids[i], w=self.ws[i],
+                      prof=None if prof is None else prof[i])
+
+    def capture(self, prof=None):
+        """Capture one pass over all layers (run one eager pass first to set up)."""
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph, capture_error_mode="relaxed"):
+            self._run(prof)
+        return self.graph
+
+    def replay(self):
+        if self.graph is None:
+            raise RuntimeError("capture() first")
+        self.graph.replay()
