@@ -229,6 +229,48 @@ constexpr int kTmaThreads = kFfnThreads + 32;
 
 __device__ __forceinline__ int ffn_slot_of(const FfnArgs& a, int e) { return a.e2s ? a.e2s[e] : e; }
 
+// Packed fp32 pairs for fma.rn.f32x2 (two independent IEEE fp32 fmas).
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_bf16(uint32_t v) {  // bf16 pair -> fp32 pair (exact)
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(v << 16), "r"(v & 0xffff0000u));
+  return r;
+}
+__device__ __forceinline__ void f2_fma(uint64_t& d, uint64_t a, uint64_t b) {
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(d) : "l"(a), "l"(b));
+}
+__device__ __forceinline__ float2 f2_unpack(uint64_t v) {
+  float2 f;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(f.x), "=f"(f.y) : "l"(v));
+  return f;
+}
+
+// Activations of one row for RB tokens from the [K][RB] staging layout.
+template <int RB>
+__device__ __forceinline__ void load_row_x(const float* __restrict__ xs, int row, float (&xv)[RB]) {
+  const float* p = xs + (size_t)row * RB;
+  if (RB == 1) {
+    xv[0] = p[0];
+  } else if (RB == 2) {
+    const float2 v = *reinterpret_cast<const float2*>(p);
+    xv[0] = v.x;
+    xv[1] = v.y;
+  } else {
+#pragma unroll
+    for (int r4 = 0; r4 < RB / 4; ++r4) {
+      const float4 v = *reinterpret_cast<const float4*>(p + 4 * r4);
+      xv[4 * r4] = v.x;
+      xv[4 * r4 + 1] = v.y;
+      xv[4 * r4 + 2] = v.z;
+      xv[4 * r4 + 3] = v.w;
+    }
+  }
+}
+
 template <bool kDown, int RB>
 __device__ __forceinline__ void tma_consume_batch(const FfnArgs& a, int tile, int p0, int nb, unsigned char* stages,
                                                   uint64_t* full, uint64_t* empty, float* __restrict__ in_s,
@@ -236,39 +278,40 @@ __device__ __forceinline__ void tma_consume_batch(const FfnArgs& a, int tile, in
   const int tid = threadIdx.x, c = tid & 7, g = tid >> 3, lane = tid & 31;
   const int H = a.H, I = a.I;
   const int K = kDown ? I : H;
-  // stage the batch's inputs (x rows, or h rows) as fp32 [RB][K]
+  // Stage the batch's inputs (x rows, or h rows) as fp32 [K][RB]: thread owns
+  // input index kk and writes the RB token values of it side by side.
   named_sync(1, kFfnThreads);
-  // 8 inputs per thread per step: one 16-byte load of bf16 x, or two of fp32 h
-  const int K8 = K / 8;
+  {
+    int tok[RB];
 #pragma unroll
-  for (int r = 0; r < RB; ++r) {
-    float4* dst = reinterpret_cast<float4*>(in_s + r * K);
-    if (r < nb) {
-      if (kDown) {
-        const float4* src = reinterpret_cast<const float4*>(a.hbuf + (size_t)(p0 + r) * I);
-        for (int v = tid; v < K8; v += kFfnThreads) {
-          dst[2 * v] = src[2 * v];
-          dst[2 * v + 1] = src[2 * v + 1];
-        }
-      } else {
-        const int t = a.rows[p0 + r] / a.k;
-        const uint4* src = reinterpret_cast<const uint4*>(a.x + (size_t)t * H);
-        for (int v = tid; v < K8; v += kFfnThreads) {
-          const uint4 u = src[v];
-          dst[2 * v] = make_float4(bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y));
-          dst[2 * v + 1] = make_float4(bf16_lo(u.z), bf16_hi(u.z), bf16_lo(u.w), bf16_hi(u.w));
-        }
+    for (int r = 0; r < RB; ++r) tok[r] = (!kDown && r < nb) ? a.rows[p0 + r] / a.k : 0;
+    for (int kk = tid; kk < K; kk += kFfnThreads) {
+      float v[RB];
+#pragma unroll
+      for (int r = 0; r < RB; ++r) {
+        if (r < nb)
+          v[r] = kDown ? a.hbuf[(size_t)(p0 + r) * I + kk] : bf16_to_f32(a.x[(size_t)tok[r] * H + kk]);
+        else
+          v[r] = 0.f;
       }
-    } else {
-      for (int v = tid; v < K8; v += kFfnThreads) dst[2 * v] = dst[2 * v + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      float* dst = in_s + (size_t)kk * RB;
+      if (RB == 1) {
+        dst[0] = v[0];
+      } else if (RB == 2) {
+        *reinterpret_cast<float2*>(dst) = make_float2(v[0], v[1]);
+      } else {
+#pragma unroll
+        for (int r4 = 0; r4 < RB / 4; ++r4)
+          *reinterpret_cast<float4*>(dst + 4 * r4) = make_float4(v[4 * r4], v[4 * r4 + 1], v[4 * r4 + 2], v[4 * r4 + 3]);
+      }
     }
   }
   named_sync(1, kFfnThreads);
-  float acc[RB][8];
+  uint64_t acc2[RB][4];  // acc2[r][p] = columns (2p, 2p+1) of token r
 #pragma unroll
   for (int r = 0; r < RB; ++r)
 #pragma unroll
-    for (int q = 0; q < 8; ++q) acc[r][q] = 0.f;
+    for (int p = 0; p < 4; ++p) acc2[r][p] = 0ull;
   // byte offset of this thread's 16 bytes within a stage row block
   const int mat_off = kDown ? 0 : (c < 4 ? 0 : kStageBytes / 2);
   const int row_bytes = kDown ? kDTile * 2 : kGUTile * 2;
@@ -286,19 +329,28 @@ __device__ __forceinline__ void tma_consume_batch(const FfnArgs& a, int tile, in
     for (int j = 0; j < kKB / kKG; ++j) {
       const int rl = g + kKG * j;
       const uint4 wv = *reinterpret_cast<const uint4*>(st + rl * row_bytes);
-      float wf[8];
-      unpack8(wv, wf);
-      const int row = kc * kKB + rl;
+      const uint64_t w2[4] = {f2_bf16(wv.x), f2_bf16(wv.y), f2_bf16(wv.z), f2_bf16(wv.w)};
+      float xv[RB];
+      load_row_x<RB>(in_s, kc * kKB + rl, xv);
 #pragma unroll
       for (int r = 0; r < RB; ++r) {
-        const float xv = in_s[r * K + row];
+        const uint64_t xb = f2_pack(xv[r], xv[r]);
 #pragma unroll
-        for (int q = 0; q < 8; ++q) acc[r][q] = fmaf(wf[q], xv, acc[r][q]);
+        for (int p = 0; p < 4; ++p) f2_fma(acc2[r][p], w2[p], xb);
       }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[sl]);
   }
+  float acc[RB][8];
+#pragma unroll
+  for (int r = 0; r < RB; ++r)
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+      const float2 f = f2_unpack(acc2[r][p]);
+      acc[r][2 * p] = f.x;
+      acc[r][2 * p + 1] = f.y;
+    }
   warp_partials<RB>(acc, red);
   named_sync(1, kFfnThreads);
   if (kDown) {
