@@ -4,7 +4,7 @@ The MoE layer forward -- route, permute, expert_cache_manage,
 expert_cache_gather (or zero-return), grouped SwiGLU FFN, combine -- runs in
 the CUDA kernels of ``libmoeslot.so`` (declared in ``include/moeslot.h``).
 This package only marshals arguments.  Build the library first with
-``python -m expert_slot_cache_gb300.build``.
+``python __graft_entry__.py`` (it calls build()).
 """
 from .binding import (MODE_GATHER, MODE_RESIDENT, MODE_ZERO_RETURN, POLICY_LFU, POLICY_LRU,  # noqa: F401
                       POLICY_STATIC, CacheState, LayerArgs, MoeError, SlotCachedMoELayer, bias_table,

@@ -20,7 +20,7 @@ LIB_PATH = os.path.join(_HERE, "_lib", "libmoeslot.so")
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(
-        f"{LIB_PATH} is not built; run `python -m expert_slot_cache_gb300.build` "
+        f"{LIB_PATH} is not built; run `python __graft_entry__.py` "
         "(or __graft_entry__.build()) first")
 
 lib = ctypes.CDLL(LIB_PATH)
@@ -61,7 +61,8 @@ I32 = c_int
 _status_str = _sig("moe_status_str", [c_int], ctypes.c_char_p)
 _bias_table = _sig("moe_bias_table", [V, I32, I32, c_float, V, V])
 _route = _sig("moe_route", [V, V, V, V, I32, I32, I32, I32, V, V, V, V])
-_permute = _sig("moe_permute", [V, I32, I32, V, V, V, V, V, V, V, V])
+_permute = _sig("moe_permute", [V, I32, I32, V, V, V, V, V, V, V, V, V])
+_permute_scratch = _sig("moe_permute_scratch_bytes", [I32, I32], c_size_t)
 _manage = _sig("moe_cache_manage", [V, I32, I32, I32, I32, V, V, V, V, V, V, V, V, V, V, V, V])
 _gather = _sig("moe_cache_gather", [V, V, c_size_t, I32, I32, V, V, V, I32, V, V])
 _ffn = _sig("moe_expert_ffn", [V, I32, I32, I32, I32, I32, V, V, V, V, I32, V, I32, V, V, V, V, c_size_t, V, V])
@@ -130,13 +131,16 @@ class Groups:
     n_act: torch.Tensor
 
 
-def permute(ids: torch.Tensor, E: int, dev_status: Optional[torch.Tensor] = None, stream=None) -> Groups:
+def permute(ids: torch.Tensor, E: int, dev_status: Optional[torch.Tensor] = None, stream=None,
+            chunked: bool = True) -> Groups:
     n = ids.numel()
     i32 = dict(dtype=torch.int32, device=ids.device)
     g = Groups(torch.empty(E, **i32), torch.empty(E + 1, **i32), torch.empty(n, **i32), torch.empty(n, **i32),
                torch.empty(E, **i32), torch.empty(1, **i32))
+    nb = int(_permute_scratch(n, E)) if chunked else 0
+    scratch = torch.empty(max(nb // 4, 1), **i32) if nb else None
     _ck(_permute(_p(ids), n, E, _p(g.count), _p(g.offset), _p(g.rows), _p(g.pos), _p(g.act_e), _p(g.n_act),
-                 _p(dev_status), _s(stream)), "moe_permute")
+                 _p(scratch), _p(dev_status), _s(stream)), "moe_permute")
     return g
 
 

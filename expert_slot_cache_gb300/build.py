@@ -4,7 +4,7 @@ Each .cu under csrc/ is compiled with nvcc in parallel, then linked into one
 shared library with the CUDA runtime linked statically (the library shares
 the process's CUDA context with PyTorch through the driver).
 
-    python -m expert_slot_cache_gb300.build [--verbose-ptxas]
+    python -c "import __graft_entry__ as g; g._build_module().build(force=True)"
 """
 from __future__ import annotations
 

@@ -21,6 +21,7 @@ struct LayerWs {
   int32_t *count, *offset, *rows, *pos, *act_e, *n_act, *miss_e, *miss_s, *n_miss, *hit_e, *n_hit;
   float *hbuf, *y, *logits;
   uint16_t *xp, *hb;
+  int32_t* perm;
   size_t bytes;
 };
 
@@ -49,6 +50,7 @@ static LayerWs carve(void* base, int n, int H, int E, int I, int T) {
   w.hbuf = (float*)take(4 * (size_t)n * I);
   w.y = (float*)take(4 * (size_t)n * H);
   w.logits = (float*)take(4 * (size_t)T * E);
+  w.perm = (int32_t*)take(moe_permute_scratch_bytes(n, E) + 4);
   if (prefill_extra_bytes(n, H, I) > 0) {
     w.xp = (uint16_t*)take(2 * (size_t)n * H);
     w.hb = (uint16_t*)take(2 * (size_t)n * I);
@@ -201,7 +203,8 @@ extern "C" int moe_layer_forward(const moe_layer_args* a, moe_stream_t main_s, m
     const int lmax = std::min(n, E);
     const int32_t* ids_c = a->ids + (size_t)t0 * k;
     prof.begin(MOE_PROF_PERMUTE, ms);
-    r = moe_permute(ids_c, n, E, ws.count, ws.offset, ws.rows, ws.pos, ws.act_e, ws.n_act, a->dev_status, main_s);
+    r = launch_permute(ids_c, n, E, ws.count, ws.offset, ws.rows, ws.pos, ws.act_e, ws.n_act, a->dev_status, ws.perm,
+                       ms);
     if (r != MOE_OK) return r;
     prof.end(ms);
     FfnArgs f{(const uint16_t*)a->x + (size_t)t0 * H, tc, H, I, k, E, ws.offset, ws.rows, nullptr, nullptr,

@@ -109,11 +109,16 @@ int moe_route(const void* x, const void* w_router, const float* logit_offset, co
  *   pos     device int32 [n]      grouped position of each flat index
  *   act_e   device int32 [E]      experts with count > 0, ascending
  *   n_act   device int32 [1]      their number
+ *   scratch device, moe_permute_scratch_bytes(n, E) bytes, or NULL: with it,
+ *           n > 1024 is grouped by ceil(n/1024) CTAs (histogram, scan,
+ *           scatter); without it by one CTA.  The result is the same.
  *   dev_status device int32 [1]   set to MOE_DEV_BAD_EXPERT on an id outside [0, E)
  * Errors: MOE_ERR_ARG on NULL pointers, n < 1 or E out of range.
  */
 int moe_permute(const int32_t* ids, int n, int E, int32_t* count, int32_t* offset, int32_t* rows,
-                int32_t* pos, int32_t* act_e, int32_t* n_act, int32_t* dev_status, moe_stream_t stream);
+                int32_t* pos, int32_t* act_e, int32_t* n_act, int32_t* scratch, int32_t* dev_status,
+                moe_stream_t stream);
+size_t moe_permute_scratch_bytes(int n, int E);
 
 /*
  * expert_cache_manage: update the slot cache for one step and emit the miss list.

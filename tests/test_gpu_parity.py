@@ -82,11 +82,13 @@ def test_route_parity(name, cfg, cap, offset):
 # Permute
 # ----------------------------------------------------------------------------
 
-@pytest.mark.parametrize("n,E", [(1, 16), (7, 5), (64, 128), (640, 512), (1024, 128), (3001, 288), (32768, 128)])
-def test_permute_parity(n, E):
+@pytest.mark.parametrize("chunked", [True, False], ids=["chunked", "one_cta"])
+@pytest.mark.parametrize("n,E", [(1, 16), (7, 5), (64, 128), (640, 512), (1024, 128), (1025, 16), (3001, 288),
+                                 (32768, 128)])
+def test_permute_parity(n, E, chunked):
     rng = np.random.default_rng(n * 7 + E)
     ids = rng.integers(0, E, size=n).astype(np.int32)
-    g = M.permute(torch.from_numpy(ids).to(DEV), E)
+    g = M.permute(torch.from_numpy(ids).to(DEV), E, chunked=chunked)
     torch.cuda.synchronize()
     count, offset, rows, pos = O.permute(ids.reshape(1, -1), E)
     assert np.array_equal(_np(g.count), count)
