@@ -60,7 +60,8 @@ V = c_void_p
 I32 = c_int
 _status_str = _sig("moe_status_str", [c_int], ctypes.c_char_p)
 _bias_table = _sig("moe_bias_table", [V, I32, I32, c_float, V, V])
-_route = _sig("moe_route", [V, V, V, V, I32, I32, I32, I32, V, V, V, V])
+_route = _sig("moe_route", [V, V, V, V, I32, I32, I32, I32, V, V, V, V, V])
+_route_scratch = _sig("moe_route_scratch_bytes", [I32, I32, I32], c_size_t)
 _permute = _sig("moe_permute", [V, I32, I32, V, V, V, V, V, V, V, V, V])
 _permute_scratch = _sig("moe_permute_scratch_bytes", [I32, I32], c_size_t)
 _manage = _sig("moe_cache_manage", [V, I32, I32, I32, I32, V, V, V, V, V, V, V, V, V, V, V, V])
@@ -110,14 +111,16 @@ def bias_table(b: torch.Tensor, n_hot: int, cap: float, stream=None) -> torch.Te
     return out
 
 
-def route(x, w_router, k, logit_offset=None, sel_bias=None, return_logits=False, stream=None):
+def route(x, w_router, k, logit_offset=None, sel_bias=None, return_logits=False, stream=None, blocked=True):
     T, H = x.shape
     E = w_router.shape[1]
     ids = torch.empty(T, k, dtype=torch.int32, device=x.device)
     w = torch.empty(T, k, dtype=torch.float32, device=x.device)
     logits = torch.empty(T, E, dtype=torch.float32, device=x.device)
-    _ck(_route(_p(x), _p(w_router), _p(logit_offset), _p(sel_bias), T, H, E, k, _p(logits), _p(ids), _p(w),
-               _s(stream)), "moe_route")
+    nb = int(_route_scratch(T, H, E)) if blocked else 0
+    scratch = torch.empty(max(nb // 4, 1), dtype=torch.float32, device=x.device) if nb else None
+    _ck(_route(_p(x), _p(w_router), _p(logit_offset), _p(sel_bias), T, H, E, k, _p(logits), _p(scratch), _p(ids),
+               _p(w), _s(stream)), "moe_route")
     return (ids, w, logits) if return_logits else (ids, w)
 
 

@@ -19,7 +19,7 @@ static size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 // Workspace layout of the layer forward, for chunks of up to n = C*k routing slots.
 struct LayerWs {
   int32_t *count, *offset, *rows, *pos, *act_e, *n_act, *miss_e, *miss_s, *n_miss, *hit_e, *n_hit;
-  float *hbuf, *y, *logits;
+  float *hbuf, *y, *logits, *route;
   uint16_t *xp, *hb;
   int32_t* perm;
   size_t bytes;
@@ -50,6 +50,7 @@ static LayerWs carve(void* base, int n, int H, int E, int I, int T) {
   w.hbuf = (float*)take(4 * (size_t)n * I);
   w.y = (float*)take(4 * (size_t)n * H);
   w.logits = (float*)take(4 * (size_t)T * E);
+  w.route = (float*)take(moe_route_scratch_bytes(T, H, E) + 4);
   w.perm = (int32_t*)take(moe_permute_scratch_bytes(n, E) + 4);
   if (prefill_extra_bytes(n, H, I) > 0) {
     w.xp = (uint16_t*)take(2 * (size_t)n * H);
@@ -193,7 +194,8 @@ extern "C" int moe_layer_forward(const moe_layer_args* a, moe_stream_t main_s, m
   if (prof.p) prof.p->used = 0;
   const size_t slab_bytes = (size_t)6 * H * I;
   prof.begin(MOE_PROF_ROUTE, ms);
-  int r = moe_route(a->x, a->w_router, a->logit_offset, a->sel_bias, T, H, E, k, ws.logits, a->ids, a->w, main_s);
+  int r = moe_route(a->x, a->w_router, a->logit_offset, a->sel_bias, T, H, E, k, ws.logits,
+                    moe_route_scratch_bytes(T, H, E) ? ws.route : nullptr, a->ids, a->w, main_s);
   if (r != MOE_OK) return r;
   prof.end(ms);
 

@@ -225,7 +225,10 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(const FfnArgs a) {
 constexpr int kStages = 6;
 constexpr int kKB = 128;
 constexpr int kStageBytes = 16384;
-constexpr int kTmaThreads = kFfnThreads + 32;
+constexpr int kTmaConsumers = 512;             // 16 consumer warps
+constexpr int kTmaKG = kTmaConsumers / 8;      // 64 k-groups of 8 column threads
+constexpr int kTmaRB = 4;                      // tokens per batch
+constexpr int kTmaThreads = kTmaConsumers + 32;
 
 __device__ __forceinline__ int ffn_slot_of(const FfnArgs& a, int e) { return a.e2s ? a.e2s[e] : e; }
 
@@ -274,18 +277,19 @@ __device__ __forceinline__ void load_row_x(const float* __restrict__ xs, int row
 template <bool kDown, int RB>
 __device__ __forceinline__ void tma_consume_batch(const FfnArgs& a, int tile, int p0, int nb, unsigned char* stages,
                                                   uint64_t* full, uint64_t* empty, float* __restrict__ in_s,
-                                                  float* __restrict__ red, uint32_t& it, volatile int* abort_flag) {
+                                                  float* __restrict__ red, uint32_t& it, volatile int* abort_flag,
+                                                  bool restage) {
   const int tid = threadIdx.x, c = tid & 7, g = tid >> 3, lane = tid & 31;
   const int H = a.H, I = a.I;
   const int K = kDown ? I : H;
   // Stage the batch's inputs (x rows, or h rows) as fp32 [K][RB]: thread owns
   // input index kk and writes the RB token values of it side by side.
-  named_sync(1, kFfnThreads);
-  {
+  named_sync(1, kTmaConsumers);
+  if (restage) {
     int tok[RB];
 #pragma unroll
     for (int r = 0; r < RB; ++r) tok[r] = (!kDown && r < nb) ? a.rows[p0 + r] / a.k : 0;
-    for (int kk = tid; kk < K; kk += kFfnThreads) {
+    for (int kk = tid; kk < K; kk += kTmaConsumers) {
       float v[RB];
 #pragma unroll
       for (int r = 0; r < RB; ++r) {
@@ -305,8 +309,8 @@ __device__ __forceinline__ void tma_consume_batch(const FfnArgs& a, int tile, in
           *reinterpret_cast<float4*>(dst + 4 * r4) = make_float4(v[4 * r4], v[4 * r4 + 1], v[4 * r4 + 2], v[4 * r4 + 3]);
       }
     }
+    named_sync(1, kTmaConsumers);
   }
-  named_sync(1, kFfnThreads);
   uint64_t acc2[RB][4];  // acc2[r][p] = columns (2p, 2p+1) of token r
 #pragma unroll
   for (int r = 0; r < RB; ++r)
@@ -326,8 +330,8 @@ __device__ __forceinline__ void tma_consume_batch(const FfnArgs& a, int tile, in
     }
     const unsigned char* st = stages + sl * kStageBytes + mat_off + col_off;
 #pragma unroll
-    for (int j = 0; j < kKB / kKG; ++j) {
-      const int rl = g + kKG * j;
+    for (int j = 0; j < kKB / kTmaKG; ++j) {
+      const int rl = g + kTmaKG * j;
       const uint4 wv = *reinterpret_cast<const uint4*>(st + rl * row_bytes);
       const uint64_t w2[4] = {f2_bf16(wv.x), f2_bf16(wv.y), f2_bf16(wv.z), f2_bf16(wv.w)};
       float xv[RB];
@@ -352,25 +356,25 @@ __device__ __forceinline__ void tma_consume_batch(const FfnArgs& a, int tile, in
       acc[r][2 * p + 1] = f.y;
     }
   warp_partials<RB>(acc, red);
-  named_sync(1, kFfnThreads);
+  named_sync(1, kTmaConsumers);
   if (kDown) {
     const int o0 = tile * kDTile;
-    for (int o = tid; o < kDTile * RB; o += kFfnThreads) {
+    for (int o = tid; o < kDTile * RB; o += kTmaConsumers) {
       const int r = o / kDTile, ol = o - r * kDTile;
       const int cg = ol >> 3, q = ol & 7;
       float s = 0.f;
 #pragma unroll
-      for (int wp = 0; wp < kFfnThreads / 32; ++wp) s += red[((wp * 8 + cg) * RB + r) * 8 + q];
+      for (int wp = 0; wp < kTmaConsumers / 32; ++wp) s += red[((wp * 8 + cg) * RB + r) * 8 + q];
       if (r < nb) a.y[(size_t)(p0 + r) * H + o0 + ol] = s;
     }
   } else {
     const int i0 = tile * kGUTile;
-    for (int o = tid; o < kGUTile * RB; o += kFfnThreads) {
+    for (int o = tid; o < kGUTile * RB; o += kTmaConsumers) {
       const int r = o / kGUTile, il = o - r * kGUTile;
       const int cg = il >> 3, q = il & 7;
       float gs = 0.f, us = 0.f;
 #pragma unroll
-      for (int wp = 0; wp < kFfnThreads / 32; ++wp) {
+      for (int wp = 0; wp < kTmaConsumers / 32; ++wp) {
         gs += red[((wp * 8 + cg) * RB + r) * 8 + q];
         us += red[((wp * 8 + cg + 4) * RB + r) * 8 + q];
       }
@@ -388,15 +392,15 @@ __global__ void __launch_bounds__(kTmaThreads, 1) ffn_tma_kernel(const FfnArgs a
   const int K = kDown ? a.I : a.H;
   unsigned char* stages = tsm;
   float* in_s = reinterpret_cast<float*>(tsm + kStages * kStageBytes);
-  float* red = in_s + kRB * K;
-  uint64_t* full = reinterpret_cast<uint64_t*>(red + 8 * 8 * kRB * 8);
+  float* red = in_s + kTmaRB * K;
+  uint64_t* full = reinterpret_cast<uint64_t*>(red + (kTmaConsumers / 32) * 8 * kTmaRB * 8);
   uint64_t* empty = full + kStages;
   __shared__ int s_abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kFfnThreads / 32);
+      mbar_init(&empty[s], kTmaConsumers / 32);
     }
     s_abort = 0;
     mbar_fence_init();
@@ -406,20 +410,25 @@ __global__ void __launch_bounds__(kTmaThreads, 1) ffn_tma_kernel(const FfnArgs a
   const int tiles = kDown ? a.H / kDTile : a.I / kGUTile;
   const int items = *a.n_list * tiles;
   const int nkc = K / kKB;
+  // a contiguous, balanced range of items per CTA: consecutive items usually
+  // share an expert, so its staged activations are reused
+  const int q = items / gridDim.x, rem = items % gridDim.x;
+  const int beg = blockIdx.x * q + min((int)blockIdx.x, rem);
+  const int end = beg + q + ((int)blockIdx.x < rem ? 1 : 0);
 
-  if (warp == kFfnThreads / 32) {
+  if (warp == kTmaConsumers / 32) {
     // producer
     if (lane == 0) {
       uint32_t it = 0;
       int last_use[kStages];
       for (int s = 0; s < kStages; ++s) last_use[s] = -1;
-      for (int item = blockIdx.x; item < items && !*abort_flag; item += gridDim.x) {
+      for (int item = beg; item < end && !*abort_flag; ++item) {
         const int li = item / tiles, tile = item - li * tiles;
         const int e = a.list_e[li];
         if (e < 0 || e >= a.E) continue;
         const int slot = ffn_slot_of(a, e);
         if (slot < 0 || slot >= a.S) continue;
-        const int nbat = (a.offset[e + 1] - a.offset[e] + kRB - 1) / kRB;
+        const int nbat = (a.offset[e + 1] - a.offset[e] + kTmaRB - 1) / kTmaRB;
         for (int b = 0; b < nbat; ++b) {
           for (int kc = 0; kc < nkc; ++kc, ++it) {
             const int sl = it % kStages;
@@ -450,7 +459,8 @@ __global__ void __launch_bounds__(kTmaThreads, 1) ffn_tma_kernel(const FfnArgs a
   } else {
     // consumers
     uint32_t it = 0;
-    for (int item = blockIdx.x; item < items; item += gridDim.x) {
+    int staged_e = -1, staged_p0 = -1;
+    for (int item = beg; item < end; ++item) {
       const int li = item / tiles, tile = item - li * tiles;
       const int e = a.list_e[li];
       if (e < 0 || e >= a.E) {
@@ -463,12 +473,17 @@ __global__ void __launch_bounds__(kTmaThreads, 1) ffn_tma_kernel(const FfnArgs a
         continue;
       }
       const int pb = a.offset[e], pe = a.offset[e + 1];
-      for (int p0 = pb; p0 < pe; p0 += kRB) {
-        const int nb = min(kRB, pe - p0);
-        if (nb == 1) tma_consume_batch<kDown, 1>(a, tile, p0, nb, stages, full, empty, in_s, red, it, abort_flag);
-        else if (nb == 2) tma_consume_batch<kDown, 2>(a, tile, p0, nb, stages, full, empty, in_s, red, it, abort_flag);
-        else if (nb <= 4) tma_consume_batch<kDown, 4>(a, tile, p0, nb, stages, full, empty, in_s, red, it, abort_flag);
-        else tma_consume_batch<kDown, 8>(a, tile, p0, nb, stages, full, empty, in_s, red, it, abort_flag);
+      for (int p0 = pb; p0 < pe; p0 += kTmaRB) {
+        const int nb = min(kTmaRB, pe - p0);
+        const bool restage = !(staged_e == e && staged_p0 == p0);
+        staged_e = e;
+        staged_p0 = p0;
+        if (nb == 1)
+          tma_consume_batch<kDown, 1>(a, tile, p0, nb, stages, full, empty, in_s, red, it, abort_flag, restage);
+        else if (nb == 2)
+          tma_consume_batch<kDown, 2>(a, tile, p0, nb, stages, full, empty, in_s, red, it, abort_flag, restage);
+        else
+          tma_consume_batch<kDown, 4>(a, tile, p0, nb, stages, full, empty, in_s, red, it, abort_flag, restage);
       }
     }
   }
@@ -476,8 +491,8 @@ __global__ void __launch_bounds__(kTmaThreads, 1) ffn_tma_kernel(const FfnArgs a
 }
 
 static size_t tma_smem_bytes(int K) {
-  return 1024 + (size_t)kStages * kStageBytes + (size_t)(kRB * K + 8 * 8 * kRB * 8) * sizeof(float) +
-         2 * kStages * sizeof(uint64_t);
+  return 1024 + (size_t)kStages * kStageBytes +
+         (size_t)(kTmaRB * K + (kTmaConsumers / 32) * 8 * kTmaRB * 8) * sizeof(float) + 2 * kStages * sizeof(uint64_t);
 }
 
 static size_t ffn_smem_bytes(int K) { return (size_t)(kRB * K + 8 * 8 * kRB * 8) * sizeof(float); }
@@ -537,50 +552,68 @@ int launch_ffn(const FfnArgs& a, int max_list, cudaStream_t stream, Prof* prof) 
 // ---------------------------------------------------------------------------
 // Combine: out[t] = sum_j w[t][j] y[pos[t*k+j]] in fp32, j ascending.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ y, const float* __restrict__ w,
-                                                      const int32_t* __restrict__ pos,
-                                                      const int32_t* __restrict__ ids,
-                                                      const int32_t* __restrict__ e2s, int k, int H, int E,
-                                                      int split, uint16_t* __restrict__ out,
-                                                      float* __restrict__ out_res, float* __restrict__ out_miss) {
+constexpr int kCombThreads = 128;  // x 4 columns = 512 columns per CTA
+
+__global__ void __launch_bounds__(kCombThreads) combine_kernel(const float* __restrict__ y, const float* __restrict__ w,
+                                                               const int32_t* __restrict__ pos,
+                                                               const int32_t* __restrict__ ids,
+                                                               const int32_t* __restrict__ e2s, int k, int H, int E,
+                                                               int split, uint16_t* __restrict__ out,
+                                                               float* __restrict__ out_res,
+                                                               float* __restrict__ out_miss) {
   const int t = blockIdx.x;
-  for (int c = threadIdx.x * 4; c < H; c += blockDim.x * 4) {
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f), accm = acc;
-    for (int j = 0; j < k; ++j) {
+  const int c = (blockIdx.y * kCombThreads + threadIdx.x) * 4;
+  if (c >= H) return;
+  // all k rows first (independent loads), then the sum in j order
+  float4 v[kMaxK];
+  float wj[kMaxK];
+  bool res[kMaxK];
+#pragma unroll
+  for (int j = 0; j < kMaxK; ++j) {
+    v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+    wj[j] = 0.f;
+    res[j] = true;
+    if (j < k) {
       const int p = pos[(size_t)t * k + j];
-      if (p < 0) continue;
-      const float wj = w[(size_t)t * k + j];
-      const float4 v = *reinterpret_cast<const float4*>(y + (size_t)p * H + c);
-      bool res = true;
-      if (split) {
-        const int e = ids[(size_t)t * k + j];
-        res = e >= 0 && e < E && e2s[e] >= 0;
+      if (p >= 0) {
+        wj[j] = w[(size_t)t * k + j];
+        v[j] = *reinterpret_cast<const float4*>(y + (size_t)p * H + c);
+        if (split) {
+          const int e = ids[(size_t)t * k + j];
+          res[j] = e >= 0 && e < E && e2s[e] >= 0;
+        }
       }
-      float4& d = res ? acc : accm;
-      d.x = fmaf(wj, v.x, d.x);
-      d.y = fmaf(wj, v.y, d.y);
-      d.z = fmaf(wj, v.z, d.z);
-      d.w = fmaf(wj, v.w, d.w);
     }
-    const size_t o = (size_t)t * H + c;
-    float4 tot = acc;
-    if (split) {
-      *reinterpret_cast<float4*>(out_res + o) = acc;
-      *reinterpret_cast<float4*>(out_miss + o) = accm;
-      tot = make_float4(acc.x + accm.x, acc.y + accm.y, acc.z + accm.z, acc.w + accm.w);
-    }
-    uint2 pk;
-    pk.x = uint32_t(f32_to_bf16(tot.x)) | (uint32_t(f32_to_bf16(tot.y)) << 16);
-    pk.y = uint32_t(f32_to_bf16(tot.z)) | (uint32_t(f32_to_bf16(tot.w)) << 16);
-    *reinterpret_cast<uint2*>(out + o) = pk;
   }
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f), accm = acc;
+#pragma unroll
+  for (int j = 0; j < kMaxK; ++j) {
+    if (j < k) {
+      float4& d = res[j] ? acc : accm;
+      d.x = fmaf(wj[j], v[j].x, d.x);
+      d.y = fmaf(wj[j], v[j].y, d.y);
+      d.z = fmaf(wj[j], v[j].z, d.z);
+      d.w = fmaf(wj[j], v[j].w, d.w);
+    }
+  }
+  const size_t o = (size_t)t * H + c;
+  float4 tot = acc;
+  if (split) {
+    *reinterpret_cast<float4*>(out_res + o) = acc;
+    *reinterpret_cast<float4*>(out_miss + o) = accm;
+    tot = make_float4(acc.x + accm.x, acc.y + accm.y, acc.z + accm.z, acc.w + accm.w);
+  }
+  uint2 pk;
+  pk.x = uint32_t(f32_to_bf16(tot.x)) | (uint32_t(f32_to_bf16(tot.y)) << 16);
+  pk.y = uint32_t(f32_to_bf16(tot.z)) | (uint32_t(f32_to_bf16(tot.w)) << 16);
+  *reinterpret_cast<uint2*>(out + o) = pk;
 }
 
 int launch_combine(const float* y, const float* w, const int32_t* pos, const int32_t* ids, const int32_t* e2s, int T,
                    int k, int H, int E, int split, void* out, float* out_res, float* out_miss, cudaStream_t stream) {
-  const int threads = std::min(256, std::max(32, H / 4));
-  combine_kernel<<<T, threads, 0, stream>>>(y, w, pos, ids, e2s, k, H, E, split, (uint16_t*)out, out_res,
-                                            out_miss);
+  const dim3 grid(T, (H / 4 + kCombThreads - 1) / kCombThreads);
+  combine_kernel<<<grid, kCombThreads, 0, stream>>>(y, w, pos, ids, e2s, k, H, E, split, (uint16_t*)out, out_res,
+                                                    out_miss);
   MOE_LAUNCH_CHECK();
   return MOE_OK;
 }

@@ -43,12 +43,14 @@ __global__ void __launch_bounds__(1024) bias_table_kernel(const float* __restric
 }
 
 // ---------------------------------------------------------------------------
-// Logits kernel.  CTA = (8*CH tokens) x (32 experts), 256 threads: warp w owns
-// token lanes t = w + 8c (c < CH), lane = expert.  Each output (t, e) is one
-// fp32 chain acc = fma(x[t][h], Wr[h][e], acc) over h = 0..H-1 in order (the
-// order the oracle follows).  Wr[:, e0:e0+32] and the CTA's x rows stream
-// through a 4-stage cp.async ring of 128-row chunks in shared memory, so the
-// chains never wait on a global load.
+// Logits.  The fp32 order (the one the oracle follows): h is cut into blocks
+// of 128 rows; block b gives part_b = fma chain from 0 over its rows in
+// order; logit = 0 + part_0 + part_1 + ... in block order.
+//
+// logits_kernel: CTA = (8*CH tokens) x (32 experts), 256 threads: warp w owns
+// token lanes t = w + 8c (c < CH), lane = expert.  Wr[:, e0:e0+32] and the
+// CTA's x rows stream through a 4-stage cp.async ring of 128-row chunks (one
+// chunk = one block), so the chains never wait on a global load.
 // ---------------------------------------------------------------------------
 constexpr int kRouteThreads = 256;
 constexpr int kEB = 32;        // experts per CTA
@@ -121,6 +123,9 @@ __global__ void __launch_bounds__(kRouteThreads) logits_kernel(const uint16_t* _
     const uint16_t* ws = reinterpret_cast<const uint16_t*>(sw);
     const uint16_t* xs = reinterpret_cast<const uint16_t*>(sw + kWBytes);
     const int hn = min(kHC, H - c * kHC);  // a multiple of 8
+    float part[CH];  // this 128-row block's chain, added to the logit afterwards
+#pragma unroll
+    for (int cc = 0; cc < CH; ++cc) part[cc] = 0.f;
     for (int h0 = 0; h0 < hn; h0 += 8) {
       // operands of 8 consecutive h first, then the 8 fma steps of each chain
       float wv[8];
@@ -129,16 +134,18 @@ __global__ void __launch_bounds__(kRouteThreads) logits_kernel(const uint16_t* _
 #pragma unroll
       for (int cc = 0; cc < CH; ++cc) {
         const uint4 xv = *reinterpret_cast<const uint4*>(xs + (warp + 8 * cc) * kHC + h0);
-        acc[cc] = fmaf(bf16_lo(xv.x), wv[0], acc[cc]);
-        acc[cc] = fmaf(bf16_hi(xv.x), wv[1], acc[cc]);
-        acc[cc] = fmaf(bf16_lo(xv.y), wv[2], acc[cc]);
-        acc[cc] = fmaf(bf16_hi(xv.y), wv[3], acc[cc]);
-        acc[cc] = fmaf(bf16_lo(xv.z), wv[4], acc[cc]);
-        acc[cc] = fmaf(bf16_hi(xv.z), wv[5], acc[cc]);
-        acc[cc] = fmaf(bf16_lo(xv.w), wv[6], acc[cc]);
-        acc[cc] = fmaf(bf16_hi(xv.w), wv[7], acc[cc]);
+        part[cc] = fmaf(bf16_lo(xv.x), wv[0], part[cc]);
+        part[cc] = fmaf(bf16_hi(xv.x), wv[1], part[cc]);
+        part[cc] = fmaf(bf16_lo(xv.y), wv[2], part[cc]);
+        part[cc] = fmaf(bf16_hi(xv.y), wv[3], part[cc]);
+        part[cc] = fmaf(bf16_lo(xv.z), wv[4], part[cc]);
+        part[cc] = fmaf(bf16_hi(xv.z), wv[5], part[cc]);
+        part[cc] = fmaf(bf16_lo(xv.w), wv[6], part[cc]);
+        part[cc] = fmaf(bf16_hi(xv.w), wv[7], part[cc]);
       }
     }
+#pragma unroll
+    for (int cc = 0; cc < CH; ++cc) acc[cc] += part[cc];
   }
   cp_async_wait<0>();
   const int e = e0 + lane;
@@ -151,30 +158,107 @@ __global__ void __launch_bounds__(kRouteThreads) logits_kernel(const uint16_t* _
   }
 }
 
+// logits_block_kernel (small T): CTA = one 128-row block x 32 experts x
+// 8*CH tokens; writes part[b][t][e].  topk_kernel adds the parts in order.
+template <int CH>
+__global__ void __launch_bounds__(kRouteThreads) logits_block_kernel(const uint16_t* __restrict__ x,
+                                                                     const uint16_t* __restrict__ wr, int T, int H,
+                                                                     int E, float* __restrict__ part) {
+  constexpr int TT = 8 * CH;
+  __shared__ __align__(16) uint16_t ws[kHC * kEB];
+  __shared__ __align__(16) uint16_t xs[TT * kHC];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int b = blockIdx.x, e0 = blockIdx.y * kEB, t0 = blockIdx.z * TT;
+  const int h0 = b * kHC;
+  const int nt = min(TT, T - t0);
+  const int hn = min(kHC, H - h0);
+  for (int v = tid; v < kHC * 4; v += kRouteThreads) {
+    const int r = v >> 2, q = v & 3;
+    const bool ok = r < hn && e0 + 8 * q < E;
+    cp_async16(reinterpret_cast<unsigned char*>(ws) + r * 64 + q * 16,
+               ok ? wr + (size_t)(h0 + r) * E + e0 + 8 * q : wr, ok);
+  }
+  for (int v = tid; v < TT * (kHC / 8); v += kRouteThreads) {
+    const int r = v / (kHC / 8), q = v % (kHC / 8);
+    const bool ok = r < nt && 8 * q < hn;
+    cp_async16(xs + r * kHC + 8 * q, ok ? x + (size_t)(t0 + r) * H + h0 + 8 * q : x, ok);
+  }
+  cp_async_commit();
+  cp_async_wait<0>();
+  __syncthreads();
+  float acc[CH];
+#pragma unroll
+  for (int cc = 0; cc < CH; ++cc) acc[cc] = 0.f;
+  for (int hh = 0; hh < hn; hh += 8) {
+    float wv[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) wv[u] = bf16_to_f32(ws[(hh + u) * kEB + lane]);
+#pragma unroll
+    for (int cc = 0; cc < CH; ++cc) {
+      const uint4 xv = *reinterpret_cast<const uint4*>(xs + (warp + 8 * cc) * kHC + hh);
+      acc[cc] = fmaf(bf16_lo(xv.x), wv[0], acc[cc]);
+      acc[cc] = fmaf(bf16_hi(xv.x), wv[1], acc[cc]);
+      acc[cc] = fmaf(bf16_lo(xv.y), wv[2], acc[cc]);
+      acc[cc] = fmaf(bf16_hi(xv.y), wv[3], acc[cc]);
+      acc[cc] = fmaf(bf16_lo(xv.z), wv[4], acc[cc]);
+      acc[cc] = fmaf(bf16_hi(xv.z), wv[5], acc[cc]);
+      acc[cc] = fmaf(bf16_lo(xv.w), wv[6], acc[cc]);
+      acc[cc] = fmaf(bf16_hi(xv.w), wv[7], acc[cc]);
+    }
+  }
+  const int e = e0 + lane;
+  if (e < E) {
+#pragma unroll
+    for (int cc = 0; cc < CH; ++cc) {
+      const int t = warp + 8 * cc;
+      if (t < nt) part[((size_t)b * T + t0 + t) * E + e] = acc[cc];
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------
 // Top-k: one warp per token.  k rounds of a warp-wide argmax over
 // score = logit + bias (ties -> lower id); the winner is marked taken.
 // Weights: softmax over the k picked, from the unbiased logits.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kRouteThreads) topk_kernel(const float* __restrict__ logits,
-                                                             const float* __restrict__ bias, int T, int E, int k,
+__global__ void __launch_bounds__(kRouteThreads) topk_kernel(float* __restrict__ logits,
+                                                             const float* __restrict__ bias,
+                                                             const float* __restrict__ part, int nb,
+                                                             const float* __restrict__ off, int T, int E, int k,
                                                              int32_t* __restrict__ ids, float* __restrict__ wout) {
   __shared__ float sel_l[kRouteThreads / 32][kMaxK];
   __shared__ int sel_i[kRouteThreads / 32][kMaxK];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int t = blockIdx.x * (kRouteThreads / 32) + warp;
   if (t >= T) return;
-  const float* lrow = logits + (size_t)t * E;
+  float* lrow = logits + (size_t)t * E;
+  if (part) {
+    // finish the logits from the block parts: 0 + part_0 + part_1 + ..., then the offset
+    for (int e = lane; e < E; e += 32) {
+      float l = 0.f;
+      for (int b = 0; b < nb; ++b) l += part[((size_t)b * T + t) * E + e];
+      lrow[e] = off ? l + off[e] : l;
+    }
+    __syncwarp();
+  }
+  // the token's scores, loaded once: lane holds experts lane + 32q
+  float sc[kMaxE / 32];
+#pragma unroll
+  for (int q = 0; q < kMaxE / 32; ++q) {
+    const int e = lane + 32 * q;
+    sc[q] = e < E ? (bias ? lrow[e] + bias[e] : lrow[e]) : 0.f;
+  }
   unsigned taken = 0;
   for (int j = 0; j < k; ++j) {
     float best = -INFINITY;
     int bi = INT_MAX;
-    for (int q = 0; lane + 32 * q < E; ++q) {
-      if ((taken >> q) & 1u) continue;
+#pragma unroll
+    for (int q = 0; q < kMaxE / 32; ++q) {
       const int e = lane + 32 * q;
-      const float s = bias ? lrow[e] + bias[e] : lrow[e];
-      if (bi == INT_MAX || s > best || (s == best && e < bi)) {
-        best = s;
+      if (e >= E || ((taken >> q) & 1u)) continue;
+      const float sv = sc[q];
+      if (bi == INT_MAX || sv > best || (sv == best && e < bi)) {
+        best = sv;
         bi = e;
       }
     }
@@ -188,11 +272,10 @@ __global__ void __launch_bounds__(kRouteThreads) topk_kernel(const float* __rest
       }
     }
     if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-    if (lane == 0) {
-      sel_i[warp][j] = bi;
-      sel_l[warp][j] = lrow[bi];
-    }
+    if (lane == 0) sel_i[warp][j] = bi;
   }
+  __syncwarp();
+  if (lane < k) sel_l[warp][lane] = lrow[sel_i[warp][lane]];
   __syncwarp();
   if (lane == 0) {
     float mx = sel_l[warp][0];
@@ -219,8 +302,14 @@ extern "C" int moe_bias_table(const float* b, int E, int n_hot, float cap, float
   return MOE_OK;
 }
 
+extern "C" size_t moe_route_scratch_bytes(int T, int H, int E) {
+  if (T < 1 || H < 1 || E < 1 || T > 256) return 0;
+  return (size_t)((H + kHC - 1) / kHC) * T * E * sizeof(float);
+}
+
 extern "C" int moe_route(const void* x, const void* w_router, const float* logit_offset, const float* sel_bias,
-                         int T, int H, int E, int k, float* logits, int32_t* ids, float* w, moe_stream_t stream) {
+                         int T, int H, int E, int k, float* logits, float* scratch, int32_t* ids, float* w,
+                         moe_stream_t stream) {
   if (!x || !w_router || !ids || !w || !logits) return MOE_ERR_ARG;
   if (T < 1 || H < 8 || H % 8 || E < 1 || E > kMaxE || E % 8 || k < 1 || k > kMaxK || k > E) return MOE_ERR_ARG;
   if ((uintptr_t)x % 16 || (uintptr_t)w_router % 16) return MOE_ERR_ALIGN;
@@ -229,14 +318,25 @@ extern "C" int moe_route(const void* x, const void* w_router, const float* logit
   MOE_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
   cudaStream_t s = (cudaStream_t)stream;
   const int eb = (E + kEB - 1) / kEB;
+  const int nblk = (H + kHC - 1) / kHC;
+  const uint16_t* xb = (const uint16_t*)x;
+  const uint16_t* wb = (const uint16_t*)w_router;
+  if (scratch && moe_route_scratch_bytes(T, H, E) > 0 && ((T + 7) / 8) * eb < sms) {
+    // few tokens: every (128-row block, 32 experts, 8 tokens) is its own CTA
+    const dim3 grid(nblk, eb, (T + 7) / 8);
+    logits_block_kernel<1><<<grid, kRouteThreads, 0, s>>>(xb, wb, T, H, E, scratch);
+    MOE_LAUNCH_CHECK();
+    topk_kernel<<<(T + 7) / 8, kRouteThreads, 0, s>>>(logits, sel_bias, scratch, nblk, logit_offset, T, E, k, ids,
+                                                      w);
+    MOE_LAUNCH_CHECK();
+    return MOE_OK;
+  }
   // tokens per CTA: fewest that still give every SM a CTA, at most 64
   int ch = 8;
   while (ch > 1 && ((T + 8 * ch - 1) / (8 * ch)) * eb < sms) ch /= 2;
   const dim3 grid((T + 8 * ch - 1) / (8 * ch), eb);
   const size_t smem = (size_t)kRStages * (kHC * kEB * 2 + 8 * ch * kHC * 2);
   static bool d1[64] = {}, d2[64] = {}, d4[64] = {}, d8[64] = {};
-  const uint16_t* xb = (const uint16_t*)x;
-  const uint16_t* wb = (const uint16_t*)w_router;
   switch (ch) {
     case 1:
       MOE_CUDA_TRY(ensure_smem(logits_kernel<1>, (int)smem, d1));
@@ -256,7 +356,7 @@ extern "C" int moe_route(const void* x, const void* w_router, const float* logit
       break;
   }
   MOE_LAUNCH_CHECK();
-  topk_kernel<<<(T + 7) / 8, kRouteThreads, 0, s>>>(logits, sel_bias, T, E, k, ids, w);
+  topk_kernel<<<(T + 7) / 8, kRouteThreads, 0, s>>>(logits, sel_bias, nullptr, 0, nullptr, T, E, k, ids, w);
   MOE_LAUNCH_CHECK();
   return MOE_OK;
 }

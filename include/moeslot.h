@@ -85,17 +85,22 @@ int moe_bias_table(const float* b, int E, int n_hot, float cap, float* bias, moe
  *   w_router     device bf16 [H][E]
  *   logit_offset device fp32 [E] added to every logit after the sum, or NULL
  *   sel_bias     device fp32 [E] selection-only bias, or NULL
- *   logits       device fp32 [T][E] output (unbiased logits; also the scratch
- *                between the logits kernel and the top-k kernel)
+ *   logits       device fp32 [T][E] output (unbiased logits)
+ *   scratch      device, moe_route_scratch_bytes(T, H, E) bytes, or NULL: with
+ *                it a small batch spreads its 128-row blocks over more CTAs
+ *                (the result is the same)
  *   ids          device int32 [T][k] output, descending score, ties -> lower id
  *   w            device fp32 [T][k] output, sums to 1 per token
- * logit[t][e] is accumulated in fp32 in h order (acc = fma(x, Wr, acc) for
- * h = 0..H-1), so ids are reproducible bit for bit.
+ * logit[t][e] is accumulated in fp32 in one fixed order: h is cut into
+ * blocks of 128 rows, each block summed from 0 with fma in h order, and the
+ * block sums added in block order; so ids are reproducible bit for bit.
  * Errors: MOE_ERR_ARG on NULL pointers or shapes out of range (H % 8 and
  * E % 8 must be 0); MOE_ERR_ALIGN if x or w_router is not 16-byte aligned.
  */
 int moe_route(const void* x, const void* w_router, const float* logit_offset, const float* sel_bias,
-              int T, int H, int E, int k, float* logits, int32_t* ids, float* w, moe_stream_t stream);
+              int T, int H, int E, int k, float* logits, float* scratch, int32_t* ids, float* w,
+              moe_stream_t stream);
+size_t moe_route_scratch_bytes(int T, int H, int E);
 
 /*
  * Permute: group the n = T*k routing slots by expert.

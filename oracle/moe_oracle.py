@@ -24,8 +24,10 @@ Sources (web pages; cited by title and section):
           missing experts is added, which gives exactly the full result.
 
 Precision.  Router logits decide integers (the top-k ids), so they are taken
-in fp32 in one fixed order that the kernels follow as well: for each (t, e),
-acc = 0 then acc = fma(x[t][h], Wr[h][e], acc) for h = 0..H-1.  A bf16 x bf16
+in fp32 in one fixed order that the kernels follow as well: h is cut into
+consecutive blocks of LOGIT_BLOCK = 128; within block b, part_b = 0 then
+part_b = fma(x[t][h], Wr[h][e], part_b) for h ascending; then
+logit = 0 + part_0 + part_1 + ... in block order (fp32 adds).  A bf16 x bf16
 product is exact in fp32, so "multiply then add in fp32" is that same fma.
 Selection compares fp32 scores logit + bias (one IEEE add).  Everything else
 (softmax weights, the SwiGLU expert FFN, the combine) is evaluated in fp64.
@@ -64,8 +66,11 @@ RESIDENT, GATHER, ZERO_RETURN = 0, 1, 2
 # Routing  [SGB "The method in five lines"]
 # ----------------------------------------------------------------------------
 
+LOGIT_BLOCK = 128
+
+
 def router_logits(x: np.ndarray, wr: np.ndarray, logit_offset=None) -> np.ndarray:
-    """logit[t][e] = sum_h x[t][h] * Wr[h][e], fp32, h ascending.
+    """logit[t][e] = sum_h x[t][h] * Wr[h][e] in fp32, blocked order (see above).
 
     ``x`` [T][H] and ``wr`` [H][E] hold bf16 values (as float32 arrays).  The
     optional per-expert ``logit_offset`` [E] is added after the sum.
@@ -74,8 +79,11 @@ def router_logits(x: np.ndarray, wr: np.ndarray, logit_offset=None) -> np.ndarra
     wr = np.asarray(wr, dtype=np.float32)
     T, H = x.shape
     acc = np.zeros((T, wr.shape[1]), dtype=np.float32)
-    for h in range(H):
-        acc += x[:, h:h + 1] * wr[h:h + 1, :]
+    for h0 in range(0, H, LOGIT_BLOCK):
+        part = np.zeros_like(acc)
+        for h in range(h0, min(H, h0 + LOGIT_BLOCK)):
+            part += x[:, h:h + 1] * wr[h:h + 1, :]
+        acc += part
     if logit_offset is not None:
         acc = acc + np.asarray(logit_offset, dtype=np.float32)[None, :]
     return acc

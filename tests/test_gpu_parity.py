@@ -56,8 +56,9 @@ ROUTE_CASES = [
 ]
 
 
+@pytest.mark.parametrize("blocked", [True, False], ids=["block_ctas", "ring"])
 @pytest.mark.parametrize("name,cfg,cap,offset", ROUTE_CASES, ids=[c[0] for c in ROUTE_CASES])
-def test_route_parity(name, cfg, cap, offset):
+def test_route_parity(name, cfg, cap, offset, blocked):
     x = C.draw_x(cfg, DEV)
     wr = C.draw_router(cfg, DEV)
     off = C.draw_logit_offset(cfg, DEV) if offset else None
@@ -66,7 +67,7 @@ def test_route_parity(name, cfg, cap, offset):
         b, _ = C.draw_brightness(cfg)
         bias_np = O.bias_table(b, cfg.n_hot, cap)
         bias_d = M.bias_table(torch.from_numpy(b).to(DEV), cfg.n_hot, cap)
-    ids, w, logits = M.route(x, wr, cfg.k, off, bias_d, return_logits=True)
+    ids, w, logits = M.route(x, wr, cfg.k, off, bias_d, return_logits=True, blocked=blocked)
     torch.cuda.synchronize()
     want_logits = O.router_logits(_np(x.float()), _np(wr.float()), None if off is None else _np(off))
     assert np.array_equal(_np(logits), want_logits), "logits differ"

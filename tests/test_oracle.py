@@ -37,10 +37,14 @@ def _bf16(a):
 
 def test_logit_order_golden():
     g = _gold("logit_order.json")
-    x = np.array([g["x"]], dtype=np.float32)
-    w = np.array(g["w"], dtype=np.float32)[:, None]
-    assert O.router_logits(x, w)[0, 0] == np.float32(g["logit"])
-    assert g["exact_sum"] == sum(a * b for a, b in zip(g["x"], g["w"]))
+    assert O.LOGIT_BLOCK == g["block"]
+    for case in g["cases"]:
+        x = np.zeros((1, case["H"]), dtype=np.float32)
+        for h, v in case["x"].items():
+            x[0, int(h)] = v
+        w = np.ones((case["H"], 1), dtype=np.float32)
+        assert O.router_logits(x, w)[0, 0] == np.float32(case["logit"])
+        assert case["exact_sum"] == float(x.astype(np.float64).sum())
 
 
 def test_logits_exact_on_small_integers():
