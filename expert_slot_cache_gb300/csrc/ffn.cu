@@ -410,11 +410,11 @@ __global__ void __launch_bounds__(kTmaThreads, 1) ffn_tma_kernel(const FfnArgs a
   const int tiles = kDown ? a.H / kDTile : a.I / kGUTile;
   const int items = *a.n_list * tiles;
   const int nkc = K / kKB;
-  // a contiguous, balanced range of items per CTA: consecutive items usually
-  // share an expert, so its staged activations are reused
-  const int q = items / gridDim.x, rem = items % gridDim.x;
-  const int beg = blockIdx.x * q + min((int)blockIdx.x, rem);
-  const int end = beg + q + ((int)blockIdx.x < rem ? 1 : 0);
+  // Items are expert-major and dealt round-robin: at any moment neighbouring
+  // CTAs stream neighbouring column tiles of the same weight rows, which keeps
+  // DRAM rows open (a contiguous range per CTA would put ~150 different
+  // experts' 64-byte slices in flight at once and halves the bandwidth).
+  const int beg = blockIdx.x, step = gridDim.x;
 
   if (warp == kTmaConsumers / 32) {
     // producer
@@ -422,7 +422,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) ffn_tma_kernel(const FfnArgs a
       uint32_t it = 0;
       int last_use[kStages];
       for (int s = 0; s < kStages; ++s) last_use[s] = -1;
-      for (int item = beg; item < end && !*abort_flag; ++item) {
+      for (int item = beg; item < items && !*abort_flag; item += step) {
         const int li = item / tiles, tile = item - li * tiles;
         const int e = a.list_e[li];
         if (e < 0 || e >= a.E) continue;
@@ -460,7 +460,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) ffn_tma_kernel(const FfnArgs a
     // consumers
     uint32_t it = 0;
     int staged_e = -1, staged_p0 = -1;
-    for (int item = beg; item < end; ++item) {
+    for (int item = beg; item < items; item += step) {
       const int li = item / tiles, tile = item - li * tiles;
       const int e = a.list_e[li];
       if (e < 0 || e >= a.E) {
