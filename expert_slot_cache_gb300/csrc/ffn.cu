@@ -222,7 +222,7 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(const FfnArgs a) {
 // H*I bf16: gate of slot s = matrix 3s, up = 3s+1 (both [H][I]), down = 3s+2
 // ([I][H]).  A stage holds kKB rows of the tile (16 KB).
 // ---------------------------------------------------------------------------
-constexpr int kStages = 6;
+constexpr int kStages = 10;
 constexpr int kKB = 128;
 constexpr int kStageBytes = 16384;
 constexpr int kTmaConsumers = 512;             // 16 consumer warps
@@ -511,11 +511,11 @@ int launch_ffn(const FfnArgs& a, int max_list, cudaStream_t stream, Prof* prof) 
   MOE_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
   const int g1 = std::min(max_list * (a.I / kGUTile), sms);
   const int g2 = std::min(max_list * (a.H / kDTile), sms);
-  const bool tma = a.pool_only && a.S > 0 && a.H % kKB == 0 && a.I % kKB == 0 && tma_smem_bytes(a.H) <= 200 * 1024;
+  const bool tma = a.pool_only && a.S > 0 && a.H % kKB == 0 && a.I % kKB == 0 && tma_smem_bytes(a.H) <= 220 * 1024;
   if (tma) {
     static bool done_t1[64] = {}, done_t2[64] = {};
-    MOE_CUDA_TRY(ensure_smem(ffn_tma_kernel<false>, 200 * 1024, done_t1));
-    MOE_CUDA_TRY(ensure_smem(ffn_tma_kernel<true>, 200 * 1024, done_t2));
+    MOE_CUDA_TRY(ensure_smem(ffn_tma_kernel<false>, 220 * 1024, done_t1));
+    MOE_CUDA_TRY(ensure_smem(ffn_tma_kernel<true>, 220 * 1024, done_t2));
     const size_t mat = (size_t)a.H * a.I;
     CUtensorMap m_gu, m_d;
     const uint64_t d_gu[3] = {(uint64_t)a.I, (uint64_t)a.H, 3ull * a.S};

@@ -36,6 +36,8 @@ constexpr int kPStageBytes = kPAbytes + kPBbytes;  // 48 KB
 constexpr int kPThreads = 192;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kPrefillMinRows = 4096;
+// per epilogue warp: a 32 x 33 fp32 transpose buffer (padded: conflict-free)
+constexpr int kEpiBuf = 32 * 33;
 
 // Instruction descriptor, kind::f16: D fp32, A and B bf16, A K-major,
 // B MN-major, N = 256, M = 128.
@@ -130,6 +132,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const Prefil
   uint64_t* tfull = empty + kPStages;
   uint64_t* tempty = tfull + 2;
   uint64_t* done = tempty + 2;
+  float* epi = reinterpret_cast<float*>(full + 16);  // after the 16 barrier words: [4 warps][32][33]
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   __shared__ int s_pre[kMaxE + 1];
@@ -263,10 +266,12 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const Prefil
         set_status(a.status, MOE_DEV_TIMEOUT);
       }
       tc_fence_after();
-      const int row = q * 32 + lane;
-      const bool valid = m * kPM + row < ne && !*abort_flag;
-      const size_t p = (size_t)a.offset[e] + (size_t)m * kPM + row;
+      // rows of this warp: m*128 + q*32 + r (r = 0..31); thread `lane` holds row q*32 + lane
+      const int rbase = m * kPM + q * 32;
+      const int nvalid = *abort_flag ? 0 : max(0, min(32, ne - rbase));
+      const size_t p0 = (size_t)a.offset[e] + rbase;
       const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + acc * kPN;
+      float* buf = epi + (warp & 3) * kEpiBuf;
       if (kMode == 0) {
         const int n0 = ct * 128;
 #pragma unroll 1
@@ -275,21 +280,21 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const Prefil
           tmem_ld32(taddr + 32 * c, g);
           tmem_ld32(taddr + 128 + 32 * c, u);
           tmem_ld_wait();
-          if (valid) {
-            uint4* dst = reinterpret_cast<uint4*>(a.hb + p * a.I + n0 + 32 * c);
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              uint32_t w[4];
-#pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                const float g0 = g[8 * v + 2 * j], g1 = g[8 * v + 2 * j + 1];
-                const float h0 = g0 / (1.f + expf(-g0)) * u[8 * v + 2 * j];
-                const float h1 = g1 / (1.f + expf(-g1)) * u[8 * v + 2 * j + 1];
-                w[j] = uint32_t(f32_to_bf16(h0)) | (uint32_t(f32_to_bf16(h1)) << 16);
-              }
-              dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
+          for (int j = 0; j < 32; ++j) buf[lane * 33 + j] = g[j] / (1.f + expf(-g[j])) * u[j];
+          __syncwarp();
+          // two rows per instruction: lanes 0-15 row r, 16-31 row r+1, 2 columns each (64 B per row)
+          const int half = lane >> 4, col = 2 * (lane & 15);
+#pragma unroll 4
+          for (int r = 0; r < 32; r += 2) {
+            const int rr = r + half;
+            if (rr < nvalid) {
+              const uint32_t w = uint32_t(f32_to_bf16(buf[rr * 33 + col])) |
+                                 (uint32_t(f32_to_bf16(buf[rr * 33 + col + 1])) << 16);
+              *reinterpret_cast<uint32_t*>(a.hb + (p0 + rr) * a.I + n0 + 32 * c + col) = w;
             }
           }
+          __syncwarp();
         }
       } else {
         const int o0 = ct * kPN;
@@ -298,11 +303,14 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const Prefil
           float v[32];
           tmem_ld32(taddr + 32 * c, v);
           tmem_ld_wait();
-          if (valid) {
-            float4* dst = reinterpret_cast<float4*>(a.y + p * a.H + o0 + 32 * c);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-          }
+          for (int j = 0; j < 32; ++j) buf[lane * 33 + j] = v[j];
+          __syncwarp();
+          // one row per instruction: 32 lanes x 4 B = 128 contiguous bytes
+#pragma unroll 4
+          for (int r = 0; r < 32; ++r)
+            if (r < nvalid) a.y[(p0 + r) * a.H + o0 + 32 * c + lane] = buf[r * 33 + lane];
+          __syncwarp();
         }
       }
       tc_fence_before();
@@ -331,7 +339,9 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __rest
   }
 }
 
-static size_t prefill_smem_bytes() { return 1024 + (size_t)kPStages * kPStageBytes + 16 * sizeof(uint64_t); }
+static size_t prefill_smem_bytes() {
+  return 1024 + (size_t)kPStages * kPStageBytes + 16 * sizeof(uint64_t) + 4 * kEpiBuf * sizeof(float);
+}
 
 bool prefill_eligible(const FfnArgs& a, int n) {
   return a.pool_only && a.S > 0 && a.xp && a.hb && n >= kPrefillMinRows && a.H % kPN == 0 && a.I % 128 == 0 &&

@@ -229,18 +229,32 @@ __global__ void __launch_bounds__(kRouteThreads) topk_kernel(float* __restrict__
   __shared__ float sel_l[kRouteThreads / 32][kMaxK];
   __shared__ int sel_i[kRouteThreads / 32][kMaxK];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int t = blockIdx.x * (kRouteThreads / 32) + warp;
+  const int tb = blockIdx.x * (kRouteThreads / 32);
+  if (part) {
+    // finish this CTA's logits from the block parts: 0 + part_0 + part_1 + ...
+    // (all parts loaded before the in-order sum), then the offset
+    const int nt = min(kRouteThreads / 32, T - tb);
+    for (int v = threadIdx.x; v < nt * E; v += kRouteThreads) {
+      const int tl = v / E, e = v - tl * E;
+      const float* pp = part + (size_t)(tb + tl) * E + e;
+      const size_t bstride = (size_t)T * E;
+      float l = 0.f;
+      int b = 0;
+      for (; b + 8 <= nb; b += 8) {
+        float pv[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) pv[u] = pp[(size_t)(b + u) * bstride];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) l += pv[u];
+      }
+      for (; b < nb; ++b) l += pp[(size_t)b * bstride];
+      logits[(size_t)(tb + tl) * E + e] = off ? l + off[e] : l;
+    }
+    __syncthreads();
+  }
+  const int t = tb + warp;
   if (t >= T) return;
   float* lrow = logits + (size_t)t * E;
-  if (part) {
-    // finish the logits from the block parts: 0 + part_0 + part_1 + ..., then the offset
-    for (int e = lane; e < E; e += 32) {
-      float l = 0.f;
-      for (int b = 0; b < nb; ++b) l += part[((size_t)b * T + t) * E + e];
-      lrow[e] = off ? l + off[e] : l;
-    }
-    __syncwarp();
-  }
   // the token's scores, loaded once: lane holds experts lane + 32q
   float sc[kMaxE / 32];
 #pragma unroll
