@@ -239,53 +239,61 @@ def _prof_times(p, evs) -> dict:
 def time_steps(wl: Workload, steps: int, warmup: int, dist=None, clocks=None, profile=True, graph=True):
     """K steps timed between CUDA events after W eager warm-ups.
 
-    With ``graph`` the K steps are captured into one CUDA graph first and the
-    timed region is one replay (inputs differ per step; the cache state keeps
-    evolving on the device).  Per-kernel live times come from the timing
-    events the layer forward records around each of its launches.
+    With ``graph`` the K steps are captured into one CUDA graph and the timed
+    region is one replay (inputs differ per step; the cache state keeps
+    evolving on the device).  The timed graph has no instrumentation.  With
+    ``profile``, a second graph of the next K steps carries the timing events
+    that the layer forward records around each of its launches; those give
+    the per-kernel live times (the event nodes add a little latency, so that
+    graph is not used for the step time).
     """
     M = wl.M
     for i in range(warmup):
         wl.step(i)
-    n_chunks = (wl.cfg.T + wl.chunk() - 1) // wl.chunk()
-    pairs = 4 + 12 * n_chunks
-    profs = [_make_prof(M, pairs) for _ in range(steps)] if profile else [None] * steps
     torch.cuda.synchronize()
-    g = None
-    if graph:
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, capture_error_mode="relaxed"):
-            for i in range(steps):
-                wl.step(warmup + i, prof=profs[i][0] if profile else None)
-        torch.cuda.synchronize()
     misses0, gathered0 = int(wl.layer.stats[0]), int(wl.layer.stats[2])
+
+    def run(first, prof_list):
+        g = None
+        if graph:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, capture_error_mode="relaxed"):
+                for i in range(steps):
+                    wl.step(first + i, prof=None if prof_list is None else prof_list[i][0])
+            torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        if graph:
+            g.replay()
+        else:
+            for i in range(steps):
+                wl.step(first + i, prof=None if prof_list is None else prof_list[i][0])
+        e.record()
+        torch.cuda.synchronize()
+        return s.elapsed_time(e)
+
     _barrier(dist)
     if clocks:
         clocks.start()
-    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    s.record()
-    if graph:
-        g.replay()
-    else:
-        for i in range(steps):
-            wl.step(warmup + i, prof=profs[i][0] if profile else None)
-    e.record()
-    torch.cuda.synchronize()
+    ms = run(warmup, None)
     cl = clocks.stop() if clocks else None
     _barrier(dist)
-    ms = _max_over_ranks(s.elapsed_time(e), dist)
+    ms = _max_over_ranks(ms, dist)
+    misses = int(wl.layer.stats[0]) - misses0
+    gathered = int(wl.layer.stats[2]) - gathered0
     kern = {n: 0.0 for n in PROF_NAMES}
     launches = {n: 0 for n in PROF_NAMES}
+    ms_prof = None
     if profile:
+        n_chunks = (wl.cfg.T + wl.chunk() - 1) // wl.chunk()
+        profs = [_make_prof(M, 4 + 12 * n_chunks) for _ in range(steps)]
+        ms_prof = run(warmup + steps, profs)
         for p, evs, _, _ in profs:
             for n, v in _prof_times(p, evs).items():
                 kern[n] += sum(v)
                 launches[n] += len(v)
-    misses = int(wl.layer.stats[0]) - misses0
-    gathered = int(wl.layer.stats[2]) - gathered0
-    del g
-    return {"ms": ms, "kern_ms": kern, "launches": launches, "clocks": cl, "misses": misses,
-            "gathered_bytes": gathered, "graph": graph}
+    return {"ms": ms, "ms_instrumented": ms_prof, "kern_ms": kern, "launches": launches, "clocks": cl,
+            "misses": misses, "gathered_bytes": gathered, "graph": graph}
 
 
 def count_unique_all(wl: Workload, steps: int, warmup: int) -> int:
@@ -447,20 +455,21 @@ def main():
             c = C.qwen(int(w[len("gather_T"):]), S=64)
         else:
             raise SystemExit(f"unknown workload {w}")
-        wl = Workload(c, args.steps + args.warmup, dev)
+        wl = Workload(c, 2 * args.steps + args.warmup, dev)
         r = time_steps(wl, args.steps, args.warmup)
         if rank == 0:
             print(json.dumps({"workload": w, "ms_per_step": r["ms"] / args.steps,
+                              "ms_per_step_instrumented": r["ms_instrumented"] / args.steps,
                               "tokens_per_s": c.T * args.steps / (r["ms"] * 1e-3),
                               "kernels_ms_per_step": {n: v / args.steps for n, v in r["kern_ms"].items()}}))
         return
     cfg = main_config()
     K, W = args.steps, args.warmup
 
-    wl = Workload(cfg, K + W, dev)
+    wl = Workload(cfg, 2 * K + W, dev)
     clocks = Clocks(local)
     r = time_steps(wl, K, W, dist, clocks)
-    units = count_unique_all(wl, K, W)
+    units = count_unique_all(wl, K, W + K)  # expert units of the instrumented steps (kernel times)
     value = ws * cfg.T * K / (r["ms"] * 1e-3)
     link_peak = host_link_peak(dev)
     kern = r["kern_ms"]
@@ -492,18 +501,18 @@ def main():
         # all-resident control: the HBM roofline of the decode FFN
         for T in (1, 8, 64):
             c2 = C.qwen(T, S=128, mode=C.MODE_RESIDENT)
-            w2 = Workload(c2, 10 + 3, dev)
+            w2 = Workload(c2, 2 * 10 + 3, dev)
             r2 = time_steps(w2, 10, 3)
-            u2 = count_unique_all(w2, 10, 3)
+            u2 = count_unique_all(w2, 10, 3 + 10)
             var[f"all_resident_T{T}"] = {"tokens_per_s": T * 10 / (r2["ms"] * 1e-3), "ms_per_step": r2["ms"] / 10,
                                          "kernels_ms_per_step": {n: v / 10 for n, v in r2["kern_ms"].items()},
                                          "ffn_hbm": ffn_roofline(w2, r2, u2, peaks),
-                                         "layer_hbm_frac": u2 * c2.slab_bytes / (r2["ms"] * 1e-3) / 1e9
-                                         / peaks["hbm_gbs"]}
+                                         "layer_hbm_frac": count_unique_all(w2, 10, 3) * c2.slab_bytes
+                                         / (r2["ms"] * 1e-3) / 1e9 / peaks["hbm_gbs"]}
             del w2
         # prefill: all experts resident, T=4096, skewed groups (tcgen05 grouped GEMMs)
         cp = C.PREFILL
-        wp = Workload(cp, 3 + 3, dev)
+        wp = Workload(cp, 2 * 3 + 3, dev)
         rp = time_steps(wp, 3, 3)
         flops = 6.0 * cp.T * cp.k * cp.H * cp.I
         t_ffn = (rp["kern_ms"]["ffn_gateup"] + rp["kern_ms"]["ffn_down"]) * 1e-3 / 3
@@ -519,7 +528,7 @@ def main():
         torch.cuda.empty_cache()
         for T in (1, 8, 32):
             c3 = C.qwen(T, S=64)
-            w3 = Workload(c3, 10 + 3, dev)
+            w3 = Workload(c3, 2 * 10 + 3, dev)
             r3 = time_steps(w3, 10, 3, profile=False)
             var[f"gather_T{T}"] = {"tokens_per_s": T * 10 / (r3["ms"] * 1e-3), "ms_per_step": r3["ms"] / 10,
                                    "misses_per_step": r3["misses"] / 10}
