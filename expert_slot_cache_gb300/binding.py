@@ -46,7 +46,8 @@ class LayerArgs(ctypes.Structure):
                 ("e2s", c_void_p), ("s2e", c_void_p), ("prio", c_void_p), ("stamp", c_void_p),
                 ("ids", c_void_p), ("w", c_void_p), ("out", c_void_p), ("out_res", c_void_p),
                 ("out_miss", c_void_p), ("stats", c_void_p), ("dev_status", c_void_p),
-                ("workspace", c_void_p), ("workspace_bytes", c_size_t), ("prof", POINTER(Prof))]
+                ("workspace", c_void_p), ("workspace_bytes", c_size_t), ("prof", POINTER(Prof)),
+                ("affinity", c_float)]
 
 
 def _sig(name, argtypes, restype=c_int):
@@ -60,7 +61,7 @@ V = c_void_p
 I32 = c_int
 _status_str = _sig("moe_status_str", [c_int], ctypes.c_char_p)
 _bias_table = _sig("moe_bias_table", [V, I32, I32, c_float, V, V])
-_route = _sig("moe_route", [V, V, V, V, I32, I32, I32, I32, V, V, V, V, V])
+_route = _sig("moe_route", [V, V, V, V, V, c_float, I32, I32, I32, I32, V, V, V, V, V])
 _route_scratch = _sig("moe_route_scratch_bytes", [I32, I32, I32], c_size_t)
 _permute = _sig("moe_permute", [V, I32, I32, V, V, V, V, V, V, V, V, V])
 _permute_scratch = _sig("moe_permute_scratch_bytes", [I32, I32], c_size_t)
@@ -111,7 +112,8 @@ def bias_table(b: torch.Tensor, n_hot: int, cap: float, stream=None) -> torch.Te
     return out
 
 
-def route(x, w_router, k, logit_offset=None, sel_bias=None, return_logits=False, stream=None, blocked=True):
+def route(x, w_router, k, logit_offset=None, sel_bias=None, return_logits=False, stream=None, blocked=True,
+          e2s=None, affinity=0.0):
     T, H = x.shape
     E = w_router.shape[1]
     ids = torch.empty(T, k, dtype=torch.int32, device=x.device)
@@ -119,8 +121,8 @@ def route(x, w_router, k, logit_offset=None, sel_bias=None, return_logits=False,
     logits = torch.empty(T, E, dtype=torch.float32, device=x.device)
     nb = int(_route_scratch(T, H, E)) if blocked else 0
     scratch = torch.empty(max(nb // 4, 1), dtype=torch.float32, device=x.device) if nb else None
-    _ck(_route(_p(x), _p(w_router), _p(logit_offset), _p(sel_bias), T, H, E, k, _p(logits), _p(scratch), _p(ids),
-               _p(w), _s(stream)), "moe_route")
+    _ck(_route(_p(x), _p(w_router), _p(logit_offset), _p(sel_bias), _p(e2s), affinity, T, H, E, k, _p(logits),
+               _p(scratch), _p(ids), _p(w), _s(stream)), "moe_route")
     return (ids, w, logits) if return_logits else (ids, w)
 
 
@@ -245,13 +247,14 @@ class SlotCachedMoELayer:
     """
 
     def __init__(self, w_router, pool, k, I, mode, policy=POLICY_LRU, host_slabs=None, state=None,
-                 logit_offset=None, sel_bias=None, max_tokens=64, side_stream=True):
+                 logit_offset=None, sel_bias=None, max_tokens=64, side_stream=True, affinity=0.0):
         self.w_router, self.pool, self.k, self.I = w_router, pool, k, I
         self.H, self.E = w_router.shape
         self.S = pool.shape[0]
         self.mode, self.policy = mode, policy
         self.host_slabs, self.state = host_slabs, state
         self.logit_offset, self.sel_bias = logit_offset, sel_bias
+        self.affinity = float(affinity)
         dev = pool.device
         self.stats = torch.zeros(4, dtype=torch.int64, device=dev)
         self.dev_status = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -279,7 +282,7 @@ class SlotCachedMoELayer:
                       _ptr(st.prio if st else None), _ptr(st.stamp if st else None),
                       ids.data_ptr(), w.data_ptr(), out.data_ptr(), _ptr(out_res), _ptr(out_miss),
                       self.stats.data_ptr(), self.dev_status.data_ptr(), self.workspace.data_ptr(),
-                      self.workspace.numel(), ctypes.pointer(prof) if prof is not None else None)
+                      self.workspace.numel(), ctypes.pointer(prof) if prof is not None else None, self.affinity)
         main = torch.cuda.current_stream() if stream is None else stream
         # the library forks to and joins back from the side stream itself
         _ck(_layer(ctypes.byref(a), c_void_p(main.cuda_stream),

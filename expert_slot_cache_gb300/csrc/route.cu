@@ -223,6 +223,7 @@ __global__ void __launch_bounds__(kRouteThreads) logits_block_kernel(const uint1
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kRouteThreads) topk_kernel(float* __restrict__ logits,
                                                              const float* __restrict__ bias,
+                                                             const int32_t* __restrict__ e2s, float affinity,
                                                              const float* __restrict__ part, int nb,
                                                              const float* __restrict__ off, int T, int E, int k,
                                                              int32_t* __restrict__ ids, float* __restrict__ wout) {
@@ -260,7 +261,12 @@ __global__ void __launch_bounds__(kRouteThreads) topk_kernel(float* __restrict__
 #pragma unroll
   for (int q = 0; q < kMaxE / 32; ++q) {
     const int e = lane + 32 * q;
-    sc[q] = e < E ? (bias ? lrow[e] + bias[e] : lrow[e]) : 0.f;
+    float v = 0.f;
+    if (e < E) {
+      v = bias ? lrow[e] + bias[e] : lrow[e];
+      if (e2s && affinity != 0.f && e2s[e] >= 0) v = v + affinity;  // live-cache affinity
+    }
+    sc[q] = v;
   }
   unsigned taken = 0;
   for (int j = 0; j < k; ++j) {
@@ -322,8 +328,8 @@ extern "C" size_t moe_route_scratch_bytes(int T, int H, int E) {
 }
 
 extern "C" int moe_route(const void* x, const void* w_router, const float* logit_offset, const float* sel_bias,
-                         int T, int H, int E, int k, float* logits, float* scratch, int32_t* ids, float* w,
-                         moe_stream_t stream) {
+                         const int32_t* e2s, float affinity, int T, int H, int E, int k, float* logits,
+                         float* scratch, int32_t* ids, float* w, moe_stream_t stream) {
   if (!x || !w_router || !ids || !w || !logits) return MOE_ERR_ARG;
   if (T < 1 || H < 8 || H % 8 || E < 1 || E > kMaxE || E % 8 || k < 1 || k > kMaxK || k > E) return MOE_ERR_ARG;
   if ((uintptr_t)x % 16 || (uintptr_t)w_router % 16) return MOE_ERR_ALIGN;
@@ -340,8 +346,8 @@ extern "C" int moe_route(const void* x, const void* w_router, const float* logit
     const dim3 grid(nblk, eb, (T + 7) / 8);
     logits_block_kernel<1><<<grid, kRouteThreads, 0, s>>>(xb, wb, T, H, E, scratch);
     MOE_LAUNCH_CHECK();
-    topk_kernel<<<(T + 7) / 8, kRouteThreads, 0, s>>>(logits, sel_bias, scratch, nblk, logit_offset, T, E, k, ids,
-                                                      w);
+    topk_kernel<<<(T + 7) / 8, kRouteThreads, 0, s>>>(logits, sel_bias, e2s, affinity, scratch, nblk, logit_offset,
+                                                      T, E, k, ids, w);
     MOE_LAUNCH_CHECK();
     return MOE_OK;
   }
@@ -370,7 +376,8 @@ extern "C" int moe_route(const void* x, const void* w_router, const float* logit
       break;
   }
   MOE_LAUNCH_CHECK();
-  topk_kernel<<<(T + 7) / 8, kRouteThreads, 0, s>>>(logits, sel_bias, nullptr, 0, nullptr, T, E, k, ids, w);
+  topk_kernel<<<(T + 7) / 8, kRouteThreads, 0, s>>>(logits, sel_bias, e2s, affinity, nullptr, 0, nullptr, T, E, k,
+                                                    ids, w);
   MOE_LAUNCH_CHECK();
   return MOE_OK;
 }

@@ -77,7 +77,7 @@ const char* moe_status_str(int status);
 int moe_bias_table(const float* b, int E, int n_hot, float cap, float* bias, moe_stream_t stream);
 
 /*
- * Router: logits, top-k by logit + bias, softmax weights over the picked k.
+ * Router: logits, top-k by logit + bias (+ affinity), softmax weights over the picked k.
  * Source: "Nudge, don't cut" (PGO-SGB), "The method in five lines" (pick
  * top-k by logit + bias; weights are the router's own softmax over the k
  * picked, from the unbiased logits).
@@ -85,6 +85,11 @@ int moe_bias_table(const float* b, int E, int n_hot, float cap, float* bias, moe
  *   w_router     device bf16 [H][E]
  *   logit_offset device fp32 [E] added to every logit after the sum, or NULL
  *   sel_bias     device fp32 [E] selection-only bias, or NULL
+ *   e2s, affinity  live-cache affinity ("Nudge, don't cut", "Then Maya's own
+ *                knob beat ours"): with e2s (device int32 [E], the cache's
+ *                expert -> slot table) and affinity != 0, experts with
+ *                e2s[e] >= 0 get `affinity` added to their selection score
+ *                (after the bias, fp32).  NULL / 0 = off.
  *   logits       device fp32 [T][E] output (unbiased logits)
  *   scratch      device, moe_route_scratch_bytes(T, H, E) bytes, or NULL: with
  *                it a small batch spreads its 128-row blocks over more CTAs
@@ -98,8 +103,8 @@ int moe_bias_table(const float* b, int E, int n_hot, float cap, float* bias, moe
  * E % 8 must be 0); MOE_ERR_ALIGN if x or w_router is not 16-byte aligned.
  */
 int moe_route(const void* x, const void* w_router, const float* logit_offset, const float* sel_bias,
-              int T, int H, int E, int k, float* logits, float* scratch, int32_t* ids, float* w,
-              moe_stream_t stream);
+              const int32_t* e2s, float affinity, int T, int H, int E, int k, float* logits, float* scratch,
+              int32_t* ids, float* w, moe_stream_t stream);
 size_t moe_route_scratch_bytes(int T, int H, int E);
 
 /*
@@ -313,6 +318,7 @@ typedef struct moe_layer_args {
   void* workspace;           /* device scratch, moe_layer_workspace_bytes() */
   size_t workspace_bytes;
   moe_prof* prof;            /* host struct, or NULL: per-kernel timing events */
+  float affinity;            /* live-cache affinity lambda (0 = off); uses e2s before this step's manage */
 } moe_layer_args;
 
 /*

@@ -106,10 +106,18 @@ def bias_table(b: np.ndarray, n_hot: int, cap: float) -> np.ndarray:
     return out
 
 
-def select_topk(logits: np.ndarray, k: int, bias=None) -> np.ndarray:
-    """ids[t][0..k-1]: the k largest fp32 scores logit + bias, descending, ties -> lower id."""
+def select_topk(logits: np.ndarray, k: int, bias=None, resident=None, affinity: float = 0.0) -> np.ndarray:
+    """ids[t][0..k-1]: the k largest fp32 scores, descending, ties -> lower id.
+
+    score = logit + bias (when a bias is given), then + affinity for experts
+    resident in VRAM right now (live-cache affinity: "Nudge, don't cut",
+    "Then Maya's own knob beat ours"), each add in fp32.
+    """
     logits = np.asarray(logits, dtype=np.float32)
     scores = logits if bias is None else (logits + np.asarray(bias, dtype=np.float32)[None, :])
+    if resident is not None and affinity != 0.0:
+        lam = np.where(np.asarray(resident, dtype=bool), np.float32(affinity), np.float32(0.0)).astype(np.float32)
+        scores = np.where(lam[None, :] != 0, scores + lam[None, :], scores).astype(np.float32)
     T, E = scores.shape
     ids = np.empty((T, k), dtype=np.int32)
     for t in range(T):
@@ -129,9 +137,9 @@ def route_weights(logits: np.ndarray, ids: np.ndarray) -> np.ndarray:
     return w
 
 
-def route(x, wr, k, logit_offset=None, bias=None):
+def route(x, wr, k, logit_offset=None, bias=None, resident=None, affinity=0.0):
     logits = router_logits(x, wr, logit_offset)
-    ids = select_topk(logits, k, bias)
+    ids = select_topk(logits, k, bias, resident, affinity)
     return ids, route_weights(logits, ids), logits
 
 
@@ -321,7 +329,7 @@ def combine(y, w, pos, T, k, resident=None):
 # ----------------------------------------------------------------------------
 
 def layer_forward(x, wr, host, H, I, k, mode, policy=LRU, state=None, pool=None,
-                  logit_offset=None, bias=None):
+                  logit_offset=None, bias=None, affinity=0.0):
     """One MoE layer forward with the slot cache.
 
     ``host`` [E][3HI] holds every expert (authoritative copy); ``pool``
@@ -332,7 +340,8 @@ def layer_forward(x, wr, host, H, I, k, mode, policy=LRU, state=None, pool=None,
     x = np.asarray(x, dtype=np.float32)
     T = x.shape[0]
     E = wr.shape[1]
-    ids, w, logits = route(x, wr, k, logit_offset, bias)
+    resident = None if (state is None or affinity == 0.0) else state.e2s >= 0
+    ids, w, logits = route(x, wr, k, logit_offset, bias, resident, affinity)
     out = np.zeros((T, H))
     out_res = np.zeros((T, H))
     out_miss = np.zeros((T, H))

@@ -42,11 +42,12 @@ def test_host_side_argument_errors(lib):
     p = ctypes.cast(buf, ctypes.c_void_p)
     null = ctypes.c_void_p(0)
     # NULL inputs
-    assert lib.moe_route(null, null, null, null, 4, 256, 16, 2, null, null, null, null, null) == -1
+    f0 = ctypes.c_float(0.0)
+    assert lib.moe_route(null, null, null, null, null, f0, 4, 256, 16, 2, null, null, null, null, null) == -1
     # k > E
-    assert lib.moe_route(p, p, null, null, 4, 256, 8, 9, p, null, p, p, null) == -1
+    assert lib.moe_route(p, p, null, null, null, f0, 4, 256, 8, 9, p, null, p, p, null) == -1
     # logits buffer is required
-    assert lib.moe_route(p, p, null, null, 4, 256, 16, 2, null, null, p, p, null) == -1
+    assert lib.moe_route(p, p, null, null, null, f0, 4, 256, 16, 2, null, null, p, p, null) == -1
     # a step larger than the pool when the policy can evict
     assert lib.moe_cache_manage(p, 65, 128, 64, 0, p, p, p, p, p, p, p, null, null, null, null, null) == -2
     # bad policy

@@ -401,3 +401,52 @@ def test_expert_ffn_tensor_core_parity(T, skew):
     for e in used:
         a, b = offset[e], offset[e + 1]
         assert rel_l2(got[a:b], want[a:b]) <= 2 * RL2_Y_BF16_H, f"expert {e} ({b - a} rows)"
+
+
+# ----------------------------------------------------------------------------
+# Live-cache affinity ("Nudge, don't cut", "Then Maya's own knob beat ours")
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("blocked", [True, False], ids=["block_ctas", "ring"])
+def test_route_affinity_parity(blocked):
+    cfg = C.qwen(16)
+    x = C.draw_x(cfg, DEV)
+    wr = C.draw_router(cfg, DEV)
+    e2s = np.full(cfg.E, -1, dtype=np.int32)
+    s2e = C.initial_residency(cfg)
+    e2s[s2e] = np.arange(cfg.S, dtype=np.int32)
+    ids, w, logits = M.route(x, wr, cfg.k, return_logits=True, blocked=blocked,
+                             e2s=torch.from_numpy(e2s).to(DEV), affinity=0.3)
+    torch.cuda.synchronize()
+    want_logits = O.router_logits(_np(x.float()), _np(wr.float()))
+    want = O.select_topk(want_logits, cfg.k, resident=e2s >= 0, affinity=0.3)
+    assert np.array_equal(_np(ids), want)
+    assert not np.array_equal(want, O.select_topk(want_logits, cfg.k))
+    assert np.abs(_np(w) - O.route_weights(want_logits, want)).max() <= 1e-6
+
+
+def test_layer_gather_with_affinity_matches_oracle_and_misses_less():
+    cfg = C.qwen(8)
+    st = stage_layer(cfg)
+    s2e0 = C.initial_residency(cfg)
+    res = {}
+    for lam in (0.0, 0.5):
+        pool = st["slabs_dev"][torch.from_numpy(s2e0.astype(np.int64)).to(DEV)].contiguous()
+        gstate = M.CacheState.from_slots(s2e0, cfg.E)
+        ostate = O.CacheState.from_slots(s2e0, cfg.E)
+        layer = M.SlotCachedMoELayer(st["wr"], pool, cfg.k, cfg.I, cfg.mode, cfg.policy, host_slabs=st["host"],
+                                     state=gstate, max_tokens=cfg.T, affinity=lam)
+        misses = 0
+        for step in range(4):
+            x = C.draw_x(cfg, DEV, step=step)
+            r = layer.forward(x)
+            torch.cuda.synchronize()
+            want = O.layer_forward(_np(x.float()), _np(st["wr"].float()), HostSlabs(st["host"]), cfg.H, cfg.I, cfg.k,
+                                   cfg.mode, cfg.policy, ostate, affinity=lam)
+            assert np.array_equal(_np(r["ids"]), want["ids"]), (lam, step)
+            assert_out_close(_np(r["out"].float()), want["out"], f"affinity {lam} step {step}")
+            _check_state(gstate, ostate, f"affinity {lam} step {step}")
+            misses += sum(len(c["miss_e"]) for c in want["chunks"])
+        assert int(layer.stats[0]) == misses
+        res[lam] = misses
+    assert res[0.5] < res[0.0]

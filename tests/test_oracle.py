@@ -450,3 +450,24 @@ def test_gather_mode_chunked_equals_resident():
     assert np.allclose(g["out"], full["out"], rtol=1e-12, atol=1e-14)
     for s, e in enumerate(st.s2e):
         assert np.array_equal(pool[s], host[e])
+
+
+def test_affinity_golden():
+    g = _gold("affinity_example.json")
+    logits = np.array([g["logits"]], dtype=np.float32)
+    ids = O.select_topk(logits, g["k"], resident=np.array(g["resident"]), affinity=g["affinity"])
+    assert ids[0].tolist() == g["ids"]
+    assert O.select_topk(logits, g["k"])[0].tolist() == g["ids_without"]
+    assert np.allclose(O.route_weights(logits, ids)[0], g["w"], atol=1e-9)
+
+
+def test_affinity_zero_or_nothing_resident_is_plain_topk():
+    rng = np.random.default_rng(21)
+    logits = rng.normal(size=(6, 40)).astype(np.float32)
+    res = rng.random(40) < 0.5
+    plain = O.select_topk(logits, 5)
+    assert np.array_equal(O.select_topk(logits, 5, resident=res, affinity=0.0), plain)
+    assert np.array_equal(O.select_topk(logits, 5, resident=np.zeros(40, bool), affinity=0.7), plain)
+    # a large affinity picks only resident experts while at least k are resident
+    ids = O.select_topk(logits, 5, resident=res, affinity=100.0)
+    assert res[ids].all()
