@@ -130,7 +130,7 @@ extern "C" int moe_expert_ffn(const void* x, int T, int H, int I, int k, int E, 
   }
   FfnArgs a{(const uint16_t*)x, T, H, I, k, E, offset, rows, list_e, n_list, (const uint16_t*)pool, e2s,
             (const uint16_t*)host_slabs, (size_t)3 * H * I, (float*)workspace, y, dev_status, S,
-            host_slabs == nullptr, nullptr, nullptr};
+            host_slabs == nullptr, nullptr, nullptr, nullptr};
   if (prefill_extra_bytes((int)n, H, I) > 0 && workspace_bytes >= moe_ffn_workspace_bytes(T, H, k, I)) {
     char* b = (char*)workspace + align256(4 * n * I);
     a.xp = (uint16_t*)b;
@@ -212,7 +212,10 @@ extern "C" int moe_layer_forward(const moe_layer_args* a, moe_stream_t main_s, m
     prof.end(ms);
     FfnArgs f{(const uint16_t*)a->x + (size_t)t0 * H, tc, H, I, k, E, ws.offset, ws.rows, nullptr, nullptr,
               (const uint16_t*)a->pool, a->e2s, (const uint16_t*)a->host_slabs, (size_t)3 * H * I, ws.hbuf, ws.y,
-              a->dev_status, S, 1, ws.xp, ws.hb};
+              a->dev_status, S, 1, ws.xp, ws.hb, nullptr};
+    // tensor-core path: y travels as bf16 through the same buffer (half the bytes)
+    const bool y_bf16 = mode != MOE_MODE_ZERO_RETURN && prefill_eligible(f, n);
+    if (y_bf16) f.yb = (uint16_t*)ws.y;
     if (mode == MOE_MODE_RESIDENT) {
       f.list_e = ws.act_e;
       f.n_list = ws.n_act;
@@ -259,7 +262,7 @@ extern "C" int moe_layer_forward(const moe_layer_args* a, moe_stream_t main_s, m
     prof.begin(MOE_PROF_COMBINE, ms);
     r = launch_combine(ws.y, a->w + (size_t)t0 * k, ws.pos, ids_c, a->e2s, tc, k, H, E, split,
                        (uint16_t*)a->out + (size_t)t0 * H, split ? a->out_res + (size_t)t0 * H : nullptr,
-                       split ? a->out_miss + (size_t)t0 * H : nullptr, ms);
+                       split ? a->out_miss + (size_t)t0 * H : nullptr, ms, y_bf16 ? (const uint16_t*)ws.y : nullptr);
     if (r != MOE_OK) return r;
     prof.end(ms);
   }

@@ -560,7 +560,8 @@ __global__ void __launch_bounds__(kCombThreads) combine_kernel(const float* __re
                                                                const int32_t* __restrict__ e2s, int k, int H, int E,
                                                                int split, uint16_t* __restrict__ out,
                                                                float* __restrict__ out_res,
-                                                               float* __restrict__ out_miss) {
+                                                               float* __restrict__ out_miss,
+                                                               const uint16_t* __restrict__ yb) {
   const int t = blockIdx.x;
   const int c = (blockIdx.y * kCombThreads + threadIdx.x) * 4;
   if (c >= H) return;
@@ -577,7 +578,12 @@ __global__ void __launch_bounds__(kCombThreads) combine_kernel(const float* __re
       const int p = pos[(size_t)t * k + j];
       if (p >= 0) {
         wj[j] = w[(size_t)t * k + j];
-        v[j] = *reinterpret_cast<const float4*>(y + (size_t)p * H + c);
+        if (yb) {
+          const uint2 u = *reinterpret_cast<const uint2*>(yb + (size_t)p * H + c);
+          v[j] = make_float4(bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y));
+        } else {
+          v[j] = *reinterpret_cast<const float4*>(y + (size_t)p * H + c);
+        }
         if (split) {
           const int e = ids[(size_t)t * k + j];
           res[j] = e >= 0 && e < E && e2s[e] >= 0;
@@ -610,10 +616,11 @@ __global__ void __launch_bounds__(kCombThreads) combine_kernel(const float* __re
 }
 
 int launch_combine(const float* y, const float* w, const int32_t* pos, const int32_t* ids, const int32_t* e2s, int T,
-                   int k, int H, int E, int split, void* out, float* out_res, float* out_miss, cudaStream_t stream) {
+                   int k, int H, int E, int split, void* out, float* out_res, float* out_miss, cudaStream_t stream,
+                   const uint16_t* yb) {
   const dim3 grid(T, (H / 4 + kCombThreads - 1) / kCombThreads);
   combine_kernel<<<grid, kCombThreads, 0, stream>>>(y, w, pos, ids, e2s, k, H, E, split, (uint16_t*)out, out_res,
-                                                    out_miss);
+                                                    out_miss, yb);
   MOE_LAUNCH_CHECK();
   return MOE_OK;
 }

@@ -23,6 +23,7 @@ struct FfnArgs {
   int pool_only;          // every listed expert is in the pool (e2s[e] >= 0 or e2s == NULL)
   uint16_t* xp;           // bf16 [T*k][H] grouped copy of x (tensor-core path), or NULL
   uint16_t* hb;           // bf16 [T*k][I] h for the tensor-core path, or NULL
+  uint16_t* yb;           // tensor-core path: write y as bf16 [T*k][H] here instead of fp32 y (or NULL)
 };
 
 // Records (start, end) event pairs around kernel launches when tracing is on.
@@ -59,7 +60,8 @@ bool prefill_eligible(const FfnArgs& a, int n);
 size_t prefill_extra_bytes(int n, int H, int I);
 int launch_prefill(const FfnArgs& a, int n, int max_list, cudaStream_t stream, Prof* prof);
 int launch_combine(const float* y, const float* w, const int32_t* pos, const int32_t* ids, const int32_t* e2s, int T,
-                   int k, int H, int E, int split, void* out, float* out_res, float* out_miss, cudaStream_t stream);
+                   int k, int H, int E, int split, void* out, float* out_res, float* out_miss, cudaStream_t stream,
+                   const uint16_t* yb = nullptr);
 int launch_manage(const int32_t* ids, int n, int E, int S, int policy, int32_t* e2s, int32_t* s2e, uint32_t* prio,
                   uint32_t* stamp, int32_t* miss_e, int32_t* miss_s, int32_t* n_miss, int32_t* hit_e,
                   int32_t* n_hit, int32_t* sid, int64_t* stats, int32_t* dev_status, cudaStream_t stream);

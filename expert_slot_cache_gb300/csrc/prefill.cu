@@ -102,8 +102,9 @@ struct PrefillArgs {
   const int32_t* e2s;     // NULL = expert e in slot e
   int S;
   uint16_t* hb;  // bf16 [n][I]: GEMM 1 output
-  float* y;      // fp32 [n][H]: GEMM 2 output
+  float* y;      // fp32 [n][H]: GEMM 2 output (when yb == NULL)
   int32_t* status;
+  uint16_t* yb;  // bf16 [n][H]: GEMM 2 output, or NULL
 };
 
 // Locate tile t: expert list index (by prefix search), row tile, column tile.
@@ -306,10 +307,24 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const Prefil
 #pragma unroll
           for (int j = 0; j < 32; ++j) buf[lane * 33 + j] = v[j];
           __syncwarp();
-          // one row per instruction: 32 lanes x 4 B = 128 contiguous bytes
+          if (a.yb) {
+            // bf16: two rows per instruction, 2 columns per lane (64 B per row)
+            const int half = lane >> 4, col = 2 * (lane & 15);
 #pragma unroll 4
-          for (int r = 0; r < 32; ++r)
-            if (r < nvalid) a.y[(p0 + r) * a.H + o0 + 32 * c + lane] = buf[r * 33 + lane];
+            for (int r = 0; r < 32; r += 2) {
+              const int rr = r + half;
+              if (rr < nvalid) {
+                const uint32_t wv = uint32_t(f32_to_bf16(buf[rr * 33 + col])) |
+                                    (uint32_t(f32_to_bf16(buf[rr * 33 + col + 1])) << 16);
+                *reinterpret_cast<uint32_t*>(a.yb + (p0 + rr) * a.H + o0 + 32 * c + col) = wv;
+              }
+            }
+          } else {
+            // one row per instruction: 32 lanes x 4 B = 128 contiguous bytes
+#pragma unroll 4
+            for (int r = 0; r < 32; ++r)
+              if (r < nvalid) a.y[(p0 + r) * a.H + o0 + 32 * c + lane] = buf[r * 33 + lane];
+          }
           __syncwarp();
         }
       }
@@ -386,7 +401,7 @@ int launch_prefill(const FfnArgs& a, int n, int max_list, cudaStream_t stream, P
     const uint32_t b[3] = {64, kPK, 1};
     if (encode_tmap_3d_bf16(&md, a.pool, d, s, b, CU_TENSOR_MAP_SWIZZLE_128B) != MOE_OK) return MOE_ERR_CUDA;
   }
-  PrefillArgs p{a.H, a.I, a.E, n, a.offset, a.list_e, a.n_list, a.e2s, a.S, a.hb, a.y, a.status};
+  PrefillArgs p{a.H, a.I, a.E, n, a.offset, a.list_e, a.n_list, a.e2s, a.S, a.hb, a.y, a.status, a.yb};
   (void)max_list;
   if (prof) prof->begin(MOE_PROF_FFN_ROWS, stream);
   gather_rows_kernel<<<std::min(n, sms * 8), 256, 0, stream>>>(a.x, a.rows, n, a.H, a.k, a.xp);

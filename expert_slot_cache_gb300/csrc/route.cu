@@ -69,17 +69,34 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// Packed fp32 pairs for fma.rn.f32x2 (two independent IEEE fp32 fmas).
+__device__ __forceinline__ uint64_t rf2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void rf2_fma(uint64_t& d, uint64_t a, uint64_t b) {
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(d) : "l"(a), "l"(b));
+}
+__device__ __forceinline__ float2 rf2_unpack(uint64_t v) {
+  float2 f;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(f.x), "=f"(f.y) : "l"(v));
+  return f;
+}
+
 template <int CH>
 __global__ void __launch_bounds__(kRouteThreads) logits_kernel(const uint16_t* __restrict__ x,
                                                                const uint16_t* __restrict__ wr,
                                                                const float* __restrict__ off, int T, int H, int E,
                                                                float* __restrict__ logits) {
   constexpr int TT = 8 * CH;
-  // stage s: W [kHC][kEB] bf16 (8 KB) | x [TT][kHC] bf16
+  constexpr int kXRow = kHC + 8;  // bf16 x row, padded against bank conflicts in the conversion
+  // stage s: W [kHC][kEB] bf16 (8 KB) | x [TT][kXRow] bf16;  then xf [kHC][TT] fp32 (token-minor)
   constexpr int kWBytes = kHC * kEB * 2;
-  constexpr int kXBytes = TT * kHC * 2;
+  constexpr int kXBytes = TT * kXRow * 2;
   constexpr int kStage = kWBytes + kXBytes;
   extern __shared__ __align__(16) unsigned char rsm[];
+  float* xf = reinterpret_cast<float*>(rsm + kRStages * kStage);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int t0 = blockIdx.x * TT, e0 = blockIdx.y * kEB;
   const int nt = min(TT, T - t0);
@@ -89,22 +106,21 @@ __global__ void __launch_bounds__(kRouteThreads) logits_kernel(const uint16_t* _
     unsigned char* sw = rsm + st * kStage;
     unsigned char* sx = sw + kWBytes;
     const int h0 = c * kHC;
-    // W: kHC rows x 64 bytes = 4 x 16 B per row
     for (int v = tid; v < kHC * 4; v += kRouteThreads) {
       const int r = v >> 2, q = v & 3;
       const bool ok = h0 + r < H && e0 + 8 * q < E;
       const uint16_t* src = ok ? wr + (size_t)(h0 + r) * E + e0 + 8 * q : wr;
       cp_async16(sw + r * 64 + q * 16, src, ok);
     }
-    // x: TT rows x kHC bf16 = TT x 16 x 16 B
     for (int v = tid; v < TT * (kHC / 8); v += kRouteThreads) {
       const int r = v / (kHC / 8), q = v % (kHC / 8);
       const bool ok = r < nt && h0 + 8 * q < H;
       const uint16_t* src = ok ? x + (size_t)(t0 + r) * H + h0 + 8 * q : x;
-      cp_async16(sx + (r * kHC + 8 * q) * 2, src, ok);
+      cp_async16(sx + (r * kXRow + 8 * q) * 2, src, ok);
     }
   };
 
+  // warp w owns tokens w*CH .. w*CH+CH-1; lane = expert
   float acc[CH];
 #pragma unroll
   for (int c = 0; c < CH; ++c) acc[c] = 0.f;
@@ -116,32 +132,61 @@ __global__ void __launch_bounds__(kRouteThreads) logits_kernel(const uint16_t* _
   for (int c = 0; c < nchunk; ++c) {
     cp_async_wait<kRStages - 2>();
     __syncthreads();
-    // refill the stage freed by chunk c-1
     if (c + kRStages - 1 < nchunk) load_chunk(c + kRStages - 1, (c + kRStages - 1) % kRStages);
     cp_async_commit();
     const unsigned char* sw = rsm + (c % kRStages) * kStage;
     const uint16_t* ws = reinterpret_cast<const uint16_t*>(sw);
     const uint16_t* xs = reinterpret_cast<const uint16_t*>(sw + kWBytes);
     const int hn = min(kHC, H - c * kHC);  // a multiple of 8
-    float part[CH];  // this 128-row block's chain, added to the logit afterwards
+    // x of this chunk to fp32, token-minor, converted once for all 32 expert lanes
+    for (int v = tid; v < TT * (kHC / 8); v += kRouteThreads) {
+      const int r = v % TT, q = v / TT;
+      const uint4 u = *reinterpret_cast<const uint4*>(xs + r * kXRow + 8 * q);
+      float* d = xf + (8 * q) * TT + r;
+      d[0 * TT] = bf16_lo(u.x);
+      d[1 * TT] = bf16_hi(u.x);
+      d[2 * TT] = bf16_lo(u.y);
+      d[3 * TT] = bf16_hi(u.y);
+      d[4 * TT] = bf16_lo(u.z);
+      d[5 * TT] = bf16_hi(u.z);
+      d[6 * TT] = bf16_lo(u.w);
+      d[7 * TT] = bf16_hi(u.w);
+    }
+    __syncthreads();
+    // this 128-row block's chains, then added to the logits in block order
+    float part[CH];
+    uint64_t part2[(CH + 1) / 2];
 #pragma unroll
     for (int cc = 0; cc < CH; ++cc) part[cc] = 0.f;
-    for (int h0 = 0; h0 < hn; h0 += 8) {
-      // operands of 8 consecutive h first, then the 8 fma steps of each chain
-      float wv[8];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) wv[u] = bf16_to_f32(ws[(h0 + u) * kEB + lane]);
+    for (int p = 0; p < (CH + 1) / 2; ++p) part2[p] = 0ull;
+    const float* xw = xf + warp * CH;
+    for (int h = 0; h < hn; ++h) {
+      const float wv = bf16_to_f32(ws[h * kEB + lane]);
+      const float* xr = xw + h * TT;
+      if (CH == 1) {
+        part[0] = fmaf(xr[0], wv, part[0]);
+      } else {
+        const uint64_t w2 = rf2_pack(wv, wv);
 #pragma unroll
-      for (int cc = 0; cc < CH; ++cc) {
-        const uint4 xv = *reinterpret_cast<const uint4*>(xs + (warp + 8 * cc) * kHC + h0);
-        part[cc] = fmaf(bf16_lo(xv.x), wv[0], part[cc]);
-        part[cc] = fmaf(bf16_hi(xv.x), wv[1], part[cc]);
-        part[cc] = fmaf(bf16_lo(xv.y), wv[2], part[cc]);
-        part[cc] = fmaf(bf16_hi(xv.y), wv[3], part[cc]);
-        part[cc] = fmaf(bf16_lo(xv.z), wv[4], part[cc]);
-        part[cc] = fmaf(bf16_hi(xv.z), wv[5], part[cc]);
-        part[cc] = fmaf(bf16_lo(xv.w), wv[6], part[cc]);
-        part[cc] = fmaf(bf16_hi(xv.w), wv[7], part[cc]);
+        for (int p4 = 0; p4 < CH / 4 + (CH == 2 ? 1 : 0); ++p4) {
+          if (CH == 2) {
+            const float2 xv = *reinterpret_cast<const float2*>(xr);
+            rf2_fma(part2[0], rf2_pack(xv.x, xv.y), w2);
+          } else {
+            const float4 xv = *reinterpret_cast<const float4*>(xr + 4 * p4);
+            rf2_fma(part2[2 * p4], rf2_pack(xv.x, xv.y), w2);
+            rf2_fma(part2[2 * p4 + 1], rf2_pack(xv.z, xv.w), w2);
+          }
+        }
+      }
+    }
+    if (CH > 1) {
+#pragma unroll
+      for (int p = 0; p < CH / 2; ++p) {
+        const float2 f = rf2_unpack(part2[p]);
+        part[2 * p] = f.x;
+        part[2 * p + 1] = f.y;
       }
     }
 #pragma unroll
@@ -152,7 +197,7 @@ __global__ void __launch_bounds__(kRouteThreads) logits_kernel(const uint16_t* _
   if (e < E) {
 #pragma unroll
     for (int cc = 0; cc < CH; ++cc) {
-      const int t = warp + 8 * cc;
+      const int t = warp * CH + cc;
       if (t < nt) logits[(size_t)(t0 + t) * E + e] = off ? acc[cc] + off[e] : acc[cc];
     }
   }
@@ -355,7 +400,7 @@ extern "C" int moe_route(const void* x, const void* w_router, const float* logit
   int ch = 8;
   while (ch > 1 && ((T + 8 * ch - 1) / (8 * ch)) * eb < sms) ch /= 2;
   const dim3 grid((T + 8 * ch - 1) / (8 * ch), eb);
-  const size_t smem = (size_t)kRStages * (kHC * kEB * 2 + 8 * ch * kHC * 2);
+  const size_t smem = (size_t)kRStages * (kHC * kEB * 2 + 8 * ch * (kHC + 8) * 2) + (size_t)kHC * 8 * ch * 4;
   static bool d1[64] = {}, d2[64] = {}, d4[64] = {}, d8[64] = {};
   switch (ch) {
     case 1:
