@@ -219,6 +219,36 @@ class StackWorkload:
         self.stack.x_all.copy_(self.inputs[st])
 
 
+def policy_replay(trace: np.ndarray, E: int, S: int, dev: str, slab_bytes: int) -> dict:
+    """Replay one routing trace through expert_cache_manage under each policy
+    ("Porting vllm-expert-cache to NVIDIA GPUs", "Measuring, without fooling
+    yourself": count misses, not tokens).  STATIC keeps its seeded set; the
+    hindsight baseline is STATIC with the S experts used most over the trace
+    (the transcript's "oracle ... picked the best possible fixed set")."""
+    import expert_slot_cache_gb300 as M
+    steps, T, k = trace.shape
+    ids_d = torch.from_numpy(trace).to(dev)
+    seeded = C.initial_residency(C.TINY.with_(E=E, S=S, seed=E))
+    counts = np.bincount(trace.reshape(-1), minlength=E)
+    best = np.sort(np.argsort(-counts, kind="stable")[:S]).astype(np.int32)
+    runs = {"lru": (C.POLICY_LRU, seeded), "lfu": (C.POLICY_LFU, seeded), "static": (C.POLICY_STATIC, seeded),
+            "static_best_fixed": (C.POLICY_STATIC, best)}
+    out = {}
+    for name, (pol, s2e0) in runs.items():
+        st = M.CacheState.from_slots(s2e0, E, dev)
+        tot = torch.zeros(1, dtype=torch.int64, device=dev)
+        for i in range(steps):
+            tot += M.cache_manage(ids_d[i], st, pol).n_miss
+        misses = int(tot.item())
+        needed = sum(len(np.unique(trace[i])) for i in range(steps))
+        out[name] = {"misses": misses, "hit_rate": 1.0 - misses / needed,
+                     "host_link_GB": misses * slab_bytes / 1e9 if pol != C.POLICY_STATIC else 0.0,
+                     "missed_expert_bytes_GB": misses * slab_bytes / 1e9}
+    out["trace"] = {"steps": steps, "T": T, "k": k, "E": E, "S": S,
+                    "recipe": "Zipf(1.1) popularity over a ranking drifting by 2 swaps per step"}
+    return out
+
+
 def _make_prof(M, pairs: int):
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * pairs)]
     for ev in evs:  # torch creates the underlying event lazily, on its first record
@@ -534,6 +564,8 @@ def main():
                                    "misses_per_step": r3["misses"] / 10}
             del w3
         torch.cuda.empty_cache()
+        var["policy_replay"] = policy_replay(C.drifting_trace(cfg.E, cfg.k, 8, 400), cfg.E, cfg.S, dev,
+                                             cfg.slab_bytes)
         line["variants"] = var
 
     if not args.no_cpu_baseline and rank == 0:

@@ -174,3 +174,32 @@ def e2s_from_s2e(s2e: np.ndarray, E: int) -> np.ndarray:
         if e >= 0:
             e2s[e] = s
     return e2s
+
+
+# ----------------------------------------------------------------------------
+# Routing traces for policy replay
+# ----------------------------------------------------------------------------
+
+def drifting_trace(E: int, k: int, T: int, steps: int, seed: int = 7, s: float = 1.1,
+                   swaps_per_step: int = 2) -> np.ndarray:
+    """Synthetic routing ids [steps][T][k] with a popularity that drifts.
+
+    Expert popularity is Zipf(s) over a ranking that changes slowly: after
+    each step, ``swaps_per_step`` random pairs of ranks trade places, so the
+    hot set drifts while any short window keeps temporal locality (the
+    transcript's "the useful set drifts").  Each token draws k distinct
+    experts from that popularity.  numpy's seeded Generator: a test input,
+    drawn once on the host.
+    """
+    rng = np.random.default_rng(seed)
+    p = np.arange(1, E + 1, dtype=np.float64) ** -s
+    p /= p.sum()
+    order = rng.permutation(E)  # order[r] = expert at rank r
+    out = np.empty((steps, T, k), dtype=np.int32)
+    for st in range(steps):
+        for t in range(T):
+            out[st, t] = order[rng.choice(E, size=k, replace=False, p=p)]
+        for _ in range(swaps_per_step):
+            a, b = rng.integers(0, E, size=2)
+            order[a], order[b] = order[b], order[a]
+    return out
