@@ -486,9 +486,9 @@ def main():
         else:
             raise SystemExit(f"unknown workload {w}")
         wl = Workload(c, 2 * args.steps + args.warmup, dev)
-        r = time_steps(wl, args.steps, args.warmup)
+        r = time_steps(wl, args.steps, args.warmup, clocks=Clocks(local))
         if rank == 0:
-            print(json.dumps({"workload": w, "ms_per_step": r["ms"] / args.steps,
+            print(json.dumps({"workload": w, "clocks": r["clocks"], "ms_per_step": r["ms"] / args.steps,
                               "ms_per_step_instrumented": r["ms_instrumented"] / args.steps,
                               "tokens_per_s": c.T * args.steps / (r["ms"] * 1e-3),
                               "kernels_ms_per_step": {n: v / args.steps for n, v in r["kern_ms"].items()}}))

@@ -552,8 +552,10 @@ int launch_ffn(const FfnArgs& a, int max_list, cudaStream_t stream, Prof* prof) 
 // ---------------------------------------------------------------------------
 // Combine: out[t] = sum_j w[t][j] y[pos[t*k+j]] in fp32, j ascending.
 // ---------------------------------------------------------------------------
-constexpr int kCombThreads = 128;  // x 4 columns = 512 columns per CTA
+constexpr int kCombThreads = 128;
 
+// Combine over CPT columns per thread (4 from fp32 y, 8 from bf16 y: one 16-byte load per row either way).
+template <int CPT>
 __global__ void __launch_bounds__(kCombThreads) combine_kernel(const float* __restrict__ y, const float* __restrict__ w,
                                                                const int32_t* __restrict__ pos,
                                                                const int32_t* __restrict__ ids,
@@ -563,27 +565,24 @@ __global__ void __launch_bounds__(kCombThreads) combine_kernel(const float* __re
                                                                float* __restrict__ out_miss,
                                                                const uint16_t* __restrict__ yb) {
   const int t = blockIdx.x;
-  const int c = (blockIdx.y * kCombThreads + threadIdx.x) * 4;
+  const int c = (blockIdx.y * kCombThreads + threadIdx.x) * CPT;
   if (c >= H) return;
   // all k rows first (independent loads), then the sum in j order
-  float4 v[kMaxK];
+  uint4 raw[kMaxK];
   float wj[kMaxK];
-  bool res[kMaxK];
+  bool res[kMaxK], have[kMaxK];
 #pragma unroll
   for (int j = 0; j < kMaxK; ++j) {
-    v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-    wj[j] = 0.f;
+    have[j] = false;
     res[j] = true;
+    wj[j] = 0.f;
     if (j < k) {
       const int p = pos[(size_t)t * k + j];
       if (p >= 0) {
+        have[j] = true;
         wj[j] = w[(size_t)t * k + j];
-        if (yb) {
-          const uint2 u = *reinterpret_cast<const uint2*>(yb + (size_t)p * H + c);
-          v[j] = make_float4(bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y));
-        } else {
-          v[j] = *reinterpret_cast<const float4*>(y + (size_t)p * H + c);
-        }
+        raw[j] = CPT == 8 ? *reinterpret_cast<const uint4*>(yb + (size_t)p * H + c)
+                          : *reinterpret_cast<const uint4*>(y + (size_t)p * H + c);
         if (split) {
           const int e = ids[(size_t)t * k + j];
           res[j] = e >= 0 && e < E && e2s[e] >= 0;
@@ -591,36 +590,58 @@ __global__ void __launch_bounds__(kCombThreads) combine_kernel(const float* __re
       }
     }
   }
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f), accm = acc;
+  float acc[CPT], accm[CPT];
+#pragma unroll
+  for (int q = 0; q < CPT; ++q) acc[q] = accm[q] = 0.f;
 #pragma unroll
   for (int j = 0; j < kMaxK; ++j) {
-    if (j < k) {
-      float4& d = res[j] ? acc : accm;
-      d.x = fmaf(wj[j], v[j].x, d.x);
-      d.y = fmaf(wj[j], v[j].y, d.y);
-      d.z = fmaf(wj[j], v[j].z, d.z);
-      d.w = fmaf(wj[j], v[j].w, d.w);
+    if (j < k && have[j]) {
+      float v[CPT];
+      if (CPT == 8) {
+        v[0] = bf16_lo(raw[j].x); v[1] = bf16_hi(raw[j].x); v[2] = bf16_lo(raw[j].y); v[3] = bf16_hi(raw[j].y);
+        v[4] = bf16_lo(raw[j].z); v[5] = bf16_hi(raw[j].z); v[6] = bf16_lo(raw[j].w); v[7] = bf16_hi(raw[j].w);
+      } else {
+        v[0] = __uint_as_float(raw[j].x); v[1] = __uint_as_float(raw[j].y);
+        v[2] = __uint_as_float(raw[j].z); v[3] = __uint_as_float(raw[j].w);
+      }
+#pragma unroll
+      for (int q = 0; q < CPT; ++q) {
+        if (res[j]) acc[q] = fmaf(wj[j], v[q], acc[q]);
+        else accm[q] = fmaf(wj[j], v[q], accm[q]);
+      }
     }
   }
   const size_t o = (size_t)t * H + c;
-  float4 tot = acc;
+  float tot[CPT];
+#pragma unroll
+  for (int q = 0; q < CPT; ++q) tot[q] = split ? acc[q] + accm[q] : acc[q];
   if (split) {
-    *reinterpret_cast<float4*>(out_res + o) = acc;
-    *reinterpret_cast<float4*>(out_miss + o) = accm;
-    tot = make_float4(acc.x + accm.x, acc.y + accm.y, acc.z + accm.z, acc.w + accm.w);
+#pragma unroll
+    for (int q4 = 0; q4 < CPT / 4; ++q4) {
+      *reinterpret_cast<float4*>(out_res + o + 4 * q4) = make_float4(acc[4 * q4], acc[4 * q4 + 1], acc[4 * q4 + 2], acc[4 * q4 + 3]);
+      *reinterpret_cast<float4*>(out_miss + o + 4 * q4) =
+          make_float4(accm[4 * q4], accm[4 * q4 + 1], accm[4 * q4 + 2], accm[4 * q4 + 3]);
+    }
   }
-  uint2 pk;
-  pk.x = uint32_t(f32_to_bf16(tot.x)) | (uint32_t(f32_to_bf16(tot.y)) << 16);
-  pk.y = uint32_t(f32_to_bf16(tot.z)) | (uint32_t(f32_to_bf16(tot.w)) << 16);
-  *reinterpret_cast<uint2*>(out + o) = pk;
+  uint32_t pk[CPT / 2];
+#pragma unroll
+  for (int q = 0; q < CPT / 2; ++q) pk[q] = uint32_t(f32_to_bf16(tot[2 * q])) | (uint32_t(f32_to_bf16(tot[2 * q + 1])) << 16);
+  if (CPT == 8) *reinterpret_cast<uint4*>(out + o) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+  else *reinterpret_cast<uint2*>(out + o) = make_uint2(pk[0], pk[1]);
 }
 
 int launch_combine(const float* y, const float* w, const int32_t* pos, const int32_t* ids, const int32_t* e2s, int T,
                    int k, int H, int E, int split, void* out, float* out_res, float* out_miss, cudaStream_t stream,
                    const uint16_t* yb) {
-  const dim3 grid(T, (H / 4 + kCombThreads - 1) / kCombThreads);
-  combine_kernel<<<grid, kCombThreads, 0, stream>>>(y, w, pos, ids, e2s, k, H, E, split, (uint16_t*)out, out_res,
-                                                    out_miss, yb);
+  if (yb) {
+    const dim3 grid(T, (H / 8 + kCombThreads - 1) / kCombThreads);
+    combine_kernel<8><<<grid, kCombThreads, 0, stream>>>(y, w, pos, ids, e2s, k, H, E, split, (uint16_t*)out,
+                                                         out_res, out_miss, yb);
+  } else {
+    const dim3 grid(T, (H / 4 + kCombThreads - 1) / kCombThreads);
+    combine_kernel<4><<<grid, kCombThreads, 0, stream>>>(y, w, pos, ids, e2s, k, H, E, split, (uint16_t*)out,
+                                                         out_res, out_miss, nullptr);
+  }
   MOE_LAUNCH_CHECK();
   return MOE_OK;
 }
