@@ -22,6 +22,8 @@ struct LayerWs {
   float *hbuf, *y, *logits, *route;
   uint16_t *xp, *hb;
   int32_t* perm;
+  float* skp;
+  size_t skp_bytes;
   size_t bytes;
 };
 
@@ -56,6 +58,8 @@ static LayerWs carve(void* base, int n, int H, int E, int I, int T) {
     w.xp = (uint16_t*)take(2 * (size_t)n * H);
     w.hb = (uint16_t*)take(2 * (size_t)n * I);
   }
+  w.skp_bytes = sk_part_bytes(n, H, I);
+  if (w.skp_bytes) w.skp = (float*)take(w.skp_bytes);
   w.bytes = off;
   return w;
 }
@@ -110,6 +114,8 @@ extern "C" size_t moe_ffn_workspace_bytes(int T, int H, int k, int I) {
   const size_t n = (size_t)T * k;
   size_t b = align256(4 * n * I);
   if (prefill_extra_bytes((int)n, H, I) > 0) b += align256(2 * n * H) + align256(2 * n * I);
+  const size_t skb = sk_part_bytes((int)n, H, I);
+  if (skb) b += 256 + skb;  // 256: the parts start on a 256-byte boundary of a 16-byte aligned workspace
   return b;
 }
 
@@ -130,11 +136,16 @@ extern "C" int moe_expert_ffn(const void* x, int T, int H, int I, int k, int E, 
   }
   FfnArgs a{(const uint16_t*)x, T, H, I, k, E, offset, rows, list_e, n_list, (const uint16_t*)pool, e2s,
             (const uint16_t*)host_slabs, (size_t)3 * H * I, (float*)workspace, y, dev_status, S,
-            host_slabs == nullptr, nullptr, nullptr, nullptr};
-  if (prefill_extra_bytes((int)n, H, I) > 0 && workspace_bytes >= moe_ffn_workspace_bytes(T, H, k, I)) {
+            host_slabs == nullptr, nullptr, nullptr, nullptr, nullptr, 0};
+  if (workspace_bytes >= moe_ffn_workspace_bytes(T, H, k, I)) {
     char* b = (char*)workspace + align256(4 * n * I);
-    a.xp = (uint16_t*)b;
-    a.hb = (uint16_t*)(b + align256(2 * n * H));
+    if (prefill_extra_bytes((int)n, H, I) > 0) {
+      a.xp = (uint16_t*)b;
+      a.hb = (uint16_t*)(b + align256(2 * n * H));
+      b += align256(2 * n * H) + align256(2 * n * I);
+    }
+    a.skp_bytes = sk_part_bytes((int)n, H, I);
+    if (a.skp_bytes) a.skp = (float*)(((uintptr_t)b + 255) & ~uintptr_t(255));
   }
   return launch_ffn(a, std::min(max_list, E), (cudaStream_t)stream);
 }
@@ -212,7 +223,7 @@ extern "C" int moe_layer_forward(const moe_layer_args* a, moe_stream_t main_s, m
     prof.end(ms);
     FfnArgs f{(const uint16_t*)a->x + (size_t)t0 * H, tc, H, I, k, E, ws.offset, ws.rows, nullptr, nullptr,
               (const uint16_t*)a->pool, a->e2s, (const uint16_t*)a->host_slabs, (size_t)3 * H * I, ws.hbuf, ws.y,
-              a->dev_status, S, 1, ws.xp, ws.hb, nullptr};
+              a->dev_status, S, 1, ws.xp, ws.hb, nullptr, ws.skp, ws.skp_bytes};
     // tensor-core path: y travels as bf16 through the same buffer (half the bytes)
     const bool y_bf16 = mode != MOE_MODE_ZERO_RETURN && prefill_eligible(f, n);
     if (y_bf16) f.yb = (uint16_t*)ws.y;

@@ -500,6 +500,7 @@ static size_t ffn_smem_bytes(int K) { return (size_t)(kRB * K + 8 * 8 * kRB * 8)
 int launch_ffn(const FfnArgs& a, int max_list, cudaStream_t stream, Prof* prof) {
   if (max_list <= 0) return MOE_OK;
   if (prefill_eligible(a, a.T * a.k)) return launch_prefill(a, a.T * a.k, max_list, stream, prof);
+  if (sk_eligible(a)) return launch_ffn_sk(a, max_list, stream, prof);
   constexpr int kSmemCap = 160 * 1024;
   const size_t smem_gu = ffn_smem_bytes(a.H), smem_d = ffn_smem_bytes(a.I);
   if (smem_gu > (size_t)kSmemCap || smem_d > (size_t)kSmemCap) return MOE_ERR_ARG;

@@ -1,0 +1,494 @@
+// Decode expert FFN as a balanced stream over full weight rows, on tcgen05.
+//
+// The expert GEMM of "Porting vllm-expert-cache to NVIDIA GPUs" ("What this
+// package does": the expert GEMM runs on slot-remapped ids) for decode-sized
+// groups, where it is a weight stream: every listed expert's weights are read
+// once per batch of up to 16 of its tokens.
+//
+// Work split ("stream-K"): the listed experts' matrices are cut into stages
+// of 16 consecutive input rows times all output columns.  The n_list * NSR
+// stages of a pass are dealt out as contiguous, equal ranges of L stages, one
+// range per CTA, so every SM streams the same number of weight bytes however
+// many experts there are.  A CTA whose range covers part of an expert writes
+// that part's sums, for all output columns and the batch's tokens, to
+//   part[j][p][N],  j = CTA index - first CTA of the expert,
+// and a reduce kernel adds the parts in j order: for gate/up it forms
+// h = silu(g) * u (bf16, the down pass's operand), for down it writes y.  All
+// sums run in a fixed order, so results do not depend on timing.
+//
+// Math: per stage and per 128 output columns, one tcgen05.mma with M = 128
+// output columns (A = the stage's weights, MN-major, 128-byte swizzle as the
+// tensor-map load writes it), N = 16 tokens (B = the tokens' activations for
+// the stage's 16 rows, K-major, no swizzle) and K = 16, accumulating in TMEM.
+// Roles: warp 0 loads (TMA), warp 1 issues the MMAs, warps 2-5 move finished
+// accumulators (TMEM, double-buffered) to the parts.  Every wait is bounded.
+//
+// The activations (x grouped by expert, or h) come from the kernel before in
+// the stream; each pass is launched as a programmatic dependent and streams
+// its first weight stages before it waits (griddepcontrol.wait) for them.
+#include <algorithm>
+
+#include "internal.cuh"
+#include "tc05.cuh"
+
+namespace moe {
+
+constexpr int kDM = 128;                          // output columns per MMA (M)
+constexpr int kDN = 16;                           // tokens per batch (N)
+constexpr int kDK = 16;                           // weight rows per stage (K)
+constexpr int kDBoxBytes = 64 * kDK * 2;          // one {64 columns x 16 rows} weight box, 2 KB
+constexpr int kDActBox = 8 * kDN * 2;             // one {8 rows x 16 tokens} activation box, 256 B
+constexpr int kDRing = 200 * 1024;
+constexpr int kDMaxStages = 8;
+constexpr int kDThreads = 192;
+constexpr uint32_t kDTmemMax = 512;
+constexpr int kDJcapMax = 160;
+constexpr size_t kDPartBudget = size_t(16) << 20;  // bytes of parts per pass (soft cap)
+constexpr int kDMaxRows = 4096;
+constexpr uint32_t kDIdesc = idesc_bf16(kDM, kDN, 1, 0);
+
+struct SkPass {
+  float* part;  // [jcap][n][N]
+  int N, K;     // output columns, weight rows
+  int ntiles;   // N / 128
+  int NSR;      // stages per expert
+  int nst;      // ring stages
+  int wbytes;   // weight bytes per stage
+  int stride;   // stage stride in shared memory
+  int G, jcap;
+  uint32_t tcols;  // TMEM columns allocated: two accumulator buffers, rounded up to a power of two
+};
+
+// Stages per CTA range: equal ranges covering all stages with at most G CTAs,
+// and no expert spanning more than jcap ranges.
+__device__ __forceinline__ int sk_len(int n_list, int NSR, int G, int jcap) {
+  const int total = n_list * NSR;
+  int L = (total + G - 1) / G;
+  if ((NSR + L - 1) / L + 1 > jcap) L = (NSR + jcap - 2) / (jcap - 1);
+  return L;
+}
+
+__device__ __forceinline__ bool sk_slot(const FfnArgs& a, int li, int& e, int& slot) {
+  e = a.list_e[li];
+  if (e < 0 || e >= a.E) return false;
+  slot = a.e2s ? a.e2s[e] : e;
+  return slot >= 0 && slot < a.S;
+}
+
+struct SkSeg {
+  int e, slot, s_lo, s_hi, j, p0, nb;
+};
+
+// Calls f(seg) for each (expert part, token batch) of this CTA's range in
+// order; stops early when f returns false.  Every role walks the same list.
+template <class F>
+__device__ __forceinline__ void sk_segments(const FfnArgs& a, const SkPass& sp, int L, int beg, int end, F&& f) {
+  for (int li = beg / sp.NSR; li * sp.NSR < end; ++li) {
+    SkSeg g;
+    if (!sk_slot(a, li, g.e, g.slot)) continue;
+    g.s_lo = max(beg, li * sp.NSR) - li * sp.NSR;
+    g.s_hi = min(end, (li + 1) * sp.NSR) - li * sp.NSR;
+    g.j = (int)blockIdx.x - (li * sp.NSR) / L;
+    const int pb = a.offset[g.e], pe = a.offset[g.e + 1];
+    for (g.p0 = pb; g.p0 < pe; g.p0 += kDN) {
+      g.nb = min(kDN, pe - g.p0);
+      if (!f(g)) return;
+    }
+  }
+}
+
+template <bool DOWN>
+__global__ void __launch_bounds__(kDThreads, 1) ffn_sk_kernel(const FfnArgs a, const SkPass sp,
+                                                              const __grid_constant__ CUtensorMap mw,
+                                                              const __grid_constant__ CUtensorMap mact) {
+  extern __shared__ __align__(16) unsigned char sk_raw[];
+  unsigned char* ring =
+      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(sk_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(ring + sp.nst * sp.stride);
+  uint64_t* empty = full + kDMaxStages;
+  uint64_t* tfull = empty + kDMaxStages;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* done = tempty + 2;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_trigger();
+  const int n_list = *a.n_list;
+  const int n = a.T * a.k;
+  const int L = n_list > 0 ? sk_len(n_list, sp.NSR, sp.G, sp.jcap) : 1;
+  const int total = n_list * sp.NSR;
+  const int beg = blockIdx.x * L, end = min(beg + L, total);
+  if (beg >= end) return;  // uniform over the CTA: nothing allocated yet
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < sp.nst; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&tfull[s], 1);
+      mbar_init(&tempty[s], 4);
+    }
+    mbar_init(done, 1);
+    s_abort = 0;
+    for (int li = beg / sp.NSR; li * sp.NSR < end; ++li) {
+      int e, slot;
+      if (!sk_slot(a, li, e, slot)) set_status(a.status, e < 0 || e >= a.E ? MOE_DEV_BAD_EXPERT : MOE_DEV_BAD_SLOT);
+    }
+    mbar_fence_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&s_tmem, sp.tcols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  volatile int* abort_flag = &s_abort;
+  const uint32_t acc_cols = (uint32_t)sp.ntiles * kDN;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      uint32_t it = 0;
+      bool waited = false;
+      int ndef = 0, d_row[kDMaxStages], d_p0[kDMaxStages], last_use[kDMaxStages];
+      for (int s = 0; s < kDMaxStages; ++s) last_use[s] = -1;
+      auto issue_act = [&](int sl, int row0, int p0) {
+        unsigned char* dst = ring + sl * sp.stride + sp.wbytes;
+        tma_load_3d(dst, &mact, &full[sl], row0, p0, 0);
+        tma_load_3d(dst + kDActBox, &mact, &full[sl], row0 + 8, p0, 0);
+      };
+      auto flush = [&]() {
+        pdl_wait();
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        for (int d = 0; d < ndef; ++d) issue_act(d, d_row[d], d_p0[d]);
+        ndef = 0;
+        waited = true;
+      };
+      const int nbox = sp.N / 64;
+      sk_segments(a, sp, L, beg, end, [&](const SkSeg& g) {
+        for (int s = g.s_lo; s < g.s_hi; ++s, ++it) {
+          const int sl = it % sp.nst;
+          const uint32_t use = it / sp.nst;
+          if (use > 0) {
+            if (!waited) flush();
+            if (!*abort_flag && !mbar_wait(&empty[sl], (use - 1) & 1u)) {
+              *abort_flag = 1;
+              set_status(a.status, MOE_DEV_TIMEOUT);
+            }
+          }
+          if (*abort_flag) return false;
+          unsigned char* dst = ring + sl * sp.stride;
+          const int row0 = s * kDK;
+          mbar_expect_tx(&full[sl], sp.wbytes + 2 * kDActBox);
+          if (DOWN) {
+            for (int c = 0; c < nbox; ++c)
+              tma_load_3d(dst + c * kDBoxBytes, &mw, &full[sl], 64 * c, row0, 3 * g.slot + 2);
+          } else {
+            const int hb = nbox / 2;  // boxes per matrix
+            for (int c = 0; c < hb; ++c) {
+              tma_load_3d(dst + c * kDBoxBytes, &mw, &full[sl], 64 * c, row0, 3 * g.slot);
+              tma_load_3d(dst + (hb + c) * kDBoxBytes, &mw, &full[sl], 64 * c, row0, 3 * g.slot + 1);
+            }
+          }
+          if (waited) {
+            issue_act(sl, row0, g.p0);
+          } else {
+            d_row[ndef] = row0;
+            d_p0[ndef] = g.p0;
+            ++ndef;
+          }
+          last_use[sl] = (int)use;
+        }
+        return true;
+      });
+      // every issued stage gets its activation copies, so every full barrier completes
+      if (!waited) flush();
+      if (*abort_flag)
+        for (int s = 0; s < sp.nst; ++s)
+          if (last_use[s] >= 0) mbar_wait(&full[s], (uint32_t)last_use[s] & 1u);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      uint32_t it = 0, seg = 0;
+      sk_segments(a, sp, L, beg, end, [&](const SkSeg& g) {
+        const uint32_t buf = seg & 1u, use = seg >> 1;
+        if (use > 0 && !*abort_flag && !mbar_wait(&tempty[buf], (use - 1) & 1u)) {
+          *abort_flag = 1;
+          set_status(a.status, MOE_DEV_TIMEOUT);
+        }
+        tc_fence_after();
+        const uint32_t d = tmem + buf * acc_cols;
+        for (int s = g.s_lo; s < g.s_hi; ++s, ++it) {
+          const int sl = it % sp.nst;
+          if (!*abort_flag && !mbar_wait(&full[sl], (it / sp.nst) & 1u)) {
+            *abort_flag = 1;
+            set_status(a.status, MOE_DEV_TIMEOUT);
+          }
+          tc_fence_after();
+          if (!*abort_flag) {
+            const uint32_t sa = smem_u32(ring + sl * sp.stride);
+            // B: tokens x 16 rows, K-major core matrices: 8 rows apart = 256 B, 8 tokens apart = 128 B
+            const uint64_t bd = smem_desc_l(sa + sp.wbytes, kDActBox, 128, kLayoutNone);
+            for (int m = 0; m < sp.ntiles; ++m) {
+              // A: 128 output columns = two 64-column boxes 2 KB apart, 8-row groups 1 KB apart
+              const uint64_t ad = smem_desc_l(sa + m * 2 * kDBoxBytes, kDBoxBytes, 1024, kLayoutSw128);
+              umma_f16(d + m * kDN, ad, bd, kDIdesc, s > g.s_lo);
+            }
+          }
+          umma_commit(&empty[sl]);
+        }
+        umma_commit(&tfull[buf]);
+        ++seg;
+        return true;
+      });
+      // all MMAs issued by this thread have finished once `done` completes
+      umma_commit(done);
+      mbar_wait(done, 0);
+    }
+  } else {
+    // epilogue warps 2..5; TMEM lane quarter q = warp % 4 holds output columns q*32 .. q*32+31 of each tile
+    const int q = warp & 3;
+    uint32_t seg = 0;
+    sk_segments(a, sp, L, beg, end, [&](const SkSeg& g) {
+      const uint32_t buf = seg & 1u, use = seg >> 1;
+      if (!*abort_flag && !mbar_wait(&tfull[buf], use & 1u)) {
+        *abort_flag = 1;
+        set_status(a.status, MOE_DEV_TIMEOUT);
+      }
+      tc_fence_after();
+      if (!*abort_flag) {
+        float* base = sp.part + ((size_t)g.j * n + g.p0) * sp.N + q * 32 + lane;
+        for (int m = 0; m < sp.ntiles; ++m) {
+          float v[16];
+          tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + buf * acc_cols + m * kDN, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int t = 0; t < kDN; ++t)
+            if (t < g.nb) base[(size_t)t * sp.N + m * kDM] = v[t];
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[buf]);
+      ++seg;
+      return true;
+    });
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, sp.tcols);
+  }
+}
+
+// Adds the parts of each listed expert's rows in j order.
+//   SWIGLU: hb [n][I] bf16 = silu(sum g) * (sum u); parts hold [g | u]
+//   else:   y [n][H] fp32 = sum of parts
+constexpr int kSkRedThreads = 128;
+
+template <bool SWIGLU>
+__global__ void __launch_bounds__(kSkRedThreads) sk_reduce_kernel(const FfnArgs a, const float* __restrict__ part,
+                                                                  int N, int NSR, int G, int jcap,
+                                                                  float* __restrict__ y, uint16_t* __restrict__ hb) {
+  pdl_trigger();
+  pdl_wait();
+  const int li = blockIdx.y;
+  const int n_list = *a.n_list;
+  if (li >= n_list) return;
+  int e, slot;
+  if (!sk_slot(a, li, e, slot)) return;
+  const int L = sk_len(n_list, NSR, G, jcap);
+  const int j0 = (li * NSR) / L;
+  const int J = ((li + 1) * NSR - 1) / L - j0 + 1;
+  const int n = a.T * a.k;
+  const int ncol = SWIGLU ? N / 2 : N;
+  const int ncol4 = ncol / 4;
+  const int pb = a.offset[e], pe = a.offset[e + 1];
+  const size_t pstride = (size_t)n * N;
+  for (int p = pb; p < pe; ++p) {
+    for (int c4 = blockIdx.x * kSkRedThreads + threadIdx.x; c4 < ncol4; c4 += gridDim.x * kSkRedThreads) {
+      const float* src = part + (size_t)p * N + 4 * c4;
+      float4 g = make_float4(0.f, 0.f, 0.f, 0.f), u = g;
+      for (int jj = 0; jj < J; ++jj) {
+        const float4 t = *reinterpret_cast<const float4*>(src + jj * pstride);
+        g.x += t.x;
+        g.y += t.y;
+        g.z += t.z;
+        g.w += t.w;
+        if (SWIGLU) {
+          const float4 v = *reinterpret_cast<const float4*>(src + jj * pstride + ncol);
+          u.x += v.x;
+          u.y += v.y;
+          u.z += v.z;
+          u.w += v.w;
+        }
+      }
+      if (SWIGLU) {
+        const float h0 = g.x / (1.f + expf(-g.x)) * u.x, h1 = g.y / (1.f + expf(-g.y)) * u.y;
+        const float h2 = g.z / (1.f + expf(-g.z)) * u.z, h3 = g.w / (1.f + expf(-g.w)) * u.w;
+        uint2 w;
+        w.x = uint32_t(f32_to_bf16(h0)) | (uint32_t(f32_to_bf16(h1)) << 16);
+        w.y = uint32_t(f32_to_bf16(h2)) | (uint32_t(f32_to_bf16(h3)) << 16);
+        *reinterpret_cast<uint2*>(hb + (size_t)p * ncol + 4 * c4) = w;
+      } else {
+        *reinterpret_cast<float4*>(y + (size_t)p * ncol + 4 * c4) = g;
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+static int sk_jcap(int n, int N) {
+  const size_t per = (size_t)n * N * 4;
+  const size_t j = per ? kDPartBudget / per : 0;
+  return (int)std::max<size_t>(3, std::min<size_t>(j, kDJcapMax));
+}
+
+static size_t al256(size_t v) { return (v + 255) & ~size_t(255); }
+
+static size_t sk_half_bytes(int n, int H, int I) {
+  const size_t g = (size_t)sk_jcap(n, 2 * I) * n * 2 * I * 4, d = (size_t)sk_jcap(n, H) * n * H * 4;
+  return al256(std::max(g, d));
+}
+
+// Layout: [gate/up parts | down parts] (two equal halves), then x grouped by
+// expert (bf16 [n][H]) and h (bf16 [n][I]).  A chunk smaller than the one the
+// buffer was sized for gets as many parts as fit.
+size_t sk_part_bytes(int n, int H, int I) {
+  if (n < 1 || n > kDMaxRows) return 0;
+  return 2 * sk_half_bytes(n, H, I) + al256((size_t)n * H * 2) + al256((size_t)n * I * 2);
+}
+
+struct SkCarve {
+  float *gpart, *ypart;
+  uint16_t *xp, *hb;
+  int jg, jd;
+};
+
+static bool sk_carve(const FfnArgs& a, SkCarve* c) {
+  const int n = a.T * a.k;
+  const size_t act = al256((size_t)n * a.H * 2) + al256((size_t)n * a.I * 2);
+  if (!a.skp || a.skp_bytes < act + 512) return false;
+  const size_t half = ((a.skp_bytes - act) / 2) & ~size_t(255);
+  c->gpart = a.skp;
+  c->ypart = a.skp + half / 4;
+  c->xp = reinterpret_cast<uint16_t*>(reinterpret_cast<char*>(a.skp) + 2 * half);
+  c->hb = c->xp + al256((size_t)n * a.H * 2) / 2;
+  c->jg = (int)std::min<size_t>(sk_jcap(n, 2 * a.I), half / ((size_t)n * 2 * a.I * 4));
+  c->jd = (int)std::min<size_t>(sk_jcap(n, a.H), half / ((size_t)n * a.H * 4));
+  return c->jg >= 2 && c->jd >= 2;
+}
+
+static bool sk_pass(bool down, const FfnArgs& a, int G, float* part, int jcap, SkPass* out) {
+  SkPass sp{};
+  sp.part = part;
+  sp.N = down ? a.H : 2 * a.I;
+  sp.K = down ? a.I : a.H;
+  if (sp.N % kDM || sp.K % kDK) return false;
+  if (!down && a.I % kDM) return false;  // a tile never straddles the gate and up columns
+  sp.ntiles = sp.N / kDM;
+  if ((uint32_t)sp.ntiles * kDN * 2 > kDTmemMax) return false;  // two accumulator buffers in TMEM
+  sp.tcols = 32;
+  while (sp.tcols < (uint32_t)sp.ntiles * kDN * 2) sp.tcols *= 2;
+  sp.NSR = sp.K / kDK;
+  sp.wbytes = sp.N * kDK * 2;
+  sp.stride = sp.wbytes + 1024;  // activation boxes, padded so every stage starts 1 KB aligned
+  sp.nst = std::min(kDMaxStages, kDRing / sp.stride);
+  if (sp.nst < 2) return false;
+  sp.G = G;
+  sp.jcap = jcap;
+  *out = sp;
+  return true;
+}
+
+static size_t sk_smem(const SkPass& sp) { return 1024 + (size_t)sp.nst * sp.stride + (2 * kDMaxStages + 5) * 8; }
+
+bool sk_eligible(const FfnArgs& a) {
+  const int n = a.T * a.k;
+  if (!a.pool_only || a.S <= 0 || n > kDMaxRows) return false;
+  if ((uintptr_t)a.x % 16 || (uintptr_t)a.pool % 16 || (uintptr_t)a.skp % 256 || (uintptr_t)a.y % 16) return false;
+  SkCarve c;
+  if (!sk_carve(a, &c)) return false;
+  SkPass g, d;
+  return sk_pass(false, a, 1, nullptr, c.jg, &g) && sk_pass(true, a, 1, nullptr, c.jd, &d);
+}
+
+template <typename K, typename... Args>
+static cudaError_t sk_launch(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
+                             Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+int launch_ffn_sk(const FfnArgs& a, int max_list, cudaStream_t stream, Prof* prof) {
+  int dev = 0, sms = 0;
+  MOE_CUDA_TRY(cudaGetDevice(&dev));
+  MOE_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  const int n = a.T * a.k;
+  SkCarve c;
+  if (!sk_carve(a, &c)) return MOE_ERR_ARG;
+  SkPass g, d;
+  if (!sk_pass(false, a, sms, c.gpart, c.jg, &g) || !sk_pass(true, a, sms, c.ypart, c.jd, &d)) return MOE_ERR_ARG;
+  static bool done_g[64] = {}, done_d[64] = {};
+  // the limit is raised once per device, to the largest ring any shape uses
+  constexpr int kSmemMax = 1024 + kDRing + (2 * kDMaxStages + 5) * 8;
+  MOE_CUDA_TRY(ensure_smem(ffn_sk_kernel<false>, kSmemMax, done_g));
+  MOE_CUDA_TRY(ensure_smem(ffn_sk_kernel<true>, kSmemMax, done_d));
+  const size_t mat = (size_t)a.H * a.I;
+  CUtensorMap mwg, mwd, mx, mh;
+  {
+    const uint64_t dims[3] = {(uint64_t)a.I, (uint64_t)a.H, 3ull * a.S};
+    const uint64_t str[2] = {(uint64_t)a.I * 2, mat * 2};
+    const uint32_t box[3] = {64, kDK, 1};
+    if (encode_tmap_3d_bf16(&mwg, a.pool, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B) != MOE_OK) return MOE_ERR_CUDA;
+  }
+  {
+    const uint64_t dims[3] = {(uint64_t)a.H, (uint64_t)a.I, 3ull * a.S};
+    const uint64_t str[2] = {(uint64_t)a.H * 2, mat * 2};
+    const uint32_t box[3] = {64, kDK, 1};
+    if (encode_tmap_3d_bf16(&mwd, a.pool, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B) != MOE_OK) return MOE_ERR_CUDA;
+  }
+  {
+    const uint64_t dims[3] = {(uint64_t)a.H, (uint64_t)n, 1};
+    const uint64_t str[2] = {(uint64_t)a.H * 2, (uint64_t)n * a.H * 2};
+    const uint32_t box[3] = {8, kDN, 1};
+    if (encode_tmap_3d_bf16(&mx, c.xp, dims, str, box, CU_TENSOR_MAP_SWIZZLE_NONE) != MOE_OK) return MOE_ERR_CUDA;
+  }
+  {
+    const uint64_t dims[3] = {(uint64_t)a.I, (uint64_t)n, 1};
+    const uint64_t str[2] = {(uint64_t)a.I * 2, (uint64_t)n * a.I * 2};
+    const uint32_t box[3] = {8, kDN, 1};
+    if (encode_tmap_3d_bf16(&mh, c.hb, dims, str, box, CU_TENSOR_MAP_SWIZZLE_NONE) != MOE_OK) return MOE_ERR_CUDA;
+  }
+  const dim3 rg_gu((a.I / 4 + kSkRedThreads - 1) / kSkRedThreads, max_list);
+  const dim3 rg_d((a.H / 4 + kSkRedThreads - 1) / kSkRedThreads, max_list);
+  if (prof) prof->begin(MOE_PROF_FFN_GATEUP, stream);
+  int r = launch_gather_rows(a.x, a.rows, n, a.H, a.k, c.xp, sms, stream);
+  if (r != MOE_OK) return r;
+  MOE_CUDA_TRY(sk_launch(ffn_sk_kernel<false>, dim3(sms), dim3(kDThreads), sk_smem(g), stream, true, a, g, mwg, mx));
+  MOE_CUDA_TRY(sk_launch(sk_reduce_kernel<true>, rg_gu, dim3(kSkRedThreads), 0, stream, true, a,
+                         (const float*)c.gpart, g.N, g.NSR, g.G, g.jcap, (float*)nullptr, c.hb));
+  if (prof) prof->end(stream);
+  if (prof) prof->begin(MOE_PROF_FFN_DOWN, stream);
+  MOE_CUDA_TRY(sk_launch(ffn_sk_kernel<true>, dim3(sms), dim3(kDThreads), sk_smem(d), stream, true, a, d, mwd, mh));
+  MOE_CUDA_TRY(sk_launch(sk_reduce_kernel<false>, rg_d, dim3(kSkRedThreads), 0, stream, true, a,
+                         (const float*)c.ypart, d.N, d.NSR, d.G, d.jcap, a.y, (uint16_t*)nullptr));
+  if (prof) prof->end(stream);
+  return MOE_OK;
+}
+
+}  // namespace moe

@@ -24,6 +24,8 @@ struct FfnArgs {
   uint16_t* xp;           // bf16 [T*k][H] grouped copy of x (tensor-core path), or NULL
   uint16_t* hb;           // bf16 [T*k][I] h for the tensor-core path, or NULL
   uint16_t* yb;           // tensor-core path: write y as bf16 [T*k][H] here instead of fp32 y (or NULL)
+  float* skp;             // partial sums of the decode stream path (sk_part_bytes), or NULL
+  size_t skp_bytes;
 };
 
 // Records (start, end) event pairs around kernel launches when tracing is on.
@@ -57,6 +59,11 @@ struct Prof {
 
 int launch_ffn(const FfnArgs& a, int max_list, cudaStream_t stream, Prof* prof = nullptr);
 bool prefill_eligible(const FfnArgs& a, int n);
+int launch_gather_rows(const uint16_t* x, const int32_t* rows, int n, int H, int k, uint16_t* xp, int sms,
+                       cudaStream_t stream);
+size_t sk_part_bytes(int n, int H, int I);
+bool sk_eligible(const FfnArgs& a);
+int launch_ffn_sk(const FfnArgs& a, int max_list, cudaStream_t stream, Prof* prof);
 size_t prefill_extra_bytes(int n, int H, int I);
 int launch_prefill(const FfnArgs& a, int n, int max_list, cudaStream_t stream, Prof* prof);
 int launch_combine(const float* y, const float* w, const int32_t* pos, const int32_t* ids, const int32_t* e2s, int T,

@@ -22,7 +22,7 @@
 // TMEM, two 256-column buffers so the epilogue of one tile overlaps the MMAs
 // of the next.
 #include "internal.cuh"
-#include "tma.cuh"
+#include "tc05.cuh"
 
 namespace moe {
 
@@ -39,59 +39,14 @@ constexpr int kPrefillMinRows = 4096;
 // per epilogue warp: a 32 x 33 fp32 transpose buffer (padded: conflict-free)
 constexpr int kEpiBuf = 32 * 33;
 
-// Instruction descriptor, kind::f16: D fp32, A and B bf16, A K-major,
-// B MN-major, N = 256, M = 128.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (0u << 15) | (1u << 16) |
-                            (uint32_t(kPN >> 3) << 17) | (uint32_t(kPM >> 4) << 24);
+// Instruction descriptor: D fp32, A and B bf16, A K-major, B MN-major, N = 256, M = 128.
+constexpr uint32_t kIdesc = idesc_bf16(kPM, kPN, 0, 1);
 
 __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-  return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
-         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
-}
-
-__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)), "r"(ncols)
-               : "memory");
-}
-__device__ __forceinline__ void tmem_relinquish() {
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+  return smem_desc_l(saddr, lbo, sbo, kLayoutSw128);
 }
 __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n"
-      " .reg .pred p;\n"
-      " setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n"
-      "}\n" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
-      : "memory");
-}
-__device__ __forceinline__ void umma_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-               : "memory");
-}
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-
-// 32 lanes x 32 consecutive fp32 columns: thread (lane) gets its row's 32 values.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[32];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr)
-      : "memory");
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+  umma_f16(d_tmem, adesc, bdesc, kIdesc, accumulate);
 }
 
 struct PrefillArgs {
@@ -345,6 +300,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const Prefil
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __restrict__ x,
                                                           const int32_t* __restrict__ rows, int n, int H, int k,
                                                           uint16_t* __restrict__ xp) {
+  pdl_trigger();
   const int H8 = H / 8;
   for (int p = blockIdx.x; p < n; p += gridDim.x) {
     const int t = rows[p] / k;
@@ -352,6 +308,13 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __rest
     uint4* dst = reinterpret_cast<uint4*>(xp + (size_t)p * H);
     for (int v = threadIdx.x; v < H8; v += blockDim.x) dst[v] = src[v];
   }
+}
+
+int launch_gather_rows(const uint16_t* x, const int32_t* rows, int n, int H, int k, uint16_t* xp, int sms,
+                       cudaStream_t stream) {
+  gather_rows_kernel<<<std::min(n, sms * 8), 256, 0, stream>>>(x, rows, n, H, k, xp);
+  MOE_LAUNCH_CHECK();
+  return MOE_OK;
 }
 
 static size_t prefill_smem_bytes() {

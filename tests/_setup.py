@@ -35,6 +35,12 @@ def assert_out_close(got, want, what="out"):
     assert ma <= ATOL_OUT and rl <= RL2_OUT, f"{what}: max-abs {ma:.3e} rel-L2 {rl:.3e}"
 
 
+# The tensor-core FFN paths hand h to the down projection in bf16: rounding
+# h (relative 2^-9, random sign) gives y a relative L2 error of about
+# 2^-9 / sqrt(3) ~ 1.1e-3.
+RL2_Y_BF16_H = 5e-3
+
+
 def assert_f32_close(got, want, what="y"):
     rl = rel_l2(got, want)
     assert rl <= RL2_F32, f"{what}: rel-L2 {rl:.3e}"
