@@ -23,9 +23,15 @@
 // Roles: warp 0 loads (TMA), warp 1 issues the MMAs, warps 2-5 move finished
 // accumulators (TMEM, double-buffered) to the parts.  Every wait is bounded.
 //
-// The activations (x grouped by expert, or h) come from the kernel before in
-// the stream; each pass is launched as a programmatic dependent and streams
-// its first weight stages before it waits (griddepcontrol.wait) for them.
+// Activations, per stage and token batch: the gate/up pass copies batches of
+// one or two tokens straight from x (16-byte bulk copies, one per token and 8
+// rows), larger batches from x grouped by expert (two boxes of 8 rows x 16
+// tokens, written by a row gather launched just before); the down pass copies
+// the batch's h rows (bf16, grouped order) that the gate/up reduce wrote.
+// Both passes are launched as programmatic dependents: they set up and stream
+// their first weight stages before they wait (griddepcontrol.wait) for the
+// kernel before them, and the gate/up pass waits only when a batch needs the
+// grouped rows (and once before it exits).
 #include <algorithm>
 
 #include "internal.cuh"
@@ -45,6 +51,7 @@ constexpr uint32_t kDTmemMax = 512;
 constexpr int kDJcapMax = 160;
 constexpr size_t kDPartBudget = size_t(16) << 20;  // bytes of parts per pass (soft cap)
 constexpr int kDMaxRows = 4096;
+constexpr int kDDirectMax = 2;  // gate/up batches of at most this many tokens read x directly
 constexpr uint32_t kDIdesc = idesc_bf16(kDM, kDN, 1, 0);
 
 struct SkPass {
@@ -97,6 +104,26 @@ __device__ __forceinline__ void sk_segments(const FfnArgs& a, const SkPass& sp, 
   }
 }
 
+// Accumulator columns 0..W-1 (tokens) of every tile -> parts; loads of up to
+// 32 registers are issued before one wait.
+template <int W>
+__device__ __forceinline__ void sk_epilogue(uint32_t taddr, float* base, const SkPass& sp, int nb) {
+  constexpr int G = W >= 32 ? 1 : 32 / W;
+  for (int m0 = 0; m0 < sp.ntiles; m0 += G) {
+    float v[G][W];
+#pragma unroll
+    for (int gi = 0; gi < G; ++gi)
+      if (m0 + gi < sp.ntiles) tmem_ld_w<W>(taddr + (m0 + gi) * kDN, v[gi]);
+    tmem_ld_wait();
+#pragma unroll
+    for (int gi = 0; gi < G; ++gi)
+      if (m0 + gi < sp.ntiles)
+#pragma unroll
+        for (int t = 0; t < W; ++t)
+          if (t < nb) base[(size_t)t * sp.N + (m0 + gi) * kDM] = v[gi][t];
+  }
+}
+
 template <bool DOWN>
 __global__ void __launch_bounds__(kDThreads, 1) ffn_sk_kernel(const FfnArgs a, const SkPass sp,
                                                               const __grid_constant__ CUtensorMap mw,
@@ -113,12 +140,20 @@ __global__ void __launch_bounds__(kDThreads, 1) ffn_sk_kernel(const FfnArgs a, c
   __shared__ int s_abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   pdl_trigger();
+  if (threadIdx.x == 0) {
+    prefetch_tmap(&mw);
+    prefetch_tmap(&mact);
+  }
+  // the lists predate the kernel before (the row gather, or the gate/up reduce)
   const int n_list = *a.n_list;
   const int n = a.T * a.k;
   const int L = n_list > 0 ? sk_len(n_list, sp.NSR, sp.G, sp.jcap) : 1;
   const int total = n_list * sp.NSR;
   const int beg = blockIdx.x * L, end = min(beg + L, total);
-  if (beg >= end) return;  // uniform over the CTA: nothing allocated yet
+  if (beg >= end) {  // uniform over the CTA: nothing allocated yet
+    pdl_wait();       // still complete only after the kernel before
+    return;
+  }
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < sp.nst; ++s) {
@@ -131,10 +166,6 @@ __global__ void __launch_bounds__(kDThreads, 1) ffn_sk_kernel(const FfnArgs a, c
     }
     mbar_init(done, 1);
     s_abort = 0;
-    for (int li = beg / sp.NSR; li * sp.NSR < end; ++li) {
-      int e, slot;
-      if (!sk_slot(a, li, e, slot)) set_status(a.status, e < 0 || e >= a.E ? MOE_DEV_BAD_EXPERT : MOE_DEV_BAD_SLOT);
-    }
     mbar_fence_init();
   }
   if (warp == 1) {
@@ -154,6 +185,7 @@ __global__ void __launch_bounds__(kDThreads, 1) ffn_sk_kernel(const FfnArgs a, c
       bool waited = false;
       int ndef = 0, d_row[kDMaxStages], d_p0[kDMaxStages], last_use[kDMaxStages];
       for (int s = 0; s < kDMaxStages; ++s) last_use[s] = -1;
+      // rows p0..p0+15 of x grouped (gate/up) or of h (down), 8 rows per box -> core matrices [k group][token][8]
       auto issue_act = [&](int sl, int row0, int p0) {
         unsigned char* dst = ring + sl * sp.stride + sp.wbytes;
         tma_load_3d(dst, &mact, &full[sl], row0, p0, 0);
@@ -166,13 +198,17 @@ __global__ void __launch_bounds__(kDThreads, 1) ffn_sk_kernel(const FfnArgs a, c
         ndef = 0;
         waited = true;
       };
-      const int nbox = sp.N / 64;
       sk_segments(a, sp, L, beg, end, [&](const SkSeg& g) {
+        const bool direct = !DOWN && g.nb <= kDDirectMax;
+        int tok[kDDirectMax];
+        if (direct)
+          for (int t = 0; t < g.nb; ++t) tok[t] = a.rows[g.p0 + t] / a.k;
+        if (!DOWN && !direct && !waited) flush();  // grouped rows: the row gather must be done
         for (int s = g.s_lo; s < g.s_hi; ++s, ++it) {
           const int sl = it % sp.nst;
           const uint32_t use = it / sp.nst;
           if (use > 0) {
-            if (!waited) flush();
+            if (DOWN && !waited) flush();  // h copies deferred so far must go before a slot is reused
             if (!*abort_flag && !mbar_wait(&empty[sl], (use - 1) & 1u)) {
               *abort_flag = 1;
               set_status(a.status, MOE_DEV_TIMEOUT);
@@ -181,18 +217,23 @@ __global__ void __launch_bounds__(kDThreads, 1) ffn_sk_kernel(const FfnArgs a, c
           if (*abort_flag) return false;
           unsigned char* dst = ring + sl * sp.stride;
           const int row0 = s * kDK;
-          mbar_expect_tx(&full[sl], sp.wbytes + 2 * kDActBox);
+          mbar_expect_tx(&full[sl], sp.wbytes + (direct ? g.nb * 32 : 2 * kDActBox));
+          // weights: one 4-D box per matrix = 16 rows x all columns, as 64-column swizzle atoms 2 KB apart
           if (DOWN) {
-            for (int c = 0; c < nbox; ++c)
-              tma_load_3d(dst + c * kDBoxBytes, &mw, &full[sl], 64 * c, row0, 3 * g.slot + 2);
+            tma_load_4d(dst, &mw, &full[sl], 0, row0, 0, 3 * g.slot + 2);
           } else {
-            const int hb = nbox / 2;  // boxes per matrix
-            for (int c = 0; c < hb; ++c) {
-              tma_load_3d(dst + c * kDBoxBytes, &mw, &full[sl], 64 * c, row0, 3 * g.slot);
-              tma_load_3d(dst + (hb + c) * kDBoxBytes, &mw, &full[sl], 64 * c, row0, 3 * g.slot + 1);
-            }
+            tma_load_4d(dst, &mw, &full[sl], 0, row0, 0, 3 * g.slot);
+            tma_load_4d(dst + sp.wbytes / 2, &mw, &full[sl], 0, row0, 0, 3 * g.slot + 1);
           }
-          if (waited) {
+          if (direct) {
+            // x[token][row0 .. row0+15] -> core matrices [k group][token][8]: 16-byte bulk copies
+            unsigned char* act = dst + sp.wbytes;
+            for (int t = 0; t < g.nb; ++t) {
+              const uint16_t* xr = a.x + (size_t)tok[t] * a.H + row0;
+              bulk_load(act + t * 16, xr, 16, &full[sl]);
+              bulk_load(act + kDActBox + t * 16, xr + 8, 16, &full[sl]);
+            }
+          } else if (waited) {
             issue_act(sl, row0, g.p0);
           } else {
             d_row[ndef] = row0;
@@ -203,7 +244,8 @@ __global__ void __launch_bounds__(kDThreads, 1) ffn_sk_kernel(const FfnArgs a, c
         }
         return true;
       });
-      // every issued stage gets its activation copies, so every full barrier completes
+      // every issued stage gets its activation copies, so every full barrier completes;
+      // and the kernel before has completed before this one does
       if (!waited) flush();
       if (*abort_flag)
         for (int s = 0; s < sp.nst; ++s)
@@ -211,6 +253,10 @@ __global__ void __launch_bounds__(kDThreads, 1) ffn_sk_kernel(const FfnArgs a, c
     }
   } else if (warp == 1) {
     if (lane == 0) {
+      for (int li = beg / sp.NSR; li * sp.NSR < end; ++li) {
+        int e, slot;
+        if (!sk_slot(a, li, e, slot)) set_status(a.status, e < 0 || e >= a.E ? MOE_DEV_BAD_EXPERT : MOE_DEV_BAD_SLOT);
+      }
       uint32_t it = 0, seg = 0;
       sk_segments(a, sp, L, beg, end, [&](const SkSeg& g) {
         const uint32_t buf = seg & 1u, use = seg >> 1;
@@ -260,14 +306,17 @@ __global__ void __launch_bounds__(kDThreads, 1) ffn_sk_kernel(const FfnArgs a, c
       tc_fence_after();
       if (!*abort_flag) {
         float* base = sp.part + ((size_t)g.j * n + g.p0) * sp.N + q * 32 + lane;
-        for (int m = 0; m < sp.ntiles; ++m) {
-          float v[16];
-          tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + buf * acc_cols + m * kDN, v);
-          tmem_ld_wait();
-#pragma unroll
-          for (int t = 0; t < kDN; ++t)
-            if (t < g.nb) base[(size_t)t * sp.N + m * kDM] = v[t];
-        }
+        const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + buf * acc_cols;
+        if (g.nb <= 1)
+          sk_epilogue<1>(taddr, base, sp, g.nb);
+        else if (g.nb <= 2)
+          sk_epilogue<2>(taddr, base, sp, g.nb);
+        else if (g.nb <= 4)
+          sk_epilogue<4>(taddr, base, sp, g.nb);
+        else if (g.nb <= 8)
+          sk_epilogue<8>(taddr, base, sp, g.nb);
+        else
+          sk_epilogue<16>(taddr, base, sp, g.nb);
       }
       tc_fence_before();
       __syncwarp();
@@ -276,6 +325,8 @@ __global__ void __launch_bounds__(kDThreads, 1) ffn_sk_kernel(const FfnArgs a, c
       return true;
     });
   }
+  // warps 0 and 1 ran their loops on lane 0 alone: reconverge before the CTA barrier
+  __syncwarp();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -284,35 +335,49 @@ __global__ void __launch_bounds__(kDThreads, 1) ffn_sk_kernel(const FfnArgs a, c
   }
 }
 
-// Adds the parts of each listed expert's rows in j order.
+// Adds the parts of each listed expert's rows: warp w sums parts j = w, w+8,
+// ..., then the 8 warp sums are added in warp order (fixed).
 //   SWIGLU: hb [n][I] bf16 = silu(sum g) * (sum u); parts hold [g | u]
 //   else:   y [n][H] fp32 = sum of parts
-constexpr int kSkRedThreads = 128;
+// A block covers 128 columns (32 lanes x float4) of one listed expert's rows.
+constexpr int kSkRedWarps = 8;
 
 template <bool SWIGLU>
-__global__ void __launch_bounds__(kSkRedThreads) sk_reduce_kernel(const FfnArgs a, const float* __restrict__ part,
-                                                                  int N, int NSR, int G, int jcap,
-                                                                  float* __restrict__ y, uint16_t* __restrict__ hb) {
+__global__ void __launch_bounds__(32 * kSkRedWarps) sk_reduce_kernel(const FfnArgs a, const float* __restrict__ part,
+                                                                     int N, int NSR, int G, int jcap,
+                                                                     float* __restrict__ y,
+                                                                     uint16_t* __restrict__ hb) {
+  __shared__ float4 sg[kSkRedWarps][32], su[kSkRedWarps][32];
   pdl_trigger();
-  pdl_wait();
+  // the lists and offsets predate the pass before: read them while it finishes
   const int li = blockIdx.y;
   const int n_list = *a.n_list;
-  if (li >= n_list) return;
+  if (li >= n_list) {
+    pdl_wait();  // complete only after the pass before (ordering for later kernels)
+    return;
+  }
   int e, slot;
-  if (!sk_slot(a, li, e, slot)) return;
+  if (!sk_slot(a, li, e, slot)) {
+    pdl_wait();
+    return;
+  }
   const int L = sk_len(n_list, NSR, G, jcap);
   const int j0 = (li * NSR) / L;
   const int J = ((li + 1) * NSR - 1) / L - j0 + 1;
   const int n = a.T * a.k;
   const int ncol = SWIGLU ? N / 2 : N;
   const int ncol4 = ncol / 4;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int c4 = blockIdx.x * 32 + lane;
   const int pb = a.offset[e], pe = a.offset[e + 1];
   const size_t pstride = (size_t)n * N;
+  pdl_wait();
   for (int p = pb; p < pe; ++p) {
-    for (int c4 = blockIdx.x * kSkRedThreads + threadIdx.x; c4 < ncol4; c4 += gridDim.x * kSkRedThreads) {
+    float4 g = make_float4(0.f, 0.f, 0.f, 0.f), u = g;
+    if (c4 < ncol4) {
       const float* src = part + (size_t)p * N + 4 * c4;
-      float4 g = make_float4(0.f, 0.f, 0.f, 0.f), u = g;
-      for (int jj = 0; jj < J; ++jj) {
+#pragma unroll 4
+      for (int jj = w; jj < J; jj += kSkRedWarps) {
         const float4 t = *reinterpret_cast<const float4*>(src + jj * pstride);
         g.x += t.x;
         g.y += t.y;
@@ -326,17 +391,37 @@ __global__ void __launch_bounds__(kSkRedThreads) sk_reduce_kernel(const FfnArgs 
           u.w += v.w;
         }
       }
+    }
+    sg[w][lane] = g;
+    if (SWIGLU) su[w][lane] = u;
+    __syncthreads();
+    if (w == 0 && c4 < ncol4) {
+      for (int k2 = 1; k2 < kSkRedWarps; ++k2) {
+        const float4 t = sg[k2][lane];
+        g.x += t.x;
+        g.y += t.y;
+        g.z += t.z;
+        g.w += t.w;
+        if (SWIGLU) {
+          const float4 v = su[k2][lane];
+          u.x += v.x;
+          u.y += v.y;
+          u.z += v.z;
+          u.w += v.w;
+        }
+      }
       if (SWIGLU) {
         const float h0 = g.x / (1.f + expf(-g.x)) * u.x, h1 = g.y / (1.f + expf(-g.y)) * u.y;
         const float h2 = g.z / (1.f + expf(-g.z)) * u.z, h3 = g.w / (1.f + expf(-g.w)) * u.w;
-        uint2 w;
-        w.x = uint32_t(f32_to_bf16(h0)) | (uint32_t(f32_to_bf16(h1)) << 16);
-        w.y = uint32_t(f32_to_bf16(h2)) | (uint32_t(f32_to_bf16(h3)) << 16);
-        *reinterpret_cast<uint2*>(hb + (size_t)p * ncol + 4 * c4) = w;
+        uint2 wv;
+        wv.x = uint32_t(f32_to_bf16(h0)) | (uint32_t(f32_to_bf16(h1)) << 16);
+        wv.y = uint32_t(f32_to_bf16(h2)) | (uint32_t(f32_to_bf16(h3)) << 16);
+        *reinterpret_cast<uint2*>(hb + (size_t)p * ncol + 4 * c4) = wv;
       } else {
         *reinterpret_cast<float4*>(y + (size_t)p * ncol + 4 * c4) = g;
       }
     }
+    __syncthreads();
   }
 }
 
@@ -357,8 +442,8 @@ static size_t sk_half_bytes(int n, int H, int I) {
 }
 
 // Layout: [gate/up parts | down parts] (two equal halves), then x grouped by
-// expert (bf16 [n][H]) and h (bf16 [n][I]).  A chunk smaller than the one the
-// buffer was sized for gets as many parts as fit.
+// expert (bf16 [n][H]) and h (bf16 [n][I], grouped order).  A chunk smaller
+// than the one the buffer was sized for gets as many parts as fit.
 size_t sk_part_bytes(int n, int H, int I) {
   if (n < 1 || n > kDMaxRows) return 0;
   return 2 * sk_half_bytes(n, H, I) + al256((size_t)n * H * 2) + al256((size_t)n * I * 2);
@@ -450,17 +535,18 @@ int launch_ffn_sk(const FfnArgs& a, int max_list, cudaStream_t stream, Prof* pro
   MOE_CUDA_TRY(ensure_smem(ffn_sk_kernel<true>, kSmemMax, done_d));
   const size_t mat = (size_t)a.H * a.I;
   CUtensorMap mwg, mwd, mx, mh;
+  // weight matrices viewed as [matrix][column atom][row][64 columns]: one box = 16 rows x all columns
   {
-    const uint64_t dims[3] = {(uint64_t)a.I, (uint64_t)a.H, 3ull * a.S};
-    const uint64_t str[2] = {(uint64_t)a.I * 2, mat * 2};
-    const uint32_t box[3] = {64, kDK, 1};
-    if (encode_tmap_3d_bf16(&mwg, a.pool, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B) != MOE_OK) return MOE_ERR_CUDA;
+    const uint64_t dims[4] = {64, (uint64_t)a.H, (uint64_t)a.I / 64, 3ull * a.S};
+    const uint64_t str[3] = {(uint64_t)a.I * 2, 128, mat * 2};
+    const uint32_t box[4] = {64, kDK, (uint32_t)a.I / 64, 1};
+    if (encode_tmap_bf16(&mwg, a.pool, 4, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B) != MOE_OK) return MOE_ERR_CUDA;
   }
   {
-    const uint64_t dims[3] = {(uint64_t)a.H, (uint64_t)a.I, 3ull * a.S};
-    const uint64_t str[2] = {(uint64_t)a.H * 2, mat * 2};
-    const uint32_t box[3] = {64, kDK, 1};
-    if (encode_tmap_3d_bf16(&mwd, a.pool, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B) != MOE_OK) return MOE_ERR_CUDA;
+    const uint64_t dims[4] = {64, (uint64_t)a.I, (uint64_t)a.H / 64, 3ull * a.S};
+    const uint64_t str[3] = {(uint64_t)a.H * 2, 128, mat * 2};
+    const uint32_t box[4] = {64, kDK, (uint32_t)a.H / 64, 1};
+    if (encode_tmap_bf16(&mwd, a.pool, 4, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B) != MOE_OK) return MOE_ERR_CUDA;
   }
   {
     const uint64_t dims[3] = {(uint64_t)a.H, (uint64_t)n, 1};
@@ -474,18 +560,19 @@ int launch_ffn_sk(const FfnArgs& a, int max_list, cudaStream_t stream, Prof* pro
     const uint32_t box[3] = {8, kDN, 1};
     if (encode_tmap_3d_bf16(&mh, c.hb, dims, str, box, CU_TENSOR_MAP_SWIZZLE_NONE) != MOE_OK) return MOE_ERR_CUDA;
   }
-  const dim3 rg_gu((a.I / 4 + kSkRedThreads - 1) / kSkRedThreads, max_list);
-  const dim3 rg_d((a.H / 4 + kSkRedThreads - 1) / kSkRedThreads, max_list);
+  const dim3 rg_gu((a.I / 4 + 31) / 32, max_list);
+  const dim3 rg_d((a.H / 4 + 31) / 32, max_list);
+  const dim3 rb(32 * kSkRedWarps);
   if (prof) prof->begin(MOE_PROF_FFN_GATEUP, stream);
   int r = launch_gather_rows(a.x, a.rows, n, a.H, a.k, c.xp, sms, stream);
   if (r != MOE_OK) return r;
   MOE_CUDA_TRY(sk_launch(ffn_sk_kernel<false>, dim3(sms), dim3(kDThreads), sk_smem(g), stream, true, a, g, mwg, mx));
-  MOE_CUDA_TRY(sk_launch(sk_reduce_kernel<true>, rg_gu, dim3(kSkRedThreads), 0, stream, true, a,
+  MOE_CUDA_TRY(sk_launch(sk_reduce_kernel<true>, rg_gu, rb, 0, stream, true, a,
                          (const float*)c.gpart, g.N, g.NSR, g.G, g.jcap, (float*)nullptr, c.hb));
   if (prof) prof->end(stream);
   if (prof) prof->begin(MOE_PROF_FFN_DOWN, stream);
   MOE_CUDA_TRY(sk_launch(ffn_sk_kernel<true>, dim3(sms), dim3(kDThreads), sk_smem(d), stream, true, a, d, mwd, mh));
-  MOE_CUDA_TRY(sk_launch(sk_reduce_kernel<false>, rg_d, dim3(kSkRedThreads), 0, stream, true, a,
+  MOE_CUDA_TRY(sk_launch(sk_reduce_kernel<false>, rg_d, rb, 0, stream, true, a,
                          (const float*)c.ypart, d.N, d.NSR, d.G, d.jcap, a.y, (uint16_t*)nullptr));
   if (prof) prof->end(stream);
   return MOE_OK;

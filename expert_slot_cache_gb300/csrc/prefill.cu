@@ -288,6 +288,8 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const Prefil
       if (lane == 0) mbar_arrive(&tempty[acc]);
     }
   }
+  // warps 0 and 1 ran their loops on lane 0 alone: reconverge before the CTA barrier
+  __syncwarp();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
