@@ -261,6 +261,83 @@ __global__ void __launch_bounds__(kRouteThreads) logits_block_kernel(const uint1
   }
 }
 
+// logits_tile_kernel (large T): CTA = 64 tokens x 64 experts x one 128-row
+// block, 128 threads; writes part[b][t][e].  The tile is converted to fp32
+// in shared memory once (x token-minor, Wr expert-minor); thread (tx, ty)
+// owns experts 4tx..4tx+3 and tokens 8ty..8ty+7, each chain an fma over the
+// block's rows in order (packed fp32 pairs along the experts).  topk_kernel
+// adds the parts in block order.
+constexpr int kTT = 64;   // tokens per tile
+constexpr int kTE = 64;   // experts per tile
+constexpr int kTileThreads = 128;
+
+__global__ void __launch_bounds__(kTileThreads) logits_tile_kernel(const uint16_t* __restrict__ x,
+                                                                  const uint16_t* __restrict__ wr, int T, int H,
+                                                                  int E, float* __restrict__ part) {
+  extern __shared__ __align__(16) float tsm[];
+  float* xf = tsm;               // [kHC][kTT]
+  float* wf = tsm + kHC * kTT;   // [kHC][kTE]
+  const int tid = threadIdx.x;
+  const int t0 = blockIdx.x * kTT, e0 = blockIdx.y * kTE, b = blockIdx.z;
+  const int h0 = b * kHC;
+  const int hn = min(kHC, H - h0);  // a multiple of 8
+  // x rows: chunk v = (token r, 8 rows q): lanes take consecutive tokens, so the
+  // transposed fp32 stores of a warp hit 32 different banks
+  for (int v = tid; v < kTT * (kHC / 8); v += kTileThreads) {
+    const int r = v % kTT, q = v / kTT;
+    uint4 u = make_uint4(0u, 0u, 0u, 0u);
+    if (t0 + r < T && 8 * q < hn) u = *reinterpret_cast<const uint4*>(x + (size_t)(t0 + r) * H + h0 + 8 * q);
+    float* d = xf + (8 * q) * kTT + r;
+    d[0 * kTT] = bf16_lo(u.x);
+    d[1 * kTT] = bf16_hi(u.x);
+    d[2 * kTT] = bf16_lo(u.y);
+    d[3 * kTT] = bf16_hi(u.y);
+    d[4 * kTT] = bf16_lo(u.z);
+    d[5 * kTT] = bf16_hi(u.z);
+    d[6 * kTT] = bf16_lo(u.w);
+    d[7 * kTT] = bf16_hi(u.w);
+  }
+  // Wr rows: chunk v = (row r, 8 experts q)
+  for (int v = tid; v < kHC * (kTE / 8); v += kTileThreads) {
+    const int r = v / (kTE / 8), q = v % (kTE / 8);
+    uint4 u = make_uint4(0u, 0u, 0u, 0u);
+    if (r < hn && e0 + 8 * q < E) u = *reinterpret_cast<const uint4*>(wr + (size_t)(h0 + r) * E + e0 + 8 * q);
+    float4* d = reinterpret_cast<float4*>(wf + r * kTE + 8 * q);
+    d[0] = make_float4(bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y));
+    d[1] = make_float4(bf16_lo(u.z), bf16_hi(u.z), bf16_lo(u.w), bf16_hi(u.w));
+  }
+  __syncthreads();
+  const int tx = tid & 15, ty = tid >> 4;
+  uint64_t acc[8][2];
+#pragma unroll
+  for (int t = 0; t < 8; ++t) acc[t][0] = acc[t][1] = 0ull;
+#pragma unroll 4
+  for (int h = 0; h < hn; ++h) {
+    const float4 wv = *reinterpret_cast<const float4*>(wf + h * kTE + 4 * tx);
+    const float4 xa = *reinterpret_cast<const float4*>(xf + h * kTT + 8 * ty);
+    const float4 xb = *reinterpret_cast<const float4*>(xf + h * kTT + 8 * ty + 4);
+    const uint64_t w01 = rf2_pack(wv.x, wv.y), w23 = rf2_pack(wv.z, wv.w);
+    const float xs[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+      const uint64_t xx = rf2_pack(xs[t], xs[t]);
+      rf2_fma(acc[t][0], w01, xx);
+      rf2_fma(acc[t][1], w23, xx);
+    }
+  }
+  const int e = e0 + 4 * tx;
+  if (e < E) {  // E % 8 == 0, so all four experts are in range together
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+      const int tt = t0 + 8 * ty + t;
+      if (tt < T) {
+        const float2 a01 = rf2_unpack(acc[t][0]), a23 = rf2_unpack(acc[t][1]);
+        *reinterpret_cast<float4*>(part + ((size_t)b * T + tt) * E + e) = make_float4(a01.x, a01.y, a23.x, a23.y);
+      }
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------
 // Top-k: one warp per token.  k rounds of a warp-wide argmax over
 // score = logit + bias (ties -> lower id); the winner is marked taken.
@@ -271,33 +348,34 @@ __global__ void __launch_bounds__(kRouteThreads) topk_kernel(float* __restrict__
                                                              const int32_t* __restrict__ e2s, float affinity,
                                                              const float* __restrict__ part, int nb,
                                                              const float* __restrict__ off, int T, int E, int k,
-                                                             int32_t* __restrict__ ids, float* __restrict__ wout) {
+                                                             int tpc, int32_t* __restrict__ ids,
+                                                             float* __restrict__ wout) {
   __shared__ float sel_l[kRouteThreads / 32][kMaxK];
   __shared__ int sel_i[kRouteThreads / 32][kMaxK];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int tb = blockIdx.x * (kRouteThreads / 32);
+  const int tb = blockIdx.x * tpc;  // tokens tb .. tb+tpc-1, one warp each (tpc <= 8)
   if (part) {
     // finish this CTA's logits from the block parts: 0 + part_0 + part_1 + ...
-    // (all parts loaded before the in-order sum), then the offset
-    const int nt = min(kRouteThreads / 32, T - tb);
+    // (a value's parts are loaded, 16 at a time, before its in-order sum), then the offset
+    const int nt = min(tpc, T - tb);
+    const size_t bstride = (size_t)T * E;
     for (int v = threadIdx.x; v < nt * E; v += kRouteThreads) {
       const int tl = v / E, e = v - tl * E;
       const float* pp = part + (size_t)(tb + tl) * E + e;
-      const size_t bstride = (size_t)T * E;
       float l = 0.f;
-      int b = 0;
-      for (; b + 8 <= nb; b += 8) {
-        float pv[8];
+      for (int b = 0; b < nb; b += 16) {
+        float pv[16];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) pv[u] = pp[(size_t)(b + u) * bstride];
+        for (int u = 0; u < 16; ++u) pv[u] = b + u < nb ? pp[(size_t)(b + u) * bstride] : 0.f;
 #pragma unroll
-        for (int u = 0; u < 8; ++u) l += pv[u];
+        for (int u = 0; u < 16; ++u)
+          if (b + u < nb) l += pv[u];
       }
-      for (; b < nb; ++b) l += pp[(size_t)b * bstride];
       logits[(size_t)(tb + tl) * E + e] = off ? l + off[e] : l;
     }
     __syncthreads();
   }
+  if (warp >= tpc) return;
   const int t = tb + warp;
   if (t >= T) return;
   float* lrow = logits + (size_t)t * E;
@@ -368,7 +446,7 @@ extern "C" int moe_bias_table(const float* b, int E, int n_hot, float cap, float
 }
 
 extern "C" size_t moe_route_scratch_bytes(int T, int H, int E) {
-  if (T < 1 || H < 1 || E < 1 || T > 256) return 0;
+  if (T < 1 || H < 1 || E < 1) return 0;
   return (size_t)((H + kHC - 1) / kHC) * T * E * sizeof(float);
 }
 
@@ -391,8 +469,25 @@ extern "C" int moe_route(const void* x, const void* w_router, const float* logit
     const dim3 grid(nblk, eb, (T + 7) / 8);
     logits_block_kernel<1><<<grid, kRouteThreads, 0, s>>>(xb, wb, T, H, E, scratch);
     MOE_LAUNCH_CHECK();
-    topk_kernel<<<(T + 7) / 8, kRouteThreads, 0, s>>>(logits, sel_bias, e2s, affinity, scratch, nblk, logit_offset,
-                                                      T, E, k, ids, w);
+    // tokens per CTA: 8 while that fills the SMs, else 2 (each thread then finishes about one logit)
+    const int tpc = (T + 7) / 8 >= sms ? 8 : 2;
+    topk_kernel<<<(T + tpc - 1) / tpc, kRouteThreads, 0, s>>>(logits, sel_bias, e2s, affinity, scratch, nblk,
+                                                              logit_offset, T, E, k, tpc, ids, w);
+    MOE_LAUNCH_CHECK();
+    return MOE_OK;
+  }
+  if (scratch && moe_route_scratch_bytes(T, H, E) > 0 && E % 4 == 0) {
+    // many tokens: (64 tokens, 64 experts, 128-row block) tiles, parts added in block order by the top-k
+    constexpr int smem = (kHC * kTT + kHC * kTE) * (int)sizeof(float);
+    static bool dt[64] = {};
+    MOE_CUDA_TRY(ensure_smem(logits_tile_kernel, smem, dt));
+    const dim3 grid((T + kTT - 1) / kTT, (E + kTE - 1) / kTE, nblk);
+    logits_tile_kernel<<<grid, kTileThreads, smem, s>>>(xb, wb, T, H, E, scratch);
+    MOE_LAUNCH_CHECK();
+    // tokens per CTA: 8 while that fills the SMs, else 2 (each thread then finishes about one logit)
+    const int tpc = (T + 7) / 8 >= sms ? 8 : 2;
+    topk_kernel<<<(T + tpc - 1) / tpc, kRouteThreads, 0, s>>>(logits, sel_bias, e2s, affinity, scratch, nblk,
+                                                              logit_offset, T, E, k, tpc, ids, w);
     MOE_LAUNCH_CHECK();
     return MOE_OK;
   }
@@ -422,7 +517,7 @@ extern "C" int moe_route(const void* x, const void* w_router, const float* logit
   }
   MOE_LAUNCH_CHECK();
   topk_kernel<<<(T + 7) / 8, kRouteThreads, 0, s>>>(logits, sel_bias, e2s, affinity, nullptr, 0, nullptr, T, E, k,
-                                                    ids, w);
+                                                    8, ids, w);
   MOE_LAUNCH_CHECK();
   return MOE_OK;
 }

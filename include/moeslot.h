@@ -91,9 +91,10 @@ int moe_bias_table(const float* b, int E, int n_hot, float cap, float* bias, moe
  *                e2s[e] >= 0 get `affinity` added to their selection score
  *                (after the bias, fp32).  NULL / 0 = off.
  *   logits       device fp32 [T][E] output (unbiased logits)
- *   scratch      device, moe_route_scratch_bytes(T, H, E) bytes, or NULL: with
- *                it a small batch spreads its 128-row blocks over more CTAs
- *                (the result is the same)
+ *   scratch      device, moe_route_scratch_bytes(T, H, E) bytes (one fp32 [T][E]
+ *                part per 128-row block), or NULL: with it the 128-row blocks
+ *                are spread over more CTAs and the parts added in block order
+ *                (the result is the same bit for bit)
  *   ids          device int32 [T][k] output, descending score, ties -> lower id
  *   w            device fp32 [T][k] output, sums to 1 per token
  * logit[t][e] is accumulated in fp32 in one fixed order: h is cut into

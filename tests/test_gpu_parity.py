@@ -54,6 +54,9 @@ ROUTE_CASES = [
     ("flash_T16_bias", C.FLASH, -1.0, False),
     ("stack_T32_E288", C.STACK, None, False),
     ("prefill_T4096_offset", C.PREFILL, None, True),
+    # enough tokens for the (64 tokens x 64 experts x 128 rows) tile path: ragged token and expert tiles
+    ("qwen_T300_tiles", C.qwen(300), None, False),
+    ("stack_T200_E288_tiles", C.STACK.with_(T=200), None, False),
 ]
 
 
