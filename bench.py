@@ -41,6 +41,10 @@ sys.path.insert(0, ROOT)
 
 from harness import configs as C  # noqa: E402
 
+# DRAM bytes (read + write) of gather_kernel per missed Qwen-shaped expert, from an ncu capture of
+# the gather_T8 workload: 161,741,568 B written + 224,512 B read for a launch of 17 misses (the host
+# side travels over NVLink-C2C and is not DRAM traffic).  Valid while the gather kernel is unchanged.
+GATHER_DRAM_BYTES_PER_MISS = (161_741_568 + 224_512) / 17
 METRIC = "MoE-layer tokens/s at 1 GB300; decode HBM GB/s vs roofline; prefill TFLOP/s"
 UNIT = "tokens/s"
 PROF_NAMES = ("route", "permute", "manage", "gather", "ffn_gateup", "ffn_down", "combine", "ffn_rows")
@@ -507,8 +511,11 @@ def main():
     if dominant == "gather":
         t = kern["gather"] * 1e-3
         ach = r["gathered_bytes"] / t / 1e9 if t > 0 else 0.0
+        n_launch = max(1, r["launches"].get("gather", 0))
         roof = {"bound": "host-link", "achieved": ach, "peak": link_peak, "unit": "GB/s", "frac": ach / link_peak,
-                "traffic": None, "kernel": "gather", "bytes_per_unit": cfg.slab_bytes,
+                "traffic": GATHER_DRAM_BYTES_PER_MISS * r["misses"] / n_launch,
+                "traffic_unit": "bytes per launch (ncu dram read + write per miss x misses per launch)",
+                "kernel": "gather", "bytes_per_unit": cfg.slab_bytes,
                 "units": r["misses"], "peak_source": "pinned-host->device cudaMemcpyAsync measured in this run"}
     else:
         roof = ffn_roofline(wl, r, units, peaks)
@@ -520,8 +527,7 @@ def main():
             "gpu_launches": sum(r["launches"].values()),
             "kernels_ms_per_step": {n: v / K for n, v in kern.items()},
             "misses_per_step": r["misses"] / K, "gathered_GB_per_step": r["gathered_bytes"] / K / 1e9,
-            "host_link_peak_gbs": link_peak,
-            "roofline_ffn_hbm": ffn_roofline(wl, r, units, peaks)}
+            "host_link_peak_gbs": link_peak}
     line["e2e"] = e2e_steps(wl, K, W, dist)
     del wl
     torch.cuda.empty_cache()
