@@ -22,6 +22,13 @@ Sources (web pages; cited by title and section):
           "Designing a fixed expert cache with zero-return for missing
           experts": a missing expert returns zeros; a second pass over the
           missing experts is added, which gives exactly the full result.
+  [SGB2]  same PGO-SGB page, introduction (two ways to use a profile: a hard
+          mask, cold experts can never be picked; or a soft bias) and the KL
+          comparison of a graded bias against a flat one (a flat -0.75,
+          -0.5, -1); "Qwen on Strata" (selection-only against damped
+          weights: the bias also enters the weights); "The same idea on
+          GLM-5.3-Flash" (GLM's router is a sigmoid and the bias is added
+          after the sigmoid, in probability space).
 
 Precision.  Router logits decide integers (the top-k ids), so they are taken
 in fp32 in one fixed order that the kernels follow as well: h is cut into
@@ -51,6 +58,15 @@ Readings of points the pages leave open (each listed in the design notes):
     in turn; S < k cannot be served.
   * zero-return: residency is e2s[e] >= 0 after a STATIC manage; the output is
     the sum of the resident partial and the missing partial.
+  * bias modes: graded (the formula above), flat (every cold expert gets one
+    constant), hard mask (cold experts get -inf, so they are never picked
+    while k hot experts exist).
+  * damped weights: w = softmax over the k picked of logit + bias (the bias
+    table only; affinity stays selection-only).
+  * sigmoid router: s = sigmoid(logit); pick top-k by s + bias; weights =
+    the picked experts' sigmoid values normalised to sum 1 (the router's own
+    probabilities).  So that the ids are reproducible bit for bit, the fp32
+    sigmoid is defined operation by operation (exp32 below).
 """
 from __future__ import annotations
 
@@ -89,8 +105,13 @@ def router_logits(x: np.ndarray, wr: np.ndarray, logit_offset=None) -> np.ndarra
     return acc
 
 
-def bias_table(b: np.ndarray, n_hot: int, cap: float) -> np.ndarray:
-    """Soft selection bias for one layer: 0 on the hot set, else max(cap, ln(b/b_edge))."""
+BIAS_GRADED, BIAS_FLAT, BIAS_HARD = 0, 1, 2
+
+
+def bias_table(b: np.ndarray, n_hot: int, cap: float, mode: int = BIAS_GRADED) -> np.ndarray:
+    """Selection bias for one layer: 0 on the hot set; on cold experts
+    max(cap, ln(b/b_edge)) (graded, [SGB]), the constant ``cap`` (flat) or
+    -inf (hard mask) [SGB2]."""
     b = np.asarray(b, dtype=np.float32)
     E = b.shape[0]
     order = sorted(range(E), key=lambda e: (-float(b[e]), e))
@@ -100,21 +121,72 @@ def bias_table(b: np.ndarray, n_hot: int, cap: float) -> np.ndarray:
     for e in range(E):
         if e in hot:
             continue
-        be = float(b[e])
-        val = cap if be <= 0.0 else max(cap, float(np.log(be / b_edge)))
-        out[e] = np.float32(val)
+        if mode == BIAS_FLAT:
+            out[e] = np.float32(cap)
+        elif mode == BIAS_HARD:
+            out[e] = np.float32(-np.inf)
+        else:
+            be = float(b[e])
+            val = cap if be <= 0.0 else max(cap, float(np.log(be / b_edge)))
+            out[e] = np.float32(val)
     return out
 
 
-def select_topk(logits: np.ndarray, k: int, bias=None, resident=None, affinity: float = 0.0) -> np.ndarray:
+# fp32 exp, defined operation by operation (each an IEEE fp32 multiply, add or
+# subtract, none fused), after Cody and Waite's argument reduction: n = the
+# integer nearest x*log2(e), r = x - n*ln2 with ln2 split into a short high
+# part (n*LN2_HI is exact) and a low part, then the degree-7 Taylor polynomial
+# of e^r in Horner form, scaled by 2^n.  exp32(x) = +inf above 88 and 0 below
+# -80 (the sigmoid saturates there); in between 2^n stays a normal number.
+_F = np.float32
+_LOG2E = _F(float.fromhex("0x1.715476p+0"))
+_LN2_HI = _F(float.fromhex("0x1.63p-1"))
+_LN2_LO = _F(float.fromhex("-0x1.bd0106p-13"))
+_TAYLOR = [_F(float.fromhex(h)) for h in ("0x1.a01a02p-13", "0x1.6c16c2p-10", "0x1.111112p-7",
+                                           "0x1.555556p-5", "0x1.555556p-3", "0x1p-1", "0x1p+0", "0x1p+0")]
+
+
+def exp32(x) -> np.ndarray:
+    x = np.asarray(x, dtype=np.float32)
+    with np.errstate(over="ignore", under="ignore", invalid="ignore"):
+        n = np.rint(x * _LOG2E).astype(np.float32)
+        r = (x - n * _LN2_HI).astype(np.float32)
+        r = (r - n * _LN2_LO).astype(np.float32)
+        p = _TAYLOR[0]
+        for c in _TAYLOR[1:]:
+            p = (p * r).astype(np.float32)
+            p = (p + c).astype(np.float32)
+        ni = np.clip(n, -126, 127).astype(np.int32)
+        scale = ((ni + 127).astype(np.uint32) << np.uint32(23)).view(np.float32)
+        out = (p * scale).astype(np.float32)
+    out = np.where(x > _F(88.0), _F(np.inf), out)
+    out = np.where(x < _F(-80.0), _F(0.0), out)
+    return out.astype(np.float32)
+
+
+def sigmoid32(l) -> np.ndarray:
+    """fp32 sigmoid 1 / (1 + exp32(-l)): one fp32 add and one IEEE fp32 divide."""
+    l = np.asarray(l, dtype=np.float32)
+    with np.errstate(over="ignore"):
+        d = (_F(1.0) + exp32(-l)).astype(np.float32)
+        return (_F(1.0) / d).astype(np.float32)
+
+
+ROUTER_SOFTMAX, ROUTER_SIGMOID = 0, 1
+
+
+def select_topk(logits: np.ndarray, k: int, bias=None, resident=None, affinity: float = 0.0,
+                router: int = ROUTER_SOFTMAX) -> np.ndarray:
     """ids[t][0..k-1]: the k largest fp32 scores, descending, ties -> lower id.
 
-    score = logit + bias (when a bias is given), then + affinity for experts
-    resident in VRAM right now (live-cache affinity: "Nudge, don't cut",
-    "Then Maya's own knob beat ours"), each add in fp32.
+    score = logit (softmax router) or sigmoid32(logit) (sigmoid router, [SGB2]),
+    + bias when a bias is given, then + affinity for experts resident in VRAM
+    right now (live-cache affinity: "Nudge, don't cut", "Then Maya's own knob
+    beat ours"), each add in fp32.
     """
     logits = np.asarray(logits, dtype=np.float32)
-    scores = logits if bias is None else (logits + np.asarray(bias, dtype=np.float32)[None, :])
+    base = sigmoid32(logits) if router == ROUTER_SIGMOID else logits
+    scores = base if bias is None else (base + np.asarray(bias, dtype=np.float32)[None, :]).astype(np.float32)
     if resident is not None and affinity != 0.0:
         lam = np.where(np.asarray(resident, dtype=bool), np.float32(affinity), np.float32(0.0)).astype(np.float32)
         scores = np.where(lam[None, :] != 0, scores + lam[None, :], scores).astype(np.float32)
@@ -126,21 +198,37 @@ def select_topk(logits: np.ndarray, k: int, bias=None, resident=None, affinity: 
     return ids
 
 
-def route_weights(logits: np.ndarray, ids: np.ndarray) -> np.ndarray:
-    """w[t][j] = exp(logit[t][ids[t][j]]) / sum_j' exp(logit[t][ids[t][j']]), fp64, unbiased logits."""
+def route_weights(logits: np.ndarray, ids: np.ndarray, router: int = ROUTER_SOFTMAX, bias=None,
+                  damped: bool = False) -> np.ndarray:
+    """Routing weights over the k picked, fp64.
+
+    softmax router: w[t][j] = exp(z_j) / sum_j' exp(z_j'), z = the unbiased
+    logit (selection-only, [SGB]) or logit + bias (damped weights, [SGB2]);
+    sigmoid router: w[t][j] = s_j / sum_j' s_j', s = sigmoid(logit) [SGB2].
+    """
     T, k = ids.shape
     w = np.empty((T, k), dtype=np.float64)
+    bz = None if (bias is None or not damped) else np.asarray(bias, dtype=np.float64)
     for t in range(T):
         l = np.array([float(logits[t, e]) for e in ids[t]], dtype=np.float64)
+        if router == ROUTER_SIGMOID:
+            sv = 1.0 / (1.0 + np.exp(-l))
+            w[t] = sv / sv.sum()
+            continue
+        if bz is not None:
+            l = l + np.array([bz[e] for e in ids[t]])
         p = np.exp(l - l.max())
         w[t] = p / p.sum()
     return w
 
 
-def route(x, wr, k, logit_offset=None, bias=None, resident=None, affinity=0.0):
+def route(x, wr, k, logit_offset=None, bias=None, resident=None, affinity=0.0, router=ROUTER_SOFTMAX,
+          damped=False):
+    if router == ROUTER_SIGMOID and damped:
+        raise ValueError("damped weights are defined for the softmax router only")
     logits = router_logits(x, wr, logit_offset)
-    ids = select_topk(logits, k, bias, resident, affinity)
-    return ids, route_weights(logits, ids), logits
+    ids = select_topk(logits, k, bias, resident, affinity, router)
+    return ids, route_weights(logits, ids, router, bias, damped), logits
 
 
 # ----------------------------------------------------------------------------
@@ -329,7 +417,7 @@ def combine(y, w, pos, T, k, resident=None):
 # ----------------------------------------------------------------------------
 
 def layer_forward(x, wr, host, H, I, k, mode, policy=LRU, state=None, pool=None,
-                  logit_offset=None, bias=None, affinity=0.0):
+                  logit_offset=None, bias=None, affinity=0.0, router=ROUTER_SOFTMAX, damped=False):
     """One MoE layer forward with the slot cache.
 
     ``host`` [E][3HI] holds every expert (authoritative copy); ``pool``
@@ -341,7 +429,7 @@ def layer_forward(x, wr, host, H, I, k, mode, policy=LRU, state=None, pool=None,
     T = x.shape[0]
     E = wr.shape[1]
     resident = None if (state is None or affinity == 0.0) else state.e2s >= 0
-    ids, w, logits = route(x, wr, k, logit_offset, bias, resident, affinity)
+    ids, w, logits = route(x, wr, k, logit_offset, bias, resident, affinity, router, damped)
     out = np.zeros((T, H))
     out_res = np.zeros((T, H))
     out_miss = np.zeros((T, H))

@@ -471,3 +471,81 @@ def test_affinity_zero_or_nothing_resident_is_plain_topk():
     # a large affinity picks only resident experts while at least k are resident
     ids = O.select_topk(logits, 5, resident=res, affinity=100.0)
     assert res[ids].all()
+
+
+# ----------------------------------------------------------------------------
+# Routing variants ("Nudge, don't cut": hard mask, flat bias, damped weights,
+# GLM's sigmoid router)
+# ----------------------------------------------------------------------------
+
+def _ulp32(v):
+    v = np.abs(np.asarray(v, dtype=np.float64))
+    return np.spacing(v.astype(np.float32)).astype(np.float64)
+
+
+def test_exp32_within_two_ulp_of_the_exact_exponential():
+    xs = np.concatenate([np.linspace(-80.0, 88.0, 400001, dtype=np.float32),
+                         np.array([0.0, 1.0, -1.0, 0.5, 1e-8, -1e-8, 0.34657, -0.34657, 0.6931472], np.float32)])
+    got = O.exp32(xs).astype(np.float64)
+    want = np.exp(xs.astype(np.float64))
+    assert np.all(np.abs(got - want) <= 2 * _ulp32(want))
+    assert O.exp32(np.float32(0.0)) == np.float32(1.0)
+    assert O.exp32(np.float32(89.0)) == np.float32(np.inf) and O.exp32(np.float32(-81.0)) == 0.0
+
+
+def test_sigmoid32_within_three_ulp_and_symmetric():
+    ls = np.linspace(-30.0, 30.0, 200001, dtype=np.float32)
+    got = O.sigmoid32(ls).astype(np.float64)
+    want = 1.0 / (1.0 + np.exp(-ls.astype(np.float64)))
+    assert np.all(np.abs(got - want) <= 3 * _ulp32(want))
+    assert O.sigmoid32(np.float32(0.0)) == np.float32(0.5)
+    assert np.all(np.abs(O.sigmoid32(ls).astype(np.float64) + O.sigmoid32(-ls).astype(np.float64) - 1.0) < 2e-7)
+
+
+def test_bias_modes_golden():
+    g = _gold("route_variants.json")["bias_modes"]
+    b = np.array(g["b"], dtype=np.float32)
+    assert O.bias_table(b, g["n_hot"], g["flat_value"], O.BIAS_FLAT).tolist() == g["flat"]
+    hard = O.bias_table(b, g["n_hot"], -1.0, O.BIAS_HARD)
+    want = [float(v) for v in g["hard"]]
+    assert hard.tolist() == want
+
+
+def test_hard_mask_picks_the_top_k_of_the_hot_set():
+    rng = np.random.default_rng(5)
+    E, k, n_hot = 40, 6, 12
+    b = rng.random(E).astype(np.float32)
+    bias = O.bias_table(b, n_hot, -1.0, O.BIAS_HARD)
+    hot = np.isfinite(bias)
+    logits = rng.normal(size=(9, E)).astype(np.float32)
+    ids = O.select_topk(logits, k, bias)
+    masked = np.where(hot[None, :], logits.astype(np.float64), -np.inf)
+    want = np.argsort(-masked, axis=1, kind="stable")[:, :k]
+    assert np.array_equal(ids, want)
+
+
+def test_damped_and_selection_only_weights_golden():
+    g = _gold("route_variants.json")["damped"]
+    logits = np.array([g["logits"]], dtype=np.float32)
+    bias = np.array(g["bias"], dtype=np.float32)
+    ids, w, _ = _route_from_logits(logits, g["k"], bias, damped=True)
+    assert ids[0].tolist() == g["ids"]
+    assert np.allclose(w[0], g["w_damped"], rtol=0, atol=1e-12)
+    ids, w, _ = _route_from_logits(logits, g["k"], bias, damped=False)
+    assert np.allclose(w[0], g["w_select_only"], rtol=0, atol=1e-12)
+
+
+def test_sigmoid_router_golden():
+    g = _gold("route_variants.json")["sigmoid"]
+    logits = np.array([g["logits"]], dtype=np.float32)
+    bias = np.array(g["bias"], dtype=np.float32)
+    ids, w, _ = _route_from_logits(logits, g["k"], bias, router=O.ROUTER_SIGMOID)
+    assert ids[0].tolist() == g["ids_sigmoid"]
+    assert np.allclose(w[0], g["w_sigmoid"], rtol=0, atol=1e-12)
+    ids, _, _ = _route_from_logits(logits, g["k"], bias, router=O.ROUTER_SOFTMAX)
+    assert ids[0].tolist() == g["ids_softmax"]
+
+
+def _route_from_logits(logits, k, bias, router=0, damped=False):
+    ids = O.select_topk(logits, k, bias, router=router)
+    return ids, O.route_weights(logits, ids, router, bias, damped), logits
