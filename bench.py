@@ -223,6 +223,35 @@ class StackWorkload:
         self.stack.x_all.copy_(self.inputs[st])
 
 
+def routing_variants(dev: str, steps: int = 10, warmup: int = 3) -> dict:
+    """The Flash-Next zero-return layer (512 experts, top-10, the 192 brightest
+    in VRAM slots, STATIC) under each way of using the brightness profile
+    ("Nudge, don't cut": no bias, graded bias at two caps, a flat bias, a hard
+    mask, damped weights, GLM's sigmoid router with a graded bias): step time
+    and missing experts per step (each one a second-pass read over the host
+    link)."""
+    import expert_slot_cache_gb300 as M
+    cfg = C.FLASH
+    wl = Workload(cfg, 2 * steps + warmup, dev)
+    b, _ = C.draw_brightness(cfg)
+    bd = torch.from_numpy(b).to(dev)
+    arms = [("none", None, None, 0), ("graded_cap-1", M.BIAS_GRADED, -1.0, 0),
+            ("graded_cap-0.5", M.BIAS_GRADED, -0.5, 0), ("flat-0.5", M.BIAS_FLAT, -0.5, 0),
+            ("hard_mask", M.BIAS_HARD, 0.0, 0), ("damped_graded_cap-1", M.BIAS_GRADED, -1.0, M.ROUTE_DAMPED),
+            ("sigmoid_graded_cap-0.25", M.BIAS_GRADED, -0.25, M.ROUTE_SIGMOID)]
+    out = {"workload": "flash-next-shaped zero-return layer, T=16, E=512, k=10, H=2048, I=512, S=192 STATIC "
+                       "(the 192 brightest), Zipf(1.1) brightness"}
+    for name, mode, val, rf in arms:
+        wl.layer.sel_bias = None if mode is None else M.bias_table(bd, cfg.n_hot, val, mode=mode)
+        wl.layer.route_flags = rf
+        r = time_steps(wl, steps, warmup, profile=False)
+        out[name] = {"ms_per_step": r["ms"] / steps, "tokens_per_s": cfg.T * steps / (r["ms"] * 1e-3),
+                     "missing_experts_per_step": r["misses"] / steps,
+                     "host_link_GB_per_step": r["misses"] / steps * cfg.slab_bytes / 1e9}
+    del wl
+    return out
+
+
 def policy_replay(trace: np.ndarray, E: int, S: int, dev: str, slab_bytes: int) -> dict:
     """Replay one routing trace through expert_cache_manage under each policy
     ("Porting vllm-expert-cache to NVIDIA GPUs", "Measuring, without fooling
@@ -466,7 +495,7 @@ def main():
     ap.add_argument("--no-variants", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="main",
-                    help="main (default) | prefill | resident_T<n> | gather_T<n>: one workload alone "
+                    help="main (default) | prefill | resident_T<n> | gather_T<n> | routing_variants: one workload alone "
                          "(for profiling); prints its own JSON line")
     args = ap.parse_args()
     ws, rank, local, dist = _dist()
@@ -479,6 +508,10 @@ def main():
     torch.cuda.set_device(local)
     dev = f"cuda:{local}"
     peaks = _peaks()
+    if args.workload == "routing_variants":
+        if rank == 0:
+            print(json.dumps({"workload": "routing_variants", **routing_variants(dev, args.steps, args.warmup)}))
+        return
     if args.workload != "main":
         w = args.workload
         if w == "prefill":
@@ -572,6 +605,8 @@ def main():
         torch.cuda.empty_cache()
         var["policy_replay"] = policy_replay(C.drifting_trace(cfg.E, cfg.k, 8, 400), cfg.E, cfg.S, dev,
                                              cfg.slab_bytes)
+        torch.cuda.empty_cache()
+        var["routing_variants"] = routing_variants(dev)
         line["variants"] = var
 
     if not args.no_cpu_baseline and rank == 0:

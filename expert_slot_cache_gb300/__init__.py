@@ -9,4 +9,5 @@ This package only marshals arguments.  Build the library first with
 from .binding import (MODE_GATHER, MODE_RESIDENT, MODE_ZERO_RETURN, POLICY_LFU, POLICY_LRU,  # noqa: F401
                       POLICY_STATIC, CacheState, LayerArgs, MoeError, SlotCachedMoELayer, bias_table,
                       cache_gather, cache_manage, combine, expert_ffn, ffn_workspace_bytes, layer_workspace_bytes,
-                      lib, permute, route, status_str, LayerStack)
+                      lib, permute, route, status_str, LayerStack, BIAS_GRADED, BIAS_FLAT, BIAS_HARD,
+                      ROUTE_SIGMOID, ROUTE_DAMPED)

@@ -47,7 +47,7 @@ class LayerArgs(ctypes.Structure):
                 ("ids", c_void_p), ("w", c_void_p), ("out", c_void_p), ("out_res", c_void_p),
                 ("out_miss", c_void_p), ("stats", c_void_p), ("dev_status", c_void_p),
                 ("workspace", c_void_p), ("workspace_bytes", c_size_t), ("prof", POINTER(Prof)),
-                ("affinity", c_float)]
+                ("affinity", c_float), ("route_flags", c_int32)]
 
 
 def _sig(name, argtypes, restype=c_int):
@@ -61,7 +61,12 @@ V = c_void_p
 I32 = c_int
 _status_str = _sig("moe_status_str", [c_int], ctypes.c_char_p)
 _bias_table = _sig("moe_bias_table", [V, I32, I32, c_float, V, V])
+_bias_table_mode = _sig("moe_bias_table_mode", [V, I32, I32, I32, c_float, V, V])
 _route = _sig("moe_route", [V, V, V, V, V, c_float, I32, I32, I32, I32, V, V, V, V, V])
+_route_ex = _sig("moe_route_ex", [V, V, V, V, V, c_float, I32, I32, I32, I32, I32, V, V, V, V, V])
+
+BIAS_GRADED, BIAS_FLAT, BIAS_HARD = 0, 1, 2
+ROUTE_SIGMOID, ROUTE_DAMPED = 1, 2
 _route_scratch = _sig("moe_route_scratch_bytes", [I32, I32, I32], c_size_t)
 _permute = _sig("moe_permute", [V, I32, I32, V, V, V, V, V, V, V, V, V])
 _permute_scratch = _sig("moe_permute_scratch_bytes", [I32, I32], c_size_t)
@@ -106,14 +111,17 @@ def _s(stream=None):
 # Single calls
 # ---------------------------------------------------------------------------
 
-def bias_table(b: torch.Tensor, n_hot: int, cap: float, stream=None) -> torch.Tensor:
+def bias_table(b: torch.Tensor, n_hot: int, cap: float, stream=None, mode: int = BIAS_GRADED) -> torch.Tensor:
     out = torch.empty_like(b)
-    _ck(_bias_table(_p(b), b.numel(), n_hot, cap, _p(out), _s(stream)), "moe_bias_table")
+    if mode == BIAS_GRADED:
+        _ck(_bias_table(_p(b), b.numel(), n_hot, cap, _p(out), _s(stream)), "moe_bias_table")
+    else:
+        _ck(_bias_table_mode(_p(b), b.numel(), n_hot, mode, cap, _p(out), _s(stream)), "moe_bias_table_mode")
     return out
 
 
 def route(x, w_router, k, logit_offset=None, sel_bias=None, return_logits=False, stream=None, blocked=True,
-          e2s=None, affinity=0.0):
+          e2s=None, affinity=0.0, rflags=0):
     T, H = x.shape
     E = w_router.shape[1]
     ids = torch.empty(T, k, dtype=torch.int32, device=x.device)
@@ -121,8 +129,12 @@ def route(x, w_router, k, logit_offset=None, sel_bias=None, return_logits=False,
     logits = torch.empty(T, E, dtype=torch.float32, device=x.device)
     nb = int(_route_scratch(T, H, E)) if blocked else 0
     scratch = torch.empty(max(nb // 4, 1), dtype=torch.float32, device=x.device) if nb else None
-    _ck(_route(_p(x), _p(w_router), _p(logit_offset), _p(sel_bias), _p(e2s), affinity, T, H, E, k, _p(logits),
-               _p(scratch), _p(ids), _p(w), _s(stream)), "moe_route")
+    if rflags:
+        _ck(_route_ex(_p(x), _p(w_router), _p(logit_offset), _p(sel_bias), _p(e2s), affinity, rflags, T, H, E, k,
+                      _p(logits), _p(scratch), _p(ids), _p(w), _s(stream)), "moe_route_ex")
+    else:
+        _ck(_route(_p(x), _p(w_router), _p(logit_offset), _p(sel_bias), _p(e2s), affinity, T, H, E, k,
+                   _p(logits), _p(scratch), _p(ids), _p(w), _s(stream)), "moe_route")
     return (ids, w, logits) if return_logits else (ids, w)
 
 
@@ -247,7 +259,8 @@ class SlotCachedMoELayer:
     """
 
     def __init__(self, w_router, pool, k, I, mode, policy=POLICY_LRU, host_slabs=None, state=None,
-                 logit_offset=None, sel_bias=None, max_tokens=64, side_stream=True, affinity=0.0):
+                 logit_offset=None, sel_bias=None, max_tokens=64, side_stream=True, affinity=0.0,
+                 route_flags=0):
         self.w_router, self.pool, self.k, self.I = w_router, pool, k, I
         self.H, self.E = w_router.shape
         self.S = pool.shape[0]
@@ -255,6 +268,7 @@ class SlotCachedMoELayer:
         self.host_slabs, self.state = host_slabs, state
         self.logit_offset, self.sel_bias = logit_offset, sel_bias
         self.affinity = float(affinity)
+        self.route_flags = int(route_flags)
         dev = pool.device
         self.stats = torch.zeros(4, dtype=torch.int64, device=dev)
         self.dev_status = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -282,7 +296,8 @@ class SlotCachedMoELayer:
                       _ptr(st.prio if st else None), _ptr(st.stamp if st else None),
                       ids.data_ptr(), w.data_ptr(), out.data_ptr(), _ptr(out_res), _ptr(out_miss),
                       self.stats.data_ptr(), self.dev_status.data_ptr(), self.workspace.data_ptr(),
-                      self.workspace.numel(), ctypes.pointer(prof) if prof is not None else None, self.affinity)
+                      self.workspace.numel(), ctypes.pointer(prof) if prof is not None else None, self.affinity,
+                      self.route_flags)
         main = torch.cuda.current_stream() if stream is None else stream
         # the library forks to and joins back from the side stream itself
         _ck(_layer(ctypes.byref(a), c_void_p(main.cuda_stream),

@@ -205,9 +205,9 @@ extern "C" int moe_layer_forward(const moe_layer_args* a, moe_stream_t main_s, m
   if (prof.p) prof.p->used = 0;
   const size_t slab_bytes = (size_t)6 * H * I;
   prof.begin(MOE_PROF_ROUTE, ms);
-  int r = moe_route(a->x, a->w_router, a->logit_offset, a->sel_bias, a->affinity != 0.f ? a->e2s : nullptr,
-                    a->affinity, T, H, E, k, ws.logits, moe_route_scratch_bytes(T, H, E) ? ws.route : nullptr,
-                    a->ids, a->w, main_s);
+  int r = moe_route_ex(a->x, a->w_router, a->logit_offset, a->sel_bias, a->affinity != 0.f ? a->e2s : nullptr,
+                       a->affinity, a->route_flags, T, H, E, k, ws.logits,
+                       moe_route_scratch_bytes(T, H, E) ? ws.route : nullptr, a->ids, a->w, main_s);
   if (r != MOE_OK) return r;
   prof.end(ms);
 

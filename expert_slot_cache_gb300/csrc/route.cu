@@ -15,7 +15,7 @@ namespace moe {
 // Bias table: one CTA of >= E threads (E <= 1024).  Runs once per layer.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(1024) bias_table_kernel(const float* __restrict__ b, int E, int n_hot,
-                                                          float cap, float* __restrict__ bias) {
+                                                          int mode, float cap, float* __restrict__ bias) {
   __shared__ float sb[kMaxE];
   __shared__ int shot[kMaxE];
   const int e = threadIdx.x;
@@ -35,8 +35,14 @@ __global__ void __launch_bounds__(1024) bias_table_kernel(const float* __restric
       if (shot[f]) edge = fminf(edge, sb[f]);
     float v = 0.f;
     if (!shot[e]) {
-      const double be = sb[e];
-      v = be <= 0.0 ? cap : (float)fmax((double)cap, log(be / (double)edge));
+      if (mode == MOE_BIAS_FLAT) {
+        v = cap;
+      } else if (mode == MOE_BIAS_HARD) {
+        v = -INFINITY;
+      } else {
+        const double be = sb[e];
+        v = be <= 0.0 ? cap : (float)fmax((double)cap, log(be / (double)edge));
+      }
     }
     bias[e] = v;
   }
@@ -338,6 +344,34 @@ __global__ void __launch_bounds__(kTileThreads) logits_tile_kernel(const uint16_
   }
 }
 
+// fp32 exp defined operation by operation, so that a score built on it is
+// reproducible bit for bit off the GPU: Cody and Waite's reduction
+// n = rint(x log2 e), r = (x - n LN2_HI) - n LN2_LO (n LN2_HI exact), the
+// degree-7 Taylor polynomial of e^r in Horner form, times 2^n.  Every step is
+// one IEEE fp32 multiply, add or subtract (the _rn intrinsics keep the
+// compiler from fusing them).  +inf above 88, 0 below -80 (2^n stays normal
+// in between).
+__device__ __forceinline__ float exp32_def(float x) {
+  if (x > 88.f) return INFINITY;
+  if (x < -80.f) return 0.f;
+  const float n = rintf(__fmul_rn(x, 0x1.715476p+0f));
+  float r = __fsub_rn(x, __fmul_rn(n, 0x1.63p-1f));
+  r = __fsub_rn(r, __fmul_rn(n, -0x1.bd0106p-13f));
+  float p = 0x1.a01a02p-13f;
+  p = __fadd_rn(__fmul_rn(p, r), 0x1.6c16c2p-10f);
+  p = __fadd_rn(__fmul_rn(p, r), 0x1.111112p-7f);
+  p = __fadd_rn(__fmul_rn(p, r), 0x1.555556p-5f);
+  p = __fadd_rn(__fmul_rn(p, r), 0x1.555556p-3f);
+  p = __fadd_rn(__fmul_rn(p, r), 0x1p-1f);
+  p = __fadd_rn(__fmul_rn(p, r), 1.f);
+  p = __fadd_rn(__fmul_rn(p, r), 1.f);
+  return __fmul_rn(p, __int_as_float(((int)n + 127) << 23));
+}
+
+// Sigmoid router score ("Nudge, don't cut", "The same idea on GLM-5.3-Flash":
+// the bias is added after the sigmoid): 1 / (1 + exp32(-l)), IEEE add and divide.
+__device__ __forceinline__ float sigmoid32_def(float l) { return __fdiv_rn(1.f, __fadd_rn(1.f, exp32_def(-l))); }
+
 // ---------------------------------------------------------------------------
 // Top-k: one warp per token.  k rounds of a warp-wide argmax over
 // score = logit + bias (ties -> lower id); the winner is marked taken.
@@ -348,7 +382,7 @@ __global__ void __launch_bounds__(kRouteThreads) topk_kernel(float* __restrict__
                                                              const int32_t* __restrict__ e2s, float affinity,
                                                              const float* __restrict__ part, int nb,
                                                              const float* __restrict__ off, int T, int E, int k,
-                                                             int tpc, int32_t* __restrict__ ids,
+                                                             int tpc, int rflags, int32_t* __restrict__ ids,
                                                              float* __restrict__ wout) {
   __shared__ float sel_l[kRouteThreads / 32][kMaxK];
   __shared__ int sel_i[kRouteThreads / 32][kMaxK];
@@ -386,7 +420,8 @@ __global__ void __launch_bounds__(kRouteThreads) topk_kernel(float* __restrict__
     const int e = lane + 32 * q;
     float v = 0.f;
     if (e < E) {
-      v = bias ? lrow[e] + bias[e] : lrow[e];
+      const float base = (rflags & MOE_ROUTE_SIGMOID) ? sigmoid32_def(lrow[e]) : lrow[e];
+      v = bias ? __fadd_rn(base, bias[e]) : base;
       if (e2s && affinity != 0.f && e2s[e] >= 0) v = v + affinity;  // live-cache affinity
     }
     sc[q] = v;
@@ -418,9 +453,24 @@ __global__ void __launch_bounds__(kRouteThreads) topk_kernel(float* __restrict__
     if (lane == 0) sel_i[warp][j] = bi;
   }
   __syncwarp();
-  if (lane < k) sel_l[warp][lane] = lrow[sel_i[warp][lane]];
+  if (lane < k) {
+    const int e = sel_i[warp][lane];
+    float z = lrow[e];
+    if (rflags & MOE_ROUTE_SIGMOID) z = sigmoid32_def(z);
+    else if ((rflags & MOE_ROUTE_DAMPED) && bias) z = z + bias[e];  // damped: the bias enters the weights too
+    sel_l[warp][lane] = z;
+  }
   __syncwarp();
-  if (lane == 0) {
+  if (lane == 0 && (rflags & MOE_ROUTE_SIGMOID)) {
+    // the router's own probabilities of the picked k, normalised
+    float sum = 0.f;
+    for (int j = 0; j < k; ++j) sum += sel_l[warp][j];
+    const size_t base = (size_t)t * k;
+    for (int j = 0; j < k; ++j) {
+      ids[base + j] = sel_i[warp][j];
+      wout[base + j] = sel_l[warp][j] / sum;
+    }
+  } else if (lane == 0) {
     float mx = sel_l[warp][0];
     for (int j = 1; j < k; ++j) mx = fmaxf(mx, sel_l[warp][j]);
     float sum = 0.f;
@@ -437,12 +487,18 @@ __global__ void __launch_bounds__(kRouteThreads) topk_kernel(float* __restrict__
 
 using namespace moe;
 
-extern "C" int moe_bias_table(const float* b, int E, int n_hot, float cap, float* bias, moe_stream_t stream) {
+extern "C" int moe_bias_table_mode(const float* b, int E, int n_hot, int mode, float value, float* bias,
+                                   moe_stream_t stream) {
   if (!b || !bias || E < 1 || E > kMaxE || n_hot < 1 || n_hot > E) return MOE_ERR_ARG;
+  if (mode != MOE_BIAS_GRADED && mode != MOE_BIAS_FLAT && mode != MOE_BIAS_HARD) return MOE_ERR_ARG;
   const int threads = ((E + 31) / 32) * 32;
-  bias_table_kernel<<<1, threads, 0, (cudaStream_t)stream>>>(b, E, n_hot, cap, bias);
+  bias_table_kernel<<<1, threads, 0, (cudaStream_t)stream>>>(b, E, n_hot, mode, value, bias);
   MOE_LAUNCH_CHECK();
   return MOE_OK;
+}
+
+extern "C" int moe_bias_table(const float* b, int E, int n_hot, float cap, float* bias, moe_stream_t stream) {
+  return moe_bias_table_mode(b, E, n_hot, MOE_BIAS_GRADED, cap, bias, stream);
 }
 
 extern "C" size_t moe_route_scratch_bytes(int T, int H, int E) {
@@ -450,10 +506,12 @@ extern "C" size_t moe_route_scratch_bytes(int T, int H, int E) {
   return (size_t)((H + kHC - 1) / kHC) * T * E * sizeof(float);
 }
 
-extern "C" int moe_route(const void* x, const void* w_router, const float* logit_offset, const float* sel_bias,
-                         const int32_t* e2s, float affinity, int T, int H, int E, int k, float* logits,
-                         float* scratch, int32_t* ids, float* w, moe_stream_t stream) {
+extern "C" int moe_route_ex(const void* x, const void* w_router, const float* logit_offset, const float* sel_bias,
+                            const int32_t* e2s, float affinity, int rflags, int T, int H, int E, int k,
+                            float* logits, float* scratch, int32_t* ids, float* w, moe_stream_t stream) {
   if (!x || !w_router || !ids || !w || !logits) return MOE_ERR_ARG;
+  if (rflags & ~(MOE_ROUTE_SIGMOID | MOE_ROUTE_DAMPED)) return MOE_ERR_ARG;
+  if ((rflags & MOE_ROUTE_SIGMOID) && (rflags & MOE_ROUTE_DAMPED)) return MOE_ERR_ARG;
   if (T < 1 || H < 8 || H % 8 || E < 1 || E > kMaxE || E % 8 || k < 1 || k > kMaxK || k > E) return MOE_ERR_ARG;
   if ((uintptr_t)x % 16 || (uintptr_t)w_router % 16) return MOE_ERR_ALIGN;
   int sms = 0, dev = 0;
@@ -472,7 +530,7 @@ extern "C" int moe_route(const void* x, const void* w_router, const float* logit
     // tokens per CTA: 8 while that fills the SMs, else 2 (each thread then finishes about one logit)
     const int tpc = (T + 7) / 8 >= sms ? 8 : 2;
     topk_kernel<<<(T + tpc - 1) / tpc, kRouteThreads, 0, s>>>(logits, sel_bias, e2s, affinity, scratch, nblk,
-                                                              logit_offset, T, E, k, tpc, ids, w);
+                                                              logit_offset, T, E, k, tpc, rflags, ids, w);
     MOE_LAUNCH_CHECK();
     return MOE_OK;
   }
@@ -487,7 +545,7 @@ extern "C" int moe_route(const void* x, const void* w_router, const float* logit
     // tokens per CTA: 8 while that fills the SMs, else 2 (each thread then finishes about one logit)
     const int tpc = (T + 7) / 8 >= sms ? 8 : 2;
     topk_kernel<<<(T + tpc - 1) / tpc, kRouteThreads, 0, s>>>(logits, sel_bias, e2s, affinity, scratch, nblk,
-                                                              logit_offset, T, E, k, tpc, ids, w);
+                                                              logit_offset, T, E, k, tpc, rflags, ids, w);
     MOE_LAUNCH_CHECK();
     return MOE_OK;
   }
@@ -517,7 +575,14 @@ extern "C" int moe_route(const void* x, const void* w_router, const float* logit
   }
   MOE_LAUNCH_CHECK();
   topk_kernel<<<(T + 7) / 8, kRouteThreads, 0, s>>>(logits, sel_bias, e2s, affinity, nullptr, 0, nullptr, T, E, k,
-                                                    8, ids, w);
+                                                    8, rflags, ids, w);
   MOE_LAUNCH_CHECK();
   return MOE_OK;
+}
+
+extern "C" int moe_route(const void* x, const void* w_router, const float* logit_offset, const float* sel_bias,
+                         const int32_t* e2s, float affinity, int T, int H, int E, int k, float* logits,
+                         float* scratch, int32_t* ids, float* w, moe_stream_t stream) {
+  return moe_route_ex(x, w_router, logit_offset, sel_bias, e2s, affinity, 0, T, H, E, k, logits, scratch, ids, w,
+                      stream);
 }

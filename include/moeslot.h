@@ -76,6 +76,20 @@ const char* moe_status_str(int status);
  */
 int moe_bias_table(const float* b, int E, int n_hot, float cap, float* bias, moe_stream_t stream);
 
+/* Bias table modes ("Nudge, don't cut", introduction: "Hard mask: cold
+ * experts can never be picked" vs a soft bias; and its comparison of the
+ * graded bias with a flat one). */
+#define MOE_BIAS_GRADED 0 /* cold: max(value, ln(b / b_edge)), as moe_bias_table with cap = value */
+#define MOE_BIAS_FLAT 1   /* cold: value (one constant, e.g. -0.5) */
+#define MOE_BIAS_HARD 2   /* cold: -inf, so a cold expert is never picked while k hot experts exist */
+
+/*
+ * The bias table in any of the three modes; hot experts get 0 in all of them.
+ * Arguments and errors as moe_bias_table; MOE_ERR_ARG also for an unknown mode.
+ */
+int moe_bias_table_mode(const float* b, int E, int n_hot, int mode, float value, float* bias,
+                        moe_stream_t stream);
+
 /*
  * Router: logits, top-k by logit + bias (+ affinity), softmax weights over the picked k.
  * Source: "Nudge, don't cut" (PGO-SGB), "The method in five lines" (pick
@@ -107,6 +121,28 @@ int moe_route(const void* x, const void* w_router, const float* logit_offset, co
               const int32_t* e2s, float affinity, int T, int H, int E, int k, float* logits, float* scratch,
               int32_t* ids, float* w, moe_stream_t stream);
 size_t moe_route_scratch_bytes(int T, int H, int E);
+
+/* Router flags for moe_route_ex. */
+#define MOE_ROUTE_SIGMOID 1 /* GLM's sigmoid router ("Nudge, don't cut", "The same idea on GLM-5.3-Flash":
+                               the bias is added after the sigmoid, in probability space) */
+#define MOE_ROUTE_DAMPED 2  /* damped weights ("Qwen on Strata": selection-only against damped): the
+                               bias also enters the weights */
+
+/*
+ * moe_route with a router variant (rflags = 0 is moe_route):
+ *   MOE_ROUTE_SIGMOID  score = sigmoid(logit) + bias (+ affinity), picked as
+ *                      above; w[j] = sigmoid(logit_j) / sum over the picked k.
+ *                      sigmoid(l) = 1 / (1 + e(-l)) in fp32, with e() one fixed
+ *                      sequence of IEEE fp32 operations (Cody-Waite reduction,
+ *                      degree-7 Taylor polynomial, times 2^n; +inf above 88, 0
+ *                      below -80), so the ids are reproducible bit for bit.
+ *   MOE_ROUTE_DAMPED   softmax router; w = softmax over the picked k of
+ *                      logit + sel_bias (affinity stays selection-only).
+ * Errors: as moe_route; MOE_ERR_ARG for unknown flags or SIGMOID with DAMPED.
+ */
+int moe_route_ex(const void* x, const void* w_router, const float* logit_offset, const float* sel_bias,
+                 const int32_t* e2s, float affinity, int rflags, int T, int H, int E, int k, float* logits,
+                 float* scratch, int32_t* ids, float* w, moe_stream_t stream);
 
 /*
  * Permute: group the n = T*k routing slots by expert.
@@ -320,6 +356,7 @@ typedef struct moe_layer_args {
   size_t workspace_bytes;
   moe_prof* prof;            /* host struct, or NULL: per-kernel timing events */
   float affinity;            /* live-cache affinity lambda (0 = off); uses e2s before this step's manage */
+  int32_t route_flags;       /* moe_route_ex flags (0 = softmax router, selection-only bias) */
 } moe_layer_args;
 
 /*

@@ -331,15 +331,17 @@ def test_combine_parity_split():
 # Whole layer
 # ----------------------------------------------------------------------------
 
-def _run_layer(cfg, steps=1, side=True, policy=None, T=None):
+def _run_layer(cfg, steps=1, side=True, policy=None, T=None, bias_mode=O.BIAS_GRADED, rflags=0):
     T = cfg.T if T is None else T
     policy = cfg.policy if policy is None else policy
     st = stage_layer(cfg)
     bias_np = bias_d = None
     if cfg.bias_cap is not None:
         b, _ = C.draw_brightness(cfg)
-        bias_np = O.bias_table(b, cfg.n_hot, cfg.bias_cap)
-        bias_d = M.bias_table(torch.from_numpy(b).to(DEV), cfg.n_hot, cfg.bias_cap)
+        bias_np = O.bias_table(b, cfg.n_hot, cfg.bias_cap, bias_mode)
+        bias_d = M.bias_table(torch.from_numpy(b).to(DEV), cfg.n_hot, cfg.bias_cap, mode=bias_mode)
+    router = O.ROUTER_SIGMOID if rflags & M.ROUTE_SIGMOID else O.ROUTER_SOFTMAX
+    damped = bool(rflags & M.ROUTE_DAMPED)
     s2e0 = C.initial_residency(cfg)
     if cfg.mode == C.MODE_RESIDENT:
         pool, gstate, ostate, opool = st["slabs_dev"], None, None, None
@@ -353,7 +355,8 @@ def _run_layer(cfg, steps=1, side=True, policy=None, T=None):
         opool = None
     layer = M.SlotCachedMoELayer(st["wr"], pool, cfg.k, cfg.I, cfg.mode, policy,
                                  host_slabs=None if cfg.mode == C.MODE_RESIDENT else st["host"], state=gstate,
-                                 logit_offset=st["logit_offset"], sel_bias=bias_d, max_tokens=T, side_stream=side)
+                                 logit_offset=st["logit_offset"], sel_bias=bias_d, max_tokens=T, side_stream=side,
+                                 route_flags=rflags)
     wr_np = _np(st["wr"].float())
     off_np = None if st["logit_offset"] is None else _np(st["logit_offset"])
     slabs = HostSlabs(st["host"])
@@ -363,7 +366,7 @@ def _run_layer(cfg, steps=1, side=True, policy=None, T=None):
         res = layer.forward(x)
         torch.cuda.synchronize()
         want = O.layer_forward(_np(x.float()), wr_np, slabs, cfg.H, cfg.I, cfg.k, cfg.mode, policy, ostate,
-                               opool, off_np, bias_np)
+                               opool, off_np, bias_np, router=router, damped=damped)
         assert np.array_equal(_np(res["ids"]), want["ids"]), f"step {step}: ids"
         assert np.abs(_np(res["w"]) - want["w"]).max() <= 1e-6
         assert_out_close(_np(res["out"].float()), want["out"], f"step {step}: out")
@@ -371,7 +374,8 @@ def _run_layer(cfg, steps=1, side=True, policy=None, T=None):
             # resident experts run the stream path (bf16 h); missing ones read host memory in fp32
             assert rel_l2(_np(res["out_res"]), want["out_res"]) <= RL2_Y_BF16_H
             assert_f32_close(_np(res["out_miss"]), want["out_miss"], "out_miss")
-            assert np.abs(want["out_miss"]).max() > 0
+            if bias_mode != O.BIAS_HARD:
+                assert np.abs(want["out_miss"]).max() > 0
         if ostate is not None:
             _check_state(gstate, ostate, f"step {step}")
             total_miss += sum(len(c["miss_e"]) for c in want["chunks"])
@@ -510,3 +514,77 @@ def test_layer_gather_with_affinity_matches_oracle_and_misses_less():
         assert int(layer.stats[0]) == misses
         res[lam] = misses
     assert res[0.5] < res[0.0]
+
+
+# ----------------------------------------------------------------------------
+# Routing variants ("Nudge, don't cut": hard mask, flat bias, damped weights,
+# GLM's sigmoid router)
+# ----------------------------------------------------------------------------
+
+def test_bias_table_modes_bit_exact():
+    cfg = C.FLASH
+    b, _ = C.draw_brightness(cfg)
+    bd = torch.from_numpy(b).to(DEV)
+    for mode, val in ((O.BIAS_GRADED, -1.0), (O.BIAS_FLAT, -0.5), (O.BIAS_HARD, 0.0)):
+        got = _np(M.bias_table(bd, cfg.n_hot, val, mode=mode))
+        want = O.bias_table(b, cfg.n_hot, val, mode)
+        assert np.array_equal(got, want), mode
+    assert np.isneginf(_np(M.bias_table(bd, cfg.n_hot, 0.0, mode=O.BIAS_HARD))).sum() == cfg.E - cfg.n_hot
+
+
+ROUTE_VARIANT_CASES = [
+    ("flash_flat", C.FLASH, O.BIAS_FLAT, -0.5, 0),
+    ("flash_hard_mask", C.FLASH, O.BIAS_HARD, 0.0, 0),
+    ("flash_damped", C.FLASH, O.BIAS_GRADED, -1.0, 2),
+    ("glm_stack_sigmoid_graded", C.STACK.with_(n_hot=144, zipf_s=1.1), O.BIAS_GRADED, -0.25, 1),
+    ("qwen_T300_sigmoid_flat_tiles", C.qwen(300).with_(n_hot=64, zipf_s=1.1), O.BIAS_FLAT, -0.05, 1),
+    ("prefill_sigmoid_offset", C.PREFILL, None, None, 1),
+]
+
+
+@pytest.mark.parametrize("blocked", [True, False], ids=["block_ctas", "ring"])
+@pytest.mark.parametrize("name,cfg,mode,val,rflags", ROUTE_VARIANT_CASES, ids=[c[0] for c in ROUTE_VARIANT_CASES])
+def test_route_variant_parity(name, cfg, mode, val, rflags, blocked):
+    x = C.draw_x(cfg, DEV)
+    wr = C.draw_router(cfg, DEV)
+    off = C.draw_logit_offset(cfg, DEV)
+    bias_np = bias_d = None
+    if mode is not None:
+        b, _ = C.draw_brightness(cfg)
+        bias_np = O.bias_table(b, cfg.n_hot, val, mode)
+        bias_d = M.bias_table(torch.from_numpy(b).to(DEV), cfg.n_hot, val, mode=mode)
+    ids, w, logits = M.route(x, wr, cfg.k, off, bias_d, return_logits=True, blocked=blocked, rflags=rflags)
+    torch.cuda.synchronize()
+    want_logits = O.router_logits(_np(x.float()), _np(wr.float()), None if off is None else _np(off))
+    assert np.array_equal(_np(logits), want_logits), "logits differ"
+    router = O.ROUTER_SIGMOID if rflags & 1 else O.ROUTER_SOFTMAX
+    want_ids = O.select_topk(want_logits, cfg.k, bias_np, router=router)
+    assert np.array_equal(_np(ids), want_ids), "ids differ"
+    want_w = O.route_weights(want_logits, want_ids, router, bias_np, bool(rflags & 2))
+    assert np.abs(_np(w) - want_w).max() <= 1e-6
+    if mode == O.BIAS_HARD:
+        assert np.isfinite(bias_np[want_ids]).all()  # every pick in the hot set
+    if rflags & 2:  # damped weights differ from the selection-only ones where a cold expert was picked
+        assert np.abs(want_w - O.route_weights(want_logits, want_ids)).max() > 1e-3
+
+
+def test_route_flags_rejected():
+    cfg = C.TINY
+    x, wr = C.draw_x(cfg, DEV), C.draw_router(cfg, DEV)
+    for bad in (3, 4):
+        with pytest.raises(M.MoeError) as ei:
+            M.route(x, wr, cfg.k, rflags=bad)
+        assert ei.value.code == -1
+
+
+def test_layer_gather_sigmoid_router_flat_bias():
+    _run_layer(C.qwen(8).with_(n_hot=64, bias_cap=-0.05, zipf_s=1.1), steps=2, bias_mode=O.BIAS_FLAT, rflags=M.ROUTE_SIGMOID)
+
+
+def test_layer_flash_zero_return_damped_weights():
+    _run_layer(C.FLASH, steps=1, rflags=M.ROUTE_DAMPED)
+
+
+def test_layer_flash_zero_return_hard_mask_never_misses():
+    layer = _run_layer(C.FLASH, steps=1, bias_mode=O.BIAS_HARD)
+    assert int(_np(layer.stats)[0]) == 0  # the hot set is the pool: a hard mask never picks a missing expert
