@@ -22,6 +22,10 @@ Sources (web pages; cited by title and section):
           "Designing a fixed expert cache with zero-return for missing
           experts": a missing expert returns zeros; a second pass over the
           missing experts is added, which gives exactly the full result.
+  [REPICK] transcript, the chapter on code and chat profiles: the hot set is
+          static, yet the useful set drifts; "every 500 tokens, say, have
+          another look. Swap out whatever's gone cold and then leave it alone
+          again", paying for transfers once per window.
   [SGB2]  same PGO-SGB page, introduction (two ways to use a profile: a hard
           mask, cold experts can never be picked; or a soft bias) and the KL
           comparison of a graded bias against a flat one (a flat -0.75,
@@ -63,6 +67,11 @@ Readings of points the pages leave open (each listed in the design notes):
     while k hot experts exist).
   * damped weights: w = softmax over the k picked of logit + bias (the bias
     table only; affinity stays selection-only).
+  * periodic re-pick (STATIC pool): every routing adds 1 to its expert's
+    window count; a re-pick takes the S experts with the largest counts
+    (ties: resident before cold, then lower id) as the new set, loads the
+    new members into the slots of experts that left it (empty slots first,
+    then ascending slot; new members in ascending id), and clears the counts.
   * sigmoid router: s = sigmoid(logit); pick top-k by s + bias; weights =
     the picked experts' sigmoid values normalised to sum 1 (the router's own
     probabilities).  So that the ids are reproducible bit for bit, the fp32
@@ -329,6 +338,40 @@ def manage(state: CacheState, ids: np.ndarray, policy: int) -> ManageResult:
         res.miss_s = list(victims)
     res.sid = np.array([state.e2s[e] for e in flat], dtype=np.int32).reshape(np.asarray(ids).shape)
     return res
+
+
+def window_count(counts: np.ndarray, ids: np.ndarray) -> None:
+    """Add one per routing to its expert's window count [REPICK]."""
+    for e in np.asarray(ids).reshape(-1):
+        counts[int(e)] += 1
+
+
+def repick(state: CacheState, counts: np.ndarray) -> ManageResult:
+    """Re-pick the resident set of a STATIC pool from the window counts [REPICK].
+
+    New set: the S experts ranked first by (count descending, resident before
+    cold, id ascending).  Its members that are not resident (ascending id) take,
+    in order, the slots that are empty or hold an expert outside the new set
+    (empty slots first, then ascending slot).  Priorities and stamp are left
+    alone (STATIC); the counts are cleared.
+    """
+    E = state.e2s.shape[0]
+    S = state.s2e.shape[0]
+    resident = state.e2s >= 0
+    order = sorted(range(E), key=lambda e: (-int(counts[e]), 0 if resident[e] else 1, e))
+    new = set(order[:min(S, E)])
+    miss_e = [e for e in range(E) if e in new and not resident[e]]
+    empty = [s for s in range(S) if state.s2e[s] < 0]
+    leaving = [s for s in range(S) if state.s2e[s] >= 0 and int(state.s2e[s]) not in new]
+    victims = (empty + leaving)[:len(miss_e)]
+    for e, s in zip(miss_e, victims):
+        old = int(state.s2e[s])
+        if old >= 0:
+            state.e2s[old] = -1
+        state.s2e[s] = e
+        state.e2s[e] = s
+    counts[:] = 0
+    return ManageResult(miss_e=list(miss_e), miss_s=list(victims))
 
 
 def gather(host: np.ndarray, pool: np.ndarray, miss_e, miss_s) -> None:

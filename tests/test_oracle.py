@@ -549,3 +549,46 @@ def test_sigmoid_router_golden():
 def _route_from_logits(logits, k, bias, router=0, damped=False):
     ids = O.select_topk(logits, k, bias, router=router)
     return ids, O.route_weights(logits, ids, router, bias, damped), logits
+
+
+# ----------------------------------------------------------------------------
+# Periodic re-pick of a STATIC pool (transcript: "every 500 tokens, say, have
+# another look. Swap out whatever's gone cold")
+# ----------------------------------------------------------------------------
+
+def test_repick_golden_traces():
+    g = _gold("repick_traces.json")
+    for c in g["cases"]:
+        st = O.CacheState.from_slots(np.array(c["s2e"], dtype=np.int32), c["E"])
+        counts = np.array(c["counts"], dtype=np.int64)
+        r = O.repick(st, counts)
+        assert r.miss_e == c["miss_e"] and r.miss_s == c["miss_s"], c["name"]
+        assert st.s2e.tolist() == c["s2e_after"], c["name"]
+        assert sorted(e for e in st.s2e.tolist() if e >= 0) == sorted(c["new_set"]), c["name"]
+        assert not counts.any()
+
+
+def test_repick_matches_lexsort_top_s_and_keeps_stayers_in_place():
+    rng = np.random.default_rng(12)
+    for trial in range(200):
+        E = int(rng.integers(4, 40))
+        S = int(rng.integers(1, E + 1))
+        perm = rng.permutation(E)
+        s2e = np.full(S, -1, dtype=np.int32)
+        n_res = int(rng.integers(0, S + 1))
+        s2e[rng.permutation(S)[:n_res]] = perm[:n_res]
+        st = O.CacheState.from_slots(s2e, E)
+        counts = rng.integers(0, 4, size=E)
+        old_e2s = st.e2s.copy()
+        resident = old_e2s >= 0
+        # independent ranking: lexsort keys (last key is primary)
+        order = np.lexsort((np.arange(E), (~resident).astype(int), -counts))
+        want = set(order[:S].tolist())
+        r = O.repick(st, counts.copy())
+        now = {int(e) for e in st.s2e if e >= 0}
+        assert now == want
+        assert len(r.miss_e) == len(want - {e for e in range(E) if resident[e]})
+        for e in want:
+            if resident[e]:
+                assert st.e2s[e] == old_e2s[e]  # experts that stay never move
+        assert all(st.s2e[st.e2s[e]] == e for e in range(E) if st.e2s[e] >= 0)
