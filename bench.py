@@ -277,6 +277,25 @@ def policy_replay(trace: np.ndarray, E: int, S: int, dev: str, slab_bytes: int) 
         out[name] = {"misses": misses, "hit_rate": 1.0 - misses / needed,
                      "host_link_GB": misses * slab_bytes / 1e9 if pol != C.POLICY_STATIC else 0.0,
                      "missed_expert_bytes_GB": misses * slab_bytes / 1e9}
+    # STATIC with a periodic re-pick (the transcript's "every 500 tokens, have another look"): between
+    # re-picks the set stays fixed (misses are served from host memory, zero-return); each re-pick loads
+    # the experts that entered the set
+    for every in (500, 2000):
+        st = M.CacheState.from_slots(seeded, E, dev)
+        counts = torch.zeros(E, dtype=torch.int32, device=dev)
+        tot = torch.zeros(1, dtype=torch.int64, device=dev)
+        loads = torch.zeros(1, dtype=torch.int64, device=dev)
+        per = max(1, every // T)
+        for i in range(steps):
+            tot += M.cache_manage(ids_d[i], st, C.POLICY_STATIC).n_miss
+            M.cache_count(ids_d[i], E, counts)
+            if (i + 1) % per == 0:
+                loads += M.cache_repick(counts, st).n_miss
+        misses, n_loads = int(tot.item()), int(loads.item())
+        needed = sum(len(np.unique(trace[i])) for i in range(steps))
+        out[f"static_repick_every_{every}_tokens"] = {
+            "misses": misses, "hit_rate": 1.0 - misses / needed, "repick_loads": n_loads,
+            "host_link_GB": n_loads * slab_bytes / 1e9, "missed_expert_bytes_GB": misses * slab_bytes / 1e9}
     out["trace"] = {"steps": steps, "T": T, "k": k, "E": E, "S": S,
                     "recipe": "Zipf(1.1) popularity over a ranking drifting by 2 swaps per step"}
     return out

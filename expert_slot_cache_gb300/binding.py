@@ -47,7 +47,7 @@ class LayerArgs(ctypes.Structure):
                 ("ids", c_void_p), ("w", c_void_p), ("out", c_void_p), ("out_res", c_void_p),
                 ("out_miss", c_void_p), ("stats", c_void_p), ("dev_status", c_void_p),
                 ("workspace", c_void_p), ("workspace_bytes", c_size_t), ("prof", POINTER(Prof)),
-                ("affinity", c_float), ("route_flags", c_int32)]
+                ("affinity", c_float), ("route_flags", c_int32), ("window_counts", c_void_p)]
 
 
 def _sig(name, argtypes, restype=c_int):
@@ -72,6 +72,8 @@ _permute = _sig("moe_permute", [V, I32, I32, V, V, V, V, V, V, V, V, V])
 _permute_scratch = _sig("moe_permute_scratch_bytes", [I32, I32], c_size_t)
 _manage = _sig("moe_cache_manage", [V, I32, I32, I32, I32, V, V, V, V, V, V, V, V, V, V, V, V])
 _gather = _sig("moe_cache_gather", [V, V, c_size_t, I32, I32, V, V, V, I32, V, V])
+_count = _sig("moe_cache_count", [V, I32, I32, V, V, V])
+_repick = _sig("moe_cache_repick", [V, I32, I32, V, V, V, V, V, V])
 _ffn = _sig("moe_expert_ffn", [V, I32, I32, I32, I32, I32, V, V, V, V, I32, V, I32, V, V, V, V, c_size_t, V, V])
 _ffn_ws = _sig("moe_ffn_workspace_bytes", [I32, I32, I32, I32], c_size_t)
 _combine = _sig("moe_combine", [V, V, V, V, V, I32, I32, I32, I32, I32, V, V, V, V])
@@ -214,6 +216,28 @@ def cache_gather(host_slabs, pool, miss_e, miss_s, n_miss, max_miss, dev_status=
                 _p(dev_status), _s(stream)), "moe_cache_gather")
 
 
+def cache_count(ids, E, counts, dev_status=None, stream=None) -> None:
+    """counts[e] += number of routings of expert e in ``ids`` (window counts for a re-pick)."""
+    _ck(_count(_p(ids), ids.numel(), E, _p(counts), _p(dev_status), _s(stream)), "moe_cache_count")
+
+
+@dataclass
+class RepickResult:
+    miss_e: torch.Tensor
+    miss_s: torch.Tensor
+    n_miss: torch.Tensor
+
+
+def cache_repick(counts, state: "CacheState", stream=None) -> RepickResult:
+    """Re-pick a STATIC pool's resident set from the window counts (clears them)."""
+    E, S = state.e2s.numel(), state.s2e.numel()
+    i32 = dict(dtype=torch.int32, device=counts.device)
+    r = RepickResult(torch.empty(min(S, E), **i32), torch.empty(min(S, E), **i32), torch.zeros(1, **i32))
+    _ck(_repick(_p(counts), E, S, _p(state.e2s), _p(state.s2e), _p(r.miss_e), _p(r.miss_s), _p(r.n_miss),
+                _s(stream)), "moe_cache_repick")
+    return r
+
+
 def ffn_workspace_bytes(T: int, H: int, k: int, I: int) -> int:
     return int(_ffn_ws(T, H, k, I))
 
@@ -260,7 +284,7 @@ class SlotCachedMoELayer:
 
     def __init__(self, w_router, pool, k, I, mode, policy=POLICY_LRU, host_slabs=None, state=None,
                  logit_offset=None, sel_bias=None, max_tokens=64, side_stream=True, affinity=0.0,
-                 route_flags=0):
+                 route_flags=0, window_counts=None):
         self.w_router, self.pool, self.k, self.I = w_router, pool, k, I
         self.H, self.E = w_router.shape
         self.S = pool.shape[0]
@@ -269,6 +293,7 @@ class SlotCachedMoELayer:
         self.logit_offset, self.sel_bias = logit_offset, sel_bias
         self.affinity = float(affinity)
         self.route_flags = int(route_flags)
+        self.window_counts = window_counts
         dev = pool.device
         self.stats = torch.zeros(4, dtype=torch.int64, device=dev)
         self.dev_status = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -297,7 +322,7 @@ class SlotCachedMoELayer:
                       ids.data_ptr(), w.data_ptr(), out.data_ptr(), _ptr(out_res), _ptr(out_miss),
                       self.stats.data_ptr(), self.dev_status.data_ptr(), self.workspace.data_ptr(),
                       self.workspace.numel(), ctypes.pointer(prof) if prof is not None else None, self.affinity,
-                      self.route_flags)
+                      self.route_flags, _ptr(self.window_counts))
         main = torch.cuda.current_stream() if stream is None else stream
         # the library forks to and joins back from the side stream itself
         _ck(_layer(ctypes.byref(a), c_void_p(main.cuda_stream),
@@ -306,6 +331,13 @@ class SlotCachedMoELayer:
         if self.mode == MODE_ZERO_RETURN:
             res["out_res"], res["out_miss"] = out_res, out_miss
         return res
+
+    def repick(self, stream=None) -> RepickResult:
+        """Re-pick the resident set from ``window_counts`` and copy the new members into their slots."""
+        r = cache_repick(self.window_counts, self.state, stream)
+        cache_gather(self.host_slabs, self.pool, r.miss_e, r.miss_s, r.n_miss, r.miss_e.numel(), self.dev_status,
+                     stream)
+        return r
 
 
 class LayerStack:

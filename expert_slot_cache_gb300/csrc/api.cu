@@ -221,6 +221,7 @@ extern "C" int moe_layer_forward(const moe_layer_args* a, moe_stream_t main_s, m
                        ms);
     if (r != MOE_OK) return r;
     prof.end(ms);
+    if (a->window_counts && (r = launch_window_add(ws.count, E, a->window_counts, ms)) != MOE_OK) return r;
     FfnArgs f{(const uint16_t*)a->x + (size_t)t0 * H, tc, H, I, k, E, ws.offset, ws.rows, nullptr, nullptr,
               (const uint16_t*)a->pool, a->e2s, (const uint16_t*)a->host_slabs, (size_t)3 * H * I, ws.hbuf, ws.y,
               a->dev_status, S, 1, ws.xp, ws.hb, nullptr, ws.skp, ws.skp_bytes};

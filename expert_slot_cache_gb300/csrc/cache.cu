@@ -209,6 +209,103 @@ __global__ void __launch_bounds__(kGatherThreads) gather_kernel(const uint4* __r
   if (stats && blockIdx.x == 0 && threadIdx.x == 0) stats[2] += (int64_t)nm * (int64_t)slab_vec * 16;
 }
 
+// ---------------------------------------------------------------------------
+// Periodic re-pick of a STATIC pool.  "RTX 3060 runs a 35B MoE with
+// llama.cpp" (video transcript), chapter on code and chat profiles: the hot
+// set is chosen once, yet the useful set drifts; "every 500 tokens, say, have
+// another look. Swap out whatever's gone cold and then leave it alone again".
+// Every routing adds one to its expert's window count; a re-pick keeps the S
+// experts ranked first by (count desc, resident first, id asc), loads the new
+// members (ascending id) into empty slots first and then into the slots of
+// experts that left (ascending slot), and clears the counts.  One CTA, rank by
+// compare and block scans: no atomics, deterministic.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kManageThreads) window_count_kernel(const int32_t* __restrict__ ids, int n, int E,
+                                                                      int32_t* __restrict__ counts,
+                                                                      int32_t* __restrict__ status) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+    const int e = ids[i];
+    if (e < 0 || e >= E) {
+      set_status(status, MOE_DEV_BAD_EXPERT);
+      continue;
+    }
+    atomicAdd(&counts[e], 1);  // integer sums: the result does not depend on the order
+  }
+}
+
+__global__ void __launch_bounds__(kManageThreads) window_add_kernel(const int32_t* __restrict__ count, int E,
+                                                                    int32_t* __restrict__ counts) {
+  for (int e = threadIdx.x; e < E; e += blockDim.x) counts[e] += count[e];
+}
+
+// Shared memory (dynamic): cnt[E] | res[E] | mlist[E] | innew[E] | s2e[S]
+__global__ void __launch_bounds__(kManageThreads) repick_kernel(int32_t* __restrict__ counts, int E, int S,
+                                                                int32_t* __restrict__ e2s_g,
+                                                                int32_t* __restrict__ s2e_g,
+                                                                int32_t* __restrict__ miss_e,
+                                                                int32_t* __restrict__ miss_s,
+                                                                int32_t* __restrict__ n_miss) {
+  extern __shared__ int rp_smem[];
+  int* cnt = rp_smem;
+  int* res = cnt + E;
+  int* mlist = res + E;
+  int* innew = mlist + E;
+  int* s2e = innew + E;
+  __shared__ int tmp[33];
+  const int tid = threadIdx.x, nt = blockDim.x;
+  for (int e = tid; e < E; e += nt) {
+    cnt[e] = counts[e];
+    res[e] = e2s_g[e] >= 0;
+  }
+  for (int q = tid; q < S; q += nt) s2e[q] = s2e_g[q];
+  __syncthreads();
+  const int keep = min(S, E);
+  int mine = 0;
+  if (tid < E) {  // E <= blockDim
+    const int c = cnt[tid], r = res[tid];
+    int rank = 0;
+    for (int f = 0; f < E; ++f) {
+      const int cf = cnt[f], rf = res[f];
+      rank += (cf > c) || (cf == c && (rf > r || (rf == r && f < tid)));
+    }
+    innew[tid] = rank < keep;
+    mine = rank < keep && !r;
+  }
+  __syncthreads();
+  int nmiss = 0;
+  const int mi = block_exclusive_scan(mine, tmp, &nmiss);
+  if (mine) mlist[mi] = tid;
+  __syncthreads();
+  // victims: empty slots first, then slots whose expert left the set, each in ascending slot order
+  int base = 0;
+  for (int pass = 0; pass < 2; ++pass) {
+    for (int q0 = 0; q0 < S; q0 += nt) {
+      const int q = q0 + tid;
+      int fl = 0;
+      if (q < S) fl = pass == 0 ? s2e[q] < 0 : (s2e[q] >= 0 && !innew[s2e[q]]);
+      int tot = 0;
+      const int idx = block_exclusive_scan(fl, tmp, &tot);
+      if (fl && base + idx < nmiss) {
+        const int v = base + idx, e = mlist[v], old = s2e[q];
+        if (old >= 0) e2s_g[old] = -1;  // the leaving expert is outside the new set: no other thread writes it
+        s2e_g[q] = e;
+        e2s_g[e] = q;
+        miss_e[v] = e;
+        miss_s[v] = q;
+      }
+      base += tot;
+    }
+  }
+  for (int e = tid; e < E; e += nt) counts[e] = 0;
+  if (tid == 0) *n_miss = nmiss;
+}
+
+int launch_window_add(const int32_t* count, int E, int32_t* counts, cudaStream_t stream) {
+  window_add_kernel<<<1, 256, 0, stream>>>(count, E, counts);
+  MOE_LAUNCH_CHECK();
+  return MOE_OK;
+}
+
 int launch_manage(const int32_t* ids, int n, int E, int S, int policy, int32_t* e2s, int32_t* s2e, uint32_t* prio,
                   uint32_t* stamp, int32_t* miss_e, int32_t* miss_s, int32_t* n_miss, int32_t* hit_e,
                   int32_t* n_hit, int32_t* sid, int64_t* stats, int32_t* dev_status, cudaStream_t stream) {
@@ -276,4 +373,26 @@ extern "C" int moe_cache_gather(const void* host_slabs, void* pool, size_t slab_
   if (acc != MOE_OK) return acc;
   return launch_gather(host_slabs, pool, slab_bytes, E, S, miss_e, miss_s, n_miss, max_miss, nullptr, dev_status,
                        (cudaStream_t)stream);
+}
+
+extern "C" int moe_cache_count(const int32_t* ids, int n, int E, int32_t* counts, int32_t* dev_status,
+                               moe_stream_t stream) {
+  if (!ids || !counts || n < 0 || E < 1 || E > kMaxE) return MOE_ERR_ARG;
+  if (n == 0) return MOE_OK;
+  const int grid = std::min((n + kManageThreads - 1) / kManageThreads, 64);
+  window_count_kernel<<<grid, kManageThreads, 0, (cudaStream_t)stream>>>(ids, n, E, counts, dev_status);
+  MOE_LAUNCH_CHECK();
+  return MOE_OK;
+}
+
+extern "C" int moe_cache_repick(int32_t* counts, int E, int S, int32_t* e2s, int32_t* s2e, int32_t* miss_e,
+                                int32_t* miss_s, int32_t* n_miss, moe_stream_t stream) {
+  if (!counts || !e2s || !s2e || !miss_e || !miss_s || !n_miss) return MOE_ERR_ARG;
+  if (E < 1 || E > kMaxE || S < 1 || S > kMaxS) return MOE_ERR_ARG;
+  const size_t smem = (size_t)4 * E * sizeof(int) + (size_t)S * sizeof(int);
+  static bool attr_done[64] = {};
+  MOE_CUDA_TRY(ensure_smem(repick_kernel, (int)(4 * kMaxE * 4 + kMaxS * 4), attr_done));
+  repick_kernel<<<1, kManageThreads, smem, (cudaStream_t)stream>>>(counts, E, S, e2s, s2e, miss_e, miss_s, n_miss);
+  MOE_LAUNCH_CHECK();
+  return MOE_OK;
 }

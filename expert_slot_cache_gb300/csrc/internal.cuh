@@ -76,6 +76,7 @@ int launch_gather(const void* host_slabs, void* pool, size_t slab_bytes, int E, 
                   const int32_t* miss_s, const int32_t* n_miss, int max_miss, int64_t* stats, int32_t* dev_status,
                   cudaStream_t stream);
 int check_host_accessible(const void* p);
+int launch_window_add(const int32_t* count, int E, int32_t* counts, cudaStream_t stream);
 int launch_permute(const int32_t* ids, int n, int E, int32_t* count, int32_t* offset, int32_t* rows, int32_t* pos,
                    int32_t* act_e, int32_t* n_act, int32_t* dev_status, int32_t* scratch, cudaStream_t s);
 

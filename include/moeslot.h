@@ -330,6 +330,31 @@ typedef struct moe_prof {
   int32_t* tags;    /* [capacity / 2] out */
 } moe_prof;
 
+/*
+ * Periodic re-pick of a STATIC pool.
+ * Source: "RTX 3060 runs a 35B MoE with llama.cpp" (video transcript),
+ * chapter on code and chat profiles: the static hot set is chosen once, yet
+ * the useful set drifts; every few hundred tokens, have another look, swap
+ * out whatever has gone cold and leave it alone again (transfers are paid
+ * once per window, not per token).
+ *
+ * moe_cache_count adds one to counts[e] for every routing id e (device int32
+ * [n] ids, device int32 [E] counts, both caller-owned; ids out of range set
+ * MOE_DEV_BAD_EXPERT in dev_status and are skipped).
+ *
+ * moe_cache_repick keeps the S experts ranked first by (counts desc, resident
+ * before cold, id asc).  New members (ascending id) take the empty slots
+ * first, then the slots of experts that left the set (ascending slot); e2s and
+ * s2e are updated, the loads are written as miss_e / miss_s (device int32 >=
+ * min(S, E) entries) with their count in n_miss (device int32), and the counts
+ * are cleared.  Priorities and stamp are untouched (the pool stays STATIC).
+ * Copy the new members with moe_cache_gather on the same lists.
+ * Errors: MOE_ERR_ARG on NULL pointers, E not in [1, 1024], S not in [1, 4096].
+ */
+int moe_cache_count(const int32_t* ids, int n, int E, int32_t* counts, int32_t* dev_status, moe_stream_t stream);
+int moe_cache_repick(int32_t* counts, int E, int S, int32_t* e2s, int32_t* s2e, int32_t* miss_e, int32_t* miss_s,
+                     int32_t* n_miss, moe_stream_t stream);
+
 /* Arguments of moe_layer_forward.  Field meanings as in the calls above. */
 typedef struct moe_layer_args {
   int32_t T, H, E, k, I, S;
@@ -357,6 +382,7 @@ typedef struct moe_layer_args {
   moe_prof* prof;            /* host struct, or NULL: per-kernel timing events */
   float affinity;            /* live-cache affinity lambda (0 = off); uses e2s before this step's manage */
   int32_t route_flags;       /* moe_route_ex flags (0 = softmax router, selection-only bias) */
+  int32_t* window_counts;    /* device int32 [E] or NULL: each chunk's routings are added (moe_cache_count) */
 } moe_layer_args;
 
 /*
