@@ -155,16 +155,13 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const Prefil
           mbar_expect_tx(&full[s], kPStageBytes);
           tma_load_3d(st, &mapA, &full[s], kb * kPK, row0, 0);
           unsigned char* sb = st + kPAbytes;
+          // weights: one 4-D box per matrix = 64 K-rows x all of the tile's 64-column swizzle atoms (8 KB apart)
           if (kMode == 0) {
-            const int n0 = ct * 128;
-            tma_load_3d(sb, &mapB, &full[s], n0, kb * kPK, 3 * slot);
-            tma_load_3d(sb + 8192, &mapB, &full[s], n0 + 64, kb * kPK, 3 * slot);
-            tma_load_3d(sb + 16384, &mapB, &full[s], n0, kb * kPK, 3 * slot + 1);
-            tma_load_3d(sb + 24576, &mapB, &full[s], n0 + 64, kb * kPK, 3 * slot + 1);
+            const int a0 = ct * 2;  // 128 gate columns, then the same 128 up columns
+            tma_load_4d(sb, &mapB, &full[s], 0, kb * kPK, a0, 3 * slot);
+            tma_load_4d(sb + 16384, &mapB, &full[s], 0, kb * kPK, a0, 3 * slot + 1);
           } else {
-            const int o0 = ct * kPN;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) tma_load_3d(sb + 8192 * j, &mapB, &full[s], o0 + 64 * j, kb * kPK, 3 * slot + 2);
+            tma_load_4d(sb, &mapB, &full[s], 0, kb * kPK, ct * (kPN / 64), 3 * slot + 2);
           }
           last_use[s] = (int)use;
         }
@@ -354,17 +351,18 @@ int launch_prefill(const FfnArgs& a, int n, int max_list, cudaStream_t stream, P
     const uint32_t b[3] = {kPK, kPM, 1};
     if (encode_tmap_3d_bf16(&mh, a.hb, d, s, b, CU_TENSOR_MAP_SWIZZLE_128B) != MOE_OK) return MOE_ERR_CUDA;
   }
+  // weight matrices viewed as [matrix][64-column atom][K row][64 columns]
   {
-    const uint64_t d[3] = {(uint64_t)a.I, (uint64_t)a.H, 3ull * a.S};
-    const uint64_t s[2] = {(uint64_t)a.I * 2, mat * 2};
-    const uint32_t b[3] = {64, kPK, 1};
-    if (encode_tmap_3d_bf16(&mgu, a.pool, d, s, b, CU_TENSOR_MAP_SWIZZLE_128B) != MOE_OK) return MOE_ERR_CUDA;
+    const uint64_t d[4] = {64, (uint64_t)a.H, (uint64_t)a.I / 64, 3ull * a.S};
+    const uint64_t s[3] = {(uint64_t)a.I * 2, 128, mat * 2};
+    const uint32_t b[4] = {64, kPK, 2, 1};
+    if (encode_tmap_bf16(&mgu, a.pool, 4, d, s, b, CU_TENSOR_MAP_SWIZZLE_128B) != MOE_OK) return MOE_ERR_CUDA;
   }
   {
-    const uint64_t d[3] = {(uint64_t)a.H, (uint64_t)a.I, 3ull * a.S};
-    const uint64_t s[2] = {(uint64_t)a.H * 2, mat * 2};
-    const uint32_t b[3] = {64, kPK, 1};
-    if (encode_tmap_3d_bf16(&md, a.pool, d, s, b, CU_TENSOR_MAP_SWIZZLE_128B) != MOE_OK) return MOE_ERR_CUDA;
+    const uint64_t d[4] = {64, (uint64_t)a.I, (uint64_t)a.H / 64, 3ull * a.S};
+    const uint64_t s[3] = {(uint64_t)a.H * 2, 128, mat * 2};
+    const uint32_t b[4] = {64, kPK, kPN / 64, 1};
+    if (encode_tmap_bf16(&md, a.pool, 4, d, s, b, CU_TENSOR_MAP_SWIZZLE_128B) != MOE_OK) return MOE_ERR_CUDA;
   }
   PrefillArgs p{a.H, a.I, a.E, n, a.offset, a.list_e, a.n_list, a.e2s, a.S, a.hb, a.y, a.status, a.yb};
   (void)max_list;
