@@ -26,6 +26,10 @@ Sources (web pages; cited by title and section):
           static, yet the useful set drifts; "every 500 tokens, say, have
           another look. Swap out whatever's gone cold and then leave it alone
           again", paying for transfers once per window.
+  [Q8]    "Porting vllm-expert-cache to NVIDIA GPUs": the measured model is
+          Qwen3-30B-A3B W8A8 (8-bit weights and activations); "weights and
+          their scales are indexed by the same id, so both must be
+          slot-indexed" (section on traps in a new backend).
   [SGB2]  same PGO-SGB page, introduction (two ways to use a profile: a hard
           mask, cold experts can never be picked; or a soft bias) and the KL
           comparison of a graded bias against a flat one (a flat -0.75,
@@ -72,6 +76,17 @@ Readings of points the pages leave open (each listed in the design notes):
     (ties: resident before cold, then lower id) as the new set, loads the
     new members into the slots of experts that left it (empty slots first,
     then ascending slot; new members in ascending id), and clears the counts.
+  * W8A8 experts: symmetric int8, scale = amax / 127 (fp32), code =
+    rint(v / scale) clamped to [-127, 127] (a zero amax gives scale 0 and
+    code 0); weights per output channel (offline), activations per routing
+    row (x before gate/up, h before down).  Products are exact int32 sums;
+    g = (float(acc) * s_w[n]) * s_x[row], likewise u and y; h = silu(g) * u
+    with silu(g) = g / (1 + exp32(-g)); all of it fp32, one operation at a
+    time, so the codes of h and the output y are reproducible bit for bit.
+    A quantised slab holds [Wg | Wu | Wd] as int8 with every 4 consecutive
+    input rows of a column packed together (byte (k, n) at
+    ((k div 4) * N + n) * 4 + k mod 4), then the fp32 scales sg[I], su[I],
+    sd[H]; the scales travel with the weights, so they are slot-indexed too.
   * sigmoid router: s = sigmoid(logit); pick top-k by s + bias; weights =
     the picked experts' sigmoid values normalised to sum 1 (the router's own
     probabilities).  So that the ids are reproducible bit for bit, the fp32
@@ -404,6 +419,100 @@ def silu(z):
     return z / (1.0 + np.exp(-z))
 
 
+# ----------------------------------------------------------------------------
+# W8A8 experts  [Q8]
+# ----------------------------------------------------------------------------
+
+def q8_slab_bytes(H: int, I: int) -> int:
+    return 3 * H * I + 4 * (2 * I + H)
+
+
+def quantize_cols(W: np.ndarray):
+    """Per-column symmetric int8 of an fp32 [K][N] matrix: (codes int8 [K][N], scales fp32 [N])."""
+    W = np.asarray(W, dtype=np.float32)
+    amax = np.max(np.abs(W), axis=0).astype(np.float32)
+    sc = (amax / _F(127.0)).astype(np.float32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        q = np.where(sc[None, :] > 0, np.rint((W / sc[None, :]).astype(np.float32)), _F(0.0))
+    return np.clip(q, -127, 127).astype(np.int8), sc
+
+
+def quantize_rows(X: np.ndarray):
+    """Per-row symmetric int8 of an fp32 [R][K] matrix: (codes int8 [R][K], scales fp32 [R])."""
+    q, sc = quantize_cols(np.asarray(X, dtype=np.float32).T)
+    return np.ascontiguousarray(q.T), sc
+
+
+def _pack_quads(q: np.ndarray) -> np.ndarray:
+    K, N = q.shape
+    return np.ascontiguousarray(q.reshape(K // 4, 4, N).transpose(0, 2, 1)).reshape(-1)
+
+
+def _unpack_quads(b: np.ndarray, K: int, N: int) -> np.ndarray:
+    return np.ascontiguousarray(b.reshape(K // 4, N, 4).transpose(0, 2, 1)).reshape(K, N)
+
+
+def quantize_slab(slab: np.ndarray, H: int, I: int) -> np.ndarray:
+    """bf16 slab (values as fp32 [3HI]) -> quantised slab bytes (uint8 [q8_slab_bytes])."""
+    v = np.asarray(slab, dtype=np.float32).reshape(-1)
+    n = H * I
+    parts = []
+    scales = []
+    for W in (v[:n].reshape(H, I), v[n:2 * n].reshape(H, I), v[2 * n:3 * n].reshape(I, H)):
+        q, sc = quantize_cols(W)
+        parts.append(_pack_quads(q).view(np.uint8))
+        scales.append(sc.view(np.uint8))
+    return np.concatenate(parts + scales)
+
+
+def unpack_q8_slab(b: np.ndarray, H: int, I: int):
+    """-> (qg [H][I], qu [H][I], qd [I][H]) int8 and (sg [I], su [I], sd [H]) fp32."""
+    b = np.asarray(b, dtype=np.uint8).reshape(-1)
+    n = H * I
+    qg = _unpack_quads(b[:n].view(np.int8), H, I)
+    qu = _unpack_quads(b[n:2 * n].view(np.int8), H, I)
+    qd = _unpack_quads(b[2 * n:3 * n].view(np.int8), I, H)
+    o = 3 * n
+    sg = b[o:o + 4 * I].view(np.float32)
+    su = b[o + 4 * I:o + 8 * I].view(np.float32)
+    sd = b[o + 8 * I:o + 8 * I + 4 * H].view(np.float32)
+    return qg, qu, qd, sg, su, sd
+
+
+def _dequant(acc: np.ndarray, s_w: np.ndarray, s_r: np.ndarray) -> np.ndarray:
+    """(float(acc) * s_w[n]) * s_r[row], fp32, one rounding per operation."""
+    a = np.asarray(acc, dtype=np.int64).astype(np.float32)
+    return ((a * s_w[None, :]).astype(np.float32) * s_r[:, None]).astype(np.float32)
+
+
+def swiglu_expert_q8(x_rows: np.ndarray, qslab: np.ndarray, H: int, I: int) -> np.ndarray:
+    """W8A8 SwiGLU for a block of rows x [n][H] (fp32 values) -> y fp32 [n][H]  [Q8]."""
+    qg, qu, qd, sg, su, sd = unpack_q8_slab(qslab, H, I)
+    qx, sx = quantize_rows(np.asarray(x_rows, dtype=np.float32))
+    xi = qx.astype(np.int64)
+    g = _dequant(xi @ qg.astype(np.int64), sg, sx)
+    u = _dequant(xi @ qu.astype(np.int64), su, sx)
+    with np.errstate(over="ignore"):
+        d = (_F(1.0) + exp32(-g)).astype(np.float32)
+        h = ((g / d).astype(np.float32) * u).astype(np.float32)
+    qh, sh = quantize_rows(h)
+    return _dequant(qh.astype(np.int64) @ qd.astype(np.int64), sd, sh)
+
+
+def expert_ffn_q8(x, rows, offset, k, qslabs, H, I, experts=None) -> np.ndarray:
+    """Grouped W8A8 FFN (fp32 outputs, NaN for rows of experts left out)."""
+    x = np.asarray(x, dtype=np.float32)
+    E = len(offset) - 1
+    y = np.full((len(rows), H), np.nan, dtype=np.float32)
+    for e in range(E):
+        a, b = int(offset[e]), int(offset[e + 1])
+        if a == b or (experts is not None and e not in experts):
+            continue
+        tok = np.asarray(rows[a:b]) // k
+        y[a:b] = swiglu_expert_q8(x[tok], qslabs[e], H, I)
+    return y
+
+
 def swiglu_expert(x_rows: np.ndarray, slab: np.ndarray, H: int, I: int) -> np.ndarray:
     """y = (silu(x Wg) * (x Wu)) Wd for a block of rows x [n][H]."""
     wg, wu, wd = unpack_slab(slab, H, I)
@@ -460,7 +569,7 @@ def combine(y, w, pos, T, k, resident=None):
 # ----------------------------------------------------------------------------
 
 def layer_forward(x, wr, host, H, I, k, mode, policy=LRU, state=None, pool=None,
-                  logit_offset=None, bias=None, affinity=0.0, router=ROUTER_SOFTMAX, damped=False):
+                  logit_offset=None, bias=None, affinity=0.0, router=ROUTER_SOFTMAX, damped=False, quant=False):
     """One MoE layer forward with the slot cache.
 
     ``host`` [E][3HI] holds every expert (authoritative copy); ``pool``
@@ -494,7 +603,10 @@ def layer_forward(x, wr, host, H, I, k, mode, policy=LRU, state=None, pool=None,
                        stamp=state.stamp)
             if mode == GATHER and pool is not None:
                 gather(host, pool, mr.miss_e, mr.miss_s)
-        y = expert_ffn(x[t0:t1], rows, offset, k, host, H, I)
+        if quant:  # host / pool hold quantised slabs [Q8]
+            y = expert_ffn_q8(x[t0:t1], rows, offset, k, host, H, I).astype(np.float64)
+        else:
+            y = expert_ffn(x[t0:t1], rows, offset, k, host, H, I)
         if mode == ZERO_RETURN:
             resident = state.e2s[cids] >= 0
             o, r, m = combine(y, w[t0:t1], pos, t1 - t0, k, resident)

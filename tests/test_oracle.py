@@ -592,3 +592,76 @@ def test_repick_matches_lexsort_top_s_and_keeps_stayers_in_place():
             if resident[e]:
                 assert st.e2s[e] == old_e2s[e]  # experts that stay never move
         assert all(st.s2e[st.e2s[e]] == e for e in range(E) if st.e2s[e] >= 0)
+
+
+# ----------------------------------------------------------------------------
+# W8A8 experts ("Porting vllm-expert-cache to NVIDIA GPUs": W8A8 model;
+# weights and their scales indexed by the same id)
+# ----------------------------------------------------------------------------
+
+def test_quantize_cols_worked_example():
+    # column scales 254/127 = 2, 0 (all zero), 127/127 = 1; codes rint(v / s), halves to even
+    W = np.array([[254.0, 0.0, -127.0], [-127.0, 0.0, 63.5], [63.0, 0.0, 0.0]], dtype=np.float32)
+    q, sc = O.quantize_cols(W)
+    assert sc.tolist() == [2.0, 0.0, 1.0]
+    assert q.tolist() == [[127, 0, -127], [-64, 0, 64], [32, 0, 0]]
+
+
+def test_quantization_error_within_half_a_step():
+    rng = np.random.default_rng(8)
+    W = (rng.standard_normal((300, 40)) * rng.random(40) * 3).astype(np.float32)
+    q, sc = O.quantize_cols(W)
+    assert np.abs(q).max() <= 127 and (np.abs(q) == 127).any(axis=0).all()
+    err = np.abs(W.astype(np.float64) - q.astype(np.float64) * sc.astype(np.float64))
+    assert np.all(err <= 0.5 * sc.astype(np.float64) * (1 + 1e-5) + 1e-30)
+
+
+def test_q8_slab_layout_by_index_formula():
+    rng = np.random.default_rng(9)
+    H, I = 16, 8
+    slab = (rng.standard_normal(3 * H * I) * 0.02).astype(np.float32)
+    b = O.quantize_slab(slab, H, I)
+    assert b.size == O.q8_slab_bytes(H, I) == 3 * H * I + 4 * (2 * I + H)
+    qg, qu, qd, sg, su, sd = O.unpack_q8_slab(b, H, I)
+    wg = slab[:H * I].reshape(H, I)
+    q_ref, s_ref = O.quantize_cols(wg)
+    assert np.array_equal(sg, s_ref) and np.array_equal(qg, q_ref)
+    raw = b.view(np.int8)
+    for k in range(H):
+        for n in range(I):
+            assert raw[((k >> 2) * I + n) * 4 + (k & 3)] == q_ref[k, n]
+    wd = slab[2 * H * I:].reshape(I, H)
+    assert np.array_equal(qd, O.quantize_cols(wd)[0]) and np.array_equal(sd, O.quantize_cols(wd)[1])
+
+
+def test_q8_expert_exact_integer_sums_and_zero_row():
+    from oracle import moe_oracle as MO
+    rng = np.random.default_rng(10)
+    H, I = 32, 16
+    slab = (rng.standard_normal(3 * H * I) * 0.02).astype(np.float32)
+    b = O.quantize_slab(slab, H, I)
+    qg, qu, qd, sg, su, sd = O.unpack_q8_slab(b, H, I)
+    x = rng.standard_normal((3, H)).astype(np.float32)
+    x[1] = 0.0
+    qx, sx = O.quantize_rows(x)
+    # integer sums with Python ints (exact), then the defined fp32 steps
+    for r in range(3):
+        for n in range(I):
+            acc = sum(int(qx[r, kk]) * int(qg[kk, n]) for kk in range(H))
+            g = np.float32(np.float32(acc) * sg[n]) * sx[r]
+            assert np.float32(g) == MO._dequant(qx[r:r + 1].astype(np.int64) @ qg.astype(np.int64), sg, sx[r:r + 1])[0, n]
+    y = O.swiglu_expert_q8(x, b, H, I)
+    assert np.all(y[1] == 0.0) and sx[1] == 0.0
+
+
+def test_q8_expert_close_to_the_bf16_expert():
+    # three 8-bit quantisations (weights per channel, x and h per row), each a
+    # relative noise of about (amax/rms)/127/sqrt(12) ~ 1% for Gaussian data:
+    # the output's relative L2 error is a few percent at most
+    rng = np.random.default_rng(11)
+    H, I = 256, 128
+    slab = (rng.standard_normal(3 * H * I) * 0.02).astype(np.float32)
+    x = rng.standard_normal((6, H)).astype(np.float32)
+    yq = O.swiglu_expert_q8(x, O.quantize_slab(slab, H, I), H, I)
+    y = O.swiglu_expert(x, slab, H, I)
+    assert np.linalg.norm(yq - y) / np.linalg.norm(y) < 4e-2
