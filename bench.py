@@ -140,12 +140,18 @@ class Clocks:
 class Workload:
     """One layer's weights, slot pool, host store, cache state and input batches."""
 
-    def __init__(self, cfg: C.LayerConfig, n_batches: int, dev: str):
+    def __init__(self, cfg: C.LayerConfig, n_batches: int, dev: str, quant: bool = False):
         import expert_slot_cache_gb300 as M
         self.cfg, self.dev, self.M = cfg, dev, M
+        self.quant = quant
         self.wr = C.draw_router(cfg, dev)
         slabs = torch.empty(cfg.E, cfg.slab_elems, dtype=torch.bfloat16, device=dev)
         C.draw_slabs(cfg, dev, out=slabs)
+        if quant:  # W8A8 slabs (weights + slot-indexed scales)
+            qs = M.quantize_slabs(slabs, cfg.H, cfg.I)
+            del slabs
+            slabs = qs
+        self.slab_bytes = slabs[0].numel() * slabs.element_size()
         self.off = C.draw_logit_offset(cfg, dev)
         self.bias = None
         if cfg.bias_cap is not None:
@@ -154,7 +160,7 @@ class Workload:
         if cfg.mode == C.MODE_RESIDENT:
             self.host, self.pool, self.state = None, slabs, None
         else:
-            self.host = torch.empty(cfg.E, cfg.slab_elems, dtype=torch.bfloat16, pin_memory=True)
+            self.host = torch.empty(slabs.shape, dtype=slabs.dtype, pin_memory=True)
             self.host.copy_(slabs)
             s2e0 = C.initial_residency(cfg)
             self.pool = slabs[torch.from_numpy(s2e0.astype(np.int64)).to(dev)].contiguous()
@@ -162,7 +168,7 @@ class Workload:
             self.state = M.CacheState.from_slots(s2e0, cfg.E, dev)
         self.layer = M.SlotCachedMoELayer(self.wr, self.pool, cfg.k, cfg.I, cfg.mode, cfg.policy,
                                           host_slabs=self.host, state=self.state, logit_offset=self.off,
-                                          sel_bias=self.bias, max_tokens=cfg.T)
+                                          sel_bias=self.bias, max_tokens=cfg.T, quant=int(quant))
         self.xs = [C.draw_x(cfg, dev, step=i) for i in range(n_batches)]
         self.out = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16, device=dev)
         self.out_res = self.out_miss = None
@@ -221,6 +227,40 @@ class StackWorkload:
 
     def load_step(self, st: int):
         self.stack.x_all.copy_(self.inputs[st])
+
+
+def w8a8_variants(dev: str, peaks: dict, steps: int = 10, warmup: int = 3) -> dict:
+    """W8A8 experts (the vllm-expert-cache page's W8A8 model; scales
+    slot-indexed inside the slab): the all-resident decode layer at T = 1, 8,
+    64 (HBM GB/s on unique expert bytes, now 3HI + 4(2I+H) per expert) and the
+    main workload's gather configuration (half the bytes over the host link)."""
+    out = {}
+    for T in (1, 8, 64):
+        c = C.qwen(T, S=128, mode=C.MODE_RESIDENT)
+        w = Workload(c, 2 * steps + warmup, dev, quant=True)
+        r = time_steps(w, steps, warmup)
+        units = count_unique_all(w, steps, warmup + steps)
+        t_ffn = (r["kern_ms"]["ffn_gateup"] + r["kern_ms"]["ffn_down"]) * 1e-3
+        ach = units * w.slab_bytes / t_ffn / 1e9 if t_ffn > 0 else 0.0
+        layer_bytes = count_unique_all(w, steps, warmup) * w.slab_bytes
+        out[f"resident_T{T}"] = {
+            "tokens_per_s": T * steps / (r["ms"] * 1e-3), "ms_per_step": r["ms"] / steps,
+            "ffn_hbm": {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                        "frac": ach / peaks["hbm_gbs"], "kernel": "w8a8 stream (ffn_q8)", "bytes_per_unit": w.slab_bytes,
+                        "units": units},
+            "layer_hbm_frac": layer_bytes / (r["ms"] * 1e-3) / 1e9 / peaks["hbm_gbs"]}
+        del w
+        torch.cuda.empty_cache()
+    c = main_config()
+    w = Workload(c, 2 * steps + warmup, dev, quant=True)
+    r = time_steps(w, steps, warmup)
+    out["gather_T64"] = {"tokens_per_s": c.T * steps / (r["ms"] * 1e-3), "ms_per_step": r["ms"] / steps,
+                         "misses_per_step": r["misses"] / steps,
+                         "host_link_GB_per_step": r["gathered_bytes"] / steps / 1e9,
+                         "gather_GBps": r["gathered_bytes"] / (r["kern_ms"]["gather"] * 1e-3) / 1e9
+                         if r["kern_ms"]["gather"] > 0 else None}
+    del w
+    return out
 
 
 def routing_variants(dev: str, steps: int = 10, warmup: int = 3) -> dict:
@@ -527,6 +567,10 @@ def main():
     torch.cuda.set_device(local)
     dev = f"cuda:{local}"
     peaks = _peaks()
+    if args.workload == "w8a8":
+        if rank == 0:
+            print(json.dumps({"workload": "w8a8", **w8a8_variants(dev, _peaks(), args.steps, args.warmup)}))
+        return
     if args.workload == "routing_variants":
         if rank == 0:
             print(json.dumps({"workload": "routing_variants", **routing_variants(dev, args.steps, args.warmup)}))
@@ -626,6 +670,8 @@ def main():
                                              cfg.slab_bytes)
         torch.cuda.empty_cache()
         var["routing_variants"] = routing_variants(dev)
+        torch.cuda.empty_cache()
+        var["w8a8"] = w8a8_variants(dev, peaks)
         line["variants"] = var
 
     if not args.no_cpu_baseline and rank == 0:

@@ -10,4 +10,5 @@ from .binding import (MODE_GATHER, MODE_RESIDENT, MODE_ZERO_RETURN, POLICY_LFU, 
                       POLICY_STATIC, CacheState, LayerArgs, MoeError, SlotCachedMoELayer, bias_table,
                       cache_gather, cache_manage, combine, expert_ffn, ffn_workspace_bytes, layer_workspace_bytes,
                       lib, permute, route, status_str, LayerStack, BIAS_GRADED, BIAS_FLAT, BIAS_HARD,
-                      ROUTE_SIGMOID, ROUTE_DAMPED, cache_count, cache_repick)
+                      ROUTE_SIGMOID, ROUTE_DAMPED, cache_count, cache_repick,
+                      q8_slab_bytes, quantize_slabs, expert_ffn_q8)

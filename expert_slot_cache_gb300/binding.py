@@ -47,7 +47,7 @@ class LayerArgs(ctypes.Structure):
                 ("ids", c_void_p), ("w", c_void_p), ("out", c_void_p), ("out_res", c_void_p),
                 ("out_miss", c_void_p), ("stats", c_void_p), ("dev_status", c_void_p),
                 ("workspace", c_void_p), ("workspace_bytes", c_size_t), ("prof", POINTER(Prof)),
-                ("affinity", c_float), ("route_flags", c_int32), ("window_counts", c_void_p)]
+                ("affinity", c_float), ("route_flags", c_int32), ("window_counts", c_void_p), ("quant", c_int32)]
 
 
 def _sig(name, argtypes, restype=c_int):
@@ -73,6 +73,10 @@ _permute_scratch = _sig("moe_permute_scratch_bytes", [I32, I32], c_size_t)
 _manage = _sig("moe_cache_manage", [V, I32, I32, I32, I32, V, V, V, V, V, V, V, V, V, V, V, V])
 _gather = _sig("moe_cache_gather", [V, V, c_size_t, I32, I32, V, V, V, I32, V, V])
 _count = _sig("moe_cache_count", [V, I32, I32, V, V, V])
+_q8_slab = _sig("moe_q8_slab_bytes", [I32, I32], c_size_t)
+_quantize = _sig("moe_quantize_slabs", [V, I32, I32, I32, V, V])
+_ffn_q8_ws = _sig("moe_ffn_q8_workspace_bytes", [I32, I32, I32, I32], c_size_t)
+_ffn_q8 = _sig("moe_expert_ffn_q8", [V, I32, I32, I32, I32, I32, V, V, V, V, I32, V, I32, V, V, V, c_size_t, V, V])
 _repick = _sig("moe_cache_repick", [V, I32, I32, V, V, V, V, V, V])
 _ffn = _sig("moe_expert_ffn", [V, I32, I32, I32, I32, I32, V, V, V, V, I32, V, I32, V, V, V, V, c_size_t, V, V])
 _ffn_ws = _sig("moe_ffn_workspace_bytes", [I32, I32, I32, I32], c_size_t)
@@ -238,6 +242,31 @@ def cache_repick(counts, state: "CacheState", stream=None) -> RepickResult:
     return r
 
 
+def q8_slab_bytes(H: int, I: int) -> int:
+    return int(_q8_slab(H, I))
+
+
+def quantize_slabs(slabs: torch.Tensor, H: int, I: int, stream=None) -> torch.Tensor:
+    """bf16 slabs [n][3HI] (device) -> W8A8 slabs uint8 [n][q8_slab_bytes] (device)."""
+    n = slabs.shape[0]
+    out = torch.empty(n, q8_slab_bytes(H, I), dtype=torch.uint8, device=slabs.device)
+    _ck(_quantize(_p(slabs), n, H, I, _p(out), _s(stream)), "moe_quantize_slabs")
+    return out
+
+
+def expert_ffn_q8(x, k, I, E, offset, rows, list_e, n_list, max_list, pool_q, e2s=None, y=None, workspace=None,
+                  dev_status=None, stream=None) -> torch.Tensor:
+    T, H = x.shape
+    if y is None:
+        y = torch.zeros(T * k, H, dtype=torch.float32, device=x.device)
+    if workspace is None:
+        workspace = torch.empty(int(_ffn_q8_ws(T, H, k, I)), dtype=torch.uint8, device=x.device)
+    _ck(_ffn_q8(_p(x), T, H, I, k, E, _p(offset), _p(rows), _p(list_e), _p(n_list), max_list, _p(pool_q),
+                pool_q.shape[0], _p(e2s), _p(y), _p(workspace), workspace.numel(), _p(dev_status), _s(stream)),
+        "moe_expert_ffn_q8")
+    return y
+
+
 def ffn_workspace_bytes(T: int, H: int, k: int, I: int) -> int:
     return int(_ffn_ws(T, H, k, I))
 
@@ -284,7 +313,7 @@ class SlotCachedMoELayer:
 
     def __init__(self, w_router, pool, k, I, mode, policy=POLICY_LRU, host_slabs=None, state=None,
                  logit_offset=None, sel_bias=None, max_tokens=64, side_stream=True, affinity=0.0,
-                 route_flags=0, window_counts=None):
+                 route_flags=0, window_counts=None, quant=0):
         self.w_router, self.pool, self.k, self.I = w_router, pool, k, I
         self.H, self.E = w_router.shape
         self.S = pool.shape[0]
@@ -294,6 +323,7 @@ class SlotCachedMoELayer:
         self.affinity = float(affinity)
         self.route_flags = int(route_flags)
         self.window_counts = window_counts
+        self.quant = int(quant)  # pool / host hold W8A8 slabs (quantize_slabs)
         dev = pool.device
         self.stats = torch.zeros(4, dtype=torch.int64, device=dev)
         self.dev_status = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -322,7 +352,7 @@ class SlotCachedMoELayer:
                       ids.data_ptr(), w.data_ptr(), out.data_ptr(), _ptr(out_res), _ptr(out_miss),
                       self.stats.data_ptr(), self.dev_status.data_ptr(), self.workspace.data_ptr(),
                       self.workspace.numel(), ctypes.pointer(prof) if prof is not None else None, self.affinity,
-                      self.route_flags, _ptr(self.window_counts))
+                      self.route_flags, _ptr(self.window_counts), self.quant)
         main = torch.cuda.current_stream() if stream is None else stream
         # the library forks to and joins back from the side stream itself
         _ck(_layer(ctypes.byref(a), c_void_p(main.cuda_stream),

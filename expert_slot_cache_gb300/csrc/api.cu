@@ -58,7 +58,7 @@ static LayerWs carve(void* base, int n, int H, int E, int I, int T) {
     w.xp = (uint16_t*)take(2 * (size_t)n * H);
     w.hb = (uint16_t*)take(2 * (size_t)n * I);
   }
-  w.skp_bytes = sk_part_bytes(n, H, I);
+  w.skp_bytes = std::max(sk_part_bytes(n, H, I), q8_ws_bytes(n, H, I));  // bf16 stream or W8A8 buffers
   if (w.skp_bytes) w.skp = (float*)take(w.skp_bytes);
   w.bytes = off;
   return w;
@@ -184,6 +184,8 @@ extern "C" int moe_layer_forward(const moe_layer_args* a, moe_stream_t main_s, m
     return MOE_ERR_ARG;
   }
   if (mode == MOE_MODE_ZERO_RETURN && (!a->out_res || !a->out_miss)) return MOE_ERR_ARG;
+  if (a->quant != 0 && a->quant != 1) return MOE_ERR_ARG;
+  if (a->quant && (mode == MOE_MODE_ZERO_RETURN || H % 16 || I % 16)) return MOE_ERR_ARG;
   if (mode == MOE_MODE_GATHER && S < E && S < k) return MOE_ERR_CAPACITY;
   if ((uintptr_t)a->pool % 16 || (uintptr_t)a->workspace % 256 || (uintptr_t)a->x % 16) return MOE_ERR_ALIGN;
 
@@ -203,7 +205,7 @@ extern "C" int moe_layer_forward(const moe_layer_args* a, moe_stream_t main_s, m
   Prof prof;
   prof.p = a->prof;
   if (prof.p) prof.p->used = 0;
-  const size_t slab_bytes = (size_t)6 * H * I;
+  const size_t slab_bytes = a->quant ? q8_slab_bytes_h(H, I) : (size_t)6 * H * I;
   prof.begin(MOE_PROF_ROUTE, ms);
   int r = moe_route_ex(a->x, a->w_router, a->logit_offset, a->sel_bias, a->affinity != 0.f ? a->e2s : nullptr,
                        a->affinity, a->route_flags, T, H, E, k, ws.logits,
@@ -226,13 +228,17 @@ extern "C" int moe_layer_forward(const moe_layer_args* a, moe_stream_t main_s, m
               (const uint16_t*)a->pool, a->e2s, (const uint16_t*)a->host_slabs, (size_t)3 * H * I, ws.hbuf, ws.y,
               a->dev_status, S, 1, ws.xp, ws.hb, nullptr, ws.skp, ws.skp_bytes};
     // tensor-core path: y travels as bf16 through the same buffer (half the bytes)
-    const bool y_bf16 = mode != MOE_MODE_ZERO_RETURN && prefill_eligible(f, n);
+    const bool y_bf16 = !a->quant && mode != MOE_MODE_ZERO_RETURN && prefill_eligible(f, n);
+    // the FFN of one expert list: bf16 slabs (stream / prefill / CUDA-core paths) or W8A8 slabs
+    auto ffn = [&](const FfnArgs& fa, cudaStream_t st) {
+      return a->quant ? launch_ffn_q8(fa, ws.skp, ws.skp_bytes, lmax, st, &prof) : launch_ffn(fa, lmax, st, &prof);
+    };
     if (y_bf16) f.yb = (uint16_t*)ws.y;
     if (mode == MOE_MODE_RESIDENT) {
       f.list_e = ws.act_e;
       f.n_list = ws.n_act;
       f.host = nullptr;
-      if ((r = launch_ffn(f, lmax, ms, &prof)) != MOE_OK) return r;
+      if ((r = ffn(f, ms)) != MOE_OK) return r;
     } else {
       prof.begin(MOE_PROF_MANAGE, ms);
       r = launch_manage(ids_c, n, E, S, policy, a->e2s, a->s2e, a->prio, a->stamp, ws.miss_e, ws.miss_s, ws.n_miss,
@@ -258,15 +264,15 @@ extern "C" int moe_layer_forward(const moe_layer_args* a, moe_stream_t main_s, m
         if (r != MOE_OK) return r;
         prof.end(side);
         if (two) MOE_CUDA_TRY(cudaEventRecord(ev->join, ss));
-        if ((r = launch_ffn(fh, lmax, ms, &prof)) != MOE_OK) return r;
+        if ((r = ffn(fh, ms)) != MOE_OK) return r;
         if (two) MOE_CUDA_TRY(cudaStreamWaitEvent(ms, ev->join, 0));
-        if ((r = launch_ffn(fm, lmax, ms, &prof)) != MOE_OK) return r;
+        if ((r = ffn(fm, ms)) != MOE_OK) return r;
       } else {
         // zero-return: resident experts from the pool on main, missing ones
         // straight from the host store on the side stream; then one add.
-        if ((r = launch_ffn(fm, lmax, side, &prof)) != MOE_OK) return r;
+        if ((r = ffn(fm, side)) != MOE_OK) return r;
         if (two) MOE_CUDA_TRY(cudaEventRecord(ev->join, ss));
-        if ((r = launch_ffn(fh, lmax, ms, &prof)) != MOE_OK) return r;
+        if ((r = ffn(fh, ms)) != MOE_OK) return r;
         if (two) MOE_CUDA_TRY(cudaStreamWaitEvent(ms, ev->join, 0));
       }
     }

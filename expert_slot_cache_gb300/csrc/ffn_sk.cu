@@ -35,6 +35,7 @@
 #include <algorithm>
 
 #include "internal.cuh"
+#include "sched.cuh"
 #include "tc05.cuh"
 
 namespace moe {
@@ -65,44 +66,6 @@ struct SkPass {
   int G, jcap;
   uint32_t tcols;  // TMEM columns allocated: two accumulator buffers, rounded up to a power of two
 };
-
-// Stages per CTA range: equal ranges covering all stages with at most G CTAs,
-// and no expert spanning more than jcap ranges.
-__device__ __forceinline__ int sk_len(int n_list, int NSR, int G, int jcap) {
-  const int total = n_list * NSR;
-  int L = (total + G - 1) / G;
-  if ((NSR + L - 1) / L + 1 > jcap) L = (NSR + jcap - 2) / (jcap - 1);
-  return L;
-}
-
-__device__ __forceinline__ bool sk_slot(const FfnArgs& a, int li, int& e, int& slot) {
-  e = a.list_e[li];
-  if (e < 0 || e >= a.E) return false;
-  slot = a.e2s ? a.e2s[e] : e;
-  return slot >= 0 && slot < a.S;
-}
-
-struct SkSeg {
-  int e, slot, s_lo, s_hi, j, p0, nb;
-};
-
-// Calls f(seg) for each (expert part, token batch) of this CTA's range in
-// order; stops early when f returns false.  Every role walks the same list.
-template <class F>
-__device__ __forceinline__ void sk_segments(const FfnArgs& a, const SkPass& sp, int L, int beg, int end, F&& f) {
-  for (int li = beg / sp.NSR; li * sp.NSR < end; ++li) {
-    SkSeg g;
-    if (!sk_slot(a, li, g.e, g.slot)) continue;
-    g.s_lo = max(beg, li * sp.NSR) - li * sp.NSR;
-    g.s_hi = min(end, (li + 1) * sp.NSR) - li * sp.NSR;
-    g.j = (int)blockIdx.x - (li * sp.NSR) / L;
-    const int pb = a.offset[g.e], pe = a.offset[g.e + 1];
-    for (g.p0 = pb; g.p0 < pe; g.p0 += kDN) {
-      g.nb = min(kDN, pe - g.p0);
-      if (!f(g)) return;
-    }
-  }
-}
 
 // Accumulator columns 0..W-1 (tokens) of every tile -> parts; loads of up to
 // 32 registers are issued before one wait.
@@ -147,7 +110,7 @@ __global__ void __launch_bounds__(kDThreads, 1) ffn_sk_kernel(const FfnArgs a, c
   // the lists predate the kernel before (the row gather, or the gate/up reduce)
   const int n_list = *a.n_list;
   const int n = a.T * a.k;
-  const int L = n_list > 0 ? sk_len(n_list, sp.NSR, sp.G, sp.jcap) : 1;
+  const int L = n_list > 0 ? stream_len(n_list, sp.NSR, sp.G, sp.jcap) : 1;
   const int total = n_list * sp.NSR;
   const int beg = blockIdx.x * L, end = min(beg + L, total);
   if (beg >= end) {  // uniform over the CTA: nothing allocated yet
@@ -198,7 +161,7 @@ __global__ void __launch_bounds__(kDThreads, 1) ffn_sk_kernel(const FfnArgs a, c
         ndef = 0;
         waited = true;
       };
-      sk_segments(a, sp, L, beg, end, [&](const SkSeg& g) {
+      stream_segments<kDN>(a, sp.NSR, L, beg, end, [&](const StreamSeg& g) {
         const bool direct = !DOWN && g.nb <= kDDirectMax;
         int tok[kDDirectMax];
         if (direct)
@@ -255,10 +218,10 @@ __global__ void __launch_bounds__(kDThreads, 1) ffn_sk_kernel(const FfnArgs a, c
     if (lane == 0) {
       for (int li = beg / sp.NSR; li * sp.NSR < end; ++li) {
         int e, slot;
-        if (!sk_slot(a, li, e, slot)) set_status(a.status, e < 0 || e >= a.E ? MOE_DEV_BAD_EXPERT : MOE_DEV_BAD_SLOT);
+        if (!stream_slot(a, li, e, slot)) set_status(a.status, e < 0 || e >= a.E ? MOE_DEV_BAD_EXPERT : MOE_DEV_BAD_SLOT);
       }
       uint32_t it = 0, seg = 0;
-      sk_segments(a, sp, L, beg, end, [&](const SkSeg& g) {
+      stream_segments<kDN>(a, sp.NSR, L, beg, end, [&](const StreamSeg& g) {
         const uint32_t buf = seg & 1u, use = seg >> 1;
         if (use > 0 && !*abort_flag && !mbar_wait(&tempty[buf], (use - 1) & 1u)) {
           *abort_flag = 1;
@@ -297,7 +260,7 @@ __global__ void __launch_bounds__(kDThreads, 1) ffn_sk_kernel(const FfnArgs a, c
     // epilogue warps 2..5; TMEM lane quarter q = warp % 4 holds output columns q*32 .. q*32+31 of each tile
     const int q = warp & 3;
     uint32_t seg = 0;
-    sk_segments(a, sp, L, beg, end, [&](const SkSeg& g) {
+    stream_segments<kDN>(a, sp.NSR, L, beg, end, [&](const StreamSeg& g) {
       const uint32_t buf = seg & 1u, use = seg >> 1;
       if (!*abort_flag && !mbar_wait(&tfull[buf], use & 1u)) {
         *abort_flag = 1;
@@ -357,13 +320,12 @@ __global__ void __launch_bounds__(32 * kSkRedWarps) sk_reduce_kernel(const FfnAr
     return;
   }
   int e, slot;
-  if (!sk_slot(a, li, e, slot)) {
+  if (!stream_slot(a, li, e, slot)) {
     pdl_wait();
     return;
   }
-  const int L = sk_len(n_list, NSR, G, jcap);
-  const int j0 = (li * NSR) / L;
-  const int J = ((li + 1) * NSR - 1) / L - j0 + 1;
+  const int L = stream_len(n_list, NSR, G, jcap);
+  const int J = stream_parts(li, NSR, L);
   const int n = a.T * a.k;
   const int ncol = SWIGLU ? N / 2 : N;
   const int ncol4 = ncol / 4;

@@ -62,6 +62,9 @@ bool prefill_eligible(const FfnArgs& a, int n);
 int launch_gather_rows(const uint16_t* x, const int32_t* rows, int n, int H, int k, uint16_t* xp, int sms,
                        cudaStream_t stream);
 size_t sk_part_bytes(int n, int H, int I);
+size_t q8_slab_bytes_h(int H, int I);
+size_t q8_ws_bytes(int n, int H, int I);
+int launch_ffn_q8(const FfnArgs& a, void* ws, size_t ws_bytes, int max_list, cudaStream_t stream, Prof* prof);
 bool sk_eligible(const FfnArgs& a);
 int launch_ffn_sk(const FfnArgs& a, int max_list, cudaStream_t stream, Prof* prof);
 size_t prefill_extra_bytes(int n, int H, int I);

@@ -1,0 +1,561 @@
+// W8A8 experts: 8-bit weights with per-output-channel scales, 8-bit
+// activations with per-row scales, exact int32 dot products.
+//
+// "Porting vllm-expert-cache to NVIDIA GPUs": the measured model is
+// Qwen3-30B-A3B W8A8, and "weights and their scales are indexed by the same
+// id, so both must be slot-indexed".  Here the scales travel inside the
+// quantised slab, so manage and gather move them with the weights.
+//
+// Quantised slab (q8_slab_bytes = 3HI + 4(2I + H)):
+//   Wg, Wu [H][I], Wd [I][H] as int8, every 4 consecutive input rows of a
+//   column packed into one int32 (byte (k, n) at ((k/4)*N + n)*4 + k%4), then
+//   fp32 scales sg[I], su[I], sd[H].
+// Codes: symmetric, scale = amax / 127, code = rint(v / scale) clamped to
+// +-127 (scale 0 gives code 0), all fp32 one operation at a time
+// (fp32def.cuh), so they are reproducible bit for bit.
+//
+// Decode FFN: the same balanced stream as the bf16 path (sched.cuh), on CUDA
+// cores: a stage is 16 input rows x all output columns (one 1-D bulk copy per
+// matrix), a thread owns 4 output columns and folds 4 input rows per dp4a; a
+// range's int32 sums go to parts[j][p][N]; the reduces add the parts (integer,
+// exact), dequantise, form h = silu(g)*u, quantise h per row (gate/up) or write
+// y (down).  The int8 tensor-core path is not used: decode is a weight stream
+// and the CUDA cores keep up with it.
+#include <algorithm>
+
+#include "fp32def.cuh"
+#include "internal.cuh"
+#include "sched.cuh"
+#include "tc05.cuh"
+
+namespace moe {
+
+constexpr int kQK = 16;                 // input rows per stage (4 quads)
+constexpr int kQRB = 8;                 // tokens per pass over the weights
+constexpr int kQActTok = kQRB + 4;      // tokens copied per quad (aligned start: p0 rounded down to 4)
+constexpr int kQActBytes = 4 * kQActTok * 4;  // 4 quads x 12 tokens x int32
+constexpr int kQRing = 200 * 1024;
+constexpr int kQMaxStages = 8;
+constexpr int kQMaxConsumers = 512;
+constexpr int kQJcapMax = 160;
+constexpr size_t kQPartBudget = size_t(16) << 20;
+constexpr int kQMaxRows = 4096;
+
+static size_t qal256(size_t v) { return (v + 255) & ~size_t(255); }
+
+__host__ __device__ __forceinline__ size_t q8_slab_bytes_hd(int H, int I) {
+  return (size_t)3 * H * I + (size_t)4 * (2 * I + H);
+}
+size_t q8_slab_bytes_h(int H, int I) { return q8_slab_bytes_hd(H, I); }
+
+// ---------------------------------------------------------------------------
+// Weight quantisation (offline, once per expert)
+// ---------------------------------------------------------------------------
+// grid (ceil(N/128), 3 matrices, experts); thread = one output column.
+__global__ void __launch_bounds__(128) quantize_slabs_kernel(const uint16_t* __restrict__ src, int H, int I,
+                                                             uint8_t* __restrict__ dst) {
+  const int m = blockIdx.y;
+  const int K = m < 2 ? H : I, N = m < 2 ? I : H;
+  const int n = blockIdx.x * 128 + threadIdx.x;
+  if (n >= N) return;
+  const size_t mat = (size_t)H * I;
+  const uint16_t* w = src + (size_t)blockIdx.z * 3 * mat + (size_t)m * mat;
+  uint8_t* q = dst + (size_t)blockIdx.z * q8_slab_bytes_hd(H, I) + (size_t)m * mat;
+  float amax = 0.f;
+  for (int k = 0; k < K; ++k) amax = fmaxf(amax, fabsf(bf16_to_f32(w[(size_t)k * N + n])));
+  const float s = __fdiv_rn(amax, 127.f);
+  uint32_t* q4 = reinterpret_cast<uint32_t*>(q);
+  for (int k = 0; k < K; k += 4) {
+    uint32_t pk = 0;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) pk |= (uint32_t)(q8_code(bf16_to_f32(w[(size_t)(k + b) * N + n]), s) & 0xff) << (8 * b);
+    q4[(size_t)(k >> 2) * N + n] = pk;
+  }
+  float* sc = reinterpret_cast<float*>(dst + (size_t)blockIdx.z * q8_slab_bytes_hd(H, I) + 3 * mat);
+  sc[(m == 0 ? 0 : m == 1 ? I : 2 * I) + n] = s;
+}
+
+// ---------------------------------------------------------------------------
+// Activation quantisation: x rows of the grouped positions -> codes, quad-major
+// xq[(h/4)][npad] (int32 = 4 codes), scale sx[p].  One CTA per position.
+// ---------------------------------------------------------------------------
+constexpr int kQRowThreads = 256;
+
+__device__ __forceinline__ float block_max(float v, float* red) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  __syncthreads();
+  if (lane == 0) red[w] = v;
+  __syncthreads();
+  float r = 0.f;
+  for (int i = 0; i < (int)(blockDim.x >> 5); ++i) r = fmaxf(r, red[i]);
+  return r;
+}
+
+__global__ void __launch_bounds__(kQRowThreads) q8_rows_kernel(const uint16_t* __restrict__ x,
+                                                               const int32_t* __restrict__ rows, int n, int H, int k,
+                                                               int npad, uint32_t* __restrict__ xq,
+                                                               float* __restrict__ sx) {
+  __shared__ float red[32];
+  pdl_trigger();
+  const int p = blockIdx.x;
+  const uint16_t* xr = x + (size_t)(rows[p] / k) * H;
+  float amax = 0.f;
+  for (int h = threadIdx.x; h < H; h += blockDim.x) amax = fmaxf(amax, fabsf(bf16_to_f32(xr[h])));
+  amax = block_max(amax, red);
+  const float s = __fdiv_rn(amax, 127.f);
+  for (int q = threadIdx.x; q < H / 4; q += blockDim.x) {
+    uint32_t pk = 0;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) pk |= (uint32_t)(q8_code(bf16_to_f32(xr[4 * q + b]), s) & 0xff) << (8 * b);
+    xq[(size_t)q * npad + p] = pk;
+  }
+  if (threadIdx.x == 0) sx[p] = s;
+}
+
+// ---------------------------------------------------------------------------
+// The stream (one pass: gate/up or down)
+// ---------------------------------------------------------------------------
+struct QPass {
+  int32_t* part;     // [jcap][n][N]
+  const uint32_t* act;  // quad-major codes [K/4][npad] of the pass's input rows
+  int npad;
+  int N, K, NSR, nst, wbytes, stride, G, jcap;
+  size_t qslab;      // bytes of one quantised slab
+};
+
+__device__ __forceinline__ void q8_bulk(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  bulk_load(dst, src, bytes, bar);
+}
+
+template <bool DOWN, int RB>
+__device__ __forceinline__ void q8_consume(const QPass& qp, int n, const StreamSeg& g, const unsigned char* ring,
+                                           uint64_t* full, uint64_t* empty, uint32_t& it,
+                                           volatile int* abort_flag, int32_t* status, int I) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int c = tid;  // output columns 4c .. 4c+3
+  int acc[RB][4];
+#pragma unroll
+  for (int r = 0; r < RB; ++r)
+#pragma unroll
+    for (int q = 0; q < 4; ++q) acc[r][q] = 0;
+  // byte offset of this thread's 16 bytes in quad-row 0 of a stage, and the quad-row stride
+  int off, qstride;
+  if (DOWN) {
+    off = 16 * c;
+    qstride = 4 * qp.N;
+  } else {
+    off = 4 * c < I ? 16 * c : kQK * I + 16 * c - 4 * I;  // Wu rows follow the stage's Wg rows
+    qstride = 4 * I;
+  }
+  const int ao = g.p0 & 3;  // token r of the batch sits at index ao + r of each quad's copy
+  for (int s = g.s_lo; s < g.s_hi; ++s, ++it) {
+    const int sl = it % qp.nst;
+    if (!*abort_flag && !mbar_wait(&full[sl], (it / qp.nst) & 1u)) {
+      *abort_flag = 1;
+      set_status(status, MOE_DEV_TIMEOUT);
+    }
+    const unsigned char* st = ring + sl * qp.stride;
+    const int32_t* act = reinterpret_cast<const int32_t*>(st + qp.wbytes);
+#pragma unroll
+    for (int qq = 0; qq < 4; ++qq) {
+      const int4 w = *reinterpret_cast<const int4*>(st + off + qq * qstride);
+#pragma unroll
+      for (int r = 0; r < RB; ++r) {
+        const int xa = act[qq * kQActTok + ao + r];
+        acc[r][0] = __dp4a(w.x, xa, acc[r][0]);
+        acc[r][1] = __dp4a(w.y, xa, acc[r][1]);
+        acc[r][2] = __dp4a(w.z, xa, acc[r][2]);
+        acc[r][3] = __dp4a(w.w, xa, acc[r][3]);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[sl]);
+  }
+#pragma unroll
+  for (int r = 0; r < RB; ++r)
+    if (r < g.nb)
+      *reinterpret_cast<int4*>(qp.part + ((size_t)g.j * n + g.p0 + r) * qp.N + 4 * c) =
+          make_int4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
+}
+
+template <bool DOWN>
+__global__ void __launch_bounds__(kQMaxConsumers + 32, 1) ffn_q8_kernel(const FfnArgs a, const QPass qp) {
+  extern __shared__ __align__(16) unsigned char q8_raw[];
+  unsigned char* ring =
+      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(q8_raw) + 127) & ~uintptr_t(127));
+  uint64_t* full = reinterpret_cast<uint64_t*>(ring + qp.nst * qp.stride);
+  uint64_t* empty = full + kQMaxStages;
+  __shared__ int s_abort;
+  const int nc = qp.N / 4;
+  const int tid = threadIdx.x;
+  pdl_trigger();
+  const int n_list = *a.n_list;
+  const int n = a.T * a.k;
+  const int L = n_list > 0 ? stream_len(n_list, qp.NSR, qp.G, qp.jcap) : 1;
+  const int total = n_list * qp.NSR;
+  const int beg = blockIdx.x * L, end = min(beg + L, total);
+  if (beg >= end) {
+    pdl_wait();
+    return;
+  }
+  if (tid == 0) {
+    for (int s = 0; s < qp.nst; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], nc / 32);
+    }
+    s_abort = 0;
+    mbar_fence_init();
+  }
+  __syncthreads();
+  volatile int* abort_flag = &s_abort;
+
+  if (tid == nc) {
+    // producer: weights stream at once; the activations (written by the kernel
+    // before) only after griddepcontrol.wait
+    uint32_t it = 0;
+    bool waited = false;
+    int ndef = 0, d_q0[kQMaxStages], d_p0[kQMaxStages], last_use[kQMaxStages];
+    for (int s = 0; s < kQMaxStages; ++s) last_use[s] = -1;
+    auto issue_act = [&](int sl, int q0, int p0) {
+      unsigned char* dst = ring + sl * qp.stride + qp.wbytes;
+      const uint32_t* src = qp.act + (size_t)q0 * qp.npad + (p0 & ~3);
+      for (int qq = 0; qq < 4; ++qq)
+        q8_bulk(dst + qq * kQActTok * 4, src + (size_t)qq * qp.npad, kQActTok * 4, &full[sl]);
+    };
+    auto flush = [&]() {
+      pdl_wait();
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      for (int d = 0; d < ndef; ++d) issue_act(d, d_q0[d], d_p0[d]);
+      ndef = 0;
+      waited = true;
+    };
+    stream_segments<kQRB>(a, qp.NSR, L, beg, end, [&](const StreamSeg& g) {
+      const unsigned char* w = reinterpret_cast<const unsigned char*>(a.pool) + (size_t)g.slot * qp.qslab;
+      for (int s = g.s_lo; s < g.s_hi; ++s, ++it) {
+        const int sl = it % qp.nst;
+        const uint32_t use = it / qp.nst;
+        if (use > 0) {
+          if (!waited) flush();
+          if (!*abort_flag && !mbar_wait(&empty[sl], (use - 1) & 1u)) {
+            *abort_flag = 1;
+            set_status(a.status, MOE_DEV_TIMEOUT);
+          }
+        }
+        if (*abort_flag) return false;
+        unsigned char* dst = ring + sl * qp.stride;
+        const int q0 = s * (kQK / 4);  // first quad of the stage
+        mbar_expect_tx(&full[sl], qp.wbytes + kQActBytes);
+        const size_t mat = (size_t)a.H * a.I;
+        if (DOWN) {
+          q8_bulk(dst, w + 2 * mat + (size_t)q0 * a.H * 4, qp.wbytes, &full[sl]);
+        } else {
+          const uint32_t mb = qp.wbytes / 2;
+          q8_bulk(dst, w + (size_t)q0 * a.I * 4, mb, &full[sl]);
+          q8_bulk(dst + mb, w + mat + (size_t)q0 * a.I * 4, mb, &full[sl]);
+        }
+        if (waited) {
+          issue_act(sl, q0, g.p0);
+        } else {
+          d_q0[ndef] = q0;
+          d_p0[ndef] = g.p0;
+          ++ndef;
+        }
+        last_use[sl] = (int)use;
+      }
+      return true;
+    });
+    if (!waited) flush();
+    if (*abort_flag)
+      for (int s = 0; s < qp.nst; ++s)
+        if (last_use[s] >= 0) mbar_wait(&full[s], (uint32_t)last_use[s] & 1u);
+  } else if (tid < nc) {
+    uint32_t it = 0;
+    stream_segments<kQRB>(a, qp.NSR, L, beg, end, [&](const StreamSeg& g) {
+      if (g.nb <= 1)
+        q8_consume<DOWN, 1>(qp, n, g, ring, full, empty, it, abort_flag, a.status, a.I);
+      else if (g.nb <= 2)
+        q8_consume<DOWN, 2>(qp, n, g, ring, full, empty, it, abort_flag, a.status, a.I);
+      else if (g.nb <= 4)
+        q8_consume<DOWN, 4>(qp, n, g, ring, full, empty, it, abort_flag, a.status, a.I);
+      else
+        q8_consume<DOWN, 8>(qp, n, g, ring, full, empty, it, abort_flag, a.status, a.I);
+      return true;
+    });
+  }
+  if (tid == 0)
+    for (int li = beg / qp.NSR; li * qp.NSR < end; ++li) {
+      int e, slot;
+      if (!stream_slot(a, li, e, slot)) set_status(a.status, e < 0 || e >= a.E ? MOE_DEV_BAD_EXPERT : MOE_DEV_BAD_SLOT);
+    }
+  __syncwarp();
+  __syncthreads();
+}
+
+// ---------------------------------------------------------------------------
+// Reduces.  Integer parts are added exactly (any order gives the same sum).
+// ---------------------------------------------------------------------------
+// gate/up: one CTA per listed expert; per row p: g, u (dequantised), h =
+// silu(g)*u, amax over the row, codes of h into hq (quad-major), sh[p].
+__global__ void __launch_bounds__(kQRowThreads) q8_reduce_gu_kernel(const FfnArgs a, const int32_t* __restrict__ part,
+                                                                    int NSR, int G, int jcap, size_t qslab,
+                                                                    const float* __restrict__ sx, int npad,
+                                                                    uint32_t* __restrict__ hq,
+                                                                    float* __restrict__ sh) {
+  __shared__ float red[32];
+  pdl_trigger();
+  const int li = blockIdx.x;
+  const int n_list = *a.n_list;
+  int e = -1, slot = -1;
+  const bool ok = li < n_list && stream_slot(a, li, e, slot);
+  pdl_wait();
+  if (!ok) return;
+  const int L = stream_len(n_list, NSR, G, jcap);
+  const int J = stream_parts(li, NSR, L);
+  const int n = a.T * a.k, I = a.I, N = 2 * I;
+  const size_t mat = (size_t)a.H * I;
+  const float* sc = reinterpret_cast<const float*>(reinterpret_cast<const unsigned char*>(a.pool) +
+                                                   (size_t)slot * qslab + 3 * mat);
+  const float* sg = sc;
+  const float* su = sc + I;
+  const size_t pstride = (size_t)n * N;
+  const int pb = a.offset[e], pe = a.offset[e + 1];
+  for (int p = pb; p < pe; ++p) {
+    const float s_x = sx[p];
+    float hv[4][4];  // up to 4 quads per thread (I <= 16 * blockDim)
+    float amax = 0.f;
+    int nq = 0;
+    for (int q = threadIdx.x; q < I / 4; q += blockDim.x, ++nq) {
+      int4 ag = make_int4(0, 0, 0, 0), au = ag;
+      for (int jj = 0; jj < J; ++jj) {
+        const int4 tg = *reinterpret_cast<const int4*>(part + jj * pstride + (size_t)p * N + 4 * q);
+        const int4 tu = *reinterpret_cast<const int4*>(part + jj * pstride + (size_t)p * N + I + 4 * q);
+        ag.x += tg.x; ag.y += tg.y; ag.z += tg.z; ag.w += tg.w;
+        au.x += tu.x; au.y += tu.y; au.z += tu.z; au.w += tu.w;
+      }
+      const int gi[4] = {ag.x, ag.y, ag.z, ag.w}, ui[4] = {au.x, au.y, au.z, au.w};
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const int i = 4 * q + b;
+        const float g = __fmul_rn(__fmul_rn(__int2float_rn(gi[b]), sg[i]), s_x);
+        const float u = __fmul_rn(__fmul_rn(__int2float_rn(ui[b]), su[i]), s_x);
+        const float h = __fmul_rn(silu32_def(g), u);
+        hv[nq][b] = h;
+        amax = fmaxf(amax, fabsf(h));
+      }
+    }
+    amax = block_max(amax, red);
+    const float s = __fdiv_rn(amax, 127.f);
+    nq = 0;
+    for (int q = threadIdx.x; q < I / 4; q += blockDim.x, ++nq) {
+      uint32_t pk = 0;
+#pragma unroll
+      for (int b = 0; b < 4; ++b) pk |= (uint32_t)(q8_code(hv[nq][b], s) & 0xff) << (8 * b);
+      hq[(size_t)q * npad + p] = pk;
+    }
+    if (threadIdx.x == 0) sh[p] = s;
+  }
+}
+
+// down: y[p][n] = (float(sum of parts) * sd[n]) * sh[p]; block = 128 columns of one listed expert.
+__global__ void __launch_bounds__(256) q8_reduce_d_kernel(const FfnArgs a, const int32_t* __restrict__ part, int NSR,
+                                                          int G, int jcap, size_t qslab,
+                                                          const float* __restrict__ sh, float* __restrict__ y) {
+  __shared__ int4 sp[8][32];
+  pdl_trigger();
+  const int li = blockIdx.y;
+  const int n_list = *a.n_list;
+  int e = -1, slot = -1;
+  const bool ok = li < n_list && stream_slot(a, li, e, slot);
+  pdl_wait();
+  if (!ok) return;
+  const int L = stream_len(n_list, NSR, G, jcap);
+  const int J = stream_parts(li, NSR, L);
+  const int n = a.T * a.k, H = a.H;
+  const float* sd = reinterpret_cast<const float*>(reinterpret_cast<const unsigned char*>(a.pool) +
+                                                   (size_t)slot * qslab + (size_t)3 * H * a.I + (size_t)8 * a.I);
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int c4 = blockIdx.x * 32 + lane;
+  const size_t pstride = (size_t)n * H;
+  const int pb = a.offset[e], pe = a.offset[e + 1];
+  for (int p = pb; p < pe; ++p) {
+    int4 acc = make_int4(0, 0, 0, 0);
+    if (4 * c4 < H)
+      for (int jj = w; jj < J; jj += 8) {
+        const int4 t = *reinterpret_cast<const int4*>(part + jj * pstride + (size_t)p * H + 4 * c4);
+        acc.x += t.x; acc.y += t.y; acc.z += t.z; acc.w += t.w;
+      }
+    sp[w][lane] = acc;
+    __syncthreads();
+    if (w == 0 && 4 * c4 < H) {
+      for (int k2 = 1; k2 < 8; ++k2) {
+        const int4 t = sp[k2][lane];
+        acc.x += t.x; acc.y += t.y; acc.z += t.z; acc.w += t.w;
+      }
+      const float s = sh[p];
+      const int ai[4] = {acc.x, acc.y, acc.z, acc.w};
+      float o[4];
+#pragma unroll
+      for (int b = 0; b < 4; ++b) o[b] = __fmul_rn(__fmul_rn(__int2float_rn(ai[b]), sd[4 * c4 + b]), s);
+      *reinterpret_cast<float4*>(y + (size_t)p * H + 4 * c4) = make_float4(o[0], o[1], o[2], o[3]);
+    }
+    __syncthreads();
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+static int q_jcap(int n, int N) {
+  const size_t per = (size_t)n * N * 4;
+  const size_t j = per ? kQPartBudget / per : 0;
+  return (int)std::max<size_t>(3, std::min<size_t>(j, kQJcapMax));
+}
+
+static int q_npad(int n) { return ((n + kQActTok + 3) / 4) * 4; }
+
+// Layout: [gate/up parts | down parts] (equal halves, int32), xq [H/4][npad],
+// hq [I/4][npad] (int32 quads), sx [n], sh [n] (fp32).
+size_t q8_ws_bytes(int n, int H, int I) {
+  if (n < 1 || n > kQMaxRows) return 0;
+  const size_t half = qal256(std::max((size_t)q_jcap(n, 2 * I) * n * 2 * I * 4, (size_t)q_jcap(n, H) * n * H * 4));
+  const int np = q_npad(n);
+  return 2 * half + qal256((size_t)H * np) + qal256((size_t)I * np) + 2 * qal256((size_t)4 * n);
+}
+
+struct QCarve {
+  int32_t *gpart, *ypart;
+  uint32_t *xq, *hq;
+  float *sx, *sh;
+  int jg, jd, npad;
+};
+
+static bool q_carve(const FfnArgs& a, void* base, size_t bytes, QCarve* c) {
+  const int n = a.T * a.k;
+  const int np = q_npad(n);
+  const size_t act = qal256((size_t)a.H * np) + qal256((size_t)a.I * np) + 2 * qal256((size_t)4 * n);
+  if (!base || bytes < act + 512) return false;
+  const size_t half = ((bytes - act) / 2) & ~size_t(255);
+  char* b = reinterpret_cast<char*>(base);
+  c->gpart = reinterpret_cast<int32_t*>(b);
+  c->ypart = reinterpret_cast<int32_t*>(b + half);
+  char* q = b + 2 * half;
+  c->xq = reinterpret_cast<uint32_t*>(q);
+  q += qal256((size_t)a.H * np);
+  c->hq = reinterpret_cast<uint32_t*>(q);
+  q += qal256((size_t)a.I * np);
+  c->sx = reinterpret_cast<float*>(q);
+  q += qal256((size_t)4 * n);
+  c->sh = reinterpret_cast<float*>(q);
+  c->npad = np;
+  c->jg = (int)std::min<size_t>(q_jcap(n, 2 * a.I), half / ((size_t)n * 2 * a.I * 4));
+  c->jd = (int)std::min<size_t>(q_jcap(n, a.H), half / ((size_t)n * a.H * 4));
+  return c->jg >= 2 && c->jd >= 2;
+}
+
+static bool q_pass(bool down, const FfnArgs& a, int G, int32_t* part, const uint32_t* act, int npad, int jcap,
+                   QPass* out) {
+  QPass qp{};
+  qp.part = part;
+  qp.act = act;
+  qp.npad = npad;
+  qp.N = down ? a.H : 2 * a.I;
+  qp.K = down ? a.I : a.H;
+  if (qp.N % 128 || qp.K % kQK || qp.N / 4 > kQMaxConsumers) return false;
+  qp.NSR = qp.K / kQK;
+  qp.wbytes = kQK * qp.N;  // 16 rows x N int8
+  qp.stride = qp.wbytes + 256;
+  qp.nst = std::min(kQMaxStages, kQRing / qp.stride);
+  if (qp.nst < 2) return false;
+  qp.G = G;
+  qp.jcap = jcap;
+  qp.qslab = q8_slab_bytes_h(a.H, a.I);
+  *out = qp;
+  return jcap >= 2;
+}
+
+static size_t q_smem(const QPass& qp) { return 128 + (size_t)qp.nst * qp.stride + 2 * kQMaxStages * 8; }
+
+template <typename K, typename... Args>
+static cudaError_t q_launch(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+int launch_ffn_q8(const FfnArgs& a, void* ws, size_t ws_bytes, int max_list, cudaStream_t stream, Prof* prof) {
+  if (max_list <= 0) return MOE_OK;
+  const int n = a.T * a.k;
+  if (n > kQMaxRows || !a.pool_only || a.S <= 0 || a.H % 16 || a.I % 16 || a.I / 4 > 4 * kQRowThreads)
+    return MOE_ERR_ARG;
+  if ((uintptr_t)a.pool % 16 || (uintptr_t)a.y % 16 || (uintptr_t)ws % 256) return MOE_ERR_ALIGN;
+  int dev = 0, sms = 0;
+  MOE_CUDA_TRY(cudaGetDevice(&dev));
+  MOE_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  QCarve c;
+  if (!q_carve(a, ws, ws_bytes, &c)) return MOE_ERR_ALIGN;
+  QPass g, d;
+  if (!q_pass(false, a, sms, c.gpart, c.xq, c.npad, c.jg, &g) || !q_pass(true, a, sms, c.ypart, c.hq, c.npad, c.jd, &d))
+    return MOE_ERR_ARG;
+  static bool done_g[64] = {}, done_d[64] = {};
+  constexpr int kSmemMax = 128 + kQRing + 2 * kQMaxStages * 8;
+  MOE_CUDA_TRY(ensure_smem(ffn_q8_kernel<false>, kSmemMax, done_g));
+  MOE_CUDA_TRY(ensure_smem(ffn_q8_kernel<true>, kSmemMax, done_d));
+  if (prof) prof->begin(MOE_PROF_FFN_GATEUP, stream);
+  q8_rows_kernel<<<n, kQRowThreads, 0, stream>>>(a.x, a.rows, n, a.H, a.k, c.npad, c.xq, c.sx);
+  MOE_LAUNCH_CHECK();
+  MOE_CUDA_TRY(q_launch(ffn_q8_kernel<false>, dim3(sms), dim3(g.N / 4 + 32), q_smem(g), stream, true, a, g));
+  MOE_CUDA_TRY(q_launch(q8_reduce_gu_kernel, dim3(max_list), dim3(kQRowThreads), 0, stream, true, a,
+                        (const int32_t*)c.gpart, g.NSR, g.G, g.jcap, g.qslab, (const float*)c.sx, c.npad, c.hq, c.sh));
+  if (prof) prof->end(stream);
+  if (prof) prof->begin(MOE_PROF_FFN_DOWN, stream);
+  MOE_CUDA_TRY(q_launch(ffn_q8_kernel<true>, dim3(sms), dim3(d.N / 4 + 32), q_smem(d), stream, true, a, d));
+  MOE_CUDA_TRY(q_launch(q8_reduce_d_kernel, dim3((a.H / 4 + 31) / 32, max_list), dim3(256), 0, stream, true, a,
+                        (const int32_t*)c.ypart, d.NSR, d.G, d.jcap, d.qslab, (const float*)c.sh, a.y));
+  if (prof) prof->end(stream);
+  return MOE_OK;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" size_t moe_q8_slab_bytes(int H, int I) {
+  if (H < 1 || I < 1) return 0;
+  return q8_slab_bytes_h(H, I);
+}
+
+extern "C" int moe_quantize_slabs(const void* src, int n_experts, int H, int I, void* dst, moe_stream_t stream) {
+  if (!src || !dst || n_experts < 1 || H < 16 || I < 16 || H % 16 || I % 16) return MOE_ERR_ARG;
+  if ((uintptr_t)src % 16 || (uintptr_t)dst % 16) return MOE_ERR_ALIGN;
+  const int nmax = std::max(H, I);
+  const dim3 grid((nmax + 127) / 128, 3, n_experts);
+  quantize_slabs_kernel<<<grid, 128, 0, (cudaStream_t)stream>>>((const uint16_t*)src, H, I, (uint8_t*)dst);
+  MOE_LAUNCH_CHECK();
+  return MOE_OK;
+}
+
+extern "C" size_t moe_ffn_q8_workspace_bytes(int T, int H, int k, int I) {
+  if (T < 1 || H < 1 || k < 1 || I < 1) return 0;
+  return q8_ws_bytes(T * k, H, I);
+}
+
+extern "C" int moe_expert_ffn_q8(const void* x, int T, int H, int I, int k, int E, const int32_t* offset,
+                                 const int32_t* rows, const int32_t* list_e, const int32_t* n_list, int max_list,
+                                 const void* pool_q, int S, const int32_t* e2s, float* y, void* workspace,
+                                 size_t workspace_bytes, int32_t* dev_status, moe_stream_t stream) {
+  if (!x || !offset || !rows || !list_e || !n_list || !pool_q || !y || !workspace) return MOE_ERR_ARG;
+  if (T < 1 || k < 1 || E < k || H < 16 || I < 16 || max_list < 0 || S < 1 || (!e2s && S < E)) return MOE_ERR_ARG;
+  FfnArgs a{(const uint16_t*)x, T, H, I, k, E, offset, rows, list_e, n_list, (const uint16_t*)pool_q, e2s,
+            nullptr, 0, nullptr, y, dev_status, S, 1};
+  return launch_ffn_q8(a, workspace, workspace_bytes, std::min(max_list, E), (cudaStream_t)stream, nullptr);
+}

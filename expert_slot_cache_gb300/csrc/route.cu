@@ -8,6 +8,7 @@
 #include <math.h>
 
 #include "common.cuh"
+#include "fp32def.cuh"
 
 namespace moe {
 
@@ -344,33 +345,8 @@ __global__ void __launch_bounds__(kTileThreads) logits_tile_kernel(const uint16_
   }
 }
 
-// fp32 exp defined operation by operation, so that a score built on it is
-// reproducible bit for bit off the GPU: Cody and Waite's reduction
-// n = rint(x log2 e), r = (x - n LN2_HI) - n LN2_LO (n LN2_HI exact), the
-// degree-7 Taylor polynomial of e^r in Horner form, times 2^n.  Every step is
-// one IEEE fp32 multiply, add or subtract (the _rn intrinsics keep the
-// compiler from fusing them).  +inf above 88, 0 below -80 (2^n stays normal
-// in between).
-__device__ __forceinline__ float exp32_def(float x) {
-  if (x > 88.f) return INFINITY;
-  if (x < -80.f) return 0.f;
-  const float n = rintf(__fmul_rn(x, 0x1.715476p+0f));
-  float r = __fsub_rn(x, __fmul_rn(n, 0x1.63p-1f));
-  r = __fsub_rn(r, __fmul_rn(n, -0x1.bd0106p-13f));
-  float p = 0x1.a01a02p-13f;
-  p = __fadd_rn(__fmul_rn(p, r), 0x1.6c16c2p-10f);
-  p = __fadd_rn(__fmul_rn(p, r), 0x1.111112p-7f);
-  p = __fadd_rn(__fmul_rn(p, r), 0x1.555556p-5f);
-  p = __fadd_rn(__fmul_rn(p, r), 0x1.555556p-3f);
-  p = __fadd_rn(__fmul_rn(p, r), 0x1p-1f);
-  p = __fadd_rn(__fmul_rn(p, r), 1.f);
-  p = __fadd_rn(__fmul_rn(p, r), 1.f);
-  return __fmul_rn(p, __int_as_float(((int)n + 127) << 23));
-}
-
 // Sigmoid router score ("Nudge, don't cut", "The same idea on GLM-5.3-Flash":
-// the bias is added after the sigmoid): 1 / (1 + exp32(-l)), IEEE add and divide.
-__device__ __forceinline__ float sigmoid32_def(float l) { return __fdiv_rn(1.f, __fadd_rn(1.f, exp32_def(-l))); }
+// the bias is added after the sigmoid): sigmoid32_def (fp32def.cuh).
 
 // ---------------------------------------------------------------------------
 // Top-k: one warp per token.  k rounds of a warp-wide argmax over

@@ -355,6 +355,42 @@ int moe_cache_count(const int32_t* ids, int n, int E, int32_t* counts, int32_t* 
 int moe_cache_repick(int32_t* counts, int E, int S, int32_t* e2s, int32_t* s2e, int32_t* miss_e, int32_t* miss_s,
                      int32_t* n_miss, moe_stream_t stream);
 
+/*
+ * W8A8 experts (8-bit weights and activations).
+ * Source: "Porting vllm-expert-cache to NVIDIA GPUs": the measured model is
+ * Qwen3-30B-A3B W8A8, and weights and their scales are indexed by the same
+ * id, so both must be slot-indexed (section on traps in a new backend).
+ *
+ * Quantised slab, moe_q8_slab_bytes(H, I) = 3HI + 4(2I + H) bytes:
+ *   Wg, Wu [H][I] and Wd [I][H] as int8, each column's 4 consecutive input
+ *   rows packed into one 32-bit word (byte (k, n) at ((k/4)*N + n)*4 + k%4),
+ *   then the fp32 scales sg[I], su[I], sd[H].  The scales travel with the
+ *   weights: manage and gather (slab_bytes = moe_q8_slab_bytes) keep them in
+ *   the same slot.
+ * Codes: symmetric, scale = amax / 127, code = rint(v / scale) clamped to
+ * [-127, 127] (a zero amax gives scale 0 and code 0), fp32 one operation at a
+ * time.  Weights per output column; activations per routing row: x before
+ * gate/up, h before down.  Dot products are exact int32 sums;
+ * g = (float(acc) * sg[n]) * sx[row] (likewise u and y), h = silu(g) * u with
+ * silu(g) = g / (1 + e(-g)) and e() the fp32 exp of moe_route_ex; so h's codes
+ * and y are reproducible bit for bit.
+ *
+ * moe_quantize_slabs: src device bf16 [n_experts][3HI] (the slab layout of
+ * moe_expert_ffn) -> dst device [n_experts][moe_q8_slab_bytes] (caller-owned).
+ * moe_expert_ffn_q8: as moe_expert_ffn with a pool of quantised slabs (every
+ * listed expert in a slot; no host pass); workspace of
+ * moe_ffn_q8_workspace_bytes(T, H, k, I) bytes, 256-byte aligned; T*k <= 4096.
+ * Errors: MOE_ERR_ARG on NULL pointers, H or I not a multiple of 16, too many
+ * rows; MOE_ERR_ALIGN for unaligned pointers or a small workspace.
+ */
+size_t moe_q8_slab_bytes(int H, int I);
+int moe_quantize_slabs(const void* src, int n_experts, int H, int I, void* dst, moe_stream_t stream);
+size_t moe_ffn_q8_workspace_bytes(int T, int H, int k, int I);
+int moe_expert_ffn_q8(const void* x, int T, int H, int I, int k, int E, const int32_t* offset, const int32_t* rows,
+                      const int32_t* list_e, const int32_t* n_list, int max_list, const void* pool_q, int S,
+                      const int32_t* e2s, float* y, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                      moe_stream_t stream);
+
 /* Arguments of moe_layer_forward.  Field meanings as in the calls above. */
 typedef struct moe_layer_args {
   int32_t T, H, E, k, I, S;
@@ -383,6 +419,7 @@ typedef struct moe_layer_args {
   float affinity;            /* live-cache affinity lambda (0 = off); uses e2s before this step's manage */
   int32_t route_flags;       /* moe_route_ex flags (0 = softmax router, selection-only bias) */
   int32_t* window_counts;    /* device int32 [E] or NULL: each chunk's routings are added (moe_cache_count) */
+  int32_t quant;             /* 0: bf16 slabs; 1: W8A8 slabs (moe_quantize_slabs), RESIDENT or GATHER mode */
 } moe_layer_args;
 
 /*
