@@ -32,8 +32,7 @@ namespace moe {
 
 constexpr int kQK = 16;                 // input rows per stage (4 quads)
 constexpr int kQRB = 8;                 // tokens per pass over the weights
-constexpr int kQActTok = kQRB + 4;      // tokens copied per quad (aligned start: p0 rounded down to 4)
-constexpr int kQActBytes = 4 * kQActTok * 4;  // 4 quads x 12 tokens x int32
+constexpr int kQActBytes = kQRB * 16;   // a batch's codes for one stage: 8 tokens x 16 rows
 constexpr int kQRing = 200 * 1024;
 constexpr int kQMaxStages = 8;
 constexpr int kQMaxConsumers = 512;
@@ -76,8 +75,15 @@ __global__ void __launch_bounds__(128) quantize_slabs_kernel(const uint16_t* __r
 }
 
 // ---------------------------------------------------------------------------
-// Activation quantisation: x rows of the grouped positions -> codes, quad-major
-// xq[(h/4)][npad] (int32 = 4 codes), scale sx[p].  One CTA per position.
+// Activation codes are stored stage-major: the 16 codes of position p for
+// input rows 16s .. 16s+15 are the 16 bytes at ((s * npad) + p) * 16, so one
+// copy of 8 x 16 bytes brings a stage's codes for a whole token batch.
+__device__ __forceinline__ size_t q8_act_word(int q, int p, int npad) {  // int32 index of quad q of position p
+  return ((size_t)(q >> 2) * npad + p) * 4 + (q & 3);
+}
+
+// Activation quantisation: x rows of the grouped positions -> codes (stage-major),
+// scale sx[p].  One CTA per position.
 // ---------------------------------------------------------------------------
 constexpr int kQRowThreads = 256;
 
@@ -109,7 +115,7 @@ __global__ void __launch_bounds__(kQRowThreads) q8_rows_kernel(const uint16_t* _
     uint32_t pk = 0;
 #pragma unroll
     for (int b = 0; b < 4; ++b) pk |= (uint32_t)(q8_code(bf16_to_f32(xr[4 * q + b]), s) & 0xff) << (8 * b);
-    xq[(size_t)q * npad + p] = pk;
+    xq[q8_act_word(q, p, npad)] = pk;
   }
   if (threadIdx.x == 0) sx[p] = s;
 }
@@ -119,7 +125,8 @@ __global__ void __launch_bounds__(kQRowThreads) q8_rows_kernel(const uint16_t* _
 // ---------------------------------------------------------------------------
 struct QPass {
   int32_t* part;     // [jcap][n][N]
-  const uint32_t* act;  // quad-major codes [K/4][npad] of the pass's input rows
+  int32_t* vpre;     // batches before each list index (written by the pass's CTA 0 for its reduce)
+  const uint32_t* act;  // stage-major codes of the pass's input rows (q8_act_word)
   int npad;
   int N, K, NSR, nst, wbytes, stride, G, jcap;
   size_t qslab;      // bytes of one quantised slab
@@ -149,7 +156,6 @@ __device__ __forceinline__ void q8_consume(const QPass& qp, int n, const StreamS
     off = 4 * c < I ? 16 * c : kQK * I + 16 * c - 4 * I;  // Wu rows follow the stage's Wg rows
     qstride = 4 * I;
   }
-  const int ao = g.p0 & 3;  // token r of the batch sits at index ao + r of each quad's copy
   for (int s = g.s_lo; s < g.s_hi; ++s, ++it) {
     const int sl = it % qp.nst;
     if (!*abort_flag && !mbar_wait(&full[sl], (it / qp.nst) & 1u)) {
@@ -163,7 +169,7 @@ __device__ __forceinline__ void q8_consume(const QPass& qp, int n, const StreamS
       const int4 w = *reinterpret_cast<const int4*>(st + off + qq * qstride);
 #pragma unroll
       for (int r = 0; r < RB; ++r) {
-        const int xa = act[qq * kQActTok + ao + r];
+        const int xa = act[r * 4 + qq];
         acc[r][0] = __dp4a(w.x, xa, acc[r][0]);
         acc[r][1] = __dp4a(w.y, xa, acc[r][1]);
         acc[r][2] = __dp4a(w.z, xa, acc[r][2]);
@@ -188,13 +194,19 @@ __global__ void __launch_bounds__(kQMaxConsumers + 32, 1) ffn_q8_kernel(const Ff
   uint64_t* full = reinterpret_cast<uint64_t*>(ring + qp.nst * qp.stride);
   uint64_t* empty = full + kQMaxStages;
   __shared__ int s_abort;
+  __shared__ int s_vpre[kMaxE + 1];
+  __shared__ int s_tmp[33];
   const int nc = qp.N / 4;
   const int tid = threadIdx.x;
   pdl_trigger();
-  const int n_list = *a.n_list;
+  const int n_list = min(*a.n_list, kMaxE);
   const int n = a.T * a.k;
-  const int L = n_list > 0 ? stream_len(n_list, qp.NSR, qp.G, qp.jcap) : 1;
-  const int total = n_list * qp.NSR;
+  stream_batch_prefix<kQRB>(a, n_list, s_vpre, s_tmp);
+  const int nbat = s_vpre[n_list];
+  if (blockIdx.x == 0)
+    for (int i = tid; i <= n_list; i += blockDim.x) qp.vpre[i] = s_vpre[i];
+  const int L = nbat > 0 ? stream_len(nbat, qp.NSR, qp.G, qp.jcap) : 1;
+  const int total = nbat * qp.NSR;
   const int beg = blockIdx.x * L, end = min(beg + L, total);
   if (beg >= end) {
     pdl_wait();
@@ -219,10 +231,7 @@ __global__ void __launch_bounds__(kQMaxConsumers + 32, 1) ffn_q8_kernel(const Ff
     int ndef = 0, d_q0[kQMaxStages], d_p0[kQMaxStages], last_use[kQMaxStages];
     for (int s = 0; s < kQMaxStages; ++s) last_use[s] = -1;
     auto issue_act = [&](int sl, int q0, int p0) {
-      unsigned char* dst = ring + sl * qp.stride + qp.wbytes;
-      const uint32_t* src = qp.act + (size_t)q0 * qp.npad + (p0 & ~3);
-      for (int qq = 0; qq < 4; ++qq)
-        q8_bulk(dst + qq * kQActTok * 4, src + (size_t)qq * qp.npad, kQActTok * 4, &full[sl]);
+      q8_bulk(ring + sl * qp.stride + qp.wbytes, qp.act + q8_act_word(q0, p0, qp.npad), kQActBytes, &full[sl]);
     };
     auto flush = [&]() {
       pdl_wait();
@@ -231,7 +240,7 @@ __global__ void __launch_bounds__(kQMaxConsumers + 32, 1) ffn_q8_kernel(const Ff
       ndef = 0;
       waited = true;
     };
-    stream_segments<kQRB>(a, qp.NSR, L, beg, end, [&](const StreamSeg& g) {
+    stream_segments_batched<kQRB>(a, s_vpre, n_list, qp.NSR, L, beg, end, [&](const StreamSeg& g) {
       const unsigned char* w = reinterpret_cast<const unsigned char*>(a.pool) + (size_t)g.slot * qp.qslab;
       for (int s = g.s_lo; s < g.s_hi; ++s, ++it) {
         const int sl = it % qp.nst;
@@ -272,7 +281,7 @@ __global__ void __launch_bounds__(kQMaxConsumers + 32, 1) ffn_q8_kernel(const Ff
         if (last_use[s] >= 0) mbar_wait(&full[s], (uint32_t)last_use[s] & 1u);
   } else if (tid < nc) {
     uint32_t it = 0;
-    stream_segments<kQRB>(a, qp.NSR, L, beg, end, [&](const StreamSeg& g) {
+    stream_segments_batched<kQRB>(a, s_vpre, n_list, qp.NSR, L, beg, end, [&](const StreamSeg& g) {
       if (g.nb <= 1)
         q8_consume<DOWN, 1>(qp, n, g, ring, full, empty, it, abort_flag, a.status, a.I);
       else if (g.nb <= 2)
@@ -284,11 +293,10 @@ __global__ void __launch_bounds__(kQMaxConsumers + 32, 1) ffn_q8_kernel(const Ff
       return true;
     });
   }
-  if (tid == 0)
-    for (int li = beg / qp.NSR; li * qp.NSR < end; ++li) {
-      int e, slot;
-      if (!stream_slot(a, li, e, slot)) set_status(a.status, e < 0 || e >= a.E ? MOE_DEV_BAD_EXPERT : MOE_DEV_BAD_SLOT);
-    }
+  if (blockIdx.x == 0 && tid < n_list) {
+    int e, slot;
+    if (!stream_slot(a, tid, e, slot)) set_status(a.status, e < 0 || e >= a.E ? MOE_DEV_BAD_EXPERT : MOE_DEV_BAD_SLOT);
+  }
   __syncwarp();
   __syncthreads();
 }
@@ -299,6 +307,7 @@ __global__ void __launch_bounds__(kQMaxConsumers + 32, 1) ffn_q8_kernel(const Ff
 // gate/up: one CTA per listed expert; per row p: g, u (dequantised), h =
 // silu(g)*u, amax over the row, codes of h into hq (quad-major), sh[p].
 __global__ void __launch_bounds__(kQRowThreads) q8_reduce_gu_kernel(const FfnArgs a, const int32_t* __restrict__ part,
+                                                                    const int32_t* __restrict__ vpre,
                                                                     int NSR, int G, int jcap, size_t qslab,
                                                                     const float* __restrict__ sx, int npad,
                                                                     uint32_t* __restrict__ hq,
@@ -311,8 +320,9 @@ __global__ void __launch_bounds__(kQRowThreads) q8_reduce_gu_kernel(const FfnArg
   const bool ok = li < n_list && stream_slot(a, li, e, slot);
   pdl_wait();
   if (!ok) return;
-  const int L = stream_len(n_list, NSR, G, jcap);
-  const int J = stream_parts(li, NSR, L);
+  const int nl = min(n_list, kMaxE);
+  const int L = stream_len(vpre[nl], NSR, G, jcap);  // vpre: written by the pass before (completed)
+  const int v0 = vpre[li];
   const int n = a.T * a.k, I = a.I, N = 2 * I;
   const size_t mat = (size_t)a.H * I;
   const float* sc = reinterpret_cast<const float*>(reinterpret_cast<const unsigned char*>(a.pool) +
@@ -322,6 +332,7 @@ __global__ void __launch_bounds__(kQRowThreads) q8_reduce_gu_kernel(const FfnArg
   const size_t pstride = (size_t)n * N;
   const int pb = a.offset[e], pe = a.offset[e + 1];
   for (int p = pb; p < pe; ++p) {
+    const int J = stream_parts(v0 + (p - pb) / kQRB, NSR, L);
     const float s_x = sx[p];
     float hv[4][4];  // up to 4 quads per thread (I <= 16 * blockDim)
     float amax = 0.f;
@@ -352,14 +363,15 @@ __global__ void __launch_bounds__(kQRowThreads) q8_reduce_gu_kernel(const FfnArg
       uint32_t pk = 0;
 #pragma unroll
       for (int b = 0; b < 4; ++b) pk |= (uint32_t)(q8_code(hv[nq][b], s) & 0xff) << (8 * b);
-      hq[(size_t)q * npad + p] = pk;
+      hq[q8_act_word(q, p, npad)] = pk;
     }
     if (threadIdx.x == 0) sh[p] = s;
   }
 }
 
 // down: y[p][n] = (float(sum of parts) * sd[n]) * sh[p]; block = 128 columns of one listed expert.
-__global__ void __launch_bounds__(256) q8_reduce_d_kernel(const FfnArgs a, const int32_t* __restrict__ part, int NSR,
+__global__ void __launch_bounds__(256) q8_reduce_d_kernel(const FfnArgs a, const int32_t* __restrict__ part,
+                                                          const int32_t* __restrict__ vpre, int NSR,
                                                           int G, int jcap, size_t qslab,
                                                           const float* __restrict__ sh, float* __restrict__ y) {
   __shared__ int4 sp[8][32];
@@ -370,8 +382,9 @@ __global__ void __launch_bounds__(256) q8_reduce_d_kernel(const FfnArgs a, const
   const bool ok = li < n_list && stream_slot(a, li, e, slot);
   pdl_wait();
   if (!ok) return;
-  const int L = stream_len(n_list, NSR, G, jcap);
-  const int J = stream_parts(li, NSR, L);
+  const int nl = min(n_list, kMaxE);
+  const int L = stream_len(vpre[nl], NSR, G, jcap);
+  const int v0 = vpre[li];
   const int n = a.T * a.k, H = a.H;
   const float* sd = reinterpret_cast<const float*>(reinterpret_cast<const unsigned char*>(a.pool) +
                                                    (size_t)slot * qslab + (size_t)3 * H * a.I + (size_t)8 * a.I);
@@ -380,6 +393,7 @@ __global__ void __launch_bounds__(256) q8_reduce_d_kernel(const FfnArgs a, const
   const size_t pstride = (size_t)n * H;
   const int pb = a.offset[e], pe = a.offset[e + 1];
   for (int p = pb; p < pe; ++p) {
+    const int J = stream_parts(v0 + (p - pb) / kQRB, NSR, L);
     int4 acc = make_int4(0, 0, 0, 0);
     if (4 * c4 < H)
       for (int jj = w; jj < J; jj += 8) {
@@ -413,7 +427,7 @@ static int q_jcap(int n, int N) {
   return (int)std::max<size_t>(3, std::min<size_t>(j, kQJcapMax));
 }
 
-static int q_npad(int n) { return ((n + kQActTok + 3) / 4) * 4; }
+static int q_npad(int n) { return n + kQRB; }  // a batch copy may run RB positions past the last one
 
 // Layout: [gate/up parts | down parts] (equal halves, int32), xq [H/4][npad],
 // hq [I/4][npad] (int32 quads), sx [n], sh [n] (fp32).
@@ -421,20 +435,23 @@ size_t q8_ws_bytes(int n, int H, int I) {
   if (n < 1 || n > kQMaxRows) return 0;
   const size_t half = qal256(std::max((size_t)q_jcap(n, 2 * I) * n * 2 * I * 4, (size_t)q_jcap(n, H) * n * H * 4));
   const int np = q_npad(n);
-  return 2 * half + qal256((size_t)H * np) + qal256((size_t)I * np) + 2 * qal256((size_t)4 * n);
+  return 2 * half + qal256((size_t)H * np) + qal256((size_t)I * np) + 2 * qal256((size_t)4 * n) +
+         2 * qal256((size_t)4 * (kMaxE + 1));
 }
 
 struct QCarve {
   int32_t *gpart, *ypart;
   uint32_t *xq, *hq;
   float *sx, *sh;
+  int32_t *vpre_g, *vpre_d;
   int jg, jd, npad;
 };
 
 static bool q_carve(const FfnArgs& a, void* base, size_t bytes, QCarve* c) {
   const int n = a.T * a.k;
   const int np = q_npad(n);
-  const size_t act = qal256((size_t)a.H * np) + qal256((size_t)a.I * np) + 2 * qal256((size_t)4 * n);
+  const size_t act = qal256((size_t)a.H * np) + qal256((size_t)a.I * np) + 2 * qal256((size_t)4 * n) +
+                     2 * qal256((size_t)4 * (kMaxE + 1));
   if (!base || bytes < act + 512) return false;
   const size_t half = ((bytes - act) / 2) & ~size_t(255);
   char* b = reinterpret_cast<char*>(base);
@@ -448,16 +465,21 @@ static bool q_carve(const FfnArgs& a, void* base, size_t bytes, QCarve* c) {
   c->sx = reinterpret_cast<float*>(q);
   q += qal256((size_t)4 * n);
   c->sh = reinterpret_cast<float*>(q);
+  q += qal256((size_t)4 * n);
+  c->vpre_g = reinterpret_cast<int32_t*>(q);
+  q += qal256((size_t)4 * (kMaxE + 1));
+  c->vpre_d = reinterpret_cast<int32_t*>(q);
   c->npad = np;
   c->jg = (int)std::min<size_t>(q_jcap(n, 2 * a.I), half / ((size_t)n * 2 * a.I * 4));
   c->jd = (int)std::min<size_t>(q_jcap(n, a.H), half / ((size_t)n * a.H * 4));
   return c->jg >= 2 && c->jd >= 2;
 }
 
-static bool q_pass(bool down, const FfnArgs& a, int G, int32_t* part, const uint32_t* act, int npad, int jcap,
-                   QPass* out) {
+static bool q_pass(bool down, const FfnArgs& a, int G, int32_t* part, int32_t* vpre, const uint32_t* act, int npad,
+                   int jcap, QPass* out) {
   QPass qp{};
   qp.part = part;
+  qp.vpre = vpre;
   qp.act = act;
   qp.npad = npad;
   qp.N = down ? a.H : 2 * a.I;
@@ -465,7 +487,7 @@ static bool q_pass(bool down, const FfnArgs& a, int G, int32_t* part, const uint
   if (qp.N % 128 || qp.K % kQK || qp.N / 4 > kQMaxConsumers) return false;
   qp.NSR = qp.K / kQK;
   qp.wbytes = kQK * qp.N;  // 16 rows x N int8
-  qp.stride = qp.wbytes + 256;
+  qp.stride = qp.wbytes + 128;
   qp.nst = std::min(kQMaxStages, kQRing / qp.stride);
   if (qp.nst < 2) return false;
   qp.G = G;
@@ -504,7 +526,8 @@ int launch_ffn_q8(const FfnArgs& a, void* ws, size_t ws_bytes, int max_list, cud
   QCarve c;
   if (!q_carve(a, ws, ws_bytes, &c)) return MOE_ERR_ALIGN;
   QPass g, d;
-  if (!q_pass(false, a, sms, c.gpart, c.xq, c.npad, c.jg, &g) || !q_pass(true, a, sms, c.ypart, c.hq, c.npad, c.jd, &d))
+  if (!q_pass(false, a, sms, c.gpart, c.vpre_g, c.xq, c.npad, c.jg, &g) ||
+      !q_pass(true, a, sms, c.ypart, c.vpre_d, c.hq, c.npad, c.jd, &d))
     return MOE_ERR_ARG;
   static bool done_g[64] = {}, done_d[64] = {};
   constexpr int kSmemMax = 128 + kQRing + 2 * kQMaxStages * 8;
@@ -515,12 +538,14 @@ int launch_ffn_q8(const FfnArgs& a, void* ws, size_t ws_bytes, int max_list, cud
   MOE_LAUNCH_CHECK();
   MOE_CUDA_TRY(q_launch(ffn_q8_kernel<false>, dim3(sms), dim3(g.N / 4 + 32), q_smem(g), stream, true, a, g));
   MOE_CUDA_TRY(q_launch(q8_reduce_gu_kernel, dim3(max_list), dim3(kQRowThreads), 0, stream, true, a,
-                        (const int32_t*)c.gpart, g.NSR, g.G, g.jcap, g.qslab, (const float*)c.sx, c.npad, c.hq, c.sh));
+                        (const int32_t*)c.gpart, (const int32_t*)c.vpre_g, g.NSR, g.G, g.jcap, g.qslab,
+                        (const float*)c.sx, c.npad, c.hq, c.sh));
   if (prof) prof->end(stream);
   if (prof) prof->begin(MOE_PROF_FFN_DOWN, stream);
   MOE_CUDA_TRY(q_launch(ffn_q8_kernel<true>, dim3(sms), dim3(d.N / 4 + 32), q_smem(d), stream, true, a, d));
   MOE_CUDA_TRY(q_launch(q8_reduce_d_kernel, dim3((a.H / 4 + 31) / 32, max_list), dim3(256), 0, stream, true, a,
-                        (const int32_t*)c.ypart, d.NSR, d.G, d.jcap, d.qslab, (const float*)c.sh, a.y));
+                        (const int32_t*)c.ypart, (const int32_t*)c.vpre_d, d.NSR, d.G, d.jcap, d.qslab,
+                        (const float*)c.sh, a.y));
   if (prof) prof->end(stream);
   return MOE_OK;
 }
