@@ -14,7 +14,7 @@ import torch
 
 import oracle as O
 from harness import configs as C
-from tests._setup import RL2_Y_BF16_H, HostSlabs, assert_f32_close, assert_out_close, rel_l2, stage_layer
+from tests._setup import ATOL_OUT, RL2_Y_BF16_H, HostSlabs, assert_f32_close, assert_out_close, rel_l2, stage_layer
 
 pytestmark = pytest.mark.gpu
 
@@ -465,6 +465,43 @@ def test_expert_ffn_tensor_core_parity(T, skew):
     for e in used:
         a, b = offset[e], offset[e + 1]
         assert rel_l2(got[a:b], want[a:b]) <= 2 * RL2_Y_BF16_H, f"expert {e} ({b - a} rows)"
+
+
+def test_expert_ffn_tensor_core_tile_edges():
+    """Group sizes on the grouped GEMMs' tile edges: 1 row, N rounding to 16
+    (15, 16, 17), one or two 128-row boxes per tile (127, 128, 129), one or
+    two 256-row tiles (255, 256, 257), several tiles (511 .. 513)."""
+    cfg = C.qwen(560, S=128, mode=C.MODE_RESIDENT)
+    T, E, k = cfg.T, cfg.E, cfg.k
+    edges = [1, 15, 16, 17, 31, 33, 127, 128, 129, 255, 256, 257, 511, 512, 513]
+    rng = np.random.default_rng(11)
+    counts = np.zeros(E, dtype=np.int64)
+    perm = rng.permutation(E)
+    counts[perm[:len(edges)]] = edges
+    rest = perm[len(edges):len(edges) + 60]  # the other experts stay empty
+    left = T * k - counts.sum()
+    counts[rest] = left // len(rest)
+    counts[rest[: left % len(rest)]] += 1
+    assert counts.sum() == T * k and counts.max() <= T
+    # expert-sorted list dealt column-wise: token t takes entries t, T + t, ... (distinct experts, as every run <= T)
+    lst = np.repeat(np.arange(E, dtype=np.int32), counts)
+    ids = np.ascontiguousarray(lst.reshape(k, T).T)
+    assert all(len(set(r)) == k for r in ids)
+    count, offset, rows, pos = O.permute(ids, E)
+    assert np.array_equal(count, counts)
+    x = C.draw_x(cfg, DEV, T=T)
+    st = stage_layer(cfg)
+    used = np.nonzero(count)[0]
+    g = M.permute(torch.from_numpy(ids).to(DEV), E)
+    y = M.expert_ffn(x, k, cfg.I, E, g.offset, g.rows, torch.from_numpy(used.astype(np.int32)).to(DEV),
+                     torch.tensor([len(used)], dtype=torch.int32, device=DEV), len(used), st["slabs_dev"])
+    torch.cuda.synchronize()
+    want = O.expert_ffn(_np(x.float()), rows, offset, k, HostSlabs(st["host"]), cfg.H, cfg.I)
+    got = _np(y)
+    for e in used:
+        a, b = offset[e], offset[e + 1]
+        assert rel_l2(got[a:b], want[a:b]) <= 2 * RL2_Y_BF16_H, f"expert {e} ({b - a} rows)"
+        assert np.abs(got[a:b] - want[a:b]).max() <= ATOL_OUT, f"expert {e} ({b - a} rows)"
 
 
 # ----------------------------------------------------------------------------
