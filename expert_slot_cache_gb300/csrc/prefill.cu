@@ -12,8 +12,8 @@
 // cluster of two on neighbouring SMs): the pair's MMA has M = 256 weight
 // features (128 in each CTA's shared memory and TMEM) and N = up to 256 of
 // one expert's grouped rows, rounded up to a multiple of 32, half of them in
-// each CTA's shared memory.  Each CTA thus loads 32 KB of operands per 64-deep
-// K step for a 128 x 256 x 64 share of the work, two thirds of what a lone
+// each CTA's shared memory.  Each CTA thus loads 64 KB of operands per 128-deep
+// K step for a 128 x 256 x 128 share of the work, two thirds of what a lone
 // CTA needs for the same tile.  Groups are ragged (a skewed router gives
 // 0 .. thousands of rows per expert), and rows on the N side pad a group only
 // to the next 32 rows instead of the next 128 or 256.  In GEMM 1 a CTA's 128
@@ -23,14 +23,17 @@
 // Persistent clusters over the tiles of all experts (expert-major, then
 // token tile, then feature tile, so a token tile stays hot in L2 while the
 // clusters walk the expert's weights); per CTA:
-//   warp 0: TMA producer (one thread), 6-stage ring of 32 KB stages; the
+//   warp 0: TMA producer (one thread), 3-stage ring of 64 KB stages; the
 //           loads of both CTAs complete on rank 0's barrier
 //   warp 1: TMEM allocation (both CTAs) + pair MMA issue (rank 0, one thread)
 //   warps 2-5: epilogue, TMEM -> registers -> shared (transpose) -> global
 // Shared-memory operands use the 128-byte swizzle written by the tensor-map
 // loads: weights MN-major (stored input-major: 64 output columns = 128 B per
-// K row, 8 K rows per 1 KB swizzle atom, 64-column atoms 8 KB apart), tokens
-// K-major (rows of 64 bf16 = 128 B).  Accumulators are fp32 in TMEM, two
+// K row, 8 K rows per 1 KB swizzle group, 64-column atoms 16 KB apart),
+// grouped rows K-major (rows of 64 bf16 = 128 B, the two 64-deep K halves of
+// a stage 16 KB apart).  One thread issues the MMAs, and a tcgen05.mma costs
+// it tens of cycles to issue, so a stage is 128 deep: the barrier wait, fence
+// and commit per stage are spread over eight MMAs.  Accumulators are fp32 in TMEM, two
 // 256-column buffers so the epilogue of one tile overlaps the MMAs of the
 // next.
 #include "internal.cuh"
@@ -41,11 +44,11 @@ namespace moe {
 constexpr int kPM = 128;     // weight features per CTA (the pair's MMA M is 256)
 constexpr int kPT = 256;     // grouped rows per tile, at most (MMA N)
 constexpr int kPTBox = 128;  // grouped rows per CTA and tile, at most (one tensor-map box)
-constexpr int kPK = 64;
-constexpr int kPStages = 6;
-constexpr int kPAbytes = kPM * kPK * 2;            // 16 KB of weights
-constexpr int kPBbytes = kPTBox * kPK * 2;         // 16 KB of rows
-constexpr int kPStageBytes = kPAbytes + kPBbytes;  // 32 KB
+constexpr int kPK = 128;    // K depth of a ring stage: eight 16-deep MMAs per barrier wait and commit
+constexpr int kPStages = 3;
+constexpr int kPAbytes = kPM * kPK * 2;            // 32 KB of weights: two 64-feature atoms, 16 KB apart
+constexpr int kPBbytes = kPTBox * kPK * 2;         // 32 KB of rows: two 64-deep K halves, 16 KB apart
+constexpr int kPStageBytes = kPAbytes + kPBbytes;  // 64 KB
 constexpr int kPThreads = 192;
 constexpr uint32_t kTmemCols = 2 * kPT;
 constexpr int kPBarWords = 32;  // mbarriers: full / empty per stage, two accumulators, done
@@ -172,15 +175,16 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const Prefil
           // rank 0's barrier counts the bytes of both CTAs
           if (rank == 0) mbar_expect_tx(&full[s], 2 * kPStageBytes);
           const uint32_t fb = mapa_shared(smem_u32(&full[s]), 0);
-          // weights: 64 K rows x this CTA's 128 features (two 64-column swizzle atoms, 8 KB apart)
+          // weights: 128 K rows x this CTA's 128 features (two 64-column swizzle atoms, 16 KB apart)
           if (kMode == 0) {
-            tma_load_4d_pair(st, &mapW, fb, 0, kb * kPK, watom, 3 * slot);             // 64 gate columns
-            tma_load_4d_pair(st + 8192, &mapW, fb, 0, kb * kPK, watom, 3 * slot + 1);  // the same 64 up columns
+            tma_load_4d_pair(st, &mapW, fb, 0, kb * kPK, watom, 3 * slot);              // 64 gate columns
+            tma_load_4d_pair(st + 16384, &mapW, fb, 0, kb * kPK, watom, 3 * slot + 1);  // the same 64 up columns
           } else {
             tma_load_4d_pair(st, &mapW, fb, 0, kb * kPK, watom, 3 * slot + 2);
           }
-          // grouped rows: this CTA's half of the tile, one box of 128 rows x 64 K
+          // grouped rows: this CTA's half of the tile, 128 rows x 64 K per box, the stage's two K halves
           tma_load_3d_pair(st + kPAbytes, &mapX, fb, kb * kPK, rrow, 0);
+          tma_load_3d_pair(st + kPAbytes + 16384, &mapX, fb, kb * kPK + 64, rrow, 0);
           last_use[s] = (int)use;
           if (++s == kPStages) {
             s = 0;
@@ -199,7 +203,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const Prefil
       // four MMAs and a commit (stage index and phase advance incrementally, descriptors are a base
       // plus the stage offset)
       const uint32_t sbase = smem_u32(psm);
-      const uint64_t ad0 = smem_desc(sbase, 8192, 1024);             // weights, MN-major
+      const uint64_t ad0 = smem_desc(sbase, 16384, 1024);            // weights, MN-major
       const uint64_t bd0 = smem_desc(sbase + kPAbytes, 16, 1024);    // grouped rows, K-major
       constexpr uint32_t kStageDesc = kPStageBytes >> 4;             // stage stride in descriptor units
       uint32_t s = 0, ph = 0, tc = 0;
@@ -229,7 +233,9 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const Prefil
           tc_fence_after();
           if (!dead) {
             const uint64_t so = (uint64_t)(s * kStageDesc);
+            // K 0..63 from the first K half of the rows, K 64..127 from the second (16 KB further)
             umma_f16_pair_k64(d, ad0 + so, bd0 + so, idesc, kb != 0, 2048 >> 4, 32 >> 4);
+            umma_f16_pair_k64(d, ad0 + so + 4 * (2048 >> 4), bd0 + so + (16384 >> 4), idesc, 1, 2048 >> 4, 32 >> 4);
           }
           umma_commit_pair(&empty[s]);  // frees stage s in both CTAs
           if (++s == kPStages) {
@@ -384,7 +390,7 @@ static size_t prefill_smem_bytes() {
 }
 
 bool prefill_eligible(const FfnArgs& a, int n) {
-  return a.pool_only && a.S > 0 && a.xp && a.hb && n >= kPrefillMinRows && a.H % (2 * kPM) == 0 && a.I % 128 == 0 &&
+  return a.pool_only && a.S > 0 && a.xp && a.hb && n >= kPrefillMinRows && a.H % (2 * kPM) == 0 && a.I % 128 == 0 && a.H % kPK == 0 && a.I % kPK == 0 &&
          a.E <= kMaxE;
 }
 
@@ -405,13 +411,13 @@ int launch_prefill(const FfnArgs& a, int n, int max_list, cudaStream_t stream, P
   {
     const uint64_t d[3] = {(uint64_t)a.H, (uint64_t)n, 1};
     const uint64_t s[2] = {(uint64_t)a.H * 2, (uint64_t)n * a.H * 2};
-    const uint32_t b[3] = {kPK, kPTBox, 1};
+    const uint32_t b[3] = {64, kPTBox, 1};  // 64 K = one 128-byte swizzle row
     if (encode_tmap_3d_bf16(&mx, a.xp, d, s, b, CU_TENSOR_MAP_SWIZZLE_128B) != MOE_OK) return MOE_ERR_CUDA;
   }
   {
     const uint64_t d[3] = {(uint64_t)a.I, (uint64_t)n, 1};
     const uint64_t s[2] = {(uint64_t)a.I * 2, (uint64_t)n * a.I * 2};
-    const uint32_t b[3] = {kPK, kPTBox, 1};
+    const uint32_t b[3] = {64, kPTBox, 1};
     if (encode_tmap_3d_bf16(&mh, a.hb, d, s, b, CU_TENSOR_MAP_SWIZZLE_128B) != MOE_OK) return MOE_ERR_CUDA;
   }
   // weight matrices viewed as [matrix][64-column atom][K row][64 columns]
