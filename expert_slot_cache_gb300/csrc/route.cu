@@ -345,14 +345,153 @@ __global__ void __launch_bounds__(kTileThreads) logits_tile_kernel(const uint16_
   }
 }
 
+// logits_full_kernel (many tokens): CTA = 64 tokens x 64 experts over all of
+// H, 128 threads, writing the final logits (no block parts in global memory).
+// Each 128-row block's bf16 tiles are copied with cp.async while the block
+// before is computed (two staging buffers), converted to fp32 in shared memory
+// (x token-minor, Wr expert-minor), then thread (tx, ty) runs, for experts
+// 4tx..4tx+3 and tokens 4ty..4ty+3, one fma chain per logit over the block's
+// rows in order from 0 (packed fp32 pairs along the tokens; the next row's
+// operands are loaded while the current row's 8 packed fmas issue) and adds
+// each chain to the logit's running sum in block order: the same arithmetic,
+// in the same order, as the block parts summed by topk_kernel.  One CTA per
+// SM (128 of them fill the GPU at T = 4096, E = 128) with 8 warps, two per SM
+// sub-partition, so that one warp's shared-memory and fma latencies overlap
+// the other's.
+constexpr int kFullThreads = 256;
+constexpr int kFullXRow = kHC + 8;  // bf16 staging row of x, padded against bank conflicts in the conversion
+constexpr int kFullStage = kTT * kFullXRow + kHC * kTE;  // bf16 elements per staging buffer
+
+size_t logits_full_smem_bytes() {
+  return (size_t)(kHC * kTT + kHC * kTE) * sizeof(float) + 2 * (size_t)kFullStage * 2;
+}
+
+__global__ void __launch_bounds__(kFullThreads) logits_full_kernel(const uint16_t* __restrict__ x,
+                                                                  const uint16_t* __restrict__ wr,
+                                                                  const float* __restrict__ off, int T, int H,
+                                                                  int E, float* __restrict__ logits) {
+  extern __shared__ __align__(16) float fsm[];
+  float* xf = fsm;                                                           // [kHC][kTT]
+  float* wf = fsm + kHC * kTT;                                               // [kHC][kTE]
+  uint16_t* stg = reinterpret_cast<uint16_t*>(fsm + kHC * kTT + kHC * kTE);  // 2 x (x [kTT][kFullXRow] | Wr [kHC][kTE])
+  const int tid = threadIdx.x;
+  const int t0 = blockIdx.x * kTT, e0 = blockIdx.y * kTE;
+  const int nblk = (H + kHC - 1) / kHC;
+  auto issue = [&](int b, int st) {
+    uint16_t* sx = stg + st * kFullStage;
+    uint16_t* sw = sx + kTT * kFullXRow;
+    const int h0 = b * kHC, hn = min(kHC, H - h0);
+    for (int v = tid; v < kTT * (kHC / 8); v += kFullThreads) {
+      const int r = v / (kHC / 8), q = v % (kHC / 8);
+      const bool ok = t0 + r < T && 8 * q < hn;
+      cp_async16(sx + r * kFullXRow + 8 * q, ok ? x + (size_t)(t0 + r) * H + h0 + 8 * q : x, ok);
+    }
+    for (int v = tid; v < kHC * (kTE / 8); v += kFullThreads) {
+      const int r = v / (kTE / 8), q = v % (kTE / 8);
+      const bool ok = r < hn && e0 + 8 * q < E;
+      cp_async16(sw + r * kTE + 8 * q, ok ? wr + (size_t)(h0 + r) * E + e0 + 8 * q : wr, ok);
+    }
+  };
+  issue(0, 0);
+  cp_async_commit();
+  if (nblk > 1) issue(1, 1);
+  cp_async_commit();
+  const int tx = tid & 15, ty = tid >> 4;
+  float total[4][4];  // [expert 4tx + i][token 4ty + t]
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int t = 0; t < 4; ++t) total[i][t] = 0.f;
+  for (int b = 0; b < nblk; ++b) {
+    cp_async_wait<1>();  // block b has landed (block b + 1 may still be in flight)
+    __syncthreads();     // ... for every thread's copies; and block b - 1's chains are done with xf / wf
+    const uint16_t* sx = stg + (b & 1) * kFullStage;
+    const uint16_t* sw = sx + kTT * kFullXRow;
+    const int hn = min(kHC, H - b * kHC);  // a multiple of 8
+    // x: chunk v = (token r, 8 rows q), lanes on consecutive tokens (conflict-free transposed stores)
+    for (int v = tid; v < kTT * (kHC / 8); v += kFullThreads) {
+      const int r = v % kTT, q = v / kTT;
+      const uint4 u = *reinterpret_cast<const uint4*>(sx + r * kFullXRow + 8 * q);
+      float* d = xf + (8 * q) * kTT + r;
+      d[0 * kTT] = bf16_lo(u.x);
+      d[1 * kTT] = bf16_hi(u.x);
+      d[2 * kTT] = bf16_lo(u.y);
+      d[3 * kTT] = bf16_hi(u.y);
+      d[4 * kTT] = bf16_lo(u.z);
+      d[5 * kTT] = bf16_hi(u.z);
+      d[6 * kTT] = bf16_lo(u.w);
+      d[7 * kTT] = bf16_hi(u.w);
+    }
+    // Wr: chunk v = (row r, 8 experts q)
+    for (int v = tid; v < kHC * (kTE / 8); v += kFullThreads) {
+      const int r = v / (kTE / 8), q = v % (kTE / 8);
+      const uint4 u = *reinterpret_cast<const uint4*>(sw + r * kTE + 8 * q);
+      float4* d = reinterpret_cast<float4*>(wf + r * kTE + 8 * q);
+      d[0] = make_float4(bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y));
+      d[1] = make_float4(bf16_lo(u.z), bf16_hi(u.z), bf16_lo(u.w), bf16_hi(u.w));
+    }
+    __syncthreads();  // the fp32 tiles are complete, and staging buffer b & 1 is free again
+    if (b + 2 < nblk) issue(b + 2, b & 1);
+    cp_async_commit();
+    // chains over the block: acc[i][p] holds tokens (4ty + 2p, 4ty + 2p + 1) of expert 4tx + i
+    uint64_t acc[4][2];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[i][0] = acc[i][1] = 0ull;
+    const float* wrow = wf + 4 * tx;
+    const float* xrow = xf + 4 * ty;
+    float4 wv = *reinterpret_cast<const float4*>(wrow);
+    ulonglong2 xa = *reinterpret_cast<const ulonglong2*>(xrow);
+#pragma unroll 4
+    for (int h = 0; h < hn; ++h) {
+      // the next row's operands (row kHC - 1 again after the last row: in bounds, unused)
+      const int hh = min(h + 1, kHC - 1);
+      const float4 wv1 = *reinterpret_cast<const float4*>(wrow + hh * kTE);
+      const ulonglong2 xa1 = *reinterpret_cast<const ulonglong2*>(xrow + hh * kTT);
+      const uint64_t ww[4] = {rf2_pack(wv.x, wv.x), rf2_pack(wv.y, wv.y), rf2_pack(wv.z, wv.z), rf2_pack(wv.w, wv.w)};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        rf2_fma(acc[i][0], xa.x, ww[i]);
+        rf2_fma(acc[i][1], xa.y, ww[i]);
+      }
+      wv = wv1;
+      xa = xa1;
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int p = 0; p < 2; ++p) {
+        const float2 c = rf2_unpack(acc[i][p]);
+        total[i][2 * p] = total[i][2 * p] + c.x;
+        total[i][2 * p + 1] = total[i][2 * p + 1] + c.y;
+      }
+  }
+  cp_async_wait<0>();
+  const int e = e0 + 4 * tx;
+  if (e < E) {  // E % 8 == 0, so all four experts are in range together
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (off) o = make_float4(off[e], off[e + 1], off[e + 2], off[e + 3]);
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const int tt = t0 + 4 * ty + t;
+      if (tt < T) {
+        float4 v = make_float4(total[0][t], total[1][t], total[2][t], total[3][t]);
+        if (off) v = make_float4(v.x + o.x, v.y + o.y, v.z + o.z, v.w + o.w);
+        *reinterpret_cast<float4*>(logits + (size_t)tt * E + e) = v;
+      }
+    }
+  }
+}
+
 // Sigmoid router score ("Nudge, don't cut", "The same idea on GLM-5.3-Flash":
 // the bias is added after the sigmoid): sigmoid32_def (fp32def.cuh).
 
 // ---------------------------------------------------------------------------
 // Top-k: one warp per token.  k rounds of a warp-wide argmax over
 // score = logit + bias (ties -> lower id); the winner is marked taken.
-// Weights: softmax over the k picked, from the unbiased logits.
+// Weights: softmax over the k picked, from the unbiased logits.  NQ = 32-expert
+// slots per lane (E <= 32 * NQ).
 // ---------------------------------------------------------------------------
+template <int NQ>
 __global__ void __launch_bounds__(kRouteThreads) topk_kernel(float* __restrict__ logits,
                                                              const float* __restrict__ bias,
                                                              const int32_t* __restrict__ e2s, float affinity,
@@ -390,9 +529,9 @@ __global__ void __launch_bounds__(kRouteThreads) topk_kernel(float* __restrict__
   if (t >= T) return;
   float* lrow = logits + (size_t)t * E;
   // the token's scores, loaded once: lane holds experts lane + 32q
-  float sc[kMaxE / 32];
+  float sc[NQ];
 #pragma unroll
-  for (int q = 0; q < kMaxE / 32; ++q) {
+  for (int q = 0; q < NQ; ++q) {
     const int e = lane + 32 * q;
     float v = 0.f;
     if (e < E) {
@@ -407,7 +546,7 @@ __global__ void __launch_bounds__(kRouteThreads) topk_kernel(float* __restrict__
     float best = -INFINITY;
     int bi = INT_MAX;
 #pragma unroll
-    for (int q = 0; q < kMaxE / 32; ++q) {
+    for (int q = 0; q < NQ; ++q) {
       const int e = lane + 32 * q;
       if (e >= E || ((taken >> q) & 1u)) continue;
       const float sv = sc[q];
@@ -459,6 +598,21 @@ __global__ void __launch_bounds__(kRouteThreads) topk_kernel(float* __restrict__
   }
 }
 
+// Top-k launch with the fewest 32-expert slots per lane that hold E.
+static void launch_topk(int grid, cudaStream_t s, float* logits, const float* bias, const int32_t* e2s,
+                        float affinity, const float* part, int nb, const float* off, int T, int E, int k, int tpc,
+                        int rflags, int32_t* ids, float* w) {
+  if (E <= 128)
+    topk_kernel<4><<<grid, kRouteThreads, 0, s>>>(logits, bias, e2s, affinity, part, nb, off, T, E, k, tpc, rflags,
+                                                  ids, w);
+  else if (E <= 256)
+    topk_kernel<8><<<grid, kRouteThreads, 0, s>>>(logits, bias, e2s, affinity, part, nb, off, T, E, k, tpc, rflags,
+                                                  ids, w);
+  else
+    topk_kernel<kMaxE / 32><<<grid, kRouteThreads, 0, s>>>(logits, bias, e2s, affinity, part, nb, off, T, E, k, tpc,
+                                                           rflags, ids, w);
+}
+
 }  // namespace moe
 
 using namespace moe;
@@ -505,8 +659,20 @@ extern "C" int moe_route_ex(const void* x, const void* w_router, const float* lo
     MOE_LAUNCH_CHECK();
     // tokens per CTA: 8 while that fills the SMs, else 2 (each thread then finishes about one logit)
     const int tpc = (T + 7) / 8 >= sms ? 8 : 2;
-    topk_kernel<<<(T + tpc - 1) / tpc, kRouteThreads, 0, s>>>(logits, sel_bias, e2s, affinity, scratch, nblk,
-                                                              logit_offset, T, E, k, tpc, rflags, ids, w);
+    launch_topk((T + tpc - 1) / tpc, s, logits, sel_bias, e2s, affinity, scratch, nblk, logit_offset, T, E, k, tpc,
+                rflags, ids, w);
+    MOE_LAUNCH_CHECK();
+    return MOE_OK;
+  }
+  if (E % 8 == 0 && ((T + kTT - 1) / kTT) * ((E + kTE - 1) / kTE) * 2 >= sms) {
+    // many tokens: (64 tokens, 64 experts) tiles over all of H, at least half as many CTAs as SMs
+    const int smem = (int)logits_full_smem_bytes();
+    static bool df[64] = {};
+    MOE_CUDA_TRY(ensure_smem(logits_full_kernel, smem, df));
+    const dim3 grid((T + kTT - 1) / kTT, (E + kTE - 1) / kTE);
+    logits_full_kernel<<<grid, kFullThreads, smem, s>>>(xb, wb, logit_offset, T, H, E, logits);
+    MOE_LAUNCH_CHECK();
+    launch_topk((T + 7) / 8, s, logits, sel_bias, e2s, affinity, nullptr, 0, nullptr, T, E, k, 8, rflags, ids, w);
     MOE_LAUNCH_CHECK();
     return MOE_OK;
   }
@@ -520,8 +686,8 @@ extern "C" int moe_route_ex(const void* x, const void* w_router, const float* lo
     MOE_LAUNCH_CHECK();
     // tokens per CTA: 8 while that fills the SMs, else 2 (each thread then finishes about one logit)
     const int tpc = (T + 7) / 8 >= sms ? 8 : 2;
-    topk_kernel<<<(T + tpc - 1) / tpc, kRouteThreads, 0, s>>>(logits, sel_bias, e2s, affinity, scratch, nblk,
-                                                              logit_offset, T, E, k, tpc, rflags, ids, w);
+    launch_topk((T + tpc - 1) / tpc, s, logits, sel_bias, e2s, affinity, scratch, nblk, logit_offset, T, E, k, tpc,
+                rflags, ids, w);
     MOE_LAUNCH_CHECK();
     return MOE_OK;
   }
@@ -550,8 +716,7 @@ extern "C" int moe_route_ex(const void* x, const void* w_router, const float* lo
       break;
   }
   MOE_LAUNCH_CHECK();
-  topk_kernel<<<(T + 7) / 8, kRouteThreads, 0, s>>>(logits, sel_bias, e2s, affinity, nullptr, 0, nullptr, T, E, k,
-                                                    8, rflags, ids, w);
+  launch_topk((T + 7) / 8, s, logits, sel_bias, e2s, affinity, nullptr, 0, nullptr, T, E, k, 8, rflags, ids, w);
   MOE_LAUNCH_CHECK();
   return MOE_OK;
 }

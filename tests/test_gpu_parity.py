@@ -57,6 +57,10 @@ ROUTE_CASES = [
     # enough tokens for the (64 tokens x 64 experts x 128 rows) tile path: ragged token and expert tiles
     ("qwen_T300_tiles", C.qwen(300), None, False),
     ("stack_T200_E288_tiles", C.STACK.with_(T=200), None, False),
+    # enough tokens for the (64 tokens x 64 experts) tiles over all of H: ragged token and expert tiles,
+    # and a ragged last 128-row block
+    ("stack_T2500_E288_full", C.STACK.with_(T=2500), None, False),
+    ("qwen_T2600_H1000_full", C.qwen(2600).with_(H=1000, logit_offset=True), None, True),
 ]
 
 
