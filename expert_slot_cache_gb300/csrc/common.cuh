@@ -74,6 +74,30 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* tmp, int* total)
   return res;
 }
 
+// Programmatic dependent launch: let the next kernel in the stream start /
+// wait until the previous kernel has completed and its writes are visible.
+// A kernel launched as a programmatic dependent (launch_pdl) waits before it
+// reads the previous kernel's output and before it exits, so completion stays
+// ordered along the stream; in a kernel launched plainly the wait is a no-op.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Launch `kernel` as a programmatic dependent of the kernel before it in `s`.
+template <typename K, typename... Args>
+inline cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // Raise a kernel's dynamic shared memory limit once per device.
 template <typename F>
 inline cudaError_t ensure_smem(F* func, int bytes, bool* done /* [64] per device */) {

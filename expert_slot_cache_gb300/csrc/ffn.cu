@@ -565,6 +565,8 @@ __global__ void __launch_bounds__(kCombThreads) combine_kernel(const float* __re
                                                                float* __restrict__ out_res,
                                                                float* __restrict__ out_miss,
                                                                const uint16_t* __restrict__ yb) {
+  pdl_trigger();
+  pdl_wait();  // launched as a dependent of the FFN's last kernel: y is complete
   const int t = blockIdx.x;
   const int c = (blockIdx.y * kCombThreads + threadIdx.x) * CPT;
   if (c >= H) return;
@@ -636,12 +638,12 @@ int launch_combine(const float* y, const float* w, const int32_t* pos, const int
                    const uint16_t* yb) {
   if (yb) {
     const dim3 grid(T, (H / 8 + kCombThreads - 1) / kCombThreads);
-    combine_kernel<8><<<grid, kCombThreads, 0, stream>>>(y, w, pos, ids, e2s, k, H, E, split, (uint16_t*)out,
-                                                         out_res, out_miss, yb);
+    MOE_CUDA_TRY(launch_pdl(combine_kernel<8>, grid, dim3(kCombThreads), 0, stream, y, w, pos, ids, e2s, k, H, E, split,
+                            (uint16_t*)out, out_res, out_miss, yb));
   } else {
     const dim3 grid(T, (H / 4 + kCombThreads - 1) / kCombThreads);
-    combine_kernel<4><<<grid, kCombThreads, 0, stream>>>(y, w, pos, ids, e2s, k, H, E, split, (uint16_t*)out,
-                                                         out_res, out_miss, nullptr);
+    MOE_CUDA_TRY(launch_pdl(combine_kernel<4>, grid, dim3(kCombThreads), 0, stream, y, w, pos, ids, e2s, k, H, E, split,
+                            (uint16_t*)out, out_res, out_miss, (const uint16_t*)nullptr));
   }
   MOE_LAUNCH_CHECK();
   return MOE_OK;

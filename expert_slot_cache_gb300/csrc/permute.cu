@@ -21,6 +21,8 @@ __global__ void __launch_bounds__(kPermThreads) permute_kernel(const int32_t* __
                                                                int32_t* __restrict__ act_e,
                                                                int32_t* __restrict__ n_act,
                                                                int32_t* __restrict__ status) {
+  pdl_trigger();
+  pdl_wait();  // launched as a dependent: the ids (or the previous permute step) are complete
   extern __shared__ int perm_smem[];
   int* cnt = perm_smem;
   int* base = cnt + E;
@@ -111,6 +113,8 @@ __global__ void __launch_bounds__(kPermThreads) permute_kernel(const int32_t* __
 __global__ void __launch_bounds__(kPermThreads) permute_hist_kernel(const int32_t* __restrict__ ids, int n, int E,
                                                                     int32_t* __restrict__ hist,
                                                                     int32_t* __restrict__ status) {
+  pdl_trigger();
+  pdl_wait();  // launched as a dependent: the ids (or the previous permute step) are complete
   extern __shared__ int ph_smem[];
   const int p = blockIdx.x, tid = threadIdx.x;
   for (int e = tid; e < E; e += kPermThreads) ph_smem[e] = 0;
@@ -131,6 +135,8 @@ __global__ void __launch_bounds__(kPermThreads) permute_scan_kernel(const int32_
                                                                     int32_t* __restrict__ act_e,
                                                                     int32_t* __restrict__ n_act,
                                                                     int32_t* __restrict__ base) {
+  pdl_trigger();
+  pdl_wait();  // launched as a dependent: the ids (or the previous permute step) are complete
   __shared__ int tmp[33];
   const int tid = threadIdx.x;
   int carry = 0, carry_act = 0;
@@ -166,6 +172,8 @@ __global__ void __launch_bounds__(kPermThreads) permute_scatter_kernel(const int
                                                                        const int32_t* __restrict__ base,
                                                                        int32_t* __restrict__ rows,
                                                                        int32_t* __restrict__ pos) {
+  pdl_trigger();
+  pdl_wait();  // launched as a dependent: the ids (or the previous permute step) are complete
   extern __shared__ int ps_smem[];  // wtab[32][E]
   const int p = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   int* wtab = ps_smem;
@@ -204,6 +212,8 @@ __global__ void __launch_bounds__(256) permute_small_kernel(const int32_t* __res
                                                             int32_t* __restrict__ act_e,
                                                             int32_t* __restrict__ n_act,
                                                             int32_t* __restrict__ status) {
+  pdl_trigger();
+  pdl_wait();  // launched as a dependent: the ids (or the previous permute step) are complete
   __shared__ int sid[kSmallN];
   __shared__ int soff[kMaxE];
   __shared__ int tmp[33];
@@ -260,8 +270,8 @@ int launch_permute(const int32_t* ids, int n, int E, int32_t* count, int32_t* of
                    int32_t* act_e, int32_t* n_act, int32_t* dev_status, int32_t* scratch, cudaStream_t s) {
   const int P = (n + kPermThreads - 1) / kPermThreads;
   if (n <= kSmallN) {
-    permute_small_kernel<<<1, 256, 0, s>>>(ids, n, E, count, offset, rows, pos, act_e, n_act, dev_status);
-    MOE_LAUNCH_CHECK();
+    MOE_CUDA_TRY(launch_pdl(permute_small_kernel, dim3(1), dim3(256), 0, s, ids, n, E, count, offset, rows, pos, act_e,
+                            n_act, dev_status));
     return MOE_OK;
   }
   if (P > 1 && scratch) {
@@ -270,19 +280,19 @@ int launch_permute(const int32_t* ids, int n, int E, int32_t* count, int32_t* of
     static bool d1[64] = {}, d3[64] = {};
     MOE_CUDA_TRY(ensure_smem(permute_hist_kernel, (int)(kMaxE * sizeof(int)), d1));
     MOE_CUDA_TRY(ensure_smem(permute_scatter_kernel, (int)(32 * kMaxE * sizeof(int)), d3));
-    permute_hist_kernel<<<P, kPermThreads, (size_t)E * sizeof(int), s>>>(ids, n, E, hist, dev_status);
-    MOE_LAUNCH_CHECK();
-    permute_scan_kernel<<<1, kPermThreads, 0, s>>>(hist, P, E, count, offset, act_e, n_act, base);
-    MOE_LAUNCH_CHECK();
-    permute_scatter_kernel<<<P, kPermThreads, (size_t)32 * E * sizeof(int), s>>>(ids, n, E, base, rows, pos);
-    MOE_LAUNCH_CHECK();
+    MOE_CUDA_TRY(launch_pdl(permute_hist_kernel, dim3(P), dim3(kPermThreads), (size_t)E * sizeof(int), s, ids, n, E,
+                            hist, dev_status));
+    MOE_CUDA_TRY(launch_pdl(permute_scan_kernel, dim3(1), dim3(kPermThreads), 0, s, (const int32_t*)hist, P, E, count,
+                            offset, act_e, n_act, base));
+    MOE_CUDA_TRY(launch_pdl(permute_scatter_kernel, dim3(P), dim3(kPermThreads), (size_t)32 * E * sizeof(int), s, ids,
+                            n, E, (const int32_t*)base, rows, pos));
     return MOE_OK;
   }
   const size_t smem = (size_t)(2 * E + 32 * E) * sizeof(int);
   static bool attr_done[64] = {};
   MOE_CUDA_TRY(ensure_smem(permute_kernel, (int)((2 + 32) * kMaxE * sizeof(int)), attr_done));
-  permute_kernel<<<1, kPermThreads, smem, s>>>(ids, n, E, count, offset, rows, pos, act_e, n_act, dev_status);
-  MOE_LAUNCH_CHECK();
+  MOE_CUDA_TRY(launch_pdl(permute_kernel, dim3(1), dim3(kPermThreads), smem, s, ids, n, E, count, offset, rows, pos,
+                          act_e, n_act, dev_status));
   return MOE_OK;
 }
 }  // namespace moe

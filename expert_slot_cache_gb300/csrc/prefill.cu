@@ -368,6 +368,7 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __rest
                                                           const int32_t* __restrict__ rows, int n, int H, int k,
                                                           uint16_t* __restrict__ xp) {
   pdl_trigger();
+  pdl_wait();  // launched as a dependent of the permute (stream path): rows are complete
   const int H8 = H / 8;
   for (int p = blockIdx.x; p < n; p += gridDim.x) {
     const int t = rows[p] / k;
@@ -379,8 +380,7 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __rest
 
 int launch_gather_rows(const uint16_t* x, const int32_t* rows, int n, int H, int k, uint16_t* xp, int sms,
                        cudaStream_t stream) {
-  gather_rows_kernel<<<std::min(n, sms * 8), 256, 0, stream>>>(x, rows, n, H, k, xp);
-  MOE_LAUNCH_CHECK();
+  MOE_CUDA_TRY(launch_pdl(gather_rows_kernel, dim3(std::min(n, sms * 8)), dim3(256), 0, stream, x, rows, n, H, k, xp));
   return MOE_OK;
 }
 

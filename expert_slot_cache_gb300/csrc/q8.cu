@@ -105,6 +105,7 @@ __global__ void __launch_bounds__(kQRowThreads) q8_rows_kernel(const uint16_t* _
                                                                float* __restrict__ sx) {
   __shared__ float red[32];
   pdl_trigger();
+  pdl_wait();  // launched as a dependent of the permute: rows are complete
   const int p = blockIdx.x;
   const uint16_t* xr = x + (size_t)(rows[p] / k) * H;
   float amax = 0.f;
@@ -534,8 +535,8 @@ int launch_ffn_q8(const FfnArgs& a, void* ws, size_t ws_bytes, int max_list, cud
   MOE_CUDA_TRY(ensure_smem(ffn_q8_kernel<false>, kSmemMax, done_g));
   MOE_CUDA_TRY(ensure_smem(ffn_q8_kernel<true>, kSmemMax, done_d));
   if (prof) prof->begin(MOE_PROF_FFN_GATEUP, stream);
-  q8_rows_kernel<<<n, kQRowThreads, 0, stream>>>(a.x, a.rows, n, a.H, a.k, c.npad, c.xq, c.sx);
-  MOE_LAUNCH_CHECK();
+  MOE_CUDA_TRY(launch_pdl(q8_rows_kernel, dim3(n), dim3(kQRowThreads), 0, stream, a.x, a.rows, n, a.H, a.k, c.npad,
+                          c.xq, c.sx));
   MOE_CUDA_TRY(q_launch(ffn_q8_kernel<false>, dim3(sms), dim3(g.N / 4 + 32), q_smem(g), stream, true, a, g));
   MOE_CUDA_TRY(q_launch(q8_reduce_gu_kernel, dim3(max_list), dim3(kQRowThreads), 0, stream, true, a,
                         (const int32_t*)c.gpart, (const int32_t*)c.vpre_g, g.NSR, g.G, g.jcap, g.qslab,

@@ -98,6 +98,7 @@ __global__ void __launch_bounds__(kRouteThreads) logits_kernel(const uint16_t* _
                                                                float* __restrict__ logits) {
   constexpr int TT = 8 * CH;
   constexpr int kXRow = kHC + 8;  // bf16 x row, padded against bank conflicts in the conversion
+  pdl_trigger();
   // stage s: W [kHC][kEB] bf16 (8 KB) | x [TT][kXRow] bf16;  then xf [kHC][TT] fp32 (token-minor)
   constexpr int kWBytes = kHC * kEB * 2;
   constexpr int kXBytes = TT * kXRow * 2;
@@ -219,6 +220,7 @@ __global__ void __launch_bounds__(kRouteThreads) logits_block_kernel(const uint1
   constexpr int TT = 8 * CH;
   __shared__ __align__(16) uint16_t ws[kHC * kEB];
   __shared__ __align__(16) uint16_t xs[TT * kHC];
+  pdl_trigger();  // the top-k launches meanwhile and waits for these parts
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int b = blockIdx.x, e0 = blockIdx.y * kEB, t0 = blockIdx.z * TT;
   const int h0 = b * kHC;
@@ -282,6 +284,7 @@ __global__ void __launch_bounds__(kTileThreads) logits_tile_kernel(const uint16_
                                                                   const uint16_t* __restrict__ wr, int T, int H,
                                                                   int E, float* __restrict__ part) {
   extern __shared__ __align__(16) float tsm[];
+  pdl_trigger();
   float* xf = tsm;               // [kHC][kTT]
   float* wf = tsm + kHC * kTT;   // [kHC][kTE]
   const int tid = threadIdx.x;
@@ -371,6 +374,7 @@ __global__ void __launch_bounds__(kFullThreads) logits_full_kernel(const uint16_
                                                                   const float* __restrict__ off, int T, int H,
                                                                   int E, float* __restrict__ logits) {
   extern __shared__ __align__(16) float fsm[];
+  pdl_trigger();
   float* xf = fsm;                                                           // [kHC][kTT]
   float* wf = fsm + kHC * kTT;                                               // [kHC][kTE]
   uint16_t* stg = reinterpret_cast<uint16_t*>(fsm + kHC * kTT + kHC * kTE);  // 2 x (x [kTT][kFullXRow] | Wr [kHC][kTE])
@@ -501,6 +505,8 @@ __global__ void __launch_bounds__(kRouteThreads) topk_kernel(float* __restrict__
                                                              float* __restrict__ wout) {
   __shared__ float sel_l[kRouteThreads / 32][kMaxK];
   __shared__ int sel_i[kRouteThreads / 32][kMaxK];
+  pdl_trigger();
+  pdl_wait();  // launched as a dependent of the logits kernel: its parts / logits are complete
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int tb = blockIdx.x * tpc;  // tokens tb .. tb+tpc-1, one warp each (tpc <= 8)
   if (part) {
@@ -598,19 +604,20 @@ __global__ void __launch_bounds__(kRouteThreads) topk_kernel(float* __restrict__
   }
 }
 
-// Top-k launch with the fewest 32-expert slots per lane that hold E.
-static void launch_topk(int grid, cudaStream_t s, float* logits, const float* bias, const int32_t* e2s,
-                        float affinity, const float* part, int nb, const float* off, int T, int E, int k, int tpc,
-                        int rflags, int32_t* ids, float* w) {
+// Top-k launch (a programmatic dependent of the logits kernel) with the fewest 32-expert slots per lane
+// that hold E.
+static cudaError_t launch_topk(int grid, cudaStream_t s, float* logits, const float* bias, const int32_t* e2s,
+                               float affinity, const float* part, int nb, const float* off, int T, int E, int k,
+                               int tpc, int rflags, int32_t* ids, float* w) {
+  const dim3 g(grid), b(kRouteThreads);
   if (E <= 128)
-    topk_kernel<4><<<grid, kRouteThreads, 0, s>>>(logits, bias, e2s, affinity, part, nb, off, T, E, k, tpc, rflags,
-                                                  ids, w);
-  else if (E <= 256)
-    topk_kernel<8><<<grid, kRouteThreads, 0, s>>>(logits, bias, e2s, affinity, part, nb, off, T, E, k, tpc, rflags,
-                                                  ids, w);
-  else
-    topk_kernel<kMaxE / 32><<<grid, kRouteThreads, 0, s>>>(logits, bias, e2s, affinity, part, nb, off, T, E, k, tpc,
-                                                           rflags, ids, w);
+    return launch_pdl(topk_kernel<4>, g, b, 0, s, logits, bias, e2s, affinity, part, nb, off, T, E, k, tpc, rflags,
+                      ids, w);
+  if (E <= 256)
+    return launch_pdl(topk_kernel<8>, g, b, 0, s, logits, bias, e2s, affinity, part, nb, off, T, E, k, tpc, rflags,
+                      ids, w);
+  return launch_pdl(topk_kernel<kMaxE / 32>, g, b, 0, s, logits, bias, e2s, affinity, part, nb, off, T, E, k, tpc,
+                    rflags, ids, w);
 }
 
 }  // namespace moe
@@ -659,8 +666,8 @@ extern "C" int moe_route_ex(const void* x, const void* w_router, const float* lo
     MOE_LAUNCH_CHECK();
     // tokens per CTA: 8 while that fills the SMs, else 2 (each thread then finishes about one logit)
     const int tpc = (T + 7) / 8 >= sms ? 8 : 2;
-    launch_topk((T + tpc - 1) / tpc, s, logits, sel_bias, e2s, affinity, scratch, nblk, logit_offset, T, E, k, tpc,
-                rflags, ids, w);
+    MOE_CUDA_TRY(launch_topk((T + tpc - 1) / tpc, s, logits, sel_bias, e2s, affinity, scratch, nblk, logit_offset, T,
+                             E, k, tpc, rflags, ids, w));
     MOE_LAUNCH_CHECK();
     return MOE_OK;
   }
@@ -672,7 +679,8 @@ extern "C" int moe_route_ex(const void* x, const void* w_router, const float* lo
     const dim3 grid((T + kTT - 1) / kTT, (E + kTE - 1) / kTE);
     logits_full_kernel<<<grid, kFullThreads, smem, s>>>(xb, wb, logit_offset, T, H, E, logits);
     MOE_LAUNCH_CHECK();
-    launch_topk((T + 7) / 8, s, logits, sel_bias, e2s, affinity, nullptr, 0, nullptr, T, E, k, 8, rflags, ids, w);
+    MOE_CUDA_TRY(launch_topk((T + 7) / 8, s, logits, sel_bias, e2s, affinity, nullptr, 0, nullptr, T, E, k, 8, rflags,
+                             ids, w));
     MOE_LAUNCH_CHECK();
     return MOE_OK;
   }
@@ -686,8 +694,8 @@ extern "C" int moe_route_ex(const void* x, const void* w_router, const float* lo
     MOE_LAUNCH_CHECK();
     // tokens per CTA: 8 while that fills the SMs, else 2 (each thread then finishes about one logit)
     const int tpc = (T + 7) / 8 >= sms ? 8 : 2;
-    launch_topk((T + tpc - 1) / tpc, s, logits, sel_bias, e2s, affinity, scratch, nblk, logit_offset, T, E, k, tpc,
-                rflags, ids, w);
+    MOE_CUDA_TRY(launch_topk((T + tpc - 1) / tpc, s, logits, sel_bias, e2s, affinity, scratch, nblk, logit_offset, T,
+                             E, k, tpc, rflags, ids, w));
     MOE_LAUNCH_CHECK();
     return MOE_OK;
   }
@@ -716,7 +724,8 @@ extern "C" int moe_route_ex(const void* x, const void* w_router, const float* lo
       break;
   }
   MOE_LAUNCH_CHECK();
-  launch_topk((T + 7) / 8, s, logits, sel_bias, e2s, affinity, nullptr, 0, nullptr, T, E, k, 8, rflags, ids, w);
+  MOE_CUDA_TRY(launch_topk((T + 7) / 8, s, logits, sel_bias, e2s, affinity, nullptr, 0, nullptr, T, E, k, 8, rflags,
+                           ids, w));
   MOE_LAUNCH_CHECK();
   return MOE_OK;
 }
