@@ -337,14 +337,30 @@ __global__ void __launch_bounds__(kQRowThreads) q8_reduce_gu_kernel(const FfnArg
     const float s_x = sx[p];
     float hv[4][4];  // up to 4 quads per thread (I <= 16 * blockDim)
     float amax = 0.f;
-    int nq = 0;
-    for (int q = threadIdx.x; q < I / 4; q += blockDim.x, ++nq) {
+#pragma unroll
+    for (int nq = 0; nq < 4; ++nq) {
+      const int q = threadIdx.x + nq * blockDim.x;
+      if (q >= I / 4) break;
+      // exact int32 sums, so the parts may be added in any order: eight parts' loads are issued
+      // before their adds, instead of one L2 round trip per part
       int4 ag = make_int4(0, 0, 0, 0), au = ag;
-      for (int jj = 0; jj < J; ++jj) {
-        const int4 tg = *reinterpret_cast<const int4*>(part + jj * pstride + (size_t)p * N + 4 * q);
-        const int4 tu = *reinterpret_cast<const int4*>(part + jj * pstride + (size_t)p * N + I + 4 * q);
-        ag.x += tg.x; ag.y += tg.y; ag.z += tg.z; ag.w += tg.w;
-        au.x += tu.x; au.y += tu.y; au.z += tu.z; au.w += tu.w;
+      const int32_t* pp = part + (size_t)p * N + 4 * q;
+      for (int j0 = 0; j0 < J; j0 += 8) {
+        int4 tg[8], tu[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          tg[u] = make_int4(0, 0, 0, 0);
+          tu[u] = tg[u];
+          if (j0 + u < J) {
+            tg[u] = *reinterpret_cast<const int4*>(pp + (size_t)(j0 + u) * pstride);
+            tu[u] = *reinterpret_cast<const int4*>(pp + (size_t)(j0 + u) * pstride + I);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          ag.x += tg[u].x; ag.y += tg[u].y; ag.z += tg[u].z; ag.w += tg[u].w;
+          au.x += tu[u].x; au.y += tu[u].y; au.z += tu[u].z; au.w += tu[u].w;
+        }
       }
       const int gi[4] = {ag.x, ag.y, ag.z, ag.w}, ui[4] = {au.x, au.y, au.z, au.w};
 #pragma unroll
@@ -359,8 +375,10 @@ __global__ void __launch_bounds__(kQRowThreads) q8_reduce_gu_kernel(const FfnArg
     }
     amax = block_max(amax, red);
     const float s = __fdiv_rn(amax, 127.f);
-    nq = 0;
-    for (int q = threadIdx.x; q < I / 4; q += blockDim.x, ++nq) {
+#pragma unroll
+    for (int nq = 0; nq < 4; ++nq) {
+      const int q = threadIdx.x + nq * blockDim.x;
+      if (q >= I / 4) break;
       uint32_t pk = 0;
 #pragma unroll
       for (int b = 0; b < 4; ++b) pk |= (uint32_t)(q8_code(hv[nq][b], s) & 0xff) << (8 * b);
