@@ -121,6 +121,12 @@ __global__ void __launch_bounds__(kQRowThreads) q8_rows_kernel(const uint16_t* _
   if (threadIdx.x == 0) sx[p] = s;
 }
 
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
 // ---------------------------------------------------------------------------
 // The stream (one pass: gate/up or down)
 // ---------------------------------------------------------------------------
@@ -388,6 +394,88 @@ __global__ void __launch_bounds__(kQRowThreads) q8_reduce_gu_kernel(const FfnArg
   }
 }
 
+// The same reduction with one warp per row (rows pb + w, pb + w + 8, ... of the
+// listed expert), for lists that average two or more rows per expert: an
+// expert's rows proceed in parallel and the row amax is a warp maximum.  I/4
+// quads of a row are spread over the lanes, at most 8 per lane (I <= 1024).
+constexpr int kQWarpQuads = 8;
+__global__ void __launch_bounds__(kQRowThreads) q8_reduce_gu_warp_kernel(
+    const FfnArgs a, const int32_t* __restrict__ part, const int32_t* __restrict__ vpre, int NSR, int G, int jcap,
+    size_t qslab, const float* __restrict__ sx, int npad, uint32_t* __restrict__ hq, float* __restrict__ sh) {
+  pdl_trigger();
+  const int li = blockIdx.x;
+  const int n_list = *a.n_list;
+  int e = -1, slot = -1;
+  const bool ok = li < n_list && stream_slot(a, li, e, slot);
+  pdl_wait();
+  if (!ok) return;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nl = min(n_list, kMaxE);
+  const int L = stream_len(vpre[nl], NSR, G, jcap);  // vpre: written by the pass before (completed)
+  const int v0 = vpre[li];
+  const int n = a.T * a.k, I = a.I, N = 2 * I;
+  const size_t mat = (size_t)a.H * I;
+  const float* sc = reinterpret_cast<const float*>(reinterpret_cast<const unsigned char*>(a.pool) +
+                                                   (size_t)slot * qslab + 3 * mat);
+  const float* sg = sc;
+  const float* su = sc + I;
+  const size_t pstride = (size_t)n * N;
+  const int pb = a.offset[e], pe = a.offset[e + 1];
+  for (int p = pb + warp; p < pe; p += kQRowThreads / 32) {
+    const int J = stream_parts(v0 + (p - pb) / kQRB, NSR, L);
+    const float s_x = sx[p];
+    float hv[kQWarpQuads][4];
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < kQWarpQuads; ++i) {
+      const int q = lane + 32 * i;
+      if (q >= I / 4) break;
+      // exact int32 sums: parts in batches of four loads, added in any order
+      int4 ag = make_int4(0, 0, 0, 0), au = ag;
+      const int32_t* pp = part + (size_t)p * N + 4 * q;
+      for (int j0 = 0; j0 < J; j0 += 4) {
+        int4 tg[4], tu[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          tg[u] = make_int4(0, 0, 0, 0);
+          tu[u] = tg[u];
+          if (j0 + u < J) {
+            tg[u] = *reinterpret_cast<const int4*>(pp + (size_t)(j0 + u) * pstride);
+            tu[u] = *reinterpret_cast<const int4*>(pp + (size_t)(j0 + u) * pstride + I);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          ag.x += tg[u].x; ag.y += tg[u].y; ag.z += tg[u].z; ag.w += tg[u].w;
+          au.x += tu[u].x; au.y += tu[u].y; au.z += tu[u].z; au.w += tu[u].w;
+        }
+      }
+      const int gi[4] = {ag.x, ag.y, ag.z, ag.w}, ui[4] = {au.x, au.y, au.z, au.w};
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const int c = 4 * q + b;
+        const float g = __fmul_rn(__fmul_rn(__int2float_rn(gi[b]), sg[c]), s_x);
+        const float u = __fmul_rn(__fmul_rn(__int2float_rn(ui[b]), su[c]), s_x);
+        const float h = __fmul_rn(silu32_def(g), u);
+        hv[i][b] = h;
+        amax = fmaxf(amax, fabsf(h));
+      }
+    }
+    amax = warp_max(amax);
+    const float s = __fdiv_rn(amax, 127.f);
+#pragma unroll
+    for (int i = 0; i < kQWarpQuads; ++i) {
+      const int q = lane + 32 * i;
+      if (q >= I / 4) break;
+      uint32_t pk = 0;
+#pragma unroll
+      for (int b = 0; b < 4; ++b) pk |= (uint32_t)(q8_code(hv[i][b], s) & 0xff) << (8 * b);
+      hq[q8_act_word(q, p, npad)] = pk;
+    }
+    if (lane == 0) sh[p] = s;
+  }
+}
+
 // down: y[p][n] = (float(sum of parts) * sd[n]) * sh[p]; block = 128 columns of one listed expert.
 __global__ void __launch_bounds__(256) q8_reduce_d_kernel(const FfnArgs a, const int32_t* __restrict__ part,
                                                           const int32_t* __restrict__ vpre, int NSR,
@@ -556,9 +644,11 @@ int launch_ffn_q8(const FfnArgs& a, void* ws, size_t ws_bytes, int max_list, cud
   MOE_CUDA_TRY(launch_pdl(q8_rows_kernel, dim3(n), dim3(kQRowThreads), 0, stream, a.x, a.rows, n, a.H, a.k, c.npad,
                           c.xq, c.sx));
   MOE_CUDA_TRY(q_launch(ffn_q8_kernel<false>, dim3(sms), dim3(g.N / 4 + 32), q_smem(g), stream, true, a, g));
-  MOE_CUDA_TRY(q_launch(q8_reduce_gu_kernel, dim3(max_list), dim3(kQRowThreads), 0, stream, true, a,
-                        (const int32_t*)c.gpart, (const int32_t*)c.vpre_g, g.NSR, g.G, g.jcap, g.qslab,
-                        (const float*)c.sx, c.npad, c.hq, c.sh));
+  // an expert's rows in parallel (one warp each) when the list averages two or more rows per expert
+  const bool warp_rows = n >= 2 * max_list && a.I / 4 <= 32 * kQWarpQuads;
+  MOE_CUDA_TRY(q_launch(warp_rows ? q8_reduce_gu_warp_kernel : q8_reduce_gu_kernel, dim3(max_list), dim3(kQRowThreads),
+                        0, stream, true, a, (const int32_t*)c.gpart, (const int32_t*)c.vpre_g, g.NSR, g.G, g.jcap,
+                        g.qslab, (const float*)c.sx, c.npad, c.hq, c.sh));
   if (prof) prof->end(stream);
   if (prof) prof->begin(MOE_PROF_FFN_DOWN, stream);
   MOE_CUDA_TRY(q_launch(ffn_q8_kernel<true>, dim3(sms), dim3(d.N / 4 + 32), q_smem(d), stream, true, a, d));
