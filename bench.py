@@ -229,6 +229,58 @@ class StackWorkload:
         self.stack.x_all.copy_(self.inputs[st])
 
 
+def stack_variant(dev: str, peaks: dict, cfg: "C.LayerConfig", steps: int = 8, warmup: int = 3) -> dict:
+    """The 48-layer decode stack (288 experts per layer, top-8, H 2048, I 512,
+    T = 32; all 48 layers as one CUDA-graph replay per step): tokens/s and,
+    all-resident, HBM GB/s on unique expert bytes (Betelgeuse's single-graph
+    decode over every layer).  Each step's inputs (48 x T x H) are copied into
+    place inside the timed region; the unique experts per layer and chunk come
+    from a second, untimed replay of the same steps."""
+    wl = StackWorkload(cfg, dev, steps=warmup + steps)
+    wl.load_step(0)
+    wl.stack._run()
+    torch.cuda.synchronize()
+    wl.stack.capture()
+    for st in range(warmup):
+        wl.load_step(st)
+        wl.stack.replay()
+    torch.cuda.synchronize()
+    misses0 = sum(int(l.stats[0]) for l in wl.layers)
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for st in range(warmup, warmup + steps):
+        wl.load_step(st)
+        wl.stack.replay()
+    e.record()
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e)
+    misses = sum(int(l.stats[0]) for l in wl.layers) - misses0
+    out = {"config": f"{cfg.name}: {wl.L} layers x {cfg.E} experts, T={cfg.T}, k={cfg.k}, H={cfg.H}, I={cfg.I}, "
+                     f"S={cfg.S}, {'all resident' if cfg.mode == C.MODE_RESIDENT else 'slot pool + pinned host'}",
+           "tokens_per_s": cfg.T * steps / (ms * 1e-3), "ms_per_step": ms / steps,
+           "expert_GB_in_hbm": wl.L * (cfg.S if cfg.mode != C.MODE_RESIDENT else cfg.E) * cfg.slab_bytes / 1e9}
+    if cfg.mode == C.MODE_RESIDENT:
+        units = 0
+        C_ = cfg.T  # all-resident: one chunk per layer
+        for st in range(warmup, warmup + steps):
+            wl.load_step(st)
+            wl.stack.replay()
+            torch.cuda.synchronize()
+            for l in range(wl.L):
+                ids = wl.stack.ids[l].cpu().numpy()
+                units += sum(len(np.unique(ids[t0:t0 + C_])) for t0 in range(0, cfg.T, C_))
+        byts = units * cfg.slab_bytes
+        out["unique_expert_GB_per_step"] = byts / steps / 1e9
+        out["hbm"] = {"bound": "hbm", "achieved": byts / (ms * 1e-3) / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                      "frac": byts / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], "of": "whole step (48 layers)"}
+    else:
+        out["misses_per_step"] = misses / steps
+        out["host_link_GB_per_step"] = misses * cfg.slab_bytes / steps / 1e9
+    del wl
+    torch.cuda.empty_cache()
+    return out
+
+
 def w8a8_variants(dev: str, peaks: dict, steps: int = 10, warmup: int = 3) -> dict:
     """W8A8 experts (the vllm-expert-cache page's W8A8 model; scales
     slot-indexed inside the slab): the all-resident decode layer at T = 1, 8,
@@ -554,7 +606,8 @@ def main():
     ap.add_argument("--no-variants", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="main",
-                    help="main (default) | prefill | resident_T<n> | gather_T<n> | routing_variants: one workload alone "
+                    help="main (default) | prefill | resident_T<n> | gather_T<n> | routing_variants | w8a8 | stack | "
+                         "stack_slots: one workload alone "
                          "(for profiling); prints its own JSON line")
     args = ap.parse_args()
     ws, rank, local, dist = _dist()
@@ -574,6 +627,11 @@ def main():
     if args.workload == "routing_variants":
         if rank == 0:
             print(json.dumps({"workload": "routing_variants", **routing_variants(dev, args.steps, args.warmup)}))
+        return
+    if args.workload in ("stack", "stack_slots"):
+        cfg_s = C.STACK if args.workload == "stack" else C.STACK_SLOTS
+        if rank == 0:
+            print(json.dumps({"workload": args.workload, **stack_variant(dev, peaks, cfg_s, args.steps, args.warmup)}))
         return
     if args.workload != "main":
         w = args.workload
@@ -672,6 +730,8 @@ def main():
         var["routing_variants"] = routing_variants(dev)
         torch.cuda.empty_cache()
         var["w8a8"] = w8a8_variants(dev, peaks)
+        torch.cuda.empty_cache()
+        var["stack48_resident"] = stack_variant(dev, peaks, C.STACK)
         line["variants"] = var
 
     if not args.no_cpu_baseline and rank == 0:

@@ -79,6 +79,9 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* tmp, int* total)
 // A kernel launched as a programmatic dependent (launch_pdl) waits before it
 // reads the previous kernel's output and before it exits, so completion stays
 // ordered along the stream; in a kernel launched plainly the wait is a no-op.
+// A kernel that triggers before its own wait lets its dependent start before
+// the kernel before it has completed: it may do so only when that dependent
+// reads nothing of earlier kernels before its own wait.
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 

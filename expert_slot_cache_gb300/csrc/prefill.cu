@@ -367,8 +367,11 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const Prefil
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __restrict__ x,
                                                           const int32_t* __restrict__ rows, int n, int H, int k,
                                                           uint16_t* __restrict__ xp) {
+  // Launched as a dependent of the permute (stream path).  Wait first, then let the stream kernel
+  // launch: it reads the permute's expert list and offsets before its own wait, so the permute must
+  // have completed by the time it can start.
+  pdl_wait();
   pdl_trigger();
-  pdl_wait();  // launched as a dependent of the permute (stream path): rows are complete
   const int H8 = H / 8;
   for (int p = blockIdx.x; p < n; p += gridDim.x) {
     const int t = rows[p] / k;

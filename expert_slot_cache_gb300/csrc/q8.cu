@@ -104,8 +104,10 @@ __global__ void __launch_bounds__(kQRowThreads) q8_rows_kernel(const uint16_t* _
                                                                int npad, uint32_t* __restrict__ xq,
                                                                float* __restrict__ sx) {
   __shared__ float red[32];
+  // Launched as a dependent of the permute.  Wait first, then let the stream kernel launch: it reads
+  // the permute's expert list and offsets before its own wait.
+  pdl_wait();
   pdl_trigger();
-  pdl_wait();  // launched as a dependent of the permute: rows are complete
   const int p = blockIdx.x;
   const uint16_t* xr = x + (size_t)(rows[p] / k) * H;
   float amax = 0.f;

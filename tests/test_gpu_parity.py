@@ -417,6 +417,34 @@ def test_layer_flash_zero_return():
     _run_layer(C.FLASH, steps=2)
 
 
+def test_layer_stack_shape_all_resident():
+    # 288 experts, all in the pool, T=32: up to 256 listed experts in one stream pass
+    _run_layer(C.STACK, steps=2)
+
+
+def test_layer_stack_shape_all_resident_174_experts():
+    """Layer 24 of the stack, steps 0 and 1 (the second routes to 174 experts):
+    the stream FFN must see the permute's complete lists (programmatic
+    dependent launches along the layer)."""
+    cfg = C.STACK
+    l = 24
+    wr = C.draw_router(cfg, DEV, l)
+    slabs = torch.empty(cfg.E, cfg.slab_elems, dtype=torch.bfloat16, device=DEV)
+    C.draw_slabs(cfg, DEV, l, out=slabs)
+    layer = M.SlotCachedMoELayer(wr, slabs, cfg.k, cfg.I, cfg.mode, cfg.policy, max_tokens=cfg.T)
+    wr_np = _np(wr.float())
+    slabs_h = HostSlabs(slabs.cpu())
+    for st in range(2):
+        x = C.draw_x(cfg, DEV, layer=l, step=st)
+        res = layer.forward(x)
+        torch.cuda.synchronize()
+        assert int(_np(layer.dev_status)[0]) == 0, f"step {st}"
+        want = O.layer_forward(_np(x.float()), wr_np, slabs_h, cfg.H, cfg.I, cfg.k, cfg.mode, cfg.policy)
+        assert np.array_equal(_np(res["ids"]), want["ids"]), f"step {st}: ids"
+        assert_out_close(_np(res["out"].float()), want["out"], f"step {st}: out")
+    assert len(np.unique(_np(res["ids"]))) == 174
+
+
 def test_layer_stack_shape_gather_chunked():
     _run_layer(C.STACK_SLOTS, steps=2)
 
