@@ -3,7 +3,7 @@
 // "Porting vllm-expert-cache to NVIDIA GPUs", "What this package does": the
 // expert GEMM runs on the grouped, slot-remapped ids.  When the groups are
 // large (prefill), the two GEMMs are dense contractions and run here:
-//   GEMM 1: [g | u] = Xp_e Wg_e | Xp_e Wu_e, epilogue h = silu(g) * u (bf16)
+//   GEMM 1: g = Xp_e Wg_e, u = Xp_e Wu_e, epilogue h = silu(g) * u (bf16)
 //   GEMM 2: y = h_e Wd_e (bf16, or fp32)
 // Xp is the routed rows of x in grouped order (copied once by
 // gather_rows_kernel).
@@ -12,30 +12,35 @@
 // cluster of two on neighbouring SMs): the pair's MMA has M = 256 weight
 // features (128 in each CTA's shared memory and TMEM) and N = up to 256 of
 // one expert's grouped rows, rounded up to a multiple of 32, half of them in
-// each CTA's shared memory.  Each CTA thus loads 64 KB of operands per 128-deep
-// K step for a 128 x 256 x 128 share of the work, two thirds of what a lone
-// CTA needs for the same tile.  Groups are ragged (a skewed router gives
-// 0 .. thousands of rows per expert), and rows on the N side pad a group only
-// to the next 32 rows instead of the next 128 or 256.  In GEMM 1 a CTA's 128
-// features are 64 gate columns followed by the same 64 up columns, so one
-// MMA per K step feeds both and the epilogue pairs them.
+// each CTA's shared memory.
+//
+// What sets the pace is how fast the operands reach shared memory (about
+// 40 B per clock per SM from L2 on this part), not the MMAs, so the tiles
+// are shaped to move few bytes per MMA cycle:
+//   - GEMM 1 keeps two accumulators per tile: a CTA's 128 gate features and
+//     the same 128 up features.  The grouped rows of a stage then feed 256
+//     h features per CTA pair instead of 128, and the epilogue finds g and u
+//     of one feature in the same TMEM lane.  The two accumulators fill TMEM
+//     (2 x 256 columns), so the epilogue of a tile does not overlap the MMAs
+//     of the next; it is short next to the 2048-deep main loop.
+//   - GEMM 2 (K = I, a short main loop) keeps one accumulator per tile and
+//     double-buffers it, so its epilogue overlaps the next tile.
+//   - A ragged tile loads only its rows (rounded up to 16 per CTA): tensor
+//     maps with boxes of 128, 64, 32 and 16 rows.
 //
 // Persistent clusters over the tiles of all experts (expert-major, then
 // token tile, then feature tile, so a token tile stays hot in L2 while the
 // clusters walk the expert's weights); per CTA:
-//   warp 0: TMA producer (one thread), 3-stage ring of 64 KB stages; the
-//           loads of both CTAs complete on rank 0's barrier
+//   warp 0: TMA producer (one thread); the loads of both CTAs complete on
+//           rank 0's barrier
 //   warp 1: TMEM allocation (both CTAs) + pair MMA issue (rank 0, one thread)
 //   warps 2-5: epilogue, TMEM -> registers -> shared (transpose) -> global
 // Shared-memory operands use the 128-byte swizzle written by the tensor-map
 // loads: weights MN-major (stored input-major: 64 output columns = 128 B per
-// K row, 8 K rows per 1 KB swizzle group, 64-column atoms 16 KB apart),
-// grouped rows K-major (rows of 64 bf16 = 128 B, the two 64-deep K halves of
-// a stage 16 KB apart).  One thread issues the MMAs, and a tcgen05.mma costs
-// it tens of cycles to issue, so a stage is 128 deep: the barrier wait, fence
-// and commit per stage are spread over eight MMAs.  Accumulators are fp32 in TMEM, two
-// 256-column buffers so the epilogue of one tile overlaps the MMAs of the
-// next.
+// K row, 8 K rows per 1 KB swizzle group, 64-column atoms one K depth
+// apart), grouped rows K-major (rows of 64 bf16 = 128 B).  One thread issues
+// the MMAs, and a tcgen05.mma costs it tens of cycles to issue, so each ring
+// stage carries eight MMAs per barrier wait and commit.
 #include "internal.cuh"
 #include "tc05.cuh"
 
@@ -43,20 +48,26 @@ namespace moe {
 
 constexpr int kPM = 128;     // weight features per CTA (the pair's MMA M is 256)
 constexpr int kPT = 256;     // grouped rows per tile, at most (MMA N)
-constexpr int kPTBox = 128;  // grouped rows per CTA and tile, at most (one tensor-map box)
-constexpr int kPK = 128;    // K depth of a ring stage: eight 16-deep MMAs per barrier wait and commit
-constexpr int kPStages = 3;
-constexpr int kPAbytes = kPM * kPK * 2;            // 32 KB of weights: two 64-feature atoms, 16 KB apart
-constexpr int kPBbytes = kPTBox * kPK * 2;         // 32 KB of rows: two 64-deep K halves, 16 KB apart
-constexpr int kPStageBytes = kPAbytes + kPBbytes;  // 64 KB
+constexpr int kPTBox = 128;  // grouped rows per CTA and tile, at most
 constexpr int kPThreads = 192;
-constexpr uint32_t kTmemCols = 2 * kPT;
+constexpr uint32_t kTmemCols = 512;
 constexpr int kPBarWords = 32;  // mbarriers: full / empty per stage, two accumulators, done
 constexpr int kPrefillMinRows = 4096;
-// per epilogue warp: a staging tile of 32 rows x 32 features (fp32 at most) and a 16 x 32 fp32
-// gate/up exchange buffer
-constexpr int kEpiStageBytes = 32 * 32 * 4;
-constexpr int kEpiXFloats = 16 * 32;
+constexpr int kMaxTT = 2048;    // token tiles per launch
+constexpr int kEpiStageBytes = 32 * 32 * 4;  // per epilogue warp: 32 rows x 32 features (fp32 at most)
+
+// Ring geometry.  GEMM 1: a 64-deep stage holds 128 gate and the same 128 up
+// features (2 x 16 KB) and up to 128 rows (16 KB).  GEMM 2: a 128-deep stage
+// holds 128 features (32 KB) and up to 128 rows in two 64-deep halves (32 KB).
+template <int kMode>
+struct PGeo {
+  static constexpr int K = kMode == 0 ? 64 : 128;        // K depth of a stage
+  static constexpr int Stages = kMode == 0 ? 4 : 3;
+  static constexpr int ABytes = 32768;
+  static constexpr int StageBytes = ABytes + kPTBox * K * 2;
+  static constexpr int Acc = kMode == 0 ? 1 : 2;         // accumulator buffers
+  static constexpr uint32_t AtomBytes = 64 * K * 2;      // one 64-feature column atom of a stage
+};
 
 __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
   return smem_desc_l(saddr, lbo, sbo, kLayoutSw128);
@@ -75,49 +86,82 @@ struct PrefillArgs {
   uint16_t* yb;  // bf16 [n][H]: GEMM 2 output, or NULL
 };
 
-// Locate tile t: expert list index (by prefix search), token tile, feature tile.
-__device__ __forceinline__ void find_tile(const int* pre, int nl, int t, int nf, int& li, int& m, int& ft) {
-  int lo = 0, hi = nl;  // pre[lo] <= t < pre[hi]
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (pre[mid] <= t) lo = mid;
-    else hi = mid;
+// Tensor maps of the grouped-row operand (Xp for GEMM 1, h for GEMM 2): the
+// same [n][K] matrix with boxes of 128, 64, 32 and 16 rows x 64 K.
+struct RowMaps {
+  CUtensorMap m[4];
+};
+
+// Load r rows (a multiple of 16, at most 128) from row `row`, K columns kc .. kc+63, into dst:
+// 128 rows in one box, fewer as 64 + 32 + 16 (rows of 128 B, so every piece starts on a 1 KB
+// swizzle group).
+__device__ __forceinline__ void load_rows(unsigned char* dst, const RowMaps& mx, uint32_t cbar, int kc, int row,
+                                          int r) {
+  if (r == kPTBox) {
+    tma_load_3d_pair(dst, &mx.m[0], cbar, kc, row, 0);
+    return;
   }
-  li = lo;
-  const int local = t - pre[lo];
-  m = local / nf;
-  ft = local - m * nf;
+  int d = 0;
+  if (r & 64) {
+    tma_load_3d_pair(dst, &mx.m[1], cbar, kc, row, 0);
+    d = 64;
+  }
+  if (r & 32) {
+    tma_load_3d_pair(dst + d * 128, &mx.m[2], cbar, kc, row + d, 0);
+    d += 32;
+  }
+  if (r & 16) tma_load_3d_pair(dst + d * 128, &mx.m[3], cbar, kc, row + d, 0);
 }
+
+// Tile t of the launch: token tile tt[t / nf] (expert list index and 256-row tile), feature tile
+// t % nf.
+__device__ __forceinline__ void tile_of(const int* tt, int t, int nf, int& li, int& m, int& ft) {
+  const int i = t / nf;
+  ft = t - i * nf;
+  const int p = tt[i];
+  li = p & (kMaxE - 1);
+  m = p >> 10;
+}
+static_assert(kMaxE == 1024, "token-tile entries pack the list index in 10 bits");
 
 template <int kMode>
 __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const PrefillArgs a,
-                                                                    const __grid_constant__ CUtensorMap mapX,
+                                                                    const __grid_constant__ RowMaps mapX,
                                                                     const __grid_constant__ CUtensorMap mapW) {
+  using G = PGeo<kMode>;
   extern __shared__ __align__(16) unsigned char psm_raw[];
   unsigned char* psm =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(psm_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(psm + kPStages * kPStageBytes);
-  uint64_t* empty = full + kPStages;
-  uint64_t* tfull = empty + kPStages;
+  uint64_t* full = reinterpret_cast<uint64_t*>(psm + G::Stages * G::StageBytes);
+  uint64_t* empty = full + G::Stages;
+  uint64_t* tfull = empty + G::Stages;
   uint64_t* tempty = tfull + 2;
   uint64_t* done = tempty + 2;
-  // after the barrier words: per epilogue warp a 4 KB staging tile and a 2 KB exchange buffer
-  unsigned char* epi_stage = reinterpret_cast<unsigned char*>(full + kPBarWords);
-  float* epi_x = reinterpret_cast<float*>(epi_stage + 4 * kEpiStageBytes);
+  unsigned char* epi_stage = reinterpret_cast<unsigned char*>(full + kPBarWords);  // 4 KB per epilogue warp
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
-  __shared__ int s_pre[kMaxE + 1];
-  __shared__ int s_total;
+  __shared__ int s_tt[kMaxTT];  // token tiles: (256-row tile << 10) | expert list index
+  __shared__ int s_ntt;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();
   const int cl = (int)cluster_index(), ncl = (int)cluster_count();
-  const int NF = kMode == 0 ? a.I / (2 * 64) : a.H / (2 * kPM);  // pair feature tiles per token tile
+  const int NF = kMode == 0 ? a.I / (2 * kPM) : a.H / (2 * kPM);  // pair feature tiles per token tile
   const int K = kMode == 0 ? a.H : a.I;
-  const int nkb = K / kPK;
-  const int nl = *a.n_list;
+  const int nkb = K / G::K;
+  const int nl = min(*a.n_list, kMaxE);
 
+  // Token-tile list, built by all threads: each expert's row count, an exclusive scan of the tile
+  // counts by warp 0, then each expert's entries.  The ring is not in use yet, so its first bytes
+  // hold the per-expert counts.
+  int* s_cnt = reinterpret_cast<int*>(psm);
+  int* s_pre = s_cnt + kMaxE;
+  for (int li = threadIdx.x; li < nl; li += kPThreads) {
+    const int e = a.list_e[li];
+    const int rows = (e >= 0 && e < a.E) ? a.offset[e + 1] - a.offset[e] : 0;
+    s_cnt[li] = rows > 0 ? (rows + kPT - 1) / kPT : 0;
+  }
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kPStages; ++s) {
+    for (int s = 0; s < G::Stages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
@@ -127,43 +171,60 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const Prefil
     }
     mbar_init(done, 1);
     s_abort = 0;
-    int acc = 0;
-    for (int li = 0; li < nl; ++li) {
-      s_pre[li] = acc;
-      const int e = a.list_e[li];
-      const int rows = (e >= 0 && e < a.E) ? a.offset[e + 1] - a.offset[e] : 0;
-      acc += ((rows + kPT - 1) / kPT) * NF;
-    }
-    s_pre[nl] = acc;
-    s_total = acc;
     mbar_fence_init();
   }
   if (warp == 1) {
     tmem_alloc_pair(&s_tmem, kTmemCols);
     tmem_relinquish_pair();
   }
+  __syncthreads();
+  if (warp == 0) {
+    int carry = 0;
+    for (int base = 0; base < nl; base += 32) {
+      const int li = base + lane;
+      const int c = li < nl ? s_cnt[li] : 0;
+      int incl = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(MOE_FULL_MASK, incl, o);
+        if (lane >= o) incl += v;
+      }
+      if (li < nl) s_pre[li] = carry + incl - c;
+      carry += __shfl_sync(MOE_FULL_MASK, incl, 31);
+    }
+    if (lane == 0) {
+      s_ntt = carry;
+      if (carry > kMaxTT) set_status(a.status, MOE_DEV_BAD_GROUPS);  // the host sized the table for n rows
+    }
+  }
+  __syncthreads();
+  const int ntt = s_ntt <= kMaxTT ? s_ntt : 0;
+  for (int li = threadIdx.x; li < nl; li += kPThreads)
+    for (int m = 0, p = s_pre[li]; m < s_cnt[li] && p + m < ntt; ++m) s_tt[p + m] = (m << 10) | li;
   tc_fence_before();
-  cluster_sync();  // barriers of both CTAs initialised, TMEM allocated on both
+  cluster_sync();  // barriers of both CTAs initialised, TMEM allocated on both, tile list complete
   tc_fence_after();
   const uint32_t tmem = s_tmem;
-  const int total = s_total;
+  const int total = ntt * NF;
   volatile int* abort_flag = &s_abort;
 
   if (warp == 0) {
     if (lane == 0) {
       uint32_t s = 0, use = 0;  // ring position: stage, and how often it has been filled before
-      int last_use[kPStages];
-      for (int i = 0; i < kPStages; ++i) last_use[i] = -1;
+      int last_use[G::Stages];
+      for (int i = 0; i < G::Stages; ++i) last_use[i] = -1;
       bool dead = false;
       for (int t = cl; t < total && !dead; t += ncl) {
         int li, m, ft;
-        find_tile(s_pre, nl, t, NF, li, m, ft);
+        tile_of(s_tt, t, NF, li, m, ft);
         const int e = a.list_e[li];
         const int slot = a.e2s ? a.e2s[e] : e;
         const int row0 = a.offset[e] + m * kPT;
         const int ntok = min(kPT, a.offset[e + 1] - row0);
-        const int rrow = row0 + (int)rank * (((ntok + 31) & ~31) >> 1);  // this CTA's half of the N rows
-        const int watom = kMode == 0 ? 2 * ft + (int)rank : 4 * ft + 2 * (int)rank;
+        const int r = ((ntok + 31) & ~31) >> 1;  // rows per CTA: half the MMA's N
+        const int rrow = row0 + (int)rank * r;    // this CTA's half of the tile's rows
+        const int watom = 4 * ft + 2 * (int)rank;  // this CTA's first 64-feature column atom
+        const uint32_t bytes = 2u * (uint32_t)(G::ABytes + (G::K / 64) * r * 128);  // both CTAs
         for (int kb = 0; kb < nkb; ++kb) {
           if (use > 0 && !mbar_try_wait(&empty[s], (use - 1) & 1u) && !mbar_wait(&empty[s], (use - 1) & 1u)) {
             dead = true;
@@ -171,22 +232,23 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const Prefil
             set_status(a.status, MOE_DEV_TIMEOUT);
             break;
           }
-          unsigned char* st = psm + s * kPStageBytes;
+          unsigned char* st = psm + s * G::StageBytes;
           // rank 0's barrier counts the bytes of both CTAs
-          if (rank == 0) mbar_expect_tx(&full[s], 2 * kPStageBytes);
+          if (rank == 0) mbar_expect_tx(&full[s], bytes);
           const uint32_t fb = mapa_shared(smem_u32(&full[s]), 0);
-          // weights: 128 K rows x this CTA's 128 features (two 64-column swizzle atoms, 16 KB apart)
           if (kMode == 0) {
-            tma_load_4d_pair(st, &mapW, fb, 0, kb * kPK, watom, 3 * slot);              // 64 gate columns
-            tma_load_4d_pair(st + 16384, &mapW, fb, 0, kb * kPK, watom, 3 * slot + 1);  // the same 64 up columns
+            // 64 K rows x this CTA's 128 gate features, then the same 128 up features
+            tma_load_4d_pair(st, &mapW, fb, 0, kb * G::K, watom, 3 * slot);
+            tma_load_4d_pair(st + 16384, &mapW, fb, 0, kb * G::K, watom, 3 * slot + 1);
+            load_rows(st + G::ABytes, mapX, fb, kb * G::K, rrow, r);
           } else {
-            tma_load_4d_pair(st, &mapW, fb, 0, kb * kPK, watom, 3 * slot + 2);
+            // 128 K rows x this CTA's 128 features; the rows' two 64-deep K halves 16 KB apart
+            tma_load_4d_pair(st, &mapW, fb, 0, kb * G::K, watom, 3 * slot + 2);
+            load_rows(st + G::ABytes, mapX, fb, kb * G::K, rrow, r);
+            load_rows(st + G::ABytes + 16384, mapX, fb, kb * G::K + 64, rrow, r);
           }
-          // grouped rows: this CTA's half of the tile, 128 rows x 64 K per box, the stage's two K halves
-          tma_load_3d_pair(st + kPAbytes, &mapX, fb, kb * kPK, rrow, 0);
-          tma_load_3d_pair(st + kPAbytes + 16384, &mapX, fb, kb * kPK + 64, rrow, 0);
           last_use[s] = (int)use;
-          if (++s == kPStages) {
+          if (++s == G::Stages) {
             s = 0;
             ++use;
           }
@@ -194,29 +256,30 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const Prefil
       }
       // after any timeout, rank 0 lets every load of both CTAs land before the CTAs can exit
       if ((dead || *abort_flag) && rank == 0)
-        for (int i = 0; i < kPStages; ++i)
+        for (int i = 0; i < G::Stages; ++i)
           if (last_use[i] >= 0) mbar_wait(&full[i], (uint32_t)last_use[i] & 1u);
     }
   } else if (warp == 1) {
     if (lane == 0 && rank == 0) {
-      // one thread issues every pair MMA; the loop keeps per-K-block work to a barrier test, a fence,
-      // four MMAs and a commit (stage index and phase advance incrementally, descriptors are a base
+      // one thread issues every pair MMA; the loop keeps per-stage work to a barrier test, a fence,
+      // eight MMAs and a commit (stage index and phase advance incrementally, descriptors are a base
       // plus the stage offset)
       const uint32_t sbase = smem_u32(psm);
-      const uint64_t ad0 = smem_desc(sbase, 16384, 1024);            // weights, MN-major
-      const uint64_t bd0 = smem_desc(sbase + kPAbytes, 16, 1024);    // grouped rows, K-major
-      constexpr uint32_t kStageDesc = kPStageBytes >> 4;             // stage stride in descriptor units
+      const uint64_t ad0 = smem_desc(sbase, G::AtomBytes, 1024);        // weights, MN-major
+      const uint64_t bd0 = smem_desc(sbase + G::ABytes, 16, 1024);      // grouped rows, K-major
+      constexpr uint32_t kStageDesc = G::StageBytes >> 4;               // stage stride in descriptor units
+      constexpr uint32_t kAStep = 2048 >> 4, kBStep = 32 >> 4;         // one 16-deep K step
       uint32_t s = 0, ph = 0, tc = 0;
       bool dead = false;
       for (int t = cl; t < total; t += ncl, ++tc) {
         int li, m, ft;
-        find_tile(s_pre, nl, t, NF, li, m, ft);
+        tile_of(s_tt, t, NF, li, m, ft);
         const int e = a.list_e[li];
         const int ntok = min(kPT, a.offset[e + 1] - a.offset[e] - m * kPT);
         // D^T = W^T X^T: M = 256 features (A MN-major, 128 per CTA), N = the tile's rows rounded up
         // to 32 (B K-major, half per CTA)
         const uint32_t idesc = idesc_bf16(2 * kPM, (ntok + 31) & ~31, 1, 0);
-        const uint32_t acc = tc & 1u, ause = tc >> 1;
+        const uint32_t acc = tc % G::Acc, ause = tc / G::Acc;
         if (ause > 0 && !dead && !mbar_wait(&tempty[acc], (ause - 1) & 1u)) {
           dead = true;
           *abort_flag = 1;
@@ -233,12 +296,18 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const Prefil
           tc_fence_after();
           if (!dead) {
             const uint64_t so = (uint64_t)(s * kStageDesc);
-            // K 0..63 from the first K half of the rows, K 64..127 from the second (16 KB further)
-            umma_f16_pair_k64(d, ad0 + so, bd0 + so, idesc, kb != 0, 2048 >> 4, 32 >> 4);
-            umma_f16_pair_k64(d, ad0 + so + 4 * (2048 >> 4), bd0 + so + (16384 >> 4), idesc, 1, 2048 >> 4, 32 >> 4);
+            if (kMode == 0) {
+              // gate accumulator in columns 0..255, up accumulator in 256..511
+              umma_f16_pair_k64(d, ad0 + so, bd0 + so, idesc, kb != 0, kAStep, kBStep);
+              umma_f16_pair_k64(d + kPT, ad0 + so + (16384 >> 4), bd0 + so, idesc, kb != 0, kAStep, kBStep);
+            } else {
+              // K 0..63 from the first K half of the rows, K 64..127 from the second (16 KB further)
+              umma_f16_pair_k64(d, ad0 + so, bd0 + so, idesc, kb != 0, kAStep, kBStep);
+              umma_f16_pair_k64(d, ad0 + so + 4 * kAStep, bd0 + so + (16384 >> 4), idesc, 1, kAStep, kBStep);
+            }
           }
           umma_commit_pair(&empty[s]);  // frees stage s in both CTAs
-          if (++s == kPStages) {
+          if (++s == G::Stages) {
             s = 0;
             ph ^= 1u;
           }
@@ -258,59 +327,47 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const Prefil
     unsigned char* stage = epi_stage + q * kEpiStageBytes;  // this warp's [32 rows][32 features]
     const uint32_t tempty_c0 = mapa_shared(smem_u32(&tempty[0]), 0);
     const uint32_t tempty_c1 = mapa_shared(smem_u32(&tempty[1]), 0);
+    const int f0 = kPM * (int)rank + 32 * q;  // this warp's first feature within the pair's 256
     uint32_t tc = 0;
     for (int t = cl; t < total; t += ncl, ++tc) {
       int li, m, ft;
-      find_tile(s_pre, nl, t, NF, li, m, ft);
+      tile_of(s_tt, t, NF, li, m, ft);
       const int e = a.list_e[li];
       const int ntok = min(kPT, a.offset[e + 1] - a.offset[e] - m * kPT);
       const size_t p0 = (size_t)a.offset[e] + m * kPT;
-      const uint32_t acc = tc & 1u, ause = tc >> 1;
+      const uint32_t acc = tc % G::Acc, ause = tc / G::Acc;
       if (!*abort_flag && !mbar_wait(&tfull[acc], ause & 1u)) {
         *abort_flag = 1;
         set_status(a.status, MOE_DEV_TIMEOUT);
       }
       tc_fence_after();
       const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + acc * kPT;
-      // the chunk count depends on the tile alone, so both warps of a pair take the same barriers
       const int nch = (ntok + 31) >> 5;
+      const int col0 = ft * 2 * kPM + f0;  // output column of lane 0's feature
       if (kMode == 0) {
-        // pair p = q & 1: warp q = p holds the gate values of features f0 + lane, warp q = p + 2 the
-        // same features' up values.  Each hands the other the half it does not compute (gate warp:
-        // rows 16..31 of the chunk, up warp: rows 0..15) and computes h for its own 16 rows.
-        const int p = q & 1, role = q >> 1;
-        float* xmine = epi_x + q * kEpiXFloats;
-        const float* xother = epi_x + (q ^ 2) * kEpiXFloats;
+        // lane = feature: its gate values in accumulator 0, its up values in accumulator 1
         uint16_t* st16 = reinterpret_cast<uint16_t*>(stage);
-        const int f0 = ft * 128 + 64 * (int)rank + 32 * p;
 #pragma unroll 1
         for (int c = 0; c < nch; ++c) {
-          float v[32];
-          tmem_ld32(taddr + 32 * c, v);
+          float g[32], u[32];
+          tmem_ld32(taddr + 32 * c, g);
+          tmem_ld32(taddr + kPT + 32 * c, u);
           tmem_ld_wait();
 #pragma unroll
-          for (int j = 0; j < 16; ++j) xmine[j * 32 + lane] = v[role == 0 ? 16 + j : j];
-          named_sync(1 + p, 64);
+          for (int j = 0; j < 32; ++j) st16[j * 32 + lane] = f32_to_bf16(__fdividef(g[j], 1.f + __expf(-g[j])) * u[j]);
+          __syncwarp();
+          const bool store = !*abort_flag;
+          // 32 rows x 64 B: four 16-byte pieces per lane
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float o = xother[j * 32 + lane];
-            const float g = role == 0 ? v[j] : o, u = role == 0 ? o : v[16 + j];
-            st16[j * 32 + lane] = f32_to_bf16(__fdividef(g, 1.f + __expf(-g)) * u);
+          for (int i = 0; i < 4; ++i) {
+            const int idx = i * 32 + lane, r = idx >> 2, seg = idx & 3;
+            const int tok = 32 * c + r;
+            const uint4 val = *reinterpret_cast<const uint4*>(st16 + r * 32 + seg * 8);
+            if (store && tok < ntok) *reinterpret_cast<uint4*>(a.hb + (p0 + tok) * a.I + col0 + seg * 8) = val;
           }
           __syncwarp();
-          // 16 rows x 64 B: two 16-byte pieces per lane
-#pragma unroll
-          for (int i = 0; i < 2; ++i) {
-            const int idx = i * 32 + lane, r = idx >> 2, seg = idx & 3;
-            const int tok = 32 * c + 16 * role + r;
-            const uint4 val = *reinterpret_cast<const uint4*>(st16 + r * 32 + seg * 8);
-            if (tok < ntok && !*abort_flag)
-              *reinterpret_cast<uint4*>(a.hb + (p0 + tok) * a.I + f0 + seg * 8) = val;
-          }
-          named_sync(1 + p, 64);  // both warps are done with the exchange and staging buffers
         }
       } else {
-        const int o0 = ft * 2 * kPM + kPM * (int)rank + 32 * q;
 #pragma unroll 1
         for (int c = 0; c < nch; ++c) {
           float v[32];
@@ -328,7 +385,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const Prefil
               const int idx = i * 32 + lane, r = idx >> 2, seg = idx & 3;
               const int tok = 32 * c + r;
               const uint4 val = *reinterpret_cast<const uint4*>(st16 + r * 32 + seg * 8);
-              if (store && tok < ntok) *reinterpret_cast<uint4*>(a.yb + (p0 + tok) * a.H + o0 + seg * 8) = val;
+              if (store && tok < ntok) *reinterpret_cast<uint4*>(a.yb + (p0 + tok) * a.H + col0 + seg * 8) = val;
             }
           } else {
             float* st32 = reinterpret_cast<float*>(stage);
@@ -341,7 +398,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const Prefil
               const int idx = i * 32 + lane, r = idx >> 3, seg = idx & 7;
               const int tok = 32 * c + r;
               const uint4 val = *reinterpret_cast<const uint4*>(st32 + r * 32 + seg * 4);
-              if (store && tok < ntok) *reinterpret_cast<uint4*>(a.y + (p0 + tok) * a.H + o0 + seg * 4) = val;
+              if (store && tok < ntok) *reinterpret_cast<uint4*>(a.y + (p0 + tok) * a.H + col0 + seg * 4) = val;
             }
           }
           __syncwarp();
@@ -387,14 +444,17 @@ int launch_gather_rows(const uint16_t* x, const int32_t* rows, int n, int H, int
   return MOE_OK;
 }
 
+template <int kMode>
 static size_t prefill_smem_bytes() {
-  return 1024 + (size_t)kPStages * kPStageBytes + kPBarWords * sizeof(uint64_t) + 4 * kEpiStageBytes +
-         4 * kEpiXFloats * sizeof(float);
+  using G = PGeo<kMode>;
+  return 1024 + (size_t)G::Stages * G::StageBytes + kPBarWords * sizeof(uint64_t) + 4 * kEpiStageBytes;
 }
 
 bool prefill_eligible(const FfnArgs& a, int n) {
-  return a.pool_only && a.S > 0 && a.xp && a.hb && n >= kPrefillMinRows && a.H % (2 * kPM) == 0 && a.I % 128 == 0 && a.H % kPK == 0 && a.I % kPK == 0 &&
-         a.E <= kMaxE;
+  // features in whole pair tiles (256 h features in GEMM 1, 256 outputs in GEMM 2), K in whole
+  // stages, and a token-tile list that fits the kernel's table
+  return a.pool_only && a.S > 0 && a.xp && a.hb && n >= kPrefillMinRows && a.H % (2 * kPM) == 0 &&
+         a.I % (2 * kPM) == 0 && a.E <= kMaxE && (int64_t)n / kPT + a.E <= kMaxTT;
 }
 
 size_t prefill_extra_bytes(int n, int H, int I) {
@@ -402,38 +462,41 @@ size_t prefill_extra_bytes(int n, int H, int I) {
   return (size_t)n * H * 2 + (size_t)n * I * 2 + 512;
 }
 
+// The four row maps (boxes of 128, 64, 32, 16 rows x 64 K) of a bf16 [n][K] matrix.
+static int encode_row_maps(RowMaps* rm, const void* base, int n, int K) {
+  const uint64_t d[3] = {(uint64_t)K, (uint64_t)n, 1};
+  const uint64_t s[2] = {(uint64_t)K * 2, (uint64_t)n * K * 2};
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t b[3] = {64, (uint32_t)(kPTBox >> i), 1};  // 64 K = one 128-byte swizzle row
+    if (encode_tmap_3d_bf16(&rm->m[i], base, d, s, b, CU_TENSOR_MAP_SWIZZLE_128B) != MOE_OK) return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}
+
 int launch_prefill(const FfnArgs& a, int n, int max_list, cudaStream_t stream, Prof* prof) {
   static bool done0[64] = {}, done1[64] = {};
-  MOE_CUDA_TRY(ensure_smem(prefill_gemm_kernel<0>, (int)prefill_smem_bytes(), done0));
-  MOE_CUDA_TRY(ensure_smem(prefill_gemm_kernel<1>, (int)prefill_smem_bytes(), done1));
+  MOE_CUDA_TRY(ensure_smem(prefill_gemm_kernel<0>, (int)prefill_smem_bytes<0>(), done0));
+  MOE_CUDA_TRY(ensure_smem(prefill_gemm_kernel<1>, (int)prefill_smem_bytes<1>(), done1));
   int dev = 0, sms = 0;
   MOE_CUDA_TRY(cudaGetDevice(&dev));
   MOE_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
   const size_t mat = (size_t)a.H * a.I;
-  CUtensorMap mx, mh, mgu, md;
-  {
-    const uint64_t d[3] = {(uint64_t)a.H, (uint64_t)n, 1};
-    const uint64_t s[2] = {(uint64_t)a.H * 2, (uint64_t)n * a.H * 2};
-    const uint32_t b[3] = {64, kPTBox, 1};  // 64 K = one 128-byte swizzle row
-    if (encode_tmap_3d_bf16(&mx, a.xp, d, s, b, CU_TENSOR_MAP_SWIZZLE_128B) != MOE_OK) return MOE_ERR_CUDA;
-  }
-  {
-    const uint64_t d[3] = {(uint64_t)a.I, (uint64_t)n, 1};
-    const uint64_t s[2] = {(uint64_t)a.I * 2, (uint64_t)n * a.I * 2};
-    const uint32_t b[3] = {64, kPTBox, 1};
-    if (encode_tmap_3d_bf16(&mh, a.hb, d, s, b, CU_TENSOR_MAP_SWIZZLE_128B) != MOE_OK) return MOE_ERR_CUDA;
-  }
-  // weight matrices viewed as [matrix][64-column atom][K row][64 columns]
+  RowMaps mx, mh;
+  CUtensorMap mgu, md;
+  if (encode_row_maps(&mx, a.xp, n, a.H) != MOE_OK) return MOE_ERR_CUDA;
+  if (encode_row_maps(&mh, a.hb, n, a.I) != MOE_OK) return MOE_ERR_CUDA;
+  // weight matrices viewed as [matrix][64-column atom][K row][64 columns]; a box is one stage's
+  // K rows x two atoms (this CTA's 128 features)
   {
     const uint64_t d[4] = {64, (uint64_t)a.H, (uint64_t)a.I / 64, 3ull * a.S};
     const uint64_t s[3] = {(uint64_t)a.I * 2, 128, mat * 2};
-    const uint32_t b[4] = {64, kPK, 1, 1};  // one 64-column atom: the gate or the up half of a tile
+    const uint32_t b[4] = {64, (uint32_t)PGeo<0>::K, kPM / 64, 1};
     if (encode_tmap_bf16(&mgu, a.pool, 4, d, s, b, CU_TENSOR_MAP_SWIZZLE_128B) != MOE_OK) return MOE_ERR_CUDA;
   }
   {
     const uint64_t d[4] = {64, (uint64_t)a.I, (uint64_t)a.H / 64, 3ull * a.S};
     const uint64_t s[3] = {(uint64_t)a.H * 2, 128, mat * 2};
-    const uint32_t b[4] = {64, kPK, kPM / 64, 1};
+    const uint32_t b[4] = {64, (uint32_t)PGeo<1>::K, kPM / 64, 1};
     if (encode_tmap_bf16(&md, a.pool, 4, d, s, b, CU_TENSOR_MAP_SWIZZLE_128B) != MOE_OK) return MOE_ERR_CUDA;
   }
   PrefillArgs p{a.H, a.I, a.E, n, a.offset, a.list_e, a.n_list, a.e2s, a.S, a.hb, a.y, a.status, a.yb};
@@ -446,7 +509,7 @@ int launch_prefill(const FfnArgs& a, int n, int max_list, cudaStream_t stream, P
   attr[0].val.clusterDim.z = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(kPThreads);
-  cfg.dynamicSmemBytes = prefill_smem_bytes();
+  cfg.dynamicSmemBytes = prefill_smem_bytes<0>();
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
@@ -468,6 +531,7 @@ int launch_prefill(const FfnArgs& a, int n, int max_list, cudaStream_t stream, P
   MOE_CUDA_TRY(cudaLaunchKernelEx(&cfg, prefill_gemm_kernel<0>, p, mx, mgu));
   if (prof) prof->end(stream);
   if (prof) prof->begin(MOE_PROF_FFN_DOWN, stream);
+  cfg.dynamicSmemBytes = prefill_smem_bytes<1>();
   MOE_CUDA_TRY(cudaLaunchKernelEx(&cfg, prefill_gemm_kernel<1>, p, mh, md));
   if (prof) prof->end(stream);
   return MOE_OK;

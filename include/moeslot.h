@@ -59,6 +59,7 @@ typedef enum { MOE_MODE_RESIDENT = 0, MOE_MODE_GATHER = 1, MOE_MODE_ZERO_RETURN 
 #define MOE_DEV_BAD_EXPERT 1 /* an expert id outside [0, E) */
 #define MOE_DEV_BAD_SLOT 2   /* a slot id outside [0, S) where a slot was required */
 #define MOE_DEV_TIMEOUT 3    /* a kernel gave up waiting for its own asynchronous copies */
+#define MOE_DEV_BAD_GROUPS 4 /* group offsets that do not add up to the routed rows (more tiles than rows) */
 
 const char* moe_status_str(int status);
 
