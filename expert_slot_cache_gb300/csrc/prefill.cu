@@ -49,24 +49,27 @@ namespace moe {
 constexpr int kPM = 128;     // weight features per CTA (the pair's MMA M is 256)
 constexpr int kPT = 256;     // grouped rows per tile, at most (MMA N)
 constexpr int kPTBox = 128;  // grouped rows per CTA and tile, at most
-constexpr int kPThreads = 192;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kPBarWords = 32;  // mbarriers: full / empty per stage, two accumulators, done
 constexpr int kPrefillMinRows = 4096;
 constexpr int kMaxTT = 2048;    // token tiles per launch
-constexpr int kEpiStageBytes = 32 * 32 * 4;  // per epilogue warp: 32 rows x 32 features (fp32 at most)
 
-// Ring geometry.  GEMM 1: a 64-deep stage holds 128 gate and the same 128 up
-// features (2 x 16 KB) and up to 128 rows (16 KB).  GEMM 2: a 128-deep stage
-// holds 128 features (32 KB) and up to 128 rows in two 64-deep halves (32 KB).
+// Ring geometry.  GEMM 1: a 64-deep stage holds 128 gate and the same 128 up features (2 x 16 KB)
+// and up to 128 rows (16 KB).  GEMM 2: a 128-deep stage holds 128 features (32 KB) and up to 128
+// rows in two 64-deep halves (32 KB).  GEMM 1 drains its tile with eight epilogue warps (two per
+// TMEM lane quarter, alternate 32-row chunks), as that drain is not overlapped with the next
+// tile's MMAs; GEMM 2 with four.
 template <int kMode>
 struct PGeo {
   static constexpr int K = kMode == 0 ? 64 : 128;        // K depth of a stage
   static constexpr int Stages = kMode == 0 ? 4 : 3;
-  static constexpr int ABytes = 32768;
+  static constexpr int ABytes = (kMode == 0 ? 2 : 1) * kPM * K * 2;
   static constexpr int StageBytes = ABytes + kPTBox * K * 2;
   static constexpr int Acc = kMode == 0 ? 1 : 2;         // accumulator buffers
   static constexpr uint32_t AtomBytes = 64 * K * 2;      // one 64-feature column atom of a stage
+  static constexpr int EpiWarps = kMode == 0 ? 8 : 4;
+  static constexpr int Threads = 64 + 32 * EpiWarps;
+  static constexpr int EpiBytes = kMode == 0 ? 32 * 32 * 2 : 32 * 32 * 4;  // staging per epilogue warp
 };
 
 __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
@@ -125,7 +128,7 @@ __device__ __forceinline__ void tile_of(const int* tt, int t, int nf, int& li, i
 static_assert(kMaxE == 1024, "token-tile entries pack the list index in 10 bits");
 
 template <int kMode>
-__global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const PrefillArgs a,
+__global__ void __launch_bounds__(PGeo<kMode>::Threads, 1) prefill_gemm_kernel(const PrefillArgs a,
                                                                     const __grid_constant__ RowMaps mapX,
                                                                     const __grid_constant__ CUtensorMap mapW) {
   using G = PGeo<kMode>;
@@ -137,7 +140,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const Prefil
   uint64_t* tfull = empty + G::Stages;
   uint64_t* tempty = tfull + 2;
   uint64_t* done = tempty + 2;
-  unsigned char* epi_stage = reinterpret_cast<unsigned char*>(full + kPBarWords);  // 4 KB per epilogue warp
+  unsigned char* epi_stage = reinterpret_cast<unsigned char*>(full + kPBarWords);  // G::EpiBytes per epilogue warp
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   __shared__ int s_tt[kMaxTT];  // token tiles: (256-row tile << 10) | expert list index
@@ -155,7 +158,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const Prefil
   // hold the per-expert counts.
   int* s_cnt = reinterpret_cast<int*>(psm);
   int* s_pre = s_cnt + kMaxE;
-  for (int li = threadIdx.x; li < nl; li += kPThreads) {
+  for (int li = threadIdx.x; li < nl; li += G::Threads) {
     const int e = a.list_e[li];
     const int rows = (e >= 0 && e < a.E) ? a.offset[e + 1] - a.offset[e] : 0;
     s_cnt[li] = rows > 0 ? (rows + kPT - 1) / kPT : 0;
@@ -167,7 +170,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const Prefil
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&tfull[s], 1);
-      mbar_init(&tempty[s], 8);  // the epilogue warps of both CTAs
+      mbar_init(&tempty[s], 2 * G::EpiWarps);  // the epilogue warps of both CTAs
     }
     mbar_init(done, 1);
     s_abort = 0;
@@ -199,7 +202,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const Prefil
   }
   __syncthreads();
   const int ntt = s_ntt <= kMaxTT ? s_ntt : 0;
-  for (int li = threadIdx.x; li < nl; li += kPThreads)
+  for (int li = threadIdx.x; li < nl; li += G::Threads)
     for (int m = 0, p = s_pre[li]; m < s_cnt[li] && p + m < ntt; ++m) s_tt[p + m] = (m << 10) | li;
   tc_fence_before();
   cluster_sync();  // barriers of both CTAs initialised, TMEM allocated on both, tile list complete
@@ -323,8 +326,8 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const Prefil
     // 128, one grouped row per TMEM column (all N rows of the tile, in both CTAs).  A chunk is 32
     // rows: TMEM -> registers, transposed through shared memory into rows of 32 features, then
     // stored as 16-byte pieces of the output rows.
-    const int q = warp & 3;
-    unsigned char* stage = epi_stage + q * kEpiStageBytes;  // this warp's [32 rows][32 features]
+    const int q = warp & 3, half = (warp - 2) >> 2;  // lane quarter; which alternate chunks (GEMM 1)
+    unsigned char* stage = epi_stage + (warp - 2) * G::EpiBytes;  // this warp's [32 rows][32 features]
     const uint32_t tempty_c0 = mapa_shared(smem_u32(&tempty[0]), 0);
     const uint32_t tempty_c1 = mapa_shared(smem_u32(&tempty[1]), 0);
     const int f0 = kPM * (int)rank + 32 * q;  // this warp's first feature within the pair's 256
@@ -348,7 +351,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const Prefil
         // lane = feature: its gate values in accumulator 0, its up values in accumulator 1
         uint16_t* st16 = reinterpret_cast<uint16_t*>(stage);
 #pragma unroll 1
-        for (int c = 0; c < nch; ++c) {
+        for (int c = half; c < nch; c += 2) {
           float g[32], u[32];
           tmem_ld32(taddr + 32 * c, g);
           tmem_ld32(taddr + kPT + 32 * c, u);
@@ -447,7 +450,7 @@ int launch_gather_rows(const uint16_t* x, const int32_t* rows, int n, int H, int
 template <int kMode>
 static size_t prefill_smem_bytes() {
   using G = PGeo<kMode>;
-  return 1024 + (size_t)G::Stages * G::StageBytes + kPBarWords * sizeof(uint64_t) + 4 * kEpiStageBytes;
+  return 1024 + (size_t)G::Stages * G::StageBytes + kPBarWords * sizeof(uint64_t) + (size_t)G::EpiWarps * G::EpiBytes;
 }
 
 bool prefill_eligible(const FfnArgs& a, int n) {
@@ -508,7 +511,7 @@ int launch_prefill(const FfnArgs& a, int n, int max_list, cudaStream_t stream, P
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.blockDim = dim3(kPThreads);
+  cfg.blockDim = dim3(PGeo<0>::Threads);
   cfg.dynamicSmemBytes = prefill_smem_bytes<0>();
   cfg.stream = stream;
   cfg.attrs = attr;
@@ -532,6 +535,7 @@ int launch_prefill(const FfnArgs& a, int n, int max_list, cudaStream_t stream, P
   if (prof) prof->end(stream);
   if (prof) prof->begin(MOE_PROF_FFN_DOWN, stream);
   cfg.dynamicSmemBytes = prefill_smem_bytes<1>();
+  cfg.blockDim = dim3(PGeo<1>::Threads);
   MOE_CUDA_TRY(cudaLaunchKernelEx(&cfg, prefill_gemm_kernel<1>, p, mh, md));
   if (prof) prof->end(stream);
   return MOE_OK;
