@@ -555,8 +555,9 @@ int launch_ffn(const FfnArgs& a, int max_list, cudaStream_t stream, Prof* prof) 
 // ---------------------------------------------------------------------------
 constexpr int kCombThreads = 128;
 
-// Combine over CPT columns per thread (4 from fp32 y, 8 from bf16 y: one 16-byte load per row either way).
-template <int CPT>
+// Combine over CPT columns per thread (4 from fp32 y, 8 from bf16 y: one 16-byte load per row either way),
+// for k <= KM (the per-row registers are sized by KM, so k <= 8 keeps twice as many threads resident).
+template <int CPT, int KM>
 __global__ void __launch_bounds__(kCombThreads) combine_kernel(const float* __restrict__ y, const float* __restrict__ w,
                                                                const int32_t* __restrict__ pos,
                                                                const int32_t* __restrict__ ids,
@@ -571,11 +572,11 @@ __global__ void __launch_bounds__(kCombThreads) combine_kernel(const float* __re
   const int c = (blockIdx.y * kCombThreads + threadIdx.x) * CPT;
   if (c >= H) return;
   // all k rows first (independent loads), then the sum in j order
-  uint4 raw[kMaxK];
-  float wj[kMaxK];
-  bool res[kMaxK], have[kMaxK];
+  uint4 raw[KM];
+  float wj[KM];
+  bool res[KM], have[KM];
 #pragma unroll
-  for (int j = 0; j < kMaxK; ++j) {
+  for (int j = 0; j < KM; ++j) {
     have[j] = false;
     res[j] = true;
     wj[j] = 0.f;
@@ -597,7 +598,7 @@ __global__ void __launch_bounds__(kCombThreads) combine_kernel(const float* __re
 #pragma unroll
   for (int q = 0; q < CPT; ++q) acc[q] = accm[q] = 0.f;
 #pragma unroll
-  for (int j = 0; j < kMaxK; ++j) {
+  for (int j = 0; j < KM; ++j) {
     if (j < k && have[j]) {
       float v[CPT];
       if (CPT == 8) {
@@ -636,14 +637,23 @@ __global__ void __launch_bounds__(kCombThreads) combine_kernel(const float* __re
 int launch_combine(const float* y, const float* w, const int32_t* pos, const int32_t* ids, const int32_t* e2s, int T,
                    int k, int H, int E, int split, void* out, float* out_res, float* out_miss, cudaStream_t stream,
                    const uint16_t* yb) {
+  const bool k8 = k <= 8;
   if (yb) {
     const dim3 grid(T, (H / 8 + kCombThreads - 1) / kCombThreads);
-    MOE_CUDA_TRY(launch_pdl(combine_kernel<8>, grid, dim3(kCombThreads), 0, stream, y, w, pos, ids, e2s, k, H, E, split,
-                            (uint16_t*)out, out_res, out_miss, yb));
+    if (k8)
+      MOE_CUDA_TRY(launch_pdl(combine_kernel<8, 8>, grid, dim3(kCombThreads), 0, stream, y, w, pos, ids, e2s, k, H, E,
+                              split, (uint16_t*)out, out_res, out_miss, yb));
+    else
+      MOE_CUDA_TRY(launch_pdl(combine_kernel<8, kMaxK>, grid, dim3(kCombThreads), 0, stream, y, w, pos, ids, e2s, k, H,
+                              E, split, (uint16_t*)out, out_res, out_miss, yb));
   } else {
     const dim3 grid(T, (H / 4 + kCombThreads - 1) / kCombThreads);
-    MOE_CUDA_TRY(launch_pdl(combine_kernel<4>, grid, dim3(kCombThreads), 0, stream, y, w, pos, ids, e2s, k, H, E, split,
-                            (uint16_t*)out, out_res, out_miss, (const uint16_t*)nullptr));
+    if (k8)
+      MOE_CUDA_TRY(launch_pdl(combine_kernel<4, 8>, grid, dim3(kCombThreads), 0, stream, y, w, pos, ids, e2s, k, H, E,
+                              split, (uint16_t*)out, out_res, out_miss, (const uint16_t*)nullptr));
+    else
+      MOE_CUDA_TRY(launch_pdl(combine_kernel<4, kMaxK>, grid, dim3(kCombThreads), 0, stream, y, w, pos, ids, e2s, k, H,
+                              E, split, (uint16_t*)out, out_res, out_miss, (const uint16_t*)nullptr));
   }
   MOE_LAUNCH_CHECK();
   return MOE_OK;

@@ -349,18 +349,15 @@ __global__ void __launch_bounds__(kTileThreads) logits_tile_kernel(const uint16_
 }
 
 // logits_full_kernel (many tokens): CTA = 64 tokens x 64 experts over all of
-// H, 128 threads, writing the final logits (no block parts in global memory).
+// H, 256 threads, writing the final logits (no block parts in global memory).
 // Each 128-row block's bf16 tiles are copied with cp.async while the block
 // before is computed (two staging buffers), converted to fp32 in shared memory
 // (x token-minor, Wr expert-minor), then thread (tx, ty) runs, for experts
 // 4tx..4tx+3 and tokens 4ty..4ty+3, one fma chain per logit over the block's
-// rows in order from 0 (packed fp32 pairs along the tokens; the next row's
-// operands are loaded while the current row's 8 packed fmas issue) and adds
-// each chain to the logit's running sum in block order: the same arithmetic,
-// in the same order, as the block parts summed by topk_kernel.  One CTA per
-// SM (128 of them fill the GPU at T = 4096, E = 128) with 8 warps, two per SM
-// sub-partition, so that one warp's shared-memory and fma latencies overlap
-// the other's.
+// rows in order from 0 (operands read four rows at a time) and adds each chain
+// to the logit's running sum in block order: the same arithmetic, in the same
+// order, as the block parts summed by topk_kernel.  One CTA per SM (128 of
+// them at T = 4096, E = 128) with 8 warps, two per SM sub-partition.
 constexpr int kFullThreads = 256;
 constexpr int kFullXRow = kHC + 8;  // bf16 staging row of x, padded against bank conflicts in the conversion
 constexpr int kFullStage = kTT * kFullXRow + kHC * kTE;  // bf16 elements per staging buffer
@@ -400,7 +397,10 @@ __global__ void __launch_bounds__(kFullThreads) logits_full_kernel(const uint16_
   cp_async_commit();
   if (nblk > 1) issue(1, 1);
   cp_async_commit();
-  const int tx = tid & 15, ty = tid >> 4;
+  // warp = 8 expert quads x 4 token quads: a row's operands are one 128-byte and one 64-byte
+  // shared-memory read per warp
+  const int lane = tid & 31, warp = tid >> 5;
+  const int tx = (lane & 7) + 8 * (warp & 1), ty = (lane >> 3) + 4 * (warp >> 1);
   float total[4][4];  // [expert 4tx + i][token 4ty + t]
 #pragma unroll
   for (int i = 0; i < 4; ++i)
@@ -437,37 +437,36 @@ __global__ void __launch_bounds__(kFullThreads) logits_full_kernel(const uint16_
     __syncthreads();  // the fp32 tiles are complete, and staging buffer b & 1 is free again
     if (b + 2 < nblk) issue(b + 2, b & 1);
     cp_async_commit();
-    // chains over the block: acc[i][p] holds tokens (4ty + 2p, 4ty + 2p + 1) of expert 4tx + i
-    uint64_t acc[4][2];
+    // chains over the block: acc[i][t] = fma chain of expert 4tx + i and token 4ty + t, rows in
+    // order; four rows of operands are read before their 64 fmas
+    float acc[4][4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) acc[i][0] = acc[i][1] = 0ull;
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int t = 0; t < 4; ++t) acc[i][t] = 0.f;
     const float* wrow = wf + 4 * tx;
     const float* xrow = xf + 4 * ty;
-    float4 wv = *reinterpret_cast<const float4*>(wrow);
-    ulonglong2 xa = *reinterpret_cast<const ulonglong2*>(xrow);
-#pragma unroll 4
-    for (int h = 0; h < hn; ++h) {
-      // the next row's operands (row kHC - 1 again after the last row: in bounds, unused)
-      const int hh = min(h + 1, kHC - 1);
-      const float4 wv1 = *reinterpret_cast<const float4*>(wrow + hh * kTE);
-      const ulonglong2 xa1 = *reinterpret_cast<const ulonglong2*>(xrow + hh * kTT);
-      const uint64_t ww[4] = {rf2_pack(wv.x, wv.x), rf2_pack(wv.y, wv.y), rf2_pack(wv.z, wv.z), rf2_pack(wv.w, wv.w)};
+#pragma unroll 1
+    for (int h = 0; h < hn; h += 4) {  // hn is a multiple of 8
+      float4 wv[4], xv[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        rf2_fma(acc[i][0], xa.x, ww[i]);
-        rf2_fma(acc[i][1], xa.y, ww[i]);
+      for (int u = 0; u < 4; ++u) {
+        wv[u] = *reinterpret_cast<const float4*>(wrow + (h + u) * kTE);
+        xv[u] = *reinterpret_cast<const float4*>(xrow + (h + u) * kTT);
       }
-      wv = wv1;
-      xa = xa1;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float w4[4] = {wv[u].x, wv[u].y, wv[u].z, wv[u].w}, x4[4] = {xv[u].x, xv[u].y, xv[u].z, xv[u].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int t = 0; t < 4; ++t) acc[i][t] = fmaf(x4[t], w4[i], acc[i][t]);
+      }
     }
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
-      for (int p = 0; p < 2; ++p) {
-        const float2 c = rf2_unpack(acc[i][p]);
-        total[i][2 * p] = total[i][2 * p] + c.x;
-        total[i][2 * p + 1] = total[i][2 * p + 1] + c.y;
-      }
+      for (int t = 0; t < 4; ++t) total[i][t] = total[i][t] + acc[i][t];
   }
   cp_async_wait<0>();
   const int e = e0 + 4 * tx;
