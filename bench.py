@@ -705,6 +705,8 @@ def main():
         wp = Workload(cp, 2 * 3 + 3, dev)
         rp = time_steps(wp, 3, 3)
         flops = 6.0 * cp.T * cp.k * cp.H * cp.I
+        # unique experts' weights per step, over the instrumented steps the kernel times come from
+        w_bytes = count_unique_all(wp, 3, 3 + 3) * cp.slab_bytes / 3.0
         t_ffn = (rp["kern_ms"]["ffn_gateup"] + rp["kern_ms"]["ffn_down"]) * 1e-3 / 3
         t_layer = rp["ms"] * 1e-3 / 3
         pk = peaks["bf16_tflops"]
@@ -713,6 +715,13 @@ def main():
                                 "ffn_tensor": {"bound": "tensor", "achieved": flops / t_ffn / 1e12, "peak": pk,
                                                "unit": "TFLOP/s", "frac": flops / t_ffn / 1e12 / pk,
                                                "flops_per_step": flops, "kernel": "ffn_gateup+ffn_down (tcgen05)"},
+                                # the same kernels against HBM: each routed expert's weights once per step (about 256
+                                # flop per weight byte, below this part's ridge of bf16 peak / HBM bandwidth)
+                                "ffn_hbm": {"bound": "hbm", "achieved": w_bytes / t_ffn / 1e9, "peak": peaks["hbm_gbs"],
+                                            "unit": "GB/s", "frac": w_bytes / t_ffn / 1e9 / peaks["hbm_gbs"],
+                                            "bytes_per_step": w_bytes, "flop_per_byte": flops / w_bytes,
+                                            "ridge_flop_per_byte": pk * 1e12 / (peaks["hbm_gbs"] * 1e9),
+                                            "kernel": "ffn_gateup+ffn_down (tcgen05)"},
                                 "layer_tflops": flops / t_layer / 1e12}
         del wp
         torch.cuda.empty_cache()
