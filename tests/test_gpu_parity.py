@@ -400,6 +400,23 @@ def test_layer_tiny_resident():
     _run_layer(C.TINY, steps=2)
 
 
+def test_layer_largest_expert_count_and_top_k():
+    """The largest shapes the library takes: E = 1024 experts and top-16, all resident."""
+    _run_layer(C.TINY.with_(E=1024, k=16, S=1024, T=6), steps=2)
+
+
+def test_layer_top_k_equals_expert_count():
+    """Degenerate routing: every token picks every expert (k = E), so top-k is a full sort and each
+    expert's group holds every token."""
+    _run_layer(C.TINY.with_(E=16, k=16, S=16, T=5), steps=2)
+
+
+def test_layer_gather_one_token_per_chunk():
+    """A pool exactly k slots deep: every chunk is one token (floor(S / k) = 1), each managing,
+    gathering and computing on its own; 1024 experts, top-16."""
+    _run_layer(C.TINY.with_(E=1024, k=16, S=16, T=3, mode=C.MODE_GATHER), steps=2)
+
+
 @pytest.mark.parametrize("T", [1, 8, 32, 64])
 def test_layer_qwen_gather_lru(T):
     _run_layer(C.qwen(T), steps=2)
