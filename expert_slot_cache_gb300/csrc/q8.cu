@@ -396,14 +396,16 @@ __global__ void __launch_bounds__(kQRowThreads) q8_reduce_gu_kernel(const FfnArg
   }
 }
 
-// The same reduction with one warp per row (rows pb + w, pb + w + 8, ... of the
-// listed expert), for lists that average two or more rows per expert: an
-// expert's rows proceed in parallel and the row amax is a warp maximum.  I/4
-// quads of a row are spread over the lanes, at most 8 per lane (I <= 1024).
-constexpr int kQWarpQuads = 8;
-__global__ void __launch_bounds__(kQRowThreads) q8_reduce_gu_warp_kernel(
+// The same reduction with an expert's rows four at a time: 64 threads per row, each owning up to
+// four quads of it (I <= 1024), with every part's loads for those quads issued before their adds
+// (four parts a batch), and the row amax from the row's two warps.  All rows of a CTA take the same
+// number of steps, so the block barrier is uniform.
+constexpr int kQRowQuads = 4;   // quads per thread and row
+constexpr int kQPartBatch = 4;  // parts whose loads are in flight together
+__global__ void __launch_bounds__(kQRowThreads, 1) q8_reduce_gu_rows_kernel(
     const FfnArgs a, const int32_t* __restrict__ part, const int32_t* __restrict__ vpre, int NSR, int G, int jcap,
     size_t qslab, const float* __restrict__ sx, int npad, uint32_t* __restrict__ hq, float* __restrict__ sh) {
+  __shared__ float red[kQRowThreads / 32];
   pdl_trigger();
   const int li = blockIdx.x;
   const int n_list = *a.n_list;
@@ -411,11 +413,10 @@ __global__ void __launch_bounds__(kQRowThreads) q8_reduce_gu_warp_kernel(
   const bool ok = li < n_list && stream_slot(a, li, e, slot);
   pdl_wait();
   if (!ok) return;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int nl = min(n_list, kMaxE);
   const int L = stream_len(vpre[nl], NSR, G, jcap);  // vpre: written by the pass before (completed)
   const int v0 = vpre[li];
-  const int n = a.T * a.k, I = a.I, N = 2 * I;
+  const int n = a.T * a.k, I = a.I, N = 2 * I, nq4 = I / 4;
   const size_t mat = (size_t)a.H * I;
   const float* sc = reinterpret_cast<const float*>(reinterpret_cast<const unsigned char*>(a.pool) +
                                                    (size_t)slot * qslab + 3 * mat);
@@ -423,62 +424,83 @@ __global__ void __launch_bounds__(kQRowThreads) q8_reduce_gu_warp_kernel(
   const float* su = sc + I;
   const size_t pstride = (size_t)n * N;
   const int pb = a.offset[e], pe = a.offset[e + 1];
-  for (int p = pb + warp; p < pe; p += kQRowThreads / 32) {
-    const int J = stream_parts(v0 + (p - pb) / kQRB, NSR, L);
-    const float s_x = sx[p];
-    float hv[kQWarpQuads][4];
+  const int grp = threadIdx.x >> 6, t64 = threadIdx.x & 63, w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int p0 = pb; p0 < pe; p0 += kQRowThreads / 64) {
+    const int p = p0 + grp;
+    const bool row = p < pe;
+    float hv[kQRowQuads][4];
     float amax = 0.f;
+    if (row) {
+      const int J = stream_parts(v0 + (p - pb) / kQRB, NSR, L);
+      const float s_x = sx[p];
+      int4 ag[kQRowQuads], au[kQRowQuads];
 #pragma unroll
-    for (int i = 0; i < kQWarpQuads; ++i) {
-      const int q = lane + 32 * i;
-      if (q >= I / 4) break;
-      // exact int32 sums: parts in batches of four loads, added in any order
-      int4 ag = make_int4(0, 0, 0, 0), au = ag;
-      const int32_t* pp = part + (size_t)p * N + 4 * q;
-      for (int j0 = 0; j0 < J; j0 += 4) {
-        int4 tg[4], tu[4];
+      for (int i = 0; i < kQRowQuads; ++i) ag[i] = au[i] = make_int4(0, 0, 0, 0);
+      const int32_t* pp = part + (size_t)p * N + 4 * t64;
+      for (int j0 = 0; j0 < J; j0 += kQPartBatch) {
+        int4 tg[kQRowQuads][kQPartBatch], tu[kQRowQuads][kQPartBatch];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          tg[u] = make_int4(0, 0, 0, 0);
-          tu[u] = tg[u];
-          if (j0 + u < J) {
-            tg[u] = *reinterpret_cast<const int4*>(pp + (size_t)(j0 + u) * pstride);
-            tu[u] = *reinterpret_cast<const int4*>(pp + (size_t)(j0 + u) * pstride + I);
+        for (int i = 0; i < kQRowQuads; ++i)
+#pragma unroll
+          for (int u = 0; u < kQPartBatch; ++u) {
+            tg[i][u] = tu[i][u] = make_int4(0, 0, 0, 0);
+            if (t64 + 64 * i < nq4 && j0 + u < J) {
+              const int32_t* src = pp + (size_t)(j0 + u) * pstride + 256 * i;
+              tg[i][u] = *reinterpret_cast<const int4*>(src);
+              tu[i][u] = *reinterpret_cast<const int4*>(src + I);
+            }
+          }
+#pragma unroll
+        for (int i = 0; i < kQRowQuads; ++i)
+#pragma unroll
+          for (int u = 0; u < kQPartBatch; ++u) {
+            ag[i].x += tg[i][u].x; ag[i].y += tg[i][u].y; ag[i].z += tg[i][u].z; ag[i].w += tg[i][u].w;
+            au[i].x += tu[i][u].x; au[i].y += tu[i][u].y; au[i].z += tu[i][u].z; au[i].w += tu[i][u].w;
+          }
+      }
+#pragma unroll
+      for (int i = 0; i < kQRowQuads; ++i) {
+        const int q = t64 + 64 * i;
+        const int gi[4] = {ag[i].x, ag[i].y, ag[i].z, ag[i].w}, ui[4] = {au[i].x, au[i].y, au[i].z, au[i].w};
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          hv[i][b] = 0.f;
+          if (q < nq4) {
+            const int c = 4 * q + b;
+            const float g = __fmul_rn(__fmul_rn(__int2float_rn(gi[b]), sg[c]), s_x);
+            const float u = __fmul_rn(__fmul_rn(__int2float_rn(ui[b]), su[c]), s_x);
+            const float h = __fmul_rn(silu32_def(g), u);
+            hv[i][b] = h;
+            amax = fmaxf(amax, fabsf(h));
           }
         }
+      }
+    }
+    // the row's amax: its two warps' maxima (every thread reaches both barriers)
+    amax = warp_max(amax);
+    if (lane == 0) red[w] = amax;
+    __syncthreads();
+    amax = fmaxf(red[2 * grp], red[2 * grp + 1]);
+    __syncthreads();  // red is reused by the next rows
+    if (row) {
+      const float s = __fdiv_rn(amax, 127.f);
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          ag.x += tg[u].x; ag.y += tg[u].y; ag.z += tg[u].z; ag.w += tg[u].w;
-          au.x += tu[u].x; au.y += tu[u].y; au.z += tu[u].z; au.w += tu[u].w;
+      for (int i = 0; i < kQRowQuads; ++i) {
+        const int q = t64 + 64 * i;
+        if (q < nq4) {
+          uint32_t pk = 0;
+#pragma unroll
+          for (int b = 0; b < 4; ++b) pk |= (uint32_t)(q8_code(hv[i][b], s) & 0xff) << (8 * b);
+          hq[q8_act_word(q, p, npad)] = pk;
         }
       }
-      const int gi[4] = {ag.x, ag.y, ag.z, ag.w}, ui[4] = {au.x, au.y, au.z, au.w};
-#pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        const int c = 4 * q + b;
-        const float g = __fmul_rn(__fmul_rn(__int2float_rn(gi[b]), sg[c]), s_x);
-        const float u = __fmul_rn(__fmul_rn(__int2float_rn(ui[b]), su[c]), s_x);
-        const float h = __fmul_rn(silu32_def(g), u);
-        hv[i][b] = h;
-        amax = fmaxf(amax, fabsf(h));
-      }
+      if (t64 == 0) sh[p] = s;
     }
-    amax = warp_max(amax);
-    const float s = __fdiv_rn(amax, 127.f);
-#pragma unroll
-    for (int i = 0; i < kQWarpQuads; ++i) {
-      const int q = lane + 32 * i;
-      if (q >= I / 4) break;
-      uint32_t pk = 0;
-#pragma unroll
-      for (int b = 0; b < 4; ++b) pk |= (uint32_t)(q8_code(hv[i][b], s) & 0xff) << (8 * b);
-      hq[q8_act_word(q, p, npad)] = pk;
-    }
-    if (lane == 0) sh[p] = s;
   }
 }
 
-// down: y[p][n] = (float(sum of parts) * sd[n]) * sh[p]; block = 128 columns of one listed expert.
+// down: y[p][n] = (float(sum of parts) * sd[n]) * sh[p]; block = 128 columns of one listed expert.  The
+// block's branch (rows or parts over the warps) depends only on the expert's row count, so it is uniform.
 __global__ void __launch_bounds__(256) q8_reduce_d_kernel(const FfnArgs a, const int32_t* __restrict__ part,
                                                           const int32_t* __restrict__ vpre, int NSR,
                                                           int G, int jcap, size_t qslab,
@@ -501,6 +523,34 @@ __global__ void __launch_bounds__(256) q8_reduce_d_kernel(const FfnArgs a, const
   const int c4 = blockIdx.x * 32 + lane;
   const size_t pstride = (size_t)n * H;
   const int pb = a.offset[e], pe = a.offset[e + 1];
+  if (pe - pb >= 4) {
+    // enough rows to go around: warp w takes rows pb + w, pb + w + 8, ...; a lane adds every part of its
+    // quad, eight parts' loads in flight before their adds (no barriers on this path)
+    if (4 * c4 < H)
+      for (int p = pb + w; p < pe; p += 8) {
+        const int J = stream_parts(v0 + (p - pb) / kQRB, NSR, L);
+        const int32_t* src = part + (size_t)p * H + 4 * c4;
+        int4 acc = make_int4(0, 0, 0, 0);
+        for (int j0 = 0; j0 < J; j0 += 8) {
+          int4 t[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            t[u] = j0 + u < J ? *reinterpret_cast<const int4*>(src + (size_t)(j0 + u) * pstride) : make_int4(0, 0, 0, 0);
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            acc.x += t[u].x; acc.y += t[u].y; acc.z += t[u].z; acc.w += t[u].w;
+          }
+        }
+        const float s = sh[p];
+        const int ai[4] = {acc.x, acc.y, acc.z, acc.w};
+        float o[4];
+#pragma unroll
+        for (int b = 0; b < 4; ++b) o[b] = __fmul_rn(__fmul_rn(__int2float_rn(ai[b]), sd[4 * c4 + b]), s);
+        *reinterpret_cast<float4*>(y + (size_t)p * H + 4 * c4) = make_float4(o[0], o[1], o[2], o[3]);
+      }
+    return;
+  }
+  // few rows: the warps split each row's parts, then warp 0 adds the eight sums
   for (int p = pb; p < pe; ++p) {
     const int J = stream_parts(v0 + (p - pb) / kQRB, NSR, L);
     int4 acc = make_int4(0, 0, 0, 0);
@@ -646,9 +696,9 @@ int launch_ffn_q8(const FfnArgs& a, void* ws, size_t ws_bytes, int max_list, cud
   MOE_CUDA_TRY(launch_pdl(q8_rows_kernel, dim3(n), dim3(kQRowThreads), 0, stream, a.x, a.rows, n, a.H, a.k, c.npad,
                           c.xq, c.sx));
   MOE_CUDA_TRY(q_launch(ffn_q8_kernel<false>, dim3(sms), dim3(g.N / 4 + 32), q_smem(g), stream, true, a, g));
-  // an expert's rows in parallel (one warp each) when the list averages two or more rows per expert
-  const bool warp_rows = n >= 2 * max_list && a.I / 4 <= 32 * kQWarpQuads;
-  MOE_CUDA_TRY(q_launch(warp_rows ? q8_reduce_gu_warp_kernel : q8_reduce_gu_kernel, dim3(max_list), dim3(kQRowThreads),
+  // an expert's rows four at a time when a row fits 64 threads x 4 quads (I <= 1024)
+  const bool rows4 = a.I / 4 <= 64 * kQRowQuads;
+  MOE_CUDA_TRY(q_launch(rows4 ? q8_reduce_gu_rows_kernel : q8_reduce_gu_kernel, dim3(max_list), dim3(kQRowThreads),
                         0, stream, true, a, (const int32_t*)c.gpart, (const int32_t*)c.vpre_g, g.NSR, g.G, g.jcap,
                         g.qslab, (const float*)c.sx, c.npad, c.hq, c.sh));
   if (prof) prof->end(stream);
