@@ -298,8 +298,11 @@ __global__ void __launch_bounds__(kDThreads, 1) ffn_sk_kernel(const FfnArgs a, c
   }
 }
 
-// Adds the parts of each listed expert's rows: warp w sums parts j = w, w+8,
-// ..., then the 8 warp sums are added in warp order (fixed).
+// Adds the parts of each listed expert's rows.  An expert with four or more
+// rows: its rows are spread over the warps and a lane adds its parts in j
+// order.  Fewer rows: warp w sums parts j = w, w+8, ..., then the 8 warp sums
+// are added in warp order.  Either order is fixed, so results do not depend
+// on timing.
 //   SWIGLU: hb [n][I] bf16 = silu(sum g) * (sum u); parts hold [g | u]
 //   else:   y [n][H] fp32 = sum of parts
 // A block covers 128 columns (32 lanes x float4) of one listed expert's rows.
@@ -334,6 +337,45 @@ __global__ void __launch_bounds__(32 * kSkRedWarps) sk_reduce_kernel(const FfnAr
   const int pb = a.offset[e], pe = a.offset[e + 1];
   const size_t pstride = (size_t)n * N;
   pdl_wait();
+  if (pe - pb >= 4) {
+    // enough rows to go around: warp w takes rows pb + w, pb + w + 8, ...; a lane adds its quad's parts in
+    // j order, eight parts' loads in flight before their adds (no barriers on this path; the branch
+    // depends only on the expert's row count, so it is uniform over the block)
+    if (c4 < ncol4)
+      for (int p = pb + w; p < pe; p += kSkRedWarps) {
+        const float* src = part + (size_t)p * N + 4 * c4;
+        float4 g = make_float4(0.f, 0.f, 0.f, 0.f), u = g;
+        for (int j0 = 0; j0 < J; j0 += 8) {
+          float4 tg[8], tu[8];
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj)
+            if (j0 + jj < J) {
+              tg[jj] = *reinterpret_cast<const float4*>(src + (j0 + jj) * pstride);
+              if (SWIGLU) tu[jj] = *reinterpret_cast<const float4*>(src + (j0 + jj) * pstride + ncol);
+            }
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj)
+            if (j0 + jj < J) {
+              g.x += tg[jj].x; g.y += tg[jj].y; g.z += tg[jj].z; g.w += tg[jj].w;
+              if (SWIGLU) {
+                u.x += tu[jj].x; u.y += tu[jj].y; u.z += tu[jj].z; u.w += tu[jj].w;
+              }
+            }
+        }
+        if (SWIGLU) {
+          const float h0 = g.x / (1.f + expf(-g.x)) * u.x, h1 = g.y / (1.f + expf(-g.y)) * u.y;
+          const float h2 = g.z / (1.f + expf(-g.z)) * u.z, h3 = g.w / (1.f + expf(-g.w)) * u.w;
+          uint2 wv;
+          wv.x = uint32_t(f32_to_bf16(h0)) | (uint32_t(f32_to_bf16(h1)) << 16);
+          wv.y = uint32_t(f32_to_bf16(h2)) | (uint32_t(f32_to_bf16(h3)) << 16);
+          *reinterpret_cast<uint2*>(hb + (size_t)p * ncol + 4 * c4) = wv;
+        } else {
+          *reinterpret_cast<float4*>(y + (size_t)p * ncol + 4 * c4) = g;
+        }
+      }
+    return;
+  }
+  // few rows: the warps split each row's parts, then warp 0 adds the eight sums
   for (int p = pb; p < pe; ++p) {
     float4 g = make_float4(0.f, 0.f, 0.f, 0.f), u = g;
     if (c4 < ncol4) {
