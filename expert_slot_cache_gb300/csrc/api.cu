@@ -207,9 +207,13 @@ extern "C" int moe_layer_forward(const moe_layer_args* a, moe_stream_t main_s, m
   if (prof.p) prof.p->used = 0;
   const size_t slab_bytes = a->quant ? q8_slab_bytes_h(H, I) : (size_t)6 * H * I;
   prof.begin(MOE_PROF_ROUTE, ms);
-  int r = moe_route_ex(a->x, a->w_router, a->logit_offset, a->sel_bias, a->affinity != 0.f ? a->e2s : nullptr,
-                       a->affinity, a->route_flags, T, H, E, k, ws.logits,
-                       moe_route_scratch_bytes(T, H, E) ? ws.route : nullptr, a->ids, a->w, main_s);
+  // a one-chunk step: the top-k CTA may group the batch by expert itself (then no permute launch)
+  const PermOut perm0{ws.count, ws.offset, ws.rows, ws.pos, ws.act_e, ws.n_act, a->dev_status};
+  bool grouped = false;
+  int r = route_impl(a->x, a->w_router, a->logit_offset, a->sel_bias, a->affinity != 0.f ? a->e2s : nullptr,
+                     a->affinity, a->route_flags, T, H, E, k, ws.logits,
+                     moe_route_scratch_bytes(T, H, E) ? ws.route : nullptr, a->ids, a->w, ms,
+                     C >= T ? &perm0 : nullptr, &grouped);
   if (r != MOE_OK) return r;
   prof.end(ms);
 
@@ -219,9 +223,11 @@ extern "C" int moe_layer_forward(const moe_layer_args* a, moe_stream_t main_s, m
     const int lmax = std::min(n, E);
     const int32_t* ids_c = a->ids + (size_t)t0 * k;
     prof.begin(MOE_PROF_PERMUTE, ms);
-    r = launch_permute(ids_c, n, E, ws.count, ws.offset, ws.rows, ws.pos, ws.act_e, ws.n_act, a->dev_status, ws.perm,
-                       ms);
-    if (r != MOE_OK) return r;
+    if (!(grouped && t0 == 0)) {
+      r = launch_permute(ids_c, n, E, ws.count, ws.offset, ws.rows, ws.pos, ws.act_e, ws.n_act, a->dev_status, ws.perm,
+                         ms);
+      if (r != MOE_OK) return r;
+    }
     prof.end(ms);
     if (a->window_counts && (r = launch_window_add(ws.count, E, a->window_counts, ms)) != MOE_OK) return r;
     FfnArgs f{(const uint16_t*)a->x + (size_t)t0 * H, tc, H, I, k, E, ws.offset, ws.rows, nullptr, nullptr,

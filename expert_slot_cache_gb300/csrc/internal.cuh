@@ -2,6 +2,7 @@
 #pragma once
 
 #include "common.cuh"
+#include "perm_small.cuh"
 
 namespace moe {
 
@@ -80,6 +81,9 @@ int launch_gather(const void* host_slabs, void* pool, size_t slab_bytes, int E, 
                   cudaStream_t stream);
 int check_host_accessible(const void* p);
 int launch_window_add(const int32_t* count, int E, int32_t* counts, cudaStream_t stream);
+int route_impl(const void* x, const void* w_router, const float* logit_offset, const float* sel_bias,
+               const int32_t* e2s, float affinity, int rflags, int T, int H, int E, int k, float* logits,
+               float* scratch, int32_t* ids, float* w, cudaStream_t stream, const PermOut* perm, bool* fused);
 int launch_permute(const int32_t* ids, int n, int E, int32_t* count, int32_t* offset, int32_t* rows, int32_t* pos,
                    int32_t* act_e, int32_t* n_act, int32_t* dev_status, int32_t* scratch, cudaStream_t s);
 

@@ -6,6 +6,7 @@
 // GEMM runs on grouped, slot-remapped ids).  Within an expert the order is
 // ascending flat index, so the result is unique and checked bit for bit.
 #include "common.cuh"
+#include "perm_small.cuh"
 
 namespace moe {
 
@@ -202,66 +203,12 @@ __global__ void __launch_bounds__(kPermThreads) permute_scatter_kernel(const int
 using namespace moe;
 
 namespace moe {
-// Small n (decode batches): one CTA, stable rank by counting.  count[e] and a
-// slot's rank among equal ids are plain counts over the ids in shared memory.
-constexpr int kSmallN = 256;
+// Small n (decode batches): one CTA, stable rank by counting (perm_small.cuh).
 __global__ void __launch_bounds__(256) permute_small_kernel(const int32_t* __restrict__ ids, int n, int E,
-                                                            int32_t* __restrict__ count,
-                                                            int32_t* __restrict__ offset,
-                                                            int32_t* __restrict__ rows, int32_t* __restrict__ pos,
-                                                            int32_t* __restrict__ act_e,
-                                                            int32_t* __restrict__ n_act,
-                                                            int32_t* __restrict__ status) {
+                                                            const PermOut o) {
   pdl_trigger();
   pdl_wait();  // launched as a dependent: the ids (or the previous permute step) are complete
-  __shared__ int sid[kSmallN];
-  __shared__ int soff[kMaxE];
-  __shared__ int tmp[33];
-  const int tid = threadIdx.x;
-  if (tid < n) {
-    int e = ids[tid];
-    if (e < 0 || e >= E) {
-      set_status(status, MOE_DEV_BAD_EXPERT);
-      e = -1;
-    }
-    sid[tid] = e;
-  }
-  __syncthreads();
-  int carry = 0, carry_act = 0;
-  for (int e0 = 0; e0 < E; e0 += 256) {
-    const int e = e0 + tid;
-    int c = 0;
-    if (e < E)
-      for (int i = 0; i < n; ++i) c += sid[i] == e;
-    int tot, tot_act;
-    const int ex = block_exclusive_scan(c, tmp, &tot);
-    const int exa = block_exclusive_scan(c > 0 ? 1 : 0, tmp, &tot_act);
-    if (e < E) {
-      soff[e] = carry + ex;
-      offset[e] = carry + ex;
-      count[e] = c;
-      if (c > 0) act_e[carry_act + exa] = e;
-    }
-    carry += tot;
-    carry_act += tot_act;
-  }
-  if (tid == 0) {
-    offset[E] = carry;
-    *n_act = carry_act;
-  }
-  __syncthreads();
-  if (tid < n) {
-    const int e = sid[tid];
-    if (e >= 0) {
-      int r = 0;
-      for (int i = 0; i < tid; ++i) r += sid[i] == e;
-      const int p = soff[e] + r;
-      rows[p] = tid;
-      pos[tid] = p;
-    } else {
-      pos[tid] = -1;
-    }
-  }
+  permute_small_block(ids, n, E, o);
 }
 }  // namespace moe
 
@@ -270,8 +217,8 @@ int launch_permute(const int32_t* ids, int n, int E, int32_t* count, int32_t* of
                    int32_t* act_e, int32_t* n_act, int32_t* dev_status, int32_t* scratch, cudaStream_t s) {
   const int P = (n + kPermThreads - 1) / kPermThreads;
   if (n <= kSmallN) {
-    MOE_CUDA_TRY(launch_pdl(permute_small_kernel, dim3(1), dim3(256), 0, s, ids, n, E, count, offset, rows, pos, act_e,
-                            n_act, dev_status));
+    const PermOut o{count, offset, rows, pos, act_e, n_act, dev_status};
+    MOE_CUDA_TRY(launch_pdl(permute_small_kernel, dim3(1), dim3(256), 0, s, ids, n, E, o));
     return MOE_OK;
   }
   if (P > 1 && scratch) {

@@ -9,6 +9,7 @@
 
 #include "common.cuh"
 #include "fp32def.cuh"
+#include "perm_small.cuh"
 
 namespace moe {
 
@@ -489,49 +490,13 @@ __global__ void __launch_bounds__(kFullThreads) logits_full_kernel(const uint16_
 // the bias is added after the sigmoid): sigmoid32_def (fp32def.cuh).
 
 // ---------------------------------------------------------------------------
-// Top-k: one warp per token.  k rounds of a warp-wide argmax over
-// score = logit + bias (ties -> lower id); the winner is marked taken.
-// Weights: softmax over the k picked, from the unbiased logits.  NQ = 32-expert
-// slots per lane (E <= 32 * NQ).
-// ---------------------------------------------------------------------------
+// One warp routes token t: k rounds of a warp-wide argmax over the scores, then the weights.
 template <int NQ>
-__global__ void __launch_bounds__(kRouteThreads) topk_kernel(float* __restrict__ logits,
-                                                             const float* __restrict__ bias,
-                                                             const int32_t* __restrict__ e2s, float affinity,
-                                                             const float* __restrict__ part, int nb,
-                                                             const float* __restrict__ off, int T, int E, int k,
-                                                             int tpc, int rflags, int32_t* __restrict__ ids,
-                                                             float* __restrict__ wout) {
-  __shared__ float sel_l[kRouteThreads / 32][kMaxK];
-  __shared__ int sel_i[kRouteThreads / 32][kMaxK];
-  pdl_trigger();
-  pdl_wait();  // launched as a dependent of the logits kernel: its parts / logits are complete
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int tb = blockIdx.x * tpc;  // tokens tb .. tb+tpc-1, one warp each (tpc <= 8)
-  if (part) {
-    // finish this CTA's logits from the block parts: 0 + part_0 + part_1 + ...
-    // (a value's parts are loaded, 16 at a time, before its in-order sum), then the offset
-    const int nt = min(tpc, T - tb);
-    const size_t bstride = (size_t)T * E;
-    for (int v = threadIdx.x; v < nt * E; v += kRouteThreads) {
-      const int tl = v / E, e = v - tl * E;
-      const float* pp = part + (size_t)(tb + tl) * E + e;
-      float l = 0.f;
-      for (int b = 0; b < nb; b += 16) {
-        float pv[16];
-#pragma unroll
-        for (int u = 0; u < 16; ++u) pv[u] = b + u < nb ? pp[(size_t)(b + u) * bstride] : 0.f;
-#pragma unroll
-        for (int u = 0; u < 16; ++u)
-          if (b + u < nb) l += pv[u];
-      }
-      logits[(size_t)(tb + tl) * E + e] = off ? l + off[e] : l;
-    }
-    __syncthreads();
-  }
-  if (warp >= tpc) return;
-  const int t = tb + warp;
-  if (t >= T) return;
+__device__ __forceinline__ void topk_token_impl(float* __restrict__ logits, const float* __restrict__ bias,
+                                                const int32_t* __restrict__ e2s, float affinity, int E, int k,
+                                                int rflags, int t, int warp, int lane,
+                                                float (*sel_l)[kMaxK], int (*sel_i)[kMaxK],
+                                                int32_t* __restrict__ ids, float* __restrict__ wout) {
   float* lrow = logits + (size_t)t * E;
   // the token's scores, loaded once: lane holds experts lane + 32q
   float sc[NQ];
@@ -603,20 +568,71 @@ __global__ void __launch_bounds__(kRouteThreads) topk_kernel(float* __restrict__
   }
 }
 
+// Top-k: one warp per token.  k rounds of a warp-wide argmax over
+// score = logit + bias (ties -> lower id); the winner is marked taken.
+// Weights: softmax over the k picked, from the unbiased logits.  NQ = 32-expert
+// slots per lane (E <= 32 * NQ).
+// ---------------------------------------------------------------------------
+template <int NQ>
+__global__ void __launch_bounds__(kRouteThreads) topk_kernel(float* __restrict__ logits,
+                                                             const float* __restrict__ bias,
+                                                             const int32_t* __restrict__ e2s, float affinity,
+                                                             const float* __restrict__ part, int nb,
+                                                             const float* __restrict__ off, int T, int E, int k,
+                                                             int tpc, int rflags, int32_t* __restrict__ ids,
+                                                             float* __restrict__ wout, const PermOut perm) {
+  __shared__ float sel_l[kRouteThreads / 32][kMaxK];
+  __shared__ int sel_i[kRouteThreads / 32][kMaxK];
+  pdl_trigger();
+  pdl_wait();  // launched as a dependent of the logits kernel: its parts / logits are complete
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int tb = blockIdx.x * tpc;  // tokens tb .. tb+tpc-1, one warp each (tpc <= 8)
+  if (part) {
+    // finish this CTA's logits from the block parts: 0 + part_0 + part_1 + ...
+    // (a value's parts are loaded, 16 at a time, before its in-order sum), then the offset
+    const int nt = min(tpc, T - tb);
+    const size_t bstride = (size_t)T * E;
+    for (int v = threadIdx.x; v < nt * E; v += kRouteThreads) {
+      const int tl = v / E, e = v - tl * E;
+      const float* pp = part + (size_t)(tb + tl) * E + e;
+      float l = 0.f;
+      for (int b = 0; b < nb; b += 16) {
+        float pv[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u) pv[u] = b + u < nb ? pp[(size_t)(b + u) * bstride] : 0.f;
+#pragma unroll
+        for (int u = 0; u < 16; ++u)
+          if (b + u < nb) l += pv[u];
+      }
+      logits[(size_t)(tb + tl) * E + e] = off ? l + off[e] : l;
+    }
+    __syncthreads();
+  }
+  const int t = tb + warp;
+  if (warp < tpc && t < T)
+    topk_token_impl<NQ>(logits, bias, e2s, affinity, E, k, rflags, t, warp, lane, sel_l, sel_i, ids, wout);
+  // a CTA that routed the whole batch also groups it by expert (the ids it wrote are visible to the
+  // block after the barrier)
+  if (perm.count && gridDim.x == 1) {
+    __syncthreads();
+    permute_small_block(ids, T * k, E, perm);
+  }
+}
+
 // Top-k launch (a programmatic dependent of the logits kernel) with the fewest 32-expert slots per lane
 // that hold E.
 static cudaError_t launch_topk(int grid, cudaStream_t s, float* logits, const float* bias, const int32_t* e2s,
                                float affinity, const float* part, int nb, const float* off, int T, int E, int k,
-                               int tpc, int rflags, int32_t* ids, float* w) {
+                               int tpc, int rflags, int32_t* ids, float* w, const PermOut& perm) {
   const dim3 g(grid), b(kRouteThreads);
   if (E <= 128)
     return launch_pdl(topk_kernel<4>, g, b, 0, s, logits, bias, e2s, affinity, part, nb, off, T, E, k, tpc, rflags,
-                      ids, w);
+                      ids, w, perm);
   if (E <= 256)
     return launch_pdl(topk_kernel<8>, g, b, 0, s, logits, bias, e2s, affinity, part, nb, off, T, E, k, tpc, rflags,
-                      ids, w);
+                      ids, w, perm);
   return launch_pdl(topk_kernel<kMaxE / 32>, g, b, 0, s, logits, bias, e2s, affinity, part, nb, off, T, E, k, tpc,
-                    rflags, ids, w);
+                    rflags, ids, w, perm);
 }
 
 }  // namespace moe
@@ -642,9 +658,22 @@ extern "C" size_t moe_route_scratch_bytes(int T, int H, int E) {
   return (size_t)((H + kHC - 1) / kHC) * T * E * sizeof(float);
 }
 
-extern "C" int moe_route_ex(const void* x, const void* w_router, const float* logit_offset, const float* sel_bias,
-                            const int32_t* e2s, float affinity, int rflags, int T, int H, int E, int k,
-                            float* logits, float* scratch, int32_t* ids, float* w, moe_stream_t stream) {
+namespace moe {
+
+// The route entry's work; when `perm` is given and the top-k runs as one CTA over at most kSmallN
+// routing slots, that CTA also groups the batch by expert into *perm and *fused is set.
+int route_impl(const void* x, const void* w_router, const float* logit_offset, const float* sel_bias,
+               const int32_t* e2s, float affinity, int rflags, int T, int H, int E, int k, float* logits,
+               float* scratch, int32_t* ids, float* w, cudaStream_t stream, const PermOut* perm, bool* fused) {
+  if (fused) *fused = false;
+  const PermOut none{};
+  auto pk = [&](int grid) -> PermOut {
+    if (perm && fused && grid == 1 && T * k <= kSmallN) {
+      *fused = true;
+      return *perm;
+    }
+    return none;
+  };
   if (!x || !w_router || !ids || !w || !logits) return MOE_ERR_ARG;
   if (rflags & ~(MOE_ROUTE_SIGMOID | MOE_ROUTE_DAMPED)) return MOE_ERR_ARG;
   if ((rflags & MOE_ROUTE_SIGMOID) && (rflags & MOE_ROUTE_DAMPED)) return MOE_ERR_ARG;
@@ -666,7 +695,7 @@ extern "C" int moe_route_ex(const void* x, const void* w_router, const float* lo
     // tokens per CTA: 8 while that fills the SMs, else 2 (each thread then finishes about one logit)
     const int tpc = (T + 7) / 8 >= sms ? 8 : 2;
     MOE_CUDA_TRY(launch_topk((T + tpc - 1) / tpc, s, logits, sel_bias, e2s, affinity, scratch, nblk, logit_offset, T,
-                             E, k, tpc, rflags, ids, w));
+                             E, k, tpc, rflags, ids, w, pk((T + tpc - 1) / tpc)));
     MOE_LAUNCH_CHECK();
     return MOE_OK;
   }
@@ -679,7 +708,7 @@ extern "C" int moe_route_ex(const void* x, const void* w_router, const float* lo
     logits_full_kernel<<<grid, kFullThreads, smem, s>>>(xb, wb, logit_offset, T, H, E, logits);
     MOE_LAUNCH_CHECK();
     MOE_CUDA_TRY(launch_topk((T + 7) / 8, s, logits, sel_bias, e2s, affinity, nullptr, 0, nullptr, T, E, k, 8, rflags,
-                             ids, w));
+                             ids, w, pk((T + 7) / 8)));
     MOE_LAUNCH_CHECK();
     return MOE_OK;
   }
@@ -694,7 +723,7 @@ extern "C" int moe_route_ex(const void* x, const void* w_router, const float* lo
     // tokens per CTA: 8 while that fills the SMs, else 2 (each thread then finishes about one logit)
     const int tpc = (T + 7) / 8 >= sms ? 8 : 2;
     MOE_CUDA_TRY(launch_topk((T + tpc - 1) / tpc, s, logits, sel_bias, e2s, affinity, scratch, nblk, logit_offset, T,
-                             E, k, tpc, rflags, ids, w));
+                             E, k, tpc, rflags, ids, w, pk((T + tpc - 1) / tpc)));
     MOE_LAUNCH_CHECK();
     return MOE_OK;
   }
@@ -724,9 +753,18 @@ extern "C" int moe_route_ex(const void* x, const void* w_router, const float* lo
   }
   MOE_LAUNCH_CHECK();
   MOE_CUDA_TRY(launch_topk((T + 7) / 8, s, logits, sel_bias, e2s, affinity, nullptr, 0, nullptr, T, E, k, 8, rflags,
-                           ids, w));
+                           ids, w, pk((T + 7) / 8)));
   MOE_LAUNCH_CHECK();
   return MOE_OK;
+}
+
+}  // namespace moe
+
+extern "C" int moe_route_ex(const void* x, const void* w_router, const float* logit_offset, const float* sel_bias,
+                            const int32_t* e2s, float affinity, int rflags, int T, int H, int E, int k,
+                            float* logits, float* scratch, int32_t* ids, float* w, moe_stream_t stream) {
+  return route_impl(x, w_router, logit_offset, sel_bias, e2s, affinity, rflags, T, H, E, k, logits, scratch, ids, w,
+                    (cudaStream_t)stream, nullptr, nullptr);
 }
 
 extern "C" int moe_route(const void* x, const void* w_router, const float* logit_offset, const float* sel_bias,
