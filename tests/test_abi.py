@@ -76,3 +76,37 @@ def test_workspace_sizes(lib):
     assert lib.moe_ffn_workspace_bytes(64, 2048, 8, 768) == 4 * 512 * 768 + 256 + stream
     # the tensor-core path adds bf16 grouped x and bf16 h
     assert lib.moe_ffn_workspace_bytes(4096, 2048, 8, 768) == 4 * 32768 * 768 + 2 * 32768 * (2048 + 768)
+
+
+def test_layer_forward_rejects_bad_arguments_on_the_host():
+    """moe_layer_forward checks shapes, buffers and mode/policy pairs before any CUDA call: gather
+    evicts (LRU or LFU), zero-return keeps a STATIC pool, a resident pool smaller than E needs a slot
+    table, and the quantised path is on or off."""
+    import expert_slot_cache_gb300.binding as b
+    buf = (ctypes.c_int32 * 64)()
+    p = ctypes.cast(buf, ctypes.c_void_p).value
+
+    def args(**kw):
+        a = b.LayerArgs()
+        a.T, a.H, a.E, a.k, a.I, a.S = 4, 256, 16, 2, 128, 16
+        for f in ("x", "w_router", "pool", "ids", "w", "out", "workspace"):
+            setattr(a, f, p)
+        for key, val in kw.items():
+            setattr(a, key, val)
+        return a
+
+    def call(a):
+        return b._layer(ctypes.byref(a), None, None)
+
+    assert call(args(mode=9)) == -1                    # no such mode
+    assert call(args(mode=1, policy=2)) == -1          # gather with a pool that never evicts
+    assert call(args(mode=2, policy=0)) == -1          # zero-return with an evicting policy
+    assert call(args(mode=1, policy=0)) == -1          # gather without cache state / host store
+    assert call(args(S=8)) == -1                       # resident, fewer slots than experts, no table
+    assert call(args(T=0)) == -1
+    assert call(args(k=17)) == -1                      # top-k above the largest supported
+    assert call(args(H=100)) == -1                     # H not a multiple of 64
+    assert call(args(x=None)) == -1
+    assert call(args(quant=3)) == -1
+    assert b._layer(None, None, None) == -1
+    assert b._layer_ws(0, 2048, 128, 8, 768, 64) == 0  # no workspace for an empty step
