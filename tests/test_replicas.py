@@ -23,7 +23,7 @@ def _worker(rank, world, port, out):
 
 def test_two_gloo_replicas_take_the_max_time():
     port = 29500 + (os.getpid() % 1000)
-    out = mp.Manager().dict()
+    out = mp.get_context("spawn").Manager().dict()
     mp.spawn(_worker, args=(2, port, out), nprocs=2, join=True)
     assert dict(out) == {0: 11.0, 1: 11.0}
 
