@@ -398,8 +398,9 @@ __global__ void __launch_bounds__(kQRowThreads) q8_reduce_gu_kernel(const FfnArg
 
 // The same reduction with an expert's rows four at a time: 64 threads per row, each owning up to
 // four quads of it (I <= 1024), with every part's loads for those quads issued before their adds
-// (four parts a batch), and the row amax from the row's two warps.  All rows of a CTA take the same
-// number of steps, so the block barrier is uniform.
+// (four parts a batch), and the row amax from the row's two warps.  An expert with a single row and
+// more than four parts has that row's parts split over the four groups instead.  The path and the number of steps
+// depend only on the expert's rows, so every block barrier is uniform.
 constexpr int kQRowQuads = 4;   // quads per thread and row
 constexpr int kQPartBatch = 4;  // parts whose loads are in flight together
 __global__ void __launch_bounds__(kQRowThreads, 1) q8_reduce_gu_rows_kernel(
@@ -425,6 +426,93 @@ __global__ void __launch_bounds__(kQRowThreads, 1) q8_reduce_gu_rows_kernel(
   const size_t pstride = (size_t)n * N;
   const int pb = a.offset[e], pe = a.offset[e + 1];
   const int grp = threadIdx.x >> 6, t64 = threadIdx.x & 63, w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (pe - pb == 1 && stream_parts(v0, NSR, L) > kQPartBatch) {
+    // a single row with more parts than one batch (small decode batches): all four groups work on it,
+    // group g taking parts g, g+4, ...; the exact int32 sums meet in shared memory
+    __shared__ int s_acc[2 * 4 * 64 * kQRowQuads];  // [g | u][column] for the row
+    for (int p = pb; p < pe; ++p) {
+      for (int i = threadIdx.x; i < 2 * I; i += kQRowThreads) s_acc[i] = 0;
+      __syncthreads();
+      const int J = stream_parts(v0 + (p - pb) / kQRB, NSR, L);
+      int4 ag[kQRowQuads], au[kQRowQuads];
+#pragma unroll
+      for (int i = 0; i < kQRowQuads; ++i) ag[i] = au[i] = make_int4(0, 0, 0, 0);
+      const int32_t* pp = part + (size_t)p * N + 4 * t64;
+      for (int j0 = grp; j0 < J; j0 += 4 * kQPartBatch) {
+        int4 tg[kQRowQuads][kQPartBatch], tu[kQRowQuads][kQPartBatch];
+#pragma unroll
+        for (int i = 0; i < kQRowQuads; ++i)
+#pragma unroll
+          for (int u = 0; u < kQPartBatch; ++u) {
+            tg[i][u] = tu[i][u] = make_int4(0, 0, 0, 0);
+            const int j = j0 + 4 * u;
+            if (t64 + 64 * i < nq4 && j < J) {
+              const int32_t* src = pp + (size_t)j * pstride + 256 * i;
+              tg[i][u] = *reinterpret_cast<const int4*>(src);
+              tu[i][u] = *reinterpret_cast<const int4*>(src + I);
+            }
+          }
+#pragma unroll
+        for (int i = 0; i < kQRowQuads; ++i)
+#pragma unroll
+          for (int u = 0; u < kQPartBatch; ++u) {
+            ag[i].x += tg[i][u].x; ag[i].y += tg[i][u].y; ag[i].z += tg[i][u].z; ag[i].w += tg[i][u].w;
+            au[i].x += tu[i][u].x; au[i].y += tu[i][u].y; au[i].z += tu[i][u].z; au[i].w += tu[i][u].w;
+          }
+      }
+#pragma unroll
+      for (int i = 0; i < kQRowQuads; ++i) {
+        const int q = t64 + 64 * i;
+        if (q < nq4) {
+          int* dg = s_acc + 4 * q;
+          int* du = s_acc + I + 4 * q;
+          atomicAdd(dg, ag[i].x); atomicAdd(dg + 1, ag[i].y); atomicAdd(dg + 2, ag[i].z); atomicAdd(dg + 3, ag[i].w);
+          atomicAdd(du, au[i].x); atomicAdd(du + 1, au[i].y); atomicAdd(du + 2, au[i].z); atomicAdd(du + 3, au[i].w);
+        }
+      }
+      __syncthreads();
+      // group 0 forms the row's h; its two warps give the amax
+      const float s_x = sx[p];
+      float hv[kQRowQuads][4];
+      float amax = 0.f;
+#pragma unroll
+      for (int i = 0; i < kQRowQuads; ++i) {
+        const int q = t64 + 64 * i;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          hv[i][b] = 0.f;
+          if (grp == 0 && q < nq4) {
+            const int c = 4 * q + b;
+            const float g = __fmul_rn(__fmul_rn(__int2float_rn(s_acc[c]), sg[c]), s_x);
+            const float u = __fmul_rn(__fmul_rn(__int2float_rn(s_acc[I + c]), su[c]), s_x);
+            const float h = __fmul_rn(silu32_def(g), u);
+            hv[i][b] = h;
+            amax = fmaxf(amax, fabsf(h));
+          }
+        }
+      }
+      amax = warp_max(amax);
+      if (lane == 0) red[w] = amax;
+      __syncthreads();
+      amax = fmaxf(red[0], red[1]);
+      if (grp == 0) {
+        const float s = __fdiv_rn(amax, 127.f);
+#pragma unroll
+        for (int i = 0; i < kQRowQuads; ++i) {
+          const int q = t64 + 64 * i;
+          if (q < nq4) {
+            uint32_t pk = 0;
+#pragma unroll
+            for (int b = 0; b < 4; ++b) pk |= (uint32_t)(q8_code(hv[i][b], s) & 0xff) << (8 * b);
+            hq[q8_act_word(q, p, npad)] = pk;
+          }
+        }
+        if (t64 == 0) sh[p] = s;
+      }
+      __syncthreads();  // s_acc and red are reused by the next row
+    }
+    return;
+  }
   for (int p0 = pb; p0 < pe; p0 += kQRowThreads / 64) {
     const int p = p0 + grp;
     const bool row = p < pe;
