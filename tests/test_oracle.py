@@ -665,3 +665,102 @@ def test_q8_expert_close_to_the_bf16_expert():
     yq = O.swiglu_expert_q8(x, O.quantize_slab(slab, H, I), H, I)
     y = O.swiglu_expert(x, slab, H, I)
     assert np.linalg.norm(yq - y) / np.linalg.norm(y) < 4e-2
+
+
+def _q8_hand_slab(g, wd_factor=1.0):
+    """bf16 slab values (code x scale, exact in bf16) of the hand-worked W8A8 expert."""
+    wg = np.array(g["qg"], dtype=np.float32) * np.float32(g["weight_scale_g"])
+    wu = np.array(g["qu"], dtype=np.float32) * np.float32(g["weight_scale_u"])
+    wd = np.array(g["qd"], dtype=np.float32) * np.float32(g["weight_scale_d"] * wd_factor)
+    slab = np.concatenate([wg.reshape(-1), wu.reshape(-1), wd.reshape(-1)])
+    assert np.array_equal(_bf16(slab), slab)  # the slab is exactly representable in bf16
+    return slab
+
+
+def test_q8_expert_hand_worked_example():
+    g = _gold("q8_example.json")
+    H, I = g["H"], g["I"]
+    b = O.quantize_slab(_q8_hand_slab(g), H, I)
+    qg, qu, qd, sg, su, sd = O.unpack_q8_slab(b, H, I)
+    assert qg.tolist() == g["qg"] and qu.tolist() == g["qu"] and qd.tolist() == g["qd"]
+    assert np.all(sg == g["weight_scale_g"]) and np.all(su == g["weight_scale_u"])
+    assert np.all(sd == g["weight_scale_d"])
+    x = np.array(g["x"], dtype=np.float32)
+    qx, sx = O.quantize_rows(x)
+    assert qx.tolist() == g["x_codes"] and sx.tolist() == g["x_scales"]
+    qh, sh = O.quantize_rows(np.array(g["h"], dtype=np.float32))
+    assert qh.tolist() == g["h_codes"] and sh.tolist() == g["h_scales"]
+    y = O.swiglu_expert_q8(x, b, H, I)
+    assert y.dtype == np.float32 and y.tolist() == g["y"]  # every step is exact for this example
+
+
+def test_q8_hand_example_tells_row_from_column_quantisation_of_h():
+    # the planted mistake: h quantised per column instead of per routing row
+    g = _gold("q8_example.json")
+    h = np.array(g["h"], dtype=np.float32)
+    qh_col, sh_col = O.quantize_cols(h)
+    qd = np.array(g["qd"], dtype=np.float64)
+    y_col = (qh_col.astype(np.float64) * sh_col.astype(np.float64)[None, :]) @ qd * g["weight_scale_d"]
+    assert sh_col.tolist() != g["h_scales"]
+    assert np.abs(y_col - np.array(g["y"])).max() > 1.0
+
+
+def test_grouped_q8_ffn_hand_example():
+    # two experts: expert 0 is the hand-worked one, expert 1 the same with Wd doubled (same codes,
+    # doubled down scales, so exactly twice its y); token 0 -> [1, 0], token 1 -> [0, 1]
+    g = _gold("q8_example.json")
+    H, I, k = g["H"], g["I"], 2
+    qslabs = [O.quantize_slab(_q8_hand_slab(g, f), H, I) for f in (1.0, 2.0)]
+    ids = np.array([[1, 0], [0, 1]], dtype=np.int32)
+    count, offset, rows, pos = O.permute(ids, 2)
+    assert rows.tolist() == [1, 2, 0, 3]
+    y = O.expert_ffn_q8(np.array(g["x"], dtype=np.float32), rows, offset, k, qslabs, H, I)
+    want = np.array(g["y"], dtype=np.float32)
+    for t in range(2):
+        for j in range(k):
+            assert y[pos[t * k + j]].tolist() == (want[t] * (1 + ids[t, j])).tolist()
+    left_out = O.expert_ffn_q8(np.array(g["x"], dtype=np.float32), rows, offset, k, qslabs, H, I, experts={0})
+    assert np.isnan(left_out[offset[1]:offset[2]]).all() and not np.isnan(left_out[offset[0]:offset[1]]).any()
+
+
+def test_layer_forward_quant_hand_example():
+    # a zero router gives equal logits: ties pick [0, 1] and the weights are 1/2 each, so
+    # out[t] = y0[t] / 2 + y1[t] / 2 = 1.5 y[t] exactly
+    g = _gold("q8_example.json")
+    H, I = g["H"], g["I"]
+    qslabs = [O.quantize_slab(_q8_hand_slab(g, f), H, I) for f in (1.0, 2.0)]
+    res = O.layer_forward(np.array(g["x"], dtype=np.float32), np.zeros((H, 2), dtype=np.float32), qslabs, H, I, 2,
+                          O.RESIDENT, quant=True)
+    assert res["ids"].tolist() == [[0, 1], [0, 1]] and res["w"].tolist() == [[0.5, 0.5], [0.5, 0.5]]
+    assert res["out"].tolist() == (1.5 * np.array(g["y"], dtype=np.float64)).tolist()
+
+
+def test_layer_forward_quant_equals_per_routing_experts_combined_by_hand():
+    cfg = C.TINY
+    rng = np.random.default_rng(21)
+    H, I, E, k, T = cfg.H, cfg.I, cfg.E, cfg.k, cfg.T
+    x = _bf16(rng.standard_normal((T, H)))
+    wr = _bf16(rng.standard_normal((H, E)) * 0.02)
+    qslabs = [O.quantize_slab(_bf16(rng.standard_normal(3 * H * I) * 0.02), H, I) for _ in range(E)]
+    res = O.layer_forward(x, wr, qslabs, H, I, k, O.RESIDENT, quant=True)
+    want = np.zeros((T, H))
+    for t in range(T):
+        for j in range(k):
+            # per-row activation scales: one routing row alone gives the same codes as inside its group
+            y = O.swiglu_expert_q8(x[t:t + 1], qslabs[int(res["ids"][t, j])], H, I)[0]
+            want[t] += res["w"][t, j] * y.astype(np.float64)
+    assert np.array_equal(res["out"], want)
+
+
+def test_window_count_golden():
+    g = _gold("window_count.json")
+    counts = np.array(g["counts_before"], dtype=np.int64)
+    O.window_count(counts, np.array(g["ids"], dtype=np.int32))
+    assert counts.tolist() == g["counts_after"]
+    # the window count is a histogram of the routings: adding traces in pieces gives the same counts
+    rng = np.random.default_rng(22)
+    ids = rng.integers(0, 7, size=(9, 3))
+    a = np.zeros(7, dtype=np.int64)
+    for t in range(9):
+        O.window_count(a, ids[t:t + 1])
+    assert a.tolist() == np.bincount(ids.reshape(-1), minlength=7).tolist()
