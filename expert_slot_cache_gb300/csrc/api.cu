@@ -9,11 +9,6 @@
 
 namespace moe {
 
-static bool shape_ok(int T, int H, int I, int k, int E) {
-  return T >= 1 && H >= 64 && H % 64 == 0 && I >= 32 && I % 32 == 0 && k >= 1 && k <= kMaxK && E >= k &&
-         E <= kMaxE;
-}
-
 static size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
 // Workspace layout of the layer forward, for chunks of up to n = C*k routing slots.
@@ -164,6 +159,10 @@ extern "C" size_t moe_layer_workspace_bytes(int T, int H, int E, int k, int I, i
   if (T < 1 || k < 1 || E < 1 || S < 1) return 0;
   // Worst case over modes: the largest chunk is all T tokens.
   return carve(nullptr, T * k, H, E, I, T).bytes;
+}
+
+extern "C" size_t moe_workspace_bytes(int T, int H, int I, int E, int k) {
+  return moe_layer_workspace_bytes(T, H, E, k, I, E);
 }
 
 extern "C" int moe_layer_forward(const moe_layer_args* a, moe_stream_t main_s, moe_stream_t side_s) {

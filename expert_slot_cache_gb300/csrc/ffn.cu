@@ -39,11 +39,11 @@ __device__ __forceinline__ void unpack8(const uint4 v, float* f) {
   f[7] = bf16_hi(v.w);
 }
 
-// Weights of expert e (slot copy when resident, else the host store).
+// Weights of expert e (slot copy when resident, else the host store); NULL
+// when the slot lies outside the pool's S slots (S = 0: not checked).
 __device__ __forceinline__ const uint16_t* expert_weights(const FfnArgs& a, int e) {
-  if (!a.e2s) return a.pool + (size_t)e * a.slab_elems;
-  const int s = a.e2s[e];
-  if (s >= 0) return a.pool + (size_t)s * a.slab_elems;
+  const int s = a.e2s ? a.e2s[e] : e;
+  if (s >= 0) return (a.S > 0 && s >= a.S) ? nullptr : a.pool + (size_t)s * a.slab_elems;
   return a.host ? a.host + (size_t)e * a.slab_elems : nullptr;
 }
 

@@ -58,6 +58,12 @@ struct Prof {
   }
 };
 
+// Shapes every FFN entry point accepts (H % 64, I % 32, 1 <= k <= kMaxK, k <= E <= kMaxE).
+inline bool shape_ok(int T, int H, int I, int k, int E) {
+  return T >= 1 && H >= 64 && H % 64 == 0 && I >= 32 && I % 32 == 0 && k >= 1 && k <= kMaxK && E >= k &&
+         E <= kMaxE;
+}
+
 int launch_ffn(const FfnArgs& a, int max_list, cudaStream_t stream, Prof* prof = nullptr);
 bool prefill_eligible(const FfnArgs& a, int n);
 int launch_gather_rows(const uint16_t* x, const int32_t* rows, int n, int H, int k, uint16_t* xp, int sms,

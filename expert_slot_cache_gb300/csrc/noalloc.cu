@@ -50,13 +50,13 @@ using namespace moe;
 
 extern "C" int moe_expert_ffn_noalloc(const void* x, int T, int H, int I, int k, int E, const int32_t* offset,
                                       const int32_t* rows, const int32_t* list_e, const int32_t* n_list,
-                                      int max_list, const void* pool, const int32_t* e2s, const void* host_slabs,
-                                      float* y, int32_t* dev_status, moe_stream_t stream) {
+                                      int max_list, const void* pool, int S, const int32_t* e2s,
+                                      const void* host_slabs, float* y, int32_t* dev_status, moe_stream_t stream) {
+  // the argument checks of moe_expert_ffn, minus the workspace
   if (!x || !offset || !rows || !list_e || !n_list || !pool || !y) return MOE_ERR_ARG;
-  if (T < 1 || H < 64 || H % 64 || I < 32 || I % 32 || k < 1 || k > kMaxK || E < k || E > kMaxE || max_list < 0)
-    return MOE_ERR_ARG;
+  if (!shape_ok(T, H, I, k, E) || max_list < 0 || S < 1 || (!e2s && S < E)) return MOE_ERR_ARG;
+  if ((uintptr_t)pool % 16 || (uintptr_t)y % 16 || (uintptr_t)x % 16) return MOE_ERR_ALIGN;
   if ((size_t)T * (size_t)k * (size_t)I > kNoAllocScratchFloats) return MOE_ERR_SCRATCH_LIMIT;
-  if ((uintptr_t)pool % 16 || (uintptr_t)y % 16) return MOE_ERR_ALIGN;
   if (host_slabs) {
     if ((uintptr_t)host_slabs % 16) return MOE_ERR_ALIGN;
     const int acc = check_host_accessible(host_slabs);
@@ -67,7 +67,9 @@ extern "C" int moe_expert_ffn_noalloc(const void* x, int T, int H, int I, int k,
   if (r != MOE_OK) return r;
   // Nothing in the scratch has to start at zero: every h row the down
   // projection reads is written earlier in the same call, on the same stream.
+  // Without a host store every listed expert is in the pool, so the weight
+  // tiles can be streamed by tensor-map copies; slots are checked against S.
   FfnArgs a{(const uint16_t*)x, T, H, I, k, E, offset, rows, list_e, n_list, (const uint16_t*)pool, e2s,
-            (const uint16_t*)host_slabs, (size_t)3 * H * I, h, y, dev_status};
+            (const uint16_t*)host_slabs, (size_t)3 * H * I, h, y, dev_status, S, host_slabs == nullptr};
   return launch_ffn(a, max_list < E ? max_list : E, (cudaStream_t)stream);
 }

@@ -271,7 +271,14 @@ size_t moe_ffn_workspace_bytes(int T, int H, int k, int I);
  * fixed device array inside the library, MOE_FFN_NOALLOC_MAX_H fp32 values
  * (4 MiB) that every GPU which loads the library holds until the process
  * exits.  It calls no cudaMalloc, cudaFree or other allocating routine.
- * Arguments, outputs and results are those of moe_expert_ffn.
+ * Arguments, outputs, argument checks and results are those of
+ * moe_expert_ffn without the workspace: S is the pool's slot count, a slot
+ * outside [0, S) found on the device sets MOE_DEV_BAD_SLOT and skips the
+ * expert.  With host_slabs == NULL the weight tiles are streamed through
+ * shared memory by tensor-map copies (the CUDA-core kernel that takes no
+ * partial-sum buffers); with host_slabs the host-weights kernel runs.  h is
+ * kept in fp32, so y can differ from moe_expert_ffn's tensor-core paths by
+ * the rounding of h to bf16 there.
  *   - Limit: T * k * I <= MOE_FFN_NOALLOC_MAX_H, else MOE_ERR_SCRATCH_LIMIT
  *     is returned and nothing is enqueued.
  *   - The first call on a device looks up the array's device address
@@ -285,7 +292,7 @@ size_t moe_ffn_workspace_bytes(int T, int H, int k, int I);
 #define MOE_FFN_NOALLOC_MAX_H (1u << 20)
 int moe_expert_ffn_noalloc(const void* x, int T, int H, int I, int k, int E, const int32_t* offset,
                            const int32_t* rows, const int32_t* list_e, const int32_t* n_list, int max_list,
-                           const void* pool, const int32_t* e2s, const void* host_slabs, float* y,
+                           const void* pool, int S, const int32_t* e2s, const void* host_slabs, float* y,
                            int32_t* dev_status, moe_stream_t stream);
 
 /*
@@ -443,6 +450,11 @@ typedef struct moe_layer_args {
 int moe_layer_forward(const moe_layer_args* args, moe_stream_t main, moe_stream_t side);
 
 size_t moe_layer_workspace_bytes(int T, int H, int E, int k, int I, int S);
+
+/* The same size with the arguments in the order (T, H, I, E, k): the
+ * workspace moe_layer_forward needs for up to T tokens in any mode, schedule
+ * and pool size. */
+size_t moe_workspace_bytes(int T, int H, int I, int E, int k);
 
 #ifdef __cplusplus
 }
