@@ -61,9 +61,18 @@ Readings of points the pages leave open (each listed in the design notes):
     slots not needed by the call: empty slots first (ascending slot), then
     ascending prio, then ascending slot.  The i-th missing expert (ascending
     id) takes the i-th victim.  Eviction clears the old expert's entry.
-  * a step larger than the pool (T*k > S while S < E) is split into chunks of
-    floor(S/k) consecutive tokens, each chunk managed, gathered and computed
-    in turn; S < k cannot be served.
+  * a step larger than the pool (T*k > S while S < E), token-chunk schedule:
+    split into chunks of floor(S/k) consecutive tokens, each chunk managed,
+    gathered and computed in turn; S < k cannot be served.
+  * the same, expert-wave schedule (each missing expert loaded at most once
+    per step; [PORT] "Measuring, without fooling yourself": count misses, not
+    tokens): one manage call over the whole step updates the hits and loads
+    as many misses (ascending id) as there are slots the step does not need;
+    the misses left over are deferred.  The hits and the loaded misses are
+    computed; then the deferred experts are taken in ascending id, at most S
+    at a time, each batch one manage call whose victims may be any slot (every
+    expert already resident has been computed: the rest of the step no longer
+    needs it), gathered and computed in turn.  An empty batch is no call.
   * zero-return: residency is e2s[e] >= 0 after a STATIC manage; the output is
     the sum of the resident partial and the missing partial.
   * bias modes: graded (the formula above), flat (every cold expert gets one
@@ -311,20 +320,27 @@ class ManageResult:
     miss_s: list = field(default_factory=list)
     hit_e: list = field(default_factory=list)
     sid: np.ndarray = None
+    deferred: list = field(default_factory=list)
 
 
 class CapacityError(ValueError):
     pass
 
 
-def manage(state: CacheState, ids: np.ndarray, policy: int) -> ManageResult:
-    """One expert_cache_manage call on the flat routing ids of a step (updates ``state``)."""
+def manage(state: CacheState, ids: np.ndarray, policy: int, defer: bool = False) -> ManageResult:
+    """One expert_cache_manage call on the flat routing ids of a step (updates ``state``).
+
+    With ``defer`` a call that needs more experts than the pool holds is
+    allowed: the misses (ascending id) take the victims in order while they
+    last, and the rest are listed in ``deferred`` and left cold (the first
+    call of the expert-wave schedule).
+    """
     flat = [int(e) for e in np.asarray(ids).reshape(-1)]
     S = state.s2e.shape[0]
     state.stamp += 1
     stamp = state.stamp
     needed = sorted(set(flat))
-    if policy != STATIC and len(needed) > S:
+    if policy != STATIC and len(needed) > S and not defer:
         raise CapacityError(f"{len(needed)} experts needed, {S} slots")
     hits = [e for e in needed if state.e2s[e] >= 0]
     misses = [e for e in needed if state.e2s[e] < 0]
@@ -343,6 +359,8 @@ def manage(state: CacheState, ids: np.ndarray, policy: int) -> ManageResult:
         empty = [s for s in cands if state.s2e[s] < 0]
         full = sorted((s for s in cands if state.s2e[s] >= 0), key=lambda s: (int(state.prio[s]), s))
         victims = (empty + full)[: len(misses)]
+        res.deferred = misses[len(victims):]
+        res.miss_e = misses[:len(victims)]
         for e, s in zip(misses, victims):
             old = int(state.s2e[s])
             if old >= 0:
@@ -393,6 +411,21 @@ def gather(host: np.ndarray, pool: np.ndarray, miss_e, miss_s) -> None:
     """Copy each missing expert's slab bytes from the host store into its slot."""
     for e, s in zip(miss_e, miss_s):
         pool[s] = host[e]
+
+
+def manage_waves(state: CacheState, ids: np.ndarray, policy: int) -> list:
+    """The manage calls of one step under the expert-wave schedule (see the
+    readings above): wave 0 over the whole step with deferral, then one call
+    per batch of at most S deferred experts.  Returns the ManageResults in
+    order; wave 0's ``hit_e`` and ``miss_e`` and each later wave's ``miss_e``
+    are the expert lists computed after that wave's gather."""
+    S = state.s2e.shape[0]
+    first = manage(state, ids, policy, defer=True)
+    waves = [first]
+    left = list(first.deferred)
+    for b0 in range(0, len(left), S):
+        waves.append(manage(state, np.array(left[b0:b0 + S], dtype=np.int32), policy))
+    return waves
 
 
 def chunk_tokens(T: int, k: int, S: int, E: int) -> int:
@@ -568,15 +601,25 @@ def combine(y, w, pos, T, k, resident=None):
 # Whole layer
 # ----------------------------------------------------------------------------
 
+SCHED_CHUNKS, SCHED_WAVES = 0, 1
+
+
 def layer_forward(x, wr, host, H, I, k, mode, policy=LRU, state=None, pool=None,
-                  logit_offset=None, bias=None, affinity=0.0, router=ROUTER_SOFTMAX, damped=False, quant=False):
+                  logit_offset=None, bias=None, affinity=0.0, router=ROUTER_SOFTMAX, damped=False, quant=False,
+                  schedule=SCHED_CHUNKS):
     """One MoE layer forward with the slot cache.
 
     ``host`` [E][3HI] holds every expert (authoritative copy); ``pool``
     [S][3HI] the slot contents (updated by the gather); ``state`` the cache
     state (updated).  Returns a dict with the routing, the per-chunk cache
-    results and the outputs (fp64).
+    results and the outputs (fp64).  In GATHER mode ``schedule`` picks token
+    chunks or expert waves for a step larger than the pool; with waves the
+    step is one chunk and its record carries ``waves``: per manage call the
+    loaded experts, their slots and the cache state after the call.
     """
+    if mode == GATHER and schedule == SCHED_WAVES:
+        return _layer_forward_waves(x, wr, host, H, I, k, policy, state, pool, logit_offset, bias, affinity,
+                                    router, damped, quant)
     x = np.asarray(x, dtype=np.float32)
     T = x.shape[0]
     E = wr.shape[1]
@@ -618,3 +661,33 @@ def layer_forward(x, wr, host, H, I, k, mode, policy=LRU, state=None, pool=None,
     if mode == ZERO_RETURN:
         res["out_res"], res["out_miss"] = out_res, out_miss
     return res
+
+
+def _layer_forward_waves(x, wr, host, H, I, k, policy, state, pool, logit_offset, bias, affinity, router, damped,
+                         quant):
+    """GATHER mode, expert-wave schedule: route and group the whole step once,
+    run the manage calls of ``manage_waves`` (gathering each call's loads),
+    then the expert FFN of every routed expert and one combine."""
+    x = np.asarray(x, dtype=np.float32)
+    T = x.shape[0]
+    E = wr.shape[1]
+    resident = None if affinity == 0.0 else state.e2s >= 0
+    ids, w, logits = route(x, wr, k, logit_offset, bias, resident, affinity, router, damped)
+    count, offset, rows, pos = permute(ids, E)
+    waves = []
+    for r in manage_waves(state, ids, policy):
+        if pool is not None:
+            gather(host, pool, r.miss_e, r.miss_s)
+        waves.append({"hit_e": r.hit_e, "miss_e": r.miss_e, "miss_s": r.miss_s, "deferred": r.deferred,
+                      "e2s": state.e2s.copy(), "s2e": state.s2e.copy(), "prio": state.prio.copy(),
+                      "stamp": state.stamp})
+    if quant:
+        y = expert_ffn_q8(x, rows, offset, k, host, H, I).astype(np.float64)
+    else:
+        y = expert_ffn(x, rows, offset, k, host, H, I)
+    out = combine(y, w, pos, T, k)
+    rec = {"t0": 0, "t1": T, "count": count, "offset": offset, "rows": rows, "pos": pos, "waves": waves,
+           "miss_e": [e for wv in waves for e in wv["miss_e"]], "miss_s": [s for wv in waves for s in wv["miss_s"]],
+           "hit_e": waves[0]["hit_e"], "e2s": state.e2s.copy(), "s2e": state.s2e.copy(),
+           "prio": state.prio.copy(), "stamp": state.stamp}
+    return {"ids": ids, "w": w, "logits": logits, "out": out, "chunks": [rec]}

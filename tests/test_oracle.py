@@ -327,6 +327,145 @@ def test_manage_capacity_and_chunking():
         O.chunk_tokens(4, 8, 6, 128)
 
 
+def _state(tr):
+    st = O.CacheState.from_slots(np.array(tr["s2e0"], dtype=np.int32), tr["E"])
+    st.prio[:] = tr["prio0"]
+    st.stamp = tr["stamp0"]
+    return st
+
+
+@pytest.mark.parametrize("trace", _gold("wave_traces.json")["traces"], ids=lambda t: t["name"])
+def test_wave_golden_traces(trace):
+    st = _state(trace)
+    waves = O.manage_waves(st, np.array(trace["ids"], dtype=np.int32), trace["policy"])
+    assert len(waves) == len(trace["waves"])
+    # replay the calls one at a time to compare the state after each
+    st = _state(trace)
+    first = True
+    left = []
+    for r, want in zip(waves, trace["waves"]):
+        assert r.hit_e == want["hit_e"] and r.miss_e == want["miss_e"] and r.miss_s == want["miss_s"]
+        if first:
+            got = O.manage(st, np.array(trace["ids"], dtype=np.int32), trace["policy"], defer=True)
+            left = list(got.deferred)
+            assert got.deferred == want["deferred"]
+            first = False
+        else:
+            O.manage(st, np.array(left[:trace["S"]], dtype=np.int32), trace["policy"])
+            left = left[trace["S"]:]
+        assert st.s2e.tolist() == want["s2e"] and st.prio.tolist() == want["prio"] and st.stamp == want["stamp"]
+    if "loads_token_chunks" in trace:
+        st = _state(trace)
+        ids = np.array(trace["ids"], dtype=np.int32)
+        C_ = O.chunk_tokens(ids.shape[0], trace["k"], trace["S"], trace["E"])
+        loads = sum(len(O.manage(st, ids[t0:t0 + C_], trace["policy"]).miss_e) for t0 in range(0, ids.shape[0], C_))
+        assert loads == trace["loads_token_chunks"]
+        assert sum(len(w["miss_e"]) for w in trace["waves"]) < loads
+
+
+def _second_model_waves(m, ids, S):
+    """The expert-wave schedule on the second cache model, written from the reading
+    independently of manage_waves: greedy victims per load, deferral when the
+    step's free slots run out, then batches of at most S."""
+    m.calls += 1
+    want = sorted(set(int(e) for e in ids))
+    where = {e: s for s, e in m.occ.items() if e >= 0}
+    hits = [e for e in want if e in where]
+    for e in hits:
+        m.score[where[e]] = m.calls if m.policy == O.LRU else m.score[where[e]] + 1
+    busy = {where[e] for e in hits}
+    waves = [[]]
+    deferred = []
+    for e in (e for e in want if e not in where):
+        pool = [s for s in m.occ if s not in busy]
+        if not pool:
+            deferred.append(e)
+            continue
+        s = min(pool, key=lambda s: (m.occ[s] >= 0, m.score[s] if m.occ[s] >= 0 else 0, s))
+        m.occ[s], m.score[s] = e, (m.calls if m.policy == O.LRU else 1)
+        busy.add(s)
+        waves[0].append((e, s))
+    for b0 in range(0, len(deferred), S):
+        m.calls += 1
+        busy = set()
+        waves.append([])
+        for e in deferred[b0:b0 + S]:
+            s = min((s for s in m.occ if s not in busy), key=lambda s: (m.occ[s] >= 0, m.score[s], s))
+            m.occ[s], m.score[s] = e, (m.calls if m.policy == O.LRU else 1)
+            busy.add(s)
+            waves[-1].append((e, s))
+    return hits, waves
+
+
+@pytest.mark.parametrize("policy", [O.LRU, O.LFU])
+@pytest.mark.parametrize("dist", ["uniform", "zipf"])
+def test_waves_match_second_model_and_load_each_miss_once(policy, dist):
+    rng = np.random.default_rng(300 + 3 * policy + (dist == "zipf"))
+    E, k = 40, 4
+    for S in (3, 7, 16):
+        s2e0 = rng.permutation(E)[:S].astype(np.int32)
+        s2e0[rng.integers(0, S)] = -1
+        st = O.CacheState.from_slots(s2e0, E)
+        m = _SecondModel(s2e0, E, policy)
+        T = 6
+        traces = _zipf_ids(rng, 30, T, k, E) if dist == "zipf" else \
+            [np.stack([rng.choice(E, k, replace=False) for _ in range(T)]).astype(np.int32) for _ in range(30)]
+        for ids in traces:
+            before = {int(e) for e in np.nonzero(st.e2s >= 0)[0]}
+            need = {int(e) for e in ids.reshape(-1)}
+            waves = O.manage_waves(st, ids, policy)
+            hits, mw = _second_model_waves(m, ids.reshape(-1), S)
+            assert waves[0].hit_e == hits
+            assert [list(zip(w.miss_e, w.miss_s)) for w in waves] == mw
+            s2e, e2s, score = m.tables()
+            assert st.s2e.tolist() == s2e and st.e2s.tolist() == e2s and st.prio.tolist() == score
+            loaded = [e for w in waves for e in w.miss_e]
+            assert sorted(loaded) == sorted(need - before)  # each missing expert loaded exactly once
+            assert all(len(w.miss_e) <= S for w in waves) and all(len(w.miss_e) > 0 for w in waves[1:])
+            assert set(waves[0].hit_e) | set(loaded) == need
+
+
+def test_waves_never_load_more_than_token_chunks():
+    rng = np.random.default_rng(77)
+    E, k, T = 32, 4, 12
+    for S in (4, 9, 16):
+        s2e0 = rng.permutation(E)[:S].astype(np.int32)
+        a, b = O.CacheState.from_slots(s2e0, E), O.CacheState.from_slots(s2e0, E)
+        C_ = O.chunk_tokens(T, k, S, E)
+        la = lb = 0
+        for ids in _zipf_ids(rng, 25, T, k, E):
+            la += sum(len(w.miss_e) for w in O.manage_waves(a, ids, O.LRU))
+            lb += sum(len(O.manage(b, ids[t0:t0 + C_], O.LRU).miss_e) for t0 in range(0, T, C_))
+        assert la < lb
+
+
+def test_wave_layer_equals_resident_layer_and_fills_slots():
+    cfg = C.TINY.with_(T=6, S=5, mode=C.MODE_GATHER)
+    rng = np.random.default_rng(5)
+    H, I, E, k, T = cfg.H, cfg.I, cfg.E, cfg.k, cfg.T
+    x = _bf16(rng.standard_normal((T, H)))
+    wr = _bf16(rng.standard_normal((H, E)) * 0.02)
+    host = _bf16(rng.standard_normal((E, 3 * H * I)) * 0.02)
+    s2e0 = rng.permutation(E)[:cfg.S].astype(np.int32)
+    st = O.CacheState.from_slots(s2e0, E)
+    pool = host[s2e0].copy()
+    res = O.layer_forward(x, wr, host, H, I, k, O.GATHER, O.LRU, st, pool, schedule=O.SCHED_WAVES)
+    ref = O.layer_forward(x, wr, host, H, I, k, O.RESIDENT)
+    assert np.array_equal(res["out"], ref["out"]) and np.array_equal(res["ids"], ref["ids"])
+    waves = res["chunks"][0]["waves"]
+    assert len(waves) >= 2  # the step needs more experts than the pool holds
+    for s, e in enumerate(st.s2e):
+        if e >= 0:
+            assert np.array_equal(pool[s], host[e])
+    # a step that fits the pool is one manage call, as in the token-chunk schedule
+    st2 = O.CacheState.from_slots(s2e0, E)
+    st3 = O.CacheState.from_slots(s2e0, E)
+    r2 = O.layer_forward(x[:2], wr, host, H, I, k, O.GATHER, O.LRU, st2, schedule=O.SCHED_WAVES)
+    r3 = O.layer_forward(x[:2], wr, host, H, I, k, O.GATHER, O.LRU, st3)
+    assert r2["chunks"][0]["miss_e"] == r3["chunks"][0]["miss_e"]
+    assert np.array_equal(st2.s2e, st3.s2e) and np.array_equal(st2.prio, st3.prio) and st2.stamp == st3.stamp
+
+
 def test_gather_copies_bytes():
     rng = np.random.default_rng(2)
     host = rng.integers(0, 2 ** 16, size=(8, 40), dtype=np.uint16)
