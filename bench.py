@@ -5,15 +5,18 @@ Default workload (one "step" = one full layer forward: route, permute,
 expert_cache_manage, expert_cache_gather on a side stream, grouped SwiGLU
 FFN, combine): a Qwen3-30B-A3B-shaped decode layer, T=64 tokens, hidden 2048,
 128 experts, top-8, intermediate 768, bf16, 64 of 128 experts in the VRAM slot
-pool, the rest in pinned host memory, LRU.  Each step gets a fresh seeded
-batch, so the routing (near-uniform) changes every step and the cache sees a
-steady miss stream.  Inputs are synthetic (no weights or traces exist here).
+pool, the rest in pinned host memory, LRU, expert-wave schedule (each missing
+expert loaded at most once per step).  Each step gets a fresh seeded batch,
+so the routing (near-uniform) changes every step and the cache sees a steady
+miss stream.  Inputs are synthetic (no weights or traces exist here).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
-Prints one JSON line (rank 0).  --impl reference times the CPU oracle on the
-host cores on a bounded sample of the same workload.  N > 1 (under torchrun)
-runs N independent replicas, one per GPU: the path has no exchange step.
+Prints one JSON line (rank 0), kept short; its last key, ``targets``, holds
+the other workloads' figures (all-resident decode, prefill, token chunks,
+W8A8, the 48-layer stack).  --impl reference times the CPU oracle on the host
+cores on a bounded sample of the same workload.  N > 1 (under torchrun) runs
+N independent replicas, one per GPU: the path has no exchange step.
 """
 from __future__ import annotations
 
@@ -29,7 +32,7 @@ from typing import Optional
 
 if "--impl" in sys.argv and "reference" in sys.argv:
     # the oracle leg: pin the BLAS pools before numpy loads, so "cores" is exact
-    _thr = os.environ.get("MOE_ORACLE_THREADS", "1")
+    _thr = os.environ.get("MOE_ORACLE_THREADS", str(os.cpu_count() or 1))
     for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
         os.environ[_v] = _thr
 
@@ -168,7 +171,8 @@ class Workload:
             self.state = M.CacheState.from_slots(s2e0, cfg.E, dev)
         self.layer = M.SlotCachedMoELayer(self.wr, self.pool, cfg.k, cfg.I, cfg.mode, cfg.policy,
                                           host_slabs=self.host, state=self.state, logit_offset=self.off,
-                                          sel_bias=self.bias, max_tokens=cfg.T, quant=int(quant))
+                                          sel_bias=self.bias, max_tokens=cfg.T, quant=int(quant),
+                                          schedule=cfg.schedule)
         self.xs = [C.draw_x(cfg, dev, step=i) for i in range(n_batches)]
         self.out = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16, device=dev)
         self.out_res = self.out_miss = None
@@ -180,7 +184,7 @@ class Workload:
 
     def chunk(self) -> int:
         c = self.cfg
-        if c.mode != C.MODE_GATHER or c.S >= c.E or c.T * c.k <= c.S:
+        if c.mode != C.MODE_GATHER or c.S >= c.E or c.T * c.k <= c.S or c.schedule == C.SCHED_WAVES:
             return c.T
         return c.S // c.k
 
@@ -217,7 +221,7 @@ class StackWorkload:
                 state = M.CacheState.from_slots(s2e0, cfg.E, dev)
             self.hosts.append(host)
             self.layers.append(M.SlotCachedMoELayer(wr, pool, cfg.k, cfg.I, cfg.mode, cfg.policy, host_slabs=host,
-                                                    state=state, max_tokens=cfg.T))
+                                                    state=state, max_tokens=cfg.T, schedule=cfg.schedule))
         self.stack = M.LayerStack(self.layers, cfg.T)
         # inputs of every step and layer, drawn up front: [steps][L][T][H]
         self.inputs = torch.empty(max(steps, 1), L, cfg.T, cfg.H, dtype=torch.bfloat16, device=dev)
@@ -393,6 +397,30 @@ def policy_replay(trace: np.ndarray, E: int, S: int, dev: str, slab_bytes: int) 
     return out
 
 
+def graph_kernel_nodes(g) -> Optional[int]:
+    """Kernel nodes of a captured torch CUDA graph (kept with keep_graph=True),
+    counted with the driver API: the launches one replay of it makes."""
+    import ctypes
+    try:
+        cu = ctypes.CDLL("libcuda.so.1")
+        graph = ctypes.c_void_p(g.raw_cuda_graph())
+        n = ctypes.c_size_t(0)
+        if cu.cuGraphGetNodes(graph, None, ctypes.byref(n)) != 0:
+            return None
+        nodes = (ctypes.c_void_p * n.value)()
+        if cu.cuGraphGetNodes(graph, nodes, ctypes.byref(n)) != 0:
+            return None
+        kinds = ctypes.c_int(0)
+        count = 0
+        for i in range(n.value):
+            if cu.cuGraphNodeGetType(ctypes.c_void_p(nodes[i]), ctypes.byref(kinds)) != 0:
+                return None
+            count += kinds.value == 0  # CU_GRAPH_NODE_TYPE_KERNEL
+        return count
+    except Exception:
+        return None
+
+
 def _make_prof(M, pairs: int):
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * pairs)]
     for ev in evs:  # torch creates the underlying event lazily, on its first record
@@ -427,13 +455,18 @@ def time_steps(wl: Workload, steps: int, warmup: int, dist=None, clocks=None, pr
     torch.cuda.synchronize()
     misses0, gathered0 = int(wl.layer.stats[0]), int(wl.layer.stats[2])
 
+    nodes = [None]
+
     def run(first, prof_list):
         g = None
         if graph:
-            g = torch.cuda.CUDAGraph()
+            g = torch.cuda.CUDAGraph(keep_graph=True)
             with torch.cuda.graph(g, capture_error_mode="relaxed"):
                 for i in range(steps):
                     wl.step(first + i, prof=None if prof_list is None else prof_list[i][0])
+            if prof_list is None:
+                nodes[0] = graph_kernel_nodes(g)
+            g.instantiate()
             torch.cuda.synchronize()
         s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         s.record()
@@ -467,7 +500,7 @@ def time_steps(wl: Workload, steps: int, warmup: int, dist=None, clocks=None, pr
                 kern[n] += sum(v)
                 launches[n] += len(v)
     return {"ms": ms, "ms_instrumented": ms_prof, "kern_ms": kern, "launches": launches, "clocks": cl,
-            "misses": misses, "gathered_bytes": gathered, "graph": graph}
+            "misses": misses, "gathered_bytes": gathered, "graph": graph, "kernel_nodes": nodes[0]}
 
 
 def count_unique_all(wl: Workload, steps: int, warmup: int) -> int:
@@ -545,15 +578,18 @@ def oracle_sample(cfg: C.LayerConfig, steps: int, warmup: int, dev: str):
     off = None if off is None else off.cpu().numpy()
     xs = [C.draw_x(cfg, gen_dev, step=i).float().cpu().numpy() for i in range(warmup + steps)]
     for i in range(warmup):
-        O.layer_forward(xs[i], wr, _S(), cfg.H, cfg.I, cfg.k, mode, cfg.policy, st, None, off)
+        O.layer_forward(xs[i], wr, _S(), cfg.H, cfg.I, cfg.k, mode, cfg.policy, st, None, off,
+                        schedule=cfg.schedule)
     t0 = time.perf_counter()
     for i in range(steps):
-        O.layer_forward(xs[warmup + i], wr, _S(), cfg.H, cfg.I, cfg.k, mode, cfg.policy, st, None, off)
+        O.layer_forward(xs[warmup + i], wr, _S(), cfg.H, cfg.I, cfg.k, mode, cfg.policy, st, None, off,
+                        schedule=cfg.schedule)
     dt = time.perf_counter() - t0
     cores = int(os.environ.get("OPENBLAS_NUM_THREADS", "0") or 0) or os.cpu_count()
     return {"value": cfg.T * steps / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"{steps} full layer forward(s) of the benchmarked workload (T={cfg.T}), after {warmup} "
-                      f"warm-up; numpy oracle, fp64 FFN", "seconds": dt}
+                      f"warm-up; numpy oracle (python loops for top-k, permute and cache; the fp64 FFN "
+                      f"matmuls in numpy's BLAS on {cores} thread(s))", "seconds": dt}
 
 
 def run_reference(args, ws, rank, dist):
@@ -575,15 +611,17 @@ def run_reference(args, ws, rank, dist):
 # main
 # ----------------------------------------------------------------------------
 
-def main_config() -> C.LayerConfig:
-    return C.qwen(64, S=64, mode=C.MODE_GATHER, policy=C.POLICY_LRU)
+def main_config(schedule: int = C.SCHED_WAVES) -> C.LayerConfig:
+    return C.qwen(64, S=64, mode=C.MODE_GATHER, policy=C.POLICY_LRU, schedule=schedule)
 
 
 def config_obj(cfg: C.LayerConfig) -> dict:
+    sched = "expert waves" if cfg.schedule == C.SCHED_WAVES else "token chunks"
     return {"workload": f"qwen3-30b-a3b-shaped MoE decode layer, T={cfg.T}, H={cfg.H}, E={cfg.E}, k={cfg.k}, "
-                        f"I={cfg.I}, bf16, slot pool {cfg.S} of {cfg.E} (rest pinned host), LRU, gather",
+                        f"I={cfg.I}, bf16, slot pool {cfg.S} of {cfg.E} (rest pinned host), LRU, gather, {sched}",
             "T": cfg.T, "H": cfg.H, "E": cfg.E, "k": cfg.k, "I": cfg.I, "S": cfg.S, "mode": "gather",
-            "policy": "lru", "l2": "inputs larger than L2 (expert weights 1.21 GB; every step streams its experts)",
+            "policy": "lru", "schedule": sched,
+            "l2": "inputs larger than L2 (expert weights 1.21 GB; every step streams its experts)",
             "parallelism": "replicas"}
 
 
@@ -597,6 +635,95 @@ def ffn_roofline(wl: Workload, r: dict, units: int, peaks: dict) -> dict:
             "bytes_per_unit": bytes_per_unit, "units": units, "peak_source": peaks["source"]}
 
 
+def _r(v, d=4):
+    """Round to d significant digits (keeps the JSON line short)."""
+    if v is None or not isinstance(v, float):
+        return v
+    return float(f"{v:.{d}g}")
+
+
+def resident_decode(dev: str, peaks: dict, T: int, quant: bool = False, steps: int = 10, warmup: int = 3) -> dict:
+    """All-resident Qwen-shaped decode layer: step time, FFN and whole-layer HBM fractions on unique expert bytes."""
+    c = C.qwen(T, S=128, mode=C.MODE_RESIDENT)
+    w = Workload(c, 2 * steps + warmup, dev, quant=quant)
+    r = time_steps(w, steps, warmup)
+    units = count_unique_all(w, steps, warmup + steps)
+    t_ffn = (r["kern_ms"]["ffn_gateup"] + r["kern_ms"]["ffn_down"]) * 1e-3
+    ffn = units * w.slab_bytes / t_ffn / 1e9 / peaks["hbm_gbs"] if t_ffn > 0 else 0.0
+    layer = count_unique_all(w, steps, warmup) * w.slab_bytes / (r["ms"] * 1e-3) / 1e9 / peaks["hbm_gbs"]
+    del w
+    torch.cuda.empty_cache()
+    return {"us": 1e3 * r["ms"] / steps, "layer_hbm": layer, "ffn_hbm": ffn}
+
+
+def prefill_line(dev: str, peaks: dict, steps: int = 3, warmup: int = 3) -> dict:
+    """Prefill T=4096, all experts resident, skewed groups: FFN GEMMs against bf16 peak (and HBM)."""
+    cp = C.PREFILL
+    wp = Workload(cp, 2 * steps + warmup, dev)
+    rp = time_steps(wp, steps, warmup)
+    flops = 6.0 * cp.T * cp.k * cp.H * cp.I
+    w_bytes = count_unique_all(wp, steps, warmup + steps) * cp.slab_bytes / steps
+    t_ffn = (rp["kern_ms"]["ffn_gateup"] + rp["kern_ms"]["ffn_down"]) * 1e-3 / steps
+    t_layer = rp["ms"] * 1e-3 / steps
+    del wp
+    torch.cuda.empty_cache()
+    return {"ms": t_layer * 1e3, "tok_s": cp.T / t_layer, "ffn_tflops": flops / t_ffn / 1e12,
+            "ffn_tc": flops / t_ffn / 1e12 / peaks["bf16_tflops"], "ffn_hbm": w_bytes / t_ffn / 1e9 / peaks["hbm_gbs"],
+            "layer_tflops": flops / t_layer / 1e12}
+
+
+def gather_line(dev: str, T: int, schedule: int, quant: bool = False, steps: int = 10, warmup: int = 3) -> dict:
+    c = C.qwen(T, S=64, schedule=schedule)
+    w = Workload(c, 2 * steps + warmup, dev, quant=quant)
+    r = time_steps(w, steps, warmup, profile=False)
+    del w
+    torch.cuda.empty_cache()
+    return {"tok_s": T * steps / (r["ms"] * 1e-3), "misses": r["misses"] / steps}
+
+
+def targets(dev: str, peaks: dict) -> dict:
+    """The figures the performance targets are stated in, one flat object."""
+    t = {}
+    for T in (1, 8, 64):
+        d = resident_decode(dev, peaks, T)
+        t[f"res_T{T}_us"], t[f"res_T{T}_layer_hbm"], t[f"res_T{T}_ffn_hbm"] = d["us"], d["layer_hbm"], d["ffn_hbm"]
+    p = prefill_line(dev, peaks)
+    t["prefill_ms"], t["prefill_ffn_tc"], t["prefill_ffn_tflops"], t["prefill_ffn_hbm"] = \
+        p["ms"], p["ffn_tc"], p["ffn_tflops"], p["ffn_hbm"]
+    for T in (1, 8, 32):
+        g = gather_line(dev, T, C.SCHED_WAVES)
+        t[f"gather_T{T}_tok_s"] = g["tok_s"]
+    g = gather_line(dev, 64, C.SCHED_CHUNKS)
+    t["gather_T64_chunks_tok_s"], t["gather_T64_chunks_misses"] = g["tok_s"], g["misses"]
+    for T in (1, 8, 64):
+        d = resident_decode(dev, peaks, T, quant=True)
+        t[f"q8_res_T{T}_us"], t[f"q8_res_T{T}_ffn_hbm"] = d["us"], d["ffn_hbm"]
+    t["q8_gather_T64_tok_s"] = gather_line(dev, 64, C.SCHED_WAVES, quant=True)["tok_s"]
+    st = stack_variant(dev, peaks, C.STACK)
+    t["stack48_tok_s"], t["stack48_hbm"] = st["tokens_per_s"], st["hbm"]["frac"]
+    st = stack_variant(dev, peaks, C.STACK_SLOTS.with_(schedule=C.SCHED_WAVES), steps=4)
+    t["stack48_slots_tok_s"], t["stack48_slots_link_GB"] = st["tokens_per_s"], st["host_link_GB_per_step"]
+    return {k: _r(v) for k, v in t.items()}
+
+
+def oracle_baselines(local: int) -> dict:
+    """The oracle leg timed twice: numpy's BLAS on one thread and on every host core."""
+    out = {}
+    for thr in ("1", str(os.cpu_count() or 1)):
+        env = dict(os.environ, MOE_ORACLE_THREADS=thr, WORLD_SIZE="1", RANK="0", LOCAL_RANK=str(local))
+        p = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "2",
+                            "--warmup", "0"], capture_output=True, text=True, env=env)
+        try:
+            out[thr] = json.loads(p.stdout.strip().splitlines()[-1])["cpu_baseline"]
+        except Exception:
+            out[thr] = {"value": None, "error": (p.stderr or p.stdout)[-200:]}
+    one, allc = out["1"], out[str(os.cpu_count() or 1)]
+    best = allc if (allc.get("value") or 0) >= (one.get("value") or 0) else one
+    return {"value": best.get("value"), "unit": UNIT, "cores": best.get("cores"), "kind": "oracle",
+            "sample": best.get("sample", best.get("error")), "value_cores_1": _r(one.get("value")),
+            "value_cores_all": _r(allc.get("value")), "cores_all": os.cpu_count()}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -606,8 +733,8 @@ def main():
     ap.add_argument("--no-variants", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="main",
-                    help="main (default) | prefill | resident_T<n> | gather_T<n> | routing_variants | w8a8 | stack | "
-                         "stack_slots: one workload alone "
+                    help="main (default) | prefill | resident_T<n> | gather_T<n> | chunks_T<n> | routing_variants | "
+                         "policy_replay | w8a8 | stack | stack_slots | stack_slots_chunks: one workload alone "
                          "(for profiling); prints its own JSON line")
     args = ap.parse_args()
     ws, rank, local, dist = _dist()
@@ -628,8 +755,16 @@ def main():
         if rank == 0:
             print(json.dumps({"workload": "routing_variants", **routing_variants(dev, args.steps, args.warmup)}))
         return
-    if args.workload in ("stack", "stack_slots"):
-        cfg_s = C.STACK if args.workload == "stack" else C.STACK_SLOTS
+    if args.workload == "policy_replay":
+        cfg = main_config()
+        if rank == 0:
+            print(json.dumps({"workload": "policy_replay",
+                              **policy_replay(C.drifting_trace(cfg.E, cfg.k, 8, 400), cfg.E, cfg.S, dev,
+                                              cfg.slab_bytes)}))
+        return
+    if args.workload in ("stack", "stack_slots", "stack_slots_chunks"):
+        cfg_s = {"stack": C.STACK, "stack_slots": C.STACK_SLOTS.with_(schedule=C.SCHED_WAVES),
+                 "stack_slots_chunks": C.STACK_SLOTS}[args.workload]
         if rank == 0:
             print(json.dumps({"workload": args.workload, **stack_variant(dev, peaks, cfg_s, args.steps, args.warmup)}))
         return
@@ -640,7 +775,9 @@ def main():
         elif w.startswith("resident_T"):
             c = C.qwen(int(w[len("resident_T"):]), S=128, mode=C.MODE_RESIDENT)
         elif w.startswith("gather_T"):
-            c = C.qwen(int(w[len("gather_T"):]), S=64)
+            c = C.qwen(int(w[len("gather_T"):]), S=64, schedule=C.SCHED_WAVES)
+        elif w.startswith("chunks_T"):
+            c = C.qwen(int(w[len("chunks_T"):]), S=64)
         else:
             raise SystemExit(f"unknown workload {w}")
         wl = Workload(c, 2 * args.steps + args.warmup, dev)
@@ -649,6 +786,9 @@ def main():
             print(json.dumps({"workload": w, "clocks": r["clocks"], "ms_per_step": r["ms"] / args.steps,
                               "ms_per_step_instrumented": r["ms_instrumented"] / args.steps,
                               "tokens_per_s": c.T * args.steps / (r["ms"] * 1e-3),
+                              "misses_per_step": r["misses"] / args.steps,
+                              "kernel_nodes_per_step": None if r["kernel_nodes"] is None
+                              else r["kernel_nodes"] / args.steps,
                               "kernels_ms_per_step": {n: v / args.steps for n, v in r["kern_ms"].items()}}))
         return
     cfg = main_config()
@@ -657,7 +797,6 @@ def main():
     wl = Workload(cfg, 2 * K + W, dev)
     clocks = Clocks(local)
     r = time_steps(wl, K, W, dist, clocks)
-    units = count_unique_all(wl, K, W + K)  # expert units of the instrumented steps (kernel times)
     value = ws * cfg.T * K / (r["ms"] * 1e-3)
     link_peak = host_link_peak(dev)
     kern = r["kern_ms"]
@@ -666,92 +805,31 @@ def main():
         t = kern["gather"] * 1e-3
         ach = r["gathered_bytes"] / t / 1e9 if t > 0 else 0.0
         n_launch = max(1, r["launches"].get("gather", 0))
-        roof = {"bound": "host-link", "achieved": ach, "peak": link_peak, "unit": "GB/s", "frac": ach / link_peak,
-                "traffic": GATHER_DRAM_BYTES_PER_MISS * r["misses"] / n_launch,
-                "traffic_unit": "bytes per launch (ncu dram read + write per miss x misses per launch)",
-                "kernel": "gather", "bytes_per_unit": cfg.slab_bytes,
-                "units": r["misses"], "peak_source": "pinned-host->device cudaMemcpyAsync measured in this run"}
+        roof = {"bound": "host-link", "achieved": _r(ach), "peak": _r(link_peak), "unit": "GB/s",
+                "frac": _r(ach / link_peak), "traffic": _r(GATHER_DRAM_BYTES_PER_MISS * r["misses"] / n_launch),
+                "kernel": "gather", "bytes_per_unit": cfg.slab_bytes, "units": r["misses"],
+                "peak_source": "pinned-host->device cudaMemcpyAsync measured in this run"}
     else:
-        roof = ffn_roofline(wl, r, units, peaks)
+        units = count_unique_all(wl, K, W + K)
+        roof = {k: _r(v) for k, v in ffn_roofline(wl, r, units, peaks).items()}
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": K, "warmup": W,
             "ms_per_step": r["ms"] / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "timed_as": "one CUDA-graph replay of the K steps (eager warm-ups)",
             "dtype": "bf16", "data": "synthetic (seeded, Irwin-Hall normal weights/activations)",
             "config": config_obj(cfg), "roofline": roof, "clocks": r["clocks"],
-            "gpu_launches": sum(r["launches"].values()),
-            "kernels_ms_per_step": {n: v / K for n, v in kern.items()},
-            "misses_per_step": r["misses"] / K, "gathered_GB_per_step": r["gathered_bytes"] / K / 1e9,
-            "host_link_peak_gbs": link_peak}
+            "gpu_launches": r["kernel_nodes"] if r["kernel_nodes"] is not None else sum(r["launches"].values()),
+            "timed_as": "one CUDA-graph replay of the K steps (eager warm-ups)",
+            "misses_per_step": r["misses"] / K,
+            "kernels_ms_per_step": {n: _r(v / K) for n, v in kern.items() if v > 0}}
     line["e2e"] = e2e_steps(wl, K, W, dist)
     del wl
     torch.cuda.empty_cache()
-
+    tg = None
     if not args.no_variants:
-        var = {}
-        # all-resident control: the HBM roofline of the decode FFN
-        for T in (1, 8, 64):
-            c2 = C.qwen(T, S=128, mode=C.MODE_RESIDENT)
-            w2 = Workload(c2, 2 * 10 + 3, dev)
-            r2 = time_steps(w2, 10, 3)
-            u2 = count_unique_all(w2, 10, 3 + 10)
-            var[f"all_resident_T{T}"] = {"tokens_per_s": T * 10 / (r2["ms"] * 1e-3), "ms_per_step": r2["ms"] / 10,
-                                         "kernels_ms_per_step": {n: v / 10 for n, v in r2["kern_ms"].items()},
-                                         "ffn_hbm": ffn_roofline(w2, r2, u2, peaks),
-                                         "layer_hbm_frac": count_unique_all(w2, 10, 3) * c2.slab_bytes
-                                         / (r2["ms"] * 1e-3) / 1e9 / peaks["hbm_gbs"]}
-            del w2
-        # prefill: all experts resident, T=4096, skewed groups (tcgen05 grouped GEMMs)
-        cp = C.PREFILL
-        wp = Workload(cp, 2 * 3 + 3, dev)
-        rp = time_steps(wp, 3, 3)
-        flops = 6.0 * cp.T * cp.k * cp.H * cp.I
-        # unique experts' weights per step, over the instrumented steps the kernel times come from
-        w_bytes = count_unique_all(wp, 3, 3 + 3) * cp.slab_bytes / 3.0
-        t_ffn = (rp["kern_ms"]["ffn_gateup"] + rp["kern_ms"]["ffn_down"]) * 1e-3 / 3
-        t_layer = rp["ms"] * 1e-3 / 3
-        pk = peaks["bf16_tflops"]
-        var["prefill_T4096"] = {"tokens_per_s": cp.T / t_layer, "ms_per_step": rp["ms"] / 3,
-                                "kernels_ms_per_step": {n: v / 3 for n, v in rp["kern_ms"].items()},
-                                "ffn_tensor": {"bound": "tensor", "achieved": flops / t_ffn / 1e12, "peak": pk,
-                                               "unit": "TFLOP/s", "frac": flops / t_ffn / 1e12 / pk,
-                                               "flops_per_step": flops, "kernel": "ffn_gateup+ffn_down (tcgen05)"},
-                                # the same kernels against HBM: each routed expert's weights once per step (about 256
-                                # flop per weight byte, below this part's ridge of bf16 peak / HBM bandwidth)
-                                "ffn_hbm": {"bound": "hbm", "achieved": w_bytes / t_ffn / 1e9, "peak": peaks["hbm_gbs"],
-                                            "unit": "GB/s", "frac": w_bytes / t_ffn / 1e9 / peaks["hbm_gbs"],
-                                            "bytes_per_step": w_bytes, "flop_per_byte": flops / w_bytes,
-                                            "ridge_flop_per_byte": pk * 1e12 / (peaks["hbm_gbs"] * 1e9),
-                                            "kernel": "ffn_gateup+ffn_down (tcgen05)"},
-                                "layer_tflops": flops / t_layer / 1e12}
-        del wp
-        torch.cuda.empty_cache()
-        for T in (1, 8, 32):
-            c3 = C.qwen(T, S=64)
-            w3 = Workload(c3, 2 * 10 + 3, dev)
-            r3 = time_steps(w3, 10, 3, profile=False)
-            var[f"gather_T{T}"] = {"tokens_per_s": T * 10 / (r3["ms"] * 1e-3), "ms_per_step": r3["ms"] / 10,
-                                   "misses_per_step": r3["misses"] / 10}
-            del w3
-        torch.cuda.empty_cache()
-        var["policy_replay"] = policy_replay(C.drifting_trace(cfg.E, cfg.k, 8, 400), cfg.E, cfg.S, dev,
-                                             cfg.slab_bytes)
-        torch.cuda.empty_cache()
-        var["routing_variants"] = routing_variants(dev)
-        torch.cuda.empty_cache()
-        var["w8a8"] = w8a8_variants(dev, peaks)
-        torch.cuda.empty_cache()
-        var["stack48_resident"] = stack_variant(dev, peaks, C.STACK)
-        line["variants"] = var
-
+        tg = targets(dev, peaks)
     if not args.no_cpu_baseline and rank == 0:
-        env = dict(os.environ, MOE_ORACLE_THREADS="1", WORLD_SIZE="1", RANK="0", LOCAL_RANK=str(local))
-        p = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "2",
-                            "--warmup", "0"], capture_output=True, text=True, env=env)
-        try:
-            ref = json.loads(p.stdout.strip().splitlines()[-1])
-            line["cpu_baseline"] = ref["cpu_baseline"]
-        except Exception:
-            line["cpu_baseline"] = {"value": None, "error": (p.stderr or p.stdout)[-300:]}
+        line["cpu_baseline"] = oracle_baselines(local)
+    if tg is not None:
+        line["targets"] = tg  # last: the end of the line is what a truncated log keeps
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist is not None:

@@ -11,4 +11,4 @@ from .binding import (MODE_GATHER, MODE_RESIDENT, MODE_ZERO_RETURN, POLICY_LFU, 
                       cache_gather, cache_manage, combine, expert_ffn, ffn_workspace_bytes, layer_workspace_bytes,
                       lib, permute, route, status_str, LayerStack, BIAS_GRADED, BIAS_FLAT, BIAS_HARD,
                       ROUTE_SIGMOID, ROUTE_DAMPED, cache_count, cache_repick,
-                      q8_slab_bytes, quantize_slabs, expert_ffn_q8)
+                      q8_slab_bytes, quantize_slabs, expert_ffn_q8, SCHED_CHUNKS, SCHED_WAVES)

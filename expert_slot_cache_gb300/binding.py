@@ -47,7 +47,8 @@ class LayerArgs(ctypes.Structure):
                 ("ids", c_void_p), ("w", c_void_p), ("out", c_void_p), ("out_res", c_void_p),
                 ("out_miss", c_void_p), ("stats", c_void_p), ("dev_status", c_void_p),
                 ("workspace", c_void_p), ("workspace_bytes", c_size_t), ("prof", POINTER(Prof)),
-                ("affinity", c_float), ("route_flags", c_int32), ("window_counts", c_void_p), ("quant", c_int32)]
+                ("affinity", c_float), ("route_flags", c_int32), ("window_counts", c_void_p), ("quant", c_int32),
+                ("schedule", c_int32)]
 
 
 def _sig(name, argtypes, restype=c_int):
@@ -66,6 +67,7 @@ _route = _sig("moe_route", [V, V, V, V, V, c_float, I32, I32, I32, I32, V, V, V,
 _route_ex = _sig("moe_route_ex", [V, V, V, V, V, c_float, I32, I32, I32, I32, I32, V, V, V, V, V])
 
 BIAS_GRADED, BIAS_FLAT, BIAS_HARD = 0, 1, 2
+SCHED_CHUNKS, SCHED_WAVES = 0, 1
 ROUTE_SIGMOID, ROUTE_DAMPED = 1, 2
 _route_scratch = _sig("moe_route_scratch_bytes", [I32, I32, I32], c_size_t)
 _permute = _sig("moe_permute", [V, I32, I32, V, V, V, V, V, V, V, V, V])
@@ -313,7 +315,7 @@ class SlotCachedMoELayer:
 
     def __init__(self, w_router, pool, k, I, mode, policy=POLICY_LRU, host_slabs=None, state=None,
                  logit_offset=None, sel_bias=None, max_tokens=64, side_stream=True, affinity=0.0,
-                 route_flags=0, window_counts=None, quant=0):
+                 route_flags=0, window_counts=None, quant=0, schedule=0):
         self.w_router, self.pool, self.k, self.I = w_router, pool, k, I
         self.H, self.E = w_router.shape
         self.S = pool.shape[0]
@@ -324,6 +326,7 @@ class SlotCachedMoELayer:
         self.route_flags = int(route_flags)
         self.window_counts = window_counts
         self.quant = int(quant)  # pool / host hold W8A8 slabs (quantize_slabs)
+        self.schedule = int(schedule)  # SCHED_CHUNKS or SCHED_WAVES (GATHER steps larger than the pool)
         dev = pool.device
         self.stats = torch.zeros(4, dtype=torch.int64, device=dev)
         self.dev_status = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -352,7 +355,7 @@ class SlotCachedMoELayer:
                       ids.data_ptr(), w.data_ptr(), out.data_ptr(), _ptr(out_res), _ptr(out_miss),
                       self.stats.data_ptr(), self.dev_status.data_ptr(), self.workspace.data_ptr(),
                       self.workspace.numel(), ctypes.pointer(prof) if prof is not None else None, self.affinity,
-                      self.route_flags, _ptr(self.window_counts), self.quant)
+                      self.route_flags, _ptr(self.window_counts), self.quant, self.schedule)
         main = torch.cuda.current_stream() if stream is None else stream
         # the library forks to and joins back from the side stream itself
         _ck(_layer(ctypes.byref(a), c_void_p(main.cuda_stream),

@@ -13,7 +13,7 @@ static size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
 // Workspace layout of the layer forward, for chunks of up to n = C*k routing slots.
 struct LayerWs {
-  int32_t *count, *offset, *rows, *pos, *act_e, *n_act, *miss_e, *miss_s, *n_miss, *hit_e, *n_hit;
+  int32_t *count, *offset, *rows, *pos, *act_e, *n_act, *miss_e, *miss_s, *n_miss, *hit_e, *n_hit, *def_e, *n_def;
   float *hbuf, *y, *logits, *route;
   uint16_t *xp, *hb;
   int32_t* perm;
@@ -44,6 +44,8 @@ static LayerWs carve(void* base, int n, int H, int E, int I, int T) {
   w.n_miss = (int32_t*)take(4);
   w.hit_e = (int32_t*)take(4 * (size_t)lmax);
   w.n_hit = (int32_t*)take(4);
+  w.def_e = (int32_t*)take(4 * (size_t)lmax);
+  w.n_def = (int32_t*)take(4);
   w.hbuf = (float*)take(4 * (size_t)n * I);
   w.y = (float*)take(4 * (size_t)n * H);
   w.logits = (float*)take(4 * (size_t)T * E);
@@ -59,10 +61,17 @@ static LayerWs carve(void* base, int n, int H, int E, int I, int T) {
   return w;
 }
 
-static int chunk_tokens(int T, int k, int S, int E, int mode, int policy) {
-  if (mode != MOE_MODE_GATHER || policy == MOE_POLICY_STATIC) return T;
+static int chunk_tokens(int T, int k, int S, int E, int mode, int policy, int schedule) {
+  if (mode != MOE_MODE_GATHER || policy == MOE_POLICY_STATIC || schedule == MOE_SCHED_WAVES) return T;
   if (S >= E || T * k <= S) return T;
   return S / k;
+}
+
+// Manage calls after the first one in the expert-wave schedule: the deferred
+// experts (at most min(n, E) - S of them) in batches of S.
+static int later_waves(int n, int E, int S) {
+  const int most = std::min(n, E) - S;
+  return most > 0 ? (most + S - 1) / S : 0;
 }
 
 // Two cached events per device for the fork/join with the side stream.
@@ -185,10 +194,12 @@ extern "C" int moe_layer_forward(const moe_layer_args* a, moe_stream_t main_s, m
   if (mode == MOE_MODE_ZERO_RETURN && (!a->out_res || !a->out_miss)) return MOE_ERR_ARG;
   if (a->quant != 0 && a->quant != 1) return MOE_ERR_ARG;
   if (a->quant && (mode == MOE_MODE_ZERO_RETURN || H % 16 || I % 16)) return MOE_ERR_ARG;
-  if (mode == MOE_MODE_GATHER && S < E && S < k) return MOE_ERR_CAPACITY;
+  if (a->schedule != MOE_SCHED_CHUNKS && a->schedule != MOE_SCHED_WAVES) return MOE_ERR_ARG;
+  const bool waves = mode == MOE_MODE_GATHER && a->schedule == MOE_SCHED_WAVES;
+  if (mode == MOE_MODE_GATHER && !waves && S < E && S < k) return MOE_ERR_CAPACITY;
   if ((uintptr_t)a->pool % 16 || (uintptr_t)a->workspace % 256 || (uintptr_t)a->x % 16) return MOE_ERR_ALIGN;
 
-  const int C = chunk_tokens(T, k, S, E, mode, policy);
+  const int C = chunk_tokens(T, k, S, E, mode, policy, a->schedule);
   LayerWs ws = carve(a->workspace, C * k, H, E, I, T);
   if (a->workspace_bytes < ws.bytes) return MOE_ERR_ALIGN;
 
@@ -246,8 +257,11 @@ extern "C" int moe_layer_forward(const moe_layer_args* a, moe_stream_t main_s, m
       if ((r = ffn(f, ms)) != MOE_OK) return r;
     } else {
       prof.begin(MOE_PROF_MANAGE, ms);
+      ManageWave w0;  // expert waves: the misses that find no free slot are deferred
+      w0.def_e = ws.def_e;
+      w0.n_def = ws.n_def;
       r = launch_manage(ids_c, n, E, S, policy, a->e2s, a->s2e, a->prio, a->stamp, ws.miss_e, ws.miss_s, ws.n_miss,
-                        ws.hit_e, ws.n_hit, nullptr, stats, a->dev_status, ms);
+                        ws.hit_e, ws.n_hit, nullptr, stats, a->dev_status, ms, waves ? &w0 : nullptr);
       if (r != MOE_OK) return r;
       prof.end(ms);
       FfnArgs fh = f, fm = f;
@@ -272,6 +286,34 @@ extern "C" int moe_layer_forward(const moe_layer_args* a, moe_stream_t main_s, m
         if ((r = ffn(fh, ms)) != MOE_OK) return r;
         if (two) MOE_CUDA_TRY(cudaStreamWaitEvent(ms, ev->join, 0));
         if ((r = ffn(fm, ms)) != MOE_OK) return r;
+        // later waves: the next S deferred experts evict slots whose experts this
+        // step has computed already; their gather follows those FFN launches
+        const int nw = waves ? later_waves(n, E, S) : 0;
+        const int wmax = std::min(S, lmax);
+        for (int wv = 1; wv <= nw; ++wv) {
+          ManageWave bw;
+          bw.n_dev = ws.n_def;
+          bw.n_off = (wv - 1) * S;
+          prof.begin(MOE_PROF_MANAGE, ms);
+          r = launch_manage(ws.def_e, wmax, E, S, policy, a->e2s, a->s2e, a->prio, a->stamp, ws.miss_e, ws.miss_s,
+                            ws.n_miss, nullptr, nullptr, nullptr, stats, a->dev_status, ms, &bw);
+          if (r != MOE_OK) return r;
+          prof.end(ms);
+          if (two) {
+            MOE_CUDA_TRY(cudaEventRecord(ev->fork, ms));
+            MOE_CUDA_TRY(cudaStreamWaitEvent(ss, ev->fork, 0));
+          }
+          prof.begin(MOE_PROF_GATHER, side);
+          r = launch_gather(a->host_slabs, a->pool, slab_bytes, E, S, ws.miss_e, ws.miss_s, ws.n_miss, wmax, stats,
+                            a->dev_status, side);
+          if (r != MOE_OK) return r;
+          prof.end(side);
+          if (two) {
+            MOE_CUDA_TRY(cudaEventRecord(ev->join, ss));
+            MOE_CUDA_TRY(cudaStreamWaitEvent(ms, ev->join, 0));
+          }
+          if ((r = ffn(fm, ms)) != MOE_OK) return r;
+        }
       } else {
         // zero-return: resident experts from the pool on main, missing ones
         // straight from the host store on the side stream; then one add.

@@ -19,13 +19,33 @@ constexpr int kManageThreads = 1024;
 constexpr int kMaxS = 4096;
 
 // Shared memory (dynamic): need[E] | e2s[E] | mrank[E] | hrank[E] | s2e[S] | prio[S] | cand[S] | vict[S]
+//
+// ids[0 .. n) are the call's routing ids.  With n_dev the call reads
+// ids[n_off .. n_off + m) instead, m = clamp(*n_dev - n_off, 0, n): a batch of
+// a device-side list (the later waves of the expert-wave schedule); m = 0 is
+// no call (nothing changes, stamp included).  With def_e (wave 0 of that
+// schedule) the misses beyond the available victims are not loaded: they go,
+// in ascending id, to def_e / *n_def, and *n_miss counts the loaded ones.
 __global__ void __launch_bounds__(kManageThreads) manage_kernel(
-    const int32_t* __restrict__ ids, int n, int E, int S, int policy, int32_t* __restrict__ e2s_g,
-    int32_t* __restrict__ s2e_g, uint32_t* __restrict__ prio_g, uint32_t* __restrict__ stamp_g,
-    int32_t* __restrict__ miss_e, int32_t* __restrict__ miss_s, int32_t* __restrict__ n_miss,
-    int32_t* __restrict__ hit_e, int32_t* __restrict__ n_hit, int32_t* __restrict__ sid,
+    const int32_t* __restrict__ ids, int n, const int32_t* __restrict__ n_dev, int n_off, int E, int S, int policy,
+    int32_t* __restrict__ e2s_g, int32_t* __restrict__ s2e_g, uint32_t* __restrict__ prio_g,
+    uint32_t* __restrict__ stamp_g, int32_t* __restrict__ miss_e, int32_t* __restrict__ miss_s,
+    int32_t* __restrict__ n_miss, int32_t* __restrict__ hit_e, int32_t* __restrict__ n_hit,
+    int32_t* __restrict__ sid, int32_t* __restrict__ def_e, int32_t* __restrict__ n_def,
     int64_t* __restrict__ stats, int32_t* __restrict__ status) {
   extern __shared__ int man_smem[];
+  if (n_dev) {
+    n = min(max(*n_dev - n_off, 0), n);
+    ids += n_off;
+    if (n == 0) {
+      if (threadIdx.x == 0) {
+        *n_miss = 0;
+        if (n_hit) *n_hit = 0;
+        if (n_def) *n_def = 0;
+      }
+      return;
+    }
+  }
   int* need = man_smem;
   int* e2s = need + E;
   int* mrank = e2s + E;
@@ -80,12 +100,23 @@ __global__ void __launch_bounds__(kManageThreads) manage_kernel(
     s_nhit = carry_h;
   }
   // Candidate slots: not holding an expert this step needs.
-  for (int s = tid; s < S; s += kManageThreads) {
-    const int e = s2e[s];
-    cand[s] = !(e >= 0 && e < E && need[e]);
+  int carry_c = 0;
+  for (int s0 = 0; s0 < S; s0 += kManageThreads) {
+    const int s = s0 + tid;
+    int c = 0;
+    if (s < S) {
+      const int e = s2e[s];
+      c = !(e >= 0 && e < E && need[e]);
+      cand[s] = c;
+    }
+    int tc;
+    block_exclusive_scan(c, tmp, &tc);
+    carry_c += tc;
   }
   __syncthreads();
   const int nm = s_nmiss;
+  // misses that get a slot: all of them, or with deferral as many as there are candidates
+  const int nl = (def_e && policy != MOE_POLICY_STATIC) ? min(nm, carry_c) : nm;
 
   if (policy != MOE_POLICY_STATIC) {
     // Victim rank of each candidate: empty first (ascending slot), then
@@ -126,6 +157,10 @@ __global__ void __launch_bounds__(kManageThreads) manage_kernel(
   for (int e = tid; e < E; e += kManageThreads) {
     const int r = mrank[e];
     if (r < 0) continue;
+    if (r >= nl) {  // deferred to a later wave: stays cold
+      def_e[r - nl] = e;
+      continue;
+    }
     miss_e[r] = e;
     if (policy == MOE_POLICY_STATIC) {
       miss_s[r] = -1;
@@ -157,10 +192,11 @@ __global__ void __launch_bounds__(kManageThreads) manage_kernel(
   }
   if (tid == 0) {
     *stamp_g = stamp;
-    *n_miss = nm;
+    *n_miss = nl;
     if (n_hit) *n_hit = s_nhit;
+    if (n_def) *n_def = nm - nl;
     if (stats) {
-      stats[0] += nm;
+      stats[0] += nl;
       stats[1] += 1;
     }
   }
@@ -308,12 +344,16 @@ int launch_window_add(const int32_t* count, int E, int32_t* counts, cudaStream_t
 
 int launch_manage(const int32_t* ids, int n, int E, int S, int policy, int32_t* e2s, int32_t* s2e, uint32_t* prio,
                   uint32_t* stamp, int32_t* miss_e, int32_t* miss_s, int32_t* n_miss, int32_t* hit_e,
-                  int32_t* n_hit, int32_t* sid, int64_t* stats, int32_t* dev_status, cudaStream_t stream) {
+                  int32_t* n_hit, int32_t* sid, int64_t* stats, int32_t* dev_status, cudaStream_t stream,
+                  const ManageWave* wave) {
   const size_t smem = (size_t)4 * E * sizeof(int) + (size_t)4 * S * sizeof(int);
   static bool attr_done[64] = {};
   MOE_CUDA_TRY(ensure_smem(manage_kernel, (int)(4 * kMaxE * 4 + 4 * kMaxS * 4), attr_done));
-  manage_kernel<<<1, kManageThreads, smem, stream>>>(ids, n, E, S, policy, e2s, s2e, prio, stamp, miss_e, miss_s,
-                                                     n_miss, hit_e, n_hit, sid, stats, dev_status);
+  const ManageWave nw{};
+  const ManageWave& w = wave ? *wave : nw;
+  manage_kernel<<<1, kManageThreads, smem, stream>>>(ids, n, w.n_dev, w.n_off, E, S, policy, e2s, s2e, prio, stamp,
+                                                     miss_e, miss_s, n_miss, hit_e, n_hit, sid, w.def_e, w.n_def,
+                                                     stats, dev_status);
   MOE_LAUNCH_CHECK();
   return MOE_OK;
 }

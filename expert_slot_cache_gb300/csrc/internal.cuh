@@ -79,9 +79,19 @@ int launch_prefill(const FfnArgs& a, int n, int max_list, cudaStream_t stream, P
 int launch_combine(const float* y, const float* w, const int32_t* pos, const int32_t* ids, const int32_t* e2s, int T,
                    int k, int H, int E, int split, void* out, float* out_res, float* out_miss, cudaStream_t stream,
                    const uint16_t* yb = nullptr);
+// Expert-wave options of one manage call: wave 0 defers the misses that find no
+// victim (def_e, n_def); a later wave manages ids[n_off .. n_off + m) with
+// m = clamp(*n_dev - n_off, 0, n) read on the device (no call when m = 0).
+struct ManageWave {
+  int32_t* def_e = nullptr;
+  int32_t* n_def = nullptr;
+  const int32_t* n_dev = nullptr;
+  int n_off = 0;
+};
 int launch_manage(const int32_t* ids, int n, int E, int S, int policy, int32_t* e2s, int32_t* s2e, uint32_t* prio,
                   uint32_t* stamp, int32_t* miss_e, int32_t* miss_s, int32_t* n_miss, int32_t* hit_e,
-                  int32_t* n_hit, int32_t* sid, int64_t* stats, int32_t* dev_status, cudaStream_t stream);
+                  int32_t* n_hit, int32_t* sid, int64_t* stats, int32_t* dev_status, cudaStream_t stream,
+                  const ManageWave* wave = nullptr);
 int launch_gather(const void* host_slabs, void* pool, size_t slab_bytes, int E, int S, const int32_t* miss_e,
                   const int32_t* miss_s, const int32_t* n_miss, int max_miss, int64_t* stats, int32_t* dev_status,
                   cudaStream_t stream);

@@ -31,6 +31,8 @@ MODE_ZERO_RETURN = 2
 POLICY_LRU = 0
 POLICY_LFU = 1
 POLICY_STATIC = 2
+SCHED_CHUNKS = 0
+SCHED_WAVES = 1
 
 W_SIGMA = 0.02
 X_SIGMA = 1.0
@@ -56,6 +58,8 @@ class LayerConfig:
     zipf_s: float = 0.0
     layers: int = 1
     steps: int = 1
+    # GATHER steps larger than the pool: token chunks or expert waves
+    schedule: int = SCHED_CHUNKS
 
     @property
     def slab_elems(self) -> int:
@@ -75,8 +79,9 @@ QWEN = LayerConfig("qwen3-30b-a3b-decode", T=8, H=2048, E=128, k=8, I=768, S=64,
                    seed=2, x_seed=2008, mode=MODE_GATHER, policy=POLICY_LRU)
 
 
-def qwen(T: int, S: int = 64, mode: int = MODE_GATHER, policy: int = POLICY_LRU) -> LayerConfig:
-    return QWEN.with_(T=T, S=S, x_seed=2000 + T, mode=mode, policy=policy)
+def qwen(T: int, S: int = 64, mode: int = MODE_GATHER, policy: int = POLICY_LRU,
+         schedule: int = SCHED_CHUNKS) -> LayerConfig:
+    return QWEN.with_(T=T, S=S, x_seed=2000 + T, mode=mode, policy=policy, schedule=schedule)
 
 
 FLASH = LayerConfig("flash-next-zero-return", T=16, H=2048, E=512, k=10, I=512, S=192,

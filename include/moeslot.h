@@ -399,6 +399,31 @@ int moe_expert_ffn_q8(const void* x, int T, int H, int I, int k, int E, const in
                       const int32_t* e2s, float* y, void* workspace, size_t workspace_bytes, int32_t* dev_status,
                       moe_stream_t stream);
 
+/*
+ * How GATHER mode serves a step that needs more experts than the pool holds
+ * ("Porting vllm-expert-cache to NVIDIA GPUs", "Measuring, without fooling
+ * yourself": a step is served from slots only when tokens x top_k <= slots;
+ * count misses, not tokens).
+ *   MOE_SCHED_CHUNKS  the step is cut into chunks of floor(S/k) consecutive
+ *                     tokens, each managed, gathered, computed and combined in
+ *                     turn (an expert needed by several chunks may be loaded
+ *                     once per chunk).  Needs S >= k.
+ *   MOE_SCHED_WAVES   each missing expert is loaded at most once per step.
+ *                     Wave 0 is one manage call over the whole step: hits are
+ *                     updated, and the misses (ascending id) take the slots
+ *                     the step does not need while they last; the rest are
+ *                     deferred.  The hits' FFN runs while wave 0's loads are
+ *                     gathered on the side stream, then the loaded experts'
+ *                     FFN.  Then the deferred experts follow in batches of at
+ *                     most S (ascending id), each one manage call whose victims
+ *                     may be any slot (its expert has been computed), a gather
+ *                     and the batch's FFN.  One combine at the end.  An empty
+ *                     batch changes nothing (stamp included).  Any S >= 1.
+ * A step with T*k <= S, or S >= E, is one manage call under both.
+ */
+#define MOE_SCHED_CHUNKS 0
+#define MOE_SCHED_WAVES 1
+
 /* Arguments of moe_layer_forward.  Field meanings as in the calls above. */
 typedef struct moe_layer_args {
   int32_t T, H, E, k, I, S;
@@ -428,6 +453,7 @@ typedef struct moe_layer_args {
   int32_t route_flags;       /* moe_route_ex flags (0 = softmax router, selection-only bias) */
   int32_t* window_counts;    /* device int32 [E] or NULL: each chunk's routings are added (moe_cache_count) */
   int32_t quant;             /* 0: bf16 slabs; 1: W8A8 slabs (moe_quantize_slabs), RESIDENT or GATHER mode */
+  int32_t schedule;          /* GATHER steps larger than the pool: MOE_SCHED_CHUNKS or MOE_SCHED_WAVES */
 } moe_layer_args;
 
 /*
@@ -438,14 +464,14 @@ typedef struct moe_layer_args {
  * ... on an RTX 3060", "What it actually does under the hood" (hits are
  * resolved on the device, no host sync inside the step, the decode pass
  * replays as one CUDA graph).
- * Chunking: when the policy can evict, S < E and T*k > S, the tokens are
- * processed in chunks of floor(S/k) consecutive tokens (a step is served
- * from slots only when tokens x top_k <= slots), each chunk managed,
- * gathered and computed in turn.  ZERO_RETURN (STATIC) never chunks.
+ * Steps larger than the pool (GATHER, S < E, T*k > S): token chunks or
+ * expert waves, as args->schedule says (MOE_SCHED_*).  ZERO_RETURN (STATIC)
+ * never chunks.
  * `side` may be NULL or equal to `main` (then everything runs on `main`).
  * The sequence of launches depends only on the shapes, so it can be
  * captured into a CUDA graph.
- * Errors: as the calls above; MOE_ERR_CAPACITY if S < k in GATHER mode.
+ * Errors: as the calls above; MOE_ERR_CAPACITY if S < k in GATHER mode with
+ * token chunks; MOE_ERR_ARG for an unknown schedule.
  */
 int moe_layer_forward(const moe_layer_args* args, moe_stream_t main, moe_stream_t side);
 

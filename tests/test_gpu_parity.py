@@ -335,9 +335,10 @@ def test_combine_parity_split():
 # Whole layer
 # ----------------------------------------------------------------------------
 
-def _run_layer(cfg, steps=1, side=True, policy=None, T=None, bias_mode=O.BIAS_GRADED, rflags=0):
+def _run_layer(cfg, steps=1, side=True, policy=None, T=None, bias_mode=O.BIAS_GRADED, rflags=0, schedule=None):
     T = cfg.T if T is None else T
     policy = cfg.policy if policy is None else policy
+    schedule = cfg.schedule if schedule is None else schedule
     st = stage_layer(cfg)
     bias_np = bias_d = None
     if cfg.bias_cap is not None:
@@ -360,17 +361,17 @@ def _run_layer(cfg, steps=1, side=True, policy=None, T=None, bias_mode=O.BIAS_GR
     layer = M.SlotCachedMoELayer(st["wr"], pool, cfg.k, cfg.I, cfg.mode, policy,
                                  host_slabs=None if cfg.mode == C.MODE_RESIDENT else st["host"], state=gstate,
                                  logit_offset=st["logit_offset"], sel_bias=bias_d, max_tokens=T, side_stream=side,
-                                 route_flags=rflags)
+                                 route_flags=rflags, schedule=schedule)
     wr_np = _np(st["wr"].float())
     off_np = None if st["logit_offset"] is None else _np(st["logit_offset"])
     slabs = HostSlabs(st["host"])
-    total_miss = 0
+    total_miss = total_calls = 0
     for step in range(steps):
         x = C.draw_x(cfg, DEV, step=step, T=T)
         res = layer.forward(x)
         torch.cuda.synchronize()
         want = O.layer_forward(_np(x.float()), wr_np, slabs, cfg.H, cfg.I, cfg.k, cfg.mode, policy, ostate,
-                               opool, off_np, bias_np, router=router, damped=damped)
+                               opool, off_np, bias_np, router=router, damped=damped, schedule=schedule)
         assert np.array_equal(_np(res["ids"]), want["ids"]), f"step {step}: ids"
         assert np.abs(_np(res["w"]) - want["w"]).max() <= 1e-6
         assert_out_close(_np(res["out"].float()), want["out"], f"step {step}: out")
@@ -383,10 +384,12 @@ def _run_layer(cfg, steps=1, side=True, policy=None, T=None, bias_mode=O.BIAS_GR
         if ostate is not None:
             _check_state(gstate, ostate, f"step {step}")
             total_miss += sum(len(c["miss_e"]) for c in want["chunks"])
+            total_calls += sum(len(c.get("waves", [None])) for c in want["chunks"])
     assert int(_np(layer.dev_status)[0]) == 0
     if ostate is not None:
         stats = _np(layer.stats)
         assert stats[0] == total_miss
+        assert stats[1] == total_calls  # manage calls (an empty wave is no call)
         if cfg.mode == C.MODE_GATHER:
             assert stats[2] == total_miss * cfg.slab_bytes
             # every occupied slot holds exactly its expert's bytes
