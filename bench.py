@@ -50,7 +50,7 @@ from harness import configs as C  # noqa: E402
 GATHER_DRAM_BYTES_PER_MISS = (161_741_568 + 224_512) / 17
 METRIC = "MoE-layer tokens/s at 1 GB300; decode HBM GB/s vs roofline; prefill TFLOP/s"
 UNIT = "tokens/s"
-PROF_NAMES = ("route", "permute", "manage", "gather", "ffn_gateup", "ffn_down", "combine", "ffn_rows")
+PROF_NAMES = ("route", "permute", "manage", "gather", "ffn_gateup", "ffn_down", "combine", "ffn_rows", "decode")
 
 
 def _peaks():

@@ -48,7 +48,7 @@ class LayerArgs(ctypes.Structure):
                 ("out_miss", c_void_p), ("stats", c_void_p), ("dev_status", c_void_p),
                 ("workspace", c_void_p), ("workspace_bytes", c_size_t), ("prof", POINTER(Prof)),
                 ("affinity", c_float), ("route_flags", c_int32), ("window_counts", c_void_p), ("quant", c_int32),
-                ("schedule", c_int32)]
+                ("schedule", c_int32), ("decode_kernels", c_int32)]
 
 
 def _sig(name, argtypes, restype=c_int):
@@ -315,7 +315,7 @@ class SlotCachedMoELayer:
 
     def __init__(self, w_router, pool, k, I, mode, policy=POLICY_LRU, host_slabs=None, state=None,
                  logit_offset=None, sel_bias=None, max_tokens=64, side_stream=True, affinity=0.0,
-                 route_flags=0, window_counts=None, quant=0, schedule=0):
+                 route_flags=0, window_counts=None, quant=0, schedule=0, decode_kernels=0):
         self.w_router, self.pool, self.k, self.I = w_router, pool, k, I
         self.H, self.E = w_router.shape
         self.S = pool.shape[0]
@@ -327,11 +327,13 @@ class SlotCachedMoELayer:
         self.window_counts = window_counts
         self.quant = int(quant)  # pool / host hold W8A8 slabs (quantize_slabs)
         self.schedule = int(schedule)  # SCHED_CHUNKS or SCHED_WAVES (GATHER steps larger than the pool)
+        self.decode_kernels = int(decode_kernels)  # 0: persistent decode kernel where it applies, 1: separate
         dev = pool.device
         self.stats = torch.zeros(4, dtype=torch.int64, device=dev)
         self.dev_status = torch.zeros(1, dtype=torch.int32, device=dev)
         self.max_tokens = max_tokens
-        self.workspace = torch.empty(layer_workspace_bytes(max_tokens, self.H, self.E, k, I, self.S),
+        # zero-filled once: the persistent decode kernel's counters live at its start
+        self.workspace = torch.zeros(layer_workspace_bytes(max_tokens, self.H, self.E, k, I, self.S),
                                      dtype=torch.uint8, device=dev)
         self.side = torch.cuda.Stream(device=dev) if side_stream else None
 
@@ -355,7 +357,8 @@ class SlotCachedMoELayer:
                       ids.data_ptr(), w.data_ptr(), out.data_ptr(), _ptr(out_res), _ptr(out_miss),
                       self.stats.data_ptr(), self.dev_status.data_ptr(), self.workspace.data_ptr(),
                       self.workspace.numel(), ctypes.pointer(prof) if prof is not None else None, self.affinity,
-                      self.route_flags, _ptr(self.window_counts), self.quant, self.schedule)
+                      self.route_flags, _ptr(self.window_counts), self.quant, self.schedule,
+                      self.decode_kernels)
         main = torch.cuda.current_stream() if stream is None else stream
         # the library forks to and joins back from the side stream itself
         _ck(_layer(ctypes.byref(a), c_void_p(main.cuda_stream),

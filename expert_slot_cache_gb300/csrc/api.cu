@@ -13,6 +13,7 @@ static size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
 // Workspace layout of the layer forward, for chunks of up to n = C*k routing slots.
 struct LayerWs {
+  int32_t* ctr;  // arrival counters of the persistent decode kernel (zero between calls)
   int32_t *count, *offset, *rows, *pos, *act_e, *n_act, *miss_e, *miss_s, *n_miss, *hit_e, *n_hit, *def_e, *n_def;
   float *hbuf, *y, *logits, *route;
   uint16_t *xp, *hb;
@@ -33,6 +34,7 @@ static LayerWs carve(void* base, int n, int H, int E, int I, int T) {
     return p;
   };
   const int lmax = std::min(n, E);
+  w.ctr = (int32_t*)take(4 * decode_ctr_ints(E));  // first, so its place does not depend on n
   w.count = (int32_t*)take(4 * (size_t)E);
   w.offset = (int32_t*)take(4 * (size_t)(E + 1));
   w.rows = (int32_t*)take(4 * (size_t)n);
@@ -195,9 +197,13 @@ extern "C" int moe_layer_forward(const moe_layer_args* a, moe_stream_t main_s, m
   if (a->quant != 0 && a->quant != 1) return MOE_ERR_ARG;
   if (a->quant && (mode == MOE_MODE_ZERO_RETURN || H % 16 || I % 16)) return MOE_ERR_ARG;
   if (a->schedule != MOE_SCHED_CHUNKS && a->schedule != MOE_SCHED_WAVES) return MOE_ERR_ARG;
+  if (a->decode_kernels != 0 && a->decode_kernels != 1) return MOE_ERR_ARG;
+  if (a->route_flags & ~(MOE_ROUTE_SIGMOID | MOE_ROUTE_DAMPED)) return MOE_ERR_ARG;
+  if ((a->route_flags & MOE_ROUTE_SIGMOID) && (a->route_flags & MOE_ROUTE_DAMPED)) return MOE_ERR_ARG;
   const bool waves = mode == MOE_MODE_GATHER && a->schedule == MOE_SCHED_WAVES;
   if (mode == MOE_MODE_GATHER && !waves && S < E && S < k) return MOE_ERR_CAPACITY;
-  if ((uintptr_t)a->pool % 16 || (uintptr_t)a->workspace % 256 || (uintptr_t)a->x % 16) return MOE_ERR_ALIGN;
+  if ((uintptr_t)a->pool % 16 || (uintptr_t)a->workspace % 256 || (uintptr_t)a->x % 16 || (uintptr_t)a->out % 8)
+    return MOE_ERR_ALIGN;
 
   const int C = chunk_tokens(T, k, S, E, mode, policy, a->schedule);
   LayerWs ws = carve(a->workspace, C * k, H, E, I, T);
@@ -216,6 +222,14 @@ extern "C" int moe_layer_forward(const moe_layer_args* a, moe_stream_t main_s, m
   prof.p = a->prof;
   if (prof.p) prof.p->used = 0;
   const size_t slab_bytes = a->quant ? q8_slab_bytes_h(H, I) : (size_t)6 * H * I;
+  if (mode == MOE_MODE_RESIDENT && !a->quant && !a->window_counts && a->decode_kernels == 0 && H % 8 == 0 &&
+      ws.skp && decode_eligible(T, H, E, k, I, S, a->x, a->w_router, a->pool)) {
+    // a small all-resident step: the whole layer in one persistent launch
+    prof.begin(MOE_PROF_DECODE, ms);
+    const int rd = launch_decode(a, ws.route, ws.logits, ws.skp, ws.skp_bytes, ws.ctr, ms);
+    prof.end(ms);
+    return rd;
+  }
   prof.begin(MOE_PROF_ROUTE, ms);
   // a one-chunk step: the top-k CTA may group the batch by expert itself (then no permute launch)
   const PermOut perm0{ws.count, ws.offset, ws.rows, ws.pos, ws.act_e, ws.n_act, a->dev_status};

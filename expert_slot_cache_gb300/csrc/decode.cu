@@ -1,0 +1,792 @@
+// One persistent kernel for a small all-resident decode step.
+//
+// The whole layer of a decode batch of a few tokens -- router logits, top-k,
+// grouping by expert, the gate/up and down weight streams on tcgen05, and the
+// weighted combine -- runs as one cooperative launch with one CTA per SM.
+// "Betelgeuse: Running Qwen 3.8 Flash Next ... on an RTX 3060", "What it
+// actually does under the hood": hits are resolved in-stream on the device and
+// a decode pass replays as one CUDA graph; "Porting vllm-expert-cache to
+// NVIDIA GPUs", "1. Kernels" (a fused cache-and-expert kernel).  At one token
+// the eight experts' 75.5 MB stream in about 11 us, while a chain of eight
+// dependent launches costs more than that in ramps and gaps; here the weight
+// stream never stops between the two projections.
+//
+// Phases (grid-wide waits are bounded spins on counters in the workspace; a
+// cooperative launch keeps every CTA resident, so a CTA can wait on another):
+//  1. router logits: units (128-row block b, 32 experts, token t) over all
+//     warps; part_b = fma chain from 0 over the block's rows in order, the
+//     same fp32 order as the router kernels; then a grid-wide arrival.
+//  2. every CTA adds the parts in block order (+ the offset), runs the
+//     per-warp top-k and groups the step's routings by expert in shared
+//     memory; CTA 0 writes logits, ids and weights.
+//  3. gate/up stream: the listed experts' [Wg | Wu] cut into stages of 16
+//     rows, dealt as equal contiguous ranges to the CTAs (the decode stream
+//     schedule); parts [j][p][2I] to global memory; after each part a release
+//     on the expert's counter.
+//  4. the loader goes straight on to the CTA's down stages (weights only), so
+//     the DRAM stream continues while the epilogue warps wait for the gate/up
+//     parts of those experts and build h = silu(sum g) * (sum u) in bf16 in
+//     shared memory, laid out as the MMA's B operand.
+//  5. down MMAs, parts [j][p][H]; a grid-wide arrival; then every CTA reduces
+//     and combines a share of the output: out[t] = sum_j w[t][j] y[pos(t, j)]
+//     in fp32, j ascending, rounded to bf16.
+// The last CTA to leave puts every counter back to zero.
+#include <algorithm>
+
+#include "internal.cuh"
+#include "sched.cuh"
+#include "tc05.cuh"
+#include "fp32def.cuh"
+
+namespace moe {
+
+constexpr int kPThreads = 192;  // warp 0 loads, warp 1 issues MMAs, warps 2-5 epilogue
+constexpr int kPWarps = kPThreads / 32;
+constexpr int kPM = 128;        // output columns per MMA (M)
+constexpr int kPN = 16;         // tokens per MMA (N)
+constexpr int kPK = 16;         // weight rows per stage (K)
+constexpr int kPBox = 64 * kPK * 2;  // one {64 columns x 16 rows} swizzle atom, 2 KB
+constexpr int kPAct = 8 * kPN * 2;   // {8 rows x 16 tokens} bf16 core matrices, 256 B
+constexpr int kPHStage = 2 * kPAct;  // h of one down stage, 512 B
+constexpr uint32_t kPIdesc = idesc_bf16(kPM, kPN, 1, 0);
+constexpr int kPMaxT = 8;
+constexpr int kPMaxN = 64;      // T * k
+constexpr int kPMaxE = 256;
+constexpr int kPMaxStages = 4;
+constexpr uint32_t kPTmemCols = 512;  // two accumulator buffers of up to 256 columns
+constexpr int kPSpin = 1 << 22;
+constexpr int kPSmemMax = 232448 - 12 * 1024;  // dynamic shared memory cap (static shared memory below)
+constexpr int kPStage = 8192 + 256;            // one warp's router staging: Wr [128][32] bf16 + x [128] bf16
+
+// Counters after the E per-expert gate/up counters.
+constexpr int kCtrLogits = 0, kCtrDown = 1, kCtrExit = 2, kCtrRoute = 3, kCtrCount = 4;
+
+struct DecodeArgs {
+  const uint16_t* x;   // bf16 [T][H]
+  const uint16_t* wr;  // bf16 [H][E]
+  const float* off;    // fp32 [E] or NULL
+  const float* bias;   // fp32 [E] or NULL
+  const int32_t* e2s;  // [E] or NULL (expert e in slot e)
+  float affinity;
+  int rflags;
+  int T, H, E, k, I, S;
+  const uint16_t* pool;
+  float* lpart;   // fp32 [H/128][T][E]
+  float* logits;  // fp32 [T][E]
+  int32_t* ids;
+  float* w;
+  uint16_t* out;  // bf16 [T][H]
+  float* gpart;   // fp32 [jg][n][2I]
+  float* ypart;   // fp32 [jd][n][H]
+  int jg, jd;
+  int32_t* ctr;  // E + kCtrCount, zero on entry and on exit
+  int32_t* status;
+  int stride, nst, hcap;  // ring stage stride and count; down stages the h area holds
+  int ring_bytes;         // >= nst * stride and >= the router's staging (kPWarps * kPStage)
+};
+
+__device__ __forceinline__ int ld_acquire(const int32_t* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void add_release(int32_t* p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Bounded wait until *p >= target; on giving up, flags the call and returns false.
+__device__ __forceinline__ bool wait_count(const int32_t* p, int target, int32_t* status) {
+  for (int i = 0; i < kPSpin; ++i) {
+    if (ld_acquire(p) >= target) return true;
+    __nanosleep(32);
+  }
+  set_status(status, MOE_DEV_TIMEOUT);
+  return false;
+}
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_16(void* smem, const void* gmem) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem)), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
+// sum_{j < J} p[j * stride] in j order, from 0; the loads of up to 16 parts are in flight together.
+__device__ __forceinline__ float sum_parts(const float* p, size_t stride, int J) {
+  float s = 0.f;
+  for (int j0 = 0; j0 < J; j0 += 16) {
+    float v[16];
+#pragma unroll
+    for (int u = 0; u < 16; ++u) v[u] = j0 + u < J ? __ldcg(p + (size_t)(j0 + u) * stride) : 0.f;
+#pragma unroll
+    for (int u = 0; u < 16; ++u)
+      if (j0 + u < J) s += v[u];
+  }
+  return s;
+}
+
+// TMEM accumulator columns 0..W-1 (tokens) of every tile -> parts.
+template <int W>
+__device__ __forceinline__ void dec_epilogue(uint32_t taddr, float* base, int ntiles, int N, int nb) {
+  constexpr int G = W >= 32 ? 1 : 32 / W;
+  for (int m0 = 0; m0 < ntiles; m0 += G) {
+    float v[G][W];
+#pragma unroll
+    for (int gi = 0; gi < G; ++gi)
+      if (m0 + gi < ntiles) tmem_ld_w<W>(taddr + (m0 + gi) * kPN, v[gi]);
+    tmem_ld_wait();
+#pragma unroll
+    for (int gi = 0; gi < G; ++gi)
+      if (m0 + gi < ntiles)
+#pragma unroll
+        for (int t = 0; t < W; ++t)
+          if (t < nb) base[(size_t)t * N + (m0 + gi) * kPM] = v[gi][t];
+  }
+}
+
+__device__ __forceinline__ void drain_tile(uint32_t taddr, float* base, int ntiles, int N, int nb) {
+  if (nb <= 1)
+    dec_epilogue<1>(taddr, base, ntiles, N, nb);
+  else if (nb <= 2)
+    dec_epilogue<2>(taddr, base, ntiles, N, nb);
+  else if (nb <= 4)
+    dec_epilogue<4>(taddr, base, ntiles, N, nb);
+  else
+    dec_epilogue<8>(taddr, base, ntiles, N, nb);
+}
+
+__global__ void __launch_bounds__(kPThreads, 1) decode_layer_kernel(const DecodeArgs a,
+                                                                    const __grid_constant__ CUtensorMap mwg,
+                                                                    const __grid_constant__ CUtensorMap mwd) {
+  extern __shared__ __align__(16) unsigned char dsm_raw[];
+  // 1024-byte aligned, by an offset from the shared array (so the compiler keeps shared-space accesses)
+  unsigned char* ring = dsm_raw + ((1024u - (smem_u32(dsm_raw) & 1023u)) & 1023u);
+  unsigned char* hsm = ring + a.ring_bytes;  // h of the down stages; the logits and scores before that
+  float* slog = reinterpret_cast<float*>(hsm);
+  float* ssc = slog + a.T * a.E;
+  const size_t hb0 = (size_t)a.hcap * kPHStage, lb0 = (size_t)a.T * a.E * 8;
+  const size_t hbytes = ((hb0 > lb0 ? hb0 : lb0) + 15) & ~size_t(15);
+  uint64_t* full = reinterpret_cast<uint64_t*>(hsm + hbytes);
+  uint64_t* empty = full + kPMaxStages;
+  uint64_t* tfull = empty + kPMaxStages;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* done = tempty + 2;
+  uint64_t* hbar = done + 1;  // [hcap]: h of local down stage i is in place
+  __shared__ int s_ids[kPMaxN], s_rows[kPMaxN], s_pos[kPMaxN];
+  __shared__ float s_w[kPMaxN];
+  __shared__ int s_cnt[kPMaxE], s_off[kPMaxE + 1], s_act[kPMaxE], s_li[kPMaxE];
+  __shared__ int tmp[33];
+  __shared__ float4 s_y[kPThreads];
+  __shared__ int s_nact, s_abort;
+  __shared__ uint32_t s_tmem;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int T = a.T, E = a.E, k = a.k, H = a.H, I = a.I, n = T * k;
+  const int G = gridDim.x;
+  if (tid == 0) {
+    prefetch_tmap(&mwg);
+    prefetch_tmap(&mwd);
+    for (int s = 0; s < a.nst; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&tfull[s], 1);
+      mbar_init(&tempty[s], 4);
+    }
+    mbar_init(done, 1);
+    for (int i = 0; i < a.hcap; ++i) mbar_init(&hbar[i], 1);
+    s_abort = 0;
+    mbar_fence_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&s_tmem, kPTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  volatile int* abort_flag = &s_abort;
+
+  // ---- 1. router logits: block parts -------------------------------------------------
+  const int nblk = H / 128, neg = (E + 31) / 32;
+  const int units = nblk * neg * T;
+  {
+    // the warp's staging area in the ring: Wr rows [128][32 experts] bf16 (8 KB), then the x row (256 B)
+    unsigned char* wst = ring + warp * kPStage;
+    const uint16_t* ws16 = reinterpret_cast<const uint16_t*>(wst);
+    for (int u = blockIdx.x * kPWarps + warp; u < units; u += G * kPWarps) {
+      const int b = u % nblk, rest = u / nblk, eg = rest % neg, t = rest / neg;
+      const int e0 = eg * 32, e = e0 + lane;
+      for (int c = lane; c < 128 * 4; c += 32) {  // 16-byte pieces: row c / 4, experts e0 + 8 (c % 4) ..
+        const int r = c >> 2, q = c & 3;
+        if (e0 + 8 * q < E) cp_async_16(wst + r * 64 + q * 16, a.wr + (size_t)(b * 128 + r) * E + e0 + 8 * q);
+      }
+      if (lane < 16) cp_async_16(wst + 8192 + lane * 16, a.x + (size_t)t * H + b * 128 + 8 * lane);
+      cp_async_wait_all();
+      __syncwarp();
+      const uint16_t* xs16 = ws16 + 4096;
+      float acc = 0.f;
+#pragma unroll 8
+      for (int r = 0; r < 128; ++r) acc = fmaf(bf16_to_f32(xs16[r]), bf16_to_f32(ws16[r * 32 + lane]), acc);
+      if (e < E) a.lpart[((size_t)b * T + t) * E + e] = acc;
+      __syncwarp();
+    }
+  }
+  fence_async_smem();  // the ring's staging bytes are overwritten by tensor-map copies later
+  __syncthreads();
+  if (tid == 0) {  // the barrier orders the CTA's stores before this (cumulative) release
+    add_release(&a.ctr[E + kCtrLogits], 1);
+    if (!wait_count(&a.ctr[E + kCtrLogits], G, a.status)) s_abort = 1;
+  }
+  __syncthreads();
+
+  // ---- 2. logits, top-k and weights ------------------------------------------------------
+  // A few tokens: every CTA routes all of them.  More: CTA t routes token t and publishes its ids and
+  // weights, and every CTA reads them back after one more grid-wide wait.
+  const bool spread = T >= 3;
+  const int t_lo = spread ? blockIdx.x : 0, t_hi = spread ? min((int)blockIdx.x + 1, T) : T;
+  if (t_lo < t_hi) {
+    for (int v = t_lo * E + tid; v < t_hi * E; v += kPThreads) {
+      const int e = v % E;
+      float l = sum_parts(a.lpart + v, (size_t)T * E, nblk);  // part b of (t, e) at [b][t][e]
+      if (a.off) l = l + a.off[e];
+      slog[v] = l;
+      // selection score: as the router's top-k (sigmoid router, bias, live-cache affinity)
+      const float base = (a.rflags & MOE_ROUTE_SIGMOID) ? sigmoid32_def(l) : l;
+      float sc = a.bias ? __fadd_rn(base, a.bias[e]) : base;
+      if (a.e2s && a.affinity != 0.f && a.e2s[e] >= 0) sc = sc + a.affinity;
+      ssc[v] = sc;
+    }
+    __syncthreads();
+    if (spread || blockIdx.x == 0)
+      for (int v = t_lo * E + tid; v < t_hi * E; v += kPThreads) a.logits[v] = slog[v];
+    // top-k by rank: expert e of token t is the r-th pick, r = the number of experts ranked before it
+    // (higher score, or an equal score and a lower id); ranks below k are the picks, in order
+    for (int v = t_lo * E + tid; v < t_hi * E; v += kPThreads) {
+      const int t = v / E, e = v - t * E;
+      const float4* row4 = reinterpret_cast<const float4*>(ssc + t * E);  // E % 8 == 0
+      const float se = ssc[v];
+      int r = 0;
+#pragma unroll 4
+      for (int f4 = 0; f4 < E / 4; ++f4) {
+        const float4 q = row4[f4];
+        const int f = 4 * f4;
+        r += (q.x > se) || (q.x == se && f < e);
+        r += (q.y > se) || (q.y == se && f + 1 < e);
+        r += (q.z > se) || (q.z == se && f + 2 < e);
+        r += (q.w > se) || (q.w == se && f + 3 < e);
+      }
+      if (r < k) s_ids[t * k + r] = e;
+    }
+    __syncthreads();
+    // the weights of token t over its k picks (the router's softmax, or its sigmoids normalised): one
+    // warp per token, lane j for pick j; the sums run as a fixed butterfly
+    for (int t = t_lo + warp; t < t_hi; t += kPWarps) {
+      float zj = 0.f;
+      if (lane < k) {
+        const int e = s_ids[t * k + lane];
+        zj = slog[t * E + e];
+        if (a.rflags & MOE_ROUTE_SIGMOID) zj = sigmoid32_def(zj);
+        else if ((a.rflags & MOE_ROUTE_DAMPED) && a.bias) zj = zj + a.bias[e];
+      }
+      float mx = lane < k ? zj : -INFINITY;
+#pragma unroll
+      for (int d = 16; d; d >>= 1) mx = fmaxf(mx, __shfl_xor_sync(MOE_FULL_MASK, mx, d));
+      const bool sig = (a.rflags & MOE_ROUTE_SIGMOID) != 0;
+      const float num = lane < k ? (sig ? zj : expf(zj - mx)) : 0.f;
+      float sum = num;
+#pragma unroll
+      for (int d = 16; d; d >>= 1) sum += __shfl_xor_sync(MOE_FULL_MASK, sum, d);
+      if (lane < k) s_w[t * k + lane] = num / sum;
+    }
+    __syncthreads();
+    if (spread || blockIdx.x == 0)
+      for (int i = t_lo * k + tid; i < t_hi * k; i += kPThreads) {
+        a.ids[i] = s_ids[i];
+        a.w[i] = s_w[i];
+      }
+  }
+  if (spread) {
+    __syncthreads();
+    if (tid == 0) {
+      if (t_lo < t_hi) add_release(&a.ctr[E + kCtrRoute], 1);
+      if (!wait_count(&a.ctr[E + kCtrRoute], T, a.status)) s_abort = 1;
+    }
+    __syncthreads();
+    for (int i = tid; i < n; i += kPThreads) {
+      s_ids[i] = __ldcg(a.ids + i);
+      s_w[i] = __ldcg(a.w + i);
+    }
+    __syncthreads();
+  }
+  {
+    int carry = 0, carry_act = 0;
+    for (int e0 = 0; e0 < E; e0 += kPThreads) {
+      const int e = e0 + tid;
+      int c = 0;
+      if (e < E)
+        for (int i = 0; i < n; ++i) c += s_ids[i] == e;
+      int tp;  // count in the low 16 bits, active flag in the high 16 (n <= 64, E <= 256: no carry)
+      const int xp = block_exclusive_scan(c | ((c > 0 ? 1 : 0) << 16), tmp, &tp);
+      const int ex = xp & 0xffff, exa = xp >> 16, tot = tp & 0xffff, tota = tp >> 16;
+      if (e < E) {
+        s_cnt[e] = c;
+        s_off[e] = carry + ex;
+        s_li[e] = c > 0 ? carry_act + exa : -1;
+        if (c > 0) s_act[carry_act + exa] = e;
+      }
+      carry += tot;
+      carry_act += tota;
+    }
+    if (tid == 0) {
+      s_off[E] = carry;
+      s_nact = carry_act;
+    }
+  }
+  __syncthreads();
+  if (tid < n) {
+    const int e = s_ids[tid];
+    int r = 0;
+    for (int i = 0; i < tid; ++i) r += s_ids[i] == e;
+    const int p = s_off[e] + r;
+    s_rows[p] = tid;
+    s_pos[tid] = p;
+  }
+  __syncthreads();
+
+  // ---- 3-5. the two weight streams -----------------------------------------------------
+  FfnArgs fa{};
+  fa.E = E;
+  fa.S = a.S;
+  fa.e2s = a.e2s;
+  fa.list_e = s_act;
+  fa.offset = s_off;
+  const int n_list = s_nact;
+  const int NSRg = H / kPK, NSRd = I / kPK;
+  const int Ng = 2 * I;
+  const int Lg = stream_len(n_list, NSRg, G, a.jg), Ld = stream_len(n_list, NSRd, G, a.jd);
+  const int bg = blockIdx.x * Lg, eg_end = min(bg + Lg, n_list * NSRg);
+  const int bd = blockIdx.x * Ld, ed_end = min(bd + Ld, n_list * NSRd);
+  const int wbytes_g = 2 * I * kPK * 2, wbytes_d = H * kPK * 2;
+  if (Ld > a.hcap) {  // the host sizes the h area for the largest range: cannot happen
+    if (tid == 0) set_status(a.status, MOE_DEV_BAD_GROUPS);
+    s_abort = 1;
+  }
+  __syncthreads();
+
+  if (warp == 0) {
+    if (lane == 0) {
+      uint32_t it = 0;
+      int last_use[kPMaxStages];
+      for (int s = 0; s < kPMaxStages; ++s) last_use[s] = -1;
+      auto claim = [&](int sl, uint32_t use) {
+        if (use > 0 && !*abort_flag && !mbar_wait(&empty[sl], (use - 1) & 1u)) {
+          *abort_flag = 1;
+          set_status(a.status, MOE_DEV_TIMEOUT);
+        }
+        return !*abort_flag;
+      };
+      if (bg < eg_end)
+        stream_segments<kPN>(fa, NSRg, Lg, bg, eg_end, [&](const StreamSeg& g) {
+          int tok[kPMaxT];
+          for (int t = 0; t < g.nb; ++t) tok[t] = s_rows[g.p0 + t] / k;
+          for (int s = g.s_lo; s < g.s_hi; ++s, ++it) {
+            const int sl = it % a.nst;
+            const uint32_t use = it / a.nst;
+            if (!claim(sl, use)) return false;
+            unsigned char* dst = ring + sl * a.stride;
+            const int row0 = s * kPK;
+            mbar_expect_tx(&full[sl], wbytes_g + g.nb * 32);
+            tma_load_4d(dst, &mwg, &full[sl], 0, row0, 0, 3 * g.slot);
+            tma_load_4d(dst + wbytes_g / 2, &mwg, &full[sl], 0, row0, 0, 3 * g.slot + 1);
+            unsigned char* act = dst + wbytes_g;
+            for (int t = 0; t < g.nb; ++t) {
+              const uint16_t* xr = a.x + (size_t)tok[t] * H + row0;
+              bulk_load(act + t * 16, xr, 16, &full[sl]);
+              bulk_load(act + kPAct + t * 16, xr + 8, 16, &full[sl]);
+            }
+            last_use[sl] = (int)use;
+          }
+          return true;
+        });
+      if (bd < ed_end)
+        stream_segments<kPN>(fa, NSRd, Ld, bd, ed_end, [&](const StreamSeg& g) {
+          for (int s = g.s_lo; s < g.s_hi; ++s, ++it) {
+            const int sl = it % a.nst;
+            const uint32_t use = it / a.nst;
+            if (!claim(sl, use)) return false;
+            mbar_expect_tx(&full[sl], wbytes_d);
+            tma_load_4d(ring + sl * a.stride, &mwd, &full[sl], 0, s * kPK, 0, 3 * g.slot + 2);
+            last_use[sl] = (int)use;
+          }
+          return true;
+        });
+      if (*abort_flag)  // let every copy issued land before the CTA moves on
+        for (int s = 0; s < a.nst; ++s)
+          if (last_use[s] >= 0) mbar_wait(&full[s], (uint32_t)last_use[s] & 1u);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      for (int li = bg / NSRg; li * NSRg < eg_end && li < n_list; ++li) {
+        int e, slot;
+        if (!stream_slot(fa, li, e, slot)) set_status(a.status, MOE_DEV_BAD_SLOT);
+      }
+      uint32_t it = 0, seg = 0;
+      auto run = [&](const StreamSeg& g, bool down) {
+        const uint32_t buf = seg & 1u, use = seg >> 1;
+        if (use > 0 && !*abort_flag && !mbar_wait(&tempty[buf], (use - 1) & 1u)) {
+          *abort_flag = 1;
+          set_status(a.status, MOE_DEV_TIMEOUT);
+        }
+        tc_fence_after();
+        const uint32_t d = tmem + buf * 256u;
+        const int ntiles = down ? H / kPM : Ng / kPM;
+        const int lbase = down ? s_li[g.e] * NSRd - bd : 0;
+        for (int s = g.s_lo; s < g.s_hi; ++s, ++it) {
+          const int sl = it % a.nst;
+          if (!*abort_flag && !mbar_wait(&full[sl], (it / a.nst) & 1u)) {
+            *abort_flag = 1;
+            set_status(a.status, MOE_DEV_TIMEOUT);
+          }
+          // down: this stage's h is in place (written by the epilogue warps)
+          if (down && !*abort_flag && lbase + s < a.hcap && !mbar_wait(&hbar[lbase + s], 0)) {
+            *abort_flag = 1;
+            set_status(a.status, MOE_DEV_TIMEOUT);
+          }
+          tc_fence_after();
+          if (!*abort_flag) {
+            const uint32_t sa = smem_u32(ring + sl * a.stride);
+            const uint32_t sb = down ? smem_u32(hsm + (size_t)(lbase + s) * kPHStage) : sa + wbytes_g;
+            const uint64_t bdesc = smem_desc_l(sb, kPAct, 128, kLayoutNone);
+            for (int m = 0; m < ntiles; ++m) {
+              const uint64_t adesc = smem_desc_l(sa + m * 2 * kPBox, kPBox, 1024, kLayoutSw128);
+              umma_f16(d + m * kPN, adesc, bdesc, kPIdesc, s > g.s_lo);
+            }
+          }
+          umma_commit(&empty[sl]);
+        }
+        umma_commit(&tfull[buf]);
+        ++seg;
+        return true;
+      };
+      if (bg < eg_end)
+        stream_segments<kPN>(fa, NSRg, Lg, bg, eg_end, [&](const StreamSeg& g) { return run(g, false); });
+      if (bd < ed_end)
+        stream_segments<kPN>(fa, NSRd, Ld, bd, ed_end, [&](const StreamSeg& g) { return run(g, true); });
+      umma_commit(done);  // every MMA issued has finished once `done` completes
+      mbar_wait(done, 0);
+    }
+  } else {
+    // epilogue warps 2..5; TMEM lane quarter q = warp % 4 holds output columns q*32 .. q*32+31 of each tile
+    const int q = warp & 3, etid = tid - 64;
+    uint32_t seg = 0;
+    auto drain = [&](const StreamSeg& g, bool down) {
+      const uint32_t buf = seg & 1u, use = seg >> 1;
+      if (!*abort_flag && !mbar_wait(&tfull[buf], use & 1u)) {
+        *abort_flag = 1;
+        set_status(a.status, MOE_DEV_TIMEOUT);
+      }
+      tc_fence_after();
+      if (!*abort_flag) {
+        const int N = down ? H : Ng;
+        float* base = (down ? a.ypart : a.gpart) + ((size_t)g.j * n + g.p0) * N + q * 32 + lane;
+        drain_tile(tmem + ((uint32_t)(q * 32) << 16) + buf * 256u, base, N / kPM, N, g.nb);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[buf]);
+      ++seg;
+    };
+    if (bg < eg_end)
+      stream_segments<kPN>(fa, NSRg, Lg, bg, eg_end, [&](const StreamSeg& g) {
+        drain(g, false);
+        // publish this part of the expert's sums (the barrier orders every epilogue thread's stores
+        // before the signalling thread's release)
+        named_sync(1, 128);
+        if (etid == 0) add_release(&a.ctr[s_li[g.e]], 1);
+        return true;
+      });
+    if (bd < ed_end) {
+      // h for this CTA's down stages, from every part of the experts' gate/up sums.  Every epilogue
+      // warp walks the same segments and reaches every named barrier; only the stores depend on
+      // h_ok, which is the same for the whole CTA and never changes.
+      const bool h_ok = Ld <= a.hcap;
+      stream_segments<kPN>(fa, NSRd, Ld, bd, ed_end, [&](const StreamSeg& g) {
+        const int li = s_li[g.e];
+        const int Jg = stream_parts(li, NSRg, Lg);
+        if (etid == 0 && !wait_count(&a.ctr[li], Jg, a.status)) *abort_flag = 1;
+        named_sync(1, 128);
+        const int lbase = li * NSRd - bd;
+        // (stage, row, token) elements of the batch's tokens; lane pairs take the gate sum (even lane)
+        // and the up sum (odd lane) of one element; four items per thread have their parts in flight
+        const int nst_seg = g.s_hi - g.s_lo;
+        const int nel = nst_seg * kPK * g.nb;
+        const size_t pstride = (size_t)n * Ng;
+        // one item per thread with its parts 32 at a time, or four items with 8 parts each in flight
+        if (2 * nel <= 128) {
+          const int v = etid, el = v >> 1;
+          const bool okv = el < nel;
+          int st = 0, t = 0, r = 0;
+          const float* src = a.gpart;
+          if (okv) {
+            st = el / (kPK * g.nb);
+            const int rem = el - st * (kPK * g.nb);
+            t = rem / kPK;
+            r = rem - t * kPK;
+            src = a.gpart + (size_t)(g.p0 + t) * Ng + (g.s_lo + st) * kPK + r + ((v & 1) ? I : 0);
+          }
+          float acc = 0.f;
+          for (int j0 = 0; j0 < Jg; j0 += 32) {
+            float pv[32];
+#pragma unroll
+            for (int u = 0; u < 32; ++u) pv[u] = (okv && j0 + u < Jg) ? __ldcg(src + (size_t)(j0 + u) * pstride) : 0.f;
+#pragma unroll
+            for (int u = 0; u < 32; ++u)
+              if (j0 + u < Jg) acc += pv[u];
+          }
+          const float other = __shfl_xor_sync(MOE_FULL_MASK, acc, 1);
+          if (okv && !(v & 1) && h_ok) {
+            const float hv = acc / (1.f + expf(-acc)) * other;
+            *reinterpret_cast<uint16_t*>(hsm + (size_t)(lbase + g.s_lo + st) * kPHStage + (r >> 3) * kPAct +
+                                         t * 16 + (r & 7) * 2) = f32_to_bf16(hv);
+          }
+        } else
+        for (int v0 = 0; v0 < 2 * nel; v0 += 4 * 128) {  // the same trip count in every epilogue thread
+          float acc[4] = {0.f, 0.f, 0.f, 0.f};
+          const float* src[4];
+          bool ok[4];
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            const int v = v0 + q4 * 128 + etid, el = v >> 1;
+            ok[q4] = el < nel;
+            src[q4] = a.gpart;
+            if (ok[q4]) {
+              const int st = el / (kPK * g.nb), rem = el - st * (kPK * g.nb), t = rem / kPK, r = rem - t * kPK;
+              src[q4] = a.gpart + (size_t)(g.p0 + t) * Ng + (g.s_lo + st) * kPK + r + ((v & 1) ? I : 0);
+            }
+          }
+          for (int j0 = 0; j0 < Jg; j0 += 8) {
+            float pv[4][8];
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4)
+#pragma unroll
+              for (int u = 0; u < 8; ++u)
+                pv[q4][u] = (ok[q4] && j0 + u < Jg) ? __ldcg(src[q4] + (size_t)(j0 + u) * pstride) : 0.f;
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4)
+#pragma unroll
+              for (int u = 0; u < 8; ++u)
+                if (j0 + u < Jg) acc[q4] += pv[q4][u];
+          }
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            const float other = __shfl_xor_sync(MOE_FULL_MASK, acc[q4], 1);
+            const int v = v0 + q4 * 128 + etid, el = v >> 1;
+            if (ok[q4] && !(v & 1) && h_ok) {
+              const int st = el / (kPK * g.nb), rem = el - st * (kPK * g.nb), t = rem / kPK, r = rem - t * kPK;
+              const float hv = acc[q4] / (1.f + expf(-acc[q4])) * other;
+              *reinterpret_cast<uint16_t*>(hsm + (size_t)(lbase + g.s_lo + st) * kPHStage + (r >> 3) * kPAct +
+                                           t * 16 + (r & 7) * 2) = f32_to_bf16(hv);
+            }
+          }
+        }
+        // the padding tokens of the MMA (t >= nb) read zeros
+        const int npad = nst_seg * kPK * (kPN - g.nb);
+        for (int v = etid; v < npad && h_ok; v += 128) {
+          const int st = v / (kPK * (kPN - g.nb)), rem = v - st * (kPK * (kPN - g.nb));
+          const int t = g.nb + rem / kPK, r = rem % kPK;
+          *reinterpret_cast<uint16_t*>(hsm + (size_t)(lbase + g.s_lo + st) * kPHStage + (r >> 3) * kPAct + t * 16 +
+                                       (r & 7) * 2) = 0;
+        }
+        // this segment's stages may go to the tensor cores
+        fence_async_smem();
+        named_sync(1, 128);
+        if (etid == 0)
+          for (int s = g.s_lo; s < g.s_hi; ++s)
+            if (lbase + s < a.hcap) mbar_arrive(&hbar[lbase + s]);
+        return true;
+      });
+      stream_segments<kPN>(fa, NSRd, Ld, bd, ed_end, [&](const StreamSeg& g) {
+        drain(g, true);
+        return true;
+      });
+    }
+  }
+  // warps 0 and 1 ran their loops on lane 0 alone: reconverge before the CTA barrier
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kPTmemCols);
+  }
+  if (tid == 0) {
+    add_release(&a.ctr[E + kCtrDown], 1);
+    wait_count(&a.ctr[E + kCtrDown], G, a.status);
+  }
+  __syncthreads();
+
+  // ---- combine: out[t] = sum_j w[t][j] * (sum of y's parts), j ascending ---------------
+  {
+    // item = (token, cpi 16-byte column groups); thread = (pick jj, column group cc, part group pg):
+    // part group pg adds parts pg, pg + npg, ... in order, the npg sums are added in pg order
+    const int nc4 = H / 4;
+    const int cpi = max(1, min(kPThreads / k, (T * nc4 + G - 1) / G));
+    const int npg = max(1, kPThreads / (k * cpi));
+    const int pg = tid % npg, rest = tid / npg, cc = rest % cpi, jj = rest / cpi;
+    const int chunks = (nc4 + cpi - 1) / cpi;
+    for (int item = blockIdx.x; item < T * chunks; item += G) {
+      const int t = item / chunks, c4 = (item - t * chunks) * cpi + cc;
+      const bool act = jj < k && c4 < nc4;
+      if (act) {
+        const int i = t * k + jj, p = s_pos[i];
+        const int Jd = stream_parts(s_li[s_ids[i]], NSRd, Ld);
+        const float4* src = reinterpret_cast<const float4*>(a.ypart + (size_t)p * H) + c4;
+        const size_t stride4 = (size_t)n * H / 4;
+        float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int j0 = pg; j0 < Jd; j0 += 4 * npg) {
+          float4 v[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            if (j0 + u * npg < Jd) v[u] = __ldcg(src + (size_t)(j0 + u * npg) * stride4);
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            if (j0 + u * npg < Jd) {
+              y.x += v[u].x;
+              y.y += v[u].y;
+              y.z += v[u].z;
+              y.w += v[u].w;
+            }
+        }
+        s_y[tid] = y;
+      }
+      __syncthreads();
+      if (act && jj == 0 && pg == 0) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int j = 0; j < k; ++j) {
+          const float wj = s_w[t * k + j];
+          float4 yj = s_y[(j * cpi + cc) * npg];
+          for (int q = 1; q < npg; ++q) {
+            const float4 v = s_y[(j * cpi + cc) * npg + q];
+            yj.x += v.x;
+            yj.y += v.y;
+            yj.z += v.z;
+            yj.w += v.w;
+          }
+          acc.x = fmaf(wj, yj.x, acc.x);
+          acc.y = fmaf(wj, yj.y, acc.y);
+          acc.z = fmaf(wj, yj.z, acc.z);
+          acc.w = fmaf(wj, yj.w, acc.w);
+        }
+        uint2 o;
+        o.x = uint32_t(f32_to_bf16(acc.x)) | (uint32_t(f32_to_bf16(acc.y)) << 16);
+        o.y = uint32_t(f32_to_bf16(acc.z)) | (uint32_t(f32_to_bf16(acc.w)) << 16);
+        *reinterpret_cast<uint2*>(a.out + (size_t)t * H + 4 * c4) = o;
+      }
+      __syncthreads();
+    }
+  }
+  // the last CTA out resets the counters: every other CTA is past its last wait
+  if (tid == 0) {
+    __threadfence();
+    if (atomicAdd(&a.ctr[E + kCtrExit], 1) == G - 1) {
+      for (int i = 0; i < E + kCtrCount; ++i) a.ctr[i] = 0;
+      __threadfence();
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+static int dec_stride(int H, int I) {
+  const int s = std::max(2 * I * kPK * 2 + 2 * kPAct, H * kPK * 2);
+  return (s + 1023) & ~1023;
+}
+
+bool decode_eligible(int T, int H, int E, int k, int I, int S, const void* x, const void* wr, const void* pool) {
+  const int n = T * k;
+  if (T < 1 || T > kPMaxT || n > kPMaxN || E > kPMaxE || E % 8 || k > kMaxK) return false;
+  // accumulators of at most 16 tiles (256 TMEM columns) per projection: 2I <= 2048 and H <= 2048
+  if (H % 128 || I % 128 || H > 2048 || I > 1024) return false;
+  if (S < 1 || (uintptr_t)x % 16 || (uintptr_t)wr % 16 || (uintptr_t)pool % 16) return false;
+  return dec_stride(H, I) * 2 + 1024 + 16 * 1024 <= kPSmemMax;
+}
+
+size_t decode_ctr_ints(int E) { return (size_t)E + kCtrCount; }
+
+int launch_decode(const moe_layer_args* la, float* lpart, float* logits, float* skp, size_t skp_bytes, int32_t* ctr,
+                  cudaStream_t stream) {
+  const int T = la->T, H = la->H, E = la->E, k = la->k, I = la->I, n = T * k;
+  int dev = 0, sms = 0;
+  MOE_CUDA_TRY(cudaGetDevice(&dev));
+  MOE_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  DecodeArgs a{};
+  a.x = (const uint16_t*)la->x;
+  a.wr = (const uint16_t*)la->w_router;
+  a.off = la->logit_offset;
+  a.bias = la->sel_bias;
+  a.e2s = la->e2s;
+  a.affinity = la->affinity;
+  a.rflags = la->route_flags;
+  a.T = T;
+  a.H = H;
+  a.E = E;
+  a.k = k;
+  a.I = I;
+  a.S = la->S;
+  a.pool = (const uint16_t*)la->pool;
+  a.lpart = lpart;
+  a.logits = logits;
+  a.ids = la->ids;
+  a.w = la->w;
+  a.out = (uint16_t*)la->out;
+  if (!sk_part_layout(n, H, I, skp, skp_bytes, &a.gpart, &a.ypart, &a.jg, &a.jd)) return MOE_ERR_ALIGN;
+  a.ctr = ctr;
+  a.status = la->dev_status;
+  a.stride = dec_stride(H, I);
+  // the largest down range a CTA can get (stream_len with every routed expert distinct)
+  const int NSRd = I / kPK, lmax = std::min(n, E);
+  a.hcap = std::max((lmax * NSRd + sms - 1) / sms, (NSRd + a.jd - 2) / (a.jd - 1)) + 1;
+  const size_t hbytes = (std::max((size_t)a.hcap * kPHStage, (size_t)T * E * 8) + 15) & ~size_t(15);
+  const size_t fixed = 1024 + hbytes + 8 * (2 * kPMaxStages + 5 + a.hcap);
+  a.nst = (int)std::min<size_t>(kPMaxStages, (kPSmemMax - fixed) / a.stride);
+  if (a.nst < 2) return MOE_ERR_ARG;
+  a.ring_bytes = std::max(a.nst * a.stride, (kPWarps * kPStage + 1023) & ~1023);
+  const size_t smem = fixed + (size_t)a.ring_bytes;
+  if (smem > (size_t)kPSmemMax) return MOE_ERR_ARG;
+  static bool attr[64] = {};
+  MOE_CUDA_TRY(ensure_smem(decode_layer_kernel, kPSmemMax, attr));
+  int occ = 0;
+  MOE_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, decode_layer_kernel, kPThreads, smem));
+  if (occ < 1) return MOE_ERR_ARG;
+  const size_t mat = (size_t)H * I;
+  CUtensorMap mwg, mwd;
+  {
+    const uint64_t dims[4] = {64, (uint64_t)H, (uint64_t)I / 64, 3ull * la->S};
+    const uint64_t str[3] = {(uint64_t)I * 2, 128, mat * 2};
+    const uint32_t box[4] = {64, kPK, (uint32_t)I / 64, 1};
+    if (encode_tmap_bf16(&mwg, la->pool, 4, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B) != MOE_OK) return MOE_ERR_CUDA;
+  }
+  {
+    const uint64_t dims[4] = {64, (uint64_t)I, (uint64_t)H / 64, 3ull * la->S};
+    const uint64_t str[3] = {(uint64_t)H * 2, 128, mat * 2};
+    const uint32_t box[4] = {64, kPK, (uint32_t)H / 64, 1};
+    if (encode_tmap_bf16(&mwd, la->pool, 4, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B) != MOE_OK) return MOE_ERR_CUDA;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(sms);
+  cfg.blockDim = dim3(kPThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeCooperative;
+  at[0].val.cooperative = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  MOE_CUDA_TRY(cudaLaunchKernelEx(&cfg, decode_layer_kernel, a, mwg, mwd));
+  return MOE_OK;
+}
+
+}  // namespace moe

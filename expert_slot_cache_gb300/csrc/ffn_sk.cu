@@ -473,6 +473,24 @@ static bool sk_carve(const FfnArgs& a, SkCarve* c) {
   return c->jg >= 2 && c->jd >= 2;
 }
 
+bool sk_part_layout(int n, int H, int I, float* skp, size_t skp_bytes, float** gpart, float** ypart, int* jg,
+                    int* jd) {
+  FfnArgs a{};
+  a.T = n;
+  a.k = 1;
+  a.H = H;
+  a.I = I;
+  a.skp = skp;
+  a.skp_bytes = skp_bytes;
+  SkCarve c;
+  if (!sk_carve(a, &c)) return false;
+  *gpart = c.gpart;
+  *ypart = c.ypart;
+  *jg = c.jg;
+  *jd = c.jd;
+  return true;
+}
+
 static bool sk_pass(bool down, const FfnArgs& a, int G, float* part, int jcap, SkPass* out) {
   SkPass sp{};
   sp.part = part;

@@ -69,6 +69,9 @@ bool prefill_eligible(const FfnArgs& a, int n);
 int launch_gather_rows(const uint16_t* x, const int32_t* rows, int n, int H, int k, uint16_t* xp, int sms,
                        cudaStream_t stream);
 size_t sk_part_bytes(int n, int H, int I);
+// Gate/up parts [jg][n][2I] and down parts [jd][n][H] (fp32) inside a buffer of sk_part_bytes(n, H, I).
+bool sk_part_layout(int n, int H, int I, float* skp, size_t skp_bytes, float** gpart, float** ypart, int* jg,
+                    int* jd);
 size_t q8_slab_bytes_h(int H, int I);
 size_t q8_ws_bytes(int n, int H, int I);
 int launch_ffn_q8(const FfnArgs& a, void* ws, size_t ws_bytes, int max_list, cudaStream_t stream, Prof* prof);
@@ -97,6 +100,11 @@ int launch_gather(const void* host_slabs, void* pool, size_t slab_bytes, int E, 
                   cudaStream_t stream);
 int check_host_accessible(const void* p);
 int launch_window_add(const int32_t* count, int E, int32_t* counts, cudaStream_t stream);
+// The persistent decode kernel (all-resident small batches, one cooperative launch).
+bool decode_eligible(int T, int H, int E, int k, int I, int S, const void* x, const void* wr, const void* pool);
+size_t decode_ctr_ints(int E);
+int launch_decode(const moe_layer_args* la, float* lpart, float* logits, float* skp, size_t skp_bytes, int32_t* ctr,
+                  cudaStream_t stream);
 int route_impl(const void* x, const void* w_router, const float* logit_offset, const float* sel_bias,
                const int32_t* e2s, float affinity, int rflags, int T, int H, int E, int k, float* logits,
                float* scratch, int32_t* ids, float* w, cudaStream_t stream, const PermOut* perm, bool* fused);

@@ -329,7 +329,8 @@ enum {
   MOE_PROF_FFN_DOWN = 5,
   MOE_PROF_COMBINE = 6,
   MOE_PROF_FFN_ROWS = 7, /* grouped copy of the routed rows of x (tensor-core path) */
-  MOE_PROF_CLASSES = 8
+  MOE_PROF_DECODE = 8,   /* the persistent decode kernel: the whole layer in one launch */
+  MOE_PROF_CLASSES = 9
 };
 typedef struct moe_prof {
   void** events;    /* cudaEvent_t[capacity] */
@@ -454,6 +455,7 @@ typedef struct moe_layer_args {
   int32_t* window_counts;    /* device int32 [E] or NULL: each chunk's routings are added (moe_cache_count) */
   int32_t quant;             /* 0: bf16 slabs; 1: W8A8 slabs (moe_quantize_slabs), RESIDENT or GATHER mode */
   int32_t schedule;          /* GATHER steps larger than the pool: MOE_SCHED_CHUNKS or MOE_SCHED_WAVES */
+  int32_t decode_kernels;    /* RESIDENT: 0 = the persistent decode kernel where it applies, 1 = separate kernels */
 } moe_layer_args;
 
 /*
@@ -467,6 +469,15 @@ typedef struct moe_layer_args {
  * Steps larger than the pool (GATHER, S < E, T*k > S): token chunks or
  * expert waves, as args->schedule says (MOE_SCHED_*).  ZERO_RETURN (STATIC)
  * never chunks.
+ * Small all-resident steps (RESIDENT, bf16, T <= 8, T*k <= 64, E <= 256,
+ * H % 128 == 0 and H <= 2048, I % 128 == 0 and I <= 1024, no window counts,
+ * decode_kernels == 0) run as one persistent cooperative launch, one CTA per
+ * SM: router logits, a grid-wide wait, the top-k and grouping in every CTA,
+ * the gate/up weight stream, the down weight stream (its weights loaded while
+ * h is formed from the gate/up sums) and the combine.  Its grid-wide waits
+ * are bounded: a wait that gives up sets MOE_DEV_TIMEOUT.  It keeps arrival
+ * counters at the start of the workspace, which must therefore be
+ * zero-filled once before the first call on it (each call leaves them zero).
  * `side` may be NULL or equal to `main` (then everything runs on `main`).
  * The sequence of launches depends only on the shapes, so it can be
  * captured into a CUDA graph.
@@ -475,6 +486,8 @@ typedef struct moe_layer_args {
  */
 int moe_layer_forward(const moe_layer_args* args, moe_stream_t main, moe_stream_t side);
 
+/* Workspace of moe_layer_forward (device, 256-byte aligned, zero-filled once
+ * before its first use: see above). */
 size_t moe_layer_workspace_bytes(int T, int H, int E, int k, int I, int S);
 
 /* The same size with the arguments in the order (T, H, I, E, k): the

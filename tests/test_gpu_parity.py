@@ -335,7 +335,8 @@ def test_combine_parity_split():
 # Whole layer
 # ----------------------------------------------------------------------------
 
-def _run_layer(cfg, steps=1, side=True, policy=None, T=None, bias_mode=O.BIAS_GRADED, rflags=0, schedule=None):
+def _run_layer(cfg, steps=1, side=True, policy=None, T=None, bias_mode=O.BIAS_GRADED, rflags=0, schedule=None,
+               decode_kernels=0):
     T = cfg.T if T is None else T
     policy = cfg.policy if policy is None else policy
     schedule = cfg.schedule if schedule is None else schedule
@@ -361,7 +362,7 @@ def _run_layer(cfg, steps=1, side=True, policy=None, T=None, bias_mode=O.BIAS_GR
     layer = M.SlotCachedMoELayer(st["wr"], pool, cfg.k, cfg.I, cfg.mode, policy,
                                  host_slabs=None if cfg.mode == C.MODE_RESIDENT else st["host"], state=gstate,
                                  logit_offset=st["logit_offset"], sel_bias=bias_d, max_tokens=T, side_stream=side,
-                                 route_flags=rflags, schedule=schedule)
+                                 route_flags=rflags, schedule=schedule, decode_kernels=decode_kernels)
     wr_np = _np(st["wr"].float())
     off_np = None if st["logit_offset"] is None else _np(st["logit_offset"])
     slabs = HostSlabs(st["host"])
