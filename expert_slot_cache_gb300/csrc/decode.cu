@@ -175,7 +175,7 @@ __global__ void __launch_bounds__(kPThreads, 1) decode_layer_kernel(const Decode
   __shared__ float s_w[kPMaxN];
   __shared__ int s_cnt[kPMaxE], s_off[kPMaxE + 1], s_act[kPMaxE], s_li[kPMaxE];
   __shared__ int tmp[33];
-  __shared__ float4 s_y[kPThreads];
+  __shared__ float4 s_y[2][kPThreads];
   __shared__ int s_nact, s_abort;
   __shared__ uint32_t s_tmem;
 
@@ -518,24 +518,44 @@ __global__ void __launch_bounds__(kPThreads, 1) decode_layer_kernel(const Decode
         if (etid == 0 && !wait_count(&a.ctr[li], Jg, a.status)) *abort_flag = 1;
         named_sync(1, 128);
         const int lbase = li * NSRd - bd;
-        // (stage, row, token) elements of the batch's tokens; lane pairs take the gate sum (even lane)
-        // and the up sum (odd lane) of one element; four items per thread have their parts in flight
+        // (stage, row, token) elements of the batch's tokens, stage-major; lane pairs take the gate sum
+        // (even lane) and the up sum (odd lane) of one element.  After each round the stages it
+        // completed get their padding tokens (t >= nb, zeros) and go to the tensor cores.
         const int nst_seg = g.s_hi - g.s_lo;
-        const int nel = nst_seg * kPK * g.nb;
+        const int per_st = kPK * g.nb;
+        const int nel = nst_seg * per_st;
         const size_t pstride = (size_t)n * Ng;
-        // one item per thread with its parts 32 at a time, or four items with 8 parts each in flight
-        if (2 * nel <= 128) {
-          const int v = etid, el = v >> 1;
-          const bool okv = el < nel;
-          int st = 0, t = 0, r = 0;
-          const float* src = a.gpart;
-          if (okv) {
-            st = el / (kPK * g.nb);
-            const int rem = el - st * (kPK * g.nb);
-            t = rem / kPK;
-            r = rem - t * kPK;
-            src = a.gpart + (size_t)(g.p0 + t) * Ng + (g.s_lo + st) * kPK + r + ((v & 1) ? I : 0);
+        int done_st = 0;
+        auto release = [&](int st_hi) {  // uniform over the epilogue warps
+          const int npad = (st_hi - done_st) * kPK * (kPN - g.nb);
+          for (int v = etid; v < npad && h_ok; v += 128) {
+            const int st = done_st + v / (kPK * (kPN - g.nb)), rem = v % (kPK * (kPN - g.nb));
+            const int t = g.nb + rem / kPK, r = rem % kPK;
+            *reinterpret_cast<uint16_t*>(hsm + (size_t)(lbase + g.s_lo + st) * kPHStage + (r >> 3) * kPAct +
+                                         t * 16 + (r & 7) * 2) = 0;
           }
+          fence_async_smem();
+          named_sync(1, 128);
+          if (etid == 0)
+            for (int st = done_st; st < st_hi; ++st)
+              if (lbase + g.s_lo + st < a.hcap) mbar_arrive(&hbar[lbase + g.s_lo + st]);
+          done_st = st_hi;
+        };
+        auto store_h = [&](int el, float gsum, float usum) {
+          const int st = el / per_st, rem = el - st * per_st, t = rem / kPK, r = rem - t * kPK;
+          const float hv = gsum / (1.f + expf(-gsum)) * usum;
+          *reinterpret_cast<uint16_t*>(hsm + (size_t)(lbase + g.s_lo + st) * kPHStage + (r >> 3) * kPAct +
+                                       t * 16 + (r & 7) * 2) = f32_to_bf16(hv);
+        };
+        auto src_of = [&](int v) {
+          const int el = v >> 1, st = el / per_st, rem = el - st * per_st, t = rem / kPK, r = rem - t * kPK;
+          return a.gpart + (size_t)(g.p0 + t) * Ng + (g.s_lo + st) * kPK + r + ((v & 1) ? I : 0);
+        };
+        if (2 * nel <= 128) {
+          // one item per thread, its parts 32 at a time
+          const int v = etid;
+          const bool okv = (v >> 1) < nel;
+          const float* src = okv ? src_of(v) : a.gpart;
           float acc = 0.f;
           for (int j0 = 0; j0 < Jg; j0 += 32) {
             float pv[32];
@@ -546,65 +566,42 @@ __global__ void __launch_bounds__(kPThreads, 1) decode_layer_kernel(const Decode
               if (j0 + u < Jg) acc += pv[u];
           }
           const float other = __shfl_xor_sync(MOE_FULL_MASK, acc, 1);
-          if (okv && !(v & 1) && h_ok) {
-            const float hv = acc / (1.f + expf(-acc)) * other;
-            *reinterpret_cast<uint16_t*>(hsm + (size_t)(lbase + g.s_lo + st) * kPHStage + (r >> 3) * kPAct +
-                                         t * 16 + (r & 7) * 2) = f32_to_bf16(hv);
-          }
-        } else
-        for (int v0 = 0; v0 < 2 * nel; v0 += 4 * 128) {  // the same trip count in every epilogue thread
-          float acc[4] = {0.f, 0.f, 0.f, 0.f};
-          const float* src[4];
-          bool ok[4];
+          if (okv && !(v & 1) && h_ok) store_h(v >> 1, acc, other);
+        } else {
+          // four items per thread with 8 parts each in flight
+          for (int v0 = 0; v0 < 2 * nel; v0 += 4 * 128) {  // the same trip count in every epilogue thread
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            const float* src[4];
+            bool ok[4];
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            const int v = v0 + q4 * 128 + etid, el = v >> 1;
-            ok[q4] = el < nel;
-            src[q4] = a.gpart;
-            if (ok[q4]) {
-              const int st = el / (kPK * g.nb), rem = el - st * (kPK * g.nb), t = rem / kPK, r = rem - t * kPK;
-              src[q4] = a.gpart + (size_t)(g.p0 + t) * Ng + (g.s_lo + st) * kPK + r + ((v & 1) ? I : 0);
+            for (int q4 = 0; q4 < 4; ++q4) {
+              const int v = v0 + q4 * 128 + etid;
+              ok[q4] = (v >> 1) < nel;
+              src[q4] = ok[q4] ? src_of(v) : a.gpart;
             }
-          }
-          for (int j0 = 0; j0 < Jg; j0 += 8) {
-            float pv[4][8];
+            for (int j0 = 0; j0 < Jg; j0 += 8) {
+              float pv[4][8];
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4)
+              for (int q4 = 0; q4 < 4; ++q4)
 #pragma unroll
-              for (int u = 0; u < 8; ++u)
-                pv[q4][u] = (ok[q4] && j0 + u < Jg) ? __ldcg(src[q4] + (size_t)(j0 + u) * pstride) : 0.f;
+                for (int u = 0; u < 8; ++u)
+                  pv[q4][u] = (ok[q4] && j0 + u < Jg) ? __ldcg(src[q4] + (size_t)(j0 + u) * pstride) : 0.f;
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4)
+              for (int q4 = 0; q4 < 4; ++q4)
 #pragma unroll
-              for (int u = 0; u < 8; ++u)
-                if (j0 + u < Jg) acc[q4] += pv[q4][u];
-          }
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            const float other = __shfl_xor_sync(MOE_FULL_MASK, acc[q4], 1);
-            const int v = v0 + q4 * 128 + etid, el = v >> 1;
-            if (ok[q4] && !(v & 1) && h_ok) {
-              const int st = el / (kPK * g.nb), rem = el - st * (kPK * g.nb), t = rem / kPK, r = rem - t * kPK;
-              const float hv = acc[q4] / (1.f + expf(-acc[q4])) * other;
-              *reinterpret_cast<uint16_t*>(hsm + (size_t)(lbase + g.s_lo + st) * kPHStage + (r >> 3) * kPAct +
-                                           t * 16 + (r & 7) * 2) = f32_to_bf16(hv);
+                for (int u = 0; u < 8; ++u)
+                  if (j0 + u < Jg) acc[q4] += pv[q4][u];
             }
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+              const float other = __shfl_xor_sync(MOE_FULL_MASK, acc[q4], 1);
+              const int v = v0 + q4 * 128 + etid;
+              if (ok[q4] && !(v & 1) && h_ok) store_h(v >> 1, acc[q4], other);
+            }
+            release(min(nel, (v0 + 4 * 128) >> 1) / per_st);
           }
         }
-        // the padding tokens of the MMA (t >= nb) read zeros
-        const int npad = nst_seg * kPK * (kPN - g.nb);
-        for (int v = etid; v < npad && h_ok; v += 128) {
-          const int st = v / (kPK * (kPN - g.nb)), rem = v - st * (kPK * (kPN - g.nb));
-          const int t = g.nb + rem / kPK, r = rem % kPK;
-          *reinterpret_cast<uint16_t*>(hsm + (size_t)(lbase + g.s_lo + st) * kPHStage + (r >> 3) * kPAct + t * 16 +
-                                       (r & 7) * 2) = 0;
-        }
-        // this segment's stages may go to the tensor cores
-        fence_async_smem();
-        named_sync(1, 128);
-        if (etid == 0)
-          for (int s = g.s_lo; s < g.s_hi; ++s)
-            if (lbase + s < a.hcap) mbar_arrive(&hbar[lbase + s]);
+        if (done_st < nst_seg) release(nst_seg);
         return true;
       });
       stream_segments<kPN>(fa, NSRd, Ld, bd, ed_end, [&](const StreamSeg& g) {
@@ -629,72 +626,78 @@ __global__ void __launch_bounds__(kPThreads, 1) decode_layer_kernel(const Decode
 
   // ---- combine: out[t] = sum_j w[t][j] * (sum of y's parts), j ascending ---------------
   {
-    // item = (token, cpi 16-byte column groups); thread = (pick jj, column group cc, part group pg):
-    // part group pg adds parts pg, pg + npg, ... in order, the npg sums are added in pg order
+    // item = (token, cpi x cpt 16-byte column groups); thread = (pick jj, column group cc, part group
+    // pg) for each of its cpt column groups: part group pg adds parts pg, pg + npg, ... in order, the
+    // npg sums are added in pg order.  cpt = 2 when one group per thread would leave a CTA two items.
     const int nc4 = H / 4;
     const int cpi = max(1, min(kPThreads / k, (T * nc4 + G - 1) / G));
+    const int cpt = (cpi == kPThreads / k && (T * nc4 + G * cpi - 1) / (G * cpi) > 1) ? 2 : 1;
     const int npg = max(1, kPThreads / (k * cpi));
     const int pg = tid % npg, rest = tid / npg, cc = rest % cpi, jj = rest / cpi;
-    const int chunks = (nc4 + cpi - 1) / cpi;
+    const int chunks = (nc4 + cpi * cpt - 1) / (cpi * cpt);
     for (int item = blockIdx.x; item < T * chunks; item += G) {
-      const int t = item / chunks, c4 = (item - t * chunks) * cpi + cc;
-      const bool act = jj < k && c4 < nc4;
-      if (act) {
+      const int t = item / chunks, cbase = (item - t * chunks) * cpt * cpi + cc;
+      if (jj < k) {
         const int i = t * k + jj, p = s_pos[i];
         const int Jd = stream_parts(s_li[s_ids[i]], NSRd, Ld);
-        const float4* src = reinterpret_cast<const float4*>(a.ypart + (size_t)p * H) + c4;
         const size_t stride4 = (size_t)n * H / 4;
-        float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
+        float4 y[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
         for (int j0 = pg; j0 < Jd; j0 += 4 * npg) {
-          float4 v[4];
+          float4 v[2][4];
 #pragma unroll
-          for (int u = 0; u < 4; ++u)
-            if (j0 + u * npg < Jd) v[u] = __ldcg(src + (size_t)(j0 + u * npg) * stride4);
+          for (int sb = 0; sb < 2; ++sb) {
+            const int c4 = cbase + sb * cpi;
+            const float4* src = reinterpret_cast<const float4*>(a.ypart + (size_t)p * H) + c4;
 #pragma unroll
-          for (int u = 0; u < 4; ++u)
-            if (j0 + u * npg < Jd) {
-              y.x += v[u].x;
-              y.y += v[u].y;
-              y.z += v[u].z;
-              y.w += v[u].w;
-            }
+            for (int u = 0; u < 4; ++u)
+              if (sb < cpt && c4 < nc4 && j0 + u * npg < Jd) v[sb][u] = __ldcg(src + (size_t)(j0 + u * npg) * stride4);
+          }
+#pragma unroll
+          for (int sb = 0; sb < 2; ++sb)
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              if (sb < cpt && cbase + sb * cpi < nc4 && j0 + u * npg < Jd) {
+                y[sb].x += v[sb][u].x;
+                y[sb].y += v[sb][u].y;
+                y[sb].z += v[sb][u].z;
+                y[sb].w += v[sb][u].w;
+              }
         }
-        s_y[tid] = y;
+        s_y[0][tid] = y[0];
+        s_y[1][tid] = y[1];
       }
       __syncthreads();
-      if (act && jj == 0 && pg == 0) {
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int j = 0; j < k; ++j) {
-          const float wj = s_w[t * k + j];
-          float4 yj = s_y[(j * cpi + cc) * npg];
-          for (int q = 1; q < npg; ++q) {
-            const float4 v = s_y[(j * cpi + cc) * npg + q];
-            yj.x += v.x;
-            yj.y += v.y;
-            yj.z += v.z;
-            yj.w += v.w;
+      if (jj == 0 && pg == 0)
+        for (int sb = 0; sb < cpt; ++sb) {
+          const int c4 = cbase + sb * cpi;
+          if (c4 >= nc4) continue;
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int j = 0; j < k; ++j) {
+            const float wj = s_w[t * k + j];
+            float4 yj = s_y[sb][(j * cpi + cc) * npg];
+            for (int q = 1; q < npg; ++q) {
+              const float4 v = s_y[sb][(j * cpi + cc) * npg + q];
+              yj.x += v.x;
+              yj.y += v.y;
+              yj.z += v.z;
+              yj.w += v.w;
+            }
+            acc.x = fmaf(wj, yj.x, acc.x);
+            acc.y = fmaf(wj, yj.y, acc.y);
+            acc.z = fmaf(wj, yj.z, acc.z);
+            acc.w = fmaf(wj, yj.w, acc.w);
           }
-          acc.x = fmaf(wj, yj.x, acc.x);
-          acc.y = fmaf(wj, yj.y, acc.y);
-          acc.z = fmaf(wj, yj.z, acc.z);
-          acc.w = fmaf(wj, yj.w, acc.w);
+          uint2 o;
+          o.x = uint32_t(f32_to_bf16(acc.x)) | (uint32_t(f32_to_bf16(acc.y)) << 16);
+          o.y = uint32_t(f32_to_bf16(acc.z)) | (uint32_t(f32_to_bf16(acc.w)) << 16);
+          *reinterpret_cast<uint2*>(a.out + (size_t)t * H + 4 * c4) = o;
         }
-        uint2 o;
-        o.x = uint32_t(f32_to_bf16(acc.x)) | (uint32_t(f32_to_bf16(acc.y)) << 16);
-        o.y = uint32_t(f32_to_bf16(acc.z)) | (uint32_t(f32_to_bf16(acc.w)) << 16);
-        *reinterpret_cast<uint2*>(a.out + (size_t)t * H + 4 * c4) = o;
-      }
       __syncthreads();
     }
   }
   // the last CTA out resets the counters: every other CTA is past its last wait
-  if (tid == 0) {
-    __threadfence();
-    if (atomicAdd(&a.ctr[E + kCtrExit], 1) == G - 1) {
-      for (int i = 0; i < E + kCtrCount; ++i) a.ctr[i] = 0;
-      __threadfence();
-    }
-  }
+  if (tid == 0 && atomicAdd(&a.ctr[E + kCtrExit], 1) == G - 1)
+    for (int i = 0; i < E + kCtrCount; ++i) a.ctr[i] = 0;
 }
 
 // ---------------------------------------------------------------------------
