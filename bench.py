@@ -490,17 +490,20 @@ def time_steps(wl: Workload, steps: int, warmup: int, dist=None, clocks=None, pr
     gathered = int(wl.layer.stats[2]) - gathered0
     kern = {n: 0.0 for n in PROF_NAMES}
     launches = {n: 0 for n in PROF_NAMES}
+    per_launch = {n: [] for n in PROF_NAMES}
     ms_prof = None
     if profile:
         n_chunks = (wl.cfg.T + wl.chunk() - 1) // wl.chunk()
-        profs = [_make_prof(M, 4 + 12 * n_chunks) for _ in range(steps)]
+        profs = [_make_prof(M, 8 + 40 * n_chunks) for _ in range(steps)]
         ms_prof = run(warmup + steps, profs)
         for p, evs, _, _ in profs:
             for n, v in _prof_times(p, evs).items():
                 kern[n] += sum(v)
                 launches[n] += len(v)
+                per_launch[n].extend(v)
     return {"ms": ms, "ms_instrumented": ms_prof, "kern_ms": kern, "launches": launches, "clocks": cl,
-            "misses": misses, "gathered_bytes": gathered, "graph": graph, "kernel_nodes": nodes[0]}
+            "misses": misses, "gathered_bytes": gathered, "graph": graph, "kernel_nodes": nodes[0],
+            "per_launch": per_launch}
 
 
 def count_unique_all(wl: Workload, steps: int, warmup: int) -> int:
@@ -648,7 +651,9 @@ def resident_decode(dev: str, peaks: dict, T: int, quant: bool = False, steps: i
     w = Workload(c, 2 * steps + warmup, dev, quant=quant)
     r = time_steps(w, steps, warmup)
     units = count_unique_all(w, steps, warmup + steps)
-    t_ffn = (r["kern_ms"]["ffn_gateup"] + r["kern_ms"]["ffn_down"]) * 1e-3
+    # the FFN kernels' live time; for the persistent decode kernel its whole launch (routing and combine
+    # included, so the fraction is a lower bound for its weight streams)
+    t_ffn = (r["kern_ms"]["ffn_gateup"] + r["kern_ms"]["ffn_down"] + r["kern_ms"]["decode"]) * 1e-3
     ffn = units * w.slab_bytes / t_ffn / 1e9 / peaks["hbm_gbs"] if t_ffn > 0 else 0.0
     layer = count_unique_all(w, steps, warmup) * w.slab_bytes / (r["ms"] * 1e-3) / 1e9 / peaks["hbm_gbs"]
     del w
@@ -789,6 +794,7 @@ def main():
                               "misses_per_step": r["misses"] / args.steps,
                               "kernel_nodes_per_step": None if r["kernel_nodes"] is None
                               else r["kernel_nodes"] / args.steps,
+                              "gather_launch_ms": [round(v, 4) for v in r["per_launch"]["gather"][:12]],
                               "kernels_ms_per_step": {n: v / args.steps for n, v in r["kern_ms"].items()}}))
         return
     cfg = main_config()

@@ -11,9 +11,14 @@ namespace moe {
 
 static size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
+// A later wave's loads go in up to kMaxSub sub-batches: the side stream gathers them back to back
+// while the main stream runs each sub-batch's FFN once its gather has landed.
+constexpr int kMaxSub = 4;
+
 // Workspace layout of the layer forward, for chunks of up to n = C*k routing slots.
 struct LayerWs {
   int32_t* ctr;  // arrival counters of the persistent decode kernel (zero between calls)
+  int32_t* sub_n;  // per-sub-batch counts of a later wave's loads
   int32_t *count, *offset, *rows, *pos, *act_e, *n_act, *miss_e, *miss_s, *n_miss, *hit_e, *n_hit, *def_e, *n_def;
   float *hbuf, *y, *logits, *route;
   uint16_t *xp, *hb;
@@ -35,6 +40,7 @@ static LayerWs carve(void* base, int n, int H, int E, int I, int T) {
   };
   const int lmax = std::min(n, E);
   w.ctr = (int32_t*)take(4 * decode_ctr_ints(E));  // first, so its place does not depend on n
+  w.sub_n = (int32_t*)take(4 * kMaxSub);
   w.count = (int32_t*)take(4 * (size_t)E);
   w.offset = (int32_t*)take(4 * (size_t)(E + 1));
   w.rows = (int32_t*)take(4 * (size_t)n);
@@ -304,10 +310,14 @@ extern "C" int moe_layer_forward(const moe_layer_args* a, moe_stream_t main_s, m
         // step has computed already; their gather follows those FFN launches
         const int nw = waves ? later_waves(n, E, S) : 0;
         const int wmax = std::min(S, lmax);
+        const int sub_b = (wmax + kMaxSub - 1) / kMaxSub, n_sub = (wmax + sub_b - 1) / sub_b;
         for (int wv = 1; wv <= nw; ++wv) {
           ManageWave bw;
           bw.n_dev = ws.n_def;
           bw.n_off = (wv - 1) * S;
+          bw.sub_n = ws.sub_n;
+          bw.sub_b = sub_b;
+          bw.n_sub = n_sub;
           prof.begin(MOE_PROF_MANAGE, ms);
           r = launch_manage(ws.def_e, wmax, E, S, policy, a->e2s, a->s2e, a->prio, a->stamp, ws.miss_e, ws.miss_s,
                             ws.n_miss, nullptr, nullptr, nullptr, stats, a->dev_status, ms, &bw);
@@ -317,16 +327,24 @@ extern "C" int moe_layer_forward(const moe_layer_args* a, moe_stream_t main_s, m
             MOE_CUDA_TRY(cudaEventRecord(ev->fork, ms));
             MOE_CUDA_TRY(cudaStreamWaitEvent(ss, ev->fork, 0));
           }
-          prof.begin(MOE_PROF_GATHER, side);
-          r = launch_gather(a->host_slabs, a->pool, slab_bytes, E, S, ws.miss_e, ws.miss_s, ws.n_miss, wmax, stats,
-                            a->dev_status, side);
-          if (r != MOE_OK) return r;
-          prof.end(side);
-          if (two) {
-            MOE_CUDA_TRY(cudaEventRecord(ev->join, ss));
-            MOE_CUDA_TRY(cudaStreamWaitEvent(ms, ev->join, 0));
+          for (int b = 0; b < n_sub; ++b) {
+            // the sub-batch's slots are its own (one manage call gave every load a different victim)
+            prof.begin(MOE_PROF_GATHER, side);
+            r = launch_gather(a->host_slabs, a->pool, slab_bytes, E, S, ws.miss_e + b * sub_b, ws.miss_s + b * sub_b,
+                              ws.sub_n + b, sub_b, stats, a->dev_status, side);
+            if (r != MOE_OK) return r;
+            prof.end(side);
+            if (two) {
+              MOE_CUDA_TRY(cudaEventRecord(ev->join, ss));
+              MOE_CUDA_TRY(cudaStreamWaitEvent(ms, ev->join, 0));
+            }
+            FfnArgs fb = fm;
+            fb.list_e = ws.miss_e + b * sub_b;
+            fb.n_list = ws.sub_n + b;
+            if ((r = (a->quant ? launch_ffn_q8(fb, ws.skp, ws.skp_bytes, sub_b, ms, &prof)
+                               : launch_ffn(fb, sub_b, ms, &prof))) != MOE_OK)
+              return r;
           }
-          if ((r = ffn(fm, ms)) != MOE_OK) return r;
         }
       } else {
         // zero-return: resident experts from the pool on main, missing ones

@@ -32,7 +32,7 @@ __global__ void __launch_bounds__(kManageThreads) manage_kernel(
     uint32_t* __restrict__ stamp_g, int32_t* __restrict__ miss_e, int32_t* __restrict__ miss_s,
     int32_t* __restrict__ n_miss, int32_t* __restrict__ hit_e, int32_t* __restrict__ n_hit,
     int32_t* __restrict__ sid, int32_t* __restrict__ def_e, int32_t* __restrict__ n_def,
-    int64_t* __restrict__ stats, int32_t* __restrict__ status) {
+    int32_t* __restrict__ sub_n, int sub_b, int n_sub, int64_t* __restrict__ stats, int32_t* __restrict__ status) {
   extern __shared__ int man_smem[];
   if (n_dev) {
     n = min(max(*n_dev - n_off, 0), n);
@@ -42,6 +42,8 @@ __global__ void __launch_bounds__(kManageThreads) manage_kernel(
         *n_miss = 0;
         if (n_hit) *n_hit = 0;
         if (n_def) *n_def = 0;
+        if (sub_n)
+          for (int b = 0; b < n_sub; ++b) sub_n[b] = 0;
       }
       return;
     }
@@ -195,6 +197,8 @@ __global__ void __launch_bounds__(kManageThreads) manage_kernel(
     *n_miss = nl;
     if (n_hit) *n_hit = s_nhit;
     if (n_def) *n_def = nm - nl;
+    if (sub_n)
+      for (int b = 0; b < n_sub; ++b) sub_n[b] = min(max(nl - b * sub_b, 0), sub_b);
     if (stats) {
       stats[0] += nl;
       stats[1] += 1;
@@ -353,7 +357,7 @@ int launch_manage(const int32_t* ids, int n, int E, int S, int policy, int32_t* 
   const ManageWave& w = wave ? *wave : nw;
   manage_kernel<<<1, kManageThreads, smem, stream>>>(ids, n, w.n_dev, w.n_off, E, S, policy, e2s, s2e, prio, stamp,
                                                      miss_e, miss_s, n_miss, hit_e, n_hit, sid, w.def_e, w.n_def,
-                                                     stats, dev_status);
+                                                     w.sub_n, w.sub_b, w.n_sub, stats, dev_status);
   MOE_LAUNCH_CHECK();
   return MOE_OK;
 }
@@ -375,11 +379,12 @@ int launch_gather(const void* host_slabs, void* pool, size_t slab_bytes, int E, 
   if (max_miss <= 0) return MOE_OK;
   const size_t slab_vec = slab_bytes / 16;
   const size_t chunks = (slab_vec + kGatherChunkVec - 1) / kGatherChunkVec;
-  int sms = 0, dev = 0;
-  MOE_CUDA_TRY(cudaGetDevice(&dev));
-  MOE_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  // The host link, not the SMs, bounds the copy: on GB300 (NVLink-C2C, pinned memory) 24 CTAs of 256
+  // threads with 32 KB each in flight already reach the link's 211 GB/s (16: 201, 8: 133).  Twice that
+  // leaves the other SMs to the FFN that runs beside the gather on the main stream.
+  constexpr size_t kGatherCtas = 48;
   const size_t items = (size_t)max_miss * chunks;
-  const int grid = (int)std::min<size_t>(items, (size_t)sms * 8);
+  const int grid = (int)std::min<size_t>(items, kGatherCtas);
   gather_kernel<<<grid, kGatherThreads, 0, stream>>>((const uint4*)host_slabs, (uint4*)pool, slab_vec, E, S,
                                                       miss_e, miss_s, n_miss, stats, dev_status);
   MOE_LAUNCH_CHECK();

@@ -90,6 +90,8 @@ struct ManageWave {
   int32_t* n_def = nullptr;
   const int32_t* n_dev = nullptr;
   int n_off = 0;
+  int32_t* sub_n = nullptr;  // with sub_b: sub_n[b] = clamp(n_miss - b*sub_b, 0, sub_b) for b < n_sub
+  int sub_b = 0, n_sub = 0;
 };
 int launch_manage(const int32_t* ids, int n, int E, int S, int policy, int32_t* e2s, int32_t* s2e, uint32_t* prio,
                   uint32_t* stamp, int32_t* miss_e, int32_t* miss_s, int32_t* n_miss, int32_t* hit_e,
