@@ -259,10 +259,11 @@ def stack_variant(dev: str, peaks: dict, cfg: "C.LayerConfig", steps: int = 8, w
     torch.cuda.synchronize()
     ms = s.elapsed_time(e)
     misses = sum(int(l.stats[0]) for l in wl.layers) - misses0
+    slots = sum(C.layer_S(cfg, l) for l in range(wl.L)) if cfg.mode != C.MODE_RESIDENT else wl.L * cfg.E
     out = {"config": f"{cfg.name}: {wl.L} layers x {cfg.E} experts, T={cfg.T}, k={cfg.k}, H={cfg.H}, I={cfg.I}, "
-                     f"S={cfg.S}, {'all resident' if cfg.mode == C.MODE_RESIDENT else 'slot pool + pinned host'}",
+                     f"{slots} slots, {'all resident' if cfg.mode == C.MODE_RESIDENT else 'slot pool + pinned host'}",
            "tokens_per_s": cfg.T * steps / (ms * 1e-3), "ms_per_step": ms / steps,
-           "expert_GB_in_hbm": wl.L * (cfg.S if cfg.mode != C.MODE_RESIDENT else cfg.E) * cfg.slab_bytes / 1e9}
+           "expert_GB_in_hbm": slots * cfg.slab_bytes / 1e9}
     if cfg.mode == C.MODE_RESIDENT:
         units = 0
         C_ = cfg.T  # all-resident: one chunk per layer
@@ -708,6 +709,8 @@ def targets(dev: str, peaks: dict) -> dict:
     t["stack48_tok_s"], t["stack48_hbm"] = st["tokens_per_s"], st["hbm"]["frac"]
     st = stack_variant(dev, peaks, C.STACK_SLOTS.with_(schedule=C.SCHED_WAVES), steps=4)
     t["stack48_slots_tok_s"], t["stack48_slots_link_GB"] = st["tokens_per_s"], st["host_link_GB_per_step"]
+    st = stack_variant(dev, peaks, C.STACK_BUDGET, steps=4)
+    t["stack48_budget_tok_s"], t["stack48_budget_link_GB"] = st["tokens_per_s"], st["host_link_GB_per_step"]
     return {k: _r(v) for k, v in t.items()}
 
 
@@ -739,7 +742,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="main",
                     help="main (default) | prefill | resident_T<n> | gather_T<n> | chunks_T<n> | routing_variants | "
-                         "policy_replay | w8a8 | stack | stack_slots | stack_slots_chunks: one workload alone "
+                         "policy_replay | w8a8 | stack | stack_slots | stack_slots_chunks | stack_budget: one workload alone "
                          "(for profiling); prints its own JSON line")
     args = ap.parse_args()
     ws, rank, local, dist = _dist()
@@ -767,9 +770,9 @@ def main():
                               **policy_replay(C.drifting_trace(cfg.E, cfg.k, 8, 400), cfg.E, cfg.S, dev,
                                               cfg.slab_bytes)}))
         return
-    if args.workload in ("stack", "stack_slots", "stack_slots_chunks"):
+    if args.workload in ("stack", "stack_slots", "stack_slots_chunks", "stack_budget"):
         cfg_s = {"stack": C.STACK, "stack_slots": C.STACK_SLOTS.with_(schedule=C.SCHED_WAVES),
-                 "stack_slots_chunks": C.STACK_SLOTS}[args.workload]
+                 "stack_slots_chunks": C.STACK_SLOTS, "stack_budget": C.STACK_BUDGET}[args.workload]
         if rank == 0:
             print(json.dumps({"workload": args.workload, **stack_variant(dev, peaks, cfg_s, args.steps, args.warmup)}))
         return

@@ -60,6 +60,8 @@ class LayerConfig:
     steps: int = 1
     # GATHER steps larger than the pool: token chunks or expert waves
     schedule: int = SCHED_CHUNKS
+    # per-layer slot counts of a stack (None: every layer has S slots)
+    s_per_layer: Optional[tuple] = None
 
     @property
     def slab_elems(self) -> int:
@@ -95,6 +97,24 @@ STACK = LayerConfig("stack48", T=32, H=2048, E=288, k=8, I=512, S=288, seed=5, x
                     mode=MODE_RESIDENT, layers=48, steps=64)
 
 STACK_SLOTS = STACK.with_(name="stack48-slots", S=144, mode=MODE_GATHER, policy=POLICY_LRU)
+
+
+def budget_slots(E: int, layers: int) -> tuple:
+    """Non-uniform slots per layer after "Betelgeuse ... on an RTX 3060", "Arrival-Slack VRAM Slot Pool":
+    240 slots per layer on layers 0-4 (no compute slack there), 92 on the middle layers, 60 on the tail
+    layers, for 512 experts per layer and about 5,000 slots in all -- which puts 38 layers in the middle
+    and 5 at the tail of 48.  Here the same fractions of E per layer: E*240/512 on the first 5 layers,
+    E*60/512 on the last 5, E*92/512 between."""
+    early, tail = 5, 5
+    return tuple(round(E * (240 if l < early else 60 if l >= layers - tail else 92) / 512) for l in range(layers))
+
+
+STACK_BUDGET = STACK_SLOTS.with_(name="stack48-budget", schedule=SCHED_WAVES, s_per_layer=budget_slots(288, 48))
+
+
+def layer_S(cfg: LayerConfig, layer: int = 0) -> int:
+    """Slots of one layer of a stack."""
+    return cfg.s_per_layer[layer] if cfg.s_per_layer else cfg.S
 
 
 # ----------------------------------------------------------------------------
@@ -158,7 +178,7 @@ def initial_residency(cfg: LayerConfig, layer: int = 0) -> np.ndarray:
     sorted, in slots 0..S-1.  Soft-bias configs: the n_hot experts ranked
     brightest (rank <= n_hot), sorted.  S >= E: expert e in slot e.
     """
-    S, E = cfg.S, cfg.E
+    S, E = layer_S(cfg, layer), cfg.E
     s2e = np.full(S, -1, dtype=np.int32)
     if S >= E:
         s2e[:E] = np.arange(E, dtype=np.int32)

@@ -94,3 +94,16 @@ def test_streams_and_permutations():
     assert np.array_equal(p, gen.permutation(7, 3, 1000))
     assert not np.array_equal(p, gen.permutation(7, 4, 1000))
     assert gen.stream_id(0x3, 0x12, 0x3456) == (0x3 << 24) | (0x12 << 16) | 0x3456
+
+
+def test_budget_slots_follow_the_page_profile():
+    # "Betelgeuse ... on an RTX 3060", "Arrival-Slack VRAM Slot Pool": 240 slots per layer on layers 0-4,
+    # 92 in the middle, 60 at the tail, about 5,000 in all for 48 layers of 512 experts
+    from harness import configs as C
+    b = C.budget_slots(512, 48)
+    assert b[:5] == (240,) * 5 and b[5:43] == (92,) * 38 and b[43:] == (60,) * 5
+    assert abs(sum(b) - 5000) < 25
+    s = C.budget_slots(288, 48)
+    assert s[0] == 135 and s[20] == 52 and s[47] == 34
+    assert [C.layer_S(C.STACK_BUDGET, l) for l in (0, 4, 5, 42, 43, 47)] == [135, 135, 52, 52, 34, 34]
+    assert len(C.initial_residency(C.STACK_BUDGET, 47)) == 34
