@@ -30,6 +30,11 @@ def test_decode_qwen_resident(T):
     _run_layer(C.qwen(T, S=128, mode=C.MODE_RESIDENT), steps=3)
 
 
+def test_decode_one_token_small_shape():
+    # one token on the small shape: two tiles per projection, fewer weight stages than CTAs
+    _run_layer(C.TINY.with_(T=1), steps=4)
+
+
 def test_decode_tiny_resident_with_offset_and_bias():
     cfg = C.TINY.with_(T=7, logit_offset=True, bias_cap=-0.5, n_hot=6, zipf_s=1.1)
     _run_layer(cfg, steps=3)
