@@ -102,3 +102,24 @@ def test_decode_graph_replay_matches_oracle_every_step():
     assert int(_np(layer.dev_status)[0]) == 0
     # the arrival counters (start of the workspace) are back at zero
     assert int(layer.workspace[: 4 * (cfg.E + 4)].count_nonzero()) == 0
+
+
+def test_decode_with_a_remapped_pool():
+    # all experts resident, but in a shuffled slot order (e2s): the kernel reads each expert from its slot
+    import expert_slot_cache_gb300 as M
+    cfg = C.qwen(4, S=128, mode=C.MODE_RESIDENT)
+    st = stage_layer(cfg)
+    perm = np.random.default_rng(9).permutation(cfg.E).astype(np.int32)  # slot s holds expert perm[s]
+    pool = st["slabs_dev"][torch.from_numpy(perm.astype(np.int64)).to(DEV)].contiguous()
+    state = M.CacheState.from_slots(perm, cfg.E)
+    layer = M.SlotCachedMoELayer(st["wr"], pool, cfg.k, cfg.I, C.MODE_RESIDENT, state=state,
+                                 logit_offset=st["logit_offset"], max_tokens=cfg.T)
+    wr_np = _np(st["wr"].float())
+    for step in range(2):
+        x = C.draw_x(cfg, DEV, step=step)
+        r = layer.forward(x)
+        torch.cuda.synchronize()
+        want = O.layer_forward(_np(x.float()), wr_np, HostSlabs(st["host"]), cfg.H, cfg.I, cfg.k, O.RESIDENT)
+        assert np.array_equal(_np(r["ids"]), want["ids"]), step
+        assert_out_close(_np(r["out"].float()), want["out"], f"step {step}")
+    assert int(_np(layer.dev_status)[0]) == 0

@@ -90,11 +90,12 @@ def test_expert_ffn_q8_bit_exact(name, cfg, T, skew):
     assert np.array_equal(got, want), f"max |diff| {np.nanmax(np.abs(got - want))}"
 
 
-@pytest.mark.parametrize("mode,T", [(C.MODE_GATHER, 8), (C.MODE_GATHER, 32), (C.MODE_RESIDENT, 64)],
-                         ids=["gather_T8", "gather_T32_chunked", "resident_T64"])
-def test_layer_w8a8(mode, T):
+@pytest.mark.parametrize("mode,T,sched", [(C.MODE_GATHER, 8, C.SCHED_CHUNKS), (C.MODE_GATHER, 32, C.SCHED_CHUNKS),
+                                          (C.MODE_GATHER, 64, C.SCHED_WAVES), (C.MODE_RESIDENT, 64, C.SCHED_CHUNKS)],
+                         ids=["gather_T8", "gather_T32_chunked", "gather_T64_waves", "resident_T64"])
+def test_layer_w8a8(mode, T, sched):
     import expert_slot_cache_gb300 as M
-    cfg = C.qwen(T, S=64 if mode == C.MODE_GATHER else 128, mode=mode)
+    cfg = C.qwen(T, S=64 if mode == C.MODE_GATHER else 128, mode=mode, schedule=sched)
     wr = C.draw_router(cfg, DEV)
     bf_dev = torch.empty(cfg.E, cfg.slab_elems, dtype=torch.bfloat16, device=DEV)
     C.draw_slabs(cfg, DEV, out=bf_dev)
@@ -111,18 +112,20 @@ def test_layer_w8a8(mode, T):
         gst, ost = M.CacheState.from_slots(s2e0, cfg.E), O.CacheState.from_slots(s2e0, cfg.E)
     del bf_dev
     layer = M.SlotCachedMoELayer(wr, pool, cfg.k, cfg.I, cfg.mode, cfg.policy, host_slabs=host_q, state=gst,
-                                 max_tokens=T, quant=1)
+                                 max_tokens=T, quant=1, schedule=sched)
     wr_np = wr.float().cpu().numpy()
     for step in range(2):
         x = C.draw_x(cfg, DEV, step=step)
         res = layer.forward(x)
         torch.cuda.synchronize()
         want = O.layer_forward(x.float().cpu().numpy(), wr_np, qh, cfg.H, cfg.I, cfg.k, cfg.mode, cfg.policy, ost,
-                               None, quant=True)
+                               None, quant=True, schedule=sched)
         assert np.array_equal(res["ids"].cpu().numpy(), want["ids"]), step
         assert_out_close(res["out"].float().cpu().numpy(), want["out"], f"step {step}")
         if ost is not None:
             assert gst.s2e.cpu().numpy().tolist() == ost.s2e.tolist()
+            assert gst.prio.cpu().numpy().astype(np.uint32).tolist() == ost.prio.tolist()
+            assert int(gst.stamp.item()) == ost.stamp
     assert int(layer.dev_status.item()) == 0
     if mode == C.MODE_GATHER:
         s2e = gst.s2e.cpu().numpy()

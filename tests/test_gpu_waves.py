@@ -48,3 +48,30 @@ def test_waves_step_that_fits_equals_token_chunks():
     b = _run_layer(C.qwen(8, S=64), steps=2)
     for f in ("e2s", "s2e", "prio", "stamp"):
         assert np.array_equal(getattr(a.state, f).cpu().numpy(), getattr(b.state, f).cpu().numpy()), f
+
+
+def test_waves_with_live_cache_affinity():
+    # affinity reads the expert -> slot table before the step's first manage call
+    import expert_slot_cache_gb300 as M
+    import oracle as O
+    import torch
+    from tests._setup import HostSlabs, assert_out_close, stage_layer
+    from tests.test_gpu_parity import _check_state, _np
+    cfg = C.qwen(64, schedule=W)
+    st = stage_layer(cfg)
+    s2e0 = C.initial_residency(cfg)
+    pool = st["slabs_dev"][torch.from_numpy(s2e0.astype(np.int64)).to("cuda")].contiguous()
+    gstate = M.CacheState.from_slots(s2e0, cfg.E)
+    ostate = O.CacheState.from_slots(s2e0, cfg.E)
+    layer = M.SlotCachedMoELayer(st["wr"], pool, cfg.k, cfg.I, cfg.mode, cfg.policy, host_slabs=st["host"],
+                                 state=gstate, max_tokens=cfg.T, affinity=0.5, schedule=W)
+    for step in range(3):
+        x = C.draw_x(cfg, "cuda", step=step)
+        r = layer.forward(x)
+        torch.cuda.synchronize()
+        want = O.layer_forward(_np(x.float()), _np(st["wr"].float()), HostSlabs(st["host"]), cfg.H, cfg.I, cfg.k,
+                               cfg.mode, cfg.policy, ostate, affinity=0.5, schedule=O.SCHED_WAVES)
+        assert np.array_equal(_np(r["ids"]), want["ids"]), step
+        assert_out_close(_np(r["out"].float()), want["out"], f"step {step}")
+        _check_state(gstate, ostate, f"step {step}")
+    assert int(layer.dev_status.item()) == 0
