@@ -20,6 +20,7 @@ struct LayerWs {
   int32_t* ctr;  // arrival counters of the persistent decode kernel (zero between calls)
   int32_t* sub_n;  // per-sub-batch counts of a later wave's loads
   int32_t *count, *offset, *rows, *pos, *act_e, *n_act, *miss_e, *miss_s, *n_miss, *hit_e, *n_hit, *def_e, *n_def;
+  int32_t *wl_e, *wl_s, *n_wl, *ev_e, *kept_e, *n_kept;  // later waves: loads, evicted experts, kept experts
   float *hbuf, *y, *logits, *route;
   uint16_t *xp, *hb;
   int32_t* perm;
@@ -54,6 +55,12 @@ static LayerWs carve(void* base, int n, int H, int E, int I, int T) {
   w.n_hit = (int32_t*)take(4);
   w.def_e = (int32_t*)take(4 * (size_t)lmax);
   w.n_def = (int32_t*)take(4);
+  w.wl_e = (int32_t*)take(4 * (size_t)lmax);
+  w.wl_s = (int32_t*)take(4 * (size_t)lmax);
+  w.n_wl = (int32_t*)take(4);
+  w.ev_e = (int32_t*)take(4 * (size_t)lmax);
+  w.kept_e = (int32_t*)take(4 * (size_t)lmax);
+  w.n_kept = (int32_t*)take(4);
   w.hbuf = (float*)take(4 * (size_t)n * I);
   w.y = (float*)take(4 * (size_t)n * H);
   w.logits = (float*)take(4 * (size_t)T * E);
@@ -82,9 +89,9 @@ static int later_waves(int n, int E, int S) {
   return most > 0 ? (most + S - 1) / S : 0;
 }
 
-// Two cached events per device for the fork/join with the side stream.
+// Cached events per device for the fork/join with the side stream (one per sub-batch of a wave's gather).
 struct DevEvents {
-  cudaEvent_t fork = nullptr, join = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr, sub[kMaxSub] = {};
 };
 static DevEvents g_events[64];
 static std::mutex g_events_mu;
@@ -98,6 +105,7 @@ static int get_events(DevEvents** out) {
   if (!d.fork) {
     MOE_CUDA_TRY(cudaEventCreateWithFlags(&d.fork, cudaEventDisableTiming));
     MOE_CUDA_TRY(cudaEventCreateWithFlags(&d.join, cudaEventDisableTiming));
+    for (int b = 0; b < kMaxSub; ++b) MOE_CUDA_TRY(cudaEventCreateWithFlags(&d.sub[b], cudaEventDisableTiming));
   }
   *out = &d;
   return MOE_OK;
@@ -296,55 +304,97 @@ extern "C" int moe_layer_forward(const moe_layer_args* a, moe_stream_t main_s, m
       }
       cudaStream_t side = two ? ss : ms;
       if (mode == MOE_MODE_GATHER) {
-        // side: gather the misses; main: the hit experts' FFN meanwhile; then the misses.
-        prof.begin(MOE_PROF_GATHER, side);
-        r = launch_gather(a->host_slabs, a->pool, slab_bytes, E, S, ws.miss_e, ws.miss_s, ws.n_miss, lmax, stats,
-                          a->dev_status, side);
-        if (r != MOE_OK) return r;
-        prof.end(side);
-        if (two) MOE_CUDA_TRY(cudaEventRecord(ev->join, ss));
-        if ((r = ffn(fh, ms)) != MOE_OK) return r;
-        if (two) MOE_CUDA_TRY(cudaStreamWaitEvent(ms, ev->join, 0));
-        if ((r = ffn(fm, ms)) != MOE_OK) return r;
-        // later waves: the next S deferred experts evict slots whose experts this
-        // step has computed already; their gather follows those FFN launches
         const int nw = waves ? later_waves(n, E, S) : 0;
         const int wmax = std::min(S, lmax);
         const int sub_b = (wmax + kMaxSub - 1) / kMaxSub, n_sub = (wmax + sub_b - 1) / sub_b;
-        for (int wv = 1; wv <= nw; ++wv) {
+        // the FFN of a device-side list (slots from e2s, or from `ls` for experts already evicted)
+        auto ffn_list = [&](const int32_t* le, const int32_t* ls, const int32_t* nl, int maxl) -> int {
+          FfnArgs fb = fm;
+          fb.list_e = le;
+          fb.list_s = ls;
+          fb.n_list = nl;
+          return a->quant ? launch_ffn_q8(fb, ws.skp, ws.skp_bytes, maxl, ms, &prof) : launch_ffn(fb, maxl, ms, &prof);
+        };
+        auto gather_list = [&](const int32_t* le, const int32_t* ls, const int32_t* nl, int maxl) -> int {
+          prof.begin(MOE_PROF_GATHER, side);
+          const int rg = launch_gather(a->host_slabs, a->pool, slab_bytes, E, S, le, ls, nl, maxl, stats,
+                                       a->dev_status, side);
+          prof.end(side);
+          return rg;
+        };
+        auto manage_wave = [&](int wv, const ManageKeep* keep) -> int {
           ManageWave bw;
           bw.n_dev = ws.n_def;
           bw.n_off = (wv - 1) * S;
           bw.sub_n = ws.sub_n;
           bw.sub_b = sub_b;
           bw.n_sub = n_sub;
+          if (keep) bw.keep = *keep;
           prof.begin(MOE_PROF_MANAGE, ms);
-          r = launch_manage(ws.def_e, wmax, E, S, policy, a->e2s, a->s2e, a->prio, a->stamp, ws.miss_e, ws.miss_s,
-                            ws.n_miss, nullptr, nullptr, nullptr, stats, a->dev_status, ms, &bw);
-          if (r != MOE_OK) return r;
+          const int rm = launch_manage(ws.def_e, wmax, E, S, policy, a->e2s, a->s2e, a->prio, a->stamp, ws.wl_e,
+                                       ws.wl_s, ws.n_wl, nullptr, nullptr, nullptr, stats, a->dev_status, ms, &bw);
           prof.end(ms);
+          return rm;
+        };
+        // a later wave: the next S deferred experts evict slots whose experts this step has computed
+        // already; the side stream gathers its sub-batches back to back, the main stream runs each
+        // sub-batch's FFN once its gather has landed
+        auto later_wave = [&](int wv) -> int {
+          int rw = manage_wave(wv, nullptr);
+          if (rw != MOE_OK) return rw;
           if (two) {
             MOE_CUDA_TRY(cudaEventRecord(ev->fork, ms));
             MOE_CUDA_TRY(cudaStreamWaitEvent(ss, ev->fork, 0));
           }
           for (int b = 0; b < n_sub; ++b) {
             // the sub-batch's slots are its own (one manage call gave every load a different victim)
-            prof.begin(MOE_PROF_GATHER, side);
-            r = launch_gather(a->host_slabs, a->pool, slab_bytes, E, S, ws.miss_e + b * sub_b, ws.miss_s + b * sub_b,
-                              ws.sub_n + b, sub_b, stats, a->dev_status, side);
-            if (r != MOE_OK) return r;
-            prof.end(side);
+            if ((rw = gather_list(ws.wl_e + b * sub_b, ws.wl_s + b * sub_b, ws.sub_n + b, sub_b)) != MOE_OK)
+              return rw;
             if (two) {
               MOE_CUDA_TRY(cudaEventRecord(ev->join, ss));
               MOE_CUDA_TRY(cudaStreamWaitEvent(ms, ev->join, 0));
             }
-            FfnArgs fb = fm;
-            fb.list_e = ws.miss_e + b * sub_b;
-            fb.n_list = ws.sub_n + b;
-            if ((r = (a->quant ? launch_ffn_q8(fb, ws.skp, ws.skp_bytes, sub_b, ms, &prof)
-                               : launch_ffn(fb, sub_b, ms, &prof))) != MOE_OK)
-              return r;
+            if ((rw = ffn_list(ws.wl_e + b * sub_b, nullptr, ws.sub_n + b, sub_b)) != MOE_OK) return rw;
           }
+          return MOE_OK;
+        };
+        // With a later wave and the decode stream FFN, wave 1's manage call runs before any FFN of the
+        // step: the experts it evicts (hits or wave 0's loads) are computed first, sub-batch by
+        // sub-batch, reading their old slots, and each sub-batch's gather follows them at once; the
+        // experts that stay in place are computed while wave 1's gather runs.  The calls, and so the
+        // cache state, are those of the plain order.
+        const bool ahead = nw >= 1 && two && (a->quant || sk_eligible(fm));
+        if (ahead) {
+          const ManageKeep keep{ws.ev_e, ws.hit_e, ws.n_hit, ws.miss_e, ws.n_miss, ws.kept_e, ws.n_kept};
+          if ((r = manage_wave(1, &keep)) != MOE_OK) return r;
+          MOE_CUDA_TRY(cudaEventRecord(ev->fork, ms));
+          MOE_CUDA_TRY(cudaStreamWaitEvent(ss, ev->fork, 0));
+          if ((r = gather_list(ws.miss_e, ws.miss_s, ws.n_miss, lmax)) != MOE_OK) return r;
+          MOE_CUDA_TRY(cudaEventRecord(ev->join, ss));
+          MOE_CUDA_TRY(cudaStreamWaitEvent(ms, ev->join, 0));  // wave 0's loads are in their slots
+          for (int b = 0; b < n_sub; ++b) {
+            if ((r = ffn_list(ws.ev_e + b * sub_b, ws.wl_s + b * sub_b, ws.sub_n + b, sub_b)) != MOE_OK) return r;
+            MOE_CUDA_TRY(cudaEventRecord(ev->fork, ms));
+            MOE_CUDA_TRY(cudaStreamWaitEvent(ss, ev->fork, 0));
+            if ((r = gather_list(ws.wl_e + b * sub_b, ws.wl_s + b * sub_b, ws.sub_n + b, sub_b)) != MOE_OK) return r;
+            MOE_CUDA_TRY(cudaEventRecord(ev->sub[b], ss));
+          }
+          if ((r = ffn_list(ws.kept_e, nullptr, ws.n_kept, lmax)) != MOE_OK) return r;
+          for (int b = 0; b < n_sub; ++b) {
+            MOE_CUDA_TRY(cudaStreamWaitEvent(ms, ev->sub[b], 0));
+            if ((r = ffn_list(ws.wl_e + b * sub_b, nullptr, ws.sub_n + b, sub_b)) != MOE_OK) return r;
+          }
+          for (int wv = 2; wv <= nw; ++wv)
+            if ((r = later_wave(wv)) != MOE_OK) return r;
+        } else {
+          // side: gather the misses; main: the hit experts' FFN meanwhile; then the misses.
+          if ((r = gather_list(ws.miss_e, ws.miss_s, ws.n_miss, lmax)) != MOE_OK) return r;
+          if (two) MOE_CUDA_TRY(cudaEventRecord(ev->join, ss));
+          if ((r = ffn(fh, ms)) != MOE_OK) return r;
+          if (two) MOE_CUDA_TRY(cudaStreamWaitEvent(ms, ev->join, 0));
+          if ((r = ffn(fm, ms)) != MOE_OK) return r;
+          for (int wv = 1; wv <= nw; ++wv)
+            if ((r = later_wave(wv)) != MOE_OK) return r;
         }
       } else {
         // zero-return: resident experts from the pool on main, missing ones

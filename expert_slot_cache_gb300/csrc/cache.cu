@@ -18,6 +18,41 @@ namespace moe {
 constexpr int kManageThreads = 1024;
 constexpr int kMaxS = 4096;
 
+// kept list of a manage call: the experts of keep.in0 and keep.in1 that none of the call's nev loads
+// evicted (keep.ev_e[0 .. nev), written by this block before the call), ascending id.  flag: E ints of
+// shared memory; every thread of the block calls it.
+__device__ void write_kept(int* flag, int E, const ManageKeep& keep, int nev) {
+  __shared__ int ktmp[33];
+  const int tid = threadIdx.x;
+  for (int e = tid; e < E; e += blockDim.x) flag[e] = 0;
+  __syncthreads();
+  const int n0 = keep.n_in0 ? *keep.n_in0 : 0, n1 = keep.n_in1 ? *keep.n_in1 : 0;
+  for (int i = tid; i < n0; i += blockDim.x) {
+    const int e = keep.in0[i];
+    if (e >= 0 && e < E) flag[e] = 1;
+  }
+  for (int i = tid; i < n1; i += blockDim.x) {
+    const int e = keep.in1[i];
+    if (e >= 0 && e < E) flag[e] = 1;
+  }
+  __syncthreads();
+  for (int r = tid; r < nev; r += blockDim.x) {
+    const int e = keep.ev_e[r];
+    if (e >= 0 && e < E) flag[e] = 0;
+  }
+  __syncthreads();
+  int carry = 0;
+  for (int e0 = 0; e0 < E; e0 += blockDim.x) {
+    const int e = e0 + tid;
+    const int f = e < E ? flag[e] : 0;
+    int tot;
+    const int x = block_exclusive_scan(f, ktmp, &tot);
+    if (f) keep.kept_e[carry + x] = e;
+    carry += tot;
+  }
+  if (tid == 0) *keep.n_kept = carry;
+}
+
 // Shared memory (dynamic): need[E] | e2s[E] | mrank[E] | hrank[E] | s2e[S] | prio[S] | cand[S] | vict[S]
 //
 // ids[0 .. n) are the call's routing ids.  With n_dev the call reads
@@ -32,22 +67,9 @@ __global__ void __launch_bounds__(kManageThreads) manage_kernel(
     uint32_t* __restrict__ stamp_g, int32_t* __restrict__ miss_e, int32_t* __restrict__ miss_s,
     int32_t* __restrict__ n_miss, int32_t* __restrict__ hit_e, int32_t* __restrict__ n_hit,
     int32_t* __restrict__ sid, int32_t* __restrict__ def_e, int32_t* __restrict__ n_def,
-    int32_t* __restrict__ sub_n, int sub_b, int n_sub, int64_t* __restrict__ stats, int32_t* __restrict__ status) {
+    int32_t* __restrict__ sub_n, int sub_b, int n_sub, const ManageKeep keep, int64_t* __restrict__ stats,
+    int32_t* __restrict__ status) {
   extern __shared__ int man_smem[];
-  if (n_dev) {
-    n = min(max(*n_dev - n_off, 0), n);
-    ids += n_off;
-    if (n == 0) {
-      if (threadIdx.x == 0) {
-        *n_miss = 0;
-        if (n_hit) *n_hit = 0;
-        if (n_def) *n_def = 0;
-        if (sub_n)
-          for (int b = 0; b < n_sub; ++b) sub_n[b] = 0;
-      }
-      return;
-    }
-  }
   int* need = man_smem;
   int* e2s = need + E;
   int* mrank = e2s + E;
@@ -59,6 +81,21 @@ __global__ void __launch_bounds__(kManageThreads) manage_kernel(
   __shared__ int tmp[33];
   __shared__ int s_nmiss, s_nhit;
   const int tid = threadIdx.x;
+  if (n_dev) {
+    n = min(max(*n_dev - n_off, 0), n);
+    ids += n_off;
+    if (n == 0) {
+      if (tid == 0) {
+        *n_miss = 0;
+        if (n_hit) *n_hit = 0;
+        if (n_def) *n_def = 0;
+        if (sub_n)
+          for (int b = 0; b < n_sub; ++b) sub_n[b] = 0;
+      }
+      if (keep.kept_e) write_kept(mrank, E, keep, 0);  // nothing evicted
+      return;
+    }
+  }
 
   for (int e = tid; e < E; e += kManageThreads) {
     need[e] = 0;
@@ -172,15 +209,18 @@ __global__ void __launch_bounds__(kManageThreads) manage_kernel(
     miss_s[r] = s;
     if (s < 0) {  // cannot happen when the step fits the pool (checked on the host)
       set_status(status, MOE_DEV_BAD_SLOT);
+      if (keep.ev_e) keep.ev_e[r] = -1;
       continue;
     }
     const int old = s2e[s];
     if (old >= 0 && old < E) e2s[old] = -1;
+    if (keep.ev_e) keep.ev_e[r] = old >= 0 && old < E ? old : -1;
     s2e[s] = e;
     e2s[e] = s;
     prio[s] = policy == MOE_POLICY_LRU ? stamp : 1u;
   }
   __syncthreads();
+  if (keep.kept_e) write_kept(mrank, E, keep, nl);  // mrank is free from here on
   for (int e = tid; e < E; e += kManageThreads) e2s_g[e] = e2s[e];
   for (int s = tid; s < S; s += kManageThreads) {
     s2e_g[s] = s2e[s];
@@ -357,7 +397,7 @@ int launch_manage(const int32_t* ids, int n, int E, int S, int policy, int32_t* 
   const ManageWave& w = wave ? *wave : nw;
   manage_kernel<<<1, kManageThreads, smem, stream>>>(ids, n, w.n_dev, w.n_off, E, S, policy, e2s, s2e, prio, stamp,
                                                      miss_e, miss_s, n_miss, hit_e, n_hit, sid, w.def_e, w.n_def,
-                                                     w.sub_n, w.sub_b, w.n_sub, stats, dev_status);
+                                                     w.sub_n, w.sub_b, w.n_sub, w.keep, stats, dev_status);
   MOE_LAUNCH_CHECK();
   return MOE_OK;
 }

@@ -27,6 +27,7 @@ struct FfnArgs {
   uint16_t* yb;           // tensor-core path: write y as bf16 [T*k][H] here instead of fp32 y (or NULL)
   float* skp;             // partial sums of the decode stream path (sk_part_bytes), or NULL
   size_t skp_bytes;
+  const int32_t* list_s;  // slot of each listed expert (stream paths), or NULL: the slot comes from e2s
 };
 
 // Records (start, end) event pairs around kernel launches when tracing is on.
@@ -82,6 +83,17 @@ int launch_prefill(const FfnArgs& a, int n, int max_list, cudaStream_t stream, P
 int launch_combine(const float* y, const float* w, const int32_t* pos, const int32_t* ids, const int32_t* e2s, int T,
                    int k, int H, int E, int split, void* out, float* out_res, float* out_miss, cudaStream_t stream,
                    const uint16_t* yb = nullptr);
+// What a later wave's manage call reports for scheduling the FFN around its evictions:
+//   ev_e[r]        the expert the r-th load evicted from its slot (-1: the slot was empty)
+//   kept_e/n_kept  the experts of the lists in0 (n_in0) and in1 (n_in1) that the call did not evict,
+//                  ascending: with the step's hits and first loads as the lists, the experts that
+//                  stay in place
+struct ManageKeep {
+  int32_t* ev_e = nullptr;
+  const int32_t *in0 = nullptr, *n_in0 = nullptr, *in1 = nullptr, *n_in1 = nullptr;
+  int32_t *kept_e = nullptr, *n_kept = nullptr;
+};
+
 // Expert-wave options of one manage call: wave 0 defers the misses that find no
 // victim (def_e, n_def); a later wave manages ids[n_off .. n_off + m) with
 // m = clamp(*n_dev - n_off, 0, n) read on the device (no call when m = 0).
@@ -92,6 +104,7 @@ struct ManageWave {
   int n_off = 0;
   int32_t* sub_n = nullptr;  // with sub_b: sub_n[b] = clamp(n_miss - b*sub_b, 0, sub_b) for b < n_sub
   int sub_b = 0, n_sub = 0;
+  ManageKeep keep;
 };
 int launch_manage(const int32_t* ids, int n, int E, int S, int policy, int32_t* e2s, int32_t* s2e, uint32_t* prio,
                   uint32_t* stamp, int32_t* miss_e, int32_t* miss_s, int32_t* n_miss, int32_t* hit_e,

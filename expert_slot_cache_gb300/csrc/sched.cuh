@@ -22,7 +22,7 @@ __device__ __forceinline__ int stream_len(int n_list, int NSR, int G, int jcap) 
 __device__ __forceinline__ bool stream_slot(const FfnArgs& a, int li, int& e, int& slot) {
   e = a.list_e[li];
   if (e < 0 || e >= a.E) return false;
-  slot = a.e2s ? a.e2s[e] : e;
+  slot = a.list_s ? a.list_s[li] : a.e2s ? a.e2s[e] : e;
   return slot >= 0 && slot < a.S;
 }
 
