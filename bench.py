@@ -297,13 +297,14 @@ def w8a8_variants(dev: str, peaks: dict, steps: int = 10, warmup: int = 3) -> di
         w = Workload(c, 2 * steps + warmup, dev, quant=True)
         r = time_steps(w, steps, warmup)
         units = count_unique_all(w, steps, warmup + steps)
-        t_ffn = (r["kern_ms"]["ffn_gateup"] + r["kern_ms"]["ffn_down"]) * 1e-3
+        # T <= 8 runs the persistent W8A8 decode kernel: its whole launch counts
+        t_ffn = (r["kern_ms"]["ffn_gateup"] + r["kern_ms"]["ffn_down"] + r["kern_ms"]["decode"]) * 1e-3
         ach = units * w.slab_bytes / t_ffn / 1e9 if t_ffn > 0 else 0.0
         layer_bytes = count_unique_all(w, steps, warmup) * w.slab_bytes
         out[f"resident_T{T}"] = {
             "tokens_per_s": T * steps / (r["ms"] * 1e-3), "ms_per_step": r["ms"] / steps,
             "ffn_hbm": {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                        "frac": ach / peaks["hbm_gbs"], "kernel": "w8a8 stream (ffn_q8)", "bytes_per_unit": w.slab_bytes,
+                        "frac": ach / peaks["hbm_gbs"], "kernel": "decode_q8_kernel" if T <= 8 else "w8a8 stream (ffn_q8)", "bytes_per_unit": w.slab_bytes,
                         "units": units},
             "layer_hbm_frac": layer_bytes / (r["ms"] * 1e-3) / 1e9 / peaks["hbm_gbs"]}
         del w
@@ -703,7 +704,8 @@ def targets(dev: str, peaks: dict) -> dict:
     t["gather_T64_chunks_tok_s"], t["gather_T64_chunks_misses"] = g["tok_s"], g["misses"]
     for T in (1, 8, 64):
         d = resident_decode(dev, peaks, T, quant=True)
-        t[f"q8_res_T{T}_us"], t[f"q8_res_T{T}_ffn_hbm"] = d["us"], d["ffn_hbm"]
+        t[f"q8_res_T{T}_us"], t[f"q8_res_T{T}_layer_hbm"], t[f"q8_res_T{T}_ffn_hbm"] = \
+            d["us"], d["layer_hbm"], d["ffn_hbm"]
     t["q8_gather_T64_tok_s"] = gather_line(dev, 64, C.SCHED_WAVES, quant=True)["tok_s"]
     st = stack_variant(dev, peaks, C.STACK)
     t["stack48_tok_s"], t["stack48_hbm"] = st["tokens_per_s"], st["hbm"]["frac"]

@@ -236,13 +236,20 @@ extern "C" int moe_layer_forward(const moe_layer_args* a, moe_stream_t main_s, m
   prof.p = a->prof;
   if (prof.p) prof.p->used = 0;
   const size_t slab_bytes = a->quant ? q8_slab_bytes_h(H, I) : (size_t)6 * H * I;
-  if (mode == MOE_MODE_RESIDENT && !a->quant && !a->window_counts && a->decode_kernels == 0 && H % 8 == 0 &&
-      ws.skp && decode_eligible(T, H, E, k, I, S, a->x, a->w_router, a->pool)) {
+  if (mode == MOE_MODE_RESIDENT && !a->window_counts && a->decode_kernels == 0 && H % 8 == 0 && ws.skp) {
     // a small all-resident step: the whole layer in one persistent launch
-    prof.begin(MOE_PROF_DECODE, ms);
-    const int rd = launch_decode(a, ws.route, ws.logits, ws.skp, ws.skp_bytes, ws.ctr, ms);
-    prof.end(ms);
-    return rd;
+    int dev = 0, sms = 0;
+    MOE_CUDA_TRY(cudaGetDevice(&dev));
+    MOE_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+    const bool bf = !a->quant && decode_eligible(T, H, E, k, I, S, a->x, a->w_router, a->pool);
+    const bool q8 = a->quant && decode_q8_eligible(T, H, E, k, I, S, a->x, a->w_router, a->pool, sms);
+    if (bf || q8) {
+      prof.begin(MOE_PROF_DECODE, ms);
+      const int rd = bf ? launch_decode(a, ws.route, ws.logits, ws.skp, ws.skp_bytes, ws.ctr, ms)
+                        : launch_decode_q8(a, ws.route, ws.logits, ws.skp, ws.skp_bytes, ws.ctr, ms);
+      prof.end(ms);
+      return rd;
+    }
   }
   prof.begin(MOE_PROF_ROUTE, ms);
   // a one-chunk step: the top-k CTA may group the batch by expert itself (then no permute launch)

@@ -33,10 +33,10 @@
 // The last CTA to leave puts every counter back to zero.
 #include <algorithm>
 
+#include "decode_route.cuh"
 #include "internal.cuh"
 #include "sched.cuh"
 #include "tc05.cuh"
-#include "fp32def.cuh"
 
 namespace moe {
 
@@ -54,9 +54,7 @@ constexpr int kPMaxN = 64;      // T * k
 constexpr int kPMaxE = 256;
 constexpr int kPMaxStages = 4;
 constexpr uint32_t kPTmemCols = 512;  // two accumulator buffers of up to 256 columns
-constexpr int kPSpin = 1 << 22;
 constexpr int kPSmemMax = 232448 - 12 * 1024;  // dynamic shared memory cap (static shared memory below)
-constexpr int kPStage = 8192 + 256;            // one warp's router staging: Wr [128][32] bf16 + x [128] bf16
 
 // Counters after the E per-expert gate/up counters.
 constexpr int kCtrLogits = 0, kCtrDown = 1, kCtrExit = 2, kCtrRoute = 3, kCtrCount = 4;
@@ -82,47 +80,8 @@ struct DecodeArgs {
   int32_t* ctr;  // E + kCtrCount, zero on entry and on exit
   int32_t* status;
   int stride, nst, hcap;  // ring stage stride and count; down stages the h area holds
-  int ring_bytes;         // >= nst * stride and >= the router's staging (kPWarps * kPStage)
+  int ring_bytes;         // >= nst * stride and >= the router's staging (kPWarps * kRStage)
 };
-
-__device__ __forceinline__ int ld_acquire(const int32_t* p) {
-  int v;
-  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ void add_release(int32_t* p, int v) {
-  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-// Bounded wait until *p >= target; on giving up, flags the call and returns false.
-__device__ __forceinline__ bool wait_count(const int32_t* p, int target, int32_t* status) {
-  for (int i = 0; i < kPSpin; ++i) {
-    if (ld_acquire(p) >= target) return true;
-    __nanosleep(32);
-  }
-  set_status(status, MOE_DEV_TIMEOUT);
-  return false;
-}
-__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_16(void* smem, const void* gmem) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem)), "l"(gmem) : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() {
-  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
-}
-
-// sum_{j < J} p[j * stride] in j order, from 0; the loads of up to 16 parts are in flight together.
-__device__ __forceinline__ float sum_parts(const float* p, size_t stride, int J) {
-  float s = 0.f;
-  for (int j0 = 0; j0 < J; j0 += 16) {
-    float v[16];
-#pragma unroll
-    for (int u = 0; u < 16; ++u) v[u] = j0 + u < J ? __ldcg(p + (size_t)(j0 + u) * stride) : 0.f;
-#pragma unroll
-    for (int u = 0; u < 16; ++u)
-      if (j0 + u < J) s += v[u];
-  }
-  return s;
-}
 
 // TMEM accumulator columns 0..W-1 (tokens) of every tile -> parts.
 template <int W>
@@ -209,30 +168,9 @@ __global__ void __launch_bounds__(kPThreads, 1) decode_layer_kernel(const Decode
   volatile int* abort_flag = &s_abort;
 
   // ---- 1. router logits: block parts -------------------------------------------------
-  const int nblk = H / 128, neg = (E + 31) / 32;
-  const int units = nblk * neg * T;
-  {
-    // the warp's staging area in the ring: Wr rows [128][32 experts] bf16 (8 KB), then the x row (256 B)
-    unsigned char* wst = ring + warp * kPStage;
-    const uint16_t* ws16 = reinterpret_cast<const uint16_t*>(wst);
-    for (int u = blockIdx.x * kPWarps + warp; u < units; u += G * kPWarps) {
-      const int b = u % nblk, rest = u / nblk, eg = rest % neg, t = rest / neg;
-      const int e0 = eg * 32, e = e0 + lane;
-      for (int c = lane; c < 128 * 4; c += 32) {  // 16-byte pieces: row c / 4, experts e0 + 8 (c % 4) ..
-        const int r = c >> 2, q = c & 3;
-        if (e0 + 8 * q < E) cp_async_16(wst + r * 64 + q * 16, a.wr + (size_t)(b * 128 + r) * E + e0 + 8 * q);
-      }
-      if (lane < 16) cp_async_16(wst + 8192 + lane * 16, a.x + (size_t)t * H + b * 128 + 8 * lane);
-      cp_async_wait_all();
-      __syncwarp();
-      const uint16_t* xs16 = ws16 + 4096;
-      float acc = 0.f;
-#pragma unroll 8
-      for (int r = 0; r < 128; ++r) acc = fmaf(bf16_to_f32(xs16[r]), bf16_to_f32(ws16[r * 32 + lane]), acc);
-      if (e < E) a.lpart[((size_t)b * T + t) * E + e] = acc;
-      __syncwarp();
-    }
-  }
+  RouteIO rio{a.x, a.wr, a.off, a.bias, a.e2s, a.affinity, a.rflags, T, H, E, k,
+              a.lpart, a.logits, a.ids, a.w, &a.ctr[E + kCtrRoute], a.status};
+  route_logit_parts<kPThreads>(rio, ring);
   fence_async_smem();  // the ring's staging bytes are overwritten by tensor-map copies later
   __syncthreads();
   if (tid == 0) {  // the barrier orders the CTA's stores before this (cumulative) release
@@ -241,119 +179,11 @@ __global__ void __launch_bounds__(kPThreads, 1) decode_layer_kernel(const Decode
   }
   __syncthreads();
 
-  // ---- 2. logits, top-k and weights ------------------------------------------------------
-  // A few tokens: every CTA routes all of them.  More: CTA t routes token t and publishes its ids and
-  // weights, and every CTA reads them back after one more grid-wide wait.
-  const bool spread = T >= 3;
-  const int t_lo = spread ? blockIdx.x : 0, t_hi = spread ? min((int)blockIdx.x + 1, T) : T;
-  if (t_lo < t_hi) {
-    for (int v = t_lo * E + tid; v < t_hi * E; v += kPThreads) {
-      const int e = v % E;
-      float l = sum_parts(a.lpart + v, (size_t)T * E, nblk);  // part b of (t, e) at [b][t][e]
-      if (a.off) l = l + a.off[e];
-      slog[v] = l;
-      // selection score: as the router's top-k (sigmoid router, bias, live-cache affinity)
-      const float base = (a.rflags & MOE_ROUTE_SIGMOID) ? sigmoid32_def(l) : l;
-      float sc = a.bias ? __fadd_rn(base, a.bias[e]) : base;
-      if (a.e2s && a.affinity != 0.f && a.e2s[e] >= 0) sc = sc + a.affinity;
-      ssc[v] = sc;
-    }
-    __syncthreads();
-    if (spread || blockIdx.x == 0)
-      for (int v = t_lo * E + tid; v < t_hi * E; v += kPThreads) a.logits[v] = slog[v];
-    // top-k by rank: expert e of token t is the r-th pick, r = the number of experts ranked before it
-    // (higher score, or an equal score and a lower id); ranks below k are the picks, in order
-    for (int v = t_lo * E + tid; v < t_hi * E; v += kPThreads) {
-      const int t = v / E, e = v - t * E;
-      const float4* row4 = reinterpret_cast<const float4*>(ssc + t * E);  // E % 8 == 0
-      const float se = ssc[v];
-      int r = 0;
-#pragma unroll 4
-      for (int f4 = 0; f4 < E / 4; ++f4) {
-        const float4 q = row4[f4];
-        const int f = 4 * f4;
-        r += (q.x > se) || (q.x == se && f < e);
-        r += (q.y > se) || (q.y == se && f + 1 < e);
-        r += (q.z > se) || (q.z == se && f + 2 < e);
-        r += (q.w > se) || (q.w == se && f + 3 < e);
-      }
-      if (r < k) s_ids[t * k + r] = e;
-    }
-    __syncthreads();
-    // the weights of token t over its k picks (the router's softmax, or its sigmoids normalised): one
-    // warp per token, lane j for pick j; the sums run as a fixed butterfly
-    for (int t = t_lo + warp; t < t_hi; t += kPWarps) {
-      float zj = 0.f;
-      if (lane < k) {
-        const int e = s_ids[t * k + lane];
-        zj = slog[t * E + e];
-        if (a.rflags & MOE_ROUTE_SIGMOID) zj = sigmoid32_def(zj);
-        else if ((a.rflags & MOE_ROUTE_DAMPED) && a.bias) zj = zj + a.bias[e];
-      }
-      float mx = lane < k ? zj : -INFINITY;
-#pragma unroll
-      for (int d = 16; d; d >>= 1) mx = fmaxf(mx, __shfl_xor_sync(MOE_FULL_MASK, mx, d));
-      const bool sig = (a.rflags & MOE_ROUTE_SIGMOID) != 0;
-      const float num = lane < k ? (sig ? zj : expf(zj - mx)) : 0.f;
-      float sum = num;
-#pragma unroll
-      for (int d = 16; d; d >>= 1) sum += __shfl_xor_sync(MOE_FULL_MASK, sum, d);
-      if (lane < k) s_w[t * k + lane] = num / sum;
-    }
-    __syncthreads();
-    if (spread || blockIdx.x == 0)
-      for (int i = t_lo * k + tid; i < t_hi * k; i += kPThreads) {
-        a.ids[i] = s_ids[i];
-        a.w[i] = s_w[i];
-      }
-  }
-  if (spread) {
-    __syncthreads();
-    if (tid == 0) {
-      if (t_lo < t_hi) add_release(&a.ctr[E + kCtrRoute], 1);
-      if (!wait_count(&a.ctr[E + kCtrRoute], T, a.status)) s_abort = 1;
-    }
-    __syncthreads();
-    for (int i = tid; i < n; i += kPThreads) {
-      s_ids[i] = __ldcg(a.ids + i);
-      s_w[i] = __ldcg(a.w + i);
-    }
-    __syncthreads();
-  }
+  // ---- 2. logits, top-k, weights and the grouping by expert -------------------------------
   {
-    int carry = 0, carry_act = 0;
-    for (int e0 = 0; e0 < E; e0 += kPThreads) {
-      const int e = e0 + tid;
-      int c = 0;
-      if (e < E)
-        for (int i = 0; i < n; ++i) c += s_ids[i] == e;
-      int tp;  // count in the low 16 bits, active flag in the high 16 (n <= 64, E <= 256: no carry)
-      const int xp = block_exclusive_scan(c | ((c > 0 ? 1 : 0) << 16), tmp, &tp);
-      const int ex = xp & 0xffff, exa = xp >> 16, tot = tp & 0xffff, tota = tp >> 16;
-      if (e < E) {
-        s_cnt[e] = c;
-        s_off[e] = carry + ex;
-        s_li[e] = c > 0 ? carry_act + exa : -1;
-        if (c > 0) s_act[carry_act + exa] = e;
-      }
-      carry += tot;
-      carry_act += tota;
-    }
-    if (tid == 0) {
-      s_off[E] = carry;
-      s_nact = carry_act;
-    }
+    const RouteSm rsm{slog, ssc, s_ids, s_w, s_cnt, s_off, s_act, s_li, s_rows, s_pos, tmp, &s_nact, abort_flag};
+    route_pick_group<kPThreads>(rio, rsm);
   }
-  __syncthreads();
-  if (tid < n) {
-    const int e = s_ids[tid];
-    int r = 0;
-    for (int i = 0; i < tid; ++i) r += s_ids[i] == e;
-    const int p = s_off[e] + r;
-    s_rows[p] = tid;
-    s_pos[tid] = p;
-  }
-  __syncthreads();
 
   // ---- 3-5. the two weight streams -----------------------------------------------------
   FfnArgs fa{};
@@ -717,7 +547,7 @@ bool decode_eligible(int T, int H, int E, int k, int I, int S, const void* x, co
   return dec_stride(H, I) * 2 + 1024 + 16 * 1024 <= kPSmemMax;
 }
 
-size_t decode_ctr_ints(int E) { return (size_t)E + kCtrCount; }
+size_t decode_ctr_ints(int E) { return (size_t)E + kCtrCount; }  // the W8A8 kernel keeps the same count
 
 int launch_decode(const moe_layer_args* la, float* lpart, float* logits, float* skp, size_t skp_bytes, int32_t* ctr,
                   cudaStream_t stream) {
@@ -756,7 +586,7 @@ int launch_decode(const moe_layer_args* la, float* lpart, float* logits, float* 
   const size_t fixed = 1024 + hbytes + 8 * (2 * kPMaxStages + 5 + a.hcap);
   a.nst = (int)std::min<size_t>(kPMaxStages, (kPSmemMax - fixed) / a.stride);
   if (a.nst < 2) return MOE_ERR_ARG;
-  a.ring_bytes = std::max(a.nst * a.stride, (kPWarps * kPStage + 1023) & ~1023);
+  a.ring_bytes = std::max(a.nst * a.stride, (kPWarps * kRStage + 1023) & ~1023);
   const size_t smem = fixed + (size_t)a.ring_bytes;
   if (smem > (size_t)kPSmemMax) return MOE_ERR_ARG;
   static bool attr[64] = {};

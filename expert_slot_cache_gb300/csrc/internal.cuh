@@ -120,6 +120,13 @@ bool decode_eligible(int T, int H, int E, int k, int I, int S, const void* x, co
 size_t decode_ctr_ints(int E);
 int launch_decode(const moe_layer_args* la, float* lpart, float* logits, float* skp, size_t skp_bytes, int32_t* ctr,
                   cudaStream_t stream);
+// Its W8A8 counterpart (decode_q8.cu): CUDA-core weight streams; the step's integer sums meet in
+// accumulators of T*k*(2I + H) int32 (+ T*k row scales) at the start of `ws`.
+bool decode_q8_eligible(int T, int H, int E, int k, int I, int S, const void* x, const void* wr, const void* pool,
+                        int sms);
+size_t decode_q8_ws_bytes(int T, int k, int H, int I);
+int launch_decode_q8(const moe_layer_args* la, float* lpart, float* logits, void* ws, size_t ws_bytes, int32_t* ctr,
+                     cudaStream_t stream);
 int route_impl(const void* x, const void* w_router, const float* logit_offset, const float* sel_bias,
                const int32_t* e2s, float affinity, int rflags, int T, int H, int E, int k, float* logits,
                float* scratch, int32_t* ids, float* w, cudaStream_t stream, const PermOut* perm, bool* fused);

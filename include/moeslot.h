@@ -329,7 +329,7 @@ enum {
   MOE_PROF_FFN_DOWN = 5,
   MOE_PROF_COMBINE = 6,
   MOE_PROF_FFN_ROWS = 7, /* grouped copy of the routed rows of x (tensor-core path) */
-  MOE_PROF_DECODE = 8,   /* the persistent decode kernel: the whole layer in one launch */
+  MOE_PROF_DECODE = 8,   /* a persistent decode kernel (bf16 or W8A8): the whole layer in one launch */
   MOE_PROF_CLASSES = 9
 };
 typedef struct moe_prof {
@@ -474,10 +474,17 @@ typedef struct moe_layer_args {
  * decode_kernels == 0) run as one persistent cooperative launch, one CTA per
  * SM: router logits, a grid-wide wait, the top-k and grouping in every CTA,
  * the gate/up weight stream, the down weight stream (its weights loaded while
- * h is formed from the gate/up sums) and the combine.  Its grid-wide waits
- * are bounded: a wait that gives up sets MOE_DEV_TIMEOUT.  It keeps arrival
- * counters at the start of the workspace, which must therefore be
- * zero-filled once before the first call on it (each call leaves them zero).
+ * h is formed from the gate/up sums) and the combine.  W8A8 steps (quant = 1,
+ * RESIDENT, T <= 8, T*k <= 64, E <= 256, H % 128 == 0 and H <= 2048,
+ * I % 16 == 0 and I <= 1024, no window counts, decode_kernels == 0) have
+ * their own persistent launch: router, the tokens' 8-bit codes, the gate/up
+ * and down weight streams folded with dp4a (their exact int32 sums meet in
+ * accumulators by integer atomics), h quantised per row, and the combine;
+ * its output is bit for bit that of the separate W8A8 kernels.  The
+ * grid-wide waits of both are bounded: a wait that gives up sets
+ * MOE_DEV_TIMEOUT.  They keep arrival counters at the start of the
+ * workspace, which must therefore be zero-filled once before the first call
+ * on it (each call leaves them zero).
  * `side` may be NULL or equal to `main` (then everything runs on `main`).
  * The sequence of launches depends only on the shapes, so it can be
  * captured into a CUDA graph.

@@ -51,6 +51,22 @@ def test_decode_separate_kernels_agree():
     _run_layer(C.qwen(4, S=128, mode=C.MODE_RESIDENT), steps=2, decode_kernels=1)
 
 
+@pytest.mark.parametrize("T", [1, 8])
+def test_decode_routing_equals_router_kernels_bitwise(T):
+    # the persistent kernel's ids and weights are those of the router kernels, bit for bit
+    cfg = C.qwen(T, S=128, mode=C.MODE_RESIDENT)
+    st = stage_layer(cfg)
+    import expert_slot_cache_gb300 as M
+    lay = [M.SlotCachedMoELayer(st["wr"], st["slabs_dev"], cfg.k, cfg.I, C.MODE_RESIDENT, max_tokens=T,
+                                decode_kernels=dk) for dk in (0, 1)]
+    for step in range(3):
+        x = C.draw_x(cfg, DEV, step=step)
+        r1, r2 = lay[0].forward(x), lay[1].forward(x)
+        torch.cuda.synchronize()
+        assert torch.equal(r1["ids"], r2["ids"]) and torch.equal(r1["w"], r2["w"]), step
+        assert_out_close(_np(r1["out"].float()), _np(r2["out"].float()).astype(np.float64), f"step {step}")
+
+
 def _layer(cfg, st):
     import expert_slot_cache_gb300 as M
     return M.SlotCachedMoELayer(st["wr"], st["slabs_dev"], cfg.k, cfg.I, C.MODE_RESIDENT,
