@@ -743,7 +743,8 @@ def main():
     ap.add_argument("--no-variants", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="main",
-                    help="main (default) | prefill | resident_T<n> | gather_T<n> | chunks_T<n> | routing_variants | "
+                    help="main (default) | prefill | resident_T<n> | gather_T<n> | chunks_T<n> (each also as q8_<name>: "
+                         "W8A8 experts) | routing_variants | "
                          "policy_replay | w8a8 | stack | stack_slots | stack_slots_chunks | stack_budget: one workload alone "
                          "(for profiling); prints its own JSON line")
     args = ap.parse_args()
@@ -780,6 +781,9 @@ def main():
         return
     if args.workload != "main":
         w = args.workload
+        quant = w.startswith("q8_")  # the same workload with W8A8 experts
+        if quant:
+            w = w[3:]
         if w == "prefill":
             c = C.PREFILL
         elif w.startswith("resident_T"):
@@ -790,10 +794,10 @@ def main():
             c = C.qwen(int(w[len("chunks_T"):]), S=64)
         else:
             raise SystemExit(f"unknown workload {w}")
-        wl = Workload(c, 2 * args.steps + args.warmup, dev)
+        wl = Workload(c, 2 * args.steps + args.warmup, dev, quant=quant)
         r = time_steps(wl, args.steps, args.warmup, clocks=Clocks(local))
         if rank == 0:
-            print(json.dumps({"workload": w, "clocks": r["clocks"], "ms_per_step": r["ms"] / args.steps,
+            print(json.dumps({"workload": args.workload, "clocks": r["clocks"], "ms_per_step": r["ms"] / args.steps,
                               "ms_per_step_instrumented": r["ms_instrumented"] / args.steps,
                               "tokens_per_s": c.T * args.steps / (r["ms"] * 1e-3),
                               "misses_per_step": r["misses"] / args.steps,
