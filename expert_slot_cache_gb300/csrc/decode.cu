@@ -13,22 +13,25 @@
 //
 // Phases (grid-wide waits are bounded spins on counters in the workspace; a
 // cooperative launch keeps every CTA resident, so a CTA can wait on another):
-//  1. router logits: units (128-row block b, 32 experts, token t) over all
-//     warps; part_b = fma chain from 0 over the block's rows in order, the
-//     same fp32 order as the router kernels; then a grid-wide arrival.
-//  2. every CTA adds the parts in block order (+ the offset), runs the
-//     per-warp top-k and groups the step's routings by expert in shared
+//  1. router logits (decode_route.cuh): units (128-row block b, 32 experts,
+//     token t) over all warps; part_b = fma chain from 0 over the block's
+//     rows in order, the same fp32 order as the router kernels; every CTA also
+//     zeroes its share of the step's accumulators; a grid-wide arrival.
+//  2. every CTA adds the parts in block order (+ the offset), ranks the
+//     scores (top-k) and groups the step's routings by expert in shared
 //     memory; CTA 0 writes logits, ids and weights.
 //  3. gate/up stream: the listed experts' [Wg | Wu] cut into stages of 16
 //     rows, dealt as equal contiguous ranges to the CTAs (the decode stream
-//     schedule); parts [j][p][2I] to global memory; after each part a release
+//     schedule); each part's sums are added to the rows' accumulators
+//     gsum[p][2I] in 64-bit fixed point by integer atomics (so the sum does
+//     not depend on the order the parts arrive in); after each part a release
 //     on the expert's counter.
 //  4. the loader goes straight on to the CTA's down stages (weights only), so
-//     the DRAM stream continues while the epilogue warps wait for the gate/up
-//     parts of those experts and build h = silu(sum g) * (sum u) in bf16 in
+//     the DRAM stream continues while the epilogue warps wait for every
+//     gate/up part of those experts and build h = silu(g) * u in bf16 in
 //     shared memory, laid out as the MMA's B operand.
-//  5. down MMAs, parts [j][p][H]; a grid-wide arrival; then every CTA reduces
-//     and combines a share of the output: out[t] = sum_j w[t][j] y[pos(t, j)]
+//  5. down MMAs into ysum[p][H] the same way; a grid-wide arrival; then every
+//     CTA combines a share of the output: out[t] = sum_j w[t][j] y[pos(t, j)]
 //     in fp32, j ascending, rounded to bf16.
 // The last CTA to leave puts every counter back to zero.
 #include <algorithm>
@@ -74,18 +77,24 @@ struct DecodeArgs {
   int32_t* ids;
   float* w;
   uint16_t* out;  // bf16 [T][H]
-  float* gpart;   // fp32 [jg][n][2I]
-  float* ypart;   // fp32 [jd][n][H]
-  int jg, jd;
+  unsigned long long* gsum;  // [n][2I]: the rows' gate | up sums, 64-bit fixed point (2^-32), zeroed per step
+  unsigned long long* ysum;  // [n][H]: the rows' down sums, the same
   int32_t* ctr;  // E + kCtrCount, zero on entry and on exit
   int32_t* status;
   int stride, nst, hcap;  // ring stage stride and count; down stages the h area holds
   int ring_bytes;         // >= nst * stride and >= the router's staging (kPWarps * kRStage)
 };
 
-// TMEM accumulator columns 0..W-1 (tokens) of every tile -> parts.
+// The partial sums of a step's rows meet in 64-bit fixed point with 32 fraction bits: a part v adds
+// rint(v * 2^32) by an integer atomic, so the sum does not depend on the order in which parts arrive
+// (and is exact for every part of magnitude 2^-8 or more, whose fp32 ulp is at least 2^-32).
+constexpr float kFxScale = 4294967296.f, kFxInv = 1.f / 4294967296.f;
+__device__ __forceinline__ unsigned long long to_fx(float v) { return (unsigned long long)__float2ll_rn(v * kFxScale); }
+__device__ __forceinline__ float from_fx(unsigned long long s) { return __ll2float_rn((long long)s) * kFxInv; }
+
+// TMEM accumulator columns 0..W-1 (tokens) of every tile -> the rows' fixed-point sums.
 template <int W>
-__device__ __forceinline__ void dec_epilogue(uint32_t taddr, float* base, int ntiles, int N, int nb) {
+__device__ __forceinline__ void dec_epilogue(uint32_t taddr, unsigned long long* base, int ntiles, int N, int nb) {
   constexpr int G = W >= 32 ? 1 : 32 / W;
   for (int m0 = 0; m0 < ntiles; m0 += G) {
     float v[G][W];
@@ -98,11 +107,11 @@ __device__ __forceinline__ void dec_epilogue(uint32_t taddr, float* base, int nt
       if (m0 + gi < ntiles)
 #pragma unroll
         for (int t = 0; t < W; ++t)
-          if (t < nb) base[(size_t)t * N + (m0 + gi) * kPM] = v[gi][t];
+          if (t < nb) atomicAdd(base + (size_t)t * N + (m0 + gi) * kPM, to_fx(v[gi][t]));
   }
 }
 
-__device__ __forceinline__ void drain_tile(uint32_t taddr, float* base, int ntiles, int N, int nb) {
+__device__ __forceinline__ void drain_tile(uint32_t taddr, unsigned long long* base, int ntiles, int N, int nb) {
   if (nb <= 1)
     dec_epilogue<1>(taddr, base, ntiles, N, nb);
   else if (nb <= 2)
@@ -134,7 +143,6 @@ __global__ void __launch_bounds__(kPThreads, 1) decode_layer_kernel(const Decode
   __shared__ float s_w[kPMaxN];
   __shared__ int s_cnt[kPMaxE], s_off[kPMaxE + 1], s_act[kPMaxE], s_li[kPMaxE];
   __shared__ int tmp[33];
-  __shared__ float4 s_y[2][kPThreads];
   __shared__ int s_nact, s_abort;
   __shared__ uint32_t s_tmem;
 
@@ -171,6 +179,14 @@ __global__ void __launch_bounds__(kPThreads, 1) decode_layer_kernel(const Decode
   RouteIO rio{a.x, a.wr, a.off, a.bias, a.e2s, a.affinity, a.rflags, T, H, E, k,
               a.lpart, a.logits, a.ids, a.w, &a.ctr[E + kCtrRoute], a.status};
   route_logit_parts<kPThreads>(rio, ring);
+  {
+    // this CTA's share of the step's fixed-point accumulators (gsum and ysum are contiguous); the
+    // barrier below orders the stores before the release
+    const size_t z = (size_t)n * (2 * I + H) / 2;  // 16-byte pieces
+    ulonglong2* zp = reinterpret_cast<ulonglong2*>(a.gsum);
+    for (size_t i = blockIdx.x * z / G + tid; i < (blockIdx.x + 1) * z / G; i += kPThreads)
+      zp[i] = make_ulonglong2(0ull, 0ull);
+  }
   fence_async_smem();  // the ring's staging bytes are overwritten by tensor-map copies later
   __syncthreads();
   if (tid == 0) {  // the barrier orders the CTA's stores before this (cumulative) release
@@ -195,7 +211,8 @@ __global__ void __launch_bounds__(kPThreads, 1) decode_layer_kernel(const Decode
   const int n_list = s_nact;
   const int NSRg = H / kPK, NSRd = I / kPK;
   const int Ng = 2 * I;
-  const int Lg = stream_len(n_list, NSRg, G, a.jg), Ld = stream_len(n_list, NSRd, G, a.jd);
+  constexpr int kNoCap = 1 << 30;  // the sums meet in the fixed-point accumulators: no cap on an expert's parts
+  const int Lg = stream_len(n_list, NSRg, G, kNoCap), Ld = stream_len(n_list, NSRd, G, kNoCap);
   const int bg = blockIdx.x * Lg, eg_end = min(bg + Lg, n_list * NSRg);
   const int bd = blockIdx.x * Ld, ed_end = min(bd + Ld, n_list * NSRd);
   const int wbytes_g = 2 * I * kPK * 2, wbytes_d = H * kPK * 2;
@@ -320,7 +337,7 @@ __global__ void __launch_bounds__(kPThreads, 1) decode_layer_kernel(const Decode
       tc_fence_after();
       if (!*abort_flag) {
         const int N = down ? H : Ng;
-        float* base = (down ? a.ypart : a.gpart) + ((size_t)g.j * n + g.p0) * N + q * 32 + lane;
+        unsigned long long* base = (down ? a.ysum : a.gsum) + (size_t)g.p0 * N + q * 32 + lane;
         drain_tile(tmem + ((uint32_t)(q * 32) << 16) + buf * 256u, base, N / kPM, N, g.nb);
       }
       tc_fence_before();
@@ -331,14 +348,14 @@ __global__ void __launch_bounds__(kPThreads, 1) decode_layer_kernel(const Decode
     if (bg < eg_end)
       stream_segments<kPN>(fa, NSRg, Lg, bg, eg_end, [&](const StreamSeg& g) {
         drain(g, false);
-        // publish this part of the expert's sums (the barrier orders every epilogue thread's stores
+        // publish this part of the expert's sums (the barrier orders every epilogue thread's atomics
         // before the signalling thread's release)
         named_sync(1, 128);
         if (etid == 0) add_release(&a.ctr[s_li[g.e]], 1);
         return true;
       });
     if (bd < ed_end) {
-      // h for this CTA's down stages, from every part of the experts' gate/up sums.  Every epilogue
+      // h for this CTA's down stages, from the experts' gate/up sums once every part is in.  Every epilogue
       // warp walks the same segments and reaches every named barrier; only the stores depend on
       // h_ok, which is the same for the whole CTA and never changes.
       const bool h_ok = Ld <= a.hcap;
@@ -354,7 +371,6 @@ __global__ void __launch_bounds__(kPThreads, 1) decode_layer_kernel(const Decode
         const int nst_seg = g.s_hi - g.s_lo;
         const int per_st = kPK * g.nb;
         const int nel = nst_seg * per_st;
-        const size_t pstride = (size_t)n * Ng;
         int done_st = 0;
         auto release = [&](int st_hi) {  // uniform over the epilogue warps
           const int npad = (st_hi - done_st) * kPK * (kPN - g.nb);
@@ -377,59 +393,26 @@ __global__ void __launch_bounds__(kPThreads, 1) decode_layer_kernel(const Decode
           *reinterpret_cast<uint16_t*>(hsm + (size_t)(lbase + g.s_lo + st) * kPHStage + (r >> 3) * kPAct +
                                        t * 16 + (r & 7) * 2) = f32_to_bf16(hv);
         };
-        auto src_of = [&](int v) {
-          const int el = v >> 1, st = el / per_st, rem = el - st * per_st, t = rem / kPK, r = rem - t * kPK;
-          return a.gpart + (size_t)(g.p0 + t) * Ng + (g.s_lo + st) * kPK + r + ((v & 1) ? I : 0);
-        };
-        if (2 * nel <= 128) {
-          // one item per thread, its parts 32 at a time
-          const int v = etid;
-          const bool okv = (v >> 1) < nel;
-          const float* src = okv ? src_of(v) : a.gpart;
-          float acc = 0.f;
-          for (int j0 = 0; j0 < Jg; j0 += 32) {
-            float pv[32];
+        // elements (stage, row, token), four per thread a round, their gate and up sums loaded together
+        for (int v0 = 0; v0 < nel; v0 += 4 * 128) {  // the same trip count in every epilogue thread
+          unsigned long long gs[4], us[4];
 #pragma unroll
-            for (int u = 0; u < 32; ++u) pv[u] = (okv && j0 + u < Jg) ? __ldcg(src + (size_t)(j0 + u) * pstride) : 0.f;
-#pragma unroll
-            for (int u = 0; u < 32; ++u)
-              if (j0 + u < Jg) acc += pv[u];
+          for (int q4 = 0; q4 < 4; ++q4) {
+            const int el = v0 + q4 * 128 + etid;
+            gs[q4] = us[q4] = 0ull;
+            if (el < nel) {
+              const int st = el / per_st, rem = el - st * per_st, t = rem / kPK, r = rem - t * kPK;
+              const unsigned long long* src = a.gsum + (size_t)(g.p0 + t) * Ng + (g.s_lo + st) * kPK + r;
+              gs[q4] = __ldcg(src);
+              us[q4] = __ldcg(src + I);
+            }
           }
-          const float other = __shfl_xor_sync(MOE_FULL_MASK, acc, 1);
-          if (okv && !(v & 1) && h_ok) store_h(v >> 1, acc, other);
-        } else {
-          // four items per thread with 8 parts each in flight
-          for (int v0 = 0; v0 < 2 * nel; v0 += 4 * 128) {  // the same trip count in every epilogue thread
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
-            const float* src[4];
-            bool ok[4];
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-              const int v = v0 + q4 * 128 + etid;
-              ok[q4] = (v >> 1) < nel;
-              src[q4] = ok[q4] ? src_of(v) : a.gpart;
-            }
-            for (int j0 = 0; j0 < Jg; j0 += 8) {
-              float pv[4][8];
-#pragma unroll
-              for (int q4 = 0; q4 < 4; ++q4)
-#pragma unroll
-                for (int u = 0; u < 8; ++u)
-                  pv[q4][u] = (ok[q4] && j0 + u < Jg) ? __ldcg(src[q4] + (size_t)(j0 + u) * pstride) : 0.f;
-#pragma unroll
-              for (int q4 = 0; q4 < 4; ++q4)
-#pragma unroll
-                for (int u = 0; u < 8; ++u)
-                  if (j0 + u < Jg) acc[q4] += pv[q4][u];
-            }
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-              const float other = __shfl_xor_sync(MOE_FULL_MASK, acc[q4], 1);
-              const int v = v0 + q4 * 128 + etid;
-              if (ok[q4] && !(v & 1) && h_ok) store_h(v >> 1, acc[q4], other);
-            }
-            release(min(nel, (v0 + 4 * 128) >> 1) / per_st);
+          for (int q4 = 0; q4 < 4; ++q4) {
+            const int el = v0 + q4 * 128 + etid;
+            if (el < nel && h_ok) store_h(el, from_fx(gs[q4]), from_fx(us[q4]));
           }
+          release(min(nel, v0 + 4 * 128) / per_st);
         }
         if (done_st < nst_seg) release(nst_seg);
         return true;
@@ -454,75 +437,36 @@ __global__ void __launch_bounds__(kPThreads, 1) decode_layer_kernel(const Decode
   }
   __syncthreads();
 
-  // ---- combine: out[t] = sum_j w[t][j] * (sum of y's parts), j ascending ---------------
+  // ---- combine: out[t] = sum_j w[t][j] * y[pos(t, j)], j ascending -------------------------
   {
-    // item = (token, cpi x cpt 16-byte column groups); thread = (pick jj, column group cc, part group
-    // pg) for each of its cpt column groups: part group pg adds parts pg, pg + npg, ... in order, the
-    // npg sums are added in pg order.  cpt = 2 when one group per thread would leave a CTA two items.
-    const int nc4 = H / 4;
-    const int cpi = max(1, min(kPThreads / k, (T * nc4 + G - 1) / G));
-    const int cpt = (cpi == kPThreads / k && (T * nc4 + G * cpi - 1) / (G * cpi) > 1) ? 2 : 1;
-    const int npg = max(1, kPThreads / (k * cpi));
-    const int pg = tid % npg, rest = tid / npg, cc = rest % cpi, jj = rest / cpi;
-    const int chunks = (nc4 + cpi * cpt - 1) / (cpi * cpt);
-    for (int item = blockIdx.x; item < T * chunks; item += G) {
-      const int t = item / chunks, cbase = (item - t * chunks) * cpt * cpi + cc;
-      if (jj < k) {
-        const int i = t * k + jj, p = s_pos[i];
-        const int Jd = stream_parts(s_li[s_ids[i]], NSRd, Ld);
-        const size_t stride4 = (size_t)n * H / 4;
-        float4 y[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
-        for (int j0 = pg; j0 < Jd; j0 += 4 * npg) {
-          float4 v[2][4];
-#pragma unroll
-          for (int sb = 0; sb < 2; ++sb) {
-            const int c4 = cbase + sb * cpi;
-            const float4* src = reinterpret_cast<const float4*>(a.ypart + (size_t)p * H) + c4;
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-              if (sb < cpt && c4 < nc4 && j0 + u * npg < Jd) v[sb][u] = __ldcg(src + (size_t)(j0 + u * npg) * stride4);
-          }
-#pragma unroll
-          for (int sb = 0; sb < 2; ++sb)
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-              if (sb < cpt && cbase + sb * cpi < nc4 && j0 + u * npg < Jd) {
-                y[sb].x += v[sb][u].x;
-                y[sb].y += v[sb][u].y;
-                y[sb].z += v[sb][u].z;
-                y[sb].w += v[sb][u].w;
-              }
-        }
-        s_y[0][tid] = y[0];
-        s_y[1][tid] = y[1];
+    // (token, column quad) items dealt round-robin over the grid; one thread per (item, pick) converts
+    // its y, the thread of pick 0 adds the picks in order
+    const int nc4 = H / 4, nit = T * nc4;
+    const int my_items = nit > (int)blockIdx.x ? (nit - 1 - (int)blockIdx.x) / G + 1 : 0;
+    float4* sy = reinterpret_cast<float4*>(ring);  // every stage has been read: the ring is free
+    for (int u = tid; u < my_items * k; u += kPThreads) {
+      const int m = u / k, j = u - m * k, item = (int)blockIdx.x + G * m;
+      const int t = item / nc4, c4 = item - t * nc4, p = s_pos[t * k + j];
+      const ulonglong2* src = reinterpret_cast<const ulonglong2*>(a.ysum + (size_t)p * H + 4 * c4);
+      const ulonglong2 y01 = __ldcg(src), y23 = __ldcg(src + 1);
+      sy[u] = make_float4(from_fx(y01.x), from_fx(y01.y), from_fx(y23.x), from_fx(y23.y));
+    }
+    __syncthreads();
+    for (int m = tid; m < my_items; m += kPThreads) {
+      const int item = (int)blockIdx.x + G * m, t = item / nc4, c4 = item - t * nc4;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int j = 0; j < k; ++j) {
+        const float wj = s_w[t * k + j];
+        const float4 yj = sy[m * k + j];
+        acc.x = fmaf(wj, yj.x, acc.x);
+        acc.y = fmaf(wj, yj.y, acc.y);
+        acc.z = fmaf(wj, yj.z, acc.z);
+        acc.w = fmaf(wj, yj.w, acc.w);
       }
-      __syncthreads();
-      if (jj == 0 && pg == 0)
-        for (int sb = 0; sb < cpt; ++sb) {
-          const int c4 = cbase + sb * cpi;
-          if (c4 >= nc4) continue;
-          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-          for (int j = 0; j < k; ++j) {
-            const float wj = s_w[t * k + j];
-            float4 yj = s_y[sb][(j * cpi + cc) * npg];
-            for (int q = 1; q < npg; ++q) {
-              const float4 v = s_y[sb][(j * cpi + cc) * npg + q];
-              yj.x += v.x;
-              yj.y += v.y;
-              yj.z += v.z;
-              yj.w += v.w;
-            }
-            acc.x = fmaf(wj, yj.x, acc.x);
-            acc.y = fmaf(wj, yj.y, acc.y);
-            acc.z = fmaf(wj, yj.z, acc.z);
-            acc.w = fmaf(wj, yj.w, acc.w);
-          }
-          uint2 o;
-          o.x = uint32_t(f32_to_bf16(acc.x)) | (uint32_t(f32_to_bf16(acc.y)) << 16);
-          o.y = uint32_t(f32_to_bf16(acc.z)) | (uint32_t(f32_to_bf16(acc.w)) << 16);
-          *reinterpret_cast<uint2*>(a.out + (size_t)t * H + 4 * c4) = o;
-        }
-      __syncthreads();
+      uint2 o;
+      o.x = uint32_t(f32_to_bf16(acc.x)) | (uint32_t(f32_to_bf16(acc.y)) << 16);
+      o.y = uint32_t(f32_to_bf16(acc.z)) | (uint32_t(f32_to_bf16(acc.w)) << 16);
+      *reinterpret_cast<uint2*>(a.out + (size_t)t * H + 4 * c4) = o;
     }
   }
   // the last CTA out resets the counters: every other CTA is past its last wait
@@ -575,13 +519,16 @@ int launch_decode(const moe_layer_args* la, float* lpart, float* logits, float* 
   a.ids = la->ids;
   a.w = la->w;
   a.out = (uint16_t*)la->out;
-  if (!sk_part_layout(n, H, I, skp, skp_bytes, &a.gpart, &a.ypart, &a.jg, &a.jd)) return MOE_ERR_ALIGN;
+  // the fixed-point accumulators: gsum [n][2I] then ysum [n][H]
+  if (!skp || (uintptr_t)skp % 16 || skp_bytes < (size_t)n * (2 * I + H) * 8) return MOE_ERR_ALIGN;
+  a.gsum = reinterpret_cast<unsigned long long*>(skp);
+  a.ysum = a.gsum + (size_t)n * 2 * I;
   a.ctr = ctr;
   a.status = la->dev_status;
   a.stride = dec_stride(H, I);
   // the largest down range a CTA can get (stream_len with every routed expert distinct)
   const int NSRd = I / kPK, lmax = std::min(n, E);
-  a.hcap = std::max((lmax * NSRd + sms - 1) / sms, (NSRd + a.jd - 2) / (a.jd - 1)) + 1;
+  a.hcap = (lmax * NSRd + sms - 1) / sms + 1;
   const size_t hbytes = (std::max((size_t)a.hcap * kPHStage, (size_t)T * E * 8) + 15) & ~size_t(15);
   const size_t fixed = 1024 + hbytes + 8 * (2 * kPMaxStages + 5 + a.hcap);
   a.nst = (int)std::min<size_t>(kPMaxStages, (kPSmemMax - fixed) / a.stride);
