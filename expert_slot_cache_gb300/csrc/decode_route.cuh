@@ -24,7 +24,7 @@
 namespace moe {
 
 constexpr int kRStage = 8192 + 256;  // one warp's router staging: Wr [128][32] bf16 + x [128] bf16
-constexpr int kRSpin = 1 << 22;      // polls of a grid-wide wait before it gives up
+constexpr int kRSpin = 1 << 20;      // polls of a grid-wide wait (about 1 us each) before it gives up: ~1 s
 
 __device__ __forceinline__ int ld_acquire(const int32_t* p) {
   int v;
