@@ -13,7 +13,29 @@ static size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
 // A later wave's loads go in up to kMaxSub sub-batches: the side stream gathers them back to back
 // while the main stream runs each sub-batch's FFN once its gather has landed.
-constexpr int kMaxSub = 4;
+constexpr int kMaxSub = kMaxSubBatches;
+
+// Sub-batch boundaries of a later wave's loads (at most wmax), in eighths 1 : 3 : 3 : 1.  A small first
+// sub-batch, since the FFN of the experts it evicts keeps the host link idle until it ends; a small last
+// one, since its FFN follows the last gather.  (Measured on the T = 64, 64-slot step, graph replay:
+// quarters 3.007 ms, 1 : 3 : 3 : 1 2.998 ms, 1 : 7 : 7 : 1 3.05 ms, 1 : 15 : 15 : 1 3.2 ms; gathers of
+// many experts at once ran slower per expert.)
+static SubBatches sub_batches(int wmax) {
+  SubBatches sb;
+  if (wmax < 4) {
+    sb.n = wmax > 0 ? 1 : 0;
+    sb.off[1] = wmax;
+    return sb;
+  }
+  const int edge = std::max(1, (wmax + 4) / 8), mid = edge + (wmax - 2 * edge + 1) / 2;
+  sb.n = 4;
+  sb.off[0] = 0;
+  sb.off[1] = edge;
+  sb.off[2] = mid;
+  sb.off[3] = wmax - edge;
+  sb.off[4] = wmax;
+  return sb;
+}
 
 // Workspace layout of the layer forward, for chunks of up to n = C*k routing slots.
 struct LayerWs {
@@ -313,7 +335,9 @@ extern "C" int moe_layer_forward(const moe_layer_args* a, moe_stream_t main_s, m
       if (mode == MOE_MODE_GATHER) {
         const int nw = waves ? later_waves(n, E, S) : 0;
         const int wmax = std::min(S, lmax);
-        const int sub_b = (wmax + kMaxSub - 1) / kMaxSub, n_sub = (wmax + sub_b - 1) / sub_b;
+        const SubBatches sb = sub_batches(wmax);
+        const int n_sub = sb.n;
+        auto sub_len = [&](int b) { return sb.off[b + 1] - sb.off[b]; };
         // the FFN of a device-side list (slots from e2s, or from `ls` for experts already evicted)
         auto ffn_list = [&](const int32_t* le, const int32_t* ls, const int32_t* nl, int maxl) -> int {
           FfnArgs fb = fm;
@@ -334,8 +358,7 @@ extern "C" int moe_layer_forward(const moe_layer_args* a, moe_stream_t main_s, m
           bw.n_dev = ws.n_def;
           bw.n_off = (wv - 1) * S;
           bw.sub_n = ws.sub_n;
-          bw.sub_b = sub_b;
-          bw.n_sub = n_sub;
+          bw.sub = sb;
           if (keep) bw.keep = *keep;
           prof.begin(MOE_PROF_MANAGE, ms);
           const int rm = launch_manage(ws.def_e, wmax, E, S, policy, a->e2s, a->s2e, a->prio, a->stamp, ws.wl_e,
@@ -355,13 +378,13 @@ extern "C" int moe_layer_forward(const moe_layer_args* a, moe_stream_t main_s, m
           }
           for (int b = 0; b < n_sub; ++b) {
             // the sub-batch's slots are its own (one manage call gave every load a different victim)
-            if ((rw = gather_list(ws.wl_e + b * sub_b, ws.wl_s + b * sub_b, ws.sub_n + b, sub_b)) != MOE_OK)
+            if ((rw = gather_list(ws.wl_e + sb.off[b], ws.wl_s + sb.off[b], ws.sub_n + b, sub_len(b))) != MOE_OK)
               return rw;
             if (two) {
               MOE_CUDA_TRY(cudaEventRecord(ev->join, ss));
               MOE_CUDA_TRY(cudaStreamWaitEvent(ms, ev->join, 0));
             }
-            if ((rw = ffn_list(ws.wl_e + b * sub_b, nullptr, ws.sub_n + b, sub_b)) != MOE_OK) return rw;
+            if ((rw = ffn_list(ws.wl_e + sb.off[b], nullptr, ws.sub_n + b, sub_len(b))) != MOE_OK) return rw;
           }
           return MOE_OK;
         };
@@ -372,24 +395,28 @@ extern "C" int moe_layer_forward(const moe_layer_args* a, moe_stream_t main_s, m
         // cache state, are those of the plain order.
         const bool ahead = nw >= 1 && two && (a->quant || sk_eligible(fm));
         if (ahead) {
-          const ManageKeep keep{ws.ev_e, ws.hit_e, ws.n_hit, ws.miss_e, ws.n_miss, ws.kept_e, ws.n_kept};
-          if ((r = manage_wave(1, &keep)) != MOE_OK) return r;
+          // wave 0's loads go to slots the step does not need: their gather starts beside wave 1's manage
+          // call (which decides, on the main stream, which slots wave 1 overwrites later)
           MOE_CUDA_TRY(cudaEventRecord(ev->fork, ms));
           MOE_CUDA_TRY(cudaStreamWaitEvent(ss, ev->fork, 0));
           if ((r = gather_list(ws.miss_e, ws.miss_s, ws.n_miss, lmax)) != MOE_OK) return r;
           MOE_CUDA_TRY(cudaEventRecord(ev->join, ss));
+          const ManageKeep keep{ws.ev_e, ws.hit_e, ws.n_hit, ws.miss_e, ws.n_miss, ws.kept_e, ws.n_kept};
+          if ((r = manage_wave(1, &keep)) != MOE_OK) return r;
           MOE_CUDA_TRY(cudaStreamWaitEvent(ms, ev->join, 0));  // wave 0's loads are in their slots
           for (int b = 0; b < n_sub; ++b) {
-            if ((r = ffn_list(ws.ev_e + b * sub_b, ws.wl_s + b * sub_b, ws.sub_n + b, sub_b)) != MOE_OK) return r;
+            if ((r = ffn_list(ws.ev_e + sb.off[b], ws.wl_s + sb.off[b], ws.sub_n + b, sub_len(b))) != MOE_OK)
+              return r;
             MOE_CUDA_TRY(cudaEventRecord(ev->fork, ms));
             MOE_CUDA_TRY(cudaStreamWaitEvent(ss, ev->fork, 0));
-            if ((r = gather_list(ws.wl_e + b * sub_b, ws.wl_s + b * sub_b, ws.sub_n + b, sub_b)) != MOE_OK) return r;
+            if ((r = gather_list(ws.wl_e + sb.off[b], ws.wl_s + sb.off[b], ws.sub_n + b, sub_len(b))) != MOE_OK)
+              return r;
             MOE_CUDA_TRY(cudaEventRecord(ev->sub[b], ss));
           }
           if ((r = ffn_list(ws.kept_e, nullptr, ws.n_kept, lmax)) != MOE_OK) return r;
           for (int b = 0; b < n_sub; ++b) {
             MOE_CUDA_TRY(cudaStreamWaitEvent(ms, ev->sub[b], 0));
-            if ((r = ffn_list(ws.wl_e + b * sub_b, nullptr, ws.sub_n + b, sub_b)) != MOE_OK) return r;
+            if ((r = ffn_list(ws.wl_e + sb.off[b], nullptr, ws.sub_n + b, sub_len(b))) != MOE_OK) return r;
           }
           for (int wv = 2; wv <= nw; ++wv)
             if ((r = later_wave(wv)) != MOE_OK) return r;

@@ -67,7 +67,7 @@ __global__ void __launch_bounds__(kManageThreads) manage_kernel(
     uint32_t* __restrict__ stamp_g, int32_t* __restrict__ miss_e, int32_t* __restrict__ miss_s,
     int32_t* __restrict__ n_miss, int32_t* __restrict__ hit_e, int32_t* __restrict__ n_hit,
     int32_t* __restrict__ sid, int32_t* __restrict__ def_e, int32_t* __restrict__ n_def,
-    int32_t* __restrict__ sub_n, int sub_b, int n_sub, const ManageKeep keep, int64_t* __restrict__ stats,
+    int32_t* __restrict__ sub_n, const SubBatches sub, const ManageKeep keep, int64_t* __restrict__ stats,
     int32_t* __restrict__ status) {
   extern __shared__ int man_smem[];
   int* need = man_smem;
@@ -90,7 +90,7 @@ __global__ void __launch_bounds__(kManageThreads) manage_kernel(
         if (n_hit) *n_hit = 0;
         if (n_def) *n_def = 0;
         if (sub_n)
-          for (int b = 0; b < n_sub; ++b) sub_n[b] = 0;
+          for (int b = 0; b < sub.n; ++b) sub_n[b] = 0;
       }
       if (keep.kept_e) write_kept(mrank, E, keep, 0);  // nothing evicted
       return;
@@ -238,7 +238,7 @@ __global__ void __launch_bounds__(kManageThreads) manage_kernel(
     if (n_hit) *n_hit = s_nhit;
     if (n_def) *n_def = nm - nl;
     if (sub_n)
-      for (int b = 0; b < n_sub; ++b) sub_n[b] = min(max(nl - b * sub_b, 0), sub_b);
+      for (int b = 0; b < sub.n; ++b) sub_n[b] = min(max(nl - sub.off[b], 0), sub.off[b + 1] - sub.off[b]);
     if (stats) {
       stats[0] += nl;
       stats[1] += 1;
@@ -397,7 +397,7 @@ int launch_manage(const int32_t* ids, int n, int E, int S, int policy, int32_t* 
   const ManageWave& w = wave ? *wave : nw;
   manage_kernel<<<1, kManageThreads, smem, stream>>>(ids, n, w.n_dev, w.n_off, E, S, policy, e2s, s2e, prio, stamp,
                                                      miss_e, miss_s, n_miss, hit_e, n_hit, sid, w.def_e, w.n_def,
-                                                     w.sub_n, w.sub_b, w.n_sub, w.keep, stats, dev_status);
+                                                     w.sub_n, w.sub, w.keep, stats, dev_status);
   MOE_LAUNCH_CHECK();
   return MOE_OK;
 }

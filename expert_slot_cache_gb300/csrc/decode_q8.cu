@@ -69,7 +69,6 @@ struct DecodeQ8Args {
   uint16_t* out;              // bf16 [T][H]
   int stride, nst;            // ring slot bytes and count
   int qd;                     // int32 quad-rows (4 weight rows) of Wd per down stage: qd * 4H <= stride
-  int ring_bytes;             // >= nst * stride, the router's staging, the logits and scores
 };
 
 __device__ __forceinline__ int quad_of(const int4& v, int i) { return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w; }
@@ -616,8 +615,9 @@ int launch_decode_q8(const moe_layer_args* la, float* lpart, float* logits, void
   a.nst = (int)std::min<size_t>(kQDMaxStages, (kQDSmemMax - fixed) / a.stride);
   if (a.nst < 2) return MOE_ERR_ARG;
   const size_t staging = (size_t)(kQDThreads / 32) * kRStage, route = (size_t)2 * T * E * 4;
-  a.ring_bytes = (int)std::max((size_t)a.nst * a.stride, std::max(staging, std::max(route, (size_t)16 * kQDThreads)));
-  const size_t smem = fixed + (size_t)a.ring_bytes;
+  // the ring also holds the router's staging, the logits and scores, and the combine's values
+  const size_t ring = std::max((size_t)a.nst * a.stride, std::max(staging, std::max(route, (size_t)16 * kQDThreads)));
+  const size_t smem = fixed + ring;
   if (smem > (size_t)kQDSmemMax) return MOE_ERR_ARG;
   static bool attr[64] = {};
   MOE_CUDA_TRY(ensure_smem(decode_q8_kernel, kQDSmemMax, attr));

@@ -97,13 +97,19 @@ struct ManageKeep {
 // Expert-wave options of one manage call: wave 0 defers the misses that find no
 // victim (def_e, n_def); a later wave manages ids[n_off .. n_off + m) with
 // m = clamp(*n_dev - n_off, 0, n) read on the device (no call when m = 0).
+// Sub-batches of a wave's loads (list positions [off[b], off[b+1]) for b < n).
+constexpr int kMaxSubBatches = 4;
+struct SubBatches {
+  int off[kMaxSubBatches + 1] = {};
+  int n = 0;
+};
 struct ManageWave {
   int32_t* def_e = nullptr;
   int32_t* n_def = nullptr;
   const int32_t* n_dev = nullptr;
   int n_off = 0;
-  int32_t* sub_n = nullptr;  // with sub_b: sub_n[b] = clamp(n_miss - b*sub_b, 0, sub_b) for b < n_sub
-  int sub_b = 0, n_sub = 0;
+  int32_t* sub_n = nullptr;  // sub_n[b] = clamp(n_miss - sub.off[b], 0, sub.off[b+1] - sub.off[b]) for b < sub.n
+  SubBatches sub;
   ManageKeep keep;
 };
 int launch_manage(const int32_t* ids, int n, int E, int S, int policy, int32_t* e2s, int32_t* s2e, uint32_t* prio,
