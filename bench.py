@@ -449,7 +449,10 @@ def time_steps(wl: Workload, steps: int, warmup: int, dist=None, clocks=None, pr
     ``profile``, a second graph of the next K steps carries the timing events
     that the layer forward records around each of its launches; those give
     the per-kernel live times (the event nodes add a little latency, so that
-    graph is not used for the step time).
+    graph is not used for the step time).  That graph is replayed twice and
+    the faster replay's times are kept, so that one disturbed replay (the
+    host link or the GPU shared with another job for a moment) does not
+    stand for the kernels' durations.
     """
     M = wl.M
     for i in range(warmup):
@@ -458,6 +461,7 @@ def time_steps(wl: Workload, steps: int, warmup: int, dist=None, clocks=None, pr
     misses0, gathered0 = int(wl.layer.stats[0]), int(wl.layer.stats[2])
 
     nodes = [None]
+    prof_times = [None]
 
     def run(first, prof_list):
         g = None
@@ -470,16 +474,26 @@ def time_steps(wl: Workload, steps: int, warmup: int, dist=None, clocks=None, pr
                 nodes[0] = graph_kernel_nodes(g)
             g.instantiate()
             torch.cuda.synchronize()
-        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        s.record()
-        if graph:
-            g.replay()
-        else:
-            for i in range(steps):
-                wl.step(first + i, prof=None if prof_list is None else prof_list[i][0])
-        e.record()
-        torch.cuda.synchronize()
-        return s.elapsed_time(e)
+        best = None
+        for rep in range(2 if (graph and prof_list is not None) else 1):
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record()
+            if graph:
+                g.replay()
+            else:
+                for i in range(steps):
+                    wl.step(first + i, prof=None if prof_list is None else prof_list[i][0])
+            e.record()
+            torch.cuda.synchronize()
+            t = s.elapsed_time(e)
+            if prof_list is not None:
+                times = [_prof_times(p, evs) for p, evs, _, _ in prof_list]
+                if best is None or t < best[0]:
+                    best = (t, times)
+            else:
+                best = (t, None)
+        prof_times[0] = best[1]
+        return best[0]
 
     _barrier(dist)
     if clocks:
@@ -498,8 +512,8 @@ def time_steps(wl: Workload, steps: int, warmup: int, dist=None, clocks=None, pr
         n_chunks = (wl.cfg.T + wl.chunk() - 1) // wl.chunk()
         profs = [_make_prof(M, 8 + 40 * n_chunks) for _ in range(steps)]
         ms_prof = run(warmup + steps, profs)
-        for p, evs, _, _ in profs:
-            for n, v in _prof_times(p, evs).items():
+        for pt in prof_times[0]:
+            for n, v in pt.items():
                 kern[n] += sum(v)
                 launches[n] += len(v)
                 per_launch[n].extend(v)
