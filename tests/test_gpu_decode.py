@@ -139,3 +139,32 @@ def test_decode_with_a_remapped_pool():
         assert np.array_equal(_np(r["ids"]), want["ids"]), step
         assert_out_close(_np(r["out"].float()), want["out"], f"step {step}")
     assert int(_np(layer.dev_status)[0]) == 0
+
+
+def _check_bf16(cfg, x):
+    import expert_slot_cache_gb300 as M
+    st = stage_layer(cfg)
+    layer = M.SlotCachedMoELayer(st["wr"], st["slabs_dev"], cfg.k, cfg.I, C.MODE_RESIDENT, max_tokens=cfg.T)
+    r = layer.forward(x)
+    torch.cuda.synchronize()
+    want = O.layer_forward(_np(x.float()), _np(st["wr"].float()), HostSlabs(st["host"]), cfg.H, cfg.I, cfg.k,
+                           O.RESIDENT)
+    assert np.array_equal(_np(r["ids"]), want["ids"])
+    assert np.abs(_np(r["w"]) - want["w"]).max() <= 1e-6
+    assert_out_close(_np(r["out"].float()), want["out"], "out")
+    assert int(_np(layer.dev_status)[0]) == 0
+    return want
+
+
+def test_decode_identical_tokens_give_every_expert_eight_rows():
+    # every token routes to the same k experts: each routed expert has T = 8 rows (the widest batch)
+    cfg = C.qwen(8, S=128, mode=C.MODE_RESIDENT)
+    x = C.draw_x(cfg, DEV)[:1].repeat(cfg.T, 1).contiguous()
+    want = _check_bf16(cfg, x)
+    assert all(len(set(want["ids"][:, j])) == 1 for j in range(cfg.k))
+
+
+def test_decode_256_experts():
+    # the most experts the persistent kernel takes: eight router expert groups, the widest rank loop
+    cfg = C.qwen(8, S=256, mode=C.MODE_RESIDENT).with_(E=256, H=512, I=256)
+    _check_bf16(cfg, C.draw_x(cfg, DEV))

@@ -140,3 +140,30 @@ def test_decode_q8_graph_replay_counters_back_to_zero():
     assert int(_np(layer.dev_status)[0]) == 0
     # the arrival counters (start of the workspace) are back at zero
     assert int(layer.workspace[: 4 * (cfg.E + 4)].count_nonzero()) == 0
+
+
+def _check_q8_x(cfg, x):
+    """One step on the given x: the oracle, and bit for bit the separate W8A8 kernels."""
+    st, qh, one = _q8_layer(cfg)
+    _, _, sep = _q8_layer(cfg, decode_kernels=1)
+    r1, r2 = one.forward(x), sep.forward(x)
+    torch.cuda.synchronize()
+    want = O.layer_forward(_np(x.float()), _np(st["wr"].float()), qh, cfg.H, cfg.I, cfg.k, O.RESIDENT, quant=True)
+    assert np.array_equal(_np(r1["ids"]), want["ids"])
+    assert_out_close(_np(r1["out"].float()), want["out"], "out")
+    assert torch.equal(r1["out"], r2["out"])
+    assert int(_np(one.dev_status)[0]) == 0
+    return want
+
+
+def test_decode_q8_identical_tokens_give_every_expert_eight_rows():
+    # every routed expert has T = 8 rows: the stage loops compiled for eight rows, h of eight rows a segment
+    cfg = C.qwen(8, S=128, mode=C.MODE_RESIDENT)
+    x = C.draw_x(cfg, DEV)[:1].repeat(cfg.T, 1).contiguous()
+    want = _check_q8_x(cfg, x)
+    assert all(len(set(want["ids"][:, j])) == 1 for j in range(cfg.k))
+
+
+def test_decode_q8_256_experts():
+    cfg = C.qwen(8, S=256, mode=C.MODE_RESIDENT).with_(E=256, H=512, I=256)
+    _check_q8_x(cfg, C.draw_x(cfg, DEV))
