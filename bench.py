@@ -286,7 +286,7 @@ def stack_variant(dev: str, peaks: dict, cfg: "C.LayerConfig", steps: int = 8, w
     return out
 
 
-def w8a8_variants(dev: str, peaks: dict, steps: int = 10, warmup: int = 3) -> dict:
+def w8a8_variants(dev: str, peaks: dict, steps: int = 10, warmup: int = 3, decode_kernels: int = 0) -> dict:
     """W8A8 experts (the vllm-expert-cache page's W8A8 model; scales
     slot-indexed inside the slab): the all-resident decode layer at T = 1, 8,
     64 (HBM GB/s on unique expert bytes, now 3HI + 4(2I+H) per expert) and the
@@ -295,6 +295,7 @@ def w8a8_variants(dev: str, peaks: dict, steps: int = 10, warmup: int = 3) -> di
     for T in (1, 8, 64):
         c = C.qwen(T, S=128, mode=C.MODE_RESIDENT)
         w = Workload(c, 2 * steps + warmup, dev, quant=True)
+        w.layer.decode_kernels = decode_kernels
         r = time_steps(w, steps, warmup)
         units = count_unique_all(w, steps, warmup + steps)
         # T <= 8 runs the persistent W8A8 decode kernel: its whole launch counts
@@ -304,7 +305,8 @@ def w8a8_variants(dev: str, peaks: dict, steps: int = 10, warmup: int = 3) -> di
         out[f"resident_T{T}"] = {
             "tokens_per_s": T * steps / (r["ms"] * 1e-3), "ms_per_step": r["ms"] / steps,
             "ffn_hbm": {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                        "frac": ach / peaks["hbm_gbs"], "kernel": "decode_q8_kernel" if T <= 8 else "w8a8 stream (ffn_q8)", "bytes_per_unit": w.slab_bytes,
+                        "frac": ach / peaks["hbm_gbs"], "kernel": "decode_q8_kernel" if T <= 8 and not decode_kernels else "w8a8 stream (ffn_q8)",
+                        "bytes_per_unit": w.slab_bytes,
                         "units": units},
             "layer_hbm_frac": layer_bytes / (r["ms"] * 1e-3) / 1e9 / peaks["hbm_gbs"]}
         del w
@@ -756,6 +758,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-variants", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--separate-kernels", action="store_true",
+                    help="single workloads: small all-resident steps run as separate kernels, not the persistent one")
     ap.add_argument("--workload", default="main",
                     help="main (default) | prefill | resident_T<n> | gather_T<n> | chunks_T<n> (each also as q8_<name>: "
                          "W8A8 experts) | routing_variants | "
@@ -774,7 +778,8 @@ def main():
     peaks = _peaks()
     if args.workload == "w8a8":
         if rank == 0:
-            print(json.dumps({"workload": "w8a8", **w8a8_variants(dev, _peaks(), args.steps, args.warmup)}))
+            print(json.dumps({"workload": "w8a8", **w8a8_variants(dev, _peaks(), args.steps, args.warmup,
+                                                                    int(args.separate_kernels))}))
         return
     if args.workload == "routing_variants":
         if rank == 0:
@@ -809,6 +814,7 @@ def main():
         else:
             raise SystemExit(f"unknown workload {w}")
         wl = Workload(c, 2 * args.steps + args.warmup, dev, quant=quant)
+        wl.layer.decode_kernels = int(args.separate_kernels)
         r = time_steps(wl, args.steps, args.warmup, clocks=Clocks(local))
         if rank == 0:
             print(json.dumps({"workload": args.workload, "clocks": r["clocks"], "ms_per_step": r["ms"] / args.steps,
