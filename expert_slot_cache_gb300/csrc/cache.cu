@@ -12,6 +12,7 @@
 #include <algorithm>
 
 #include "internal.cuh"
+#include "manage_core.cuh"
 
 namespace moe {
 
@@ -78,8 +79,6 @@ __global__ void __launch_bounds__(kManageThreads) manage_kernel(
   uint32_t* prio = reinterpret_cast<uint32_t*>(s2e + S);
   int* cand = reinterpret_cast<int*>(prio + S);
   int* vict = cand + S;
-  __shared__ int tmp[33];
-  __shared__ int s_nmiss, s_nhit;
   const int tid = threadIdx.x;
   if (n_dev) {
     n = min(max(*n_dev - n_off, 0), n);
@@ -104,7 +103,6 @@ __global__ void __launch_bounds__(kManageThreads) manage_kernel(
   for (int s = tid; s < S; s += kManageThreads) {
     s2e[s] = s2e_g[s];
     prio[s] = prio_g[s];
-    vict[s] = -1;
   }
   __syncthreads();
   for (int i = tid; i < n; i += kManageThreads) {
@@ -117,108 +115,9 @@ __global__ void __launch_bounds__(kManageThreads) manage_kernel(
   }
   __syncthreads();
   const uint32_t stamp = *stamp_g + 1u;
-
-  // Ranks of misses and hits in ascending expert order.
-  int carry_m = 0, carry_h = 0;
-  for (int e0 = 0; e0 < E; e0 += kManageThreads) {
-    const int e = e0 + tid;
-    const bool nd = e < E && need[e];
-    const bool res = nd && e2s[e] >= 0 && e2s[e] < S;
-    int tm, th;
-    const int xm = block_exclusive_scan(nd && !res ? 1 : 0, tmp, &tm);
-    const int xh = block_exclusive_scan(res ? 1 : 0, tmp, &th);
-    if (e < E) {
-      mrank[e] = nd && !res ? carry_m + xm : -1;
-      hrank[e] = res ? carry_h + xh : -1;
-    }
-    carry_m += tm;
-    carry_h += th;
-  }
-  if (tid == 0) {
-    s_nmiss = carry_m;
-    s_nhit = carry_h;
-  }
-  // Candidate slots: not holding an expert this step needs.
-  int carry_c = 0;
-  for (int s0 = 0; s0 < S; s0 += kManageThreads) {
-    const int s = s0 + tid;
-    int c = 0;
-    if (s < S) {
-      const int e = s2e[s];
-      c = !(e >= 0 && e < E && need[e]);
-      cand[s] = c;
-    }
-    int tc;
-    block_exclusive_scan(c, tmp, &tc);
-    carry_c += tc;
-  }
-  __syncthreads();
-  const int nm = s_nmiss;
-  // misses that get a slot: all of them, or with deferral as many as there are candidates
-  const int nl = (def_e && policy != MOE_POLICY_STATIC) ? min(nm, carry_c) : nm;
-
-  if (policy != MOE_POLICY_STATIC) {
-    // Victim rank of each candidate: empty first (ascending slot), then
-    // ascending prio, then ascending slot.
-    for (int s = tid; s < S; s += kManageThreads) {
-      if (!cand[s]) continue;
-      const bool es = s2e[s] < 0;
-      const uint32_t ps = prio[s];
-      int r = 0;
-      for (int q = 0; q < S; ++q) {
-        if (!cand[q] || q == s) continue;
-        const bool eq = s2e[q] < 0;
-        bool before;
-        if (eq != es)
-          before = eq;
-        else if (es)
-          before = q < s;
-        else
-          before = prio[q] < ps || (prio[q] == ps && q < s);
-        r += before;
-      }
-      if (r < nm) vict[r] = s;
-    }
-  }
-  __syncthreads();
-
-  // Apply.  Hit slots and victim slots are disjoint; evicted experts are
-  // resident, missing experts are not, so no two writes touch one entry.
-  for (int e = tid; e < E; e += kManageThreads) {
-    if (hrank[e] >= 0) {
-      const int s = e2s[e];
-      if (policy == MOE_POLICY_LRU) prio[s] = stamp;
-      else if (policy == MOE_POLICY_LFU) prio[s] = prio[s] + 1u;
-      if (hit_e) hit_e[hrank[e]] = e;
-    }
-  }
-  __syncthreads();
-  for (int e = tid; e < E; e += kManageThreads) {
-    const int r = mrank[e];
-    if (r < 0) continue;
-    if (r >= nl) {  // deferred to a later wave: stays cold
-      def_e[r - nl] = e;
-      continue;
-    }
-    miss_e[r] = e;
-    if (policy == MOE_POLICY_STATIC) {
-      miss_s[r] = -1;
-      continue;
-    }
-    const int s = vict[r];
-    miss_s[r] = s;
-    if (s < 0) {  // cannot happen when the step fits the pool (checked on the host)
-      set_status(status, MOE_DEV_BAD_SLOT);
-      if (keep.ev_e) keep.ev_e[r] = -1;
-      continue;
-    }
-    const int old = s2e[s];
-    if (old >= 0 && old < E) e2s[old] = -1;
-    if (keep.ev_e) keep.ev_e[r] = old >= 0 && old < E ? old : -1;
-    s2e[s] = e;
-    e2s[e] = s;
-    prio[s] = policy == MOE_POLICY_LRU ? stamp : 1u;
-  }
+  const ManageCounts mc = manage_block(E, S, policy, def_e != nullptr, stamp, need, e2s, s2e, prio, mrank, hrank,
+                                       cand, vict, hit_e, miss_e, miss_s, def_e, keep.ev_e, status);
+  const int nm = mc.nm, nl = mc.nl;
   __syncthreads();
   if (keep.kept_e) write_kept(mrank, E, keep, nl);  // mrank is free from here on
   for (int e = tid; e < E; e += kManageThreads) e2s_g[e] = e2s[e];
@@ -235,7 +134,7 @@ __global__ void __launch_bounds__(kManageThreads) manage_kernel(
   if (tid == 0) {
     *stamp_g = stamp;
     *n_miss = nl;
-    if (n_hit) *n_hit = s_nhit;
+    if (n_hit) *n_hit = mc.nh;
     if (n_def) *n_def = nm - nl;
     if (sub_n)
       for (int b = 0; b < sub.n; ++b) sub_n[b] = min(max(nl - sub.off[b], 0), sub.off[b + 1] - sub.off[b]);
