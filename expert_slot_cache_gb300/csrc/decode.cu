@@ -34,10 +34,29 @@
 //     CTA combines a share of the output: out[t] = sum_j w[t][j] y[pos(t, j)]
 //     in fp32, j ascending, rounded to bf16.
 // The last CTA to leave puts every counter back to zero.
+//
+// Expert-cache steps (gather mode, T*k <= S, LRU or LFU) run in the same launch
+// ("Porting vllm-expert-cache to NVIDIA GPUs", "1. Kernels": a fused cache
+// manager, gather and expert kernel; "Betelgeuse ... on an RTX 3060", "What it
+// actually does under the hood": hits resolved in-stream, no host round trip):
+//  0. before its phase-1 arrival every CTA copies the cache state (e2s, s2e,
+//     prio, stamp) into shared memory; live-cache affinity reads that copy;
+//  2b. after the routing every CTA runs the manage state machine on its copy
+//     (deterministic, so every CTA gets the same result) and lists the step's
+//     experts as hits, then misses in load order; CTA 0 writes the new state;
+//  3'. CTAs 0 .. gather_ctas-1 copy the missing slabs from mapped host memory
+//     into their victim slots, miss after miss, in 24 KB pieces, counting each
+//     miss's finished pieces on a counter; the other CTAs run the weight
+//     streams over the list, and a loader that meets a missing expert waits for
+//     its counter (then a generic-to-async proxy fence) before its first
+//     tensor-map copy from that slot.  The hits stream while the link copies.
+// Every miss gets a victim slot the step does not need because T*k <= S, so no
+// expert is loaded twice and no slot is read while it is written.
 #include <algorithm>
 
 #include "decode_route.cuh"
 #include "internal.cuh"
+#include "manage_core.cuh"
 #include "sched.cuh"
 #include "tc05.cuh"
 
@@ -59,8 +78,13 @@ constexpr int kPMaxStages = 4;
 constexpr uint32_t kPTmemCols = 512;  // two accumulator buffers of up to 256 columns
 constexpr int kPSmemMax = 232448 - 12 * 1024;  // dynamic shared memory cap (static shared memory below)
 
-// Counters after the E per-expert gate/up counters.
+// Counters after the E per-expert gate/up counters; then, in gather mode, one counter of copied pieces per miss.
 constexpr int kCtrLogits = 0, kCtrDown = 1, kCtrExit = 2, kCtrRoute = 3, kCtrCount = 4;
+// Gather mode: CTAs that copy the misses (the separate gather's grid: the host link saturates well below it),
+// and the piece one CTA copies at a time (eight 16-byte loads in flight per thread).
+constexpr int kDGCtas = 48;
+constexpr int kDGUnroll = 8;
+constexpr int kDGPieceVec = kPThreads * kDGUnroll;  // 16-byte units, 24 KB
 
 struct DecodeArgs {
   const uint16_t* x;   // bf16 [T][H]
@@ -79,10 +103,20 @@ struct DecodeArgs {
   uint16_t* out;  // bf16 [T][H]
   unsigned long long* gsum;  // [n][2I]: the rows' gate | up sums, 64-bit fixed point (2^-32), zeroed per step
   unsigned long long* ysum;  // [n][H]: the rows' down sums, the same
-  int32_t* ctr;  // E + kCtrCount, zero on entry and on exit
+  int32_t* ctr;  // E + kCtrCount (+ kPMaxN in gather mode), zero on entry and on exit
   int32_t* status;
   int stride, nst, hcap;  // ring stage stride and count; down stages the h area holds
   int ring_bytes;         // >= nst * stride and >= the router's staging (kPWarps * kRStage)
+  // gather mode only: the cache state (updated in place), the host store and the copy
+  int32_t* e2s_g;
+  int32_t* s2e_g;
+  uint32_t* prio_g;
+  uint32_t* stamp_g;
+  int policy;
+  const uint4* host;  // mapped pinned host store, [E][slab]
+  uint4* pool_w;      // the slot pool, written by the copy
+  size_t slab_vec;    // 16-byte units per slab
+  int64_t* stats;     // [0] += misses, [1] += 1, [2] += bytes copied, or NULL
 };
 
 // The partial sums of a step's rows meet in 64-bit fixed point with 32 fraction bits: a part v adds
@@ -122,6 +156,9 @@ __device__ __forceinline__ void drain_tile(uint32_t taddr, unsigned long long* b
     dec_epilogue<8>(taddr, base, ntiles, N, nb);
 }
 
+__device__ __forceinline__ void fence_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+
+template <bool kGather>
 __global__ void __launch_bounds__(kPThreads, 1) decode_layer_kernel(const DecodeArgs a,
                                                                     const __grid_constant__ CUtensorMap mwg,
                                                                     const __grid_constant__ CUtensorMap mwd) {
@@ -139,12 +176,19 @@ __global__ void __launch_bounds__(kPThreads, 1) decode_layer_kernel(const Decode
   uint64_t* tempty = tfull + 2;
   uint64_t* done = tempty + 2;
   uint64_t* hbar = done + 1;  // [hcap]: h of local down stage i is in place
+  // gather mode: the cache state's copy (e2s [E], s2e [S], prio [S]) and the misses' slots [kPMaxN]
+  int* st_e2s = reinterpret_cast<int*>(hbar + a.hcap);
+  int* st_s2e = st_e2s + a.E;
+  uint32_t* st_prio = reinterpret_cast<uint32_t*>(st_s2e + a.S);
+  int* st_miss_s = reinterpret_cast<int*>(st_prio + a.S);
   __shared__ int s_ids[kPMaxN], s_rows[kPMaxN], s_pos[kPMaxN];
   __shared__ float s_w[kPMaxN];
   __shared__ int s_cnt[kPMaxE], s_off[kPMaxE + 1], s_act[kPMaxE], s_li[kPMaxE];
   __shared__ int tmp[33];
   __shared__ int s_nact, s_abort;
   __shared__ uint32_t s_tmem;
+  __shared__ int s_nh, s_nl;  // gather mode: hits, then misses, in the list
+  __shared__ uint32_t s_stamp;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int T = a.T, E = a.E, k = a.k, H = a.H, I = a.I, n = T * k;
@@ -174,9 +218,21 @@ __global__ void __launch_bounds__(kPThreads, 1) decode_layer_kernel(const Decode
   tc_fence_after();
   const uint32_t tmem = s_tmem;
   volatile int* abort_flag = &s_abort;
+  int32_t* gctr = a.ctr + E + kCtrCount;  // gather mode: pieces copied of miss m
+
+  // ---- 0. gather mode: the cache state as it stands, read before this CTA's phase-1 arrival (CTA 0
+  // writes the new state only once every CTA has arrived) -----------------------------------------
+  if constexpr (kGather) {
+    for (int e = tid; e < E; e += kPThreads) st_e2s[e] = a.e2s_g[e];
+    for (int s = tid; s < a.S; s += kPThreads) {
+      st_s2e[s] = a.s2e_g[s];
+      st_prio[s] = a.prio_g[s];
+    }
+    if (tid == 0) s_stamp = *a.stamp_g;
+  }
 
   // ---- 1. router logits: block parts -------------------------------------------------
-  RouteIO rio{a.x, a.wr, a.off, a.bias, a.e2s, a.affinity, a.rflags, T, H, E, k,
+  RouteIO rio{a.x, a.wr, a.off, a.bias, kGather ? st_e2s : a.e2s, a.affinity, a.rflags, T, H, E, k,
               a.lpart, a.logits, a.ids, a.w, &a.ctr[E + kCtrRoute], a.status};
   route_logit_parts<kPThreads>(rio, ring);
   {
@@ -201,26 +257,140 @@ __global__ void __launch_bounds__(kPThreads, 1) decode_layer_kernel(const Decode
     route_pick_group<kPThreads>(rio, rsm);
   }
 
+  // ---- 2b. gather mode: the manage state machine on this CTA's copy of the state ---------------
+  if constexpr (kGather) {
+    // work arrays in the ring (no tensor-map copy has been issued yet)
+    int* mrank = reinterpret_cast<int*>(ring);
+    int* hrank = mrank + E;
+    int* cand = hrank + E;
+    int* vict = cand + a.S;
+    int* hit_t = vict + a.S;
+    int* miss_t = hit_t + kPMaxN;
+    const uint32_t stamp = s_stamp + 1u;
+    const ManageCounts mc = manage_block(E, a.S, a.policy, false, stamp, s_cnt, st_e2s, st_s2e, st_prio, mrank,
+                                         hrank, cand, vict, hit_t, miss_t, st_miss_s, nullptr, nullptr, a.status);
+    // the list: hits (ascending id), then the misses in load order (ascending id); T*k <= S gives every
+    // miss a slot, so together they are the routed experts
+    const bool ok = mc.nh + mc.nl == s_nact && mc.nl <= kPMaxN;
+    if (ok)
+      for (int i = tid; i < s_nact; i += kPThreads) {
+        const int e = i < mc.nh ? hit_t[i] : miss_t[i - mc.nh];
+        s_act[i] = e;
+        s_li[e] = i;
+      }
+    if (blockIdx.x == 0) {
+      for (int e = tid; e < E; e += kPThreads) a.e2s_g[e] = st_e2s[e];
+      for (int s = tid; s < a.S; s += kPThreads) {
+        a.s2e_g[s] = st_s2e[s];
+        a.prio_g[s] = st_prio[s];
+      }
+      if (tid == 0) {
+        *a.stamp_g = stamp;
+        if (a.stats) {
+          a.stats[0] += mc.nl;
+          a.stats[1] += 1;
+          a.stats[2] += (int64_t)mc.nl * (int64_t)a.slab_vec * 16;
+        }
+      }
+    }
+    if (tid == 0) {
+      s_nh = mc.nh;
+      s_nl = ok ? mc.nl : 0;
+      if (!ok) {
+        set_status(a.status, MOE_DEV_BAD_SLOT);
+        s_abort = 1;
+      }
+    }
+    fence_async_smem();  // tensor-map copies overwrite the work arrays next
+    __syncthreads();
+  }
+
   // ---- 3-5. the two weight streams -----------------------------------------------------
   FfnArgs fa{};
   fa.E = E;
   fa.S = a.S;
-  fa.e2s = a.e2s;
+  fa.e2s = kGather ? st_e2s : a.e2s;
   fa.list_e = s_act;
   fa.offset = s_off;
   const int n_list = s_nact;
   const int NSRg = H / kPK, NSRd = I / kPK;
   const int Ng = 2 * I;
   constexpr int kNoCap = 1 << 30;  // the sums meet in the fixed-point accumulators: no cap on an expert's parts
-  const int Lg = stream_len(n_list, NSRg, G, kNoCap), Ld = stream_len(n_list, NSRd, G, kNoCap);
-  const int bg = blockIdx.x * Lg, eg_end = min(bg + Lg, n_list * NSRg);
-  const int bd = blockIdx.x * Ld, ed_end = min(bd + Ld, n_list * NSRd);
+  // gather mode with misses: CTAs 0 .. gg-1 copy them, the others stream
+  const int gg = kGather && s_nl > 0 ? kDGCtas : 0;
+  const int Gf = G - gg, fb = (int)blockIdx.x - gg;
+  const int Lg = stream_len(n_list, NSRg, Gf, kNoCap), Ld = stream_len(n_list, NSRd, Gf, kNoCap);
+  const int bg = fb >= 0 ? fb * Lg : 0, eg_end = fb >= 0 ? min(bg + Lg, n_list * NSRg) : 0;
+  const int bd = fb >= 0 ? fb * Ld : 0, ed_end = fb >= 0 ? min(bd + Ld, n_list * NSRd) : 0;
   const int wbytes_g = 2 * I * kPK * 2, wbytes_d = H * kPK * 2;
+  const int gpieces = kGather ? (int)((a.slab_vec + kDGPieceVec - 1) / kDGPieceVec) : 0;
   if (Ld > a.hcap) {  // the host sizes the h area for the largest range: cannot happen
     if (tid == 0) set_status(a.status, MOE_DEV_BAD_GROUPS);
     s_abort = 1;
   }
   __syncthreads();
+
+  // ---- 3'. gather mode: the copying CTAs, miss after miss -----------------------------------
+  // Software-pipelined: the next piece's host loads are in flight while this piece is stored, fenced and
+  // released, so the host link never waits on the barrier.
+  if constexpr (kGather) {
+    if ((int)blockIdx.x < gg && !*abort_flag) {
+      const int nh = s_nh;
+      const int items = s_nl * gpieces;
+      // piece `it`: its source and destination, or false (a bad list entry: nothing is copied)
+      auto piece = [&](int it, const uint4*& src, uint4*& dst, size_t& lim) {
+        const int m = it / gpieces, c = it - m * gpieces;
+        const int e = s_act[nh + m], sl = st_miss_s[m];
+        if (e < 0 || e >= E || sl < 0 || sl >= a.S) {
+          if (tid == 0) set_status(a.status, e < 0 || e >= E ? MOE_DEV_BAD_EXPERT : MOE_DEV_BAD_SLOT);
+          return false;
+        }
+        src = a.host + (size_t)e * a.slab_vec + (size_t)c * kDGPieceVec;
+        dst = a.pool_w + (size_t)sl * a.slab_vec + (size_t)c * kDGPieceVec;
+        lim = min((size_t)kDGPieceVec, a.slab_vec - (size_t)c * kDGPieceVec);
+        return true;
+      };
+      uint4 v[kDGUnroll], nv[kDGUnroll];
+      const uint4* src = nullptr;
+      uint4* dst = nullptr;
+      size_t lim = 0;
+      bool ok = (int)blockIdx.x < items && piece(blockIdx.x, src, dst, lim);
+      if (ok)
+#pragma unroll
+        for (int u = 0; u < kDGUnroll; ++u) {
+          const size_t j = tid + (size_t)u * kPThreads;
+          if (j < lim) v[u] = ldg_stream(src + j);
+        }
+      for (int it = blockIdx.x; it < items; it += gg) {
+        const int nx = it + gg;
+        const uint4* nsrc = nullptr;
+        uint4* ndst = nullptr;
+        size_t nlim = 0;
+        const bool nok = nx < items && piece(nx, nsrc, ndst, nlim);
+        if (nok)
+#pragma unroll
+          for (int u = 0; u < kDGUnroll; ++u) {
+            const size_t j = tid + (size_t)u * kPThreads;
+            if (j < nlim) nv[u] = ldg_stream(nsrc + j);
+          }
+        if (ok) {
+#pragma unroll
+          for (int u = 0; u < kDGUnroll; ++u) {
+            const size_t j = tid + (size_t)u * kPThreads;
+            if (j < lim) dst[j] = v[u];
+          }
+          fence_async_global();  // the piece is read next by other CTAs' tensor-map copies
+        }
+        __syncthreads();
+        if (tid == 0) add_release(&gctr[it / gpieces], 1);  // the barrier orders every thread's stores before it
+#pragma unroll
+        for (int u = 0; u < kDGUnroll; ++u) v[u] = nv[u];
+        ok = nok;
+        dst = ndst;
+        lim = nlim;
+      }
+    }
+  }
 
   if (warp == 0) {
     if (lane == 0) {
@@ -234,8 +404,25 @@ __global__ void __launch_bounds__(kPThreads, 1) decode_layer_kernel(const Decode
         }
         return !*abort_flag;
       };
+      // gather mode: a missing expert's slot is read once all of its pieces are in (bit m: miss m seen complete)
+      uint64_t seen = 0;
+      auto slab_ready = [&](int e) {
+        if constexpr (kGather) {
+          const int m = s_li[e] - s_nh;
+          if (m < 0 || m >= kPMaxN || ((seen >> m) & 1ull)) return true;
+          if (*abort_flag) return false;
+          if (!wait_count(&gctr[m], gpieces, a.status)) {
+            *abort_flag = 1;
+            return false;
+          }
+          fence_async_global();  // the copy's generic stores before this thread's tensor-map reads of the slot
+          seen |= 1ull << m;
+        }
+        return true;
+      };
       if (bg < eg_end)
         stream_segments<kPN>(fa, NSRg, Lg, bg, eg_end, [&](const StreamSeg& g) {
+          if (!slab_ready(g.e)) return false;
           int tok[kPMaxT];
           for (int t = 0; t < g.nb; ++t) tok[t] = s_rows[g.p0 + t] / k;
           for (int s = g.s_lo; s < g.s_hi; ++s, ++it) {
@@ -259,6 +446,7 @@ __global__ void __launch_bounds__(kPThreads, 1) decode_layer_kernel(const Decode
         });
       if (bd < ed_end)
         stream_segments<kPN>(fa, NSRd, Ld, bd, ed_end, [&](const StreamSeg& g) {
+          if (!slab_ready(g.e)) return false;
           for (int s = g.s_lo; s < g.s_hi; ++s, ++it) {
             const int sl = it % a.nst;
             const uint32_t use = it / a.nst;
@@ -471,7 +659,7 @@ __global__ void __launch_bounds__(kPThreads, 1) decode_layer_kernel(const Decode
   }
   // the last CTA out resets the counters: every other CTA is past its last wait
   if (tid == 0 && atomicAdd(&a.ctr[E + kCtrExit], 1) == G - 1)
-    for (int i = 0; i < E + kCtrCount; ++i) a.ctr[i] = 0;
+    for (int i = 0; i < E + kCtrCount + (kGather ? kPMaxN : 0); ++i) a.ctr[i] = 0;
 }
 
 // ---------------------------------------------------------------------------
@@ -491,10 +679,50 @@ bool decode_eligible(int T, int H, int E, int k, int I, int S, const void* x, co
   return dec_stride(H, I) * 2 + 1024 + 16 * 1024 <= kPSmemMax;
 }
 
-size_t decode_ctr_ints(int E) { return (size_t)E + kCtrCount; }  // the W8A8 kernel keeps the same count
+// Dynamic shared memory of one launch: ring | h of the down stages (the logits and scores before that) |
+// barriers | gather mode: the cache state's copy.
+struct DecPlan {
+  int hcap = 0, nst = 0, ring_bytes = 0;
+  size_t smem = 0;
+};
 
-int launch_decode(const moe_layer_args* la, float* lpart, float* logits, float* skp, size_t skp_bytes, int32_t* ctr,
-                  cudaStream_t stream) {
+static bool dec_plan(int T, int H, int E, int k, int I, int S, int sms, bool gather, DecPlan* p) {
+  const int n = T * k, NSRd = I / kPK, lmax = std::min(n, E);
+  // the largest down range a streaming CTA can get (stream_len with every routed expert distinct)
+  const int gf = sms - (gather ? kDGCtas : 0);
+  if (gf < 1) return false;
+  p->hcap = (lmax * NSRd + gf - 1) / gf + 1;
+  const size_t hbytes = (std::max((size_t)p->hcap * kPHStage, (size_t)T * E * 8) + 15) & ~size_t(15);
+  const size_t state = gather ? (size_t)4 * (E + 2 * S + kPMaxN) : 0;
+  const size_t fixed = 1024 + hbytes + 8 * (2 * kPMaxStages + 5 + p->hcap) + state;
+  const int stride = dec_stride(H, I);
+  if (fixed >= (size_t)kPSmemMax) return false;
+  p->nst = (int)std::min<size_t>(kPMaxStages, (kPSmemMax - fixed) / stride);
+  if (p->nst < 2) return false;
+  p->ring_bytes = std::max(p->nst * stride, (kPWarps * kRStage + 1023) & ~1023);
+  // gather mode: the manage call's work arrays sit in the ring before the streams start
+  if (gather && (size_t)p->ring_bytes < (size_t)4 * (2 * E + 2 * S + 2 * kPMaxN)) return false;
+  p->smem = fixed + (size_t)p->ring_bytes;
+  return p->smem <= (size_t)kPSmemMax;
+}
+
+bool decode_gather_eligible(int T, int H, int E, int k, int I, int S, int policy, const void* x, const void* wr,
+                            const void* pool, const void* host, int sms) {
+  if (!decode_eligible(T, H, E, k, I, S, x, wr, pool)) return false;
+  if (policy != MOE_POLICY_LRU && policy != MOE_POLICY_LFU) return false;
+  // T*k <= S: every miss finds a victim among the slots the step does not need (one manage call, no deferral)
+  if (T * k > S || S > kPMaxE || (uintptr_t)host % 16) return false;
+  if (sms < 2 * kDGCtas) return false;  // at least as many streaming CTAs as copying ones
+  DecPlan p;
+  return dec_plan(T, H, E, k, I, S, sms, true, &p);
+}
+
+// the W8A8 kernel keeps the same count (it uses no per-miss counters)
+size_t decode_ctr_ints(int E) { return (size_t)E + kCtrCount + kPMaxN; }
+
+template <bool kGather>
+static int launch_decode_impl(const moe_layer_args* la, float* lpart, float* logits, float* skp, size_t skp_bytes,
+                              int32_t* ctr, cudaStream_t stream) {
   const int T = la->T, H = la->H, E = la->E, k = la->k, I = la->I, n = T * k;
   int dev = 0, sms = 0;
   MOE_CUDA_TRY(cudaGetDevice(&dev));
@@ -504,7 +732,7 @@ int launch_decode(const moe_layer_args* la, float* lpart, float* logits, float* 
   a.wr = (const uint16_t*)la->w_router;
   a.off = la->logit_offset;
   a.bias = la->sel_bias;
-  a.e2s = la->e2s;
+  a.e2s = kGather ? nullptr : la->e2s;
   a.affinity = la->affinity;
   a.rflags = la->route_flags;
   a.T = T;
@@ -526,20 +754,27 @@ int launch_decode(const moe_layer_args* la, float* lpart, float* logits, float* 
   a.ctr = ctr;
   a.status = la->dev_status;
   a.stride = dec_stride(H, I);
-  // the largest down range a CTA can get (stream_len with every routed expert distinct)
-  const int NSRd = I / kPK, lmax = std::min(n, E);
-  a.hcap = (lmax * NSRd + sms - 1) / sms + 1;
-  const size_t hbytes = (std::max((size_t)a.hcap * kPHStage, (size_t)T * E * 8) + 15) & ~size_t(15);
-  const size_t fixed = 1024 + hbytes + 8 * (2 * kPMaxStages + 5 + a.hcap);
-  a.nst = (int)std::min<size_t>(kPMaxStages, (kPSmemMax - fixed) / a.stride);
-  if (a.nst < 2) return MOE_ERR_ARG;
-  a.ring_bytes = std::max(a.nst * a.stride, (kPWarps * kRStage + 1023) & ~1023);
-  const size_t smem = fixed + (size_t)a.ring_bytes;
-  if (smem > (size_t)kPSmemMax) return MOE_ERR_ARG;
+  if constexpr (kGather) {
+    if (!la->e2s || !la->s2e || !la->prio || !la->stamp || !la->host_slabs) return MOE_ERR_ARG;
+    a.e2s_g = la->e2s;
+    a.s2e_g = la->s2e;
+    a.prio_g = la->prio;
+    a.stamp_g = la->stamp;
+    a.policy = la->policy;
+    a.host = (const uint4*)la->host_slabs;
+    a.pool_w = (uint4*)la->pool;
+    a.slab_vec = (size_t)6 * H * I / 16;
+    a.stats = la->stats;
+  }
+  DecPlan p;
+  if (!dec_plan(T, H, E, k, I, la->S, sms, kGather, &p)) return MOE_ERR_ARG;
+  a.hcap = p.hcap;
+  a.nst = p.nst;
+  a.ring_bytes = p.ring_bytes;
   static bool attr[64] = {};
-  MOE_CUDA_TRY(ensure_smem(decode_layer_kernel, kPSmemMax, attr));
+  MOE_CUDA_TRY(ensure_smem(decode_layer_kernel<kGather>, kPSmemMax, attr));
   int occ = 0;
-  MOE_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, decode_layer_kernel, kPThreads, smem));
+  MOE_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, decode_layer_kernel<kGather>, kPThreads, p.smem));
   if (occ < 1) return MOE_ERR_ARG;
   const size_t mat = (size_t)H * I;
   CUtensorMap mwg, mwd;
@@ -558,15 +793,25 @@ int launch_decode(const moe_layer_args* la, float* lpart, float* logits, float* 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(sms);
   cfg.blockDim = dim3(kPThreads);
-  cfg.dynamicSmemBytes = smem;
+  cfg.dynamicSmemBytes = p.smem;
   cfg.stream = stream;
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeCooperative;
   at[0].val.cooperative = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  MOE_CUDA_TRY(cudaLaunchKernelEx(&cfg, decode_layer_kernel, a, mwg, mwd));
+  MOE_CUDA_TRY(cudaLaunchKernelEx(&cfg, decode_layer_kernel<kGather>, a, mwg, mwd));
   return MOE_OK;
+}
+
+int launch_decode(const moe_layer_args* la, float* lpart, float* logits, float* skp, size_t skp_bytes, int32_t* ctr,
+                  cudaStream_t stream) {
+  return launch_decode_impl<false>(la, lpart, logits, skp, skp_bytes, ctr, stream);
+}
+
+int launch_decode_gather(const moe_layer_args* la, float* lpart, float* logits, float* skp, size_t skp_bytes,
+                         int32_t* ctr, cudaStream_t stream) {
+  return launch_decode_impl<true>(la, lpart, logits, skp, skp_bytes, ctr, stream);
 }
 
 }  // namespace moe

@@ -126,6 +126,12 @@ bool decode_eligible(int T, int H, int E, int k, int I, int S, const void* x, co
 size_t decode_ctr_ints(int E);
 int launch_decode(const moe_layer_args* la, float* lpart, float* logits, float* skp, size_t skp_bytes, int32_t* ctr,
                   cudaStream_t stream);
+// The same kernel for a small expert-cache step (GATHER, T*k <= S, LRU / LFU): manage, the gather of the
+// misses and the weight streams in the one launch; the cache state is updated in place.
+bool decode_gather_eligible(int T, int H, int E, int k, int I, int S, int policy, const void* x, const void* wr,
+                            const void* pool, const void* host, int sms);
+int launch_decode_gather(const moe_layer_args* la, float* lpart, float* logits, float* skp, size_t skp_bytes,
+                         int32_t* ctr, cudaStream_t stream);
 // Its W8A8 counterpart (decode_q8.cu): CUDA-core weight streams; the step's integer sums meet in
 // accumulators of T*k*(2I + H) int32 (+ T*k row scales) at the start of `ws`.
 bool decode_q8_eligible(int T, int H, int E, int k, int I, int S, const void* x, const void* wr, const void* pool,

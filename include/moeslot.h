@@ -455,7 +455,7 @@ typedef struct moe_layer_args {
   int32_t* window_counts;    /* device int32 [E] or NULL: each chunk's routings are added (moe_cache_count) */
   int32_t quant;             /* 0: bf16 slabs; 1: W8A8 slabs (moe_quantize_slabs), RESIDENT or GATHER mode */
   int32_t schedule;          /* GATHER steps larger than the pool: MOE_SCHED_CHUNKS or MOE_SCHED_WAVES */
-  int32_t decode_kernels;    /* RESIDENT: 0 = the persistent decode kernel where it applies, 1 = separate kernels */
+  int32_t decode_kernels;    /* 0 = the persistent decode kernel where it applies (RESIDENT, GATHER), 1 = separate kernels */
 } moe_layer_args;
 
 /*
@@ -480,11 +480,20 @@ typedef struct moe_layer_args {
  * their own persistent launch: router, the tokens' 8-bit codes, the gate/up
  * and down weight streams folded with dp4a (their exact int32 sums meet in
  * accumulators by integer atomics), h quantised per row, and the combine;
- * its output is bit for bit that of the separate W8A8 kernels.  The
- * grid-wide waits of both are bounded: a wait that gives up sets
- * MOE_DEV_TIMEOUT.  They keep arrival counters at the start of the
- * workspace, which must therefore be zero-filled once before the first call
- * on it (each call leaves them zero).
+ * its output is bit for bit that of the separate W8A8 kernels.  Small
+ * expert-cache steps (GATHER, bf16, LRU or LFU, T*k <= S <= 256, the bf16
+ * shape limits above, decode_kernels == 0, at least 96 SMs) run in the bf16
+ * persistent launch too ("Porting vllm-expert-cache to NVIDIA GPUs", "1.
+ * Kernels": a fused manager, gather and expert kernel): every CTA runs the
+ * manage state machine on a shared-memory copy of the cache state, CTA 0
+ * writes the new state, 48 CTAs copy the missing slabs from host memory into
+ * their victim slots while the others stream the hit experts, and each
+ * missing expert streams once its slab is in.  The state, miss count,
+ * statistics and slot bytes are bit for bit those of the separate manage and
+ * gather calls.  The grid-wide waits of these kernels are bounded: a wait
+ * that gives up sets MOE_DEV_TIMEOUT.  They keep arrival counters at the
+ * start of the workspace, which must therefore be zero-filled once before
+ * the first call on it (each call leaves them zero).
  * `side` may be NULL or equal to `main` (then everything runs on `main`).
  * The sequence of launches depends only on the shapes, so it can be
  * captured into a CUDA graph.
