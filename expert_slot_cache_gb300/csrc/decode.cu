@@ -156,7 +156,51 @@ __device__ __forceinline__ void drain_tile(uint32_t taddr, unsigned long long* b
     dec_epilogue<8>(taddr, base, ntiles, N, nb);
 }
 
+// The same, out of line: the gather-mode kernel's phase loop keeps more state live, and the drain's
+// accumulator registers would otherwise spill.
+__device__ __noinline__ void drain_tile_call(uint32_t taddr, unsigned long long* base, int ntiles, int N, int nb) {
+  drain_tile(taddr, base, ntiles, N, nb);
+}
+
 __device__ __forceinline__ void fence_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+
+// One projection's stage schedule for one CTA, in phases.  Phase 0: list entries [0, nh) (every entry in
+// resident mode), NSR stages each, dealt as equal contiguous ranges of L stages over the Gf streaming CTAs
+// (the decode stream schedule).  Phase 1 + m (gather mode): miss m, list entry nh + m, its stages cut into
+// `per` runs of L1 = ceil(NSR / Gf) stages, run r going to streaming CTA (m * per + r) % Gf: a miss streams
+// on many CTAs at once as soon as its slab is in, and the runs of all misses spread evenly over the CTAs.
+// Every role of a CTA walks phase after phase, gate/up before down within a phase; the down stages of a
+// phase wait only for gate/up parts of the same phase, which every CTA takes before its own down stages.
+static_assert(kPMaxT <= kPN, "one token batch per expert part: a part's stages are walked once");
+struct DecSched {
+  int NSR, nh, Gf, f;  // f: this CTA among the streaming CTAs, -1 for none
+  int L, L1, per;
+  __device__ __forceinline__ void init(int NSR_, int nh_, int Gf_, int f_) {
+    NSR = NSR_;
+    nh = nh_;
+    Gf = Gf_;
+    f = f_;
+    L = nh > 0 ? stream_len(nh, NSR, Gf, 1 << 30) : 1;
+    L1 = (NSR + Gf - 1) / Gf;
+    per = (NSR + L1 - 1) / L1;
+  }
+  // this CTA's stage range [beg, end) of phase p (empty when beg >= end)
+  __device__ __forceinline__ void range(int p, int& beg, int& end) const {
+    beg = end = 0;
+    if (f < 0) return;
+    if (p == 0) {
+      beg = f * L;
+      end = min(beg + L, nh * NSR);
+      return;
+    }
+    const int m = p - 1, r = (f - (m * per) % Gf + Gf) % Gf;
+    if (r >= per) return;
+    beg = (nh + m) * NSR + r * L1;
+    end = min(beg + L1, (nh + m + 1) * NSR);
+  }
+  // the CTA parts list entry li is cut into
+  __device__ __forceinline__ int parts(int li) const { return li < nh ? stream_parts(li, NSR, L) : per; }
+};
 
 template <bool kGather>
 __global__ void __launch_bounds__(kPThreads, 1) decode_layer_kernel(const DecodeArgs a,
@@ -315,16 +359,23 @@ __global__ void __launch_bounds__(kPThreads, 1) decode_layer_kernel(const Decode
   const int n_list = s_nact;
   const int NSRg = H / kPK, NSRd = I / kPK;
   const int Ng = 2 * I;
-  constexpr int kNoCap = 1 << 30;  // the sums meet in the fixed-point accumulators: no cap on an expert's parts
   // gather mode with misses: CTAs 0 .. gg-1 copy them, the others stream
-  const int gg = kGather && s_nl > 0 ? kDGCtas : 0;
-  const int Gf = G - gg, fb = (int)blockIdx.x - gg;
-  const int Lg = stream_len(n_list, NSRg, Gf, kNoCap), Ld = stream_len(n_list, NSRd, Gf, kNoCap);
-  const int bg = fb >= 0 ? fb * Lg : 0, eg_end = fb >= 0 ? min(bg + Lg, n_list * NSRg) : 0;
-  const int bd = fb >= 0 ? fb * Ld : 0, ed_end = fb >= 0 ? min(bd + Ld, n_list * NSRd) : 0;
+  const int nl = kGather ? s_nl : 0, nh = n_list - nl, nph = 1 + nl;
+  const int gg = nl > 0 ? kDGCtas : 0;
+  const int Gf = G - gg, fb = (int)blockIdx.x >= gg ? (int)blockIdx.x - gg : -1;
+  DecSched sg, sd;
+  sg.init(NSRg, nh, Gf, fb);
+  sd.init(NSRd, nh, Gf, fb);
   const int wbytes_g = 2 * I * kPK * 2, wbytes_d = H * kPK * 2;
   const int gpieces = kGather ? (int)((a.slab_vec + kDGPieceVec - 1) / kDGPieceVec) : 0;
-  if (Ld > a.hcap) {  // the host sizes the h area for the largest range: cannot happen
+  int n_down = 0;  // this CTA's down stages: the h area holds them
+  for (int p = 0; p < nph; ++p) {
+    int b, e;
+    sd.range(p, b, e);
+    n_down += max(e - b, 0);
+  }
+  const bool h_ok = n_down <= a.hcap;  // the host sizes the h area for the most a CTA can get
+  if (!h_ok) {
     if (tid == 0) set_status(a.status, MOE_DEV_BAD_GROUPS);
     s_abort = 1;
   }
@@ -420,54 +471,62 @@ __global__ void __launch_bounds__(kPThreads, 1) decode_layer_kernel(const Decode
         }
         return true;
       };
-      if (bg < eg_end)
-        stream_segments<kPN>(fa, NSRg, Lg, bg, eg_end, [&](const StreamSeg& g) {
-          if (!slab_ready(g.e)) return false;
-          int tok[kPMaxT];
-          for (int t = 0; t < g.nb; ++t) tok[t] = s_rows[g.p0 + t] / k;
-          for (int s = g.s_lo; s < g.s_hi; ++s, ++it) {
-            const int sl = it % a.nst;
-            const uint32_t use = it / a.nst;
-            if (!claim(sl, use)) return false;
-            unsigned char* dst = ring + sl * a.stride;
-            const int row0 = s * kPK;
-            mbar_expect_tx(&full[sl], wbytes_g + g.nb * 32);
-            tma_load_4d(dst, &mwg, &full[sl], 0, row0, 0, 3 * g.slot);
-            tma_load_4d(dst + wbytes_g / 2, &mwg, &full[sl], 0, row0, 0, 3 * g.slot + 1);
-            unsigned char* act = dst + wbytes_g;
-            for (int t = 0; t < g.nb; ++t) {
-              const uint16_t* xr = a.x + (size_t)tok[t] * H + row0;
-              bulk_load(act + t * 16, xr, 16, &full[sl]);
-              bulk_load(act + kPAct + t * 16, xr + 8, 16, &full[sl]);
-            }
-            last_use[sl] = (int)use;
+      auto gate_up = [&](const StreamSeg& g) {
+        if (!slab_ready(g.e)) return false;
+        int tok[kPMaxT];
+        for (int t = 0; t < g.nb; ++t) tok[t] = s_rows[g.p0 + t] / k;
+        for (int s = g.s_lo; s < g.s_hi; ++s, ++it) {
+          const int sl = it % a.nst;
+          const uint32_t use = it / a.nst;
+          if (!claim(sl, use)) return false;
+          unsigned char* dst = ring + sl * a.stride;
+          const int row0 = s * kPK;
+          mbar_expect_tx(&full[sl], wbytes_g + g.nb * 32);
+          tma_load_4d(dst, &mwg, &full[sl], 0, row0, 0, 3 * g.slot);
+          tma_load_4d(dst + wbytes_g / 2, &mwg, &full[sl], 0, row0, 0, 3 * g.slot + 1);
+          unsigned char* act = dst + wbytes_g;
+          for (int t = 0; t < g.nb; ++t) {
+            const uint16_t* xr = a.x + (size_t)tok[t] * H + row0;
+            bulk_load(act + t * 16, xr, 16, &full[sl]);
+            bulk_load(act + kPAct + t * 16, xr + 8, 16, &full[sl]);
           }
-          return true;
-        });
-      if (bd < ed_end)
-        stream_segments<kPN>(fa, NSRd, Ld, bd, ed_end, [&](const StreamSeg& g) {
-          if (!slab_ready(g.e)) return false;
-          for (int s = g.s_lo; s < g.s_hi; ++s, ++it) {
-            const int sl = it % a.nst;
-            const uint32_t use = it / a.nst;
-            if (!claim(sl, use)) return false;
-            mbar_expect_tx(&full[sl], wbytes_d);
-            tma_load_4d(ring + sl * a.stride, &mwd, &full[sl], 0, s * kPK, 0, 3 * g.slot + 2);
-            last_use[sl] = (int)use;
-          }
-          return true;
-        });
+          last_use[sl] = (int)use;
+        }
+        return true;
+      };
+      auto down = [&](const StreamSeg& g) {
+        if (!slab_ready(g.e)) return false;
+        for (int s = g.s_lo; s < g.s_hi; ++s, ++it) {
+          const int sl = it % a.nst;
+          const uint32_t use = it / a.nst;
+          if (!claim(sl, use)) return false;
+          mbar_expect_tx(&full[sl], wbytes_d);
+          tma_load_4d(ring + sl * a.stride, &mwd, &full[sl], 0, s * kPK, 0, 3 * g.slot + 2);
+          last_use[sl] = (int)use;
+        }
+        return true;
+      };
+      bool go = true;
+      for (int p = 0; p < nph && go; ++p) {
+        int b, e;
+        sg.range(p, b, e);
+        if (b < e) stream_segments<kPN>(fa, NSRg, sg.L, b, e, [&](const StreamSeg& g) { return go = gate_up(g); });
+        sd.range(p, b, e);
+        if (go && b < e) stream_segments<kPN>(fa, NSRd, sd.L, b, e, [&](const StreamSeg& g) { return go = down(g); });
+      }
       if (*abort_flag)  // let every copy issued land before the CTA moves on
         for (int s = 0; s < a.nst; ++s)
           if (last_use[s] >= 0) mbar_wait(&full[s], (uint32_t)last_use[s] & 1u);
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      for (int li = bg / NSRg; li * NSRg < eg_end && li < n_list; ++li) {
-        int e, slot;
-        if (!stream_slot(fa, li, e, slot)) set_status(a.status, MOE_DEV_BAD_SLOT);
-      }
+      if (blockIdx.x == 0)
+        for (int li = 0; li < n_list; ++li) {
+          int e, slot;
+          if (!stream_slot(fa, li, e, slot)) set_status(a.status, MOE_DEV_BAD_SLOT);
+        }
       uint32_t it = 0, seg = 0;
+      int dbase = 0;  // the phase's down stages are one contiguous range: local index = dbase + global index
       auto run = [&](const StreamSeg& g, bool down) {
         const uint32_t buf = seg & 1u, use = seg >> 1;
         if (use > 0 && !*abort_flag && !mbar_wait(&tempty[buf], (use - 1) & 1u)) {
@@ -477,7 +536,7 @@ __global__ void __launch_bounds__(kPThreads, 1) decode_layer_kernel(const Decode
         tc_fence_after();
         const uint32_t d = tmem + buf * 256u;
         const int ntiles = down ? H / kPM : Ng / kPM;
-        const int lbase = down ? s_li[g.e] * NSRd - bd : 0;
+        const int lbase = down ? dbase + s_li[g.e] * NSRd : 0;
         for (int s = g.s_lo; s < g.s_hi; ++s, ++it) {
           const int sl = it % a.nst;
           if (!*abort_flag && !mbar_wait(&full[sl], (it / a.nst) & 1u)) {
@@ -505,10 +564,17 @@ __global__ void __launch_bounds__(kPThreads, 1) decode_layer_kernel(const Decode
         ++seg;
         return true;
       };
-      if (bg < eg_end)
-        stream_segments<kPN>(fa, NSRg, Lg, bg, eg_end, [&](const StreamSeg& g) { return run(g, false); });
-      if (bd < ed_end)
-        stream_segments<kPN>(fa, NSRd, Ld, bd, ed_end, [&](const StreamSeg& g) { return run(g, true); });
+      int dl = 0;  // local index of the phase's first down stage (its h stage and barrier)
+      for (int p = 0; p < nph; ++p) {
+        int b, e;
+        sg.range(p, b, e);
+        if (b < e) stream_segments<kPN>(fa, NSRg, sg.L, b, e, [&](const StreamSeg& g) { return run(g, false); });
+        sd.range(p, b, e);
+        if (b >= e) continue;
+        dbase = dl - b;
+        stream_segments<kPN>(fa, NSRd, sd.L, b, e, [&](const StreamSeg& g) { return run(g, true); });
+        dl += e - b;
+      }
       umma_commit(done);  // every MMA issued has finished once `done` completes
       mbar_wait(done, 0);
     }
@@ -526,33 +592,43 @@ __global__ void __launch_bounds__(kPThreads, 1) decode_layer_kernel(const Decode
       if (!*abort_flag) {
         const int N = down ? H : Ng;
         unsigned long long* base = (down ? a.ysum : a.gsum) + (size_t)g.p0 * N + q * 32 + lane;
-        drain_tile(tmem + ((uint32_t)(q * 32) << 16) + buf * 256u, base, N / kPM, N, g.nb);
+        const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + buf * 256u;
+        if constexpr (kGather)
+          drain_tile_call(taddr, base, N / kPM, N, g.nb);
+        else
+          drain_tile(taddr, base, N / kPM, N, g.nb);
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[buf]);
       ++seg;
     };
-    if (bg < eg_end)
-      stream_segments<kPN>(fa, NSRg, Lg, bg, eg_end, [&](const StreamSeg& g) {
-        drain(g, false);
-        // publish this part of the expert's sums (the barrier orders every epilogue thread's atomics
-        // before the signalling thread's release)
-        named_sync(1, 128);
-        if (etid == 0) add_release(&a.ctr[s_li[g.e]], 1);
-        return true;
-      });
-    if (bd < ed_end) {
-      // h for this CTA's down stages, from the experts' gate/up sums once every part is in.  Every epilogue
-      // warp walks the same segments and reaches every named barrier; only the stores depend on
+    int dl = 0;  // local index of the phase's first down stage (its h stage and barrier)
+    for (int p = 0; p < nph; ++p) {
+      int bg, eg, bd, ed;
+      sg.range(p, bg, eg);
+      sd.range(p, bd, ed);
+      if (bg < eg)
+        stream_segments<kPN>(fa, NSRg, sg.L, bg, eg, [&](const StreamSeg& g) {
+          drain(g, false);
+          // publish this part of the expert's sums (the barrier orders every epilogue thread's atomics
+          // before the signalling thread's release)
+          named_sync(1, 128);
+          if (etid == 0) add_release(&a.ctr[s_li[g.e]], 1);
+          return true;
+        });
+      if (bd >= ed) continue;
+      // h for this phase's down stages, from the experts' gate/up sums once every part is in.  Every
+      // epilogue warp walks the same segments and reaches every named barrier; only the stores depend on
       // h_ok, which is the same for the whole CTA and never changes.
-      const bool h_ok = Ld <= a.hcap;
-      stream_segments<kPN>(fa, NSRd, Ld, bd, ed_end, [&](const StreamSeg& g) {
+      // the phase's down stages are one contiguous range: local index = dl + (global index - bd)
+      const int dbase = dl - bd;
+      stream_segments<kPN>(fa, NSRd, sd.L, bd, ed, [&](const StreamSeg& g) {
         const int li = s_li[g.e];
-        const int Jg = stream_parts(li, NSRg, Lg);
+        const int Jg = sg.parts(li);
         if (etid == 0 && !wait_count(&a.ctr[li], Jg, a.status)) *abort_flag = 1;
         named_sync(1, 128);
-        const int lbase = li * NSRd - bd;
+        const int lbase = dbase + li * NSRd;
         // (stage, row, token) elements of the batch's tokens, stage-major; lane pairs take the gate sum
         // (even lane) and the up sum (odd lane) of one element.  After each round the stages it
         // completed get their padding tokens (t >= nb, zeros) and go to the tensor cores.
@@ -605,10 +681,11 @@ __global__ void __launch_bounds__(kPThreads, 1) decode_layer_kernel(const Decode
         if (done_st < nst_seg) release(nst_seg);
         return true;
       });
-      stream_segments<kPN>(fa, NSRd, Ld, bd, ed_end, [&](const StreamSeg& g) {
+      stream_segments<kPN>(fa, NSRd, sd.L, bd, ed, [&](const StreamSeg& g) {
         drain(g, true);
         return true;
       });
+      dl += ed - bd;
     }
   }
   // warps 0 and 1 ran their loops on lane 0 alone: reconverge before the CTA barrier
@@ -688,10 +765,18 @@ struct DecPlan {
 
 static bool dec_plan(int T, int H, int E, int k, int I, int S, int sms, bool gather, DecPlan* p) {
   const int n = T * k, NSRd = I / kPK, lmax = std::min(n, E);
-  // the largest down range a streaming CTA can get (stream_len with every routed expert distinct)
+  // the most down stages a streaming CTA can get: a contiguous range of the hits' stages (stream_len with
+  // every routed expert distinct) plus, in gather mode, its share of the misses' runs, which go round the
+  // streaming CTAs one after another
   const int gf = sms - (gather ? kDGCtas : 0);
   if (gf < 1) return false;
-  p->hcap = (lmax * NSRd + gf - 1) / gf + 1;
+  int most = (lmax * NSRd + gf - 1) / gf;
+  if (gather) {
+    const int L1 = (NSRd + gf - 1) / gf, per = (NSRd + L1 - 1) / L1;
+    for (int nh = 0; nh <= lmax; ++nh)
+      most = std::max(most, (nh * NSRd + gf - 1) / gf + ((lmax - nh) * per + gf - 1) / gf * L1);
+  }
+  p->hcap = most + 1;
   const size_t hbytes = (std::max((size_t)p->hcap * kPHStage, (size_t)T * E * 8) + 15) & ~size_t(15);
   const size_t state = gather ? (size_t)4 * (E + 2 * S + kPMaxN) : 0;
   const size_t fixed = 1024 + hbytes + 8 * (2 * kPMaxStages + 5 + p->hcap) + state;
