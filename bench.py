@@ -759,7 +759,8 @@ def main():
     ap.add_argument("--no-variants", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--separate-kernels", action="store_true",
-                    help="single workloads: small all-resident steps run as separate kernels, not the persistent one")
+                    help="single workloads: small all-resident and small expert-cache steps run as separate kernels, "
+                         "not the persistent one")
     ap.add_argument("--workload", default="main",
                     help="main (default) | prefill | resident_T<n> | gather_T<n> | chunks_T<n> (each also as q8_<name>: "
                          "W8A8 experts) | routing_variants | "
