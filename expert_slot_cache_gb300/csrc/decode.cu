@@ -322,7 +322,9 @@ __global__ void __launch_bounds__(kPThreads, 1) decode_layer_kernel(const Decode
         s_act[i] = e;
         s_li[e] = i;
       }
-    if (blockIdx.x == 0) {
+    // a step whose wait gave up before this point leaves the state (and, its copying CTAs having given up
+    // too, the pool) as it was
+    if (blockIdx.x == 0 && !*abort_flag) {
       for (int e = tid; e < E; e += kPThreads) a.e2s_g[e] = st_e2s[e];
       for (int s = tid; s < a.S; s += kPThreads) {
         a.s2e_g[s] = st_s2e[s];
