@@ -28,7 +28,7 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
-def _pair(cfg, s2e0, affinity=0.0):
+def _pair(cfg, s2e0, affinity=0.0, rflags=0, sel_bias=None):
     """The persistent-kernel layer and the separate-kernel layer on the same inputs and starting state."""
     import expert_slot_cache_gb300 as M
     st = stage_layer(cfg)
@@ -41,13 +41,21 @@ def _pair(cfg, s2e0, affinity=0.0):
         state = M.CacheState.from_slots(s2e0, cfg.E)
         layers.append(M.SlotCachedMoELayer(st["wr"], pool, cfg.k, cfg.I, cfg.mode, cfg.policy, host_slabs=st["host"],
                                            state=state, logit_offset=st["logit_offset"], max_tokens=cfg.T,
-                                           affinity=affinity, decode_kernels=dk))
+                                           affinity=affinity, route_flags=rflags, sel_bias=sel_bias,
+                                           decode_kernels=dk))
     return st, layers
 
 
-def _steps(cfg, s2e0, xs, affinity=0.0):
+def _steps(cfg, s2e0, xs, affinity=0.0, rflags=0):
     """Runs the steps on both layers and the oracle; returns the misses of each step."""
-    st, (one, sep) = _pair(cfg, s2e0, affinity)
+    import expert_slot_cache_gb300 as M
+    bias_np = bias_d = None
+    if cfg.bias_cap is not None:
+        b, _ = C.draw_brightness(cfg)
+        bias_np = O.bias_table(b, cfg.n_hot, cfg.bias_cap, O.BIAS_GRADED)
+        bias_d = M.bias_table(torch.from_numpy(b).to(DEV), cfg.n_hot, cfg.bias_cap, mode=O.BIAS_GRADED)
+    router = O.ROUTER_SIGMOID if rflags & M.ROUTE_SIGMOID else O.ROUTER_SOFTMAX
+    st, (one, sep) = _pair(cfg, s2e0, affinity, rflags, bias_d)
     ostate = O.CacheState.from_slots(s2e0, cfg.E)
     wr_np = _np(st["wr"].float())
     off_np = None if st["logit_offset"] is None else _np(st["logit_offset"])
@@ -57,7 +65,8 @@ def _steps(cfg, s2e0, xs, affinity=0.0):
         r2 = sep.forward(x)
         torch.cuda.synchronize()
         want = O.layer_forward(_np(x.float()), wr_np, HostSlabs(st["host"]), cfg.H, cfg.I, cfg.k, cfg.mode,
-                               cfg.policy, ostate, None, off_np, affinity=affinity)
+                               cfg.policy, ostate, None, off_np, bias_np, affinity=affinity, router=router,
+                               damped=bool(rflags & M.ROUTE_DAMPED))
         assert np.array_equal(_np(r1["ids"]), want["ids"]), f"step {step}: ids"
         assert np.abs(_np(r1["w"]) - want["w"]).max() <= 1e-6, f"step {step}: w"
         assert torch.equal(r1["ids"], r2["ids"]) and torch.equal(r1["w"], r2["w"]), f"step {step}: routing"
@@ -133,6 +142,16 @@ def test_decode_gather_with_affinity():
     # live-cache affinity reads the cache state as it stood before the step's manage call
     cfg = C.qwen(8)
     _steps(cfg, C.initial_residency(cfg), [C.draw_x(cfg, DEV, step=s) for s in range(3)], affinity=0.5)
+
+
+@pytest.mark.parametrize("variant", ["softmax", "sigmoid", "damped"])
+def test_decode_gather_offset_bias_and_router_variants(variant):
+    # a per-expert logit offset, a graded selection bias, and the sigmoid router or damped weights
+    import expert_slot_cache_gb300 as M
+    rflags = {"softmax": 0, "sigmoid": M.ROUTE_SIGMOID, "damped": M.ROUTE_DAMPED}[variant]
+    cfg = C.TINY.with_(mode=C.MODE_GATHER, S=12, T=6, logit_offset=True, bias_cap=-0.5, n_hot=6, zipf_s=1.1,
+                       policy=C.POLICY_LFU if variant == "damped" else C.POLICY_LRU)
+    _steps(cfg, C.initial_residency(cfg), [C.draw_x(cfg, DEV, step=s) for s in range(4)], rflags=rflags)
 
 
 def test_decode_gather_tiny_and_widest_shapes():
