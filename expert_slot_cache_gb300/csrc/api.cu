@@ -258,14 +258,19 @@ extern "C" int moe_layer_forward(const moe_layer_args* a, moe_stream_t main_s, m
   prof.p = a->prof;
   if (prof.p) prof.p->used = 0;
   const size_t slab_bytes = a->quant ? q8_slab_bytes_h(H, I) : (size_t)6 * H * I;
-  if (mode == MOE_MODE_GATHER && !a->quant && !a->window_counts && a->decode_kernels == 0 && C >= T && ws.skp) {
+  if (mode == MOE_MODE_GATHER && !a->window_counts && a->decode_kernels == 0 && C >= T && ws.skp) {
     // a small expert-cache step: manage, gather and the whole layer in one persistent launch
     int dev = 0, sms = 0;
     MOE_CUDA_TRY(cudaGetDevice(&dev));
     MOE_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-    if (decode_gather_eligible(T, H, E, k, I, S, policy, a->x, a->w_router, a->pool, a->host_slabs, sms)) {
+    const bool bf = !a->quant && decode_gather_eligible(T, H, E, k, I, S, policy, a->x, a->w_router, a->pool,
+                                                        a->host_slabs, sms);
+    const bool q8 = a->quant && decode_q8_gather_eligible(T, H, E, k, I, S, policy, a->x, a->w_router, a->pool,
+                                                          a->host_slabs, sms);
+    if (bf || q8) {
       prof.begin(MOE_PROF_DECODE, ms);
-      const int rd = launch_decode_gather(a, ws.route, ws.logits, ws.skp, ws.skp_bytes, ws.ctr, ms);
+      const int rd = bf ? launch_decode_gather(a, ws.route, ws.logits, ws.skp, ws.skp_bytes, ws.ctr, ms)
+                        : launch_decode_q8_gather(a, ws.route, ws.logits, ws.skp, ws.skp_bytes, ws.ctr, ms);
       prof.end(ms);
       return rd;
     }

@@ -33,12 +33,22 @@
 //     per (output piece, pick) so that a piece's loads are one round trip.
 // Every wait is bounded (MOE_DEV_TIMEOUT); the last CTA out puts the counters
 // back to zero.
+//
+// Expert-cache steps (gather mode, T*k <= S, LRU or LFU) run in the same
+// launch as in the bf16 kernel: the cache state copied into shared memory
+// before the first grid-wide arrival, the manage state machine in every CTA
+// after the routing, CTA 0 writing the new state, 48 CTAs copying the misses'
+// slabs (codes and scales) host-to-slot, the other CTAs streaming in phases
+// (the hits as weighted contiguous ranges, then each miss in runs over all of
+// them).  A missing expert's scales are read with coherent loads once its copy
+// is complete (the copy writes them during the launch).
 #include <algorithm>
 #include <type_traits>
 
 #include "decode_route.cuh"
 #include "fp32def.cuh"
 #include "internal.cuh"
+#include "manage_core.cuh"
 #include "sched.cuh"
 
 namespace moe {
@@ -69,7 +79,25 @@ struct DecodeQ8Args {
   uint16_t* out;              // bf16 [T][H]
   int stride, nst;            // ring slot bytes and count
   int qd;                     // int32 quad-rows (4 weight rows) of Wd per down stage: qd * 4H <= stride
+  // gather mode only: the cache state (updated in place), the host store and the copy
+  int state_off;              // byte offset of the state's copy in dynamic shared memory
+  int32_t* e2s_g;
+  int32_t* s2e_g;
+  uint32_t* prio_g;
+  uint32_t* stamp_g;
+  int policy;
+  const uint4* host;          // mapped pinned host store, [E][slab]
+  uint4* pool_w;              // the slot pool, written by the copy
+  int64_t* stats;             // [0] += misses, [1] += 1, [2] += bytes copied, or NULL
 };
+
+// Gather mode: CTAs that copy the misses, and the piece one CTA copies at a time (four 16-byte loads in
+// flight per thread, twice over with the software pipeline).
+constexpr int kQGCtas = 48;
+constexpr int kQGUnroll = 4;
+constexpr int kQGPieceVec = kQDThreads * kQGUnroll;  // 16-byte units, 34 KB
+
+__device__ __forceinline__ void q8_fence_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 
 __device__ __forceinline__ int quad_of(const int4& v, int i) { return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w; }
 
@@ -115,6 +143,35 @@ __device__ __forceinline__ void q8d_segments(const FfnArgs& a, const int* wpre, 
   }
 }
 
+// One phase of a CTA's stream schedule.  Phase 0: list entries [0, nh) (all of them in resident mode),
+// weighted contiguous ranges over the Gf streaming CTAs (the schedule above); phase 1 + m (gather mode):
+// miss m, list entry nh + m, its NSR stages cut into `per` runs of L1 = ceil(NSR / Gf), run r on streaming
+// CTA (m * per + r) % Gf, so a miss streams on many CTAs as soon as its slab is in.  fb: this CTA among
+// the streaming CTAs, -1 for none.
+template <class F>
+__device__ __forceinline__ void q8d_phase(const FfnArgs& a, const int* wpre, int nh, int NSR, int Gf, int fb, int p,
+                                          F&& f) {
+  if (fb < 0) return;
+  if (p == 0) {
+    const int W = NSR * wpre[nh];  // products with Gf stay below 2^31
+    const int beg = fb * W / Gf, end = (fb + 1) * W / Gf;
+    if (beg < end) q8d_segments(a, wpre, nh, NSR, beg, end, f);
+    return;
+  }
+  const int L1 = (NSR + Gf - 1) / Gf, per = (NSR + L1 - 1) / L1;
+  const int m = p - 1, r = (fb - (m * per) % Gf + Gf) % Gf;
+  if (r >= per) return;
+  StreamSeg g;
+  if (!stream_slot(a, nh + m, g.e, g.slot)) return;
+  g.s_lo = r * L1;
+  g.s_hi = min(NSR, g.s_lo + L1);
+  g.j = 0;
+  g.p0 = a.offset[g.e];
+  g.nb = min(kQDRB, a.offset[g.e + 1] - g.p0);
+  f(g);
+}
+
+template <bool kGather>
 __global__ void __launch_bounds__(kQDThreads, 1) decode_q8_kernel(const DecodeQ8Args a) {
   extern __shared__ __align__(16) unsigned char qd_raw[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -134,8 +191,16 @@ __global__ void __launch_bounds__(kQDThreads, 1) decode_q8_kernel(const DecodeQ8
   __shared__ float s_sx[kQDMaxT], s_shr[kQDRB];
   __shared__ int tmp[33];
   __shared__ int s_nact, s_abort;
+  __shared__ int s_nh, s_nl;  // gather mode: hits, then misses, in the list
+  __shared__ uint32_t s_stamp;
   volatile int* abort_flag = &s_abort;
   int32_t* ctr = a.ctr;
+  int32_t* gctr = ctr + E + kQCtrCount;  // gather mode: pieces copied of miss m
+  // gather mode: the cache state's copy (e2s [E], s2e [S], prio [S]) and the misses' slots [kQDMaxN]
+  int* st_e2s = reinterpret_cast<int*>(qd_raw + a.state_off);
+  int* st_s2e = st_e2s + E;
+  uint32_t* st_prio = reinterpret_cast<uint32_t*>(st_s2e + a.S);
+  int* st_miss_s = reinterpret_cast<int*>(st_prio + a.S);
   if (tid == 0) {
     for (int s = 0; s < a.nst; ++s) {
       mbar_init(&full[s], 1);
@@ -144,7 +209,20 @@ __global__ void __launch_bounds__(kQDThreads, 1) decode_q8_kernel(const DecodeQ8
     s_abort = 0;
     mbar_fence_init();
   }
+  // ---- 0. gather mode: the cache state as it stands, read before this CTA's phase-1 arrival (CTA 0
+  // writes the new state only once every CTA has arrived) -----------------------------------------
+  if constexpr (kGather) {
+    for (int e = tid; e < E; e += kQDThreads) st_e2s[e] = a.e2s_g[e];
+    for (int s = tid; s < a.S; s += kQDThreads) {
+      st_s2e[s] = a.s2e_g[s];
+      st_prio[s] = a.prio_g[s];
+    }
+    if (tid == 0) s_stamp = *a.stamp_g;
+  }
   __syncthreads();
+  RouteIO rio_g = a.r;
+  if constexpr (kGather) rio_g.e2s = st_e2s;  // live-cache affinity reads the state before this step's manage
+  const RouteIO& rio = kGather ? rio_g : a.r;
 
   // ---- 1. router logits; zero the accumulators; the tokens' codes ---------------------------
   {
@@ -163,7 +241,7 @@ __global__ void __launch_bounds__(kQDThreads, 1) decode_q8_kernel(const DecodeQ8
   const int units = (H / 128) * ((E + 31) / 32) * T;
   const int busy = min(kQDThreads / 32, max(0, (units - (int)blockIdx.x + G - 1) / G));
   if (warp < busy) {
-    route_logit_parts<kQDThreads>(a.r, ring);
+    route_logit_parts<kQDThreads>(rio, ring);
     named_sync(3, busy * 32);
     if (tid == 0) add_release(&ctr[E + kQCtrLogits], 1);  // the barriers order the CTA's stores before it
   } else {
@@ -214,7 +292,53 @@ __global__ void __launch_bounds__(kQDThreads, 1) decode_q8_kernel(const DecodeQ8
     float* slog = reinterpret_cast<float*>(ring);
     const RouteSm rsm{slog, slog + T * E, s_ids, s_w, s_cnt, s_off, s_act, s_li, s_rows, s_pos, tmp, &s_nact,
                       abort_flag};
-    route_pick_group<kQDThreads>(a.r, rsm);
+    route_pick_group<kQDThreads>(rio, rsm);
+  }
+
+  // ---- 2b. gather mode: the manage state machine on this CTA's copy of the state ---------------
+  if constexpr (kGather) {
+    __syncthreads();  // the ring's logits and scores are read: its first bytes take the work arrays
+    int* mrank = reinterpret_cast<int*>(ring);
+    int* hrank = mrank + E;
+    int* cand = hrank + E;
+    int* vict = cand + a.S;
+    int* hit_t = vict + a.S;
+    int* miss_t = hit_t + kQDMaxN;
+    const uint32_t stamp = s_stamp + 1u;
+    const ManageCounts mc = manage_block(E, a.S, a.policy, false, stamp, s_cnt, st_e2s, st_s2e, st_prio, mrank,
+                                         hrank, cand, vict, hit_t, miss_t, st_miss_s, nullptr, nullptr, a.r.status);
+    // the list: hits (ascending id), then the misses in load order (ascending id)
+    const bool ok = mc.nh + mc.nl == s_nact && mc.nl <= kQDMaxN;
+    if (ok)
+      for (int i = tid; i < s_nact; i += kQDThreads) {
+        const int e = i < mc.nh ? hit_t[i] : miss_t[i - mc.nh];
+        s_act[i] = e;
+        s_li[e] = i;
+      }
+    // a step whose wait gave up before this point leaves the state (and the pool) as it was
+    if (blockIdx.x == 0 && !*abort_flag) {
+      for (int e = tid; e < E; e += kQDThreads) a.e2s_g[e] = st_e2s[e];
+      for (int s = tid; s < a.S; s += kQDThreads) {
+        a.s2e_g[s] = st_s2e[s];
+        a.prio_g[s] = st_prio[s];
+      }
+      if (tid == 0) {
+        *a.stamp_g = stamp;
+        if (a.stats) {
+          a.stats[0] += mc.nl;
+          a.stats[1] += 1;
+          a.stats[2] += (int64_t)mc.nl * (int64_t)a.qslab;
+        }
+      }
+    }
+    if (tid == 0) {
+      s_nh = mc.nh;
+      s_nl = ok ? mc.nl : 0;
+      if (!ok) {
+        set_status(a.r.status, MOE_DEV_BAD_SLOT);
+        s_abort = 1;
+      }
+    }
   }
   fence_async_smem();  // the ring's router bytes are overwritten by bulk copies next
   __syncthreads();
@@ -223,7 +347,7 @@ __global__ void __launch_bounds__(kQDThreads, 1) decode_q8_kernel(const DecodeQ8
   FfnArgs fa{};
   fa.E = E;
   fa.S = a.S;
-  fa.e2s = a.r.e2s;
+  fa.e2s = kGather ? st_e2s : a.r.e2s;
   fa.list_e = s_act;
   fa.offset = s_off;
   const int n_list = s_nact;
@@ -237,10 +361,75 @@ __global__ void __launch_bounds__(kQDThreads, 1) decode_q8_kernel(const DecodeQ8
     if (tid == 0) s_wpre[n_list] = tot;
   }
   __syncthreads();
-  const int Wg = NSRg * s_wpre[n_list], Wd = NSRd * s_wpre[n_list];  // products with G stay below 2^31
+  // gather mode with misses: CTAs 0 .. gg-1 copy them, the others stream in phases
+  const int nl = kGather ? s_nl : 0, nh = n_list - nl, nph = 1 + nl;
+  const int gg = nl > 0 ? kQGCtas : 0;
+  const int Gf = G - gg, fb = (int)blockIdx.x >= gg ? (int)blockIdx.x - gg : -1;
+  const int wb_g = kQDK * I, wb_d = a.qd * 4 * H;  // bytes of one stage piece: Wg (or Wu), Wd
+  const int Wg = NSRg * s_wpre[n_list], Wd = NSRd * s_wpre[n_list];  // resident mode: one phase
   const int bg = (int)(blockIdx.x * Wg / G), eg_end = (int)((blockIdx.x + 1) * Wg / G);
   const int bd = (int)(blockIdx.x * Wd / G), ed_end = (int)((blockIdx.x + 1) * Wd / G);
-  const int wb_g = kQDK * I, wb_d = a.qd * 4 * H;  // bytes of one stage piece: Wg (or Wu), Wd
+  const size_t slab_vec = a.qslab / 16;
+  const int gpieces = kGather ? (int)((slab_vec + kQGPieceVec - 1) / kQGPieceVec) : 0;
+
+  // ---- 3'. gather mode: the copying CTAs, miss after miss (the next piece's host loads in flight while
+  // this piece is stored, fenced and released) ------------------------------------------------------
+  if constexpr (kGather) {
+    if ((int)blockIdx.x < gg && !*abort_flag) {
+      const int items = nl * gpieces;
+      auto piece = [&](int it, const uint4*& src, uint4*& dst, size_t& lim) {
+        const int m = it / gpieces, c = it - m * gpieces;
+        const int e = s_act[nh + m], sl = st_miss_s[m];
+        if (e < 0 || e >= E || sl < 0 || sl >= a.S) {
+          if (tid == 0) set_status(a.r.status, e < 0 || e >= E ? MOE_DEV_BAD_EXPERT : MOE_DEV_BAD_SLOT);
+          return false;
+        }
+        src = a.host + (size_t)e * slab_vec + (size_t)c * kQGPieceVec;
+        dst = a.pool_w + (size_t)sl * slab_vec + (size_t)c * kQGPieceVec;
+        lim = min((size_t)kQGPieceVec, slab_vec - (size_t)c * kQGPieceVec);
+        return true;
+      };
+      uint4 v[kQGUnroll], nv[kQGUnroll];
+      const uint4* src = nullptr;
+      uint4* dst = nullptr;
+      size_t lim = 0;
+      bool ok = (int)blockIdx.x < items && piece(blockIdx.x, src, dst, lim);
+      if (ok)
+#pragma unroll
+        for (int u = 0; u < kQGUnroll; ++u) {
+          const size_t j = tid + (size_t)u * kQDThreads;
+          if (j < lim) v[u] = ldg_stream(src + j);
+        }
+      for (int it = blockIdx.x; it < items; it += gg) {
+        const int nx = it + gg;
+        const uint4* nsrc = nullptr;
+        uint4* ndst = nullptr;
+        size_t nlim = 0;
+        const bool nok = nx < items && piece(nx, nsrc, ndst, nlim);
+        if (nok)
+#pragma unroll
+          for (int u = 0; u < kQGUnroll; ++u) {
+            const size_t j = tid + (size_t)u * kQDThreads;
+            if (j < nlim) nv[u] = ldg_stream(nsrc + j);
+          }
+        if (ok) {
+#pragma unroll
+          for (int u = 0; u < kQGUnroll; ++u) {
+            const size_t j = tid + (size_t)u * kQDThreads;
+            if (j < lim) dst[j] = v[u];
+          }
+          q8_fence_async_global();  // the piece is read next by other CTAs' bulk copies
+        }
+        __syncthreads();
+        if (tid == 0) add_release(&gctr[it / gpieces], 1);  // the barrier orders every thread's stores before it
+#pragma unroll
+        for (int u = 0; u < kQGUnroll; ++u) v[u] = nv[u];
+        ok = nok;
+        dst = ndst;
+        lim = nlim;
+      }
+    }
+  }
 
   if (warp == kQDConsumers / 32) {
     if (lane == 0) {
@@ -254,34 +443,60 @@ __global__ void __launch_bounds__(kQDThreads, 1) decode_q8_kernel(const DecodeQ8
         }
         return !*abort_flag;
       };
-      if (bg < eg_end)
-        q8d_segments(fa, s_wpre, n_list, NSRg, bg, eg_end, [&](const StreamSeg& g) {
-          const unsigned char* w = a.pool + (size_t)g.slot * a.qslab;
-          for (int s = g.s_lo; s < g.s_hi; ++s, ++it) {
-            const int sl = it % a.nst;
-            const uint32_t use = it / a.nst;
-            if (!claim(sl, use)) return false;
-            unsigned char* dst = ring + sl * a.stride;
-            mbar_expect_tx(&full[sl], 2 * wb_g);
-            bulk_load(dst, w + (size_t)s * wb_g, wb_g, &full[sl]);
-            bulk_load(dst + wb_g, w + mat + (size_t)s * wb_g, wb_g, &full[sl]);
-            last_use[sl] = (int)use;
+      // gather mode: a missing expert's slot is read once all of its pieces are in (bit m: miss m seen complete)
+      uint64_t seen = 0;
+      auto slab_ready = [&](int e) {
+        if constexpr (kGather) {
+          const int m = s_li[e] - nh;
+          if (m < 0 || m >= kQDMaxN || ((seen >> m) & 1ull)) return true;
+          if (*abort_flag) return false;
+          if (!wait_count(&gctr[m], gpieces, a.r.status)) {
+            *abort_flag = 1;
+            return false;
           }
-          return true;
-        });
-      if (bd < ed_end)
-        q8d_segments(fa, s_wpre, n_list, NSRd, bd, ed_end, [&](const StreamSeg& g) {
-          const unsigned char* w = a.pool + (size_t)g.slot * a.qslab + 2 * mat;
-          for (int s = g.s_lo; s < g.s_hi; ++s, ++it) {
-            const int sl = it % a.nst;
-            const uint32_t use = it / a.nst;
-            if (!claim(sl, use)) return false;
-            mbar_expect_tx(&full[sl], wb_d);
-            bulk_load(ring + sl * a.stride, w + (size_t)s * wb_d, wb_d, &full[sl]);
-            last_use[sl] = (int)use;
-          }
-          return true;
-        });
+          q8_fence_async_global();  // the copy's generic stores before this thread's bulk copies of the slot
+          seen |= 1ull << m;
+        }
+        return true;
+      };
+      auto gate_up = [&](const StreamSeg& g) {
+        if (!slab_ready(g.e)) return false;
+        const unsigned char* w = a.pool + (size_t)g.slot * a.qslab;
+        for (int s = g.s_lo; s < g.s_hi; ++s, ++it) {
+          const int sl = it % a.nst;
+          const uint32_t use = it / a.nst;
+          if (!claim(sl, use)) return false;
+          unsigned char* dst = ring + sl * a.stride;
+          mbar_expect_tx(&full[sl], 2 * wb_g);
+          bulk_load(dst, w + (size_t)s * wb_g, wb_g, &full[sl]);
+          bulk_load(dst + wb_g, w + mat + (size_t)s * wb_g, wb_g, &full[sl]);
+          last_use[sl] = (int)use;
+        }
+        return true;
+      };
+      auto down = [&](const StreamSeg& g) {
+        if (!slab_ready(g.e)) return false;
+        const unsigned char* w = a.pool + (size_t)g.slot * a.qslab + 2 * mat;
+        for (int s = g.s_lo; s < g.s_hi; ++s, ++it) {
+          const int sl = it % a.nst;
+          const uint32_t use = it / a.nst;
+          if (!claim(sl, use)) return false;
+          mbar_expect_tx(&full[sl], wb_d);
+          bulk_load(ring + sl * a.stride, w + (size_t)s * wb_d, wb_d, &full[sl]);
+          last_use[sl] = (int)use;
+        }
+        return true;
+      };
+      if constexpr (!kGather) {
+        if (bg < eg_end) q8d_segments(fa, s_wpre, n_list, NSRg, bg, eg_end, gate_up);
+        if (bd < ed_end) q8d_segments(fa, s_wpre, n_list, NSRd, bd, ed_end, down);
+      } else {
+        bool go = true;
+        for (int p = 0; p < nph && go; ++p) {
+          q8d_phase(fa, s_wpre, nh, NSRg, Gf, fb, p, [&](const StreamSeg& g) { return go = gate_up(g); });
+          if (go) q8d_phase(fa, s_wpre, nh, NSRd, Gf, fb, p, [&](const StreamSeg& g) { return go = down(g); });
+        }
+      }
       if (*abort_flag)  // let every copy issued land before the CTA moves on
         for (int s = 0; s < a.nst; ++s)
           if (last_use[s] >= 0) mbar_wait(&full[s], (uint32_t)last_use[s] & 1u);
@@ -306,8 +521,7 @@ __global__ void __launch_bounds__(kQDThreads, 1) decode_q8_kernel(const DecodeQ8
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[sl]);
     };
-    if (bg < eg_end)
-      q8d_segments(fa, s_wpre, n_list, NSRg, bg, eg_end, [&](const StreamSeg& g) {
+    auto cons_gate_up = [&](const StreamSeg& g) {
         // the stage loop for RB >= nb rows (rows past nb take token 0's codes and are not kept); RB is a
         // compile-time count, so a one-row expert costs one code load and 16 dp4a per stage
         auto stages = [&](auto rbc) {
@@ -359,40 +573,46 @@ __global__ void __launch_bounds__(kQDThreads, 1) decode_q8_kernel(const DecodeQ8
         named_sync(1, kQDConsumers);
         if (c == 0) add_release(&ctr[s_li[g.e]], g.s_hi - g.s_lo);
         return true;
-      });
-    if (bd < ed_end)
-      q8d_segments(fa, s_wpre, n_list, NSRd, bd, ed_end, [&](const StreamSeg& g) {
+      };
+    auto cons_down = [&](const StreamSeg& g) {
         const int li = s_li[g.e], nb = g.nb, nit = nb * IQ;
         // h of the segment's rows from the gate/up sums: items (row, quad), up to four per thread, two at a
         // time.  The first two items' scales do not depend on h: they are loaded before the wait for the
         // expert's parts.
         const float4* sc4 = reinterpret_cast<const float4*>(a.pool + (size_t)g.slot * a.qslab + 3 * mat);
         float4 sg4[2], su4[2];
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int v = c + kQDConsumers * u;
-          if (v < nit) {
-            const int q = v % IQ;
+        // gather mode: a missing expert's scales are written by this launch's copy, so they are read
+        // (coherently) once the copy is complete; a hit's are in place and go the read-only path early
+        const bool late = kGather && li >= nh;
+        auto load_sc = [&](int u, int v) {
+          const int q = v % IQ;
+          if (kGather && late) {
+            sg4[u] = __ldcg(sc4 + q);
+            su4[u] = __ldcg(sc4 + IQ + q);
+          } else {
             sg4[u] = __ldg(sc4 + q);
             su4[u] = __ldg(sc4 + IQ + q);
           }
+        };
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int v = c + kQDConsumers * u;
+          if (v < nit && !(kGather && late)) load_sc(u, v);
         }
         if (c == 0 && !*abort_flag && !wait_count(&ctr[li], NSRg, a.r.status)) *abort_flag = 1;
+        if (kGather && late && c == 0 && !*abort_flag && !wait_count(&gctr[li - nh], gpieces, a.r.status))
+          *abort_flag = 1;
         if (c < kQDRB) s_amax[c] = 0u;
         named_sync(1, kQDConsumers);
         const bool ok = !*abort_flag;
         float hv[4][4];
 #pragma unroll
         for (int u0 = 0; u0 < 4; u0 += 2) {
-          if (u0 > 0) {
+          if (u0 > 0 || (kGather && late)) {
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
               const int v = c + kQDConsumers * (u0 + u);
-              if (v < nit) {
-                const int q = v % IQ;
-                sg4[u] = __ldg(sc4 + q);
-                su4[u] = __ldg(sc4 + IQ + q);
-              }
+              if (v < nit) load_sc(u, v);
             }
           }
           int4 gi[2], ui[2];
@@ -485,7 +705,19 @@ __global__ void __launch_bounds__(kQDThreads, 1) decode_q8_kernel(const DecodeQ8
         else if (nb <= 4) stages(std::integral_constant<int, 4>{});
         else stages(std::integral_constant<int, 8>{});
         return true;
-      });
+      };
+    if constexpr (!kGather) {
+      if (bg < eg_end) q8d_segments(fa, s_wpre, n_list, NSRg, bg, eg_end, cons_gate_up);
+      if (bd < ed_end) q8d_segments(fa, s_wpre, n_list, NSRd, bd, ed_end, cons_down);
+    } else {
+      q8d_phase(fa, s_wpre, nh, NSRg, Gf, fb, 0, cons_gate_up);
+      q8d_phase(fa, s_wpre, nh, NSRd, Gf, fb, 0, cons_down);
+#pragma unroll 1
+      for (int p = 1; p < nph; ++p) {
+        q8d_phase(fa, s_wpre, nh, NSRg, Gf, fb, p, cons_gate_up);
+        q8d_phase(fa, s_wpre, nh, NSRd, Gf, fb, p, cons_down);
+      }
+    }
   }
   // ---- 5. combine: (token, column quad) items dealt round-robin over the grid, one thread per (item,
   // pick); a pick's scales are loaded before the grid-wide wait, its sums and row scale after it, and
@@ -495,16 +727,18 @@ __global__ void __launch_bounds__(kQDThreads, 1) decode_q8_kernel(const DecodeQ8
   const bool cu = !*abort_flag && tid < my_items * k;  // the host checks my_items * k <= kQDThreads
   const int cm = cu ? tid / k : 0, cj = tid - cm * k;
   const int citem = (int)blockIdx.x + G * cm, ct = citem / nc4, cc4 = citem - ct * nc4;
-  int cpos = 0;
+  int cpos = 0, cslot = 0;
   bool chave = false;
   float4 csd = make_float4(0.f, 0.f, 0.f, 0.f);
   if (cu) {
     const int i = ct * k + cj, e = s_ids[i];
-    const int slot = a.r.e2s ? a.r.e2s[e] : e;
+    const int slot = kGather ? st_e2s[e] : a.r.e2s ? a.r.e2s[e] : e;
     chave = slot >= 0 && slot < a.S;
     cpos = s_pos[i];
-    if (chave)
+    // gather mode: after the grid-wide wait (every copy is complete by then), coherently
+    if (chave && !kGather)
       csd = __ldg(reinterpret_cast<const float4*>(a.pool + (size_t)slot * a.qslab + 3 * mat) + (2 * I) / 4 + cc4);
+    if constexpr (kGather) cslot = slot;
   }
   // the loader ran its loops on lane 0 alone: reconverge before the CTA barrier
   __syncwarp();
@@ -514,6 +748,9 @@ __global__ void __launch_bounds__(kQDThreads, 1) decode_q8_kernel(const DecodeQ8
     if (!wait_count(&ctr[E + kQCtrDown], G, a.r.status)) s_abort = 1;
   }
   __syncthreads();
+  if constexpr (kGather)
+    if (cu && chave)
+      csd = __ldcg(reinterpret_cast<const float4*>(a.pool + (size_t)cslot * a.qslab + 3 * mat) + (2 * I) / 4 + cc4);
   float4* sy = reinterpret_cast<float4*>(ring);  // every stage has landed and been read: the ring is free
   if (cu) {
     float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -546,7 +783,7 @@ __global__ void __launch_bounds__(kQDThreads, 1) decode_q8_kernel(const DecodeQ8
   // the last CTA out resets the counters: every other CTA is past its last wait
   __syncthreads();
   if (tid == 0 && atomicAdd(&ctr[E + kQCtrExit], 1) == G - 1)
-    for (int i = 0; i < E + kQCtrCount; ++i) ctr[i] = 0;
+    for (int i = 0; i < E + kQCtrCount + (kGather ? kQDMaxN : 0); ++i) ctr[i] = 0;
 }
 
 // ---------------------------------------------------------------------------
@@ -563,6 +800,30 @@ static int qd_quads(int H, int I) {
   return q;
 }
 
+// Dynamic shared memory of one launch: x codes | ring | gather mode: the cache state's copy.
+struct QdPlan {
+  int nst = 0, state_off = 0;
+  size_t smem = 0;
+};
+
+static bool qd_plan(int T, int H, int E, int I, int S, bool gather, QdPlan* p) {
+  const size_t xq = ((size_t)T * H + 127) & ~size_t(127), fixed = xq + 128;
+  const size_t state = gather ? (size_t)4 * (E + 2 * S + kQDMaxN) : 0;
+  const int stride = qd_stride(H, I);
+  if (fixed + state >= (size_t)kQDSmemMax) return false;
+  p->nst = (int)std::min<size_t>(kQDMaxStages, (kQDSmemMax - fixed - state) / stride);
+  if (p->nst < 2) return false;
+  const size_t staging = (size_t)(kQDThreads / 32) * kRStage, route = (size_t)2 * T * E * 4;
+  // the ring also holds the router's staging, the logits and scores, the combine's values and, in gather
+  // mode, the manage call's work arrays
+  size_t ring = std::max((size_t)p->nst * stride, std::max(staging, std::max(route, (size_t)16 * kQDThreads)));
+  if (gather) ring = std::max(ring, (size_t)4 * (2 * E + 2 * S + 2 * kQDMaxN));
+  ring = (ring + 15) & ~size_t(15);
+  p->state_off = (int)(xq + ring);
+  p->smem = fixed + ring + state;
+  return p->smem <= (size_t)kQDSmemMax;
+}
+
 bool decode_q8_eligible(int T, int H, int E, int k, int I, int S, const void* x, const void* wr, const void* pool,
                         int sms) {
   const int n = T * k;
@@ -574,10 +835,19 @@ bool decode_q8_eligible(int T, int H, int E, int k, int I, int S, const void* x,
   if ((H / 128) * ((E + 31) / 32) * T > (kQDThreads / 32 - 4) * sms) return false;
   // the combine gives each CTA's (item, pick) pairs one thread each
   if (((T * H / 4 + sms - 1) / sms) * k > kQDThreads) return false;
-  const size_t fixed = (((size_t)T * H + 127) & ~size_t(127)) + 128;
-  const size_t staging = (size_t)(kQDThreads / 32) * kRStage, route = (size_t)2 * T * E * 4;
-  const size_t ring = std::max(2 * (size_t)qd_stride(H, I), std::max(staging, std::max(route, (size_t)16 * kQDThreads)));
-  return fixed + ring <= (size_t)kQDSmemMax;
+  QdPlan p;
+  return qd_plan(T, H, E, I, S, false, &p);
+}
+
+bool decode_q8_gather_eligible(int T, int H, int E, int k, int I, int S, int policy, const void* x, const void* wr,
+                               const void* pool, const void* host, int sms) {
+  if (!decode_q8_eligible(T, H, E, k, I, S, x, wr, pool, sms)) return false;
+  if (policy != MOE_POLICY_LRU && policy != MOE_POLICY_LFU) return false;
+  // T*k <= S: every miss finds a victim among the slots the step does not need (one manage call)
+  if (T * k > S || S > kQDMaxE || (uintptr_t)host % 16 || q8_slab_bytes_h(H, I) % 16) return false;
+  if (sms < 2 * kQGCtas) return false;  // at least as many streaming CTAs as copying ones
+  QdPlan p;
+  return qd_plan(T, H, E, I, S, true, &p);
 }
 
 size_t decode_q8_ws_bytes(int T, int k, int H, int I) {
@@ -585,18 +855,22 @@ size_t decode_q8_ws_bytes(int T, int k, int H, int I) {
   return qd_al(n * 2 * I * 4) + qd_al(n * H * 4) + qd_al(n * 4);
 }
 
-int launch_decode_q8(const moe_layer_args* la, float* lpart, float* logits, void* ws, size_t ws_bytes, int32_t* ctr,
-                     cudaStream_t stream) {
+template <bool kGather>
+static int launch_decode_q8_impl(const moe_layer_args* la, float* lpart, float* logits, void* ws, size_t ws_bytes,
+                                 int32_t* ctr, cudaStream_t stream) {
   const int T = la->T, H = la->H, E = la->E, k = la->k, I = la->I, n = T * k;
   int dev = 0, sms = 0;
   MOE_CUDA_TRY(cudaGetDevice(&dev));
   MOE_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-  if (!decode_q8_eligible(T, H, E, k, I, la->S, la->x, la->w_router, la->pool, sms)) return MOE_ERR_ARG;
+  if (kGather ? !decode_q8_gather_eligible(T, H, E, k, I, la->S, la->policy, la->x, la->w_router, la->pool,
+                                           la->host_slabs, sms)
+              : !decode_q8_eligible(T, H, E, k, I, la->S, la->x, la->w_router, la->pool, sms))
+    return MOE_ERR_ARG;
   if (!ws || ws_bytes < decode_q8_ws_bytes(T, k, H, I) || (uintptr_t)ws % 256) return MOE_ERR_ALIGN;
   DecodeQ8Args a{};
-  a.r = RouteIO{(const uint16_t*)la->x, (const uint16_t*)la->w_router, la->logit_offset, la->sel_bias, la->e2s,
-                la->affinity, la->route_flags, T, H, E, k, lpart, logits, la->ids, la->w,
-                ctr + E + kQCtrRoute, la->dev_status};
+  a.r = RouteIO{(const uint16_t*)la->x, (const uint16_t*)la->w_router, la->logit_offset, la->sel_bias,
+                kGather ? nullptr : la->e2s, la->affinity, la->route_flags, T, H, E, k, lpart, logits, la->ids,
+                la->w, ctr + E + kQCtrRoute, la->dev_status};
   a.I = I;
   a.S = la->S;
   a.pool = (const unsigned char*)la->pool;
@@ -611,31 +885,48 @@ int launch_decode_q8(const moe_layer_args* la, float* lpart, float* logits, void
   a.out = (uint16_t*)la->out;
   a.stride = qd_stride(H, I);
   a.qd = qd_quads(H, I);
-  const size_t fixed = (((size_t)T * H + 127) & ~size_t(127)) + 128;
-  a.nst = (int)std::min<size_t>(kQDMaxStages, (kQDSmemMax - fixed) / a.stride);
-  if (a.nst < 2) return MOE_ERR_ARG;
-  const size_t staging = (size_t)(kQDThreads / 32) * kRStage, route = (size_t)2 * T * E * 4;
-  // the ring also holds the router's staging, the logits and scores, and the combine's values
-  const size_t ring = std::max((size_t)a.nst * a.stride, std::max(staging, std::max(route, (size_t)16 * kQDThreads)));
-  const size_t smem = fixed + ring;
-  if (smem > (size_t)kQDSmemMax) return MOE_ERR_ARG;
+  if constexpr (kGather) {
+    if (!la->e2s || !la->s2e || !la->prio || !la->stamp || !la->host_slabs) return MOE_ERR_ARG;
+    a.e2s_g = la->e2s;
+    a.s2e_g = la->s2e;
+    a.prio_g = la->prio;
+    a.stamp_g = la->stamp;
+    a.policy = la->policy;
+    a.host = (const uint4*)la->host_slabs;
+    a.pool_w = (uint4*)la->pool;
+    a.stats = la->stats;
+  }
+  QdPlan p;
+  if (!qd_plan(T, H, E, I, la->S, kGather, &p)) return MOE_ERR_ARG;
+  a.nst = p.nst;
+  a.state_off = p.state_off;
   static bool attr[64] = {};
-  MOE_CUDA_TRY(ensure_smem(decode_q8_kernel, kQDSmemMax, attr));
+  MOE_CUDA_TRY(ensure_smem(decode_q8_kernel<kGather>, kQDSmemMax, attr));
   int occ = 0;
-  MOE_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, decode_q8_kernel, kQDThreads, smem));
+  MOE_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, decode_q8_kernel<kGather>, kQDThreads, p.smem));
   if (occ < 1) return MOE_ERR_ARG;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(sms);
   cfg.blockDim = dim3(kQDThreads);
-  cfg.dynamicSmemBytes = smem;
+  cfg.dynamicSmemBytes = p.smem;
   cfg.stream = stream;
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeCooperative;
   at[0].val.cooperative = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  MOE_CUDA_TRY(cudaLaunchKernelEx(&cfg, decode_q8_kernel, a));
+  MOE_CUDA_TRY(cudaLaunchKernelEx(&cfg, decode_q8_kernel<kGather>, a));
   return MOE_OK;
+}
+
+int launch_decode_q8(const moe_layer_args* la, float* lpart, float* logits, void* ws, size_t ws_bytes, int32_t* ctr,
+                     cudaStream_t stream) {
+  return launch_decode_q8_impl<false>(la, lpart, logits, ws, ws_bytes, ctr, stream);
+}
+
+int launch_decode_q8_gather(const moe_layer_args* la, float* lpart, float* logits, void* ws, size_t ws_bytes,
+                            int32_t* ctr, cudaStream_t stream) {
+  return launch_decode_q8_impl<true>(la, lpart, logits, ws, ws_bytes, ctr, stream);
 }
 
 }  // namespace moe

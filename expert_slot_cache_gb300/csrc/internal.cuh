@@ -139,6 +139,12 @@ bool decode_q8_eligible(int T, int H, int E, int k, int I, int S, const void* x,
 size_t decode_q8_ws_bytes(int T, int k, int H, int I);
 int launch_decode_q8(const moe_layer_args* la, float* lpart, float* logits, void* ws, size_t ws_bytes, int32_t* ctr,
                      cudaStream_t stream);
+// Its expert-cache step (GATHER, T*k <= S, LRU / LFU): manage, the copy of the misses (codes and scales)
+// and the streams in the one launch.
+bool decode_q8_gather_eligible(int T, int H, int E, int k, int I, int S, int policy, const void* x, const void* wr,
+                               const void* pool, const void* host, int sms);
+int launch_decode_q8_gather(const moe_layer_args* la, float* lpart, float* logits, void* ws, size_t ws_bytes,
+                            int32_t* ctr, cudaStream_t stream);
 int route_impl(const void* x, const void* w_router, const float* logit_offset, const float* sel_bias,
                const int32_t* e2s, float affinity, int rflags, int T, int H, int E, int k, float* logits,
                float* scratch, int32_t* ids, float* w, cudaStream_t stream, const PermOut* perm, bool* fused);

@@ -23,30 +23,38 @@ import oracle as O
 from harness import configs as C
 from tests._setup import HostSlabs, assert_out_close, stage_layer
 from tests.test_gpu_parity import _check_state, _np
+from tests.test_gpu_q8 import QHost
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
-def _pair(cfg, s2e0, affinity=0.0, rflags=0, sel_bias=None):
-    """The persistent-kernel layer and the separate-kernel layer on the same inputs and starting state."""
+def _pair(cfg, s2e0, affinity=0.0, rflags=0, sel_bias=None, quant=0):
+    """The persistent-kernel layer and the separate-kernel layer on the same inputs and starting state
+    (W8A8 slabs, codes and scales, with quant=1)."""
     import expert_slot_cache_gb300 as M
     st = stage_layer(cfg)
+    src, host = st["slabs_dev"], st["host"]
+    if quant:
+        src = M.quantize_slabs(st["slabs_dev"], cfg.H, cfg.I)
+        host = torch.empty(src.shape, dtype=src.dtype, pin_memory=True)
+        host.copy_(src)
+        st["host_q"] = host
     layers = []
     for dk in (0, 1):
-        pool = torch.zeros(cfg.S, cfg.slab_elems, dtype=torch.bfloat16, device=DEV)
+        pool = torch.zeros(cfg.S, src.shape[1], dtype=src.dtype, device=DEV)
         for s, e in enumerate(s2e0):
             if e >= 0:
-                pool[s].copy_(st["slabs_dev"][e])
+                pool[s].copy_(src[e])
         state = M.CacheState.from_slots(s2e0, cfg.E)
-        layers.append(M.SlotCachedMoELayer(st["wr"], pool, cfg.k, cfg.I, cfg.mode, cfg.policy, host_slabs=st["host"],
+        layers.append(M.SlotCachedMoELayer(st["wr"], pool, cfg.k, cfg.I, cfg.mode, cfg.policy, host_slabs=host,
                                            state=state, logit_offset=st["logit_offset"], max_tokens=cfg.T,
-                                           affinity=affinity, route_flags=rflags, sel_bias=sel_bias,
+                                           affinity=affinity, route_flags=rflags, sel_bias=sel_bias, quant=quant,
                                            decode_kernels=dk))
     return st, layers
 
 
-def _steps(cfg, s2e0, xs, affinity=0.0, rflags=0):
+def _steps(cfg, s2e0, xs, affinity=0.0, rflags=0, quant=0):
     """Runs the steps on both layers and the oracle; returns the misses of each step."""
     import expert_slot_cache_gb300 as M
     bias_np = bias_d = None
@@ -55,8 +63,10 @@ def _steps(cfg, s2e0, xs, affinity=0.0, rflags=0):
         bias_np = O.bias_table(b, cfg.n_hot, cfg.bias_cap, O.BIAS_GRADED)
         bias_d = M.bias_table(torch.from_numpy(b).to(DEV), cfg.n_hot, cfg.bias_cap, mode=O.BIAS_GRADED)
     router = O.ROUTER_SIGMOID if rflags & M.ROUTE_SIGMOID else O.ROUTER_SOFTMAX
-    st, (one, sep) = _pair(cfg, s2e0, affinity, rflags, bias_d)
+    st, (one, sep) = _pair(cfg, s2e0, affinity, rflags, bias_d, quant)
     ostate = O.CacheState.from_slots(s2e0, cfg.E)
+    ohost = QHost(st["host"], cfg.H, cfg.I) if quant else HostSlabs(st["host"])
+    slab_bytes = one.pool[0].numel() * one.pool.element_size()
     wr_np = _np(st["wr"].float())
     off_np = None if st["logit_offset"] is None else _np(st["logit_offset"])
     misses = []
@@ -64,13 +74,15 @@ def _steps(cfg, s2e0, xs, affinity=0.0, rflags=0):
         r1 = one.forward(x)
         r2 = sep.forward(x)
         torch.cuda.synchronize()
-        want = O.layer_forward(_np(x.float()), wr_np, HostSlabs(st["host"]), cfg.H, cfg.I, cfg.k, cfg.mode,
+        want = O.layer_forward(_np(x.float()), wr_np, ohost, cfg.H, cfg.I, cfg.k, cfg.mode,
                                cfg.policy, ostate, None, off_np, bias_np, affinity=affinity, router=router,
-                               damped=bool(rflags & M.ROUTE_DAMPED))
+                               damped=bool(rflags & M.ROUTE_DAMPED), quant=bool(quant))
         assert np.array_equal(_np(r1["ids"]), want["ids"]), f"step {step}: ids"
         assert np.abs(_np(r1["w"]) - want["w"]).max() <= 1e-6, f"step {step}: w"
         assert torch.equal(r1["ids"], r2["ids"]) and torch.equal(r1["w"], r2["w"]), f"step {step}: routing"
         assert_out_close(_np(r1["out"].float()), want["out"], f"step {step}: out")
+        if quant:  # the same exact integer sums and fp32 steps as the separate W8A8 kernels
+            assert torch.equal(r1["out"], r2["out"]), f"step {step}: out differs from the separate kernels'"
         _check_state(one.state, ostate, f"step {step}")
         for f in ("e2s", "s2e", "prio", "stamp"):
             assert torch.equal(getattr(one.state, f), getattr(sep.state, f)), f"step {step}: {f}"
@@ -79,11 +91,12 @@ def _steps(cfg, s2e0, xs, affinity=0.0, rflags=0):
         misses.append(sum(len(c["miss_e"]) for c in want["chunks"]))
     assert int(_np(one.dev_status)[0]) == 0 and int(_np(sep.dev_status)[0]) == 0
     # every occupied slot holds exactly its expert's bytes
+    host = st["host_q"] if quant else st["host"]
     for s, e in enumerate(_np(one.state.s2e)):
         if e >= 0:
-            assert torch.equal(one.pool[s].cpu(), st["host"][int(e)]), f"slot {s}"
+            assert torch.equal(one.pool[s].cpu(), host[int(e)]), f"slot {s}"
     stats = _np(one.stats)
-    assert stats[0] == sum(misses) and stats[1] == len(xs) and stats[2] == sum(misses) * cfg.slab_bytes
+    assert stats[0] == sum(misses) and stats[1] == len(xs) and stats[2] == sum(misses) * slab_bytes
     # the arrival and copy counters (start of the workspace) are back at zero
     assert int(one.workspace[: 4 * (cfg.E + 4 + 64)].count_nonzero()) == 0
     return misses
@@ -94,6 +107,22 @@ def test_decode_gather_qwen_lru(T):
     cfg = C.qwen(T)
     misses = _steps(cfg, C.initial_residency(cfg), [C.draw_x(cfg, DEV, step=s) for s in range(4)])
     assert sum(misses) > 0
+
+
+@pytest.mark.parametrize("T", [1, 5, 8])
+def test_decode_gather_w8a8_qwen_lru(T):
+    # W8A8 slabs (codes and slot-indexed scales) copied host-to-slot in the persistent W8A8 kernel
+    cfg = C.qwen(T)
+    misses = _steps(cfg, C.initial_residency(cfg), [C.draw_x(cfg, DEV, step=s) for s in range(4)], quant=1)
+    assert sum(misses) > 0
+
+
+def test_decode_gather_w8a8_empty_pool_lfu_and_tiny():
+    cfg = C.qwen(8, policy=C.POLICY_LFU)
+    x0 = C.draw_x(cfg, DEV)
+    _steps(cfg, np.full(cfg.S, -1, dtype=np.int32), [x0, x0, C.draw_x(cfg, DEV, step=1)], quant=1)
+    cfg = C.TINY.with_(mode=C.MODE_GATHER, S=12, T=6, logit_offset=True, bias_cap=-0.5, n_hot=6, zipf_s=1.1)
+    _steps(cfg, C.initial_residency(cfg), [C.draw_x(cfg, DEV, step=s) for s in range(3)], quant=1)
 
 
 def test_decode_gather_qwen_lfu():
