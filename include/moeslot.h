@@ -481,16 +481,16 @@ typedef struct moe_layer_args {
  * and down weight streams folded with dp4a (their exact int32 sums meet in
  * accumulators by integer atomics), h quantised per row, and the combine;
  * its output is bit for bit that of the separate W8A8 kernels.  Small
- * expert-cache steps (GATHER, bf16, LRU or LFU, T*k <= S <= 256, the bf16
- * shape limits above, decode_kernels == 0, at least 96 SMs) run in the bf16
- * persistent launch too ("Porting vllm-expert-cache to NVIDIA GPUs", "1.
- * Kernels": a fused manager, gather and expert kernel): every CTA runs the
- * manage state machine on a shared-memory copy of the cache state, CTA 0
+ * expert-cache steps (GATHER, LRU or LFU, T*k <= S <= 256, the shape limits
+ * above, decode_kernels == 0, at least 96 SMs) run in the persistent
+ * launches too, bf16 and W8A8 ("Porting vllm-expert-cache to NVIDIA GPUs",
+ * "1. Kernels": a fused manager, gather and expert kernel): every CTA runs
+ * the manage state machine on a shared-memory copy of the cache state, CTA 0
  * writes the new state, 48 CTAs copy the missing slabs from host memory into
  * their victim slots while the others stream the hit experts, and each
  * missing expert streams once its slab is in.  The state, miss count,
  * statistics and slot bytes are bit for bit those of the separate manage and
- * gather calls.  The grid-wide waits of these kernels are bounded: a wait
+ * gather calls (and, with W8A8 slabs, the output too).  The grid-wide waits of these kernels are bounded: a wait
  * that gives up sets MOE_DEV_TIMEOUT (an expert-cache step whose router
  * wait gave up leaves the cache state, statistics and pool as they were; a
  * wait that gives up later, or in some CTAs only, can leave the state and
