@@ -722,6 +722,8 @@ def targets(dev: str, peaks: dict) -> dict:
         d = resident_decode(dev, peaks, T, quant=True)
         t[f"q8_res_T{T}_us"], t[f"q8_res_T{T}_layer_hbm"], t[f"q8_res_T{T}_ffn_hbm"] = \
             d["us"], d["layer_hbm"], d["ffn_hbm"]
+    for T in (1, 8):  # one launch per step (the fused expert-cache step)
+        t[f"q8_gather_T{T}_tok_s"] = gather_line(dev, T, C.SCHED_WAVES, quant=True)["tok_s"]
     t["q8_gather_T64_tok_s"] = gather_line(dev, 64, C.SCHED_WAVES, quant=True)["tok_s"]
     st = stack_variant(dev, peaks, C.STACK)
     t["stack48_tok_s"], t["stack48_hbm"] = st["tokens_per_s"], st["hbm"]["frac"]
