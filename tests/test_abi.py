@@ -67,10 +67,10 @@ def test_workspace_sizes(lib):
     assert ws >= 4 * 512 * (768 + 2048)
     # decode-sized groups add the stream path's buffers: partial sums in two
     # equal halves, each the larger of (gate/up parts x n x 2I) and (down
-    # parts x n x H) fp32, parts per expert = 16 MiB // (n * N * 4) clamped to
+    # parts x n x H) fp32, parts per expert = 64 MiB // (n * N * 4) clamped to
     # [3, 160]; then x grouped by expert (bf16 n x H) and h (bf16 n x I)
     n = 512
-    jg, jd = max(3, min((16 << 20) // (n * 1536 * 4), 160)), max(3, min((16 << 20) // (n * 2048 * 4), 160))
+    jg, jd = max(3, min((64 << 20) // (n * 1536 * 4), 160)), max(3, min((64 << 20) // (n * 2048 * 4), 160))
     half = max(jg * n * 1536 * 4, jd * n * 2048 * 4)
     stream = 2 * half + n * 2048 * 2 + n * 768 * 2
     assert lib.moe_ffn_workspace_bytes(64, 2048, 8, 768) == 4 * 512 * 768 + 256 + stream
