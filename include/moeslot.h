@@ -490,13 +490,14 @@ typedef struct moe_layer_args {
  * their victim slots while the others stream the hit experts, and each
  * missing expert streams once its slab is in.  The state, miss count,
  * statistics and slot bytes are bit for bit those of the separate manage and
- * gather calls (and, with W8A8 slabs, the output too).  The grid-wide waits of these kernels are bounded: a wait
- * that gives up sets MOE_DEV_TIMEOUT (an expert-cache step whose router
- * wait gave up leaves the cache state, statistics and pool as they were; a
- * wait that gives up later, or in some CTAs only, can leave the state and
- * the pool disagreeing: reload both before the next step).  They keep arrival counters at the
- * start of the workspace, which must therefore be zero-filled once before
- * the first call on it (each call leaves them zero).
+ * gather calls (and, with W8A8 slabs, the output too).  The grid-wide waits
+ * of these kernels are bounded: a wait that gives up sets MOE_DEV_TIMEOUT
+ * (an expert-cache step whose router wait gave up leaves the cache state,
+ * statistics and pool as they were; a wait that gives up later, or in some
+ * CTAs only, can leave the state and the pool disagreeing: reload both
+ * before the next step).  They keep arrival counters at the start of the
+ * workspace, which must therefore be zero-filled once before the first call
+ * on it (each call leaves them zero).
  * `side` may be NULL or equal to `main` (then everything runs on `main`).
  * The sequence of launches depends only on the shapes, so it can be
  * captured into a CUDA graph.
