@@ -455,7 +455,7 @@ typedef struct moe_layer_args {
   int32_t* window_counts;    /* device int32 [E] or NULL: each chunk's routings are added (moe_cache_count) */
   int32_t quant;             /* 0: bf16 slabs; 1: W8A8 slabs (moe_quantize_slabs), RESIDENT or GATHER mode */
   int32_t schedule;          /* GATHER steps larger than the pool: MOE_SCHED_CHUNKS or MOE_SCHED_WAVES */
-  int32_t decode_kernels;    /* 0 = the persistent decode kernel where it applies (RESIDENT, GATHER), 1 = separate kernels */
+  int32_t decode_kernels;    /* 0: persistent decode kernels where they apply (RESIDENT, GATHER); 1: separate */
 } moe_layer_args;
 
 /*
